@@ -1,0 +1,120 @@
+"""Matrix shapes of the decode workloads and their algorithmic byte counts.
+
+Byte accounting follows the pages' ceiling arithmetic: a decode step reads
+every weight matrix once, so tokens/s <= bandwidth / bytes of weights per
+token (tinyinfer, "How I Built an LLM Inference Engine From Scratch in CUDA",
+TL;DR; llm-rs vs vLLM, sec. 2). Only the matrices streamed by the GEMVs are
+counted (the embedding table is gathered one row per token).
+
+Per GEMV the algorithmic bytes are weights + group scales (+ zero points)
++ the activation vector(s) x; the output y is reported alongside.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+FMT_BF16 = "bf16"
+FMT_INT4_G64 = "int4_g64"
+FMT_INT4_AWQ_G128 = "int4_awq_g128"
+
+
+@dataclass(frozen=True)
+class Mat:
+    name: str
+    N: int  # output rows
+    K: int  # reduction length
+
+
+def bits_per_weight(code_bits: int, group: int, scale_bits: int, zero_bits: int) -> float:
+    """Storage bits per weight of a grouped format: code + (scale + zero) / group."""
+    return code_bits + (scale_bits + zero_bits) / group
+
+
+def weight_bytes(fmt: str, N: int, K: int) -> int:
+    """Bytes of one stored weight matrix in the layout the library takes."""
+    if fmt == FMT_BF16:
+        return 2 * N * K
+    if fmt == FMT_INT4_G64:
+        return N * K // 2 + 2 * N * (K // 64)
+    if fmt == FMT_INT4_AWQ_G128:
+        G = K // 128
+        return N * K // 2 + 2 * N * G + N * ((G + 1) // 2)
+    raise ValueError(fmt)
+
+
+def bytes_alg(fmt: str, M: int, N: int, K: int) -> int:
+    """Algorithmic bytes of one call: weights (+ scales, zeros) + M activation rows (bf16)."""
+    return weight_bytes(fmt, N, K) + 2 * M * K
+
+
+def out_bytes(M: int, N: int) -> int:
+    return 2 * M * N
+
+
+def flops(M: int, N: int, K: int) -> int:
+    return 2 * M * N * K
+
+
+# ---------------------------------------------------------------- models ----
+# TinyLlama-1.1B: hidden 2048, MLP 5632, 22 layers, 32 query heads, 4 KV heads
+# of 64 dims, vocabulary 32000 (the model of tinyinfer's measurements).
+TINYLLAMA_LAYER = (
+    Mat("q", 2048, 2048), Mat("k", 256, 2048), Mat("v", 256, 2048), Mat("o", 2048, 2048),
+    Mat("gate", 5632, 2048), Mat("up", 5632, 2048), Mat("down", 2048, 5632),
+)
+TINYLLAMA_LAYERS = 22
+TINYLLAMA_HEAD = Mat("lm_head", 32000, 2048)
+
+# Qwen2.5-7B: hidden 3584, MLP 18944, 28 layers, 28 query heads and 4 KV heads
+# of 128 dims (Q, K, V concatenated to 4608 rows), vocabulary 152064
+# (the model of llm-rs's single-stream measurements).
+QWEN25_7B_LAYER = (
+    Mat("qkv", 4608, 3584), Mat("o", 3584, 3584), Mat("gate", 18944, 3584),
+    Mat("up", 18944, 3584), Mat("down", 3584, 18944),
+)
+QWEN25_7B_LAYERS = 28
+QWEN25_7B_HEAD = Mat("lm_head", 152064, 3584)
+
+# The four TinyLlama-shaped INT4 matrices of tinyinfer's per-matrix bandwidth table.
+TINYLLAMA_TABLE_SHAPES = (
+    Mat("q/o", 2048, 2048), Mat("gate/up", 5632, 2048), Mat("down", 2048, 5632),
+    Mat("lm_head", 32000, 2048),
+)
+
+SKINNY_M = (1, 8, 16, 32, 64, 128, 256)
+SKINNY_SHAPES = (Mat("gate/up", 18944, 3584), Mat("down", 3584, 18944))
+AWQ_M = (1, 16, 64)
+
+
+def decode_step(layer, layers: int, head: Mat) -> list[Mat]:
+    """Every matrix one decode token streams, in execution order."""
+    mats = []
+    for li in range(layers):
+        for m in layer:
+            mats.append(Mat(f"L{li}.{m.name}", m.N, m.K))
+    mats.append(head)
+    return mats
+
+
+def tinyllama_step() -> list[Mat]:
+    return decode_step(TINYLLAMA_LAYER, TINYLLAMA_LAYERS, TINYLLAMA_HEAD)
+
+
+def qwen25_7b_step() -> list[Mat]:
+    return decode_step(QWEN25_7B_LAYER, QWEN25_7B_LAYERS, QWEN25_7B_HEAD)
+
+
+def step_weight_bytes(mats, fmt: str, head_fmt: str | None = None) -> int:
+    total = 0
+    for m in mats:
+        f = head_fmt if (head_fmt is not None and m.name == "lm_head") else fmt
+        total += weight_bytes(f, m.N, m.K)
+    return total
+
+
+def step_bytes_alg(mats, fmt: str, M: int = 1, head_fmt: str | None = None) -> int:
+    return step_weight_bytes(mats, fmt, head_fmt) + sum(2 * M * m.K for m in mats)
+
+
+def step_params(mats) -> int:
+    return sum(m.N * m.K for m in mats)

@@ -1,0 +1,267 @@
+/*
+ * oracle.c -- plain, slow, obviously correct CPU reference for the decode-step
+ * weight-streaming matrix-vector product y = W.x and its skinny-batched form
+ * Y = X.W^T, in fp64.
+ *
+ * TEST INFRASTRUCTURE. Only tests/, __graft_entry__.smoke() and bench.py's
+ * cpu_baseline / reference leg may load this library. It shares no code,
+ * header, table or helper with the CUDA path (memory_bound_weight_gb300/csrc).
+ *
+ * What it computes, and where the pages define it:
+ *   - y = W.x with W stored (rows, K) row-major: "W (d,n) @ x (n,) -> xout (d,)",
+ *     one output per row, each row a dot product with x
+ *     (yalm, "Fast LLM inference from scratch", sec. 2 CPU matmul and
+ *     sec. 3.1 GPU matmul; llm-rs vs vLLM, sec. 2 "Decode with one request is
+ *     a memory problem": every weight used for one multiply and one add).
+ *   - INT4 group-64 weights: 4-bit codes plus one fp16 scale per 64 weights
+ *     (tinyinfer, "How I Built an LLM Inference Engine From Scratch in CUDA",
+ *     TL;DR). The pages give no dequant formula; this oracle takes the
+ *     symmetric reading w = (q - 8) * s.
+ *   - AWQ-style INT4 weights: 4-bit codes with an fp16 scale and a zero point
+ *     per 128 weights (llm-rs vs vLLM, sec. 6, format table); w = (q - z) * s
+ *     with z a 4-bit code.
+ *   - Batched decode: the same weights used for M activation rows
+ *     (llm-rs vs vLLM, sec. 3 "Batching moves decode from memory toward math").
+ *
+ * Readings where the pages are silent (all recorded in the design notes):
+ *   - nibble order: the low nibble of byte b holds code k = 2b (even k), the
+ *     high nibble code k = 2b + 1;
+ *   - a group is 64 (or 128) consecutive k within one row;
+ *   - AWQ zero points are packed two per byte, low nibble = even group, with
+ *     ceil(G/2) bytes per row (G = K/128 groups);
+ *   - accumulation order: k = 0 .. K-1 sequentially in fp64 per output.
+ *
+ * Every product w*x is exact in fp64 (w has at most 15 significant bits,
+ * x at most 8), so the only rounding is in the fp64 summation.
+ *
+ * Each GEMV also returns yabs[i] = sum_k |w_ik * x_k| in fp64, the quantity
+ * the parity tolerance is stated against.
+ *
+ * Parallelism: OpenMP over output rows (the row-parallel shape of yalm's
+ * OpenMP CPU matmul). Each output is summed by one thread in k order, so the
+ * result does not depend on the thread count.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Number formats, written from their definitions.                           */
+/* ------------------------------------------------------------------------ */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * exponent 0 -> subnormal 0.f * 2^-14; exponent 31 -> inf / NaN. */
+double oracle_f16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int f = h & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);                 /* f/1024 * 2^-14 */
+    else if (e == 31)
+        v = (f == 0) ? INFINITY : NAN;
+    else
+        v = ldexp(1024.0 + (double)f, e - 25);     /* (1 + f/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE 754 binary32. 1 sign bit, 8 exponent
+ * bits (bias 127), 7 fraction bits. */
+double oracle_bf16_to_double(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xFF;
+    int f = b & 0x7F;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133);                /* f/128 * 2^-126 */
+    else if (e == 255)
+        v = (f == 0) ? INFINITY : NAN;
+    else
+        v = ldexp(128.0 + (double)f, e - 134);     /* (1 + f/128) * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+/* Round a double to the nearest bfloat16, ties to even (finite inputs).
+ * Written on the value, not on bit patterns: find the bf16 spacing at |v|,
+ * round |v| / spacing to the nearest integer with ties to even. */
+uint16_t oracle_double_to_bf16_rne(double v)
+{
+    if (isnan(v))
+        return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    int ex;
+    frexp(a, &ex);                                  /* a = m * 2^ex, m in [0.5, 1) */
+    int e = ex - 1;                                 /* a in [2^e, 2^(e+1)) */
+    if (e < -126)
+        e = -126;                                   /* subnormal range: fixed spacing */
+    double ulp = ldexp(1.0, e - 7);
+    double n = a / ulp;                             /* exact: power-of-two division */
+    double fl = floor(n);
+    double rem = n - fl;
+    double r = fl;
+    if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0))
+        r = fl + 1.0;
+    double q = r * ulp;                             /* exact */
+    if (q >= ldexp(1.0, 128))                       /* rounded past the bf16 maximum */
+        return sign | 0x7F80;
+    /* encode q (a bf16 value) */
+    if (q < ldexp(1.0, -126))
+        return sign | (uint16_t)(q / ldexp(1.0, -133));
+    frexp(q, &ex);
+    int be = ex - 1 + 127;
+    int frac = (int)(q / ldexp(1.0, ex - 1 - 7)) - 128;
+    return sign | (uint16_t)(be << 7) | (uint16_t)frac;
+}
+
+/* ------------------------------------------------------------------------ */
+/* INT4 unpack and dequant, one weight at a time.                            */
+/* ------------------------------------------------------------------------ */
+
+/* 4-bit code of weight (i, k): byte i*K/2 + k/2, low nibble if k is even. */
+static int code_at(const uint8_t *codes, int64_t K, int64_t i, int64_t k)
+{
+    uint8_t b = codes[i * (K / 2) + k / 2];
+    return (k % 2 == 0) ? (b & 0x0F) : (b >> 4);
+}
+
+/* Group-64 symmetric: w = (q - 8) * s, s = fp16 scale of group k/64 of row i. */
+static double dequant_g64(const uint8_t *codes, const uint16_t *scales,
+                          int64_t K, int64_t i, int64_t k)
+{
+    int q = code_at(codes, K, i, k);
+    double s = oracle_f16_to_double(scales[i * (K / 64) + k / 64]);
+    return (double)(q - 8) * s;
+}
+
+/* AWQ-style group-128: w = (q - z) * s with scale and zero point of group
+ * g = k/128 of row i; zero points packed two per byte, low nibble = even g. */
+static double dequant_awq(const uint8_t *codes, const uint16_t *scales,
+                          const uint8_t *zeros, int64_t K, int64_t i, int64_t k)
+{
+    int64_t G = K / 128;
+    int64_t zstride = (G + 1) / 2;
+    int64_t g = k / 128;
+    int q = code_at(codes, K, i, k);
+    uint8_t zb = zeros[i * zstride + g / 2];
+    int z = (g % 2 == 0) ? (zb & 0x0F) : (zb >> 4);
+    double s = oracle_f16_to_double(scales[i * G + g]);
+    return (double)(q - z) * s;
+}
+
+void oracle_dequant_int4_g64(const uint8_t *codes, const uint16_t *scales,
+                             int64_t N, int64_t K, double *out)
+{
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < N; i++)
+        for (int64_t k = 0; k < K; k++)
+            out[i * K + k] = dequant_g64(codes, scales, K, i, k);
+}
+
+void oracle_dequant_int4_awq_g128(const uint8_t *codes, const uint16_t *scales,
+                                  const uint8_t *zeros, int64_t N, int64_t K,
+                                  double *out)
+{
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < N; i++)
+        for (int64_t k = 0; k < K; k++)
+            out[i * K + k] = dequant_awq(codes, scales, zeros, K, i, k);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Matrix-vector and skinny matrix products.                                 */
+/* Y[m][i] = sum_k X[m][k] * w(i, k); yabs[m][i] = sum_k |X[m][k] * w(i, k)|. */
+/* Output layout: Y is (M, N) row-major. M = 1 is the plain GEMV.            */
+/* ------------------------------------------------------------------------ */
+
+void oracle_gemm_bf16(const uint16_t *W, const uint16_t *X, int64_t M,
+                      int64_t N, int64_t K, double *Y, double *Yabs)
+{
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < N; i++) {
+        for (int64_t m = 0; m < M; m++) {
+            double acc = 0.0, aabs = 0.0;
+            for (int64_t k = 0; k < K; k++) {
+                double w = oracle_bf16_to_double(W[i * K + k]);
+                double x = oracle_bf16_to_double(X[m * K + k]);
+                acc += w * x;
+                aabs += fabs(w * x);
+            }
+            Y[m * N + i] = acc;
+            Yabs[m * N + i] = aabs;
+        }
+    }
+}
+
+void oracle_gemm_int4_g64(const uint8_t *codes, const uint16_t *scales,
+                          const uint16_t *X, int64_t M, int64_t N, int64_t K,
+                          double *Y, double *Yabs)
+{
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < N; i++) {
+        for (int64_t m = 0; m < M; m++) {
+            double acc = 0.0, aabs = 0.0;
+            for (int64_t k = 0; k < K; k++) {
+                double w = dequant_g64(codes, scales, K, i, k);
+                double x = oracle_bf16_to_double(X[m * K + k]);
+                acc += w * x;
+                aabs += fabs(w * x);
+            }
+            Y[m * N + i] = acc;
+            Yabs[m * N + i] = aabs;
+        }
+    }
+}
+
+void oracle_gemm_int4_awq_g128(const uint8_t *codes, const uint16_t *scales,
+                               const uint8_t *zeros, const uint16_t *X,
+                               int64_t M, int64_t N, int64_t K, double *Y,
+                               double *Yabs)
+{
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < N; i++) {
+        for (int64_t m = 0; m < M; m++) {
+            double acc = 0.0, aabs = 0.0;
+            for (int64_t k = 0; k < K; k++) {
+                double w = dequant_awq(codes, scales, zeros, K, i, k);
+                double x = oracle_bf16_to_double(X[m * K + k]);
+                acc += w * x;
+                aabs += fabs(w * x);
+            }
+            Y[m * N + i] = acc;
+            Yabs[m * N + i] = aabs;
+        }
+    }
+}
+
+/* Threads the OpenMP loops above will use (for reporting the CPU baseline). */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

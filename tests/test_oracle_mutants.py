@@ -1,0 +1,70 @@
+"""Planted mistakes in the oracle must fail at least one pin.
+
+Each case copies oracle/oracle.c to a temporary directory, plants one plausible
+mistake (a swapped nibble, a wrong group or row stride, a dropped term, a sign,
+a transposed index, a wrong exponent bias ...), compiles it, and runs the pin
+suite against it. A mutant that passes every pin would mean the pins cannot
+see that kind of mistake. The real oracle is never modified.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, text to find, replacement, which occurrence (1-based))
+MUTANTS = [
+    ("nibble_order", "(k % 2 == 0) ? (b & 0x0F) : (b >> 4)", "(k % 2 == 0) ? (b >> 4) : (b & 0x0F)", 1),
+    ("g64_zero_point", "(double)(q - 8) * s", "(double)(q - 7) * s", 1),
+    ("g64_group_index", "scales[i * (K / 64) + k / 64]", "scales[i * (K / 64) + k / 128]", 1),
+    ("g64_scale_row_stride", "scales[i * (K / 64) + k / 64]", "scales[i * (K / 128) + k / 64]", 1),
+    ("code_row_stride", "codes[i * (K / 2) + k / 2]", "codes[i * (K / 4) + k / 2]", 1),
+    ("awq_zero_nibble_order", "(g % 2 == 0) ? (zb & 0x0F) : (zb >> 4)", "(g % 2 == 0) ? (zb >> 4) : (zb & 0x0F)", 1),
+    ("awq_zero_stride", "int64_t zstride = (G + 1) / 2;", "int64_t zstride = G / 2;", 1),
+    ("awq_sign", "(double)(q - z) * s", "(double)(z - q) * s", 1),
+    ("awq_group_boundary_off_by_one", "int64_t g = k / 128;", "int64_t g = (k + 1) / 128 < G ? (k + 1) / 128 : G - 1;", 1),
+    ("f16_exponent_bias", "ldexp(1024.0 + (double)f, e - 25)", "ldexp(1024.0 + (double)f, e - 24)", 1),
+    ("f16_subnormal", "ldexp((double)f, -24)", "ldexp((double)f, -25)", 1),
+    ("f16_implicit_bit", "ldexp(1024.0 + (double)f, e - 25)", "ldexp((double)f, e - 25)", 1),
+    ("bf16_exponent_bias", "ldexp(128.0 + (double)f, e - 134)", "ldexp(128.0 + (double)f, e - 133)", 1),
+    ("bf16_subnormal", "ldexp((double)f, -133)", "ldexp((double)f, -132)", 1),
+    ("rne_ties_to_odd", "fmod(fl, 2.0) != 0.0", "fmod(fl, 2.0) == 0.0", 1),
+    ("bf16_dropped_last_term", "for (int64_t k = 0; k < K; k++) {", "for (int64_t k = 0; k < K - 1; k++) {", 1),
+    ("g64_dropped_last_term", "for (int64_t k = 0; k < K; k++) {", "for (int64_t k = 0; k < K - 1; k++) {", 2),
+    ("awq_dropped_first_term", "for (int64_t k = 0; k < K; k++) {", "for (int64_t k = 1; k < K; k++) {", 3),
+    ("g64_reversed_x", "X[m * K + k]", "X[m * K + (K - 1 - k)]", 2),
+    ("bf16_reversed_w", "W[i * K + k]", "W[i * K + (K - 1 - k)]", 1),
+    ("yabs_signed", "aabs += fabs(w * x);", "aabs += w * x;", 1),
+    ("awq_acc_sign", "acc += w * x;", "acc -= w * x;", 3),
+    ("output_transposed", "Y[m * N + i] = acc;", "Y[i * M + m] = acc;", 1),
+    ("batch_row_of_x", "X[m * K + k]", "X[0 * K + k]", 1),
+]
+
+
+def _plant(src: str, find: str, repl: str, nth: int) -> str:
+    pos = -1
+    for _ in range(nth):
+        pos = src.find(find, pos + 1)
+        assert pos >= 0, f"mutation anchor not found: {find!r} #{nth}"
+    return src[:pos] + repl + src[pos + len(find):]
+
+
+@pytest.mark.parametrize("name,find,repl,nth", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, name, find, repl, nth):
+    with open(SRC) as f:
+        src = f.read()
+    mutated = _plant(src, find, repl, nth)
+    assert mutated != src
+    path = tmp_path / f"oracle_{name}.c"
+    path.write_text(mutated)
+    lib = oracle.build(str(path), str(tmp_path / f"liboracle_{name}.so"))
+    o = oracle.load(lib)
+    for pin in oracle_pins.PINS:
+        try:
+            pin(o)
+        except Exception:  # noqa: BLE001 - any failure means the pin saw the mistake
+            return
+    pytest.fail(f"mutant {name} passed every pin")

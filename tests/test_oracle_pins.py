@@ -1,0 +1,25 @@
+"""The fp64 oracle against its pins (CPU only)."""
+import pytest
+
+import oracle
+import oracle_pins
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load()
+
+
+@pytest.mark.parametrize("pin", oracle_pins.PINS, ids=[p.__name__ for p in oracle_pins.PINS])
+def test_pin(orc, pin):
+    pin(orc)
+
+
+def test_fixture_is_hand_worked_not_generated():
+    """The golden dequant table is read as text; it carries its citation header."""
+    import os
+
+    path = os.path.join(oracle_pins.GOLDEN, "int4_dequant_hand.txt")
+    head = open(path).read(2000)
+    assert "tinyinfer" in head and "llm-rs vs vLLM" in head
+    assert len(oracle_pins.load_dequant_fixture()) >= 30
