@@ -1,0 +1,474 @@
+#!/usr/bin/env python
+"""Decode-step weight-streaming benchmark on GB300.
+
+A step is one pass of the whole hot path over one decode token: every weight
+matrix of the model streamed once by the library's GEMV kernels, each matrix
+with its own activation vector (all calls through the C ABI, captured once
+into a CUDA graph and replayed). Default workload (--workload tinyllama_int4):
+TinyLlama-1.1B-shaped INT4 group-64 weights at batch 1 -- 22 layers x
+(q 2048x2048, k 256x2048, v 256x2048, o 2048x2048, gate 5632x2048,
+up 5632x2048, down 2048x5632) + LM head 32000x2048 = 155 GEMVs and
+0.5495 GB of codes + scales per step (4.4x the L2, so no matrix is still
+cached when the step reaches it again). Synthetic seeded data (no checkpoint).
+
+Metric: achieved HBM GB/s = algorithmic bytes of the step (weights + scales
++ x) / step time, and the weight-stream ms per token.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Multi-GPU: launched by torchrun, one independent replica per GPU (the GEMV
+has no exchange step); the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from memory_bound_weight_gb300 import workloads as wl  # noqa: E402
+
+FALLBACK_HBM_GBS = 6778.3  # the machine's measured copy bandwidth, recorded copy
+# DRAM bytes (read + write) per launch of the step's dominant kernel from one
+# ncu capture, keyed by the sha256 of the kernel source it was taken on; a
+# changed kernel gets traffic = null until it is captured again.
+TRAFFIC = {}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", default="mbw", choices=["mbw", "reference"])
+    p.add_argument("--workload", default="tinyllama_int4",
+                   choices=["tinyllama_int4", "qwen_bf16", "bf16_2048"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--per-matrix", action="store_true", help="also time each distinct shape on its own")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------- distributed ----
+def dist_setup(backend):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group(backend=backend)
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v, ws, device):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- helpers ----
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json, copy kernel)"
+    except Exception:  # noqa: BLE001
+        return FALLBACK_HBM_GBS, "measured on this pool (recorded copy; MEASURED_PEAKS.json absent)"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in a thread."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except FileNotFoundError:
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.t:
+            self.t.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = [r for (ts, r) in self.rows if t0 <= ts <= t1 and len(r) >= 9]
+        window = "timed region"
+        if not rows:  # a very short timed region: take the samples around it
+            rows = [r for (ts, r) in self.rows if t0 - 1.0 <= ts <= t1 + 1.0 and len(r) >= 9]
+            window = "timed region +/- 1 s"
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "window": window}
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("gemv_simt.cu", "device.cuh"):
+        with open(os.path.join(ROOT, "memory_bound_weight_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# -------------------------------------------------------------- workloads ----
+class Step:
+    """All matrices of one decode step resident on the device, and the calls
+    that stream them."""
+
+    def __init__(self, name, fmt, mats, seed, device):
+        import torch
+
+        import memory_bound_weight_gb300 as mbw
+        from memory_bound_weight_gb300 import inputs as gen
+        from memory_bound_weight_gb300 import inputs_gpu
+
+        self.name, self.fmt, self.mats = name, fmt, mats
+        self.device = device
+        sumK = sum(m.K for m in mats)
+        sumN = sum(m.N for m in mats)
+        self.x = torch.empty(sumK, dtype=torch.bfloat16, device=device)
+        self.y = torch.empty(sumN, dtype=torch.bfloat16, device=device)
+        self.calls = []
+        ko = no = 0
+        for mi, m in enumerate(mats):
+            xv = self.x[ko:ko + m.K]
+            yv = self.y[no:no + m.N]
+            inputs_gpu.bf16_normal_(xv, seed, gen.stream_id(mi, gen.KIND_X), gen.X_SIGMA)
+            if fmt == wl.FMT_INT4_G64:
+                c = inputs_gpu.int4_codes(seed, mi, m.N, m.K, device)
+                s = inputs_gpu.f16_group_scales(seed, mi, m.N, m.K // 64, device)
+                self.calls.append((mbw.gemv_int4_g64, (c, s, xv), yv))
+            elif fmt == wl.FMT_BF16:
+                W = inputs_gpu.bf16_weights(seed, mi, m.N, m.K, device)
+                self.calls.append((mbw.gemv_bf16, (W, xv), yv))
+            else:
+                raise ValueError(fmt)
+            ko += m.K
+            no += m.N
+        self.op = mbw.OP_GEMV_INT4_G64 if fmt == wl.FMT_INT4_G64 else mbw.OP_GEMV_BF16
+        self.bytes_alg = wl.step_bytes_alg(mats, fmt)
+        self.h2d_bytes = 2 * sumK
+        self.d2h_bytes = 2 * sumN
+
+    def shapes(self):
+        return sorted({(m.N, m.K) for m in self.mats})
+
+    def run(self):
+        for fn, args, out in self.calls:
+            fn(*args, out=out)
+
+
+def make_step(workload, seed, device):
+    if workload == "tinyllama_int4":
+        return Step("TinyLlama-1.1B-shaped INT4 g64 decode step, batch 1", wl.FMT_INT4_G64, wl.tinyllama_step(),
+                    seed, device)
+    if workload == "qwen_bf16":
+        return Step("Qwen2.5-7B-shaped BF16 decode step, batch 1", wl.FMT_BF16, wl.qwen25_7b_step(), seed, device)
+    if workload == "bf16_2048":
+        # 2048x2048 BF16 GEMV; 64 distinct copies (537 MB) so that each is evicted before it recurs
+        mats = [wl.Mat(f"copy{i}", 2048, 2048) for i in range(64)]
+        return Step("BF16 GEMV 2048x2048, batch 1 (64 rotating copies)", wl.FMT_BF16, mats, seed, device)
+    raise ValueError(workload)
+
+
+# ------------------------------------------------------------- cpu oracle ----
+def cpu_baseline(workload, budget_s=10.0):
+    """The fp64 oracle on this host's cores over a bounded sample of the step."""
+    import numpy as np
+
+    import oracle
+    from memory_bound_weight_gb300 import inputs as gen
+
+    o = oracle.load()
+    if workload == "tinyllama_int4":
+        mats, fmt = wl.tinyllama_step(), wl.FMT_INT4_G64
+    elif workload == "qwen_bf16":
+        mats, fmt = wl.qwen25_7b_step(), wl.FMT_BF16
+    else:
+        mats, fmt = [wl.Mat("copy0", 2048, 2048)] * 64, wl.FMT_BF16
+    done_bytes = 0
+    spent = 0.0
+    n = 0
+    for mi, m in enumerate(mats):
+        X = gen.bf16_activations(0, mi, 1, m.K)
+        if fmt == wl.FMT_INT4_G64:
+            c = gen.int4_codes(0, mi, m.N, m.K)
+            s = gen.f16_group_scales(0, mi, m.N, m.K // 64)
+            t = time.perf_counter()
+            o.gemm_int4_g64(c, s, X)
+        else:
+            W = gen.bf16_weights(0, mi, m.N, m.K)
+            t = time.perf_counter()
+            o.gemm_bf16(W, X)
+        spent += time.perf_counter() - t
+        done_bytes += wl.bytes_alg(fmt, 1, m.N, m.K)
+        n += 1
+        if spent >= budget_s:
+            break
+    return {"value": done_bytes / spent / 1e9, "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
+            "sample": f"first {n} of {len(mats)} matrices of the step ({done_bytes / 1e9:.3f} GB), "
+                      f"fp64 C oracle, OpenMP over rows, {spent:.1f} s"}
+
+
+def run_reference(args, rank, ws):
+    """--impl reference: the oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    per_step = max(0.5, 20.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_baseline(args.workload, budget_s=per_step)
+    t0 = time.perf_counter()
+    vals = []
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(args.workload, budget_s=per_step))
+    elapsed = time.perf_counter() - t0
+    v = statistics.median(r["value"] for r in vals)
+    cb = dict(vals[0])
+    cb["value"] = v
+    cb["sample"] = f"each step: {cb['sample'].split(' (')[0]}, budget {per_step:.1f} s of oracle time"
+    line = {"impl": "reference", "metric": metric_name(args.workload), "value": v, "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed / max(1, args.steps) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(args.workload)}, "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def metric_name(workload):
+    return "decode GEMV achieved HBM GB/s (% of GB300 peak); weight-stream ms/token"
+
+
+def workload_desc(workload):
+    return {"tinyllama_int4": "TinyLlama-1.1B-shaped INT4 group-64 decode step, batch 1 (155 GEMVs)",
+            "qwen_bf16": "Qwen2.5-7B-shaped BF16 decode step, batch 1 (141 GEMVs)",
+            "bf16_2048": "BF16 GEMV 2048x2048, batch 1, 64 rotating copies"}[workload]
+
+
+# ------------------------------------------------------------------- main ----
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        rank, ws, _ = dist_setup("gloo")
+        run_reference(args, rank, ws)
+        if ws > 1:
+            barrier(ws)
+        return
+
+    import torch
+
+    rank, ws, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    from memory_bound_weight_gb300 import build as mbuild
+
+    if rank == 0 and not os.path.exists(os.path.join(ROOT, "memory_bound_weight_gb300", "libmbw.so")):
+        mbuild.build()
+    barrier(ws)
+    import memory_bound_weight_gb300 as mbw
+
+    step = make_step(args.workload, seed=0, device=device)
+    for N, K in step.shapes():
+        mbw.autotune(step.op, 1, N, K)
+    plans = {f"{N}x{K}": mbw.plan_describe(step.op, 1, N, K) for N, K in step.shapes()}
+    step.run()
+    torch.cuda.synchronize()
+
+    # one CUDA graph per step: the C-ABI calls captured in order
+    cap = torch.cuda.Stream(device)
+    g = torch.cuda.CUDAGraph()
+    n0 = mbw.launch_count()
+    with torch.cuda.graph(g, stream=cap):
+        step.run()
+    launches_per_step = mbw.launch_count() - n0
+
+    stream = torch.cuda.current_stream(device)
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(ws)
+    sampler.stop()
+    ms = e0.elapsed_time(e1)
+    ms = max_over_ranks(ms, ws, device)
+    ms_step = ms / args.steps
+    gbs_rank = step.bytes_alg / (ms_step * 1e-3) / 1e9
+    value = gbs_rank * ws
+
+    # end to end: per step, the x vectors go host->device from pinned memory,
+    # the step runs, the y vectors come back device->host.
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.empty_like(step.x, device="cpu").pin_memory()
+        xh.copy_(step.x)
+        yh = torch.empty_like(step.y, device="cpu").pin_memory()
+        ke = max(1, min(args.steps, 2000))
+        for _ in range(max(3, args.warmup // 10)):
+            step.x.copy_(xh, non_blocking=True)
+            g.replay()
+            yh.copy_(step.y, non_blocking=True)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0.record(stream)
+        for _ in range(ke):
+            step.x.copy_(xh, non_blocking=True)
+            g.replay()
+            yh.copy_(step.y, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        ems = max_over_ranks(e0.elapsed_time(e1), ws, device) / ke
+        e2e = {"value": step.bytes_alg / (ems * 1e-3) / 1e9 * ws, "unit": "GB/s",
+               "h2d_bytes_per_step": step.h2d_bytes, "d2h_bytes_per_step": step.d2h_bytes,
+               "ms_per_step": ems, "steps": ke}
+
+    per_matrix = None
+    if args.per_matrix and rank == 0:
+        per_matrix = time_per_shape(step, device)
+
+    peak, peak_src = hbm_peak()
+    sha = kernel_source_sha()
+    traffic = TRAFFIC.get(sha)
+    clocks = sampler.summary(t0, t1)
+    if rank != 0:
+        return
+    cb = None
+    if ws == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(args.workload)
+    line = {
+        "metric": metric_name(args.workload),
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(args.workload), "matrices": len(step.mats),
+                   "bytes_alg_per_step": step.bytes_alg, "batch": 1, "parallelism": f"replicas{ws}",
+                   "l2": "inputs larger than L2: each step streams %.3f GB of distinct weights" % (step.bytes_alg / 1e9),
+                   "plans": plans},
+        "weight_stream_ms_per_token": ms_step,
+        "frac_of_peak": gbs_rank / peak,
+        "roofline": {"bound": "hbm", "achieved": gbs_rank, "peak": peak, "unit": "GB/s", "frac": gbs_rank / peak,
+                     "traffic": traffic, "peak_source": peak_src,
+                     "kernel": "gemv_simt_kernel (every launch of the step)",
+                     "note": "the step is %d launches of one kernel family; its average launch duration is the "
+                             "timed region / launches, so achieved = bytes_alg per launch / that duration "
+                             "(launch gaps included)" % launches_per_step},
+        "cpu_baseline": cb,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+        "launches_per_step": launches_per_step,
+        "kernel_source_sha": sha,
+    }
+    if per_matrix:
+        line["per_matrix"] = per_matrix
+    print(json.dumps(line), flush=True)
+
+
+def time_per_shape(step, device, reps=5):
+    """Each distinct shape on its own: a CUDA graph of every matrix of that
+    shape in the step (distinct weights, so each launch reads from HBM)."""
+    import torch
+
+    out = {}
+    peak, _ = hbm_peak()
+    for N, K in step.shapes():
+        calls = [c for c, m in zip(step.calls, step.mats) if (m.N, m.K) == (N, K)]
+        mult = max(1, 64 // len(calls))
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device)
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(mult):
+                for fn, a, o in calls:
+                    fn(*a, out=o)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / (mult * len(calls)))
+        us = statistics.median(ts) * 1e3
+        b = wl.bytes_alg(step.fmt, 1, N, K)
+        out[f"{N}x{K}"] = {"us": us, "GB/s": b / (us * 1e-6) / 1e9, "frac": b / (us * 1e-6) / 1e9 / peak,
+                           "launches_per_graph": mult * len(calls)}
+    return out
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,169 @@
+/*
+ * mbw.h -- C ABI of libmbw.so: the decode-step weight-streaming matrix-vector
+ * product on GB300 (sm_103a).
+ *
+ * The operation (the one all the pages turn on):
+ *   y = W . x, W stored (N, K) row-major, x of length K, y of length N: one
+ *   output per weight row, "W (d,n) @ x (n,) -> xout (d,)" (yalm, "Fast LLM
+ *   inference from scratch", sec. 2 CPU matmul and sec. 3.1 GPU matmul). In
+ *   batch-1 decode every weight is read once per token and used for one
+ *   multiply-add, so the call is bound by memory bandwidth (llm-rs vs vLLM,
+ *   sec. 2 "Decode with one request is a memory problem"; tinyinfer, "How I
+ *   Built an LLM Inference Engine From Scratch in CUDA", TL;DR).
+ *   Batched: Y = X . W^T, X (M, K), Y (M, N): the same weights read once for M
+ *   activation rows (llm-rs vs vLLM, sec. 3 "Batching moves decode from memory
+ *   toward math").
+ *
+ * Conventions shared by every call below:
+ *   - Pointers are device pointers on the current CUDA device, row-major and
+ *     contiguous, 16-byte aligned (MBW_ERR_MISALIGNED otherwise). The caller
+ *     owns every buffer; the library never allocates on a call path.
+ *   - bf16 = IEEE bfloat16, fp16 = IEEE binary16, passed as raw bits.
+ *   - Accumulation is fp32; the output is rounded to bf16 (round to nearest
+ *     even) unless mbw_set_output_fp32(1) is in effect on the calling thread.
+ *   - N == 0 or M == 0: nothing is launched, MBW_OK. K == 0: y is set to zero.
+ *   - Calls are asynchronous on `stream`; arguments are checked on the host
+ *     before any CUDA call and reported as a status, never thrown. Launch
+ *     errors are returned as MBW_ERR_CUDA (detail in mbw_last_error()).
+ *   - y must not alias an input. Results are deterministic: the same inputs
+ *     give bitwise the same outputs, run after run.
+ *   - `workspace` / `ws_bytes` are accepted for split-K plans that need global
+ *     scratch; a NULL or short workspace never fails a call (the plan falls
+ *     back to a variant that needs none). mbw_workspace_bytes() gives the size.
+ *   - Threads: calls are thread-safe. The plan cache is shared and guarded.
+ *     Calls can be captured into a CUDA graph once their shape is planned
+ *     (mbw_autotune, or one earlier call); a shape first seen during capture
+ *     uses the built-in default plan and is never autotuned there.
+ */
+#ifndef MBW_H
+#define MBW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (a pointer to the driver's stream object).
+ * NULL selects the legacy default stream. */
+typedef struct CUstream_st *mbw_stream_t;
+
+typedef int mbw_status;
+#define MBW_OK 0
+#define MBW_ERR_INVALID_ARG 1         /* NULL pointer, negative size, bad flag */
+#define MBW_ERR_MISALIGNED 2          /* a pointer is not 16-byte aligned */
+#define MBW_ERR_BAD_SHAPE 3           /* K not a multiple of the format's unit, sizes too large */
+#define MBW_ERR_WORKSPACE_TOO_SMALL 4 /* only from calls that require scratch */
+#define MBW_ERR_UNSUPPORTED 5         /* no kernel for this device or request */
+#define MBW_ERR_CUDA 6                /* a CUDA runtime call failed */
+#define MBW_ERR_DEVICE_TIMEOUT 7      /* a device-side bounded wait gave up */
+
+/* Operation ids for the plan / workspace queries. */
+#define MBW_OP_GEMV_BF16 1
+#define MBW_OP_GEMV_INT4_G64 2
+#define MBW_OP_GEMV_INT4_AWQ_G128 3
+#define MBW_OP_GEMM_SKINNY_BF16 4
+
+/*
+ * gemv_bf16 -- y = W . x with BF16 weights (16 bits per weight; llm-rs vs
+ * vLLM, sec. 6 format table, "BF16 16").
+ *   W : bf16 [N][K]      x : bf16 [K]      y : bf16 [N] (fp32 [N] under the fp32 hook)
+ *   Requires K % 8 == 0 (16-byte rows). N, K < 2^31.
+ */
+mbw_status gemv_bf16(const void *W, const void *x, void *y, int64_t N, int64_t K,
+                     void *workspace, size_t ws_bytes, mbw_stream_t stream);
+
+/*
+ * gemv_int4_g64 -- y = W . x with INT4 group-64 weights: 4-bit codes plus one
+ * fp16 scale per 64 consecutive weights of a row (tinyinfer, TL;DR: "4 bits
+ * plus one fp16 scale per 64 weights"), dequantized as w = (q - 8) * s.
+ *   Wq     : uint8 [N][K/2], two codes per byte, low nibble = even k
+ *   scales : fp16  [N][K/64]
+ *   x      : bf16  [K]       y : bf16 [N] (fp32 under the fp32 hook)
+ *   Requires K % 64 == 0. `scales` needs only 2-byte alignment.
+ */
+mbw_status gemv_int4_g64(const uint8_t *Wq, const void *scales, const void *x, void *y,
+                         int64_t N, int64_t K, void *workspace, size_t ws_bytes,
+                         mbw_stream_t stream);
+
+/*
+ * gemv_int4_awq_g128 -- Y = X . W^T with AWQ-style INT4 weights: 4-bit codes
+ * with an fp16 scale and a 4-bit zero point per 128 consecutive weights of a
+ * row (llm-rs vs vLLM, sec. 6 format table, "AWQ: 4-bit, FP16 scale + zero per
+ * 128"), dequantized as w = (q - z) * s. M = 1 is the decode GEMV.
+ *   Wq     : uint8 [N][K/2], low nibble = even k
+ *   scales : fp16  [N][G], G = K/128
+ *   zeros  : uint8 [N][(G+1)/2], two zero points per byte, low nibble = even group
+ *   X      : bf16  [M][K]    Y : bf16 [M][N] (fp32 under the fp32 hook)
+ *   Requires K % 128 == 0. `scales` needs only 2-byte alignment, `zeros` none.
+ */
+mbw_status gemv_int4_awq_g128(const uint8_t *Wq, const void *scales, const uint8_t *zeros,
+                              const void *X, void *Y, int64_t M, int64_t N, int64_t K,
+                              void *workspace, size_t ws_bytes, mbw_stream_t stream);
+
+/*
+ * gemm_skinny_bf16 -- Y = X . W^T with BF16 weights and a skinny batch M
+ * (tuned for 1 <= M <= 256; larger M is processed in slices of 256 rows).
+ * The weights are still read once per call; at GB300's ridge (~286 FLOP per
+ * byte) every M <= 256 stays memory-bound or near the ridge.
+ *   X : bf16 [M][K]    W : bf16 [N][K]    Y : bf16 [M][N]
+ *   Requires K % 8 == 0.
+ */
+mbw_status gemm_skinny_bf16(const void *X, const void *W, void *Y, int64_t M, int64_t N,
+                            int64_t K, void *workspace, size_t ws_bytes, mbw_stream_t stream);
+
+/* Bytes of workspace the largest plan of `op` may use for this shape (0 if none). */
+size_t mbw_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
+
+/*
+ * Dequantize INT4 weights to fp32 with the same unpack the GEMV kernels use:
+ * out[i][k] = (q - 8) * s (g64) or (q - z) * s (AWQ). Both values are exact in
+ * fp32 for every fp16 scale, so the result is bit-exact. Same layouts as above.
+ */
+mbw_status mbw_dequant_int4_g64(const uint8_t *Wq, const void *scales, float *out,
+                                int64_t N, int64_t K, mbw_stream_t stream);
+mbw_status mbw_dequant_int4_awq_g128(const uint8_t *Wq, const void *scales,
+                                     const uint8_t *zeros, float *out, int64_t N,
+                                     int64_t K, mbw_stream_t stream);
+
+/* Test hook, per calling thread: 1 = later calls on this thread write fp32 y
+ * (the fp32 accumulator before bf16 rounding), 0 = bf16 y (default). */
+mbw_status mbw_set_output_fp32(int enable);
+
+/*
+ * Measure the candidate plans of (op, M, N, K) on `stream` and keep the
+ * fastest (by achieved GB/s) in the plan cache. Blocking; allocates and frees
+ * its own timing buffers; must not be called during stream capture.
+ */
+mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_stream_t stream);
+
+/* Number of candidate plans (kernel instantiation x split-K factor) valid
+ * for (op, M, N, K); 0 for a bad op or shape. */
+int mbw_plan_candidates(int op, int64_t M, int64_t N, int64_t K);
+
+/* Make candidate `index` (0 .. mbw_plan_candidates()-1) the plan of this
+ * shape, replacing the default or a tuned one. Lets a caller restore plans it
+ * measured earlier, and lets tests run every kernel instantiation. */
+mbw_status mbw_plan_select(int op, int64_t M, int64_t N, int64_t K, int index);
+
+/* Write a one-line description of the plan a call of this shape would use
+ * into buf (NUL-terminated, truncated to len). Returns MBW_OK. */
+mbw_status mbw_plan_describe(int op, int64_t M, int64_t N, int64_t K, char *buf, size_t len);
+
+/* Read and clear the device-side error flag set by bounded waits inside
+ * kernels (synchronizes the current device). MBW_OK or MBW_ERR_DEVICE_TIMEOUT. */
+mbw_status mbw_check_device_error(void);
+
+/* Number of kernel launches this library has issued on the calling thread. */
+uint64_t mbw_launch_count(void);
+
+const char *mbw_status_string(mbw_status status);
+/* Detail of the last failed call on the calling thread ("" if none). */
+const char *mbw_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MBW_H */

@@ -1,0 +1,270 @@
+"""Thin ctypes binding of libmbw.so (include/mbw.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libmbw.so. PyTorch supplies device memory and the current stream.
+If the library is missing the calls raise; there is no fallback path.
+"""
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmbw.so")
+
+MBW_OK = 0
+OP_GEMV_BF16 = 1
+OP_GEMV_INT4_G64 = 2
+OP_GEMV_INT4_AWQ_G128 = 3
+OP_GEMM_SKINNY_BF16 = 4
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_ST = ctypes.c_int
+
+_lock = threading.Lock()
+_lib = None
+
+# name -> (argtypes, restype)
+SIGNATURES = {
+    "gemv_bf16": ([_P, _P, _P, _I64, _I64, _P, _SZ, _P], _ST),
+    "gemv_int4_g64": ([_P, _P, _P, _P, _I64, _I64, _P, _SZ, _P], _ST),
+    "gemv_int4_awq_g128": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _ST),
+    "gemm_skinny_bf16": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _ST),
+    "mbw_workspace_bytes": ([ctypes.c_int, _I64, _I64, _I64], _SZ),
+    "mbw_dequant_int4_g64": ([_P, _P, _P, _I64, _I64, _P], _ST),
+    "mbw_dequant_int4_awq_g128": ([_P, _P, _P, _P, _I64, _I64, _P], _ST),
+    "mbw_set_output_fp32": ([ctypes.c_int], _ST),
+    "mbw_autotune": ([ctypes.c_int, _I64, _I64, _I64, _P], _ST),
+    "mbw_plan_candidates": ([ctypes.c_int, _I64, _I64, _I64], ctypes.c_int),
+    "mbw_plan_select": ([ctypes.c_int, _I64, _I64, _I64, ctypes.c_int], _ST),
+    "mbw_plan_describe": ([ctypes.c_int, _I64, _I64, _I64, ctypes.c_char_p, _SZ], _ST),
+    "mbw_check_device_error": ([], _ST),
+    "mbw_launch_count": ([], ctypes.c_uint64),
+    "mbw_status_string": ([_ST], ctypes.c_char_p),
+    "mbw_last_error": ([], ctypes.c_char_p),
+}
+
+
+class MbwError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str):
+        super().__init__(f"{fn} failed: status {status} ({detail})")
+        self.status = status
+        self.detail = detail
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmbw.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                       "`python -m memory_bound_weight_gb300.build`")
+                L = ctypes.CDLL(LIB_PATH)
+                for name, (args, res) in SIGNATURES.items():
+                    f = getattr(L, name)
+                    f.argtypes = args
+                    f.restype = res
+                _lib = L
+    return _lib
+
+
+def check(fn: str, status: int) -> None:
+    if status != MBW_OK:
+        L = lib()
+        name = L.mbw_status_string(status).decode()
+        detail = L.mbw_last_error().decode()
+        raise MbwError(fn, status, f"{name}: {detail}")
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _stream_ptr(device) -> int:
+    torch = _torch()
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need(t, name, dtype, ndim):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got {t.dim()}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+_tls = threading.local()
+
+
+def _out_dtype():
+    torch = _torch()
+    return torch.float32 if getattr(_tls, "fp32", False) else torch.bfloat16
+
+
+@contextlib.contextmanager
+def output_fp32():
+    """Within this block, calls on this thread write the fp32 accumulator (test hook)."""
+    check("mbw_set_output_fp32", lib().mbw_set_output_fp32(1))
+    _tls.fp32 = True
+    try:
+        yield
+    finally:
+        lib().mbw_set_output_fp32(0)
+        _tls.fp32 = False
+
+
+def _alloc_out(shape, like, out):
+    torch = _torch()
+    dt = _out_dtype()
+    if out is None:
+        return torch.empty(shape, dtype=dt, device=like.device)
+    _need(out, "out", dt, len(shape))
+    if tuple(out.shape) != tuple(shape):
+        raise ValueError(f"out must have shape {tuple(shape)}")
+    return out
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+# ----------------------------------------------------------------- calls ----
+def gemv_bf16(W, x, out=None, workspace=None):
+    """y = W . x; W bf16 (N, K), x bf16 (K,) -> y (N,)."""
+    torch = _torch()
+    _need(W, "W", torch.bfloat16, 2)
+    _need(x, "x", torch.bfloat16, 1)
+    N, K = W.shape
+    if x.shape[0] != K:
+        raise ValueError("x must have length K")
+    y = _alloc_out((N,), W, out)
+    wp, wn = _ws(workspace)
+    check("gemv_bf16", lib().gemv_bf16(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, wp, wn,
+                                       _stream_ptr(W.device)))
+    return y
+
+
+def gemv_int4_g64(Wq, scales, x, out=None, workspace=None):
+    """y = W . x; Wq uint8 (N, K/2), scales fp16 (N, K/64), x bf16 (K,) -> y (N,)."""
+    torch = _torch()
+    _need(Wq, "Wq", torch.uint8, 2)
+    _need(scales, "scales", torch.float16, 2)
+    _need(x, "x", torch.bfloat16, 1)
+    N = Wq.shape[0]
+    K = x.shape[0]
+    if Wq.shape[1] * 2 != K or tuple(scales.shape) != (N, K // 64):
+        raise ValueError("shapes: Wq (N, K/2), scales (N, K/64), x (K,)")
+    y = _alloc_out((N,), Wq, out)
+    wp, wn = _ws(workspace)
+    check("gemv_int4_g64", lib().gemv_int4_g64(Wq.data_ptr(), scales.data_ptr(), x.data_ptr(), y.data_ptr(),
+                                               N, K, wp, wn, _stream_ptr(Wq.device)))
+    return y
+
+
+def gemv_int4_awq_g128(Wq, scales, zeros, X, out=None, workspace=None):
+    """Y = X . W^T; Wq uint8 (N, K/2), scales fp16 (N, G), zeros uint8 (N, ceil(G/2)),
+    X bf16 (M, K) or (K,) -> Y (M, N) or (N,)."""
+    torch = _torch()
+    vec = X.dim() == 1
+    X2 = X.unsqueeze(0) if vec else X
+    _need(Wq, "Wq", torch.uint8, 2)
+    _need(scales, "scales", torch.float16, 2)
+    _need(zeros, "zeros", torch.uint8, 2)
+    _need(X2, "X", torch.bfloat16, 2)
+    M, K = X2.shape
+    N = Wq.shape[0]
+    G = K // 128
+    if Wq.shape[1] * 2 != K or tuple(scales.shape) != (N, G) or tuple(zeros.shape) != (N, (G + 1) // 2):
+        raise ValueError("shapes: Wq (N, K/2), scales (N, K/128), zeros (N, ceil(K/256)), X (M, K)")
+    Y = _alloc_out((M, N), Wq, None if out is None else (out.unsqueeze(0) if vec else out))
+    wp, wn = _ws(workspace)
+    check("gemv_int4_awq_g128", lib().gemv_int4_awq_g128(
+        Wq.data_ptr(), scales.data_ptr(), zeros.data_ptr(), X2.data_ptr(), Y.data_ptr(), M, N, K, wp, wn,
+        _stream_ptr(Wq.device)))
+    return Y[0] if vec else Y
+
+
+def gemm_skinny_bf16(X, W, out=None, workspace=None):
+    """Y = X . W^T; X bf16 (M, K), W bf16 (N, K) -> Y (M, N)."""
+    torch = _torch()
+    _need(X, "X", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    M, K = X.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError("W must be (N, K)")
+    Y = _alloc_out((M, N), W, out)
+    wp, wn = _ws(workspace)
+    check("gemm_skinny_bf16", lib().gemm_skinny_bf16(X.data_ptr(), W.data_ptr(), Y.data_ptr(), M, N, K, wp, wn,
+                                                     _stream_ptr(W.device)))
+    return Y
+
+
+def dequant_int4_g64(Wq, scales):
+    torch = _torch()
+    _need(Wq, "Wq", torch.uint8, 2)
+    _need(scales, "scales", torch.float16, 2)
+    N, K = Wq.shape[0], Wq.shape[1] * 2
+    out = torch.empty((N, K), dtype=torch.float32, device=Wq.device)
+    check("mbw_dequant_int4_g64", lib().mbw_dequant_int4_g64(Wq.data_ptr(), scales.data_ptr(), out.data_ptr(),
+                                                             N, K, _stream_ptr(Wq.device)))
+    return out
+
+
+def dequant_int4_awq_g128(Wq, scales, zeros):
+    torch = _torch()
+    _need(Wq, "Wq", torch.uint8, 2)
+    _need(scales, "scales", torch.float16, 2)
+    _need(zeros, "zeros", torch.uint8, 2)
+    N, K = Wq.shape[0], Wq.shape[1] * 2
+    out = torch.empty((N, K), dtype=torch.float32, device=Wq.device)
+    check("mbw_dequant_int4_awq_g128", lib().mbw_dequant_int4_awq_g128(
+        Wq.data_ptr(), scales.data_ptr(), zeros.data_ptr(), out.data_ptr(), N, K, _stream_ptr(Wq.device)))
+    return out
+
+
+def autotune(op: int, M: int, N: int, K: int) -> None:
+    torch = _torch()
+    check("mbw_autotune", lib().mbw_autotune(op, M, N, K, torch.cuda.current_stream().cuda_stream))
+
+
+def plan_describe(op: int, M: int, N: int, K: int) -> str:
+    buf = ctypes.create_string_buffer(256)
+    check("mbw_plan_describe", lib().mbw_plan_describe(op, M, N, K, buf, 256))
+    return buf.value.decode()
+
+
+def plan_candidates(op: int, M: int, N: int, K: int) -> int:
+    return int(lib().mbw_plan_candidates(op, M, N, K))
+
+
+def plan_select(op: int, M: int, N: int, K: int, index: int) -> None:
+    check("mbw_plan_select", lib().mbw_plan_select(op, M, N, K, index))
+
+
+def workspace_bytes(op: int, M: int, N: int, K: int) -> int:
+    return int(lib().mbw_workspace_bytes(op, M, N, K))
+
+
+def launch_count() -> int:
+    return int(lib().mbw_launch_count())
+
+
+def check_device_error() -> None:
+    check("mbw_check_device_error", lib().mbw_check_device_error())

@@ -1,0 +1,216 @@
+// abi.cu -- the extern "C" entry points of libmbw.so (declared in mbw.h):
+// argument checks on the host, plan lookup, launch, status reporting.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include <climits>
+#include <cstring>
+#include <string>
+
+#include "internal.h"
+#include "mbw.h"
+
+namespace mbw {
+
+static thread_local std::string g_last_error;
+static thread_local int g_out_f32 = 0;
+static thread_local uint64_t g_launches = 0;
+
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+void count_launch() { ++g_launches; }
+
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+static mbw_status fail(mbw_status st, const std::string& msg) {
+    g_last_error = msg;
+    return st;
+}
+
+static mbw_status cuda_fail(cudaError_t e, const char* where) {
+    g_last_error = std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    return MBW_ERR_CUDA;
+}
+
+static bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Common size checks. Returns MBW_OK, or an error with the detail set.
+static mbw_status check_sizes(const char* fn, int64_t M, int64_t N, int64_t K, int64_t kunit) {
+    if (M < 0 || N < 0 || K < 0) return fail(MBW_ERR_INVALID_ARG, std::string(fn) + ": negative size");
+    if (N > INT_MAX || K > INT_MAX || M > INT_MAX)
+        return fail(MBW_ERR_BAD_SHAPE, std::string(fn) + ": N, K and M must be below 2^31");
+    if (K % kunit != 0)
+        return fail(MBW_ERR_BAD_SHAPE, std::string(fn) + ": K must be a multiple of " + std::to_string(kunit));
+    return MBW_OK;
+}
+
+static mbw_status zero_output(void* y, int64_t M, int64_t N, cudaStream_t s) {
+    const size_t bytes = (size_t)M * (size_t)N * (g_out_f32 ? 4 : 2);
+    cudaError_t e = cudaMemsetAsync(y, 0, bytes, s);
+    return e == cudaSuccess ? MBW_OK : cuda_fail(e, "cudaMemsetAsync");
+}
+
+// Run a CUDA-core streaming GEMV over M activation rows, in slices of the
+// planned kernel's batch width.
+static mbw_status run_simt(int fmt, int op, const uint8_t* W, const uint16_t* scales, const uint8_t* zeros,
+                           const uint16_t* X, void* Y, int64_t M, int64_t N, int64_t K, cudaStream_t s) {
+    const Plan p = plan_lookup(op, M, N, K, s);
+    const SimtConfig c = simt_config(fmt, p.cfg);
+    GemvArgs a;
+    a.W = W;
+    a.scales = scales;
+    a.zeros = zeros;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.chunks = (int)(fmt == FMT_BF16 ? K / 8 : K / 32);
+    a.split_chunks = (a.chunks + p.split - 1) / p.split;
+    a.groups = (int)(fmt == FMT_G64 ? K / 64 : fmt == FMT_AWQ ? K / 128 : 0);
+    a.zstride = (a.groups + 1) / 2;
+    a.out_f32 = g_out_f32;
+    const size_t ybytes = g_out_f32 ? 4 : 2;
+    for (int64_t m0 = 0; m0 < M; m0 += c.mb) {
+        a.x = X + m0 * K;
+        a.y = static_cast<char*>(Y) + (size_t)m0 * (size_t)N * ybytes;
+        a.M = (int)((M - m0) < c.mb ? (M - m0) : c.mb);
+        cudaError_t e = launch_gemv_simt(fmt, p, a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
+    }
+    return MBW_OK;
+}
+
+}  // namespace mbw
+
+using namespace mbw;
+
+extern "C" {
+
+mbw_status gemv_bf16(const void* W, const void* x, void* y, int64_t N, int64_t K, void* workspace,
+                     size_t ws_bytes, mbw_stream_t stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    mbw_status st = check_sizes("gemv_bf16", 1, N, K, 8);
+    if (st != MBW_OK) return st;
+    if (N == 0) return MBW_OK;
+    if (!y || (K > 0 && (!W || !x))) return fail(MBW_ERR_INVALID_ARG, "gemv_bf16: NULL pointer");
+    if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 16))
+        return fail(MBW_ERR_MISALIGNED, "gemv_bf16: W, x and y must be 16-byte aligned");
+    if (K == 0) return zero_output(y, 1, N, (cudaStream_t)stream);
+    return run_simt(FMT_BF16, MBW_OP_GEMV_BF16, (const uint8_t*)W, nullptr, nullptr, (const uint16_t*)x, y, 1, N,
+                    K, (cudaStream_t)stream);
+}
+
+mbw_status gemv_int4_g64(const uint8_t* Wq, const void* scales, const void* x, void* y, int64_t N, int64_t K,
+                         void* workspace, size_t ws_bytes, mbw_stream_t stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    mbw_status st = check_sizes("gemv_int4_g64", 1, N, K, 64);
+    if (st != MBW_OK) return st;
+    if (N == 0) return MBW_OK;
+    if (!y || (K > 0 && (!Wq || !scales || !x))) return fail(MBW_ERR_INVALID_ARG, "gemv_int4_g64: NULL pointer");
+    if (!aligned(Wq, 16) || !aligned(x, 16) || !aligned(y, 16) || !aligned(scales, 2))
+        return fail(MBW_ERR_MISALIGNED, "gemv_int4_g64: Wq, x and y must be 16-byte aligned, scales 2-byte");
+    if (K == 0) return zero_output(y, 1, N, (cudaStream_t)stream);
+    return run_simt(FMT_G64, MBW_OP_GEMV_INT4_G64, Wq, (const uint16_t*)scales, nullptr, (const uint16_t*)x, y, 1,
+                    N, K, (cudaStream_t)stream);
+}
+
+mbw_status gemv_int4_awq_g128(const uint8_t* Wq, const void* scales, const uint8_t* zeros, const void* X, void* Y,
+                              int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
+                              mbw_stream_t stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    mbw_status st = check_sizes("gemv_int4_awq_g128", M, N, K, 128);
+    if (st != MBW_OK) return st;
+    if (N == 0 || M == 0) return MBW_OK;
+    if (!Y || (K > 0 && (!Wq || !scales || !zeros || !X)))
+        return fail(MBW_ERR_INVALID_ARG, "gemv_int4_awq_g128: NULL pointer");
+    if (!aligned(Wq, 16) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(scales, 2))
+        return fail(MBW_ERR_MISALIGNED, "gemv_int4_awq_g128: Wq, X and Y must be 16-byte aligned, scales 2-byte");
+    if (K == 0) return zero_output(Y, M, N, (cudaStream_t)stream);
+    return run_simt(FMT_AWQ, MBW_OP_GEMV_INT4_AWQ_G128, Wq, (const uint16_t*)scales, zeros, (const uint16_t*)X, Y,
+                    M, N, K, (cudaStream_t)stream);
+}
+
+mbw_status gemm_skinny_bf16(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,
+                            void* workspace, size_t ws_bytes, mbw_stream_t stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    mbw_status st = check_sizes("gemm_skinny_bf16", M, N, K, 8);
+    if (st != MBW_OK) return st;
+    if (N == 0 || M == 0) return MBW_OK;
+    if (!Y || (K > 0 && (!W || !X))) return fail(MBW_ERR_INVALID_ARG, "gemm_skinny_bf16: NULL pointer");
+    if (!aligned(W, 16) || !aligned(X, 16) || !aligned(Y, 16))
+        return fail(MBW_ERR_MISALIGNED, "gemm_skinny_bf16: X, W and Y must be 16-byte aligned");
+    if (K == 0) return zero_output(Y, M, N, (cudaStream_t)stream);
+    return run_simt(FMT_BF16, MBW_OP_GEMM_SKINNY_BF16, (const uint8_t*)W, nullptr, nullptr, (const uint16_t*)X, Y,
+                    M, N, K, (cudaStream_t)stream);
+}
+
+size_t mbw_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
+    (void)op;
+    (void)M;
+    (void)N;
+    (void)K;
+    return 0;
+}
+
+mbw_status mbw_dequant_int4_g64(const uint8_t* Wq, const void* scales, float* out, int64_t N, int64_t K,
+                                mbw_stream_t stream) {
+    mbw_status st = check_sizes("mbw_dequant_int4_g64", 1, N, K, 64);
+    if (st != MBW_OK) return st;
+    if (N == 0 || K == 0) return MBW_OK;
+    if (!Wq || !scales || !out) return fail(MBW_ERR_INVALID_ARG, "mbw_dequant_int4_g64: NULL pointer");
+    if (!aligned(scales, 2) || !aligned(out, 4)) return fail(MBW_ERR_MISALIGNED, "mbw_dequant_int4_g64: alignment");
+    cudaError_t e = launch_dequant(FMT_G64, Wq, (const uint16_t*)scales, nullptr, out, N, K, (cudaStream_t)stream);
+    return e == cudaSuccess ? MBW_OK : cuda_fail(e, "dequant launch");
+}
+
+mbw_status mbw_dequant_int4_awq_g128(const uint8_t* Wq, const void* scales, const uint8_t* zeros, float* out,
+                                     int64_t N, int64_t K, mbw_stream_t stream) {
+    mbw_status st = check_sizes("mbw_dequant_int4_awq_g128", 1, N, K, 128);
+    if (st != MBW_OK) return st;
+    if (N == 0 || K == 0) return MBW_OK;
+    if (!Wq || !scales || !zeros || !out)
+        return fail(MBW_ERR_INVALID_ARG, "mbw_dequant_int4_awq_g128: NULL pointer");
+    if (!aligned(scales, 2) || !aligned(out, 4))
+        return fail(MBW_ERR_MISALIGNED, "mbw_dequant_int4_awq_g128: alignment");
+    cudaError_t e = launch_dequant(FMT_AWQ, Wq, (const uint16_t*)scales, zeros, out, N, K, (cudaStream_t)stream);
+    return e == cudaSuccess ? MBW_OK : cuda_fail(e, "dequant launch");
+}
+
+mbw_status mbw_set_output_fp32(int enable) {
+    if (enable != 0 && enable != 1) return fail(MBW_ERR_INVALID_ARG, "mbw_set_output_fp32: 0 or 1");
+    g_out_f32 = enable;
+    return MBW_OK;
+}
+
+mbw_status mbw_check_device_error(void) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    return MBW_OK;
+}
+
+uint64_t mbw_launch_count(void) { return g_launches; }
+
+const char* mbw_status_string(mbw_status s) {
+    switch (s) {
+        case MBW_OK: return "MBW_OK";
+        case MBW_ERR_INVALID_ARG: return "MBW_ERR_INVALID_ARG";
+        case MBW_ERR_MISALIGNED: return "MBW_ERR_MISALIGNED";
+        case MBW_ERR_BAD_SHAPE: return "MBW_ERR_BAD_SHAPE";
+        case MBW_ERR_WORKSPACE_TOO_SMALL: return "MBW_ERR_WORKSPACE_TOO_SMALL";
+        case MBW_ERR_UNSUPPORTED: return "MBW_ERR_UNSUPPORTED";
+        case MBW_ERR_CUDA: return "MBW_ERR_CUDA";
+        case MBW_ERR_DEVICE_TIMEOUT: return "MBW_ERR_DEVICE_TIMEOUT";
+        default: return "MBW_ERR_UNKNOWN";
+    }
+}
+
+const char* mbw_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

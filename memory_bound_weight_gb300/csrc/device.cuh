@@ -1,0 +1,99 @@
+// device.cuh -- small sm_103a device helpers shared by the libmbw kernels:
+// streaming 16/32-byte weight loads, programmatic dependent launch controls,
+// warp reductions and the number formats the kernels read.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace mbw {
+
+// ---------------------------------------------------------------- loads ----
+// Weights are read exactly once per call: bypass L1 and mark the lines
+// evict-first in L2 so they do not push out x, scales and the next kernel's
+// prefetched tiles.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+struct u32x8 {
+    uint32_t v[8];
+};
+
+// 32-byte load (sm_100+ 256-bit ld.global), evict-first in L2.
+__device__ __forceinline__ u32x8 ld_stream32(const void* p) {
+    u32x8 r;
+    asm volatile(
+        "ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]), "=r"(r.v[4]), "=r"(r.v[5]),
+          "=r"(r.v[6]), "=r"(r.v[7])
+        : "l"(p));
+    return r;
+}
+
+// Read-only data reused across warps (x, scales): normal caching.
+__device__ __forceinline__ uint4 ld_ro16(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint16_t ld_ro_u16(const void* p) {
+    uint16_t r;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint8_t ld_ro_u8(const void* p) {
+    uint16_t r;
+    asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(r) : "l"(p));
+    return (uint8_t)r;
+}
+
+// ------------------------------------------- programmatic dependent launch ----
+// The next kernel in the stream may start its prologue (weight prefetch) once
+// every CTA of this grid has issued launch_dependents.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Block until the previous grid in the stream has completed and its memory is
+// visible. A no-op when the kernel was launched without the PDL attribute.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ------------------------------------------------------------- formats ----
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t h) {
+    return __half2float(__ushort_as_half(h));
+}
+
+// Exact float of a 4-bit code n (0..15) minus an integer offset `zf` given as
+// 2^23 + z: 2^23 + n is exact in fp32, and so is the difference n - z.
+__device__ __forceinline__ float code_minus(uint32_t n, float zf) {
+    return __uint_as_float(0x4B000000u | n) - zf;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ void store_out(void* y, int64_t idx, float v, int out_f32) {
+    if (out_f32)
+        static_cast<float*>(y)[idx] = v;
+    else
+        static_cast<__nv_bfloat16*>(y)[idx] = __float2bfloat16_rn(v);
+}
+
+}  // namespace mbw

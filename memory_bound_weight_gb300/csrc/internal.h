@@ -1,0 +1,66 @@
+// internal.h -- host-side declarations shared by the libmbw translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "mbw.h"
+
+namespace mbw {
+
+enum Fmt : int { FMT_BF16 = 0, FMT_G64 = 1, FMT_AWQ = 2 };
+
+// Arguments of one weight-streaming GEMV launch. A "chunk" is 16 bytes of one
+// weight row: 8 bf16 weights or 32 INT4 codes.
+struct GemvArgs {
+    const uint8_t* W;        // weight rows, `chunks` 16-byte chunks each
+    const uint16_t* scales;  // fp16 group scales [N][groups] (INT4 only)
+    const uint8_t* zeros;    // packed uint4 zero points [N][zstride] (AWQ only)
+    const uint16_t* x;       // bf16 activations [M][K]
+    void* y;                 // bf16 or fp32 outputs [M][N]
+    int N, K, M;
+    int chunks;        // 16-byte chunks per weight row
+    int split_chunks;  // chunks handled by one CTA of a split-K cluster
+    int groups;        // scale groups per row
+    int zstride;       // zero-point bytes per row
+    int out_f32;       // 1: write fp32 y
+};
+
+// One instantiation of the CUDA-core streaming kernel.
+struct SimtConfig {
+    int warps;  // warps per CTA, each owning its own rows
+    int r;      // rows per warp, streamed together
+    int u;      // 16-byte chunks per lane per row in flight
+    int mb;     // activation rows (batch) per launch
+};
+
+// Execution plan of one call shape.
+struct Plan {
+    int kind;   // PLAN_SIMT
+    int cfg;    // index into the kernel table of `kind`
+    int split;  // CTAs per cluster along K (1 = no split)
+};
+enum PlanKind : int { PLAN_SIMT = 0, PLAN_TC = 1 };
+
+// Kernel tables (gemv_simt.cu).
+int simt_num_configs(int fmt);
+SimtConfig simt_config(int fmt, int idx);
+cudaError_t launch_gemv_simt(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
+size_t simt_smem_bytes(int fmt, const SimtConfig& c, const GemvArgs& a, int split);
+
+cudaError_t launch_dequant(int fmt, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zeros,
+                           float* out, int64_t N, int64_t K, cudaStream_t s);
+
+// Plan cache (plan.cpp).
+Plan plan_lookup(int op, int64_t M, int64_t N, int64_t K, cudaStream_t s);
+Plan plan_default(int op, int64_t M, int64_t N, int64_t K);
+std::string plan_to_string(int op, const Plan& p);
+
+// Error reporting (abi.cu).
+void set_last_error(const std::string& msg);
+void count_launch();
+int device_sm_count();
+
+}  // namespace mbw

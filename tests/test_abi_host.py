@@ -1,0 +1,126 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute call is made).
+
+The library must load, export every function include/mbw.h declares, and
+reject bad arguments with a status before it touches CUDA.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from memory_bound_weight_gb300 import _binding as B
+from memory_bound_weight_gb300 import build as mbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mbw.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    mbuild.build()
+    return B.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\*?\s*\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while")))
+
+
+def test_header_declares_the_four_entry_points():
+    names = declared_functions()
+    for n in ("gemv_bf16", "gemv_int4_g64", "gemv_int4_awq_g128", "gemm_skinny_bf16"):
+        assert n in names
+    assert len(names) >= 16
+
+
+def test_every_declared_symbol_is_exported(L):
+    raw = ctypes.CDLL(B.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(raw, n), n
+
+
+def test_binding_covers_the_header(L):
+    assert sorted(B.SIGNATURES) == declared_functions()
+
+
+def test_input_generator_library_is_separate(L):
+    gen = ctypes.CDLL(os.path.join(os.path.dirname(B.LIB_PATH), "libmbw_inputs.so"))
+    for n in ("mbw_gen_bf16_table", "mbw_gen_bytes", "mbw_gen_f16_scales"):
+        assert hasattr(gen, n)
+    raw = ctypes.CDLL(B.LIB_PATH)
+    assert not hasattr(raw, "mbw_gen_bytes")
+
+
+def test_status_strings(L):
+    for code, name in [(0, "MBW_OK"), (1, "MBW_ERR_INVALID_ARG"), (2, "MBW_ERR_MISALIGNED"),
+                       (3, "MBW_ERR_BAD_SHAPE"), (4, "MBW_ERR_WORKSPACE_TOO_SMALL"), (5, "MBW_ERR_UNSUPPORTED"),
+                       (6, "MBW_ERR_CUDA"), (7, "MBW_ERR_DEVICE_TIMEOUT")]:
+        assert L.mbw_status_string(code).decode() == name
+
+
+A16 = 0x10000  # fake, 16-byte aligned addresses: never dereferenced on these paths
+A16b = 0x20000
+A16c = 0x30000
+
+
+@pytest.mark.parametrize("call,expect", [
+    (lambda L: L.gemv_bf16(A16, A16b, A16c, -1, 64, None, 0, None), 1),
+    (lambda L: L.gemv_bf16(A16, A16b, A16c, 8, 60, None, 0, None), 3),
+    (lambda L: L.gemv_bf16(A16 + 2, A16b, A16c, 8, 64, None, 0, None), 2),
+    (lambda L: L.gemv_bf16(A16, A16b + 8, A16c, 8, 64, None, 0, None), 2),
+    (lambda L: L.gemv_bf16(None, A16b, A16c, 8, 64, None, 0, None), 1),
+    (lambda L: L.gemv_bf16(A16, A16b, A16c, 1 << 31, 64, None, 0, None), 3),
+    (lambda L: L.gemv_bf16(None, None, None, 0, 64, None, 0, None), 0),  # N == 0: no-op
+    (lambda L: L.gemv_int4_g64(A16, A16b, A16c, A16c, 8, 96, None, 0, None), 3),
+    (lambda L: L.gemv_int4_g64(A16, A16b + 1, A16c, A16c, 8, 128, None, 0, None), 2),
+    (lambda L: L.gemv_int4_g64(A16, None, A16c, A16c, 8, 128, None, 0, None), 1),
+    (lambda L: L.gemv_int4_awq_g128(A16, A16b, A16c, A16c, A16, 1, 8, 192, None, 0, None), 3),
+    (lambda L: L.gemv_int4_awq_g128(A16, A16b, None, A16c, A16, 1, 8, 256, None, 0, None), 1),
+    (lambda L: L.gemv_int4_awq_g128(A16, A16b, A16c, A16c, A16, 0, 8, 256, None, 0, None), 0),
+    (lambda L: L.gemv_int4_awq_g128(A16, A16b, A16c, A16c, A16, -2, 8, 256, None, 0, None), 1),
+    (lambda L: L.gemm_skinny_bf16(A16, A16b, A16c, 4, 8, 12, None, 0, None), 3),
+    (lambda L: L.gemm_skinny_bf16(A16, A16b, A16c + 4, 4, 8, 16, None, 0, None), 2),
+    (lambda L: L.gemm_skinny_bf16(A16, A16b, A16c, 0, 8, 16, None, 0, None), 0),
+    (lambda L: L.mbw_dequant_int4_g64(A16, A16b, A16c, 4, 100, None), 3),
+    (lambda L: L.mbw_dequant_int4_awq_g128(A16, A16b, None, A16c, 4, 128, None), 1),
+    (lambda L: L.mbw_set_output_fp32(2), 1),
+    (lambda L: L.mbw_plan_select(9, 1, 8, 64, 0), 1),
+    (lambda L: L.mbw_autotune(9, 1, 8, 64, None), 1),
+])
+def test_argument_errors_without_cuda(L, call, expect):
+    assert call(L) == expect
+    if expect != 0:
+        assert L.mbw_last_error().decode() != ""
+
+
+def test_planner_host_logic(L):
+    # candidate enumeration and plan description run on the host
+    for op, M, N, K in [(1, 1, 2048, 2048), (2, 1, 2048, 5632), (3, 16, 3584, 18944), (4, 8, 18944, 3584)]:
+        n = L.mbw_plan_candidates(op, M, N, K)
+        assert n >= 1
+        buf = ctypes.create_string_buffer(256)
+        assert L.mbw_plan_describe(op, M, N, K, buf, 256) == 0
+        assert b"split_k=" in buf.value
+    assert L.mbw_plan_candidates(2, 1, 8, 96) == 0  # K not a multiple of 64
+    assert L.mbw_plan_candidates(7, 1, 8, 64) == 0
+    assert L.mbw_workspace_bytes(1, 1, 2048, 2048) == 0
+
+
+def test_output_hook_is_thread_local(L):
+    import threading
+
+    assert L.mbw_set_output_fp32(1) == 0
+    seen = []
+
+    def other():
+        # a fresh thread starts with bf16 output; setting it there does not leak back
+        seen.append(L.mbw_set_output_fp32(0))
+
+    t = threading.Thread(target=other)
+    t.start()
+    t.join()
+    assert seen == [0]
+    assert L.mbw_set_output_fp32(0) == 0
