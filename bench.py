@@ -53,6 +53,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--per-matrix", action="store_true", help="also time each distinct shape on its own")
+    p.add_argument("--profile-range", action="store_true",
+                   help="bracket the timed region with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     return p.parse_args()
 
 
@@ -343,6 +345,8 @@ def main():
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier(ws)
+    if args.profile_range:
+        torch.cuda.profiler.start()
     t0 = time.time()
     e0.record(stream)
     for _ in range(args.steps):
@@ -350,6 +354,8 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
+    if args.profile_range:
+        torch.cuda.profiler.stop()
     barrier(ws)
     sampler.stop()
     ms = e0.elapsed_time(e1)
