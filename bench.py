@@ -53,6 +53,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--per-matrix", action="store_true", help="also time each distinct shape on its own")
+    p.add_argument("--plans-out", default=None, help="write the tuned plan index of every shape to this JSON file")
+    p.add_argument("--plans-from", default=None, help="restore plans from a --plans-out file instead of tuning")
     p.add_argument("--profile-range", action="store_true",
                    help="bracket the timed region with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     return p.parse_args()
@@ -318,8 +320,17 @@ def main():
     import memory_bound_weight_gb300 as mbw
 
     step = make_step(args.workload, seed=0, device=device)
-    for N, K in step.shapes():
-        mbw.autotune(step.op, 1, N, K)
+    if args.plans_from:
+        with open(args.plans_from) as f:
+            saved = json.load(f)
+        for N, K in step.shapes():
+            mbw.plan_select(step.op, 1, N, K, int(saved[f"{N}x{K}"]))
+    else:
+        for N, K in step.shapes():
+            mbw.autotune(step.op, 1, N, K)
+    if args.plans_out and rank == 0:
+        with open(args.plans_out, "w") as f:
+            json.dump({f"{N}x{K}": mbw.plan_index(step.op, 1, N, K) for N, K in step.shapes()}, f)
     plans = {f"{N}x{K}": mbw.plan_describe(step.op, 1, N, K) for N, K in step.shapes()}
     step.run()
     torch.cuda.synchronize()

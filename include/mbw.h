@@ -153,6 +153,11 @@ int mbw_plan_candidates(int op, int64_t M, int64_t N, int64_t K);
  * measured earlier, and lets tests run every kernel instantiation. */
 mbw_status mbw_plan_select(int op, int64_t M, int64_t N, int64_t K, int index);
 
+/* Index (among mbw_plan_candidates) of the plan this shape currently uses, so
+ * that a tuned plan can be saved and restored with mbw_plan_select; -1 for a
+ * bad op or shape. */
+int mbw_plan_index(int op, int64_t M, int64_t N, int64_t K);
+
 /* Write a one-line description of the plan a call of this shape would use
  * into buf (NUL-terminated, truncated to len). Returns MBW_OK. */
 mbw_status mbw_plan_describe(int op, int64_t M, int64_t N, int64_t K, char *buf, size_t len);

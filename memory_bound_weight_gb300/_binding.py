@@ -41,6 +41,7 @@ SIGNATURES = {
     "mbw_autotune": ([ctypes.c_int, _I64, _I64, _I64, _P], _ST),
     "mbw_plan_candidates": ([ctypes.c_int, _I64, _I64, _I64], ctypes.c_int),
     "mbw_plan_select": ([ctypes.c_int, _I64, _I64, _I64, ctypes.c_int], _ST),
+    "mbw_plan_index": ([ctypes.c_int, _I64, _I64, _I64], ctypes.c_int),
     "mbw_plan_describe": ([ctypes.c_int, _I64, _I64, _I64, ctypes.c_char_p, _SZ], _ST),
     "mbw_check_device_error": ([], _ST),
     "mbw_launch_count": ([], ctypes.c_uint64),
@@ -256,6 +257,10 @@ def plan_candidates(op: int, M: int, N: int, K: int) -> int:
 
 def plan_select(op: int, M: int, N: int, K: int, index: int) -> None:
     check("mbw_plan_select", lib().mbw_plan_select(op, M, N, K, index))
+
+
+def plan_index(op: int, M: int, N: int, K: int) -> int:
+    return int(lib().mbw_plan_index(op, M, N, K))
 
 
 def workspace_bytes(op: int, M: int, N: int, K: int) -> int:

@@ -172,6 +172,15 @@ extern "C" int mbw_plan_candidates(int op, int64_t M, int64_t N, int64_t K) {
     return (int)candidates(op, M, N, K).size();
 }
 
+extern "C" int mbw_plan_index(int op, int64_t M, int64_t N, int64_t K) {
+    if (!shape_ok(op, M, N, K)) return -1;
+    const Plan cur = plan_lookup(op, M, N, K, nullptr);
+    const std::vector<Plan> c = candidates(op, M, N, K);
+    for (size_t i = 0; i < c.size(); ++i)
+        if (c[i].kind == cur.kind && c[i].cfg == cur.cfg && c[i].split == cur.split) return (int)i;
+    return -1;
+}
+
 extern "C" mbw_status mbw_plan_select(int op, int64_t M, int64_t N, int64_t K, int index) {
     if (!shape_ok(op, M, N, K)) {
         set_last_error("mbw_plan_select: bad op or shape");
