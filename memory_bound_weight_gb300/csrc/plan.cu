@@ -209,6 +209,20 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
         set_last_error("mbw_autotune: stream is capturing");
         return MBW_ERR_INVALID_ARG;
     }
+    // Timing graphs are captured on a private stream (the caller's may be the
+    // legacy default stream, which cannot be captured); the caller's stream
+    // is drained first so that tuning does not overlap its work.
+    cudaError_t se = cudaStreamSynchronize(stream);
+    if (se != cudaSuccess) {
+        set_last_error(std::string("mbw_autotune: ") + cudaGetErrorString(se));
+        return MBW_ERR_CUDA;
+    }
+    cudaStream_t user_stream = stream;
+    se = cudaStreamCreateWithFlags(&stream, cudaStreamNonBlocking);
+    if (se != cudaSuccess) {
+        set_last_error(std::string("mbw_autotune: ") + cudaGetErrorString(se));
+        return MBW_ERR_CUDA;
+    }
     const int64_t Mb = std::min<int64_t>(M, 8);
     const size_t wb = weight_bytes(fmt, N, K);
     const size_t wstride = (wb + 255) / 256 * 256;
@@ -291,6 +305,9 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
             }
         }
     }
+    cudaStreamSynchronize(stream);
+    cudaStreamDestroy(stream);
+    (void)user_stream;
     if (t0) cudaEventDestroy(t0);
     if (t1) cudaEventDestroy(t1);
     if (wbuf) cudaFree(wbuf);
