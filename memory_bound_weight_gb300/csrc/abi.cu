@@ -60,7 +60,7 @@ static mbw_status zero_output(void* y, int64_t M, int64_t N, cudaStream_t s) {
 static mbw_status run_simt(int fmt, int op, const uint8_t* W, const uint16_t* scales, const uint8_t* zeros,
                            const uint16_t* X, void* Y, int64_t M, int64_t N, int64_t K, cudaStream_t s) {
     const Plan p = plan_lookup(op, M, N, K, s);
-    const SimtConfig c = simt_config(fmt, p.cfg);
+    const int width = plan_batch_width(fmt, p);
     GemvArgs a;
     a.W = W;
     a.scales = scales;
@@ -73,11 +73,11 @@ static mbw_status run_simt(int fmt, int op, const uint8_t* W, const uint16_t* sc
     a.zstride = (a.groups + 1) / 2;
     a.out_f32 = g_out_f32;
     const size_t ybytes = g_out_f32 ? 4 : 2;
-    for (int64_t m0 = 0; m0 < M; m0 += c.mb) {
+    for (int64_t m0 = 0; m0 < M; m0 += width) {
         a.x = X + m0 * K;
         a.y = static_cast<char*>(Y) + (size_t)m0 * (size_t)N * ybytes;
-        a.M = (int)((M - m0) < c.mb ? (M - m0) : c.mb);
-        cudaError_t e = launch_gemv_simt(fmt, p, a, s);
+        a.M = (int)((M - m0) < width ? (M - m0) : width);
+        cudaError_t e = launch_plan(fmt, p, a, s);
         if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
     }
     return MBW_OK;

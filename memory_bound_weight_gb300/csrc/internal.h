@@ -36,13 +36,21 @@ struct SimtConfig {
     int mb;     // activation rows (batch) per launch
 };
 
+// One instantiation of the tensor-core (mma.sync) streaming kernel.
+struct MmaConfig {
+    int warps;  // warps per CTA
+    int r16;    // 16-row tiles per warp
+    int u;      // 64-byte row blocks per lane in flight
+};
+
 // Execution plan of one call shape.
 struct Plan {
-    int kind;   // PLAN_SIMT
+    int kind;   // PLAN_SIMT or PLAN_MMA
     int cfg;    // index into the kernel table of `kind`
     int split;  // CTAs per cluster along K (1 = no split)
+    int wk;     // k-slices per CTA (MMA kernels; 1 for SIMT)
 };
-enum PlanKind : int { PLAN_SIMT = 0, PLAN_TC = 1 };
+enum PlanKind : int { PLAN_SIMT = 0, PLAN_MMA = 1 };
 
 // Kernel tables (gemv_simt.cu).
 int simt_num_configs(int fmt);
@@ -50,13 +58,22 @@ SimtConfig simt_config(int fmt, int idx);
 cudaError_t launch_gemv_simt(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
 size_t simt_smem_bytes(int fmt, const SimtConfig& c, const GemvArgs& a, int split);
 
+// Tensor-core kernel tables (gemv_mma.cu).
+int mma_num_configs(int fmt);
+MmaConfig mma_config(int fmt, int idx);
+int mma_max_batch(int fmt);
+size_t mma_smem_bytes(int fmt, const MmaConfig& c, int64_t K, int M, int split, int wk);
+cudaError_t launch_gemv_mma(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
+
 cudaError_t launch_dequant(int fmt, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zeros,
                            float* out, int64_t N, int64_t K, cudaStream_t s);
 
-// Plan cache (plan.cpp).
+// Plan cache (plan.cu).
 Plan plan_lookup(int op, int64_t M, int64_t N, int64_t K, cudaStream_t s);
 Plan plan_default(int op, int64_t M, int64_t N, int64_t K);
 std::string plan_to_string(int op, const Plan& p);
+int plan_batch_width(int fmt, const Plan& p);  // activation rows per launch
+cudaError_t launch_plan(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
 
 // Error reporting (abi.cu).
 void set_last_error(const std::string& msg);
