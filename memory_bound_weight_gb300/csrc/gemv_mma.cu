@@ -5,30 +5,34 @@
 // group-128 weights and a small batch M (1..8; 1..4 for group-64).
 //
 // Why mma here: at batch 1 every weight is used for one multiply-add (llm-rs
-// vs vLLM, sec. 2), so the kernel must retire ~41 INT4 weights per SM clock to
-// keep up with HBM on GB300 -- about 3 issue slots per weight. Unpacking a
-// nibble and doing the fp32 multiply-add on the CUDA cores costs ~4. Here the
-// CUDA cores only turn codes into bf16 pairs (one LOP3 per two codes, one
-// exact bf16 subtract), and mma.sync.m16n8k16 retires the multiply-adds with
-// fp32 accumulation, taking its A operand straight from the registers the
-// weight stream was loaded into. The batch rides in the MMA's n = 8 columns.
-// (tcgen05 would need the operand staged through shared memory and a TMEM
-// round trip per group; the batched skinny GEMM uses it where M >= 16.)
+// vs vLLM, sec. 2), so at GB300's HBM rate the kernel must retire ~41 INT4
+// weights per SM clock -- about 3 issue slots per weight. Unpacking a nibble
+// and doing the fp32 multiply-add on the CUDA cores costs ~4 (measured: the
+// CUDA-core kernel saturates its integer pipe at a third of HBM bandwidth).
+// Here the CUDA cores only turn codes into bf16 pairs (one LOP3 per two codes
+// and one exact bf16 subtract), and mma.sync.m16n8k16 retires the multiply-
+// adds with fp32 accumulation, taking its A operand straight from the
+// registers the weight stream was loaded into. The batch rides in the MMA's
+// n = 8 columns. (tcgen05 would need the operand staged through shared memory
+// and a TMEM round trip per scale group; the batched skinny GEMM uses it.)
 //
-// Work decomposition:
-//   * warp task = 16*R16 weight rows x one k-slice; lane (g = lane/4,
-//     q = lane%4) loads 16 bytes of rows g and g+8 per 64-byte block of each
-//     row, i.e. the 4 lanes of a quad read 64 contiguous bytes of a row;
-//   * CTA = (W / WK) row tiles x WK k-slices; a cluster of S CTAs splits K
-//     further. Partial sums are reduced in shared memory across the CTA's
-//     k-slices and through distributed shared memory across the cluster, in a
-//     fixed order (deterministic, no global scratch, no spin waits);
-//   * every lane keeps U blocks of weights in flight (register double
-//     buffer); with programmatic dependent launch the first U blocks are
-//     requested before the kernel waits for the previous grid, and x is read
-//     only after that wait;
-//   * x (the CTA's k-range) is staged once per CTA in shared memory, in the
-//     order the B fragments need it.
+// Work decomposition (balanced and persistent):
+//   * the weight rows are cut into 16-row tiles; CTA row-group c of G owns
+//     the contiguous tile range [c*T/G, (c+1)*T/G), so no SM gets more than
+//     one tile more than another;
+//   * inside a CTA every warp owns one k-slice of every tile (K split W ways,
+//     and S ways more across a thread-block cluster for short, wide shapes);
+//     lane (g = lane/4, q = lane%4) loads 16 bytes of rows g and g+8 per
+//     64-byte row block, so a quad reads 64 contiguous bytes of a row;
+//   * a warp walks its (tile, block) sequence through a U-deep register ring:
+//     consume slot u, refill it with the block U steps ahead, so loads keep
+//     flowing across tile boundaries; per-tile partial sums go to shared
+//     memory and are summed over warps (and cluster ranks, through
+//     distributed shared memory) once, in a fixed order: deterministic, no
+//     global scratch, no spin waits;
+//   * programmatic dependent launch: the ring is filled before the kernel
+//     waits for the previous grid; x is staged (once per CTA, in the order the
+//     B fragments want it) only after that wait.
 //
 // Exactness: a code n in a bf16 pair is built as 0x4300 | n = 128 + n, and
 // 128 + n - (128 + z) = n - z is exact in bf16; products (n - z) * x are exact
@@ -52,8 +56,8 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// (v & 0x000F000F) | 0x43004300: the two nibbles at bits 0-3 and 16-19 as
-// bf16 values 128 + n.
+// (v & 0x000F000F) | 0x43004300: the nibbles at bits 0-3 and 16-19 as the
+// bf16 pair (128 + n_lo, 128 + n_hi).
 __device__ __forceinline__ uint32_t nib_pair(uint32_t v) {
     uint32_t r;
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(0x000F000Fu), "r"(0x43004300u));
@@ -92,11 +96,33 @@ struct MmaTraits<FMT_AWQ> {
     static constexpr int BK = 128;
 };
 
-template <int FMT, int W, int R16, int U>
+// Shared memory layout of one launch (bytes): x words (later reused for the
+// per-CTA sums) at 0, per-warp partial sums at red_off.
+struct MmaSmem {
+    int xwords;  // 16-byte x words per batch row
+    int ntmax;   // most tiles any CTA owns
+    size_t x_bytes, red_off, red_bytes, total;
+};
+
+__host__ __device__ inline MmaSmem mma_smem_layout(int BK, int64_t K, int N, int M, int W, int S, int G) {
+    MmaSmem L;
+    const int64_t KB = (K + BK - 1) / BK;
+    const int64_t BS = (KB + (int64_t)S * W - 1) / ((int64_t)S * W);
+    L.xwords = (int)(W * BS * (BK / 8));
+    const int T = (N + 15) / 16;
+    L.ntmax = (T + G - 1) / G;
+    L.x_bytes = (size_t)M * L.xwords * 16;
+    const size_t fin_bytes = (size_t)L.ntmax * 16 * M * 4;
+    L.red_off = ((L.x_bytes > fin_bytes ? L.x_bytes : fin_bytes) + 15) / 16 * 16;
+    L.red_bytes = (size_t)L.ntmax * W * 16 * M * 4;
+    L.total = L.red_off + L.red_bytes;
+    return L;
+}
+
+template <int FMT, int W, int U>
 __global__ void __launch_bounds__(W * 32)
-    gemv_mma_kernel(const GemvArgs a, const int S, const int WK) {
+    gemv_mma_kernel(const GemvArgs a, const int S) {
     constexpr int BK = MmaTraits<FMT>::BK;
-    constexpr int WPB = (FMT == FMT_BF16) ? 1 : 4;  // 16-byte x words per quad lane per block
     extern __shared__ uint4 smem_u4[];
 
     pdl_launch_dependents();
@@ -104,74 +130,75 @@ __global__ void __launch_bounds__(W * 32)
     const int rank = (S > 1) ? (int)cg::this_cluster().block_rank() : 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
-    const int wr = warp / WK, wk = warp - wr * WK;
-    const int KB = (a.K + BK - 1) / BK;
-    const int TS = S * WK;
-    const int BS = (KB + TS - 1) / TS;
-    const int b0 = (rank * WK + wk) * BS;
-    const int b1 = min(KB, b0 + BS);
-    const int nblk = max(0, b1 - b0);
-    const int iters = (nblk + U - 1) / U;
-    const int cb0 = rank * WK * BS;  // first block of this CTA's k-range
-    const int cnb = max(0, min(KB, cb0 + WK * BS) - cb0);
-    const int rows_cta = (W / WK) * 16 * R16;
-    const int tile_row = (blockIdx.x / S) * rows_cta + wr * 16 * R16;
-    const size_t rowbytes = (FMT == FMT_BF16) ? (size_t)a.K * 2 : (size_t)a.K / 2;
+    const int G = gridDim.x / S;
+    const int cgid = blockIdx.x / S;
+    const int T = (a.N + 15) / 16;
+    const int t0 = (int)(((long long)T * cgid) / G);
+    const int nt = (int)(((long long)T * (cgid + 1)) / G) - t0;
+    const int mb = a.M;
+    const MmaSmem L = mma_smem_layout(BK, a.K, a.N, mb, W, S, G);
 
-    int rowc[R16][2];
-    const uint8_t* wp[R16][2];
-#pragma unroll
-    for (int r = 0; r < R16; ++r)
+    const int KB = (a.K + BK - 1) / BK;
+    const int BS = (KB + S * W - 1) / (S * W);
+    const int cb0 = rank * W * BS;                  // first block of this CTA's k-range
+    const int b0 = cb0 + warp * BS;                 // this warp's k-slice
+    const int nb = max(0, min(KB, b0 + BS) - b0);
+    const int total = nt * nb;                      // (tile, block) steps of this warp
+    const size_t rowbytes = (FMT == FMT_BF16) ? (size_t)a.K * 2 : (size_t)a.K / 2;
+    const bool scale32 = (FMT == FMT_G64) && ((a.groups & 1) == 0) && ((((uintptr_t)a.scales) & 3) == 0);
+
+    // ring of U slots: codes of rows g and g+8, and their scale words
+    uint4 ring[U][2];
+    uint32_t sring[U][2];
+
+    // load the next step (tile t0 + ltile, block b0 + lblk) into slot u;
+    // steps are loaded strictly in order
+    int ltile = 0, lblk = 0;
+    auto load = [&](int u) {
+        const int b = b0 + lblk;
+        const int rbase = (t0 + ltile) * 16 + g;
+        if (++lblk == nb) {
+            lblk = 0;
+            ++ltile;
+        }
+        const bool kin = (b * BK + (q + 1) * (BK / 4)) <= a.K;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            rowc[r][h] = min(tile_row + 16 * r + g + 8 * h, a.N - 1);
-            wp[r][h] = a.W + (size_t)rowc[r][h] * rowbytes + q * 16;
-        }
-
-    uint4 cur[U][R16][2];
-    uint32_t scur[U][R16][2];  // g64: two fp16 scales; AWQ: fp16 scale | zero << 16
-
-    auto load = [&](uint4 (&buf)[U][R16][2], uint32_t (&sb)[U][R16][2], int it) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int b = b0 + it * U + u;
-            const bool ok = (b < b1) && ((b * BK + (q + 1) * (BK / 4)) <= a.K);
-#pragma unroll
-            for (int r = 0; r < R16; ++r)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    buf[u][r][h] = ok ? ld_stream16(wp[r][h] + (size_t)b * 64) : make_uint4(0, 0, 0, 0);
-                    if (FMT == FMT_G64) {
-                        const int gi = 2 * b;
-                        const uint16_t* sp = a.scales + (size_t)rowc[r][h] * a.groups + gi;
-                        const uint32_t s0 = (b < b1) ? ld_ro_u16(sp) : 0;
-                        const uint32_t s1 = (b < b1 && gi + 1 < a.groups) ? ld_ro_u16(sp + 1) : 0;
-                        sb[u][r][h] = s0 | (s1 << 16);
-                    } else if (FMT == FMT_AWQ) {
-                        const uint32_t s = (b < b1) ? ld_ro_u16(a.scales + (size_t)rowc[r][h] * a.groups + b) : 0;
-                        const uint32_t zb =
-                            (b < b1) ? ld_ro_u8(a.zeros + (size_t)rowc[r][h] * a.zstride + (b >> 1)) : 0;
-                        const uint32_t z = (b & 1) ? (zb >> 4) : (zb & 0xF);
-                        sb[u][r][h] = s | (z << 16);
-                    }
+            const int row = min(rbase + 8 * h, a.N - 1);
+            ring[u][h] = kin ? ld_stream16(a.W + (size_t)row * rowbytes + (size_t)b * 64 + q * 16)
+                             : make_uint4(0, 0, 0, 0);
+            if (FMT == FMT_G64) {
+                const uint16_t* sp = a.scales + (size_t)row * a.groups + 2 * b;
+                if (scale32) {
+                    sring[u][h] = __ldg(reinterpret_cast<const unsigned int*>(sp));
+                } else {
+                    const uint32_t s1 = (2 * b + 1 < a.groups) ? ld_ro_u16(sp + 1) : 0u;
+                    sring[u][h] = (uint32_t)ld_ro_u16(sp) | (s1 << 16);
                 }
+            } else if (FMT == FMT_AWQ) {
+                const uint32_t s = ld_ro_u16(a.scales + (size_t)row * a.groups + b);
+                const uint32_t zb = ld_ro_u8(a.zeros + (size_t)row * a.zstride + (b >> 1));
+                sring[u][h] = s | (((b & 1) ? (zb >> 4) : (zb & 0xF)) << 16);
+            }
         }
     };
 
-    if (iters > 0) load(cur, scur, 0);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (u < total) load(u);
 
+    // x is produced by the previous kernel in the stream: wait for it only now.
     pdl_wait();
 
-    // Stage x for blocks [cb0, cb0 + cnb) of every batch row:
-    // xs[m][(b - cb0) * (BK / 8) + word] (16-byte words of 8 k; INT4 pairs permuted).
-    const int mb = a.M;
-    const int xwords = cnb * (BK / 8);
-    for (int i = threadIdx.x; i < mb * xwords; i += W * 32) {
-        const int m = i / xwords;
-        const int wi = i - m * xwords;
+    // Stage x for the CTA's k-range: xs[m][w] = 16-byte word w (8 k) of batch
+    // row m, INT4 pairs permuted.
+    const int cwords = max(0, min(KB, cb0 + W * BS) - cb0) * (BK / 8);
+    for (int i = threadIdx.x; i < mb * L.xwords; i += W * 32) {
+        const int m = i / L.xwords;
+        const int wi = i - m * L.xwords;
         const int k = cb0 * BK + wi * 8;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (k < a.K) v = ld_ro16(a.x + (size_t)m * a.K + k);
+        if (wi < cwords && k < a.K) v = ld_ro16(a.x + (size_t)m * a.K + k);
         smem_u4[i] = (FMT == FMT_BF16) ? v : perm_pairs(v);
     }
     __syncthreads();
@@ -186,162 +213,144 @@ __global__ void __launch_bounds__(W * 32)
         xm = g;
         xon = xm < mb;
     }
-    const uint4* xrow = smem_u4 + (size_t)(xon ? xm : 0) * xwords;
+    const uint4* xw = smem_u4 + (size_t)(xon ? xm : 0) * L.xwords + (size_t)(b0 - cb0) * (BK / 8);
+    float* red = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.red_off);
 
-    float acc[R16][4];
-#pragma unroll
-    for (int r = 0; r < R16; ++r)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[r][i] = 0.f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int ct = 0, cb = 0;  // tile and block (within the k-slice) of the step being consumed
 
-    for (int it = 0; it < iters; ++it) {
-        uint4 nxt[U][R16][2];
-        uint32_t snxt[U][R16][2];
-        if (it + 1 < iters) load(nxt, snxt, it + 1);
+    for (int j0 = 0; j0 < total; j0 += U) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int b = b0 + it * U + u;
-            if (b < b1) {
-                const int lb = b - cb0;
+            const int j = j0 + u;
+            if (j < total) {
+                const uint4 wg = ring[u][0], wg8 = ring[u][1];
+                const uint32_t sg = sring[u][0], sg8 = sring[u][1];
+                if (j + U < total) load(u);
                 if (FMT == FMT_BF16) {
-                    const uint4 xv = xon ? xrow[lb * 4 + q] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                    for (int r = 0; r < R16; ++r) {
-                        const uint4 wg = cur[u][r][0], wg8 = cur[u][r][1];
-                        mma_bf16_16816(acc[r], wg.x, wg8.x, wg.y, wg8.y, xv.x, xv.y);
-                        mma_bf16_16816(acc[r], wg.z, wg8.z, wg.w, wg8.w, xv.z, xv.w);
-                    }
+                    const uint4 xv = xon ? xw[cb * 4 + q] : make_uint4(0, 0, 0, 0);
+                    mma_bf16_16816(acc, wg.x, wg8.x, wg.y, wg8.y, xv.x, xv.y);
+                    mma_bf16_16816(acc, wg.z, wg8.z, wg.w, wg8.w, xv.z, xv.w);
                 } else {
-                    uint4 xv[WPB];
+                    const uint32_t zg = (FMT == FMT_G64) ? 8u : (sg >> 16);
+                    const uint32_t zg8 = (FMT == FMT_G64) ? 8u : (sg8 >> 16);
+                    const uint32_t zz0 = (0x4300u | zg) * 0x00010001u;  // (128 + z, 128 + z)
+                    const uint32_t zz1 = (0x4300u | zg8) * 0x00010001u;
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                    const uint32_t wa[4] = {wg.x, wg.y, wg.z, wg.w};
+                    const uint32_t wb[4] = {wg8.x, wg8.y, wg8.z, wg8.w};
 #pragma unroll
-                    for (int j = 0; j < WPB; ++j) xv[j] = xon ? xrow[lb * 16 + 4 * q + j] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                    for (int r = 0; r < R16; ++r) {
-                        uint32_t zz[2];
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint32_t z = (FMT == FMT_G64) ? 8u : (scur[u][r][h] >> 16);
-                            zz[h] = (0x4300u | z) * 0x00010001u;  // (128 + z, 128 + z)
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const uint4 xv = xon ? xw[cb * 16 + 4 * q + jj] : make_uint4(0, 0, 0, 0);
+                        const uint32_t a4 = wa[jj] >> 4, b4 = wb[jj] >> 4;
+                        const uint32_t a8 = wa[jj] >> 8, b8 = wb[jj] >> 8;
+                        const uint32_t a12 = wa[jj] >> 12, b12 = wb[jj] >> 12;
+                        mma_bf16_16816(d, bf16x2_sub(nib_pair(wa[jj]), zz0), bf16x2_sub(nib_pair(wb[jj]), zz1),
+                                       bf16x2_sub(nib_pair(a4), zz0), bf16x2_sub(nib_pair(b4), zz1), xv.x, xv.y);
+                        mma_bf16_16816(d, bf16x2_sub(nib_pair(a8), zz0), bf16x2_sub(nib_pair(b8), zz1),
+                                       bf16x2_sub(nib_pair(a12), zz0), bf16x2_sub(nib_pair(b12), zz1), xv.z,
+                                       xv.w);
+                    }
+                    if (FMT == FMT_G64) {
+                        // columns 2m (even group) and 2m + 1 (odd group) of batch m = q
+                        acc[0] = fmaf(f16_bits_to_f32(sg & 0xFFFF), d[0], acc[0]);
+                        acc[0] = fmaf(f16_bits_to_f32(sg >> 16), d[1], acc[0]);
+                        acc[2] = fmaf(f16_bits_to_f32(sg8 & 0xFFFF), d[2], acc[2]);
+                        acc[2] = fmaf(f16_bits_to_f32(sg8 >> 16), d[3], acc[2]);
+                    } else {
+                        const float s0 = f16_bits_to_f32(sg & 0xFFFF), s1 = f16_bits_to_f32(sg8 & 0xFFFF);
+                        acc[0] = fmaf(s0, d[0], acc[0]);
+                        acc[1] = fmaf(s0, d[1], acc[1]);
+                        acc[2] = fmaf(s1, d[2], acc[2]);
+                        acc[3] = fmaf(s1, d[3], acc[3]);
+                    }
+                }
+                if (++cb == nb) {
+                    // tile done: its partials -> red[tile][warp][row][m]
+                    float* rp = red + ((size_t)(ct * W + warp) * 16) * mb;
+                    if (FMT == FMT_G64) {
+                        if (q < mb) {
+                            rp[g * mb + q] = acc[0];
+                            rp[(g + 8) * mb + q] = acc[2];
                         }
-                        float d[4] = {0.f, 0.f, 0.f, 0.f};
-                        const uint32_t* wg = &cur[u][r][0].x;
-                        const uint32_t* wg8 = &cur[u][r][1].x;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-                            for (int hh = 0; hh < 2; ++hh) {
-                                const int sh = 8 * hh;
-                                const uint32_t a0 = bf16x2_sub(nib_pair(wg[j] >> sh), zz[0]);
-                                const uint32_t a2 = bf16x2_sub(nib_pair(wg[j] >> (sh + 4)), zz[0]);
-                                const uint32_t a1 = bf16x2_sub(nib_pair(wg8[j] >> sh), zz[1]);
-                                const uint32_t a3 = bf16x2_sub(nib_pair(wg8[j] >> (sh + 4)), zz[1]);
-                                const uint32_t bb0 = hh ? xv[j].z : xv[j].x;
-                                const uint32_t bb1 = hh ? xv[j].w : xv[j].y;
-                                mma_bf16_16816(d, a0, a1, a2, a3, bb0, bb1);
-                            }
+                    } else {
+                        if (2 * q < mb) {
+                            rp[g * mb + 2 * q] = acc[0];
+                            rp[(g + 8) * mb + 2 * q] = acc[2];
                         }
-                        if (FMT == FMT_G64) {
-                            // columns 2m (even group) and 2m + 1 (odd group) of batch m = q
-                            const uint32_t sg = scur[u][r][0], sg8 = scur[u][r][1];
-                            acc[r][0] = fmaf(f16_bits_to_f32(sg & 0xFFFF), d[0], acc[r][0]);
-                            acc[r][0] = fmaf(f16_bits_to_f32(sg >> 16), d[1], acc[r][0]);
-                            acc[r][2] = fmaf(f16_bits_to_f32(sg8 & 0xFFFF), d[2], acc[r][2]);
-                            acc[r][2] = fmaf(f16_bits_to_f32(sg8 >> 16), d[3], acc[r][2]);
-                        } else {
-                            const float sg = f16_bits_to_f32(scur[u][r][0] & 0xFFFF);
-                            const float sg8 = f16_bits_to_f32(scur[u][r][1] & 0xFFFF);
-                            acc[r][0] = fmaf(sg, d[0], acc[r][0]);
-                            acc[r][1] = fmaf(sg, d[1], acc[r][1]);
-                            acc[r][2] = fmaf(sg8, d[2], acc[r][2]);
-                            acc[r][3] = fmaf(sg8, d[3], acc[r][3]);
+                        if (2 * q + 1 < mb) {
+                            rp[g * mb + 2 * q + 1] = acc[1];
+                            rp[(g + 8) * mb + 2 * q + 1] = acc[3];
                         }
                     }
+                    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                    cb = 0;
+                    ++ct;
                 }
             }
         }
-        if (it + 1 < iters) {
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int r = 0; r < R16; ++r)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        cur[u][r][h] = nxt[u][r][h];
-                        scur[u][r][h] = snxt[u][r][h];
-                    }
-        }
     }
-
-    // Partial sums -> red[row_in_cta][k-slice][m] (8 batch columns), then a
-    // fixed-order sum over the CTA's k-slices and the cluster's ranks.
-    __syncthreads();  // x staging area is reused
-    float* red = reinterpret_cast<float*>(smem_u4);
-#pragma unroll
-    for (int r = 0; r < R16; ++r) {
-        const int lr0 = wr * 16 * R16 + 16 * r + g;
-        if (FMT == FMT_G64) {
-            red[(lr0 * WK + wk) * 8 + q] = acc[r][0];
-            red[((lr0 + 8) * WK + wk) * 8 + q] = acc[r][2];
-            // columns 4..7 are never used for group-64 (batch <= 4)
-        } else {
-            red[(lr0 * WK + wk) * 8 + 2 * q] = acc[r][0];
-            red[(lr0 * WK + wk) * 8 + 2 * q + 1] = acc[r][1];
-            red[((lr0 + 8) * WK + wk) * 8 + 2 * q] = acc[r][2];
-            red[((lr0 + 8) * WK + wk) * 8 + 2 * q + 1] = acc[r][3];
+    if (nb == 0) {
+        // a warp whose k-slice is empty still contributes zeros for every tile
+        for (int t = 0; t < nt; ++t) {
+            float* rp = red + ((size_t)(t * W + warp) * 16) * mb;
+            for (int i = lane; i < 16 * mb; i += 32) rp[i] = 0.f;
         }
     }
     __syncthreads();
-    const int nout = rows_cta * mb;
-    float* fin = red + rows_cta * WK * 8;  // per-CTA sums [row][m]
-    for (int t = threadIdx.x; t < nout; t += W * 32) {
-        const int lr = t / mb, m = t - lr * mb;
+
+    // Sum over warps in warp order: fin[tile][row][m] (reuses the x area,
+    // which is no longer read).
+    float* fin = reinterpret_cast<float*>(smem_u4);
+    const int nout = nt * 16 * mb;
+    for (int i = threadIdx.x; i < nout; i += W * 32) {
+        const int t = i / (16 * mb);
+        const int rm = i - t * 16 * mb;
         float v = 0.f;
-        for (int k = 0; k < WK; ++k) v += red[(lr * WK + k) * 8 + m];
-        fin[t] = v;
+        for (int w = 0; w < W; ++w) v += red[((size_t)(t * W + w) * 16) * mb + rm];
+        fin[i] = v;
     }
-    const int row_base = (blockIdx.x / S) * rows_cta;
+    const int row0 = t0 * 16;
     if (S == 1) {
         __syncthreads();
-        for (int t = threadIdx.x; t < nout; t += W * 32) {
-            const int m = t / rows_cta, lr = t - m * rows_cta;
-            if (row_base + lr < a.N) store_out(a.y, (int64_t)m * a.N + row_base + lr, fin[lr * mb + m], a.out_f32);
+        for (int i = threadIdx.x; i < nout; i += W * 32) {
+            const int m = i / (nt * 16), lr = i - m * nt * 16;
+            if (row0 + lr < a.N) store_out(a.y, (int64_t)m * a.N + row0 + lr, fin[lr * mb + m], a.out_f32);
         }
         return;
     }
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
-    // rank s writes the rows [s * rows_cta / S, (s + 1) * rows_cta / S) of every batch row
-    const int lo = rank * rows_cta / S, hi = (rank + 1) * rows_cta / S;
+    // rank s writes rows [s * R / S, (s + 1) * R / S) of the CTA's R rows, for every batch row
+    const int R = nt * 16;
+    const int lo = rank * R / S, hi = (rank + 1) * R / S;
     const int span = hi - lo;
-    for (int t = threadIdx.x; t < span * mb; t += W * 32) {
-        const int m = t / span, lr = lo + (t - m * span);
+    for (int i = threadIdx.x; i < span * mb; i += W * 32) {
+        const int m = i / span, lr = lo + (i - m * span);
         float v = 0.f;
         for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(fin + lr * mb + m, s);
-        if (row_base + lr < a.N) store_out(a.y, (int64_t)m * a.N + row_base + lr, v, a.out_f32);
+        if (row0 + lr < a.N) store_out(a.y, (int64_t)m * a.N + row0 + lr, v, a.out_f32);
     }
     cluster.sync();
 }
 
 // ------------------------------------------------------------- tables ----
-using MmaFn = void (*)(const GemvArgs, const int, const int);
+using MmaFn = void (*)(const GemvArgs, const int);
 struct MmaEntry {
     MmaConfig cfg;
     MmaFn fn;
 };
-#define MBW_M(F, W, R, U) \
-    { {W, R, U}, gemv_mma_kernel<F, W, R, U> }
+#define MBW_M(F, W, U) \
+    { {W, U}, gemv_mma_kernel<F, W, U> }
 
 static const MmaEntry kMmaBf16[] = {
-    MBW_M(FMT_BF16, 4, 1, 4), MBW_M(FMT_BF16, 4, 2, 4), MBW_M(FMT_BF16, 8, 1, 4), MBW_M(FMT_BF16, 8, 2, 2),
-    MBW_M(FMT_BF16, 8, 1, 8),
+    MBW_M(FMT_BF16, 4, 4), MBW_M(FMT_BF16, 4, 8), MBW_M(FMT_BF16, 8, 4), MBW_M(FMT_BF16, 8, 8),
 };
 static const MmaEntry kMmaG64[] = {
-    MBW_M(FMT_G64, 4, 1, 2), MBW_M(FMT_G64, 4, 2, 2), MBW_M(FMT_G64, 8, 1, 2), MBW_M(FMT_G64, 8, 2, 1),
-    MBW_M(FMT_G64, 8, 1, 4), MBW_M(FMT_G64, 4, 1, 4),
+    MBW_M(FMT_G64, 4, 2), MBW_M(FMT_G64, 4, 4), MBW_M(FMT_G64, 8, 2), MBW_M(FMT_G64, 8, 4),
 };
 static const MmaEntry kMmaAwq[] = {
-    MBW_M(FMT_AWQ, 4, 1, 2), MBW_M(FMT_AWQ, 4, 2, 2), MBW_M(FMT_AWQ, 8, 1, 2), MBW_M(FMT_AWQ, 8, 2, 1),
-    MBW_M(FMT_AWQ, 8, 1, 4), MBW_M(FMT_AWQ, 4, 1, 4),
+    MBW_M(FMT_AWQ, 4, 2), MBW_M(FMT_AWQ, 4, 4), MBW_M(FMT_AWQ, 8, 2), MBW_M(FMT_AWQ, 8, 4),
 };
 #undef MBW_M
 
@@ -372,32 +381,36 @@ MmaConfig mma_config(int fmt, int idx) {
 
 int mma_max_batch(int fmt) { return fmt == FMT_G64 ? 4 : 8; }
 
-size_t mma_smem_bytes(int fmt, const MmaConfig& c, int64_t K, int M, int split, int wk) {
+// CTA row-groups of a launch: `occ` CTAs per SM in total, at most one per
+// 16-row tile, a multiple of the cluster size.
+int mma_row_groups(int64_t N, int split, int occ) {
+    const int sms = device_sm_count();
+    const int64_t T = (N + 15) / 16;
+    int64_t G = ((int64_t)sms * occ) / split;
+    if (G > T) G = T;
+    if (G < 1) G = 1;
+    return (int)G;
+}
+
+size_t mma_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
     const int BK = (fmt == FMT_BF16) ? 32 : 128;
-    const int64_t KB = (K + BK - 1) / BK;
-    const int64_t TS = (int64_t)split * wk;
-    const int64_t BS = (KB + TS - 1) / TS;
-    const size_t xs = (size_t)M * (size_t)(wk * BS) * (BK / 8) * 16;
-    const int rows_cta = (c.warps / wk) * 16 * c.r16;
-    const size_t red = (size_t)rows_cta * wk * 8 * 4 + (size_t)rows_cta * 8 * 4;
-    return xs > red ? xs : red;
+    const int G = mma_row_groups(N, split, occ);
+    return mma_smem_layout(BK, K, (int)N, M, c.warps, split, G).total;
 }
 
 cudaError_t launch_gemv_mma(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
     int n;
     const MmaEntry* t = mma_table(fmt, &n);
-    if (p.cfg < 0 || p.cfg >= n) return cudaErrorInvalidValue;
+    if (p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > mma_max_batch(fmt)) return cudaErrorInvalidValue;
     const MmaEntry& e = t[p.cfg];
-    if (e.cfg.warps % p.wk != 0) return cudaErrorInvalidValue;
-    const int rows_cta = (e.cfg.warps / p.wk) * 16 * e.cfg.r16;
-    const int groups = (a.N + rows_cta - 1) / rows_cta;
-    const size_t smem = mma_smem_bytes(fmt, e.cfg, a.K, a.M, p.split, p.wk);
+    const int G = mma_row_groups(a.N, p.split, p.occ);
+    const size_t smem = mma_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(groups * p.split), 1, 1);
+    cfg.gridDim = dim3((unsigned)(G * p.split), 1, 1);
     cfg.blockDim = dim3((unsigned)(e.cfg.warps * 32), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -416,7 +429,7 @@ cudaError_t launch_gemv_mma(int fmt, const Plan& p, const GemvArgs& a, cudaStrea
     cfg.attrs = attrs;
     cfg.numAttrs = na;
     count_launch();
-    return cudaLaunchKernelEx(&cfg, e.fn, a, p.split, p.wk);
+    return cudaLaunchKernelEx(&cfg, e.fn, a, p.split);
 }
 
 }  // namespace mbw

@@ -38,9 +38,8 @@ struct SimtConfig {
 
 // One instantiation of the tensor-core (mma.sync) streaming kernel.
 struct MmaConfig {
-    int warps;  // warps per CTA
-    int r16;    // 16-row tiles per warp
-    int u;      // 64-byte row blocks per lane in flight
+    int warps;  // warps per CTA; each owns one k-slice of every tile of the CTA
+    int u;      // 64-byte row blocks per lane in flight (register ring depth)
 };
 
 // Execution plan of one call shape.
@@ -48,7 +47,7 @@ struct Plan {
     int kind;   // PLAN_SIMT or PLAN_MMA
     int cfg;    // index into the kernel table of `kind`
     int split;  // CTAs per cluster along K (1 = no split)
-    int wk;     // k-slices per CTA (MMA kernels; 1 for SIMT)
+    int occ;    // MMA kernels: CTAs per SM in the persistent grid (1 for SIMT)
 };
 enum PlanKind : int { PLAN_SIMT = 0, PLAN_MMA = 1 };
 
@@ -62,7 +61,8 @@ size_t simt_smem_bytes(int fmt, const SimtConfig& c, const GemvArgs& a, int spli
 int mma_num_configs(int fmt);
 MmaConfig mma_config(int fmt, int idx);
 int mma_max_batch(int fmt);
-size_t mma_smem_bytes(int fmt, const MmaConfig& c, int64_t K, int M, int split, int wk);
+size_t mma_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ);
+int mma_row_groups(int64_t N, int split, int occ);
 cudaError_t launch_gemv_mma(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
 
 cudaError_t launch_dequant(int fmt, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zeros,

@@ -64,7 +64,7 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K) 
     (void)N;
     if (p.split < 1 || p.split > 8) return false;
     if (p.kind == PLAN_SIMT) {
-        if (p.cfg < 0 || p.cfg >= simt_num_configs(fmt) || p.wk != 1) return false;
+        if (p.cfg < 0 || p.cfg >= simt_num_configs(fmt) || p.occ != 1) return false;
         const SimtConfig c = simt_config(fmt, p.cfg);
         if (c.mb != simt_want_mb(M)) return false;
         if (simt_smem(fmt, c, K, p.split) > kSmemLimit) return false;
@@ -75,10 +75,11 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K) 
     if (p.kind == PLAN_MMA) {
         if (p.cfg < 0 || p.cfg >= mma_num_configs(fmt)) return false;
         const MmaConfig c = mma_config(fmt, p.cfg);
-        if (p.wk < 1 || c.warps % p.wk != 0) return false;
+        if (p.occ < 1 || p.occ > 2) return false;
         const int mb = (int)std::min<int64_t>(M, mma_max_batch(fmt));
-        if ((int64_t)p.split * p.wk > kblocks(fmt, K)) return false;
-        if (mma_smem_bytes(fmt, c, K, mb, p.split, p.wk) > kSmemLimit) return false;
+        // every warp of the cluster gets at least one k-block
+        if ((int64_t)p.split * c.warps > kblocks(fmt, K)) return false;
+        if (mma_smem_bytes(fmt, c, N, K, mb, p.split, p.occ) > kSmemLimit) return false;
         return true;
     }
     return false;
@@ -91,8 +92,8 @@ static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
     const int splits[4] = {1, 2, 4, 8};
     for (int cfg = 0; cfg < mma_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si)
-            for (int wk = 1; wk <= 8; wk *= 2) {
-                Plan p{PLAN_MMA, cfg, splits[si], wk};
+            for (int occ = 1; occ <= 2; ++occ) {
+                Plan p{PLAN_MMA, cfg, splits[si], occ};
                 if (plan_valid(fmt, p, Mb, N, K)) out.push_back(p);
             }
     for (int cfg = 0; cfg < simt_num_configs(fmt); ++cfg)
@@ -107,23 +108,21 @@ Plan plan_default(int op, int64_t M, int64_t N, int64_t K) {
     const int fmt = fmt_of_op(op);
     const int64_t Mb = std::min<int64_t>(M, 8);
     const int sms = device_sm_count();
-    // Tensor-core family: 8 warps, one 16-row tile per warp; split K over the
-    // CTA's warps and then over a cluster until there are ~16 warp tasks per SM.
+    // Tensor-core family: 8 warps, 4 blocks in flight, one CTA per SM; split K
+    // over a cluster while there are fewer 16-row tiles than SMs.
     int cfg = 0;
     for (int i = 0; i < mma_num_configs(fmt); ++i) {
         const MmaConfig c = mma_config(fmt, i);
-        if (c.warps == 8 && c.r16 == 1) {
+        if (c.warps == 8 && c.u == 4) {
             cfg = i;
             break;
         }
     }
     const int64_t tiles = (N + 15) / 16;
     const int64_t KB = kblocks(fmt, K);
-    const int64_t want = (int64_t)sms * 16;
-    int wk = 1, split = 1;
-    while (wk < 8 && tiles * wk * split < want && (int64_t)(wk * 2) * split <= KB) wk *= 2;
-    while (split < 8 && tiles * wk * split < want && (int64_t)wk * split * 2 <= KB) split *= 2;
-    Plan p{PLAN_MMA, cfg, split, wk};
+    int split = 1;
+    while (split < 8 && tiles * split < sms && (int64_t)8 * split * 2 <= KB) split *= 2;
+    Plan p{PLAN_MMA, cfg, split, 1};
     while (!plan_valid(fmt, p, Mb, N, K) && p.split < 8) p.split *= 2;
     if (plan_valid(fmt, p, Mb, N, K)) return p;
     const std::vector<Plan> c = candidates(op, M, N, K);
@@ -161,9 +160,8 @@ std::string plan_to_string(int op, const Plan& p) {
     char buf[192];
     if (p.kind == PLAN_MMA) {
         const MmaConfig c = mma_config(fmt, p.cfg);
-        snprintf(buf, sizeof(buf),
-                 "mma fmt=%s warps=%d row_tiles_per_warp=%d blocks_in_flight=%d kslices_per_cta=%d split_k=%d", fs,
-                 c.warps, c.r16, c.u, p.wk, p.split);
+        snprintf(buf, sizeof(buf), "mma fmt=%s warps=%d blocks_in_flight=%d ctas_per_sm=%d split_k=%d", fs, c.warps,
+                 c.u, p.occ, p.split);
     } else {
         const SimtConfig c = simt_config(fmt, p.cfg);
         snprintf(buf, sizeof(buf), "simt fmt=%s warps=%d rows_per_warp=%d chunks_in_flight=%d batch=%d split_k=%d",
@@ -218,7 +216,7 @@ extern "C" int mbw_plan_index(int op, int64_t M, int64_t N, int64_t K) {
     const Plan cur = plan_lookup(op, M, N, K, nullptr);
     const std::vector<Plan> c = candidates(op, M, N, K);
     for (size_t i = 0; i < c.size(); ++i)
-        if (c[i].kind == cur.kind && c[i].cfg == cur.cfg && c[i].split == cur.split && c[i].wk == cur.wk)
+        if (c[i].kind == cur.kind && c[i].cfg == cur.cfg && c[i].split == cur.split && c[i].occ == cur.occ)
             return (int)i;
     return -1;
 }
