@@ -1,0 +1,472 @@
+// gemv_tma.cu -- weight-streaming GEMV for sm_103a fed by the bulk-copy
+// (TMA) engine.
+//
+// Same arithmetic as gemv_mma.cu (bf16 nibble pairs, exact subtract,
+// mma.sync.m16n8k16 with fp32 accumulation, batch in the n columns), but the
+// weights reach the SM through a shared-memory ring filled by one producer
+// thread with cp.async.bulk: the consumer warps spend no issue slots on
+// address arithmetic, predicates or load bookkeeping, and the ring depth, not
+// the register file, sets how many bytes are in flight.
+//
+//   * CTA = 1 producer warp + W consumer warps. CTA row-group c of G owns the
+//     contiguous 16-row tile range [c*T/G, (c+1)*T/G); a cluster of S CTAs
+//     splits the k-range.
+//   * A ring stage holds one tile (16 rows) x W 64-byte blocks of each row
+//     (consumer warp w takes block w). Rows sit at a stride of 64*W + 64 bytes
+//     so that the two rows each 8-lane phase of a 16-byte-per-lane load
+//     touches fall in disjoint banks. The producer issues one bulk copy per row per stage
+//     (16-byte aligned, 16-byte multiple) and arms the stage's full barrier
+//     with the byte count; consumers arrive on the stage's empty barrier.
+//   * Programmatic dependent launch: the producer never waits for the
+//     previous grid (it only reads weights), so the ring fills while the
+//     previous kernel finishes; consumers wait before staging x.
+//   * Group scales (and AWQ zero points) are small: each consumer lane loads
+//     its own, one stage ahead.
+//   * Every mbarrier wait is bounded. On expiry the kernel records the fault in
+//     a device flag (read by mbw_check_device_error), the producer waits
+//     (bounded) for the copies it issued, and all threads leave normally.
+//
+// Per-tile partial sums go to shared memory and are summed over warps (and
+// over cluster ranks through distributed shared memory) once, in a fixed
+// order: deterministic, no global scratch.
+#include <cooperative_groups.h>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace mbw {
+
+__device__ int g_tma_fault;  // set by a bounded wait that expired
+
+static constexpr long long kSpinLimit = 1ll << 22;  // try_wait rounds before giving up
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait; returns false (and records the fault) if the phase never completed.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    for (long long i = 0; i < kSpinLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    atomicExch(&g_tma_fault, 1);
+    return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t nibs(uint32_t v) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(0x000F000Fu), "r"(0x43004300u));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bsub(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint4 pair_perm(uint4 v) {
+    uint4 o;
+    o.x = __byte_perm(v.x, v.z, 0x5410);
+    o.y = __byte_perm(v.x, v.z, 0x7632);
+    o.z = __byte_perm(v.y, v.w, 0x5410);
+    o.w = __byte_perm(v.y, v.w, 0x7632);
+    return o;
+}
+
+// Shared-memory layout (bytes), identical on host and device.
+struct TmaSmem {
+    int BK, xwords, ntmax, rowstride;
+    size_t ring_off, stage_bytes, x_off, red_off, bar_off, total;
+};
+
+__host__ __device__ inline TmaSmem tma_smem_layout(int fmt, int64_t K, int N, int M, int W, int D, int S, int G) {
+    TmaSmem L;
+    L.BK = (fmt == FMT_BF16) ? 32 : 128;
+    const int64_t KB = (K + L.BK - 1) / L.BK;
+    const int64_t BS = (KB + S - 1) / S;  // blocks per cluster rank
+    L.xwords = (int)(BS * (L.BK / 8));
+    const int T = (N + 15) / 16;
+    L.ntmax = (T + G - 1) / G;
+    L.rowstride = 64 * W + 64;  // rows g and g+1 land 16 banks apart
+    L.ring_off = 0;
+    L.stage_bytes = (size_t)16 * L.rowstride;
+    L.x_off = L.ring_off + (size_t)D * L.stage_bytes;
+    const size_t x_bytes = (size_t)M * L.xwords * 16;
+    const size_t fin_bytes = (size_t)L.ntmax * 16 * M * 4;
+    L.red_off = L.x_off + ((x_bytes > fin_bytes ? x_bytes : fin_bytes) + 15) / 16 * 16;
+    const size_t red_bytes = (size_t)L.ntmax * W * 16 * M * 4;
+    L.bar_off = (L.red_off + red_bytes + 15) / 16 * 16;
+    L.total = L.bar_off + (size_t)2 * D * 8;
+    return L;
+}
+
+template <int FMT, int W, int D>
+__global__ void __launch_bounds__((W + 1) * 32)
+    gemv_tma_kernel(const GemvArgs a, const int S) {
+    constexpr int BK = (FMT == FMT_BF16) ? 32 : 128;
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    pdl_launch_dependents();
+
+    const int rank = (S > 1) ? (int)cg::this_cluster().block_rank() : 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x / S;
+    const int cgid = blockIdx.x / S;
+    const int T = (a.N + 15) / 16;
+    const int t0 = (int)(((long long)T * cgid) / G);
+    const int nt = (int)(((long long)T * (cgid + 1)) / G) - t0;
+    const int mb = a.M;
+    const TmaSmem L = tma_smem_layout(FMT, a.K, a.N, mb, W, D, S, G);
+
+    const int KB = (a.K + BK - 1) / BK;
+    const int BS = (KB + S - 1) / S;
+    const int cb0 = rank * BS;                       // first block of this CTA's k-range
+    const int ncb = max(0, min(KB, cb0 + BS) - cb0);  // blocks in the k-range
+    const int nchunk = (ncb + W - 1) / W;            // stages per tile
+    const int nstage = nt * nchunk;
+    const size_t rowbytes = (FMT == FMT_BF16) ? (size_t)a.K * 2 : (size_t)a.K / 2;
+
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+    uint64_t* empty = full + D;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < D; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], W);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == W) {
+        // ------------------------------------------------------ producer ----
+        if (lane == 0) {
+            uint64_t policy;
+            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+            bool ok = true;
+            int issued = 0;
+            for (int i = 0; i < nstage && ok; ++i) {
+                const int s = i % D;
+                if (i >= D) ok = mbar_wait(&empty[s], ((i / D) - 1) & 1);
+                if (!ok) break;
+                const int tl = i / nchunk, c = i - tl * nchunk;
+                const int row0 = (t0 + tl) * 16;
+                const int nrows = min(16, a.N - row0);
+                const size_t off = (size_t)(cb0 + c * W) * 64;  // byte offset in a row
+                const uint32_t want = (uint32_t)min((size_t)min(W, ncb - c * W) * 64, rowbytes - off);
+                mbar_expect_tx(&full[s], want * (uint32_t)nrows);
+                uint8_t* st = smem + L.ring_off + (size_t)s * L.stage_bytes;
+                for (int r = 0; r < nrows; ++r)
+                    bulk_g2s(st + (size_t)r * L.rowstride, a.W + (size_t)(row0 + r) * rowbytes + off, want,
+                             &full[s], policy);
+                ++issued;
+            }
+            if (!ok) {
+                // drain: wait (bounded) for the copies already issued
+                for (int i = max(0, issued - D); i < issued; ++i) mbar_wait(&full[i % D], (i / D) & 1);
+            }
+        }
+    } else {
+        // ----------------------------------------------------- consumers ----
+        const int g = lane >> 2, q = lane & 3;
+        pdl_wait();
+        // stage x for the CTA's k-range (consumer warps only; named barrier 1)
+        const int cwords = ncb * (BK / 8);
+        uint4* xs = reinterpret_cast<uint4*>(smem + L.x_off);
+        for (int i = threadIdx.x; i < mb * L.xwords; i += W * 32) {
+            const int m = i / L.xwords;
+            const int wi = i - m * L.xwords;
+            const int k = cb0 * BK + wi * 8;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (wi < cwords && k < a.K) v = ld_ro16(a.x + (size_t)m * a.K + k);
+            xs[i] = (FMT == FMT_BF16) ? v : pair_perm(v);
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
+
+        int xm;
+        bool xon;
+        if (FMT == FMT_G64) {
+            xm = g >> 1;
+            xon = (xm < mb) && ((g & 1) == (q >> 1));
+        } else {
+            xm = g;
+            xon = xm < mb;
+        }
+        // lanes that carry no x read a zero word instead (no selects in the loop)
+        const uint4* xw = xs + (size_t)(xon ? xm : 0) * L.xwords;
+        float* red = reinterpret_cast<float*>(smem + L.red_off);
+        const int rs = L.rowstride;
+
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t sc[2] = {0, 0};  // scale words of rows g, g+8 for the current stage
+        auto load_scales = [&](int i, uint32_t (&o)[2]) {
+            const int tl = i / nchunk, c = i - tl * nchunk;
+            const int b = cb0 + c * W + warp;
+            if (b >= cb0 + ncb || FMT == FMT_BF16) return;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = min((t0 + tl) * 16 + g + 8 * h, a.N - 1);
+                if (FMT == FMT_G64) {
+                    const uint16_t* sp = a.scales + (size_t)row * a.groups + 2 * b;
+                    const uint32_t s1 = (2 * b + 1 < a.groups) ? ld_ro_u16(sp + 1) : 0u;
+                    o[h] = (uint32_t)ld_ro_u16(sp) | (s1 << 16);
+                } else {
+                    const uint32_t s = ld_ro_u16(a.scales + (size_t)row * a.groups + b);
+                    const uint32_t zb = ld_ro_u8(a.zeros + (size_t)row * a.zstride + (b >> 1));
+                    o[h] = s | (((b & 1) ? (zb >> 4) : (zb & 0xF)) << 16);
+                }
+            }
+        };
+        if (nstage > 0) load_scales(0, sc);
+
+        bool ok = true;
+        for (int i = 0; i < nstage; ++i) {
+            const int s = i % D;
+            const int tl = i / nchunk, c = i - tl * nchunk;
+            uint32_t scn[2] = {0, 0};
+            if (i + 1 < nstage) load_scales(i + 1, scn);
+            if (ok) ok = mbar_wait(&full[s], (i / D) & 1);
+            const int b = cb0 + c * W + warp;  // this warp's block in the stage
+            if (ok && b < cb0 + ncb) {
+                const uint8_t* st = smem + L.ring_off + (size_t)s * L.stage_bytes + warp * 64 + q * 16;
+                uint4 wg = *reinterpret_cast<const uint4*>(st + g * rs);
+                uint4 wg8 = *reinterpret_cast<const uint4*>(st + (g + 8) * rs);
+                const int lb = b - cb0;
+                if ((size_t)b * 64 + (q + 1) * 16 > rowbytes) {
+                    // tail of a partial block: no weights there (and no x)
+                    wg = make_uint4(0, 0, 0, 0);
+                    wg8 = make_uint4(0, 0, 0, 0);
+                }
+                if (FMT == FMT_BF16) {
+                    const uint4 xv = xw[lb * 4 + q];
+                    const uint4 x0 = xon ? xv : make_uint4(0, 0, 0, 0);
+                    mma_16816(acc, wg.x, wg8.x, wg.y, wg8.y, x0.x, x0.y);
+                    mma_16816(acc, wg.z, wg8.z, wg.w, wg8.w, x0.z, x0.w);
+                } else {
+                    const uint32_t zz0 = (0x4300u | ((FMT == FMT_G64) ? 8u : (sc[0] >> 16))) * 0x00010001u;
+                    const uint32_t zz1 = (0x4300u | ((FMT == FMT_G64) ? 8u : (sc[1] >> 16))) * 0x00010001u;
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                    const uint32_t wa[4] = {wg.x, wg.y, wg.z, wg.w};
+                    const uint32_t wb[4] = {wg8.x, wg8.y, wg8.z, wg8.w};
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        uint4 xv = xw[lb * 16 + 4 * q + jj];
+                        if (!xon) xv = make_uint4(0, 0, 0, 0);
+                        mma_16816(d, bsub(nibs(wa[jj]), zz0), bsub(nibs(wb[jj]), zz1), bsub(nibs(wa[jj] >> 4), zz0),
+                                  bsub(nibs(wb[jj] >> 4), zz1), xv.x, xv.y);
+                        mma_16816(d, bsub(nibs(wa[jj] >> 8), zz0), bsub(nibs(wb[jj] >> 8), zz1),
+                                  bsub(nibs(wa[jj] >> 12), zz0), bsub(nibs(wb[jj] >> 12), zz1), xv.z, xv.w);
+                    }
+                    if (FMT == FMT_G64) {
+                        acc[0] = fmaf(f16_bits_to_f32(sc[0] & 0xFFFF), d[0], acc[0]);
+                        acc[0] = fmaf(f16_bits_to_f32(sc[0] >> 16), d[1], acc[0]);
+                        acc[2] = fmaf(f16_bits_to_f32(sc[1] & 0xFFFF), d[2], acc[2]);
+                        acc[2] = fmaf(f16_bits_to_f32(sc[1] >> 16), d[3], acc[2]);
+                    } else {
+                        const float s0 = f16_bits_to_f32(sc[0] & 0xFFFF), s1 = f16_bits_to_f32(sc[1] & 0xFFFF);
+                        acc[0] = fmaf(s0, d[0], acc[0]);
+                        acc[1] = fmaf(s0, d[1], acc[1]);
+                        acc[2] = fmaf(s1, d[2], acc[2]);
+                        acc[3] = fmaf(s1, d[3], acc[3]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            sc[0] = scn[0];
+            sc[1] = scn[1];
+            if (c == nchunk - 1) {
+                float* rp = red + ((size_t)(tl * W + warp) * 16) * mb;
+                if (FMT == FMT_G64) {
+                    if (q < mb) {
+                        rp[g * mb + q] = acc[0];
+                        rp[(g + 8) * mb + q] = acc[2];
+                    }
+                } else {
+                    if (2 * q < mb) {
+                        rp[g * mb + 2 * q] = acc[0];
+                        rp[(g + 8) * mb + 2 * q] = acc[2];
+                    }
+                    if (2 * q + 1 < mb) {
+                        rp[g * mb + 2 * q + 1] = acc[1];
+                        rp[(g + 8) * mb + 2 * q + 1] = acc[3];
+                    }
+                }
+                acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+            }
+        }
+        if (nchunk == 0) {
+            for (int t = 0; t < nt; ++t) {
+                float* rp = red + ((size_t)(t * W + warp) * 16) * mb;
+                for (int i = lane; i < 16 * mb; i += 32) rp[i] = 0.f;
+            }
+        }
+    }
+    __syncthreads();
+
+    // Sum over the consumer warps in warp order: fin[tile][row][m] (in the x area).
+    float* red = reinterpret_cast<float*>(smem + L.red_off);
+    float* fin = reinterpret_cast<float*>(smem + L.x_off);
+    const int nthr = (W + 1) * 32;
+    const int nout = nt * 16 * mb;
+    for (int i = threadIdx.x; i < nout; i += nthr) {
+        const int t = i / (16 * mb);
+        const int rm = i - t * 16 * mb;
+        float v = 0.f;
+        for (int w = 0; w < W; ++w) v += red[((size_t)(t * W + w) * 16) * mb + rm];
+        fin[i] = v;
+    }
+    const int row0 = t0 * 16;
+    if (S == 1) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < nout; i += nthr) {
+            const int m = i / (nt * 16), lr = i - m * nt * 16;
+            if (row0 + lr < a.N) store_out(a.y, (int64_t)m * a.N + row0 + lr, fin[lr * mb + m], a.out_f32);
+        }
+        return;
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int R = nt * 16;
+    const int lo = rank * R / S, hi = (rank + 1) * R / S;
+    const int span = hi - lo;
+    for (int i = threadIdx.x; i < span * mb; i += nthr) {
+        const int m = i / span, lr = lo + (i - m * span);
+        float v = 0.f;
+        for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(fin + lr * mb + m, s);
+        if (row0 + lr < a.N) store_out(a.y, (int64_t)m * a.N + row0 + lr, v, a.out_f32);
+    }
+    cluster.sync();
+}
+
+// ------------------------------------------------------------- tables ----
+using TmaFn = void (*)(const GemvArgs, const int);
+struct TmaEntry {
+    TmaConfig cfg;
+    TmaFn fn;
+};
+#define MBW_T(F, W, D) \
+    { {W, D}, gemv_tma_kernel<F, W, D> }
+
+static const TmaEntry kTmaBf16[] = {MBW_T(FMT_BF16, 4, 8), MBW_T(FMT_BF16, 8, 4), MBW_T(FMT_BF16, 8, 8)};
+static const TmaEntry kTmaG64[] = {MBW_T(FMT_G64, 4, 8), MBW_T(FMT_G64, 8, 4), MBW_T(FMT_G64, 8, 8)};
+static const TmaEntry kTmaAwq[] = {MBW_T(FMT_AWQ, 4, 8), MBW_T(FMT_AWQ, 8, 4), MBW_T(FMT_AWQ, 8, 8)};
+#undef MBW_T
+
+static const TmaEntry* tma_table(int fmt, int* n) {
+    switch (fmt) {
+        case FMT_BF16:
+            *n = (int)(sizeof(kTmaBf16) / sizeof(kTmaBf16[0]));
+            return kTmaBf16;
+        case FMT_G64:
+            *n = (int)(sizeof(kTmaG64) / sizeof(kTmaG64[0]));
+            return kTmaG64;
+        default:
+            *n = (int)(sizeof(kTmaAwq) / sizeof(kTmaAwq[0]));
+            return kTmaAwq;
+    }
+}
+
+int tma_num_configs(int fmt) {
+    int n;
+    tma_table(fmt, &n);
+    return n;
+}
+
+TmaConfig tma_config(int fmt, int idx) {
+    int n;
+    return tma_table(fmt, &n)[idx].cfg;
+}
+
+size_t tma_smem_bytes(int fmt, const TmaConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
+    const int G = mma_row_groups(N, split, occ);
+    return tma_smem_layout(fmt, K, (int)N, M, c.warps, c.depth, split, G).total;
+}
+
+cudaError_t launch_gemv_tma(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
+    int n;
+    const TmaEntry* t = tma_table(fmt, &n);
+    if (p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > mma_max_batch(fmt)) return cudaErrorInvalidValue;
+    const TmaEntry& e = t[p.cfg];
+    const int G = mma_row_groups(a.N, p.split, p.occ);
+    const size_t smem = tma_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
+    if (smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(G * p.split), 1, 1);
+    cfg.blockDim = dim3((unsigned)((e.cfg.warps + 1) * 32), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (p.split > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)p.split;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    count_launch();
+    return cudaLaunchKernelEx(&cfg, e.fn, a, p.split);
+}
+
+// Read and clear the fault flag of the bounded waits (host side).
+int tma_take_fault() {
+    int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_tma_fault, sizeof(int)) != cudaSuccess) return -1;
+    if (v) cudaMemcpyToSymbol(g_tma_fault, &z, sizeof(int));
+    return v;
+}
+
+}  // namespace mbw

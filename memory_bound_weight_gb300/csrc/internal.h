@@ -42,6 +42,12 @@ struct MmaConfig {
     int u;      // 64-byte row blocks per lane in flight (register ring depth)
 };
 
+// One instantiation of the bulk-copy-fed tensor-core streaming kernel.
+struct TmaConfig {
+    int warps;  // consumer warps per CTA (plus one producer warp)
+    int depth;  // shared-memory ring stages
+};
+
 // Execution plan of one call shape.
 struct Plan {
     int kind;   // PLAN_SIMT or PLAN_MMA
@@ -49,7 +55,7 @@ struct Plan {
     int split;  // CTAs per cluster along K (1 = no split)
     int occ;    // MMA kernels: CTAs per SM in the persistent grid (1 for SIMT)
 };
-enum PlanKind : int { PLAN_SIMT = 0, PLAN_MMA = 1 };
+enum PlanKind : int { PLAN_SIMT = 0, PLAN_MMA = 1, PLAN_TMA = 2 };
 
 // Kernel tables (gemv_simt.cu).
 int simt_num_configs(int fmt);
@@ -64,6 +70,13 @@ int mma_max_batch(int fmt);
 size_t mma_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ);
 int mma_row_groups(int64_t N, int split, int occ);
 cudaError_t launch_gemv_mma(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
+
+// Bulk-copy-fed kernel tables (gemv_tma.cu).
+int tma_num_configs(int fmt);
+TmaConfig tma_config(int fmt, int idx);
+size_t tma_smem_bytes(int fmt, const TmaConfig& c, int64_t N, int64_t K, int M, int split, int occ);
+cudaError_t launch_gemv_tma(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
+int tma_take_fault();  // 1 if a bounded device wait expired since the last call (and clear it)
 
 cudaError_t launch_dequant(int fmt, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zeros,
                            float* out, int64_t N, int64_t K, cudaStream_t s);
