@@ -26,7 +26,9 @@
 //     64-byte row block, so a quad reads 64 contiguous bytes of a row;
 //   * a warp walks its (tile, block) sequence through a U-deep register ring:
 //     consume slot u, refill it with the block U steps ahead, so loads keep
-//     flowing across tile boundaries; per-tile partial sums go to shared
+//     flowing across tile boundaries; load pointers advance by one block and
+//     are rebuilt only at tile changes, and K is a whole number of blocks, so
+//     the loop carries no per-block predicates; per-tile partial sums go to shared
 //     memory and are summed over warps (and cluster ranks, through
 //     distributed shared memory) once, in a fixed order: deterministic, no
 //     global scratch, no spin waits;
@@ -111,7 +113,7 @@ __host__ __device__ inline MmaSmem mma_smem_layout(int BK, int64_t K, int N, int
     L.xwords = (int)(W * BS * (BK / 8));
     const int T = (N + 15) / 16;
     L.ntmax = (T + G - 1) / G;
-    L.x_bytes = (size_t)M * L.xwords * 16;
+    L.x_bytes = ((size_t)M * L.xwords + BK / 8) * 16;  // + one block of zero words
     const size_t fin_bytes = (size_t)L.ntmax * 16 * M * 4;
     L.red_off = ((L.x_bytes > fin_bytes ? L.x_bytes : fin_bytes) + 15) / 16 * 16;
     L.red_bytes = (size_t)L.ntmax * W * 16 * M * 4;
@@ -123,6 +125,8 @@ template <int FMT, int W, int U>
 __global__ void __launch_bounds__(W * 32)
     gemv_mma_kernel(const GemvArgs a, const int S) {
     constexpr int BK = MmaTraits<FMT>::BK;
+    constexpr int XW = BK / 8;                      // 16-byte x words per row block
+    constexpr int SPB = (FMT == FMT_G64) ? 2 : 1;   // scale entries per row block
     extern __shared__ uint4 smem_u4[];
 
     pdl_launch_dependents();
@@ -138,48 +142,61 @@ __global__ void __launch_bounds__(W * 32)
     const int mb = a.M;
     const MmaSmem L = mma_smem_layout(BK, a.K, a.N, mb, W, S, G);
 
-    const int KB = (a.K + BK - 1) / BK;
+    const int KB = a.K / BK;  // the plan guarantees K % BK == 0
     const int BS = (KB + S * W - 1) / (S * W);
-    const int cb0 = rank * W * BS;                  // first block of this CTA's k-range
-    const int b0 = cb0 + warp * BS;                 // this warp's k-slice
+    const int cb0 = rank * W * BS;  // first block of this CTA's k-range
+    const int b0 = cb0 + warp * BS;  // this warp's k-slice
     const int nb = max(0, min(KB, b0 + BS) - b0);
-    const int total = nt * nb;                      // (tile, block) steps of this warp
+    const int total = nt * nb;  // (tile, block) steps of this warp
     const size_t rowbytes = (FMT == FMT_BF16) ? (size_t)a.K * 2 : (size_t)a.K / 2;
-    const bool scale32 = (FMT == FMT_G64) && ((a.groups & 1) == 0) && ((((uintptr_t)a.scales) & 3) == 0);
 
-    // ring of U slots: codes of rows g and g+8, and their scale words
-    uint4 ring[U][2];
-    uint32_t sring[U][2];
-
-    // load the next step (tile t0 + ltile, block b0 + lblk) into slot u;
-    // steps are loaded strictly in order
-    int ltile = 0, lblk = 0;
-    auto load = [&](int u) {
-        const int b = b0 + lblk;
-        const int rbase = (t0 + ltile) * 16 + g;
-        if (++lblk == nb) {
-            lblk = 0;
-            ++ltile;
+    // Load cursor: pointers into rows g and g+8 of the tile being loaded.
+    // They advance by one block per load and are rebuilt only at tile changes.
+    int lt = 0, lb = 0;
+    const uint8_t* wp0 = nullptr;
+    const uint8_t* wp1 = nullptr;
+    const uint16_t* sp0 = nullptr;
+    const uint16_t* sp1 = nullptr;
+    const uint8_t* zp0 = nullptr;
+    const uint8_t* zp1 = nullptr;
+    auto set_rows = [&](int t) {
+        const int r0 = min((t0 + t) * 16 + g, a.N - 1);
+        const int r1 = min((t0 + t) * 16 + g + 8, a.N - 1);
+        wp0 = a.W + (size_t)r0 * rowbytes + (size_t)b0 * 64 + q * 16;
+        wp1 = a.W + (size_t)r1 * rowbytes + (size_t)b0 * 64 + q * 16;
+        if (FMT != FMT_BF16) {
+            sp0 = a.scales + (size_t)r0 * a.groups + (size_t)b0 * SPB;
+            sp1 = a.scales + (size_t)r1 * a.groups + (size_t)b0 * SPB;
         }
-        const bool kin = (b * BK + (q + 1) * (BK / 4)) <= a.K;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int row = min(rbase + 8 * h, a.N - 1);
-            ring[u][h] = kin ? ld_stream16(a.W + (size_t)row * rowbytes + (size_t)b * 64 + q * 16)
-                             : make_uint4(0, 0, 0, 0);
-            if (FMT == FMT_G64) {
-                const uint16_t* sp = a.scales + (size_t)row * a.groups + 2 * b;
-                if (scale32) {
-                    sring[u][h] = __ldg(reinterpret_cast<const unsigned int*>(sp));
-                } else {
-                    const uint32_t s1 = (2 * b + 1 < a.groups) ? ld_ro_u16(sp + 1) : 0u;
-                    sring[u][h] = (uint32_t)ld_ro_u16(sp) | (s1 << 16);
-                }
-            } else if (FMT == FMT_AWQ) {
-                const uint32_t s = ld_ro_u16(a.scales + (size_t)row * a.groups + b);
-                const uint32_t zb = ld_ro_u8(a.zeros + (size_t)row * a.zstride + (b >> 1));
-                sring[u][h] = s | (((b & 1) ? (zb >> 4) : (zb & 0xF)) << 16);
-            }
+        if (FMT == FMT_AWQ) {
+            zp0 = a.zeros + (size_t)r0 * a.zstride;
+            zp1 = a.zeros + (size_t)r1 * a.zstride;
+        }
+    };
+    if (nt > 0) set_rows(0);
+
+    uint4 rw[U][2];      // codes / weights of rows g and g+8
+    uint32_t rsc[U][2];  // g64: two fp16 scales; AWQ: fp16 scale | zero << 16
+
+    auto load = [&](int u) {
+        rw[u][0] = ld_stream16(wp0);
+        rw[u][1] = ld_stream16(wp1);
+        if (FMT == FMT_G64) {
+            rsc[u][0] = (uint32_t)ld_ro_u16(sp0) | ((uint32_t)ld_ro_u16(sp0 + 1) << 16);
+            rsc[u][1] = (uint32_t)ld_ro_u16(sp1) | ((uint32_t)ld_ro_u16(sp1 + 1) << 16);
+        } else if (FMT == FMT_AWQ) {
+            const int b = b0 + lb;
+            const uint32_t sh = (b & 1) * 4;
+            rsc[u][0] = (uint32_t)ld_ro_u16(sp0) | ((((uint32_t)ld_ro_u8(zp0 + (b >> 1))) >> sh & 0xF) << 16);
+            rsc[u][1] = (uint32_t)ld_ro_u16(sp1) | ((((uint32_t)ld_ro_u8(zp1 + (b >> 1))) >> sh & 0xF) << 16);
+        }
+        wp0 += 64;
+        wp1 += 64;
+        sp0 += SPB;
+        sp1 += SPB;
+        if (++lb == nb) {
+            lb = 0;
+            if (++lt < nt) set_rows(lt);
         }
     };
 
@@ -191,21 +208,26 @@ __global__ void __launch_bounds__(W * 32)
     pdl_wait();
 
     // Stage x for the CTA's k-range: xs[m][w] = 16-byte word w (8 k) of batch
-    // row m, INT4 pairs permuted.
-    const int cwords = max(0, min(KB, cb0 + W * BS) - cb0) * (BK / 8);
-    for (int i = threadIdx.x; i < mb * L.xwords; i += W * 32) {
-        const int m = i / L.xwords;
-        const int wi = i - m * L.xwords;
-        const int k = cb0 * BK + wi * 8;
+    // row m (INT4: pairs permuted), followed by XW zero words for lanes that
+    // carry no x.
+    uint4* xs = smem_u4;
+    const int cwords = max(0, min(KB, cb0 + W * BS) - cb0) * XW;
+    for (int i = threadIdx.x; i < mb * L.xwords + XW; i += W * 32) {
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (wi < cwords && k < a.K) v = ld_ro16(a.x + (size_t)m * a.K + k);
-        smem_u4[i] = (FMT == FMT_BF16) ? v : perm_pairs(v);
+        if (i < mb * L.xwords) {
+            const int m = i / L.xwords;
+            const int wi = i - m * L.xwords;
+            if (wi < cwords) v = ld_ro16(a.x + (size_t)m * a.K + (size_t)cb0 * BK + (size_t)wi * 8);
+            if (FMT != FMT_BF16) v = perm_pairs(v);
+        }
+        xs[i] = v;
     }
     __syncthreads();
 
-    // B-fragment source of this lane: column n = g.
-    int xm;
+    // B-fragment source of this lane: column n = g (batch g; group-64: batch
+    // g/2, group parity g%2 matching the lane's quad half).
     bool xon;
+    int xm;
     if (FMT == FMT_G64) {
         xm = g >> 1;
         xon = (xm < mb) && ((g & 1) == (q >> 1));
@@ -213,61 +235,67 @@ __global__ void __launch_bounds__(W * 32)
         xm = g;
         xon = xm < mb;
     }
-    const uint4* xw = smem_u4 + (size_t)(xon ? xm : 0) * L.xwords + (size_t)(b0 - cb0) * (BK / 8);
+    const uint4* xbase = xon ? xs + (size_t)xm * L.xwords + (size_t)(b0 - cb0) * XW : xs + (size_t)mb * L.xwords;
+    const int xstep = xon ? XW : 0;
+    const uint4* xp = xbase;
     float* red = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.red_off);
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    int ct = 0, cb = 0;  // tile and block (within the k-slice) of the step being consumed
+    float acc2[4] = {0.f, 0.f, 0.f, 0.f};  // second chain (BF16)
+    int cb = 0, ct = 0;
 
     for (int j0 = 0; j0 < total; j0 += U) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int j = j0 + u;
-            if (j < total) {
-                const uint4 wg = ring[u][0], wg8 = ring[u][1];
-                const uint32_t sg = sring[u][0], sg8 = sring[u][1];
-                if (j + U < total) load(u);
+            if (j0 + u < total) {
+                const uint4 w0 = rw[u][0], w1 = rw[u][1];
+                const uint32_t s0 = rsc[u][0], s1 = rsc[u][1];
+                if (j0 + u + U < total) load(u);
                 if (FMT == FMT_BF16) {
-                    const uint4 xv = xon ? xw[cb * 4 + q] : make_uint4(0, 0, 0, 0);
-                    mma_bf16_16816(acc, wg.x, wg8.x, wg.y, wg8.y, xv.x, xv.y);
-                    mma_bf16_16816(acc, wg.z, wg8.z, wg.w, wg8.w, xv.z, xv.w);
+                    const uint4 xv = xp[q];
+                    mma_bf16_16816(acc, w0.x, w1.x, w0.y, w1.y, xv.x, xv.y);
+                    mma_bf16_16816(acc2, w0.z, w1.z, w0.w, w1.w, xv.z, xv.w);
                 } else {
-                    const uint32_t zg = (FMT == FMT_G64) ? 8u : (sg >> 16);
-                    const uint32_t zg8 = (FMT == FMT_G64) ? 8u : (sg8 >> 16);
-                    const uint32_t zz0 = (0x4300u | zg) * 0x00010001u;  // (128 + z, 128 + z)
-                    const uint32_t zz1 = (0x4300u | zg8) * 0x00010001u;
-                    float d[4] = {0.f, 0.f, 0.f, 0.f};
-                    const uint32_t wa[4] = {wg.x, wg.y, wg.z, wg.w};
-                    const uint32_t wb[4] = {wg8.x, wg8.y, wg8.z, wg8.w};
+                    const uint32_t zz0 = (0x4300u | ((FMT == FMT_G64) ? 8u : (s0 >> 16))) * 0x00010001u;
+                    const uint32_t zz1 = (0x4300u | ((FMT == FMT_G64) ? 8u : (s1 >> 16))) * 0x00010001u;
+                    float d0[4] = {0.f, 0.f, 0.f, 0.f};
+                    float d1[4] = {0.f, 0.f, 0.f, 0.f};
+                    const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
+                    const uint32_t wb[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
-                        const uint4 xv = xon ? xw[cb * 16 + 4 * q + jj] : make_uint4(0, 0, 0, 0);
-                        const uint32_t a4 = wa[jj] >> 4, b4 = wb[jj] >> 4;
-                        const uint32_t a8 = wa[jj] >> 8, b8 = wb[jj] >> 8;
-                        const uint32_t a12 = wa[jj] >> 12, b12 = wb[jj] >> 12;
-                        mma_bf16_16816(d, bf16x2_sub(nib_pair(wa[jj]), zz0), bf16x2_sub(nib_pair(wb[jj]), zz1),
-                                       bf16x2_sub(nib_pair(a4), zz0), bf16x2_sub(nib_pair(b4), zz1), xv.x, xv.y);
-                        mma_bf16_16816(d, bf16x2_sub(nib_pair(a8), zz0), bf16x2_sub(nib_pair(b8), zz1),
-                                       bf16x2_sub(nib_pair(a12), zz0), bf16x2_sub(nib_pair(b12), zz1), xv.z,
-                                       xv.w);
+                        const uint4 xv = xp[4 * q + jj];
+                        mma_bf16_16816(d0, bf16x2_sub(nib_pair(wa[jj]), zz0), bf16x2_sub(nib_pair(wb[jj]), zz1),
+                                       bf16x2_sub(nib_pair(wa[jj] >> 4), zz0), bf16x2_sub(nib_pair(wb[jj] >> 4), zz1),
+                                       xv.x, xv.y);
+                        mma_bf16_16816(d1, bf16x2_sub(nib_pair(wa[jj] >> 8), zz0),
+                                       bf16x2_sub(nib_pair(wb[jj] >> 8), zz1), bf16x2_sub(nib_pair(wa[jj] >> 12), zz0),
+                                       bf16x2_sub(nib_pair(wb[jj] >> 12), zz1), xv.z, xv.w);
                     }
                     if (FMT == FMT_G64) {
                         // columns 2m (even group) and 2m + 1 (odd group) of batch m = q
-                        acc[0] = fmaf(f16_bits_to_f32(sg & 0xFFFF), d[0], acc[0]);
-                        acc[0] = fmaf(f16_bits_to_f32(sg >> 16), d[1], acc[0]);
-                        acc[2] = fmaf(f16_bits_to_f32(sg8 & 0xFFFF), d[2], acc[2]);
-                        acc[2] = fmaf(f16_bits_to_f32(sg8 >> 16), d[3], acc[2]);
+                        const float2 sg = __half22float2(*reinterpret_cast<const __half2*>(&s0));
+                        const float2 sg8 = __half22float2(*reinterpret_cast<const __half2*>(&s1));
+                        acc[0] = fmaf(sg.x, d0[0] + d1[0], acc[0]);
+                        acc[0] = fmaf(sg.y, d0[1] + d1[1], acc[0]);
+                        acc[2] = fmaf(sg8.x, d0[2] + d1[2], acc[2]);
+                        acc[2] = fmaf(sg8.y, d0[3] + d1[3], acc[2]);
                     } else {
-                        const float s0 = f16_bits_to_f32(sg & 0xFFFF), s1 = f16_bits_to_f32(sg8 & 0xFFFF);
-                        acc[0] = fmaf(s0, d[0], acc[0]);
-                        acc[1] = fmaf(s0, d[1], acc[1]);
-                        acc[2] = fmaf(s1, d[2], acc[2]);
-                        acc[3] = fmaf(s1, d[3], acc[3]);
+                        const float sa = f16_bits_to_f32(s0 & 0xFFFF), sb = f16_bits_to_f32(s1 & 0xFFFF);
+                        acc[0] = fmaf(sa, d0[0] + d1[0], acc[0]);
+                        acc[1] = fmaf(sa, d0[1] + d1[1], acc[1]);
+                        acc[2] = fmaf(sb, d0[2] + d1[2], acc[2]);
+                        acc[3] = fmaf(sb, d0[3] + d1[3], acc[3]);
                     }
                 }
+                xp += xstep;
                 if (++cb == nb) {
                     // tile done: its partials -> red[tile][warp][row][m]
                     float* rp = red + ((size_t)(ct * W + warp) * 16) * mb;
+                    if (FMT == FMT_BF16) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
+                    }
                     if (FMT == FMT_G64) {
                         if (q < mb) {
                             rp[g * mb + q] = acc[0];
@@ -283,9 +311,11 @@ __global__ void __launch_bounds__(W * 32)
                             rp[(g + 8) * mb + 2 * q + 1] = acc[3];
                         }
                     }
-                    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i] = acc2[i] = 0.f;
                     cb = 0;
                     ++ct;
+                    xp = xbase;
                 }
             }
         }
@@ -299,8 +329,7 @@ __global__ void __launch_bounds__(W * 32)
     }
     __syncthreads();
 
-    // Sum over warps in warp order: fin[tile][row][m] (reuses the x area,
-    // which is no longer read).
+    // Sum over warps in warp order: fin[tile][row][m] (reuses the x area).
     float* fin = reinterpret_cast<float*>(smem_u4);
     const int nout = nt * 16 * mb;
     for (int i = threadIdx.x; i < nout; i += W * 32) {

@@ -77,7 +77,8 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K) 
         const MmaConfig c = mma_config(fmt, p.cfg);
         if (p.occ < 1 || p.occ > 2) return false;
         const int mb = (int)std::min<int64_t>(M, mma_max_batch(fmt));
-        // every warp of the cluster gets at least one k-block
+        // whole row blocks only, and every warp of the cluster gets at least one
+        if (K % (fmt == FMT_BF16 ? 32 : 128) != 0) return false;
         if ((int64_t)p.split * c.warps > kblocks(fmt, K)) return false;
         if (mma_smem_bytes(fmt, c, N, K, mb, p.split, p.occ) > kSmemLimit) return false;
         return true;
@@ -355,6 +356,8 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
         if (e != cudaSuccess) break;
         std::sort(times, times + 3);
         const float per = times[1] / copies;
+        if (getenv("MBW_LOG") && atoi(getenv("MBW_LOG")) >= 2)
+            fprintf(stderr, "[mbw]   candidate %zu %s: %.3f us\n", ci, plan_to_string(op, p).c_str(), per * 1e3f);
         if (per < best_ms) {
             best_ms = per;
             best = p;
