@@ -14,14 +14,15 @@
 //   * A ring stage holds one tile (16 rows) x W 64-byte blocks of each row
 //     (consumer warp w takes block w). Rows sit at a stride of 64*W + 64 bytes
 //     so that the two rows each 8-lane phase of a 16-byte-per-lane load
-//     touches fall in disjoint banks. The producer issues one bulk copy per row per stage
-//     (16-byte aligned, 16-byte multiple) and arms the stage's full barrier
+//     touches fall in disjoint banks. The producer issues one bulk copy per
+//     row per stage (16-byte aligned, 16-byte multiple) and arms the stage's full barrier
 //     with the byte count; consumers arrive on the stage's empty barrier.
 //   * Programmatic dependent launch: the producer never waits for the
 //     previous grid (it only reads weights), so the ring fills while the
 //     previous kernel finishes; consumers wait before staging x.
 //   * Group scales (and AWQ zero points) are small: each consumer lane loads
-//     its own, one stage ahead.
+//     its own, two stages ahead. Producer and consumers walk the (tile,
+//     chunk) sequence with counters (no division in the loops).
 //   * Every mbarrier wait is bounded. On expiry the kernel records the fault in
 //     a device flag (read by mbw_check_device_error), the producer waits
 //     (bounded) for the copies it issued, and all threads leave normally.
@@ -136,7 +137,7 @@ __host__ __device__ inline TmaSmem tma_smem_layout(int fmt, int64_t K, int N, in
     L.ring_off = 0;
     L.stage_bytes = (size_t)16 * L.rowstride;
     L.x_off = L.ring_off + (size_t)D * L.stage_bytes;
-    const size_t x_bytes = (size_t)M * L.xwords * 16;
+    const size_t x_bytes = ((size_t)M * L.xwords + L.BK / 8) * 16;  // + one block of zero words
     const size_t fin_bytes = (size_t)L.ntmax * 16 * M * 4;
     L.red_off = L.x_off + ((x_bytes > fin_bytes ? x_bytes : fin_bytes) + 15) / 16 * 16;
     const size_t red_bytes = (size_t)L.ntmax * W * 16 * M * 4;
@@ -149,6 +150,7 @@ template <int FMT, int W, int D>
 __global__ void __launch_bounds__((W + 1) * 32)
     gemv_tma_kernel(const GemvArgs a, const int S) {
     constexpr int BK = (FMT == FMT_BF16) ? 32 : 128;
+    constexpr int XW = BK / 8;
     extern __shared__ __align__(128) uint8_t smem[];
 
     pdl_launch_dependents();
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__((W + 1) * 32)
     const int mb = a.M;
     const TmaSmem L = tma_smem_layout(FMT, a.K, a.N, mb, W, D, S, G);
 
-    const int KB = (a.K + BK - 1) / BK;
+    const int KB = a.K / BK;  // the plan guarantees K % BK == 0
     const int BS = (KB + S - 1) / S;
     const int cb0 = rank * BS;                       // first block of this CTA's k-range
     const int ncb = max(0, min(KB, cb0 + BS) - cb0);  // blocks in the k-range
@@ -184,51 +186,60 @@ __global__ void __launch_bounds__((W + 1) * 32)
 
     if (warp == W) {
         // ------------------------------------------------------ producer ----
-        if (lane == 0) {
+        if (lane == 0 && nstage > 0) {
             uint64_t policy;
             asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
             bool ok = true;
-            int issued = 0;
-            for (int i = 0; i < nstage && ok; ++i) {
-                const int s = i % D;
-                if (i >= D) ok = mbar_wait(&empty[s], ((i / D) - 1) & 1);
+            int s = 0, ph = 0;  // ring slot and its use count parity
+            int tl = 0, c = 0;  // tile and chunk of the stage being issued
+            int i = 0;
+            for (; i < nstage && ok; ++i) {
+                if (i >= D) ok = mbar_wait(&empty[s], ph ^ 1);
                 if (!ok) break;
-                const int tl = i / nchunk, c = i - tl * nchunk;
                 const int row0 = (t0 + tl) * 16;
                 const int nrows = min(16, a.N - row0);
-                const size_t off = (size_t)(cb0 + c * W) * 64;  // byte offset in a row
-                const uint32_t want = (uint32_t)min((size_t)min(W, ncb - c * W) * 64, rowbytes - off);
+                const int blk = cb0 + c * W;
+                const uint32_t want = (uint32_t)min(W, cb0 + ncb - blk) * 64;
                 mbar_expect_tx(&full[s], want * (uint32_t)nrows);
                 uint8_t* st = smem + L.ring_off + (size_t)s * L.stage_bytes;
+                const uint8_t* src = a.W + (size_t)row0 * rowbytes + (size_t)blk * 64;
                 for (int r = 0; r < nrows; ++r)
-                    bulk_g2s(st + (size_t)r * L.rowstride, a.W + (size_t)(row0 + r) * rowbytes + off, want,
-                             &full[s], policy);
-                ++issued;
+                    bulk_g2s(st + (size_t)r * L.rowstride, src + (size_t)r * rowbytes, want, &full[s], policy);
+                if (++s == D) {
+                    s = 0;
+                    ph ^= 1;
+                }
+                if (++c == nchunk) {
+                    c = 0;
+                    ++tl;
+                }
             }
             if (!ok) {
                 // drain: wait (bounded) for the copies already issued
-                for (int i = max(0, issued - D); i < issued; ++i) mbar_wait(&full[i % D], (i / D) & 1);
+                for (int j = max(0, i - 1 - D); j < i - 1; ++j) mbar_wait(&full[j % D], (j / D) & 1);
             }
         }
     } else {
         // ----------------------------------------------------- consumers ----
         const int g = lane >> 2, q = lane & 3;
         pdl_wait();
-        // stage x for the CTA's k-range (consumer warps only; named barrier 1)
-        const int cwords = ncb * (BK / 8);
+        // stage x for the CTA's k-range (+ zero words), consumer warps only
         uint4* xs = reinterpret_cast<uint4*>(smem + L.x_off);
-        for (int i = threadIdx.x; i < mb * L.xwords; i += W * 32) {
-            const int m = i / L.xwords;
-            const int wi = i - m * L.xwords;
-            const int k = cb0 * BK + wi * 8;
+        const int cwords = ncb * XW;
+        for (int i = threadIdx.x; i < mb * L.xwords + XW; i += W * 32) {
             uint4 v = make_uint4(0, 0, 0, 0);
-            if (wi < cwords && k < a.K) v = ld_ro16(a.x + (size_t)m * a.K + k);
-            xs[i] = (FMT == FMT_BF16) ? v : pair_perm(v);
+            if (i < mb * L.xwords) {
+                const int m = i / L.xwords;
+                const int wi = i - m * L.xwords;
+                if (wi < cwords) v = ld_ro16(a.x + (size_t)m * a.K + (size_t)cb0 * BK + (size_t)wi * 8);
+                if (FMT != FMT_BF16) v = pair_perm(v);
+            }
+            xs[i] = v;
         }
         asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
 
-        int xm;
         bool xon;
+        int xm;
         if (FMT == FMT_G64) {
             xm = g >> 1;
             xon = (xm < mb) && ((g & 1) == (q >> 1));
@@ -236,91 +247,111 @@ __global__ void __launch_bounds__((W + 1) * 32)
             xm = g;
             xon = xm < mb;
         }
-        // lanes that carry no x read a zero word instead (no selects in the loop)
-        const uint4* xw = xs + (size_t)(xon ? xm : 0) * L.xwords;
+        // x word of (chunk c, lane): xbase + c * xcstep; lanes without x read zeros
+        const uint4* xbase = xon ? xs + (size_t)xm * L.xwords + (size_t)warp * XW : xs + (size_t)mb * L.xwords;
+        const int xcstep = xon ? W * XW : 0;
         float* red = reinterpret_cast<float*>(smem + L.red_off);
         const int rs = L.rowstride;
+        const uint8_t* ring = smem + L.ring_off + warp * 64 + q * 16;
 
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t sc[2] = {0, 0};  // scale words of rows g, g+8 for the current stage
-        auto load_scales = [&](int i, uint32_t (&o)[2]) {
-            const int tl = i / nchunk, c = i - tl * nchunk;
-            const int b = cb0 + c * W + warp;
-            if (b >= cb0 + ncb || FMT == FMT_BF16) return;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = min((t0 + tl) * 16 + g + 8 * h, a.N - 1);
+        // scale cursor: rows g, g+8 of (tile st, chunk sc), this warp's block
+        int stt = 0, sch = 0;
+        auto scale_words = [&](uint32_t& o0, uint32_t& o1) {
+            o0 = o1 = 0;
+            if (FMT == FMT_BF16) return;
+            const int b = cb0 + sch * W + warp;
+            if (stt < nt && b < cb0 + ncb) {
+                const int r0 = min((t0 + stt) * 16 + g, a.N - 1);
+                const int r1 = min((t0 + stt) * 16 + g + 8, a.N - 1);
                 if (FMT == FMT_G64) {
-                    const uint16_t* sp = a.scales + (size_t)row * a.groups + 2 * b;
-                    const uint32_t s1 = (2 * b + 1 < a.groups) ? ld_ro_u16(sp + 1) : 0u;
-                    o[h] = (uint32_t)ld_ro_u16(sp) | (s1 << 16);
+                    const uint16_t* p0 = a.scales + (size_t)r0 * a.groups + 2 * b;
+                    const uint16_t* p1 = a.scales + (size_t)r1 * a.groups + 2 * b;
+                    o0 = (uint32_t)ld_ro_u16(p0) | ((uint32_t)ld_ro_u16(p0 + 1) << 16);
+                    o1 = (uint32_t)ld_ro_u16(p1) | ((uint32_t)ld_ro_u16(p1 + 1) << 16);
                 } else {
-                    const uint32_t s = ld_ro_u16(a.scales + (size_t)row * a.groups + b);
-                    const uint32_t zb = ld_ro_u8(a.zeros + (size_t)row * a.zstride + (b >> 1));
-                    o[h] = s | (((b & 1) ? (zb >> 4) : (zb & 0xF)) << 16);
+                    const uint32_t sh = (b & 1) * 4;
+                    o0 = (uint32_t)ld_ro_u16(a.scales + (size_t)r0 * a.groups + b) |
+                         ((((uint32_t)ld_ro_u8(a.zeros + (size_t)r0 * a.zstride + (b >> 1))) >> sh & 0xF) << 16);
+                    o1 = (uint32_t)ld_ro_u16(a.scales + (size_t)r1 * a.groups + b) |
+                         ((((uint32_t)ld_ro_u8(a.zeros + (size_t)r1 * a.zstride + (b >> 1))) >> sh & 0xF) << 16);
                 }
             }
+            if (++sch == nchunk) {
+                sch = 0;
+                ++stt;
+            }
         };
-        if (nstage > 0) load_scales(0, sc);
+        // scales two stages ahead: (sa0, sa1) for stage i, (sb0, sb1) for i + 1
+        uint32_t sa0, sa1, sb0, sb1;
+        scale_words(sa0, sa1);
+        scale_words(sb0, sb1);
 
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc2[4] = {0.f, 0.f, 0.f, 0.f};
         bool ok = true;
+        int s = 0, ph = 0, c = 0, tl = 0;
         for (int i = 0; i < nstage; ++i) {
-            const int s = i % D;
-            const int tl = i / nchunk, c = i - tl * nchunk;
-            uint32_t scn[2] = {0, 0};
-            if (i + 1 < nstage) load_scales(i + 1, scn);
-            if (ok) ok = mbar_wait(&full[s], (i / D) & 1);
-            const int b = cb0 + c * W + warp;  // this warp's block in the stage
+            uint32_t sn0, sn1;
+            scale_words(sn0, sn1);  // stage i + 2
+            if (ok) ok = mbar_wait(&full[s], ph);
+            const int b = cb0 + c * W + warp;
             if (ok && b < cb0 + ncb) {
-                const uint8_t* st = smem + L.ring_off + (size_t)s * L.stage_bytes + warp * 64 + q * 16;
-                uint4 wg = *reinterpret_cast<const uint4*>(st + g * rs);
-                uint4 wg8 = *reinterpret_cast<const uint4*>(st + (g + 8) * rs);
-                const int lb = b - cb0;
-                if ((size_t)b * 64 + (q + 1) * 16 > rowbytes) {
-                    // tail of a partial block: no weights there (and no x)
-                    wg = make_uint4(0, 0, 0, 0);
-                    wg8 = make_uint4(0, 0, 0, 0);
-                }
+                const uint8_t* st = ring + (size_t)s * L.stage_bytes;
+                const uint4 w0 = *reinterpret_cast<const uint4*>(st + g * rs);
+                const uint4 w1 = *reinterpret_cast<const uint4*>(st + (g + 8) * rs);
+                const uint4* xp = xbase + (size_t)c * xcstep;
                 if (FMT == FMT_BF16) {
-                    const uint4 xv = xw[lb * 4 + q];
-                    const uint4 x0 = xon ? xv : make_uint4(0, 0, 0, 0);
-                    mma_16816(acc, wg.x, wg8.x, wg.y, wg8.y, x0.x, x0.y);
-                    mma_16816(acc, wg.z, wg8.z, wg.w, wg8.w, x0.z, x0.w);
+                    const uint4 xv = xp[q];
+                    mma_16816(acc, w0.x, w1.x, w0.y, w1.y, xv.x, xv.y);
+                    mma_16816(acc2, w0.z, w1.z, w0.w, w1.w, xv.z, xv.w);
                 } else {
-                    const uint32_t zz0 = (0x4300u | ((FMT == FMT_G64) ? 8u : (sc[0] >> 16))) * 0x00010001u;
-                    const uint32_t zz1 = (0x4300u | ((FMT == FMT_G64) ? 8u : (sc[1] >> 16))) * 0x00010001u;
-                    float d[4] = {0.f, 0.f, 0.f, 0.f};
-                    const uint32_t wa[4] = {wg.x, wg.y, wg.z, wg.w};
-                    const uint32_t wb[4] = {wg8.x, wg8.y, wg8.z, wg8.w};
+                    const uint32_t zz0 = (0x4300u | ((FMT == FMT_G64) ? 8u : (sa0 >> 16))) * 0x00010001u;
+                    const uint32_t zz1 = (0x4300u | ((FMT == FMT_G64) ? 8u : (sa1 >> 16))) * 0x00010001u;
+                    float d0[4] = {0.f, 0.f, 0.f, 0.f};
+                    float d1[4] = {0.f, 0.f, 0.f, 0.f};
+                    const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
+                    const uint32_t wb[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
-                        uint4 xv = xw[lb * 16 + 4 * q + jj];
-                        if (!xon) xv = make_uint4(0, 0, 0, 0);
-                        mma_16816(d, bsub(nibs(wa[jj]), zz0), bsub(nibs(wb[jj]), zz1), bsub(nibs(wa[jj] >> 4), zz0),
+                        const uint4 xv = xp[4 * q + jj];
+                        mma_16816(d0, bsub(nibs(wa[jj]), zz0), bsub(nibs(wb[jj]), zz1), bsub(nibs(wa[jj] >> 4), zz0),
                                   bsub(nibs(wb[jj] >> 4), zz1), xv.x, xv.y);
-                        mma_16816(d, bsub(nibs(wa[jj] >> 8), zz0), bsub(nibs(wb[jj] >> 8), zz1),
+                        mma_16816(d1, bsub(nibs(wa[jj] >> 8), zz0), bsub(nibs(wb[jj] >> 8), zz1),
                                   bsub(nibs(wa[jj] >> 12), zz0), bsub(nibs(wb[jj] >> 12), zz1), xv.z, xv.w);
                     }
                     if (FMT == FMT_G64) {
-                        acc[0] = fmaf(f16_bits_to_f32(sc[0] & 0xFFFF), d[0], acc[0]);
-                        acc[0] = fmaf(f16_bits_to_f32(sc[0] >> 16), d[1], acc[0]);
-                        acc[2] = fmaf(f16_bits_to_f32(sc[1] & 0xFFFF), d[2], acc[2]);
-                        acc[2] = fmaf(f16_bits_to_f32(sc[1] >> 16), d[3], acc[2]);
+                        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&sa0));
+                        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&sa1));
+                        acc[0] = fmaf(f0.x, d0[0] + d1[0], acc[0]);
+                        acc[0] = fmaf(f0.y, d0[1] + d1[1], acc[0]);
+                        acc[2] = fmaf(f1.x, d0[2] + d1[2], acc[2]);
+                        acc[2] = fmaf(f1.y, d0[3] + d1[3], acc[2]);
                     } else {
-                        const float s0 = f16_bits_to_f32(sc[0] & 0xFFFF), s1 = f16_bits_to_f32(sc[1] & 0xFFFF);
-                        acc[0] = fmaf(s0, d[0], acc[0]);
-                        acc[1] = fmaf(s0, d[1], acc[1]);
-                        acc[2] = fmaf(s1, d[2], acc[2]);
-                        acc[3] = fmaf(s1, d[3], acc[3]);
+                        const float f0 = f16_bits_to_f32(sa0 & 0xFFFF), f1 = f16_bits_to_f32(sa1 & 0xFFFF);
+                        acc[0] = fmaf(f0, d0[0] + d1[0], acc[0]);
+                        acc[1] = fmaf(f0, d0[1] + d1[1], acc[1]);
+                        acc[2] = fmaf(f1, d0[2] + d1[2], acc[2]);
+                        acc[3] = fmaf(f1, d0[3] + d1[3], acc[3]);
                     }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
-            sc[0] = scn[0];
-            sc[1] = scn[1];
-            if (c == nchunk - 1) {
+            sa0 = sb0;
+            sa1 = sb1;
+            sb0 = sn0;
+            sb1 = sn1;
+            if (++s == D) {
+                s = 0;
+                ph ^= 1;
+            }
+            if (++c == nchunk) {
+                c = 0;
                 float* rp = red + ((size_t)(tl * W + warp) * 16) * mb;
+                if (FMT == FMT_BF16) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) acc[k] += acc2[k];
+                }
                 if (FMT == FMT_G64) {
                     if (q < mb) {
                         rp[g * mb + q] = acc[0];
@@ -336,13 +367,15 @@ __global__ void __launch_bounds__((W + 1) * 32)
                         rp[(g + 8) * mb + 2 * q + 1] = acc[3];
                     }
                 }
-                acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[k] = acc2[k] = 0.f;
+                ++tl;
             }
         }
         if (nchunk == 0) {
             for (int t = 0; t < nt; ++t) {
                 float* rp = red + ((size_t)(t * W + warp) * 16) * mb;
-                for (int i = lane; i < 16 * mb; i += 32) rp[i] = 0.f;
+                for (int k = lane; k < 16 * mb; k += 32) rp[k] = 0.f;
             }
         }
     }

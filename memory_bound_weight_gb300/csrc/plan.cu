@@ -88,6 +88,7 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K) 
         const TmaConfig c = tma_config(fmt, p.cfg);
         if (p.occ < 1 || p.occ > 2) return false;
         const int mb = (int)std::min<int64_t>(M, mma_max_batch(fmt));
+        if (K % (fmt == FMT_BF16 ? 32 : 128) != 0) return false;
         if ((int64_t)p.split > kblocks(fmt, K)) return false;
         if (tma_smem_bytes(fmt, c, N, K, mb, p.split, p.occ) > kSmemLimit) return false;
         return true;
