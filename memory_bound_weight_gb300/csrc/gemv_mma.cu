@@ -363,6 +363,277 @@ __global__ void __launch_bounds__(W * 32)
     cluster.sync();
 }
 
+// ----------------------------------------------------------------------------
+// "mma2": 32 bytes of each of rows g and g+8 per lane per 128-byte super-block.
+//
+// A lane's 32 bytes of a row are 64 INT4 codes = exactly one group-64 scale
+// group (or half an AWQ group-128 group, or 16 BF16 weights). The 4 lanes of a
+// quad cover 4 groups; the B fragment routes column n = 4m + j only the x of
+// quad lane j (group j) of batch m, so each MMA keeps the 4 groups apart in 4
+// columns and a lane needs only the 2 scales of its own columns. Compared to
+// 16-byte chunks this halves the load, scale and epilogue instructions per
+// weight; the nibble arithmetic (3 shifts + 4 LOP3 + 4 bf16 subtracts per 8
+// codes) is unchanged.
+//   group-64 : column n = 4m + j, batch M <= 2; lane (g,q) holds groups
+//              2(q&1), 2(q&1)+1 of batch q>>1; lanes q and q^1 are summed at
+//              the end of a tile.
+//   AWQ      : column n = 2m + j, j = group within the super-block, M <= 4;
+//              lane (g,q) holds both groups of batch q.
+//   BF16     : column n = m (M <= 8); lane q's 16 weights feed 4 MMAs.
+template <int FMT, int W, int U>
+__global__ void __launch_bounds__(W * 32)
+    gemv_mma2_kernel(const GemvArgs a, const int S) {
+    constexpr int BK = (FMT == FMT_BF16) ? 64 : 256;  // k per 128-byte row super-block
+    constexpr int XW = BK / 8;                        // 16-byte x words per super-block
+    extern __shared__ uint4 smem_u4[];
+
+    pdl_launch_dependents();
+
+    const int rank = (S > 1) ? (int)cg::this_cluster().block_rank() : 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int G = gridDim.x / S;
+    const int cgid = blockIdx.x / S;
+    const int T = (a.N + 15) / 16;
+    const int t0 = (int)(((long long)T * cgid) / G);
+    const int nt = (int)(((long long)T * (cgid + 1)) / G) - t0;
+    const int mb = a.M;
+    const MmaSmem L = mma_smem_layout(BK, a.K, a.N, mb, W, S, G);
+
+    const int KB = a.K / BK;  // the plan guarantees K % BK == 0
+    const int BS = (KB + S * W - 1) / (S * W);
+    const int cb0 = rank * W * BS;
+    const int b0 = cb0 + warp * BS;
+    const int nb = max(0, min(KB, b0 + BS) - b0);
+    const int total = nt * nb;
+    const size_t rowbytes = (FMT == FMT_BF16) ? (size_t)a.K * 2 : (size_t)a.K / 2;
+
+    // load cursor (rows g, g+8 of the tile being loaded)
+    int lb = 0, lt = 0;
+    const uint8_t* wp0 = nullptr;
+    const uint8_t* wp1 = nullptr;
+    const uint16_t* sp0 = nullptr;
+    const uint16_t* sp1 = nullptr;
+    const uint8_t* zp0 = nullptr;
+    const uint8_t* zp1 = nullptr;
+    auto set_rows = [&](int t) {
+        const int r0 = min((t0 + t) * 16 + g, a.N - 1);
+        const int r1 = min((t0 + t) * 16 + g + 8, a.N - 1);
+        wp0 = a.W + (size_t)r0 * rowbytes + (size_t)b0 * 128 + q * 32;
+        wp1 = a.W + (size_t)r1 * rowbytes + (size_t)b0 * 128 + q * 32;
+        if (FMT == FMT_G64) {
+            sp0 = a.scales + (size_t)r0 * a.groups + (size_t)b0 * 4 + 2 * (q & 1);
+            sp1 = a.scales + (size_t)r1 * a.groups + (size_t)b0 * 4 + 2 * (q & 1);
+        } else if (FMT == FMT_AWQ) {
+            sp0 = a.scales + (size_t)r0 * a.groups + (size_t)b0 * 2;
+            sp1 = a.scales + (size_t)r1 * a.groups + (size_t)b0 * 2;
+            zp0 = a.zeros + (size_t)r0 * a.zstride + b0;
+            zp1 = a.zeros + (size_t)r1 * a.zstride + b0;
+        }
+    };
+    if (nt > 0) set_rows(0);
+
+    uint4 rw[U][4];      // [u][0..1] row g (32 bytes), [u][2..3] row g+8
+    uint32_t rs[U][2];   // group-64: 2 fp16 scales per row; AWQ: 2 fp16 scales per row
+    uint32_t rz[U];      // AWQ: zero-point byte of rows g (bits 0-7) and g+8 (bits 8-15)
+
+    auto load = [&](int u) {
+        rw[u][0] = ld_stream16(wp0);
+        rw[u][1] = ld_stream16(wp0 + 16);
+        rw[u][2] = ld_stream16(wp1);
+        rw[u][3] = ld_stream16(wp1 + 16);
+        if (FMT != FMT_BF16) {
+            rs[u][0] = (uint32_t)ld_ro_u16(sp0) | ((uint32_t)ld_ro_u16(sp0 + 1) << 16);
+            rs[u][1] = (uint32_t)ld_ro_u16(sp1) | ((uint32_t)ld_ro_u16(sp1 + 1) << 16);
+        }
+        if (FMT == FMT_AWQ) rz[u] = (uint32_t)ld_ro_u8(zp0) | ((uint32_t)ld_ro_u8(zp1) << 8);
+        wp0 += 128;
+        wp1 += 128;
+        sp0 += (FMT == FMT_G64) ? 4 : 2;
+        sp1 += (FMT == FMT_G64) ? 4 : 2;
+        zp0 += 1;
+        zp1 += 1;
+        if (++lb == nb) {
+            lb = 0;
+            if (++lt < nt) set_rows(lt);
+        }
+    };
+
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (u < total) load(u);
+
+    pdl_wait();
+
+    uint4* xs = smem_u4;
+    const int cwords = max(0, min(KB, cb0 + W * BS) - cb0) * XW;
+    for (int i = threadIdx.x; i < mb * L.xwords + XW; i += W * 32) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (i < mb * L.xwords) {
+            const int m = i / L.xwords;
+            const int wi = i - m * L.xwords;
+            if (wi < cwords) v = ld_ro16(a.x + (size_t)m * a.K + (size_t)cb0 * BK + (size_t)wi * 8);
+            if (FMT != FMT_BF16) v = perm_pairs(v);
+        }
+        xs[i] = v;
+    }
+    __syncthreads();
+
+    // B fragment of this lane: column n = g
+    bool xon;
+    int xm;
+    if (FMT == FMT_G64) {
+        xm = g >> 2;
+        xon = (xm < mb) && ((g & 3) == q);
+    } else if (FMT == FMT_AWQ) {
+        xm = g >> 1;
+        xon = (xm < mb) && ((g & 1) == (q >> 1));
+    } else {
+        xm = g;
+        xon = xm < mb;
+    }
+    // lane's x words of a super-block: INT4 words 8q .. 8q+7, BF16 words 2q, 2q+1
+    const int xoff = (FMT == FMT_BF16) ? 2 * q : 8 * q;
+    const uint4* xbase = xon ? xs + (size_t)xm * L.xwords + (size_t)(b0 - cb0) * XW + xoff : xs + (size_t)mb * L.xwords;
+    const int xstep = xon ? XW : 0;
+    const uint4* xp = xbase;
+    float* red = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.red_off);
+
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+    int cb = 0, ct = 0;
+
+    for (int j0 = 0; j0 < total; j0 += U) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (j0 + u < total) {
+                const uint4 a0 = rw[u][0], a1 = rw[u][1], c0 = rw[u][2], c1 = rw[u][3];
+                const uint32_t s0 = rs[u][0], s1 = rs[u][1];
+                const uint32_t zb = (FMT == FMT_AWQ) ? rz[u] : 0u;
+                if (j0 + u + U < total) load(u);
+                if (FMT == FMT_BF16) {
+                    const uint4 x0 = xp[0], x1 = xp[1];
+                    mma_bf16_16816(acc, a0.x, c0.x, a0.y, c0.y, x0.x, x0.y);
+                    mma_bf16_16816(acc2, a0.z, c0.z, a0.w, c0.w, x0.z, x0.w);
+                    mma_bf16_16816(acc, a1.x, c1.x, a1.y, c1.y, x1.x, x1.y);
+                    mma_bf16_16816(acc2, a1.z, c1.z, a1.w, c1.w, x1.z, x1.w);
+                } else {
+                    uint32_t zz0, zz1;
+                    if (FMT == FMT_G64) {
+                        zz0 = zz1 = 0x43084308u;
+                    } else {
+                        const uint32_t sh = (q >> 1) * 4;  // this lane's group: low or high nibble
+                        zz0 = (0x4300u | ((zb >> sh) & 0xF)) * 0x00010001u;
+                        zz1 = (0x4300u | ((zb >> (8 + sh)) & 0xF)) * 0x00010001u;
+                    }
+                    float d0[4] = {0.f, 0.f, 0.f, 0.f};
+                    float d1[4] = {0.f, 0.f, 0.f, 0.f};
+                    const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                    const uint32_t wb[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const uint4 xv = xp[w];
+                        mma_bf16_16816(d0, bf16x2_sub(nib_pair(wa[w]), zz0), bf16x2_sub(nib_pair(wb[w]), zz1),
+                                       bf16x2_sub(nib_pair(wa[w] >> 4), zz0), bf16x2_sub(nib_pair(wb[w] >> 4), zz1),
+                                       xv.x, xv.y);
+                        mma_bf16_16816(d1, bf16x2_sub(nib_pair(wa[w] >> 8), zz0), bf16x2_sub(nib_pair(wb[w] >> 8), zz1),
+                                       bf16x2_sub(nib_pair(wa[w] >> 12), zz0),
+                                       bf16x2_sub(nib_pair(wb[w] >> 12), zz1), xv.z, xv.w);
+                    }
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&s0));
+                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&s1));
+                    if (FMT == FMT_G64) {
+                        // columns 2q, 2q+1 = groups 2(q&1), 2(q&1)+1 of batch q>>1
+                        acc[0] = fmaf(f0.x, d0[0] + d1[0], acc[0]);
+                        acc[0] = fmaf(f0.y, d0[1] + d1[1], acc[0]);
+                        acc[2] = fmaf(f1.x, d0[2] + d1[2], acc[2]);
+                        acc[2] = fmaf(f1.y, d0[3] + d1[3], acc[2]);
+                    } else {
+                        // columns 2q, 2q+1 = groups 0, 1 of batch q
+                        acc[0] = fmaf(f0.x, d0[0] + d1[0], acc[0]);
+                        acc[0] = fmaf(f0.y, d0[1] + d1[1], acc[0]);
+                        acc[2] = fmaf(f1.x, d0[2] + d1[2], acc[2]);
+                        acc[2] = fmaf(f1.y, d0[3] + d1[3], acc[2]);
+                    }
+                }
+                xp += xstep;
+                if (++cb == nb) {
+                    float* rp = red + ((size_t)(ct * W + warp) * 16) * mb;
+                    if (FMT == FMT_BF16) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
+                        if (2 * q < mb) {
+                            rp[g * mb + 2 * q] = acc[0];
+                            rp[(g + 8) * mb + 2 * q] = acc[2];
+                        }
+                        if (2 * q + 1 < mb) {
+                            rp[g * mb + 2 * q + 1] = acc[1];
+                            rp[(g + 8) * mb + 2 * q + 1] = acc[3];
+                        }
+                    } else if (FMT == FMT_G64) {
+                        // lanes q and q^1 hold the other two groups of the same batch
+                        const float v0 = acc[0] + __shfl_xor_sync(0xFFFFFFFFu, acc[0], 1);
+                        const float v2 = acc[2] + __shfl_xor_sync(0xFFFFFFFFu, acc[2], 1);
+                        const int m = q >> 1;
+                        if ((q & 1) == 0 && m < mb) {
+                            rp[g * mb + m] = v0;
+                            rp[(g + 8) * mb + m] = v2;
+                        }
+                    } else {
+                        if (q < mb) {
+                            rp[g * mb + q] = acc[0];
+                            rp[(g + 8) * mb + q] = acc[2];
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i] = acc2[i] = 0.f;
+                    cb = 0;
+                    ++ct;
+                    xp = xbase;
+                }
+            }
+        }
+    }
+    if (nb == 0) {
+        for (int t = 0; t < nt; ++t) {
+            float* rp = red + ((size_t)(t * W + warp) * 16) * mb;
+            for (int i = lane; i < 16 * mb; i += 32) rp[i] = 0.f;
+        }
+    }
+    __syncthreads();
+
+    float* fin = reinterpret_cast<float*>(smem_u4);
+    const int nout = nt * 16 * mb;
+    for (int i = threadIdx.x; i < nout; i += W * 32) {
+        const int t = i / (16 * mb);
+        const int rm = i - t * 16 * mb;
+        float v = 0.f;
+        for (int w = 0; w < W; ++w) v += red[((size_t)(t * W + w) * 16) * mb + rm];
+        fin[i] = v;
+    }
+    const int row0 = t0 * 16;
+    if (S == 1) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < nout; i += W * 32) {
+            const int m = i / (nt * 16), lr = i - m * nt * 16;
+            if (row0 + lr < a.N) store_out(a.y, (int64_t)m * a.N + row0 + lr, fin[lr * mb + m], a.out_f32);
+        }
+        return;
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int R = nt * 16;
+    const int lo = rank * R / S, hi = (rank + 1) * R / S;
+    const int span = hi - lo;
+    for (int i = threadIdx.x; i < span * mb; i += W * 32) {
+        const int m = i / span, lr = lo + (i - m * span);
+        float v = 0.f;
+        for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(fin + lr * mb + m, s);
+        if (row0 + lr < a.N) store_out(a.y, (int64_t)m * a.N + row0 + lr, v, a.out_f32);
+    }
+    cluster.sync();
+}
+
 // ------------------------------------------------------------- tables ----
 using MmaFn = void (*)(const GemvArgs, const int);
 struct MmaEntry {
@@ -382,6 +653,81 @@ static const MmaEntry kMmaAwq[] = {
     MBW_M(FMT_AWQ, 4, 2), MBW_M(FMT_AWQ, 4, 4), MBW_M(FMT_AWQ, 8, 2), MBW_M(FMT_AWQ, 8, 4),
 };
 #undef MBW_M
+
+#define MBW_M2(F, W, U) \
+    { {W, U}, gemv_mma2_kernel<F, W, U> }
+static const MmaEntry kMma2Bf16[] = {MBW_M2(FMT_BF16, 8, 2), MBW_M2(FMT_BF16, 8, 4), MBW_M2(FMT_BF16, 4, 4)};
+static const MmaEntry kMma2G64[] = {MBW_M2(FMT_G64, 8, 2), MBW_M2(FMT_G64, 8, 3), MBW_M2(FMT_G64, 4, 2),
+                                    MBW_M2(FMT_G64, 4, 3)};
+static const MmaEntry kMma2Awq[] = {MBW_M2(FMT_AWQ, 8, 2), MBW_M2(FMT_AWQ, 8, 3), MBW_M2(FMT_AWQ, 4, 2)};
+#undef MBW_M2
+
+static const MmaEntry* mma2_table(int fmt, int* n) {
+    switch (fmt) {
+        case FMT_BF16:
+            *n = (int)(sizeof(kMma2Bf16) / sizeof(kMma2Bf16[0]));
+            return kMma2Bf16;
+        case FMT_G64:
+            *n = (int)(sizeof(kMma2G64) / sizeof(kMma2G64[0]));
+            return kMma2G64;
+        default:
+            *n = (int)(sizeof(kMma2Awq) / sizeof(kMma2Awq[0]));
+            return kMma2Awq;
+    }
+}
+
+int mma2_num_configs(int fmt) {
+    int n;
+    mma2_table(fmt, &n);
+    return n;
+}
+
+MmaConfig mma2_config(int fmt, int idx) {
+    int n;
+    return mma2_table(fmt, &n)[idx].cfg;
+}
+
+int mma2_max_batch(int fmt) { return fmt == FMT_G64 ? 2 : fmt == FMT_AWQ ? 4 : 8; }
+int mma2_block_k(int fmt) { return fmt == FMT_BF16 ? 64 : 256; }
+
+size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
+    const int G = mma_row_groups(N, split, occ);
+    return mma_smem_layout(mma2_block_k(fmt), K, (int)N, M, c.warps, split, G).total;
+}
+
+cudaError_t launch_gemv_mma2(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
+    int n;
+    const MmaEntry* t = mma2_table(fmt, &n);
+    if (p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > mma2_max_batch(fmt)) return cudaErrorInvalidValue;
+    const MmaEntry& e = t[p.cfg];
+    const int G = mma_row_groups(a.N, p.split, p.occ);
+    const size_t smem = mma2_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
+    if (smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(G * p.split), 1, 1);
+    cfg.blockDim = dim3((unsigned)(e.cfg.warps * 32), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (p.split > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)p.split;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    count_launch();
+    return cudaLaunchKernelEx(&cfg, e.fn, a, p.split);
+}
 
 static const MmaEntry* mma_table(int fmt, int* n) {
     switch (fmt) {

@@ -55,7 +55,7 @@ struct Plan {
     int split;  // CTAs per cluster along K (1 = no split)
     int occ;    // MMA kernels: CTAs per SM in the persistent grid (1 for SIMT)
 };
-enum PlanKind : int { PLAN_SIMT = 0, PLAN_MMA = 1, PLAN_TMA = 2 };
+enum PlanKind : int { PLAN_SIMT = 0, PLAN_MMA = 1, PLAN_TMA = 2, PLAN_MMA2 = 3 };
 
 // Kernel tables (gemv_simt.cu).
 int simt_num_configs(int fmt);
@@ -70,6 +70,14 @@ int mma_max_batch(int fmt);
 size_t mma_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ);
 int mma_row_groups(int64_t N, int split, int occ);
 cudaError_t launch_gemv_mma(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
+
+// 32-bytes-per-lane tensor-core kernel tables (gemv_mma.cu).
+int mma2_num_configs(int fmt);
+MmaConfig mma2_config(int fmt, int idx);
+int mma2_max_batch(int fmt);
+int mma2_block_k(int fmt);
+size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ);
+cudaError_t launch_gemv_mma2(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
 
 // Bulk-copy-fed kernel tables (gemv_tma.cu).
 int tma_num_configs(int fmt);

@@ -51,6 +51,7 @@ static size_t simt_smem(int fmt, const SimtConfig& c, int64_t K, int split) {
 static int simt_want_mb(int64_t M) { return M <= 2 ? (int)M : M <= 4 ? 4 : 8; }
 
 int plan_batch_width(int fmt, const Plan& p) {
+    if (p.kind == PLAN_MMA2) return mma2_max_batch(fmt);
     if (p.kind == PLAN_MMA || p.kind == PLAN_TMA) return mma_max_batch(fmt);
     return simt_config(fmt, p.cfg).mb;
 }
@@ -83,6 +84,17 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K) 
         if (mma_smem_bytes(fmt, c, N, K, mb, p.split, p.occ) > kSmemLimit) return false;
         return true;
     }
+    if (p.kind == PLAN_MMA2) {
+        if (p.cfg < 0 || p.cfg >= mma2_num_configs(fmt)) return false;
+        const MmaConfig c = mma2_config(fmt, p.cfg);
+        if (p.occ < 1 || p.occ > 2) return false;
+        const int bk = mma2_block_k(fmt);
+        if (K % bk != 0) return false;
+        const int mb = (int)std::min<int64_t>(M, mma2_max_batch(fmt));
+        if ((int64_t)p.split * c.warps > K / bk) return false;
+        if (mma2_smem_bytes(fmt, c, N, K, mb, p.split, p.occ) > kSmemLimit) return false;
+        return true;
+    }
     if (p.kind == PLAN_TMA) {
         if (p.cfg < 0 || p.cfg >= tma_num_configs(fmt)) return false;
         const TmaConfig c = tma_config(fmt, p.cfg);
@@ -105,6 +117,12 @@ static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
         for (int si = 0; si < 4; ++si)
             for (int occ = 1; occ <= 2; ++occ) {
                 Plan p{PLAN_MMA, cfg, splits[si], occ};
+                if (plan_valid(fmt, p, Mb, N, K)) out.push_back(p);
+            }
+    for (int cfg = 0; cfg < mma2_num_configs(fmt); ++cfg)
+        for (int si = 0; si < 4; ++si)
+            for (int occ = 1; occ <= 2; ++occ) {
+                Plan p{PLAN_MMA2, cfg, splits[si], occ};
                 if (plan_valid(fmt, p, Mb, N, K)) out.push_back(p);
             }
     for (int cfg = 0; cfg < tma_num_configs(fmt); ++cfg)
@@ -175,7 +193,11 @@ std::string plan_to_string(int op, const Plan& p) {
     const int fmt = fmt_of_op(op);
     const char* fs = fmt == FMT_BF16 ? "bf16" : fmt == FMT_G64 ? "int4_g64" : "int4_awq_g128";
     char buf[192];
-    if (p.kind == PLAN_TMA) {
+    if (p.kind == PLAN_MMA2) {
+        const MmaConfig c = mma2_config(fmt, p.cfg);
+        snprintf(buf, sizeof(buf), "mma2 fmt=%s warps=%d superblocks_in_flight=%d ctas_per_sm=%d split_k=%d", fs,
+                 c.warps, c.u, p.occ, p.split);
+    } else if (p.kind == PLAN_TMA) {
         const TmaConfig c = tma_config(fmt, p.cfg);
         snprintf(buf, sizeof(buf), "tma fmt=%s consumer_warps=%d ring_stages=%d ctas_per_sm=%d split_k=%d", fs,
                  c.warps, c.depth, p.occ, p.split);
@@ -192,6 +214,7 @@ std::string plan_to_string(int op, const Plan& p) {
 }
 
 cudaError_t launch_plan(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
+    if (p.kind == PLAN_MMA2) return launch_gemv_mma2(fmt, p, a, s);
     if (p.kind == PLAN_TMA) return launch_gemv_tma(fmt, p, a, s);
     if (p.kind == PLAN_MMA) return launch_gemv_mma(fmt, p, a, s);
     return launch_gemv_simt(fmt, p, a, s);
