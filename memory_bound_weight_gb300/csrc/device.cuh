@@ -57,6 +57,18 @@ __device__ __forceinline__ uint8_t ld_ro_u8(const void* p) {
     return (uint8_t)r;
 }
 
+// 16-byte asynchronous global -> shared copy (L2 only), grouped per thread.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gmem_src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ------------------------------------------- programmatic dependent launch ----
 // The next kernel in the stream may start its prologue (weight prefetch) once
 // every CTA of this grid has issued launch_dependents.

@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(W * 32)
 //   AWQ      : column n = 2m + j, j = group within the super-block, M <= 4;
 //              lane (g,q) holds both groups of batch q.
 //   BF16     : column n = m (M <= 8); lane q's 16 weights feed 4 MMAs.
-template <int FMT, int W, int U>
+template <int FMT, int W, int U, int ASYNC>
 __global__ void __launch_bounds__(W * 32)
     gemv_mma2_kernel(const GemvArgs a, const int S) {
     constexpr int BK = (FMT == FMT_BF16) ? 64 : 256;  // k per 128-byte row super-block
@@ -433,15 +433,28 @@ __global__ void __launch_bounds__(W * 32)
     };
     if (nt > 0) set_rows(0);
 
-    uint4 rw[U][4];      // [u][0..1] row g (32 bytes), [u][2..3] row g+8
+    uint4 rw[U][4];      // [u][0..1] row g (32 bytes), [u][2..3] row g+8 (register ring)
+    // cp.async ring (ASYNC): slot u of this warp holds chunk c of lane l at
+    // ((warp * U + u) * 4 + c) * 512 + l * 16, so 8-lane phases touch 128
+    // contiguous bytes; each lane reads back only the bytes it copied.
+    uint8_t* aring = reinterpret_cast<uint8_t*>(smem_u4) + (L.total + 127) / 128 * 128 +
+                     (size_t)warp * U * 4 * 512 + lane * 16;
     uint32_t rs[U][2];   // group-64: 2 fp16 scales per row; AWQ: 2 fp16 scales per row
     uint32_t rz[U];      // AWQ: zero-point byte of rows g (bits 0-7) and g+8 (bits 8-15)
 
     auto load = [&](int u) {
-        rw[u][0] = ld_stream16(wp0);
-        rw[u][1] = ld_stream16(wp0 + 16);
-        rw[u][2] = ld_stream16(wp1);
-        rw[u][3] = ld_stream16(wp1 + 16);
+        if (ASYNC) {
+            uint8_t* d = aring + (size_t)u * 4 * 512;
+            cp_async16(d, wp0);
+            cp_async16(d + 512, wp0 + 16);
+            cp_async16(d + 1024, wp1);
+            cp_async16(d + 1536, wp1 + 16);
+        } else {
+            rw[u][0] = ld_stream16(wp0);
+            rw[u][1] = ld_stream16(wp0 + 16);
+            rw[u][2] = ld_stream16(wp1);
+            rw[u][3] = ld_stream16(wp1 + 16);
+        }
         if (FMT != FMT_BF16) {
             rs[u][0] = (uint32_t)ld_ro_u16(sp0) | ((uint32_t)ld_ro_u16(sp0 + 1) << 16);
             rs[u][1] = (uint32_t)ld_ro_u16(sp1) | ((uint32_t)ld_ro_u16(sp1 + 1) << 16);
@@ -460,8 +473,10 @@ __global__ void __launch_bounds__(W * 32)
     };
 
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+    for (int u = 0; u < U; ++u) {
         if (u < total) load(u);
+        if (ASYNC) cp_async_commit();  // one group per step, empty past the end
+    }
 
     pdl_wait();
 
@@ -507,10 +522,23 @@ __global__ void __launch_bounds__(W * 32)
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (j0 + u < total) {
-                const uint4 a0 = rw[u][0], a1 = rw[u][1], c0 = rw[u][2], c1 = rw[u][3];
+                uint4 a0, a1, c0, c1;
+                if (ASYNC) {
+                    cp_async_wait<U - 1>();  // step j0 + u has landed (one group per step)
+                    const uint8_t* d = aring + (size_t)u * 4 * 512;
+                    a0 = *reinterpret_cast<const uint4*>(d);
+                    a1 = *reinterpret_cast<const uint4*>(d + 512);
+                    c0 = *reinterpret_cast<const uint4*>(d + 1024);
+                    c1 = *reinterpret_cast<const uint4*>(d + 1536);
+                } else {
+                    a0 = rw[u][0];
+                    a1 = rw[u][1];
+                    c0 = rw[u][2];
+                    c1 = rw[u][3];
+                }
                 const uint32_t s0 = rs[u][0], s1 = rs[u][1];
                 const uint32_t zb = (FMT == FMT_AWQ) ? rz[u] : 0u;
-                if (j0 + u + U < total) load(u);
+                if (!ASYNC && j0 + u + U < total) load(u);
                 if (FMT == FMT_BF16) {
                     const uint4 x0 = xp[0], x1 = xp[1];
                     mma_bf16_16816(acc, a0.x, c0.x, a0.y, c0.y, x0.x, x0.y);
@@ -555,6 +583,10 @@ __global__ void __launch_bounds__(W * 32)
                         acc[2] = fmaf(f1.x, d0[2] + d1[2], acc[2]);
                         acc[2] = fmaf(f1.y, d0[3] + d1[3], acc[2]);
                     }
+                }
+                if (ASYNC) {
+                    if (j0 + u + U < total) load(u);
+                    cp_async_commit();
                 }
                 xp += xstep;
                 if (++cb == nb) {
@@ -641,7 +673,7 @@ struct MmaEntry {
     MmaFn fn;
 };
 #define MBW_M(F, W, U) \
-    { {W, U}, gemv_mma_kernel<F, W, U> }
+    { {W, U, 0}, gemv_mma_kernel<F, W, U> }
 
 static const MmaEntry kMmaBf16[] = {
     MBW_M(FMT_BF16, 4, 4), MBW_M(FMT_BF16, 4, 8), MBW_M(FMT_BF16, 8, 4), MBW_M(FMT_BF16, 8, 8),
@@ -654,12 +686,15 @@ static const MmaEntry kMmaAwq[] = {
 };
 #undef MBW_M
 
-#define MBW_M2(F, W, U) \
-    { {W, U}, gemv_mma2_kernel<F, W, U> }
-static const MmaEntry kMma2Bf16[] = {MBW_M2(FMT_BF16, 8, 2), MBW_M2(FMT_BF16, 8, 4), MBW_M2(FMT_BF16, 4, 4)};
-static const MmaEntry kMma2G64[] = {MBW_M2(FMT_G64, 8, 2), MBW_M2(FMT_G64, 8, 3), MBW_M2(FMT_G64, 4, 2),
-                                    MBW_M2(FMT_G64, 4, 3)};
-static const MmaEntry kMma2Awq[] = {MBW_M2(FMT_AWQ, 8, 2), MBW_M2(FMT_AWQ, 8, 3), MBW_M2(FMT_AWQ, 4, 2)};
+#define MBW_M2(F, W, U, A) \
+    { {W, U, A}, gemv_mma2_kernel<F, W, U, A> }
+static const MmaEntry kMma2Bf16[] = {MBW_M2(FMT_BF16, 8, 2, 0), MBW_M2(FMT_BF16, 8, 4, 0), MBW_M2(FMT_BF16, 4, 4, 0),
+                                     MBW_M2(FMT_BF16, 8, 4, 1), MBW_M2(FMT_BF16, 8, 6, 1)};
+static const MmaEntry kMma2G64[] = {MBW_M2(FMT_G64, 8, 2, 0), MBW_M2(FMT_G64, 8, 3, 0), MBW_M2(FMT_G64, 4, 2, 0),
+                                    MBW_M2(FMT_G64, 4, 3, 0), MBW_M2(FMT_G64, 8, 4, 1), MBW_M2(FMT_G64, 8, 6, 1),
+                                    MBW_M2(FMT_G64, 4, 6, 1)};
+static const MmaEntry kMma2Awq[] = {MBW_M2(FMT_AWQ, 8, 2, 0), MBW_M2(FMT_AWQ, 8, 3, 0), MBW_M2(FMT_AWQ, 4, 2, 0),
+                                    MBW_M2(FMT_AWQ, 8, 4, 1), MBW_M2(FMT_AWQ, 8, 6, 1)};
 #undef MBW_M2
 
 static const MmaEntry* mma2_table(int fmt, int* n) {
@@ -692,7 +727,9 @@ int mma2_block_k(int fmt) { return fmt == FMT_BF16 ? 64 : 256; }
 
 size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
     const int G = mma_row_groups(N, split, occ);
-    return mma_smem_layout(mma2_block_k(fmt), K, (int)N, M, c.warps, split, G).total;
+    const size_t base = mma_smem_layout(mma2_block_k(fmt), K, (int)N, M, c.warps, split, G).total;
+    if (!c.async) return base;
+    return (base + 127) / 128 * 128 + (size_t)c.warps * c.u * 4 * 512;
 }
 
 cudaError_t launch_gemv_mma2(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {

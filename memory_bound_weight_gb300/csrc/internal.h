@@ -39,7 +39,8 @@ struct SimtConfig {
 // One instantiation of the tensor-core (mma.sync) streaming kernel.
 struct MmaConfig {
     int warps;  // warps per CTA; each owns one k-slice of every tile of the CTA
-    int u;      // 64-byte row blocks per lane in flight (register ring depth)
+    int u;      // row blocks per lane in flight (ring depth)
+    int async;  // 1: the ring lives in shared memory, filled with cp.async
 };
 
 // One instantiation of the bulk-copy-fed tensor-core streaming kernel.

@@ -195,8 +195,8 @@ std::string plan_to_string(int op, const Plan& p) {
     char buf[192];
     if (p.kind == PLAN_MMA2) {
         const MmaConfig c = mma2_config(fmt, p.cfg);
-        snprintf(buf, sizeof(buf), "mma2 fmt=%s warps=%d superblocks_in_flight=%d ctas_per_sm=%d split_k=%d", fs,
-                 c.warps, c.u, p.occ, p.split);
+        snprintf(buf, sizeof(buf), "mma2 fmt=%s warps=%d superblocks_in_flight=%d ring=%s ctas_per_sm=%d split_k=%d",
+                 fs, c.warps, c.u, c.async ? "cp.async" : "registers", p.occ, p.split);
     } else if (p.kind == PLAN_TMA) {
         const TmaConfig c = tma_config(fmt, p.cfg);
         snprintf(buf, sizeof(buf), "tma fmt=%s consumer_warps=%d ring_stages=%d ctas_per_sm=%d split_k=%d", fs,
