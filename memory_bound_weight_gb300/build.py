@@ -25,7 +25,7 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-
                      "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 
 # translation units of libmbw.so (the product) and of the input generator
-LIB_SOURCES = ["abi.cu", "plan.cu", "gemv_simt.cu", "gemv_mma.cu", "gemv_tma.cu"]
+LIB_SOURCES = ["abi.cu", "plan.cu", "gemv_simt.cu", "gemv_mma.cu", "gemv_tma.cu", "gemm_tc.cu"]
 GEN_SOURCES = ["gen_inputs.cu"]
 
 
@@ -66,7 +66,7 @@ def _link(objs: list[str], out: str) -> None:
     if not _stale(out, objs):
         return
     tmp = out + ".tmp"
-    cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcuda"]
+    cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -193,8 +193,9 @@ mbw_status mbw_check_device_error(void) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
     const int f = tma_take_fault();
-    if (f < 0) return cuda_fail(cudaGetLastError(), "reading the device fault flag");
-    if (f) return fail(MBW_ERR_DEVICE_TIMEOUT, "a bounded wait inside a kernel expired");
+    const int f2 = tc_take_fault();
+    if (f < 0 || f2 < 0) return cuda_fail(cudaGetLastError(), "reading the device fault flag");
+    if (f || f2) return fail(MBW_ERR_DEVICE_TIMEOUT, "a bounded wait inside a kernel expired");
     return MBW_OK;
 }
 

@@ -56,7 +56,7 @@ struct Plan {
     int split;  // CTAs per cluster along K (1 = no split)
     int occ;    // MMA kernels: CTAs per SM in the persistent grid (1 for SIMT)
 };
-enum PlanKind : int { PLAN_SIMT = 0, PLAN_MMA = 1, PLAN_TMA = 2, PLAN_MMA2 = 3 };
+enum PlanKind : int { PLAN_SIMT = 0, PLAN_MMA = 1, PLAN_TMA = 2, PLAN_MMA2 = 3, PLAN_TC = 4 };
 
 // Kernel tables (gemv_simt.cu).
 int simt_num_configs(int fmt);
@@ -79,6 +79,12 @@ int mma2_max_batch(int fmt);
 int mma2_block_k(int fmt);
 size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ);
 cudaError_t launch_gemv_mma2(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
+
+// tcgen05 skinny GEMM (gemm_tc.cu): Y = X . W^T for the whole batch M.
+cudaError_t launch_gemm_tc(const uint16_t* X, const uint16_t* W, void* Y, int64_t M, int64_t N, int64_t K, int split,
+                           int out_f32, cudaStream_t s);
+int tc_batch_tile(int64_t M);
+int tc_take_fault();
 
 // Bulk-copy-fed kernel tables (gemv_tma.cu).
 int tma_num_configs(int fmt);

@@ -50,7 +50,13 @@ static size_t simt_smem(int fmt, const SimtConfig& c, int64_t K, int split) {
 // SIMT batch width for a call of M rows: the smallest kernel batch >= min(M, 8).
 static int simt_want_mb(int64_t M) { return M <= 2 ? (int)M : M <= 4 ? 4 : 8; }
 
+static int batch_key(int op, int64_t M) {
+    if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 8) return tc_batch_tile(M);
+    return (int)std::min<int64_t>(M, 8);
+}
+
 int plan_batch_width(int fmt, const Plan& p) {
+    if (p.kind == PLAN_TC) return 1 << 30;  // one launch covers the whole batch
     if (p.kind == PLAN_MMA2) return mma2_max_batch(fmt);
     if (p.kind == PLAN_MMA || p.kind == PLAN_TMA) return mma_max_batch(fmt);
     return simt_config(fmt, p.cfg).mb;
@@ -64,6 +70,14 @@ static int64_t kblocks(int fmt, int64_t K) {
 static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K) {
     (void)N;
     if (p.split < 1 || p.split > 8) return false;
+    if (p.kind == PLAN_TC) {
+        // tensor-core skinny GEMM: BF16, batches above the GEMV column width
+        const int64_t KS = (K + 63) / 64;
+        if (fmt != FMT_BF16 || M <= 8 || p.cfg != 0 || p.occ != 1) return false;
+        if (p.split > KS) return false;
+        const int64_t per = (KS + p.split - 1) / p.split;
+        return per * (p.split - 1) < KS;  // every cluster rank gets k-stages
+    }
     if (p.kind == PLAN_SIMT) {
         if (p.cfg < 0 || p.cfg >= simt_num_configs(fmt) || p.occ != 1) return false;
         const SimtConfig c = simt_config(fmt, p.cfg);
@@ -112,6 +126,11 @@ static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
     std::vector<Plan> out;
     const int fmt = fmt_of_op(op);
     const int64_t Mb = std::min<int64_t>(M, 8);
+    if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 8)
+        for (int sp = 1; sp <= 8; ++sp) {
+            Plan p{PLAN_TC, 0, sp, 1};
+            if (plan_valid(fmt, p, M, N, K)) out.push_back(p);
+        }
     const int splits[4] = {1, 2, 4, 8};
     for (int cfg = 0; cfg < mma_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si)
@@ -143,6 +162,16 @@ Plan plan_default(int op, int64_t M, int64_t N, int64_t K) {
     const int fmt = fmt_of_op(op);
     const int64_t Mb = std::min<int64_t>(M, 8);
     const int sms = device_sm_count();
+    if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 8) {
+        // tcgen05 tiles of 128 weight rows; split K over a cluster until the
+        // tiles cover the SMs
+        const int64_t tiles = (N + 127) / 128;
+        int split = 1;
+        while (split < 8 && tiles * (split + 1) <= sms) ++split;
+        Plan p{PLAN_TC, 0, split, 1};
+        while (!plan_valid(fmt, p, M, N, K) && p.split > 1) --p.split;
+        return p;
+    }
     // Tensor-core family: 8 warps, 4 blocks in flight, one CTA per SM; split K
     // over a cluster while there are fewer 16-row tiles than SMs.
     int cfg = 0;
@@ -172,7 +201,7 @@ static int current_device() {
 }
 
 static std::tuple<int, int, int64_t, int64_t, int64_t> key_of(int op, int64_t M, int64_t N, int64_t K) {
-    return std::make_tuple(current_device(), op, std::min<int64_t>(M, 8), N, K);
+    return std::make_tuple(current_device(), op, (int64_t)batch_key(op, M), N, K);
 }
 
 Plan plan_lookup(int op, int64_t M, int64_t N, int64_t K, cudaStream_t s) {
@@ -193,7 +222,9 @@ std::string plan_to_string(int op, const Plan& p) {
     const int fmt = fmt_of_op(op);
     const char* fs = fmt == FMT_BF16 ? "bf16" : fmt == FMT_G64 ? "int4_g64" : "int4_awq_g128";
     char buf[192];
-    if (p.kind == PLAN_MMA2) {
+    if (p.kind == PLAN_TC) {
+        snprintf(buf, sizeof(buf), "tcgen05 fmt=%s tile=128xbatch k_stage=64 split_k=%d", fs, p.split);
+    } else if (p.kind == PLAN_MMA2) {
         const MmaConfig c = mma2_config(fmt, p.cfg);
         snprintf(buf, sizeof(buf), "mma2 fmt=%s warps=%d superblocks_in_flight=%d ring=%s ctas_per_sm=%d split_k=%d",
                  fs, c.warps, c.u, c.async ? "cp.async" : "registers", p.occ, p.split);
@@ -214,6 +245,7 @@ std::string plan_to_string(int op, const Plan& p) {
 }
 
 cudaError_t launch_plan(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
+    if (p.kind == PLAN_TC) return launch_gemm_tc(a.x, (const uint16_t*)a.W, a.y, a.M, a.N, a.K, p.split, a.out_f32, s);
     if (p.kind == PLAN_MMA2) return launch_gemv_mma2(fmt, p, a, s);
     if (p.kind == PLAN_TMA) return launch_gemv_tma(fmt, p, a, s);
     if (p.kind == PLAN_MMA) return launch_gemv_mma(fmt, p, a, s);
@@ -303,7 +335,7 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
         return MBW_ERR_CUDA;
     }
     const int fmt = fmt_of_op(op);
-    const int64_t Mb = std::min<int64_t>(M, 8);
+    const int64_t Mb = (op == MBW_OP_GEMM_SKINNY_BF16) ? M : std::min<int64_t>(M, 8);
     const size_t wb = weight_bytes(fmt, N, K);
     const size_t wstride = (wb + 255) / 256 * 256;
     const size_t target = (size_t)384 << 20;  // about three times the L2
@@ -330,7 +362,7 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
         GemvArgs a{};
         a.N = (int)N;
         a.K = (int)K;
-        a.M = (int)std::min<int64_t>(Mb, plan_batch_width(fmt, p));
+        a.M = (int)std::min<int64_t>(Mb, (int64_t)plan_batch_width(fmt, p));
         a.x = xbuf;
         a.y = ybuf;
         a.chunks = chunks_of(fmt, K);

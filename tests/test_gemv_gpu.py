@@ -256,3 +256,46 @@ def test_qwen_shapes_sampled_rows(orc, N, K):
         Yd = mbw.gemv_int4_awq_g128(cd, sd, zd, Xd)
         Y, A = orc.gemm_int4_awq_g128(cr, sr, zr, host_bits16(Xd))
         assert_parity(Yd[:, torch.from_numpy(rows).cuda()], Y, A, f"awq M={M} {N}x{K} sampled")
+
+
+# -------------------------------------------------- tensor-core skinny GEMM ----
+@pytest.mark.parametrize("M,N,K", [(16, 128, 64), (16, 300, 256), (32, 257, 512), (48, 128, 1032), (64, 640, 3584),
+                                   (100, 200, 192), (128, 130, 128), (256, 384, 1024), (300, 129, 256)])
+def test_skinny_tcgen05_all_plans(orc, M, N, K):
+    W, X = bf16_case(900 + M, N, K, M)
+    Y, A = orc.gemm_bf16(W, X)
+    Wd, Xd = dev_bf16(W), dev_bf16(X)
+    seen_tc = False
+    for i, desc in each_plan(mbw.OP_GEMM_SKINNY_BF16, M, N, K):
+        seen_tc |= desc.startswith("tcgen05")
+        y = mbw.gemm_skinny_bf16(Xd, Wd)
+        assert_parity(y, Y, A, f"skinny {M}x{N}x{K} plan {desc}")
+    assert seen_tc
+
+
+def test_skinny_tcgen05_deterministic_and_scaling():
+    M, N, K = 64, 1024, 2048
+    W, X = bf16_case(950, N, K, M)
+    Wd, Xd = dev_bf16(W), dev_bf16(X)
+    with mbw.output_fp32():
+        y1 = mbw.gemm_skinny_bf16(Xd, Wd)
+        y2 = mbw.gemm_skinny_bf16(Xd, Wd)
+        y4 = mbw.gemm_skinny_bf16((Xd.float() * 4).to(torch.bfloat16), Wd)
+    assert torch.equal(y1, y2)
+    assert torch.equal(y4, y1 * 4)
+    assert mbw.plan_describe(mbw.OP_GEMM_SKINNY_BF16, M, N, K).startswith("tcgen05")
+
+
+@pytest.mark.parametrize("M", [16, 64, 256])
+@pytest.mark.parametrize("N,K", [(18944, 3584), (3584, 18944)])
+def test_skinny_config_shapes_sampled_rows(orc, M, N, K):
+    """The Qwen2.5-7B MLP shapes at the skinny batch sizes, default plan, every
+    batch row of 96 sampled weight rows against the oracle."""
+    rows = np.unique(np.concatenate([np.arange(0, 8), np.arange(N - 8, N),
+                                     np.random.default_rng(N + M).integers(0, N, 80)]))
+    Wd = inputs_gpu.bf16_weights(0, 7, N, K)
+    Xd = inputs_gpu.bf16_activations(0, 8, M, K)
+    Y = mbw.gemm_skinny_bf16(Xd, Wd)
+    Wr = np.stack([gen.bf16_weights(0, 7, N, K, row0=int(r), rows=1)[0] for r in rows])
+    Yr, Ar = orc.gemm_bf16(Wr, host_bits16(Xd))
+    assert_parity(Y[:, torch.from_numpy(rows).cuda()], Yr, Ar, f"skinny M={M} {N}x{K} sampled")
