@@ -81,6 +81,23 @@ __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Bring [base, base + bytes) into L2, the whole grid sharing the work (one
+// prefetch per 128-byte line, at most a few per thread). Issued before
+// pdl_wait() for the activations: L2 is the device's point of coherence, so
+// if the previous grid is still writing those bytes its stores update the
+// lines this brings in, and the reads after the wait hit L2 instead of DRAM.
+__device__ __forceinline__ void prefetch_l2_grid_share(const void* base, size_t bytes) {
+    const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+    const uintptr_t a0 = b & ~uintptr_t(127);
+    const size_t lines = (b + bytes - a0 + 127) / 128;
+    const size_t nthr = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < lines; i += nthr) {
+        uintptr_t p = a0 + i * 128;
+        if (p < b) p = b;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+    }
+}
+
 // ------------------------------------------------------------- formats ----
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

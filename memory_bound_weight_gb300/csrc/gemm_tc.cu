@@ -43,6 +43,8 @@ struct TcArgs {
     int m0;        // first batch row of this launch
     int kstages;   // 64-k stages per cluster rank
     int out_f32;
+    const void* xpf;   // the launch's X rows, prefetched into L2 before the wait
+    size_t xpf_bytes;
 };
 
 __device__ __forceinline__ uint32_t tc_smem(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -104,6 +106,7 @@ __global__ void __launch_bounds__(192, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     pdl_launch_dependents();
+    prefetch_l2_grid_share(a.xpf, a.xpf_bytes);
 
     const int rank = (S > 1) ? (int)cg::this_cluster().block_rank() : 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -139,27 +142,30 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer ----
         if (lane == 0) {
-            // W tiles do not depend on the previous kernel; X may: wait before
-            // the first X load only.
-            bool ok = true;
-            bool waited = false;
-            for (int i = 0; i < nks && ok; ++i) {
+            // W tiles do not depend on the previous kernel: fill the whole
+            // ring with them first, then wait, then add the X tiles (X may be
+            // the previous kernel's output).
+            const int npre = min(D, nks);
+            for (int i = 0; i < npre; ++i) {
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc_smem(&full[i])),
+                             "r"(STAGE)
+                             : "memory");
+                tc_tma_2d(smem + (size_t)i * STAGE, &mapW, (ks0 + i) * 64, row0, &full[i]);
+            }
+            pdl_wait();
+            for (int i = 0; i < npre; ++i)
+                tc_tma_2d(smem + (size_t)i * STAGE + A_BYTES, &mapX, (ks0 + i) * 64, a.m0, &full[i]);
+            for (int i = npre; i < nks; ++i) {
                 const int s = i % D;
-                if (i >= D) ok = tc_wait(&empty[s], ((i / D) - 1) & 1);
-                if (!ok) break;
+                if (!tc_wait(&empty[s], ((i / D) - 1) & 1)) break;
                 uint8_t* st = smem + (size_t)s * STAGE;
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc_smem(&full[s])),
                              "r"(STAGE)
                              : "memory");
                 const int kc = (ks0 + i) * 64;
                 tc_tma_2d(st, &mapW, kc, row0, &full[s]);
-                if (!waited) {
-                    pdl_wait();
-                    waited = true;
-                }
                 tc_tma_2d(st + A_BYTES, &mapX, kc, a.m0, &full[s]);
             }
-            if (!waited) pdl_wait();
         }
     } else if (warp == 1) {
         // --------------------------------------------------- MMA issuer ----
@@ -293,9 +299,12 @@ int tc_batch_tile(int64_t M) {
     return 256;
 }
 
-static int tc_stages(int nt) {
+// Ring depth for a shared-memory budget: ring 0 = deep (one CTA per SM),
+// ring 1 = about 100 KB, so that the next launch's CTA fits beside this one
+// and streams its first W tiles while this one finishes.
+static int tc_stages(int nt, int ring) {
     const size_t stage = 128 * 128 + (size_t)nt * 128;
-    int d = (int)((180 * 1024) / stage);
+    int d = (int)(((ring == 0 ? 180 : 96) * 1024) / stage);
     if (d > 8) d = 8;
     if (d < 2) d = 2;
     return d;
@@ -310,9 +319,9 @@ size_t tc_smem_bytes(int nt, int D, int split) {
 }
 
 template <int NT>
-static cudaError_t launch_nt(const CUtensorMap& mw, const CUtensorMap& mx, const TcArgs& a, int split, int tiles,
-                             cudaStream_t s) {
-    const int D = tc_stages(NT);
+static cudaError_t launch_nt(const CUtensorMap& mw, const CUtensorMap& mx, const TcArgs& a, int split, int ring,
+                             int tiles, cudaStream_t s) {
+    const int D = tc_stages(NT, ring);
     const size_t smem = tc_smem_bytes(NT, D, split);
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -341,7 +350,7 @@ static cudaError_t launch_nt(const CUtensorMap& mw, const CUtensorMap& mx, const
 
 // Y[M][N] = X[M][K] . W[N][K]^T, bf16, in batch slices of up to 256 rows.
 cudaError_t launch_gemm_tc(const uint16_t* X, const uint16_t* W, void* Y, int64_t M, int64_t N, int64_t K, int split,
-                           int out_f32, cudaStream_t s) {
+                           int ring, int out_f32, cudaStream_t s) {
     const int nt = tc_batch_tile(M);
     CUtensorMap mw, mx;
     if (!encode_2d(&mw, W, (uint64_t)K, (uint64_t)N, 64, 128)) return cudaErrorInvalidValue;
@@ -359,13 +368,15 @@ cudaError_t launch_gemm_tc(const uint16_t* X, const uint16_t* W, void* Y, int64_
     a.out_f32 = out_f32;
     for (int64_t m0 = 0; m0 < M; m0 += 256) {
         a.m0 = (int)m0;
+        a.xpf = X + m0 * K;
+        a.xpf_bytes = (size_t)((M - m0 < 256) ? (M - m0) : 256) * (size_t)K * 2;
         cudaError_t e;
         switch (nt) {
-            case 16: e = launch_nt<16>(mw, mx, a, split, tiles, s); break;
-            case 32: e = launch_nt<32>(mw, mx, a, split, tiles, s); break;
-            case 64: e = launch_nt<64>(mw, mx, a, split, tiles, s); break;
-            case 128: e = launch_nt<128>(mw, mx, a, split, tiles, s); break;
-            default: e = launch_nt<256>(mw, mx, a, split, tiles, s); break;
+            case 16: e = launch_nt<16>(mw, mx, a, split, ring, tiles, s); break;
+            case 32: e = launch_nt<32>(mw, mx, a, split, ring, tiles, s); break;
+            case 64: e = launch_nt<64>(mw, mx, a, split, ring, tiles, s); break;
+            case 128: e = launch_nt<128>(mw, mx, a, split, ring, tiles, s); break;
+            default: e = launch_nt<256>(mw, mx, a, split, ring, tiles, s); break;
         }
         if (e != cudaSuccess) return e;
     }

@@ -1,0 +1,465 @@
+// gemv_lat.cu -- latency-oriented GEMV for the small matrices of a decode
+// chain (batch 1..8), INT4 group-64 and BF16.
+//
+// In a decode step every GEMV waits for the one before it (its x is the
+// previous kernel's output), so a small matrix costs the chain's release
+// latency plus everything its kernel does AFTER griddepcontrol.wait, not
+// its bytes over the HBM rate. Measured on GB300 with per-CTA timestamps, a
+// streaming kernel spent ~0.6 us staging x through shared memory, ~1 us in
+// its unpack/MMA loop and ~0.5 us in a two-barrier reduction after the wait,
+// for a 2 MB matrix whose weights had arrived long before. This family moves
+// all of that off the dependent path it can:
+//   * every weight item a warp owns (16 rows x one 128-byte row super-block,
+//     as in the "mma2" layout: 32 bytes of rows g and g+8 per lane) is loaded
+//     into registers before the wait, so the next launch streams its whole
+//     share while the previous one finishes;
+//   * the first NPRE items are also unpacked to bf16 MMA fragments before the
+//     wait (INT4), the rest right after it while the x loads are in flight;
+//   * x is read straight into the B-fragment registers of the lanes that
+//     carry it (no shared-memory staging, no barrier);
+//   * one __syncthreads, then each output sums its warps' partials in a fixed
+//     order and stores (cluster ranks add theirs through distributed shared
+//     memory when K is split over a cluster).
+// The number of items a warp may own is a template constant (NI): plans
+// whose shape needs more are not offered, and the streaming families take
+// those shapes.
+//
+// Arithmetic is that of the mma2 family: codes become exact bf16 (128 + n) -
+// (128 + 8) pairs, products with bf16 x are exact, the tensor core
+// accumulates in fp32 and the group scale multiplies each group's fp32
+// partial. BF16 weights go to the tensor core unchanged.
+#include <cooperative_groups.h>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace mbw {
+
+namespace {
+
+__device__ __forceinline__ void lat_mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// the nibbles at bits 0-3 and 16-19 of v as the bf16 pair (128 + n_lo, 128 + n_hi)
+__device__ __forceinline__ uint32_t lat_nib(uint32_t v) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(0x000F000Fu), "r"(0x43004300u));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t lat_sub(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// 8 bf16 x[8w..8w+7] -> pairs (0,4) (1,5) (2,6) (3,7), the order in which the
+// INT4 fragments pair their nibbles.
+__device__ __forceinline__ uint4 lat_perm(uint4 v) {
+    uint4 o;
+    o.x = __byte_perm(v.x, v.z, 0x5410);
+    o.y = __byte_perm(v.x, v.z, 0x7632);
+    o.z = __byte_perm(v.y, v.w, 0x5410);
+    o.w = __byte_perm(v.y, v.w, 0x7632);
+    return o;
+}
+
+// INT4 fragments of one item for one lane: word w of rows g (wa) and g+8 (wb)
+// -> the A registers of the two MMAs of word w, (q - 8) exact in bf16.
+__device__ __forceinline__ void lat_unpack(const u32x8& ra, const u32x8& rb, uint32_t (&A)[8][8]) {
+    const uint32_t z = 0x43084308u;  // (128 + 8, 128 + 8)
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint32_t wa = ra.v[w], wb = rb.v[w];
+        A[w][0] = lat_sub(lat_nib(wa), z);
+        A[w][1] = lat_sub(lat_nib(wb), z);
+        A[w][2] = lat_sub(lat_nib(wa >> 4), z);
+        A[w][3] = lat_sub(lat_nib(wb >> 4), z);
+        A[w][4] = lat_sub(lat_nib(wa >> 8), z);
+        A[w][5] = lat_sub(lat_nib(wb >> 8), z);
+        A[w][6] = lat_sub(lat_nib(wa >> 12), z);
+        A[w][7] = lat_sub(lat_nib(wb >> 12), z);
+    }
+}
+
+}  // namespace
+
+// Shared memory: per-warp partials [ntmax][W][16][M], per-CTA sums
+// [ntmax][16][M] (read by the other ranks of a split-K cluster), then one
+// x slot per warp: 72 words (64 + 8 pad words of 16 bytes) per super-block
+// the warp may own.
+__host__ __device__ inline size_t lat_red_floats(int ntmax, int W, int M) {
+    return ((size_t)ntmax * (W + 1) * 16 * M + 3) / 4 * 4;  // 16-byte aligned end
+}
+__host__ __device__ inline size_t lat_smem_floats(int ntmax, int W, int M, int NI) {
+    return lat_red_floats(ntmax, W, M) + (size_t)W * 72 * 4 * NI;
+}
+
+template <int FMT, int W, int NI, int NPRE>
+__global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
+    gemv_lat_kernel(const GemvArgs a, const int S) {
+    static_assert(FMT == FMT_G64 || FMT == FMT_BF16, "INT4 group-64 and BF16 only");
+    static_assert(FMT == FMT_G64 || NPRE == 0, "BF16 needs no unpack");
+    static_assert(NPRE <= NI, "");
+    constexpr int BK = (FMT == FMT_BF16) ? 64 : 256;  // k per 128-byte row super-block
+    extern __shared__ float lat_smem[];
+
+    pdl_launch_dependents();
+
+    const int rank = (S > 1) ? (int)cg::this_cluster().block_rank() : 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int G = gridDim.x / S;
+    const int cgid = blockIdx.x / S;
+    const int T = (a.N + 15) / 16;
+    const int t0 = (int)(((long long)T * cgid) / G);
+    const int nt = (int)(((long long)T * (cgid + 1)) / G) - t0;
+    const int ntmax = (T + G - 1) / G;
+    const int mb = a.M;
+    const int KB = a.K / BK;  // the plan guarantees K % BK == 0
+    const int BS = (KB + S * W - 1) / (S * W);
+    const int b0 = rank * W * BS + warp * BS;  // this warp's k-slice of super-blocks
+    const int nb = max(0, min(KB, b0 + BS) - b0);
+    const int total = nt * nb;  // items of this warp; the plan guarantees total <= NI
+    const size_t rowbytes = (FMT == FMT_BF16) ? (size_t)a.K * 2 : (size_t)a.K / 2;
+
+    // ---------------------------------------------- before the wait ----
+    u32x8 ra[NI], rb[NI];  // 32 bytes of rows g and g+8 per item
+    uint32_t rs[NI][2];    // group-64: the 2 fp16 scales of this lane's columns, rows g and g+8
+#pragma unroll
+    for (int j = 0; j < NI; ++j) {
+        if (j < total) {
+            const int t = j / nb;
+            const int b = b0 + (j - t * nb);
+            const int r0 = min((t0 + t) * 16 + g, a.N - 1);
+            const int r1 = min((t0 + t) * 16 + g + 8, a.N - 1);
+            ra[j] = ld_stream32(a.W + (size_t)r0 * rowbytes + (size_t)b * 128 + q * 32);
+            rb[j] = ld_stream32(a.W + (size_t)r1 * rowbytes + (size_t)b * 128 + q * 32);
+            if (FMT == FMT_G64) {
+                const uint16_t* s0 = a.scales + (size_t)r0 * a.groups + (size_t)b * 4 + 2 * (q & 1);
+                const uint16_t* s1 = a.scales + (size_t)r1 * a.groups + (size_t)b * 4 + 2 * (q & 1);
+                rs[j][0] = (uint32_t)ld_ro_u16(s0) | ((uint32_t)ld_ro_u16(s0 + 1) << 16);
+                rs[j][1] = (uint32_t)ld_ro_u16(s1) | ((uint32_t)ld_ro_u16(s1 + 1) << 16);
+            }
+        }
+    }
+    uint32_t A[NPRE > 0 ? NPRE : 1][8][8];
+#pragma unroll
+    for (int j = 0; j < NPRE; ++j)
+        if (j < total) lat_unpack(ra[j], rb[j], A[j]);
+
+    // addresses of the x words this lane will read after the wait (word i of
+    // the warp's x: super-block i / (M * words per row), batch row, word)
+    constexpr int XLD = 2 * NI;  // most x loads per lane (M * words per row <= 64 per super-block)
+    const uint16_t* xsrc[XLD];
+    {
+        constexpr int XWSB0 = BK / 8;
+        const int sbw0 = mb * XWSB0;
+#pragma unroll
+        for (int r = 0; r < XLD; ++r) {
+            const int wi = lane + 32 * r;
+            xsrc[r] = nullptr;
+            if (wi < nb * sbw0) {
+                const int sb = wi / sbw0, rem = wi - sb * sbw0;
+                const int m = rem / XWSB0, w = rem - m * XWSB0;
+                xsrc[r] = a.x + (size_t)m * a.K + (size_t)(b0 + sb) * BK + w * 8;
+            }
+        }
+    }
+    prefetch_l2_grid_share(a.x, (size_t)a.M * a.K * 2);
+    // x is produced by the previous kernel in the stream: wait for it only now.
+    pdl_wait();
+
+    // ----------------------------------------------- after the wait ----
+    // B fragment of this lane: column n = g.
+    //   group-64: n = 4m + j carries batch m, group j of the super-block; lane
+    //             (g, q) supplies it only when j == q (x words 8q .. 8q+7);
+    //   BF16:     n = m; x words 2q, 2q+1 of the super-block.
+    int xm;
+    bool xon;
+    if (FMT == FMT_G64) {
+        xm = g >> 2;
+        xon = (xm < mb) && ((g & 3) == q);
+    } else {
+        xm = g;
+        xon = xm < mb;
+    }
+    constexpr int XWL = (FMT == FMT_G64) ? 8 : 2;  // x words per B-fragment lane per super-block
+    constexpr int XWSB = BK / 8;                     // 16-byte x words per batch row per super-block
+    // Right after the wait the warp reads all the x it needs -- its nb
+    // super-blocks for every batch row, word i at lane i % 32 -- in one round
+    // of 16-byte loads, and hands each B-fragment lane its words through a
+    // per-warp shared-memory slot (one pad word per 8 keeps those reads
+    // conflict-free). Loading per item, or a lane issuing eight loads itself,
+    // or eight rounds of shuffles, each cost more latency.
+    const int sbw = mb * XWSB;  // words per super-block
+    const int nxw = nb * sbw;   // words this warp reads
+    uint4* xslot = reinterpret_cast<uint4*>(lat_smem + lat_red_floats(ntmax, W, mb)) + (size_t)warp * (72 * NI);
+    {
+        uint4 v[XLD];
+#pragma unroll
+        for (int r = 0; r < XLD; ++r) {
+            v[r] = make_uint4(0, 0, 0, 0);
+            if (xsrc[r] != nullptr) v[r] = ld_ro16(xsrc[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < XLD; ++r) {
+            const int wi = lane + 32 * r;
+            if (wi < nxw) xslot[wi + (wi >> 3)] = (FMT == FMT_G64) ? lat_perm(v[r]) : v[r];
+        }
+    }
+    __syncwarp();
+    uint4 xv[XWL];
+    auto load_x = [&](int sb) {
+#pragma unroll
+        for (int w = 0; w < XWL; ++w) {
+            const int wi = sb * sbw + ((FMT == FMT_G64) ? (min(xm, 1) * 32 + 8 * q + w) : (g * 8 + 2 * q + w));
+            xv[w] = xon ? xslot[wi + (wi >> 3)] : make_uint4(0, 0, 0, 0);
+        }
+    };
+    if (total > 0) load_x(0);
+
+    float* red = lat_smem;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc2[4] = {0.f, 0.f, 0.f, 0.f};  // BF16: second MMA chain
+#pragma unroll
+    for (int j = 0; j < NI; ++j) {
+        if (j < total) {
+            const int t = j / nb;
+            const int bi = j - t * nb;
+            if (j > 0 && nb > 1) load_x(bi);
+            if (FMT == FMT_G64) {
+                uint32_t Aj[8][8];
+                if (j < NPRE) {
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) Aj[w][i] = A[j < NPRE ? j : 0][w][i];
+                } else {
+                    lat_unpack(ra[j], rb[j], Aj);
+                }
+                // four independent accumulator chains of four MMAs each
+                float d[4][4] = {};
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    lat_mma(d[(w & 1) * 2], Aj[w][0], Aj[w][1], Aj[w][2], Aj[w][3], xv[w].x, xv[w].y);
+                    lat_mma(d[(w & 1) * 2 + 1], Aj[w][4], Aj[w][5], Aj[w][6], Aj[w][7], xv[w].z, xv[w].w);
+                }
+                float ds[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) ds[i] = (d[0][i] + d[1][i]) + (d[2][i] + d[3][i]);
+                // columns 2q, 2q+1 = groups 2(q&1), 2(q&1)+1 of batch q>>1
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&rs[j][0]));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&rs[j][1]));
+                acc[0] = fmaf(f0.x, ds[0], acc[0]);
+                acc[0] = fmaf(f0.y, ds[1], acc[0]);
+                acc[2] = fmaf(f1.x, ds[2], acc[2]);
+                acc[2] = fmaf(f1.y, ds[3], acc[2]);
+            } else {
+                const u32x8& wa = ra[j];
+                const u32x8& wb = rb[j];
+                lat_mma(acc, wa.v[0], wb.v[0], wa.v[1], wb.v[1], xv[0].x, xv[0].y);
+                lat_mma(acc2, wa.v[2], wb.v[2], wa.v[3], wb.v[3], xv[0].z, xv[0].w);
+                lat_mma(acc, wa.v[4], wb.v[4], wa.v[5], wb.v[5], xv[1].x, xv[1].y);
+                lat_mma(acc2, wa.v[6], wb.v[6], wa.v[7], wb.v[7], xv[1].z, xv[1].w);
+            }
+            if (bi == nb - 1) {
+                // end of this warp's k-slice of tile t: per-warp partials
+                float* rp = red + ((size_t)(t * W + warp) * 16) * mb;
+                if (FMT == FMT_G64) {
+                    const float v0 = acc[0] + __shfl_xor_sync(0xFFFFFFFFu, acc[0], 1);
+                    const float v2 = acc[2] + __shfl_xor_sync(0xFFFFFFFFu, acc[2], 1);
+                    const int m = q >> 1;
+                    if ((q & 1) == 0 && m < mb) {
+                        rp[g * mb + m] = v0;
+                        rp[(g + 8) * mb + m] = v2;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
+                    if (2 * q < mb) {
+                        rp[g * mb + 2 * q] = acc[0];
+                        rp[(g + 8) * mb + 2 * q] = acc[2];
+                    }
+                    if (2 * q + 1 < mb) {
+                        rp[g * mb + 2 * q + 1] = acc[1];
+                        rp[(g + 8) * mb + 2 * q + 1] = acc[3];
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i] = acc2[i] = 0.f;
+            }
+        }
+    }
+    if (nb == 0) {
+        // an empty k-slice still contributes zeros for every tile
+        for (int t = 0; t < nt; ++t) {
+            float* rp = red + ((size_t)(t * W + warp) * 16) * mb;
+            for (int i = lane; i < 16 * mb; i += 32) rp[i] = 0.f;
+        }
+    }
+    __syncthreads();
+
+    // each output: the sum over warps in warp order
+    const int nout = nt * 16 * mb;
+    const int row0 = t0 * 16;
+    if (S == 1) {
+        if (mb == 1) {
+            for (int i = threadIdx.x; i < nout; i += W * 32) {
+                const float* rp = red + (i >> 4) * (W * 16) + (i & 15);
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < W; ++w) v += rp[w * 16];
+                if (row0 + i < a.N) store_out(a.y, row0 + i, v, a.out_f32);
+            }
+            return;
+        }
+        for (int i = threadIdx.x; i < nout; i += W * 32) {
+            const int t = i / (16 * mb);
+            const int rm = i - t * 16 * mb;
+            const int r = rm / mb;
+            const int m = rm - r * mb;
+            float v = 0.f;
+            const float* rp = red + (size_t)t * W * 16 * mb + rm;
+#pragma unroll
+            for (int w = 0; w < W; ++w) v += rp[(size_t)w * 16 * mb];
+            const int row = row0 + t * 16 + r;
+            if (row < a.N) store_out(a.y, (int64_t)m * a.N + row, v, a.out_f32);
+        }
+        return;
+    }
+    float* fin = red + (size_t)ntmax * W * 16 * mb;  // [tile*16 + row][m]
+    for (int i = threadIdx.x; i < nout; i += W * 32) {
+        const int t = i / (16 * mb);
+        const int rm = i - t * 16 * mb;
+        float v = 0.f;
+        const float* rp = red + (size_t)t * W * 16 * mb + rm;
+#pragma unroll
+        for (int w = 0; w < W; ++w) v += rp[(size_t)w * 16 * mb];
+        fin[i] = v;
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    // rank s writes rows [s * R / S, (s + 1) * R / S) of the CTA group's R rows
+    const int R = nt * 16;
+    const int lo = rank * R / S, hi = (rank + 1) * R / S;
+    const int span = hi - lo;
+    for (int i = threadIdx.x; i < span * mb; i += W * 32) {
+        const int lr = lo + i / mb;
+        const int m = i - (i / mb) * mb;
+        float v = 0.f;
+        for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(fin + lr * mb + m, s);
+        if (row0 + lr < a.N) store_out(a.y, (int64_t)m * a.N + row0 + lr, v, a.out_f32);
+    }
+    cluster.sync();
+}
+
+// ------------------------------------------------------------- tables ----
+namespace {
+using LatFn = void (*)(const GemvArgs, const int);
+struct LatEntry {
+    LatConfig cfg;
+    LatFn fn;
+};
+#define MBW_L(F, W, NI, NP) \
+    { {W, NI, NP}, gemv_lat_kernel<F, W, NI, NP> }
+const LatEntry kLatG64[] = {MBW_L(FMT_G64, 8, 1, 1), MBW_L(FMT_G64, 8, 1, 0), MBW_L(FMT_G64, 8, 2, 0),
+                            MBW_L(FMT_G64, 8, 3, 0), MBW_L(FMT_G64, 4, 1, 1)};
+const LatEntry kLatBf16[] = {MBW_L(FMT_BF16, 8, 2, 0), MBW_L(FMT_BF16, 8, 4, 0),
+                             MBW_L(FMT_BF16, 4, 4, 0), MBW_L(FMT_BF16, 16, 2, 0)};
+#undef MBW_L
+
+const LatEntry* lat_table(int fmt, int* n) {
+    if (fmt == FMT_G64) {
+        *n = (int)(sizeof(kLatG64) / sizeof(kLatG64[0]));
+        return kLatG64;
+    }
+    if (fmt == FMT_BF16) {
+        *n = (int)(sizeof(kLatBf16) / sizeof(kLatBf16[0]));
+        return kLatBf16;
+    }
+    *n = 0;
+    return nullptr;
+}
+}  // namespace
+
+int lat_num_configs(int fmt) {
+    int n;
+    lat_table(fmt, &n);
+    return n;
+}
+
+LatConfig lat_config(int fmt, int idx) {
+    int n;
+    return lat_table(fmt, &n)[idx].cfg;
+}
+
+int lat_max_batch(int fmt) { return fmt == FMT_G64 ? 2 : 8; }
+int lat_block_k(int fmt) { return fmt == FMT_BF16 ? 64 : 256; }
+
+// Most items any warp owns under this split (0 if the shape does not fit the family).
+int lat_items_per_warp(int fmt, const LatConfig& c, int64_t N, int64_t K, int split, int occ) {
+    const int BK = lat_block_k(fmt);
+    if (K % BK != 0) return 0;
+    const int64_t KB = K / BK;
+    const int64_t BS = (KB + (int64_t)split * c.warps - 1) / ((int64_t)split * c.warps);
+    if ((int64_t)(split - 1) * c.warps * BS >= KB) return 0;  // a cluster rank without k-range
+    const int G = mma_row_groups(N, split, occ);
+    const int64_t T = (N + 15) / 16;
+    const int64_t ntmax = (T + G - 1) / G;
+    return (int)(ntmax * BS);
+}
+
+size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int M, int split, int occ) {
+    (void)fmt;
+    const int G = mma_row_groups(N, split, occ);
+    const int64_t T = (N + 15) / 16;
+    const int ntmax = (int)((T + G - 1) / G);
+    return lat_smem_floats(ntmax, c.warps, M, c.ni) * sizeof(float);
+}
+
+cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
+    int n;
+    const LatEntry* t = lat_table(fmt, &n);
+    if (t == nullptr || p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > lat_max_batch(fmt)) return cudaErrorInvalidValue;
+    const LatEntry& e = t[p.cfg];
+    const int items = lat_items_per_warp(fmt, e.cfg, a.N, a.K, p.split, p.occ);
+    if (items < 1 || items > e.cfg.ni) return cudaErrorInvalidValue;
+    const int G = mma_row_groups(a.N, p.split, p.occ);
+    const size_t smem = lat_smem_bytes(fmt, e.cfg, a.N, a.M, p.split, p.occ);
+    if (smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(G * p.split), 1, 1);
+    cfg.blockDim = dim3((unsigned)(e.cfg.warps * 32), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (p.split > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)p.split;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    count_launch();
+    return cudaLaunchKernelEx(&cfg, e.fn, a, p.split);
+}
+
+}  // namespace mbw

@@ -122,7 +122,7 @@ __host__ __device__ inline MmaSmem mma_smem_layout(int BK, int64_t K, int N, int
 }
 
 template <int FMT, int W, int U>
-__global__ void __launch_bounds__(W * 32)
+__global__ void __launch_bounds__(W * 32, 16 / W)
     gemv_mma_kernel(const GemvArgs a, const int S) {
     constexpr int BK = MmaTraits<FMT>::BK;
     constexpr int XW = BK / 8;                      // 16-byte x words per row block
@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(W * 32)
         if (u < total) load(u);
 
     // x is produced by the previous kernel in the stream: wait for it only now.
+    prefetch_l2_grid_share(a.x, (size_t)a.M * a.K * 2);
     pdl_wait();
 
     // Stage x for the CTA's k-range: xs[m][w] = 16-byte word w (8 k) of batch
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(W * 32)
 //              lane (g,q) holds both groups of batch q.
 //   BF16     : column n = m (M <= 8); lane q's 16 weights feed 4 MMAs.
 template <int FMT, int W, int U, int ASYNC>
-__global__ void __launch_bounds__(W * 32)
+__global__ void __launch_bounds__(W * 32, 16 / W)
     gemv_mma2_kernel(const GemvArgs a, const int S) {
     constexpr int BK = (FMT == FMT_BF16) ? 64 : 256;  // k per 128-byte row super-block
     constexpr int XW = BK / 8;                        // 16-byte x words per super-block
@@ -478,6 +479,7 @@ __global__ void __launch_bounds__(W * 32)
         if (ASYNC) cp_async_commit();  // one group per step, empty past the end
     }
 
+    prefetch_l2_grid_share(a.x, (size_t)a.M * a.K * 2);
     pdl_wait();
 
     uint4* xs = smem_u4;

@@ -53,7 +53,7 @@ struct Traits<FMT_AWQ> {
 };
 
 template <int FMT, int WARPS, int R, int U, int MB>
-__global__ void __launch_bounds__(WARPS * 32)
+__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     gemv_simt_kernel(const GemvArgs a, const int S) {
     constexpr int CW = Traits<FMT>::CW;
     constexpr int PL = CW / 4;  // float4 planes per chunk
@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     if (iters > 0) load(cur, scur, zcur, 0);
 
     // x is produced by the previous kernel in the stream: wait for it only now.
+    prefetch_l2_grid_share(a.x, (size_t)a.M * a.K * 2);
     pdl_wait();
 
     // Stage this CTA's k-slice of x as fp32, plane-major:

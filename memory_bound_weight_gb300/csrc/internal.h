@@ -43,6 +43,14 @@ struct MmaConfig {
     int async;  // 1: the ring lives in shared memory, filled with cp.async
 };
 
+// One instantiation of the latency-oriented kernel (whole share in registers
+// before the wait).
+struct LatConfig {
+    int warps;  // warps per CTA; each owns one k-slice of every tile of the CTA
+    int ni;     // most items (16 rows x one 128-byte super-block) a warp may own
+    int npre;   // items unpacked to MMA fragments before the wait (INT4)
+};
+
 // One instantiation of the bulk-copy-fed tensor-core streaming kernel.
 struct TmaConfig {
     int warps;  // consumer warps per CTA (plus one producer warp)
@@ -56,7 +64,7 @@ struct Plan {
     int split;  // CTAs per cluster along K (1 = no split)
     int occ;    // MMA kernels: CTAs per SM in the persistent grid (1 for SIMT)
 };
-enum PlanKind : int { PLAN_SIMT = 0, PLAN_MMA = 1, PLAN_TMA = 2, PLAN_MMA2 = 3, PLAN_TC = 4 };
+enum PlanKind : int { PLAN_SIMT = 0, PLAN_MMA = 1, PLAN_TMA = 2, PLAN_MMA2 = 3, PLAN_TC = 4, PLAN_LAT = 5 };
 
 // Kernel tables (gemv_simt.cu).
 int simt_num_configs(int fmt);
@@ -80,9 +88,18 @@ int mma2_block_k(int fmt);
 size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ);
 cudaError_t launch_gemv_mma2(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
 
+// Latency-oriented kernel tables (gemv_lat.cu).
+int lat_num_configs(int fmt);
+LatConfig lat_config(int fmt, int idx);
+int lat_max_batch(int fmt);
+int lat_block_k(int fmt);
+int lat_items_per_warp(int fmt, const LatConfig& c, int64_t N, int64_t K, int split, int occ);
+size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int M, int split, int occ);
+cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
+
 // tcgen05 skinny GEMM (gemm_tc.cu): Y = X . W^T for the whole batch M.
 cudaError_t launch_gemm_tc(const uint16_t* X, const uint16_t* W, void* Y, int64_t M, int64_t N, int64_t K, int split,
-                           int out_f32, cudaStream_t s);
+                           int ring, int out_f32, cudaStream_t s);
 int tc_batch_tile(int64_t M);
 int tc_take_fault();
 

@@ -58,6 +58,7 @@ static int batch_key(int op, int64_t M) {
 int plan_batch_width(int fmt, const Plan& p) {
     if (p.kind == PLAN_TC) return 1 << 30;  // one launch covers the whole batch
     if (p.kind == PLAN_MMA2) return mma2_max_batch(fmt);
+    if (p.kind == PLAN_LAT) return lat_max_batch(fmt);
     if (p.kind == PLAN_MMA || p.kind == PLAN_TMA) return mma_max_batch(fmt);
     return simt_config(fmt, p.cfg).mb;
 }
@@ -73,7 +74,7 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K) 
     if (p.kind == PLAN_TC) {
         // tensor-core skinny GEMM: BF16, batches above the GEMV column width
         const int64_t KS = (K + 63) / 64;
-        if (fmt != FMT_BF16 || M <= 8 || p.cfg != 0 || p.occ != 1) return false;
+        if (fmt != FMT_BF16 || M <= 8 || p.cfg < 0 || p.cfg > 1 || p.occ != 1) return false;
         if (p.split > KS) return false;
         const int64_t per = (KS + p.split - 1) / p.split;
         return per * (p.split - 1) < KS;  // every cluster rank gets k-stages
@@ -109,6 +110,17 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K) 
         if (mma2_smem_bytes(fmt, c, N, K, mb, p.split, p.occ) > kSmemLimit) return false;
         return true;
     }
+    if (p.kind == PLAN_LAT) {
+        if (p.cfg < 0 || p.cfg >= lat_num_configs(fmt)) return false;
+        const LatConfig c = lat_config(fmt, p.cfg);
+        if (p.occ < 1 || p.occ > 2) return false;
+        const int mb = (int)std::min<int64_t>(M, lat_max_batch(fmt));
+        const int items = lat_items_per_warp(fmt, c, N, K, p.split, p.occ);
+        if (items < 1 || items > c.ni) return false;
+        if (c.ni > items + 1) return false;  // a smaller instantiation holds this share
+        if (lat_smem_bytes(fmt, c, N, mb, p.split, p.occ) > kSmemLimit) return false;
+        return true;
+    }
     if (p.kind == PLAN_TMA) {
         if (p.cfg < 0 || p.cfg >= tma_num_configs(fmt)) return false;
         const TmaConfig c = tma_config(fmt, p.cfg);
@@ -127,10 +139,11 @@ static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
     const int fmt = fmt_of_op(op);
     const int64_t Mb = std::min<int64_t>(M, 8);
     if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 8)
-        for (int sp = 1; sp <= 8; ++sp) {
-            Plan p{PLAN_TC, 0, sp, 1};
-            if (plan_valid(fmt, p, M, N, K)) out.push_back(p);
-        }
+        for (int ring = 0; ring <= 1; ++ring)
+            for (int sp = 1; sp <= 8; ++sp) {
+                Plan p{PLAN_TC, ring, sp, 1};
+                if (plan_valid(fmt, p, M, N, K)) out.push_back(p);
+            }
     const int splits[4] = {1, 2, 4, 8};
     for (int cfg = 0; cfg < mma_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si)
@@ -142,6 +155,12 @@ static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
         for (int si = 0; si < 4; ++si)
             for (int occ = 1; occ <= 2; ++occ) {
                 Plan p{PLAN_MMA2, cfg, splits[si], occ};
+                if (plan_valid(fmt, p, Mb, N, K)) out.push_back(p);
+            }
+    for (int cfg = 0; cfg < lat_num_configs(fmt); ++cfg)
+        for (int si = 0; si < 4; ++si)
+            for (int occ = 1; occ <= 2; ++occ) {
+                Plan p{PLAN_LAT, cfg, splits[si], occ};
                 if (plan_valid(fmt, p, Mb, N, K)) out.push_back(p);
             }
     for (int cfg = 0; cfg < tma_num_configs(fmt); ++cfg)
@@ -223,7 +242,12 @@ std::string plan_to_string(int op, const Plan& p) {
     const char* fs = fmt == FMT_BF16 ? "bf16" : fmt == FMT_G64 ? "int4_g64" : "int4_awq_g128";
     char buf[192];
     if (p.kind == PLAN_TC) {
-        snprintf(buf, sizeof(buf), "tcgen05 fmt=%s tile=128xbatch k_stage=64 split_k=%d", fs, p.split);
+        snprintf(buf, sizeof(buf), "tcgen05 fmt=%s tile=128xbatch k_stage=64 ring=%s split_k=%d", fs,
+                 p.cfg == 0 ? "deep" : "shared_sm", p.split);
+    } else if (p.kind == PLAN_LAT) {
+        const LatConfig c = lat_config(fmt, p.cfg);
+        snprintf(buf, sizeof(buf), "lat fmt=%s warps=%d items_per_warp<=%d unpacked_before_wait=%d ctas_per_sm=%d split_k=%d",
+                 fs, c.warps, c.ni, c.npre, p.occ, p.split);
     } else if (p.kind == PLAN_MMA2) {
         const MmaConfig c = mma2_config(fmt, p.cfg);
         snprintf(buf, sizeof(buf), "mma2 fmt=%s warps=%d superblocks_in_flight=%d ring=%s ctas_per_sm=%d split_k=%d",
@@ -245,8 +269,9 @@ std::string plan_to_string(int op, const Plan& p) {
 }
 
 cudaError_t launch_plan(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
-    if (p.kind == PLAN_TC) return launch_gemm_tc(a.x, (const uint16_t*)a.W, a.y, a.M, a.N, a.K, p.split, a.out_f32, s);
+    if (p.kind == PLAN_TC) return launch_gemm_tc(a.x, (const uint16_t*)a.W, a.y, a.M, a.N, a.K, p.split, p.cfg, a.out_f32, s);
     if (p.kind == PLAN_MMA2) return launch_gemv_mma2(fmt, p, a, s);
+    if (p.kind == PLAN_LAT) return launch_gemv_lat(fmt, p, a, s);
     if (p.kind == PLAN_TMA) return launch_gemv_tma(fmt, p, a, s);
     if (p.kind == PLAN_MMA) return launch_gemv_mma(fmt, p, a, s);
     return launch_gemv_simt(fmt, p, a, s);
