@@ -2,14 +2,16 @@
 """Decode-step weight-streaming benchmark on GB300.
 
 A step is one pass of the whole hot path over one decode token: every weight
-matrix of the model streamed once by the library's GEMV kernels, each matrix
+matrix of the model streamed once by the library's GEMV kernels, each GEMV
 with its own activation vector (all calls through the C ABI, captured once
 into a CUDA graph and replayed). Default workload (--workload tinyllama_int4):
-TinyLlama-1.1B-shaped INT4 group-64 weights at batch 1 -- 22 layers x
-(q 2048x2048, k 256x2048, v 256x2048, o 2048x2048, gate 5632x2048,
-up 5632x2048, down 2048x5632) + LM head 32000x2048 = 155 GEMVs and
-0.5495 GB of codes + scales per step (4.4x the L2, so no matrix is still
-cached when the step reaches it again). Synthetic seeded data (no checkpoint).
+TinyLlama-1.1B-shaped INT4 group-64 weights at batch 1 with the projections
+that share an input fused, as an engine runs them -- 22 layers x (qkv
+2560x2048, o 2048x2048, gate_up 11264x2048, down 2048x5632) + LM head
+32000x2048 = 89 GEMVs and 0.5495 GB of codes + scales per step (4.4x the L2,
+so no matrix is still cached when the step reaches it again);
+--workload tinyllama_int4_unfused streams the same bytes as 155 GEMVs (q, k,
+v, gate and up separately). Synthetic seeded data (no checkpoint).
 
 Metric: achieved HBM GB/s = algorithmic bytes of the step (weights + scales
 + x) / step time, and the weight-stream ms per token.
@@ -49,10 +51,13 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="mbw", choices=["mbw", "reference"])
     p.add_argument("--workload", default="tinyllama_int4",
-                   choices=["tinyllama_int4", "qwen_bf16", "bf16_2048"])
+                   choices=["tinyllama_int4", "tinyllama_int4_unfused", "qwen_bf16", "bf16_2048"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--per-matrix", action="store_true", help="also time each distinct shape on its own")
+    p.add_argument("--tune", default="step", choices=["step", "shape"],
+                   help="step: per-shape autotune, then refine the plans on the whole step graph (default); "
+                        "shape: per-shape autotune only")
     p.add_argument("--plans-out", default=None, help="write the tuned plan index of every shape to this JSON file")
     p.add_argument("--plans-from", default=None, help="restore plans from a --plans-out file instead of tuning")
     p.add_argument("--profile-range", action="store_true",
@@ -211,9 +216,9 @@ class Step:
 
 
 def make_step(workload, seed, device):
-    if workload == "tinyllama_int4":
-        return Step("TinyLlama-1.1B-shaped INT4 g64 decode step, batch 1", wl.FMT_INT4_G64, wl.tinyllama_step(),
-                    seed, device)
+    if workload in ("tinyllama_int4", "tinyllama_int4_unfused"):
+        return Step("TinyLlama-1.1B-shaped INT4 g64 decode step, batch 1", wl.FMT_INT4_G64,
+                    wl.tinyllama_step(fused=(workload == "tinyllama_int4")), seed, device)
     if workload == "qwen_bf16":
         return Step("Qwen2.5-7B-shaped BF16 decode step, batch 1", wl.FMT_BF16, wl.qwen25_7b_step(), seed, device)
     if workload == "bf16_2048":
@@ -234,8 +239,8 @@ def cpu_baseline(workload, budget_s=10.0):
     from memory_bound_weight_gb300 import inputs as gen
 
     o = oracle.load()
-    if workload == "tinyllama_int4":
-        mats, fmt = wl.tinyllama_step(), wl.FMT_INT4_G64
+    if workload in ("tinyllama_int4", "tinyllama_int4_unfused"):
+        mats, fmt = wl.tinyllama_step(fused=(workload == "tinyllama_int4")), wl.FMT_INT4_G64
     elif workload == "qwen_bf16":
         mats, fmt = wl.qwen25_7b_step(), wl.FMT_BF16
     else:
@@ -289,7 +294,8 @@ def run_reference(args, rank, ws):
     cb["value"] = v
     cb["sample"] = f"each step: {per_step:.1f} s of oracle time over the step's matrices in order; first step: " \
                    + vals[0]["sample"]
-    step_bytes = wl.step_bytes_alg(*{"tinyllama_int4": (wl.tinyllama_step(), wl.FMT_INT4_G64),
+    step_bytes = wl.step_bytes_alg(*{"tinyllama_int4": (wl.tinyllama_step(fused=True), wl.FMT_INT4_G64),
+                                     "tinyllama_int4_unfused": (wl.tinyllama_step(), wl.FMT_INT4_G64),
                                      "qwen_bf16": (wl.qwen25_7b_step(), wl.FMT_BF16),
                                      "bf16_2048": ([wl.Mat("c", 2048, 2048)] * 64, wl.FMT_BF16)}[args.workload])
     line = {"impl": "reference", "metric": metric_name(args.workload), "value": v, "unit": "GB/s", "n_gpus": 1,
@@ -305,7 +311,9 @@ def metric_name(workload):
 
 
 def workload_desc(workload):
-    return {"tinyllama_int4": "TinyLlama-1.1B-shaped INT4 group-64 decode step, batch 1 (155 GEMVs)",
+    return {"tinyllama_int4": "TinyLlama-1.1B-shaped INT4 group-64 decode step, batch 1, q/k/v and gate/up fused "
+                              "(89 GEMVs)",
+            "tinyllama_int4_unfused": "TinyLlama-1.1B-shaped INT4 group-64 decode step, batch 1 (155 GEMVs)",
             "qwen_bf16": "Qwen2.5-7B-shaped BF16 decode step, batch 1 (141 GEMVs)",
             "bf16_2048": "BF16 GEMV 2048x2048, batch 1, 64 rotating copies"}[workload]
 
@@ -342,6 +350,12 @@ def main():
     else:
         for N, K in step.shapes():
             mbw.autotune(step.op, 1, N, K)
+        if args.tune == "step":
+            from memory_bound_weight_gb300.tune import tune_sequence
+
+            res = tune_sequence(step.run, [(step.op, 1, N, K) for N, K in step.shapes()],
+                                log=(lambda m: print("[tune]", m, file=sys.stderr)))
+            print(f"[tune] step {res['_ms'][0]:.4f} -> {res['_ms'][1]:.4f} ms", file=sys.stderr)
     if args.plans_out and rank == 0:
         with open(args.plans_out, "w") as f:
             json.dump({f"{N}x{K}": mbw.plan_index(step.op, 1, N, K) for N, K in step.shapes()}, f)
@@ -467,22 +481,52 @@ def main():
     print(json.dumps(line), flush=True)
 
 
+def named_shapes(fmt):
+    """The shapes the per-matrix figures are quoted on, besides the step's own:
+    tinyinfer's four TinyLlama INT4 matrices, and the 2048x2048 BF16 GEMV."""
+    if fmt == wl.FMT_INT4_G64:
+        return [(m.N, m.K) for m in wl.TINYLLAMA_TABLE_SHAPES]
+    return [(2048, 2048)]
+
+
 def time_per_shape(step, device, reps=5):
-    """Each distinct shape on its own: a CUDA graph of every matrix of that
-    shape in the step (distinct weights, so each launch reads from HBM)."""
+    """Steady-state time per matrix of each shape: a CUDA graph of back-to-back
+    launches (programmatic dependent launch, as in the step) over distinct
+    copies of the matrix totalling at least 4x the L2, so every launch reads
+    its weights from HBM; per-matrix time = graph time / launches."""
     import torch
+
+    import memory_bound_weight_gb300 as mbw
+    from memory_bound_weight_gb300 import inputs_gpu
 
     out = {}
     peak, _ = hbm_peak()
-    for N, K in step.shapes():
-        calls = [c for c, m in zip(step.calls, step.mats) if (m.N, m.K) == (N, K)]
-        mult = max(1, 64 // len(calls))
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    shapes = sorted(set(step.shapes()) | set(named_shapes(step.fmt)))
+    for N, K in shapes:
+        b = wl.bytes_alg(step.fmt, 1, N, K)
+        copies = int(min(512, max(8, -(-4 * l2 // b))))
+        x = torch.empty((copies, K), dtype=torch.bfloat16, device=device)
+        y = torch.empty((copies, N), dtype=torch.bfloat16, device=device)
+        inputs_gpu.bf16_normal_(x.view(-1), 0, 7, 1.0)
+        calls = []
+        for i in range(copies):
+            if step.fmt == wl.FMT_INT4_G64:
+                c = inputs_gpu.int4_codes(0, 1000 + i, N, K, device)
+                sc = inputs_gpu.f16_group_scales(0, 1000 + i, N, K // 64, device)
+                calls.append((mbw.gemv_int4_g64, (c, sc, x[i]), y[i]))
+            else:
+                W = inputs_gpu.bf16_weights(0, 1000 + i, N, K, device)
+                calls.append((mbw.gemv_bf16, (W, x[i]), y[i]))
+        mbw.autotune(step.op, 1, N, K)
+        for fn, a, o in calls:
+            fn(*a, out=o)
+        torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream(device)
         with torch.cuda.graph(g, stream=s):
-            for _ in range(mult):
-                for fn, a, o in calls:
-                    fn(*a, out=o)
+            for fn, a, o in calls:
+                fn(*a, out=o)
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
@@ -494,11 +538,12 @@ def time_per_shape(step, device, reps=5):
             g.replay()
             e1.record()
             torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1) / (mult * len(calls)))
+            ts.append(e0.elapsed_time(e1) / copies)
         us = statistics.median(ts) * 1e3
-        b = wl.bytes_alg(step.fmt, 1, N, K)
         out[f"{N}x{K}"] = {"us": us, "GB/s": b / (us * 1e-6) / 1e9, "frac": b / (us * 1e-6) / 1e9 / peak,
-                           "launches_per_graph": mult * len(calls)}
+                           "copies": copies, "plan": mbw.plan_describe(step.op, 1, N, K)}
+        del calls, g
+        torch.cuda.empty_cache()
     return out
 
 

@@ -30,6 +30,8 @@
 // partial. BF16 weights go to the tensor core unchanged.
 #include <cooperative_groups.h>
 
+#include <algorithm>
+
 #include "device.cuh"
 #include "internal.h"
 
@@ -92,23 +94,37 @@ __device__ __forceinline__ void lat_unpack(const u32x8& ra, const u32x8& rb, uin
 
 }  // namespace
 
-// Shared memory: per-warp partials [ntmax][W][16][M], per-CTA sums
+// Shared memory: per-warp partials [ntmax][WK][16][M], per-CTA sums
 // [ntmax][16][M] (read by the other ranks of a split-K cluster), then one
 // x slot per warp: 72 words (64 + 8 pad words of 16 bytes) per super-block
-// the warp may own.
-__host__ __device__ inline size_t lat_red_floats(int ntmax, int W, int M) {
-    return ((size_t)ntmax * (W + 1) * 16 * M + 3) / 4 * 4;  // 16-byte aligned end
+// of the warp's k-slice (xsb = min(NI, k-slice length)); then, for the staged
+// variants, the item ring (W x NI x 2 KB).
+__host__ __device__ inline size_t lat_red_floats(int ntmax, int WK, int M) {
+    return ((size_t)ntmax * (WK + 1) * 16 * M + 3) / 4 * 4;  // 16-byte aligned end
 }
-__host__ __device__ inline size_t lat_smem_floats(int ntmax, int W, int M, int NI) {
-    return lat_red_floats(ntmax, W, M) + (size_t)W * 72 * 4 * NI;
+__host__ __device__ inline size_t lat_smem_floats(int ntmax, int W, int WK, int M, int xsb) {
+    return lat_red_floats(ntmax, WK, M) + (size_t)W * 72 * 4 * xsb;
+}
+__host__ __device__ inline size_t lat_ring_off(int ntmax, int W, int WK, int M, int xsb) {
+    return (lat_smem_floats(ntmax, W, WK, M, xsb) * 4 + 127) / 128 * 128;
 }
 
-template <int FMT, int W, int NI, int NPRE>
+// W warps = WK along K x WT along the CTA's row tiles. Warp (wk, wt) owns
+// super-blocks [b0, b0 + nb) of tiles wt, wt + WT, ... of the CTA's range.
+// NI: most items a warp may own. NPRE: items unpacked before the wait.
+// STG: items past NPRE wait in a shared-memory ring (cp.async). LEAN: the
+// INT4 unpack and MMAs stream one 32-bit word at a time from the ring, with
+// x read from the slot per word, so a warp needs few registers and 16 warps
+// fit beside the next launch.
+template <int FMT, int W, int WT, int NI, int NPRE, int STG, int LEAN>
 __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     gemv_lat_kernel(const GemvArgs a, const int S) {
     static_assert(FMT == FMT_G64 || FMT == FMT_BF16, "INT4 group-64 and BF16 only");
-    static_assert(FMT == FMT_G64 || NPRE == 0, "BF16 needs no unpack");
+    static_assert(FMT == FMT_G64 || (NPRE == 0 && LEAN == 0), "BF16 needs no unpack");
     static_assert(NPRE <= NI, "");
+    static_assert(!LEAN || (STG && NPRE == 0), "the lean path reads staged items");
+    static_assert(W % WT == 0, "");
+    constexpr int WK = W / WT;
     constexpr int BK = (FMT == FMT_BF16) ? 64 : 256;  // k per 128-byte row super-block
     extern __shared__ float lat_smem[];
 
@@ -116,6 +132,7 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
 
     const int rank = (S > 1) ? (int)cg::this_cluster().block_rank() : 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wk = warp % WK, wt = warp / WK;
     const int g = lane >> 2, q = lane & 3;
     const int G = gridDim.x / S;
     const int cgid = blockIdx.x / S;
@@ -125,24 +142,43 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     const int ntmax = (T + G - 1) / G;
     const int mb = a.M;
     const int KB = a.K / BK;  // the plan guarantees K % BK == 0
-    const int BS = (KB + S * W - 1) / (S * W);
-    const int b0 = rank * W * BS + warp * BS;  // this warp's k-slice of super-blocks
+    const int BS = (KB + S * WK - 1) / (S * WK);
+    const int b0 = rank * WK * BS + wk * BS;  // this warp's k-slice of super-blocks
     const int nb = max(0, min(KB, b0 + BS) - b0);
-    const int total = nt * nb;  // items of this warp; the plan guarantees total <= NI
+    const int ntw = (nt > wt) ? (nt - wt + WT - 1) / WT : 0;  // tiles of this warp
+    const int total = ntw * nb;  // items of this warp; the plan guarantees total <= NI
     const size_t rowbytes = (FMT == FMT_BF16) ? (size_t)a.K * 2 : (size_t)a.K / 2;
+    const int xsb = min(NI, BS);  // x super-blocks per warp slot
 
     // ---------------------------------------------- before the wait ----
-    u32x8 ra[NI], rb[NI];  // 32 bytes of rows g and g+8 per item
+    // Items live in registers (STG = 0), or -- past the first NPRE, which are
+    // unpacked early -- in a per-warp shared-memory ring filled with cp.async
+    // (STG = 1): 2 KB per item, lane l's 16-byte chunk c at c * 512 + l * 16,
+    // so every lane reads back exactly the bytes it copied.
+    u32x8 ra[NI], rb[NI];  // 32 bytes of rows g and g+8 per register-held item
     uint32_t rs[NI][2];    // group-64: the 2 fp16 scales of this lane's columns, rows g and g+8
+    uint8_t* ring = reinterpret_cast<uint8_t*>(lat_smem) + lat_ring_off(ntmax, W, WK, mb, xsb) +
+                    (size_t)warp * NI * 2048 + lane * 16;
 #pragma unroll
     for (int j = 0; j < NI; ++j) {
         if (j < total) {
-            const int t = j / nb;
-            const int b = b0 + (j - t * nb);
-            const int r0 = min((t0 + t) * 16 + g, a.N - 1);
-            const int r1 = min((t0 + t) * 16 + g + 8, a.N - 1);
-            ra[j] = ld_stream32(a.W + (size_t)r0 * rowbytes + (size_t)b * 128 + q * 32);
-            rb[j] = ld_stream32(a.W + (size_t)r1 * rowbytes + (size_t)b * 128 + q * 32);
+            const int tt = j / nb;
+            const int b = b0 + (j - tt * nb);
+            const int tile = t0 + wt + tt * WT;
+            const int r0 = min(tile * 16 + g, a.N - 1);
+            const int r1 = min(tile * 16 + g + 8, a.N - 1);
+            const uint8_t* p0 = a.W + (size_t)r0 * rowbytes + (size_t)b * 128 + q * 32;
+            const uint8_t* p1 = a.W + (size_t)r1 * rowbytes + (size_t)b * 128 + q * 32;
+            if (!STG || j < NPRE) {
+                ra[j] = ld_stream32(p0);
+                rb[j] = ld_stream32(p1);
+            } else {
+                uint8_t* d = ring + (size_t)j * 2048;
+                cp_async16(d, p0);
+                cp_async16(d + 512, p0 + 16);
+                cp_async16(d + 1024, p1);
+                cp_async16(d + 1536, p1 + 16);
+            }
             if (FMT == FMT_G64) {
                 const uint16_t* s0 = a.scales + (size_t)r0 * a.groups + (size_t)b * 4 + 2 * (q & 1);
                 const uint16_t* s1 = a.scales + (size_t)r1 * a.groups + (size_t)b * 4 + 2 * (q & 1);
@@ -151,29 +187,34 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
             }
         }
     }
+    if (STG) cp_async_commit();
     uint32_t A[NPRE > 0 ? NPRE : 1][8][8];
 #pragma unroll
     for (int j = 0; j < NPRE; ++j)
         if (j < total) lat_unpack(ra[j], rb[j], A[j]);
 
-    // addresses of the x words this lane will read after the wait (word i of
-    // the warp's x: super-block i / (M * words per row), batch row, word)
-    constexpr int XLD = 2 * NI;  // most x loads per lane (M * words per row <= 64 per super-block)
-    const uint16_t* xsrc[XLD];
-    {
-        constexpr int XWSB0 = BK / 8;
-        const int sbw0 = mb * XWSB0;
+    // Addresses of the x words this lane reads after the wait: word i of the
+    // warp's x (super-block i / (M * words per row), batch row, word) is
+    // read by lane i % 32. At batch 1 word i is simply x + b0 * BK + 8 i.
+    constexpr int XWSB = BK / 8;  // 16-byte x words per batch row per super-block
+    constexpr int XLD = 2 * NI;   // most x loads per lane (M * XWSB <= 64 per super-block)
+    const int sbw = mb * XWSB;    // words per super-block
+    const int nxw = nb * sbw;     // words this warp reads
+    auto x_addr = [&](int r) -> const uint16_t* {
+        const int wi = lane + 32 * r;
+        const int sb = wi / sbw, rem = wi - sb * sbw;
+        const int m = rem / XWSB, w = rem - m * XWSB;
+        return a.x + (size_t)m * a.K + (size_t)(b0 + sb) * BK + w * 8;
+    };
+    // the lean variant keeps its registers for after the wait and derives
+    // these there (batch > 1 only)
+    const uint16_t* xsrc[LEAN ? 1 : XLD];
+    if (!LEAN && mb > 1) {
 #pragma unroll
-        for (int r = 0; r < XLD; ++r) {
-            const int wi = lane + 32 * r;
-            xsrc[r] = nullptr;
-            if (wi < nb * sbw0) {
-                const int sb = wi / sbw0, rem = wi - sb * sbw0;
-                const int m = rem / XWSB0, w = rem - m * XWSB0;
-                xsrc[r] = a.x + (size_t)m * a.K + (size_t)(b0 + sb) * BK + w * 8;
-            }
-        }
+        for (int r = 0; r < XLD; ++r) xsrc[LEAN ? 0 : r] = (lane + 32 * r < nxw) ? x_addr(r) : nullptr;
     }
+    const uint16_t* xlin = a.x + (size_t)b0 * BK + lane * 8;
+
     prefetch_l2_grid_share(a.x, (size_t)a.M * a.K * 2);
     // x is produced by the previous kernel in the stream: wait for it only now.
     pdl_wait();
@@ -193,22 +234,19 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
         xon = xm < mb;
     }
     constexpr int XWL = (FMT == FMT_G64) ? 8 : 2;  // x words per B-fragment lane per super-block
-    constexpr int XWSB = BK / 8;                     // 16-byte x words per batch row per super-block
-    // Right after the wait the warp reads all the x it needs -- its nb
-    // super-blocks for every batch row, word i at lane i % 32 -- in one round
-    // of 16-byte loads, and hands each B-fragment lane its words through a
-    // per-warp shared-memory slot (one pad word per 8 keeps those reads
-    // conflict-free). Loading per item, or a lane issuing eight loads itself,
-    // or eight rounds of shuffles, each cost more latency.
-    const int sbw = mb * XWSB;  // words per super-block
-    const int nxw = nb * sbw;   // words this warp reads
-    uint4* xslot = reinterpret_cast<uint4*>(lat_smem + lat_red_floats(ntmax, W, mb)) + (size_t)warp * (72 * NI);
+    // The warp reads all the x it needs in one round of 16-byte loads and
+    // hands each B-fragment lane its words through a per-warp shared-memory
+    // slot (one pad word per 8 keeps those reads conflict-free). Loading per
+    // item, a lane issuing eight loads itself, or eight rounds of shuffles
+    // each cost more latency.
+    uint4* xslot = reinterpret_cast<uint4*>(lat_smem + lat_red_floats(ntmax, WK, mb)) + (size_t)warp * (72 * xsb);
     {
         uint4 v[XLD];
 #pragma unroll
         for (int r = 0; r < XLD; ++r) {
             v[r] = make_uint4(0, 0, 0, 0);
-            if (xsrc[r] != nullptr) v[r] = ld_ro16(xsrc[r]);
+            if (lane + 32 * r < nxw)
+                v[r] = ld_ro16(mb == 1 ? xlin + 256 * r : LEAN ? x_addr(r) : xsrc[LEAN ? 0 : r]);
         }
 #pragma unroll
         for (int r = 0; r < XLD; ++r) {
@@ -217,15 +255,20 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
         }
     }
     __syncwarp();
-    uint4 xv[XWL];
+    // slot index of this lane's first x word of super-block sb of its k-slice
+    auto xword0 = [&](int sb) {
+        return sb * sbw + ((FMT == FMT_G64) ? (min(xm, 1) * 32 + 8 * q) : (g * 8 + 2 * q));
+    };
+    uint4 xv[LEAN ? 1 : XWL];
     auto load_x = [&](int sb) {
 #pragma unroll
         for (int w = 0; w < XWL; ++w) {
-            const int wi = sb * sbw + ((FMT == FMT_G64) ? (min(xm, 1) * 32 + 8 * q + w) : (g * 8 + 2 * q + w));
+            const int wi = xword0(sb) + w;
             xv[w] = xon ? xslot[wi + (wi >> 3)] : make_uint4(0, 0, 0, 0);
         }
     };
-    if (total > 0) load_x(0);
+    if (!LEAN && total > 0) load_x(0);
+    if (STG) cp_async_wait<0>();  // this lane's ring bytes have landed (it reads only those)
 
     float* red = lat_smem;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -233,30 +276,35 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
 #pragma unroll
     for (int j = 0; j < NI; ++j) {
         if (j < total) {
-            const int t = j / nb;
-            const int bi = j - t * nb;
-            if (j > 0 && nb > 1) load_x(bi);
-            if (FMT == FMT_G64) {
-                uint32_t Aj[8][8];
-                if (j < NPRE) {
+            const int tt = j / nb;
+            const int bi = j - tt * nb;
+            if (LEAN) {
+                // stream the item from the ring one 32-bit word at a time
+                const uint8_t* d = ring + (size_t)j * 2048;
+                const int x0 = xword0(bi);
+                float dd[4][4] = {};
 #pragma unroll
-                    for (int w = 0; w < 8; ++w)
+                for (int c = 0; c < 2; ++c) {
+                    const uint4 ca = *reinterpret_cast<const uint4*>(d + c * 512);
+                    const uint4 cb = *reinterpret_cast<const uint4*>(d + 1024 + c * 512);
+                    const uint32_t wa4[4] = {ca.x, ca.y, ca.z, ca.w};
+                    const uint32_t wb4[4] = {cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) Aj[w][i] = A[j < NPRE ? j : 0][w][i];
-                } else {
-                    lat_unpack(ra[j], rb[j], Aj);
-                }
-                // four independent accumulator chains of four MMAs each
-                float d[4][4] = {};
-#pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    lat_mma(d[(w & 1) * 2], Aj[w][0], Aj[w][1], Aj[w][2], Aj[w][3], xv[w].x, xv[w].y);
-                    lat_mma(d[(w & 1) * 2 + 1], Aj[w][4], Aj[w][5], Aj[w][6], Aj[w][7], xv[w].z, xv[w].w);
+                    for (int u = 0; u < 4; ++u) {
+                        const int w = 4 * c + u;
+                        uint4 x4 = make_uint4(0, 0, 0, 0);
+                        if (xon) x4 = xslot[x0 + w + ((x0 + w) >> 3)];
+                        const uint32_t wa = wa4[u], wb = wb4[u];
+                        const uint32_t z = 0x43084308u;
+                        lat_mma(dd[(w & 1) * 2], lat_sub(lat_nib(wa), z), lat_sub(lat_nib(wb), z),
+                                lat_sub(lat_nib(wa >> 4), z), lat_sub(lat_nib(wb >> 4), z), x4.x, x4.y);
+                        lat_mma(dd[(w & 1) * 2 + 1], lat_sub(lat_nib(wa >> 8), z), lat_sub(lat_nib(wb >> 8), z),
+                                lat_sub(lat_nib(wa >> 12), z), lat_sub(lat_nib(wb >> 12), z), x4.z, x4.w);
+                    }
                 }
                 float ds[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) ds[i] = (d[0][i] + d[1][i]) + (d[2][i] + d[3][i]);
-                // columns 2q, 2q+1 = groups 2(q&1), 2(q&1)+1 of batch q>>1
+                for (int i = 0; i < 4; ++i) ds[i] = (dd[0][i] + dd[1][i]) + (dd[2][i] + dd[3][i]);
                 const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&rs[j][0]));
                 const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&rs[j][1]));
                 acc[0] = fmaf(f0.x, ds[0], acc[0]);
@@ -264,16 +312,56 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
                 acc[2] = fmaf(f1.x, ds[2], acc[2]);
                 acc[2] = fmaf(f1.y, ds[3], acc[2]);
             } else {
-                const u32x8& wa = ra[j];
-                const u32x8& wb = rb[j];
-                lat_mma(acc, wa.v[0], wb.v[0], wa.v[1], wb.v[1], xv[0].x, xv[0].y);
-                lat_mma(acc2, wa.v[2], wb.v[2], wa.v[3], wb.v[3], xv[0].z, xv[0].w);
-                lat_mma(acc, wa.v[4], wb.v[4], wa.v[5], wb.v[5], xv[1].x, xv[1].y);
-                lat_mma(acc2, wa.v[6], wb.v[6], wa.v[7], wb.v[7], xv[1].z, xv[1].w);
+                if (j > 0 && nb > 1) load_x(bi);
+                if (STG && j >= NPRE) {
+                    const uint8_t* d = ring + (size_t)j * 2048;
+                    const uint4 c0 = *reinterpret_cast<const uint4*>(d);
+                    const uint4 c1 = *reinterpret_cast<const uint4*>(d + 512);
+                    const uint4 c2 = *reinterpret_cast<const uint4*>(d + 1024);
+                    const uint4 c3 = *reinterpret_cast<const uint4*>(d + 1536);
+                    ra[j] = u32x8{{c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w}};
+                    rb[j] = u32x8{{c2.x, c2.y, c2.z, c2.w, c3.x, c3.y, c3.z, c3.w}};
+                }
+                if (FMT == FMT_G64) {
+                    uint32_t Aj[8][8];
+                    if (j < NPRE) {
+#pragma unroll
+                        for (int w = 0; w < 8; ++w)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) Aj[w][i] = A[j < NPRE ? j : 0][w][i];
+                    } else {
+                        lat_unpack(ra[j], rb[j], Aj);
+                    }
+                    // four independent accumulator chains of four MMAs each
+                    float d[4][4] = {};
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        lat_mma(d[(w & 1) * 2], Aj[w][0], Aj[w][1], Aj[w][2], Aj[w][3], xv[w].x, xv[w].y);
+                        lat_mma(d[(w & 1) * 2 + 1], Aj[w][4], Aj[w][5], Aj[w][6], Aj[w][7], xv[w].z, xv[w].w);
+                    }
+                    float ds[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) ds[i] = (d[0][i] + d[1][i]) + (d[2][i] + d[3][i]);
+                    // columns 2q, 2q+1 = groups 2(q&1), 2(q&1)+1 of batch q>>1
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&rs[j][0]));
+                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&rs[j][1]));
+                    acc[0] = fmaf(f0.x, ds[0], acc[0]);
+                    acc[0] = fmaf(f0.y, ds[1], acc[0]);
+                    acc[2] = fmaf(f1.x, ds[2], acc[2]);
+                    acc[2] = fmaf(f1.y, ds[3], acc[2]);
+                } else {
+                    const u32x8& wa = ra[j];
+                    const u32x8& wb = rb[j];
+                    lat_mma(acc, wa.v[0], wb.v[0], wa.v[1], wb.v[1], xv[0].x, xv[0].y);
+                    lat_mma(acc2, wa.v[2], wb.v[2], wa.v[3], wb.v[3], xv[0].z, xv[0].w);
+                    lat_mma(acc, wa.v[4], wb.v[4], wa.v[5], wb.v[5], xv[1].x, xv[1].y);
+                    lat_mma(acc2, wa.v[6], wb.v[6], wa.v[7], wb.v[7], xv[1].z, xv[1].w);
+                }
             }
             if (bi == nb - 1) {
-                // end of this warp's k-slice of tile t: per-warp partials
-                float* rp = red + ((size_t)(t * W + warp) * 16) * mb;
+                // end of this warp's k-slice of its tile: per-warp partials
+                const int t = wt + tt * WT;
+                float* rp = red + ((size_t)(t * WK + wk) * 16) * mb;
                 if (FMT == FMT_G64) {
                     const float v0 = acc[0] + __shfl_xor_sync(0xFFFFFFFFu, acc[0], 1);
                     const float v2 = acc[2] + __shfl_xor_sync(0xFFFFFFFFu, acc[2], 1);
@@ -300,24 +388,24 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
         }
     }
     if (nb == 0) {
-        // an empty k-slice still contributes zeros for every tile
-        for (int t = 0; t < nt; ++t) {
-            float* rp = red + ((size_t)(t * W + warp) * 16) * mb;
+        // an empty k-slice still contributes zeros for each of its tiles
+        for (int t = wt; t < nt; t += WT) {
+            float* rp = red + ((size_t)(t * WK + wk) * 16) * mb;
             for (int i = lane; i < 16 * mb; i += 32) rp[i] = 0.f;
         }
     }
     __syncthreads();
 
-    // each output: the sum over warps in warp order
+    // each output: the sum over the K-warps in order
     const int nout = nt * 16 * mb;
     const int row0 = t0 * 16;
     if (S == 1) {
         if (mb == 1) {
             for (int i = threadIdx.x; i < nout; i += W * 32) {
-                const float* rp = red + (i >> 4) * (W * 16) + (i & 15);
+                const float* rp = red + (i >> 4) * (WK * 16) + (i & 15);
                 float v = 0.f;
 #pragma unroll
-                for (int w = 0; w < W; ++w) v += rp[w * 16];
+                for (int w = 0; w < WK; ++w) v += rp[w * 16];
                 if (row0 + i < a.N) store_out(a.y, row0 + i, v, a.out_f32);
             }
             return;
@@ -328,22 +416,22 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
             const int r = rm / mb;
             const int m = rm - r * mb;
             float v = 0.f;
-            const float* rp = red + (size_t)t * W * 16 * mb + rm;
+            const float* rp = red + (size_t)t * WK * 16 * mb + rm;
 #pragma unroll
-            for (int w = 0; w < W; ++w) v += rp[(size_t)w * 16 * mb];
+            for (int w = 0; w < WK; ++w) v += rp[(size_t)w * 16 * mb];
             const int row = row0 + t * 16 + r;
             if (row < a.N) store_out(a.y, (int64_t)m * a.N + row, v, a.out_f32);
         }
         return;
     }
-    float* fin = red + (size_t)ntmax * W * 16 * mb;  // [tile*16 + row][m]
+    float* fin = red + (size_t)ntmax * WK * 16 * mb;  // [tile*16 + row][m]
     for (int i = threadIdx.x; i < nout; i += W * 32) {
         const int t = i / (16 * mb);
         const int rm = i - t * 16 * mb;
         float v = 0.f;
-        const float* rp = red + (size_t)t * W * 16 * mb + rm;
+        const float* rp = red + (size_t)t * WK * 16 * mb + rm;
 #pragma unroll
-        for (int w = 0; w < W; ++w) v += rp[(size_t)w * 16 * mb];
+        for (int w = 0; w < WK; ++w) v += rp[(size_t)w * 16 * mb];
         fin[i] = v;
     }
     cg::cluster_group cluster = cg::this_cluster();
@@ -369,12 +457,18 @@ struct LatEntry {
     LatConfig cfg;
     LatFn fn;
 };
-#define MBW_L(F, W, NI, NP) \
-    { {W, NI, NP}, gemv_lat_kernel<F, W, NI, NP> }
-const LatEntry kLatG64[] = {MBW_L(FMT_G64, 8, 1, 1), MBW_L(FMT_G64, 8, 1, 0), MBW_L(FMT_G64, 8, 2, 0),
-                            MBW_L(FMT_G64, 8, 3, 0), MBW_L(FMT_G64, 4, 1, 1)};
-const LatEntry kLatBf16[] = {MBW_L(FMT_BF16, 8, 2, 0), MBW_L(FMT_BF16, 8, 4, 0),
-                             MBW_L(FMT_BF16, 4, 4, 0), MBW_L(FMT_BF16, 16, 2, 0)};
+#define MBW_L(F, W, WT, NI, NP, ST, LN) \
+    { {W, WT, NI, NP, ST, LN}, gemv_lat_kernel<F, W, WT, NI, NP, ST, LN> }
+const LatEntry kLatG64[] = {
+    MBW_L(FMT_G64, 8, 1, 1, 1, 0, 0), MBW_L(FMT_G64, 8, 1, 1, 0, 0, 0), MBW_L(FMT_G64, 8, 1, 2, 0, 0, 0),
+    MBW_L(FMT_G64, 8, 1, 3, 0, 0, 0), MBW_L(FMT_G64, 4, 1, 1, 1, 0, 0), MBW_L(FMT_G64, 8, 1, 2, 1, 1, 0),
+    MBW_L(FMT_G64, 8, 1, 4, 1, 1, 0), MBW_L(FMT_G64, 8, 1, 6, 0, 1, 0), MBW_L(FMT_G64, 16, 2, 2, 0, 1, 1),
+    MBW_L(FMT_G64, 16, 2, 3, 0, 1, 1), MBW_L(FMT_G64, 16, 1, 2, 0, 1, 1), MBW_L(FMT_G64, 8, 1, 3, 0, 1, 1),
+    MBW_L(FMT_G64, 8, 1, 5, 0, 1, 1)};
+const LatEntry kLatBf16[] = {MBW_L(FMT_BF16, 8, 1, 2, 0, 0, 0), MBW_L(FMT_BF16, 8, 1, 4, 0, 0, 0),
+                             MBW_L(FMT_BF16, 4, 1, 4, 0, 0, 0), MBW_L(FMT_BF16, 16, 1, 2, 0, 0, 0),
+                             MBW_L(FMT_BF16, 16, 2, 2, 0, 0, 0), MBW_L(FMT_BF16, 8, 1, 4, 0, 1, 0),
+                             MBW_L(FMT_BF16, 8, 1, 6, 0, 1, 0)};
 #undef MBW_L
 
 const LatEntry* lat_table(int fmt, int* n) {
@@ -409,21 +503,26 @@ int lat_block_k(int fmt) { return fmt == FMT_BF16 ? 64 : 256; }
 int lat_items_per_warp(int fmt, const LatConfig& c, int64_t N, int64_t K, int split, int occ) {
     const int BK = lat_block_k(fmt);
     if (K % BK != 0) return 0;
+    const int WK = c.warps / c.wt;
     const int64_t KB = K / BK;
-    const int64_t BS = (KB + (int64_t)split * c.warps - 1) / ((int64_t)split * c.warps);
-    if ((int64_t)(split - 1) * c.warps * BS >= KB) return 0;  // a cluster rank without k-range
+    const int64_t BS = (KB + (int64_t)split * WK - 1) / ((int64_t)split * WK);
+    if ((int64_t)(split - 1) * WK * BS >= KB) return 0;  // a cluster rank without k-range
     const int G = mma_row_groups(N, split, occ);
     const int64_t T = (N + 15) / 16;
     const int64_t ntmax = (T + G - 1) / G;
-    return (int)(ntmax * BS);
+    return (int)((ntmax + c.wt - 1) / c.wt * BS);
 }
 
-size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int M, int split, int occ) {
-    (void)fmt;
+size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
     const int G = mma_row_groups(N, split, occ);
     const int64_t T = (N + 15) / 16;
     const int ntmax = (int)((T + G - 1) / G);
-    return lat_smem_floats(ntmax, c.warps, M, c.ni) * sizeof(float);
+    const int WK = c.warps / c.wt;
+    const int64_t KB = K / lat_block_k(fmt);
+    const int64_t BS = (KB + (int64_t)split * WK - 1) / ((int64_t)split * WK);
+    const int xsb = (int)std::min<int64_t>(c.ni, BS);
+    if (c.staged) return lat_ring_off(ntmax, c.warps, WK, M, xsb) + (size_t)c.warps * c.ni * 2048;
+    return lat_smem_floats(ntmax, c.warps, WK, M, xsb) * sizeof(float);
 }
 
 cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
@@ -434,7 +533,7 @@ cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStrea
     const int items = lat_items_per_warp(fmt, e.cfg, a.N, a.K, p.split, p.occ);
     if (items < 1 || items > e.cfg.ni) return cudaErrorInvalidValue;
     const int G = mma_row_groups(a.N, p.split, p.occ);
-    const size_t smem = lat_smem_bytes(fmt, e.cfg, a.N, a.M, p.split, p.occ);
+    const size_t smem = lat_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;

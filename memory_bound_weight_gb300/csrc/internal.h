@@ -46,9 +46,12 @@ struct MmaConfig {
 // One instantiation of the latency-oriented kernel (whole share in registers
 // before the wait).
 struct LatConfig {
-    int warps;  // warps per CTA; each owns one k-slice of every tile of the CTA
-    int ni;     // most items (16 rows x one 128-byte super-block) a warp may own
-    int npre;   // items unpacked to MMA fragments before the wait (INT4)
+    int warps;   // warps per CTA
+    int wt;      // warps along the CTA's row tiles (the other warps / wt split K)
+    int ni;      // most items (16 rows x one 128-byte super-block) a warp may own
+    int npre;    // items unpacked to MMA fragments before the wait (INT4)
+    int staged;  // 1: items past npre wait in a shared-memory ring (cp.async), not registers
+    int lean;    // 1: unpack and MMA one 32-bit word at a time from the ring (few registers)
 };
 
 // One instantiation of the bulk-copy-fed tensor-core streaming kernel.
@@ -94,7 +97,7 @@ LatConfig lat_config(int fmt, int idx);
 int lat_max_batch(int fmt);
 int lat_block_k(int fmt);
 int lat_items_per_warp(int fmt, const LatConfig& c, int64_t N, int64_t K, int split, int occ);
-size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int M, int split, int occ);
+size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, int split, int occ);
 cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
 
 // tcgen05 skinny GEMM (gemm_tc.cu): Y = X . W^T for the whole batch M.

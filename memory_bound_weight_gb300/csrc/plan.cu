@@ -118,7 +118,7 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K) 
         const int items = lat_items_per_warp(fmt, c, N, K, p.split, p.occ);
         if (items < 1 || items > c.ni) return false;
         if (c.ni > items + 1) return false;  // a smaller instantiation holds this share
-        if (lat_smem_bytes(fmt, c, N, mb, p.split, p.occ) > kSmemLimit) return false;
+        if (lat_smem_bytes(fmt, c, N, K, mb, p.split, p.occ) > kSmemLimit) return false;
         return true;
     }
     if (p.kind == PLAN_TMA) {
@@ -246,8 +246,11 @@ std::string plan_to_string(int op, const Plan& p) {
                  p.cfg == 0 ? "deep" : "shared_sm", p.split);
     } else if (p.kind == PLAN_LAT) {
         const LatConfig c = lat_config(fmt, p.cfg);
-        snprintf(buf, sizeof(buf), "lat fmt=%s warps=%d items_per_warp<=%d unpacked_before_wait=%d ctas_per_sm=%d split_k=%d",
-                 fs, c.warps, c.ni, c.npre, p.occ, p.split);
+        snprintf(buf, sizeof(buf),
+                 "lat fmt=%s warps=%d (k %d x tiles %d) items_per_warp<=%d unpacked_before_wait=%d staging=%s%s "
+                 "ctas_per_sm=%d split_k=%d",
+                 fs, c.warps, c.warps / c.wt, c.wt, c.ni, c.npre, c.staged ? "smem" : "registers",
+                 c.lean ? " lean" : "", p.occ, p.split);
     } else if (p.kind == PLAN_MMA2) {
         const MmaConfig c = mma2_config(fmt, p.cfg);
         snprintf(buf, sizeof(buf), "mma2 fmt=%s warps=%d superblocks_in_flight=%d ring=%s ctas_per_sm=%d split_k=%d",

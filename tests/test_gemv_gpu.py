@@ -299,3 +299,23 @@ def test_skinny_config_shapes_sampled_rows(orc, M, N, K):
     Wr = np.stack([gen.bf16_weights(0, 7, N, K, row0=int(r), rows=1)[0] for r in rows])
     Yr, Ar = orc.gemm_bf16(Wr, host_bits16(Xd))
     assert_parity(Y[:, torch.from_numpy(rows).cuda()], Yr, Ar, f"skinny M={M} {N}x{K} sampled")
+
+
+@pytest.mark.parametrize("N,K", [(2560, 2048), (11264, 2048), (2048, 5632), (5632, 2048)])
+def test_int4_g64_every_plan_at_step_shapes(orc, N, K):
+    """Every candidate plan (all families, instantiations, splits, CTAs per SM)
+    at the fused and named TinyLlama shapes, on sampled rows: the register-
+    and shared-memory-staged latency kernels own up to six items per warp
+    only at these sizes."""
+    rows = np.unique(np.concatenate([np.arange(0, 16), np.arange(N - 16, N),
+                                     np.random.default_rng(N + K).integers(0, N, 64)]))
+    cd = inputs_gpu.int4_codes(0, 3, N, K)
+    sd = inputs_gpu.f16_group_scales(0, 3, N, K // 64)
+    xd = inputs_gpu.bf16_activations(0, 4, 1, K)
+    c = np.stack([gen.int4_codes(0, 3, N, K, row0=int(r), rows=1)[0] for r in rows])
+    s = np.stack([gen.f16_group_scales(0, 3, N, K // 64, row0=int(r), rows=1)[0] for r in rows])
+    Y, A = orc.gemm_int4_g64(c, s, host_bits16(xd))
+    sel = torch.from_numpy(rows).cuda()
+    for i, desc in each_plan(mbw.OP_GEMV_INT4_G64, 1, N, K):
+        y = mbw.gemv_int4_g64(cd, sd, xd[0])
+        assert_parity(y[sel], Y[0], A[0], f"g64 {N}x{K} plan {desc}")

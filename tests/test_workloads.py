@@ -65,3 +65,12 @@ def test_config_shapes():
     assert wl.bytes_alg(wl.FMT_BF16, 1, 2048, 2048) == 2048 * 2048 * 2 + 4096
     assert wl.bytes_alg(wl.FMT_INT4_G64, 1, 2048, 2048) == 2_232_320
     assert wl.bytes_alg(wl.FMT_INT4_G64, 1, 32000, 2048) == 34_820_096
+
+
+def test_fused_tinyllama_step_streams_the_same_weights():
+    # concatenating q/k/v and gate/up changes the launches, not the bytes
+    a, b = wl.tinyllama_step(), wl.tinyllama_step(fused=True)
+    assert len(a) == 155 and len(b) == 89
+    for fmt in (wl.FMT_BF16, wl.FMT_INT4_G64, wl.FMT_INT4_AWQ_G128):
+        assert wl.step_weight_bytes(a, fmt) == wl.step_weight_bytes(b, fmt)
+    assert wl.step_params(a) == wl.step_params(b)
