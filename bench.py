@@ -38,6 +38,7 @@ sys.path.insert(0, ROOT)
 from memory_bound_weight_gb300 import workloads as wl  # noqa: E402
 
 FALLBACK_HBM_GBS = 6778.3  # the machine's measured copy bandwidth, recorded copy
+FALLBACK_BF16_TFLOPS = 1752.2  # the pool's measured sustained cuBLAS bf16, recorded copy
 # DRAM bytes (read + write) per launch of the step's dominant kernel from one
 # ncu capture, keyed by the sha256 of the kernel source it was taken on; a
 # changed kernel gets traffic = null until it is captured again.
@@ -51,7 +52,9 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="mbw", choices=["mbw", "reference"])
     p.add_argument("--workload", default="tinyllama_int4",
-                   choices=["tinyllama_int4", "tinyllama_int4_unfused", "qwen_bf16", "bf16_2048"])
+                   choices=["tinyllama_int4", "tinyllama_int4_unfused", "qwen_bf16", "qwen_awq", "bf16_2048"])
+    p.add_argument("--batch", type=int, default=1,
+                   help="activation rows per GEMV (qwen_awq: AWQ-style INT4 decode at batch M)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--per-matrix", action="store_true", help="also time each distinct shape on its own")
@@ -104,6 +107,18 @@ def hbm_peak():
         return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json, copy kernel)"
     except Exception:  # noqa: BLE001
         return FALLBACK_HBM_GBS, "measured on this pool (recorded copy; MEASURED_PEAKS.json absent)"
+
+
+def tensor_peak():
+    """bf16 dense tensor peak (TFLOP/s): the pool's sustained cuBLAS figure, the
+    one for a kernel timed inside a long step."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), "measured sustained (MEASURED_PEAKS.json, cuBLAS bf16)"
+    except Exception:  # noqa: BLE001
+        return FALLBACK_BF16_TFLOPS, "measured on this pool (recorded sustained cuBLAS bf16; MEASURED_PEAKS.json absent)"
 
 
 class ClockSampler:
@@ -170,42 +185,51 @@ def kernel_source_sha():
 # -------------------------------------------------------------- workloads ----
 class Step:
     """All matrices of one decode step resident on the device, and the calls
-    that stream them."""
+    that stream them (each GEMV with its own activation rows X [M][K])."""
 
-    def __init__(self, name, fmt, mats, seed, device):
+    def __init__(self, name, fmt, mats, seed, device, M=1):
         import torch
 
         import memory_bound_weight_gb300 as mbw
         from memory_bound_weight_gb300 import inputs as gen
         from memory_bound_weight_gb300 import inputs_gpu
 
-        self.name, self.fmt, self.mats = name, fmt, mats
+        self.name, self.fmt, self.mats, self.M = name, fmt, mats, M
         self.device = device
         sumK = sum(m.K for m in mats)
         sumN = sum(m.N for m in mats)
-        self.x = torch.empty(sumK, dtype=torch.bfloat16, device=device)
-        self.y = torch.empty(sumN, dtype=torch.bfloat16, device=device)
+        self.x = torch.empty(M * sumK, dtype=torch.bfloat16, device=device)
+        self.y = torch.empty(M * sumN, dtype=torch.bfloat16, device=device)
         self.calls = []
         ko = no = 0
         for mi, m in enumerate(mats):
-            xv = self.x[ko:ko + m.K]
-            yv = self.y[no:no + m.N]
+            xv = self.x[ko:ko + M * m.K]
+            yv = self.y[no:no + M * m.N]
             inputs_gpu.bf16_normal_(xv, seed, gen.stream_id(mi, gen.KIND_X), gen.X_SIGMA)
+            xa = xv if M == 1 else xv.view(M, m.K)
+            ya = yv if M == 1 else yv.view(M, m.N)
             if fmt == wl.FMT_INT4_G64:
                 c = inputs_gpu.int4_codes(seed, mi, m.N, m.K, device)
                 s = inputs_gpu.f16_group_scales(seed, mi, m.N, m.K // 64, device)
-                self.calls.append((mbw.gemv_int4_g64, (c, s, xv), yv))
+                self.calls.append((mbw.gemv_int4_g64, (c, s, xa), ya))
+            elif fmt == wl.FMT_INT4_AWQ_G128:
+                c = inputs_gpu.int4_codes(seed, mi, m.N, m.K, device)
+                s = inputs_gpu.f16_group_scales(seed, mi, m.N, m.K // 128, device)
+                z = inputs_gpu.u4_zero_points(seed, mi, m.N, m.K // 128, device)
+                self.calls.append((mbw.gemv_int4_awq_g128, (c, s, z, xa), ya))
             elif fmt == wl.FMT_BF16:
                 W = inputs_gpu.bf16_weights(seed, mi, m.N, m.K, device)
-                self.calls.append((mbw.gemv_bf16, (W, xv), yv))
+                self.calls.append((mbw.gemv_bf16, (W, xa), ya))
             else:
                 raise ValueError(fmt)
-            ko += m.K
-            no += m.N
-        self.op = mbw.OP_GEMV_INT4_G64 if fmt == wl.FMT_INT4_G64 else mbw.OP_GEMV_BF16
-        self.bytes_alg = wl.step_bytes_alg(mats, fmt)
-        self.h2d_bytes = 2 * sumK
-        self.d2h_bytes = 2 * sumN
+            ko += M * m.K
+            no += M * m.N
+        self.op = {wl.FMT_INT4_G64: mbw.OP_GEMV_INT4_G64, wl.FMT_INT4_AWQ_G128: mbw.OP_GEMV_INT4_AWQ_G128,
+                   wl.FMT_BF16: mbw.OP_GEMV_BF16}[fmt]
+        self.bytes_alg = wl.step_bytes_alg(mats, fmt, M)
+        self.flops = sum(wl.flops(M, m.N, m.K) for m in mats)
+        self.h2d_bytes = 2 * M * sumK
+        self.d2h_bytes = 2 * M * sumN
 
     def shapes(self):
         return sorted({(m.N, m.K) for m in self.mats})
@@ -215,12 +239,15 @@ class Step:
             fn(*args, out=out)
 
 
-def make_step(workload, seed, device):
+def make_step(workload, seed, device, M=1):
     if workload in ("tinyllama_int4", "tinyllama_int4_unfused"):
         return Step("TinyLlama-1.1B-shaped INT4 g64 decode step, batch 1", wl.FMT_INT4_G64,
                     wl.tinyllama_step(fused=(workload == "tinyllama_int4")), seed, device)
     if workload == "qwen_bf16":
         return Step("Qwen2.5-7B-shaped BF16 decode step, batch 1", wl.FMT_BF16, wl.qwen25_7b_step(), seed, device)
+    if workload == "qwen_awq":
+        return Step(f"Qwen2.5-7B-shaped AWQ-style INT4 decode step, batch {M}", wl.FMT_INT4_AWQ_G128,
+                    wl.qwen25_7b_step(), seed, device, M)
     if workload == "bf16_2048":
         # 2048x2048 BF16 GEMV; 64 distinct copies (537 MB) so that each is evicted before it recurs
         mats = [wl.Mat(f"copy{i}", 2048, 2048) for i in range(64)]
@@ -230,7 +257,7 @@ def make_step(workload, seed, device):
 
 # ------------------------------------------------------------- cpu oracle ----
 _HOST_CACHE = {}  # host copies of the step's matrices, reused across oracle runs
-def cpu_baseline(workload, budget_s=10.0):
+def cpu_baseline(workload, budget_s=10.0, M=1):
     """The fp64 oracle on this host's cores over a bounded sample of the step
     (whole passes over the step's matrices until about `budget_s` of oracle time)."""
     import numpy as np
@@ -243,32 +270,41 @@ def cpu_baseline(workload, budget_s=10.0):
         mats, fmt = wl.tinyllama_step(fused=(workload == "tinyllama_int4")), wl.FMT_INT4_G64
     elif workload == "qwen_bf16":
         mats, fmt = wl.qwen25_7b_step(), wl.FMT_BF16
+    elif workload == "qwen_awq":
+        mats, fmt = wl.qwen25_7b_step(), wl.FMT_INT4_AWQ_G128
     else:
         mats, fmt = [wl.Mat("copy0", 2048, 2048)] * 64, wl.FMT_BF16
     done_bytes = 0
     spent = 0.0
     n = 0
     order = [(mi, m) for _ in range(1000) for mi, m in enumerate(mats)]
-    cache = _HOST_CACHE.setdefault(workload, {})
+    cache = _HOST_CACHE.setdefault((workload, M), {})
     cacheable = wl.step_weight_bytes(mats, fmt) < 2e9
     for mi, m in order:
         if mi in cache:
-            X, A, B = cache[mi]
+            X, A, B, Z = cache[mi]
         else:
-            X = gen.bf16_activations(0, mi, 1, m.K)
+            X = gen.bf16_activations(0, mi, M, m.K)
+            Z = None
             if fmt == wl.FMT_INT4_G64:
                 A, B = gen.int4_codes(0, mi, m.N, m.K), gen.f16_group_scales(0, mi, m.N, m.K // 64)
+            elif fmt == wl.FMT_INT4_AWQ_G128:
+                G = m.K // 128
+                A, B = gen.int4_codes(0, mi, m.N, m.K), gen.f16_group_scales(0, mi, m.N, G)
+                Z = gen.u4_zero_points(0, mi, m.N, G)
             else:
                 A, B = gen.bf16_weights(0, mi, m.N, m.K), None
             if cacheable:
-                cache[mi] = (X, A, B)
+                cache[mi] = (X, A, B, Z)
         t = time.perf_counter()
         if fmt == wl.FMT_INT4_G64:
             o.gemm_int4_g64(A, B, X)
+        elif fmt == wl.FMT_INT4_AWQ_G128:
+            o.gemm_int4_awq_g128(A, B, Z, X)
         else:
             o.gemm_bf16(A, X)
         spent += time.perf_counter() - t
-        done_bytes += wl.bytes_alg(fmt, 1, m.N, m.K)
+        done_bytes += wl.bytes_alg(fmt, M, m.N, m.K)
         n += 1
         if spent >= budget_s:
             break
@@ -283,11 +319,11 @@ def run_reference(args, rank, ws):
         return
     per_step = max(0.5, 20.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        cpu_baseline(args.workload, budget_s=per_step)
+        cpu_baseline(args.workload, budget_s=per_step, M=args.batch)
     t0 = time.perf_counter()
     vals = []
     for _ in range(args.steps):
-        vals.append(cpu_baseline(args.workload, budget_s=per_step))
+        vals.append(cpu_baseline(args.workload, budget_s=per_step, M=args.batch))
     elapsed = time.perf_counter() - t0
     v = statistics.median(r["value"] for r in vals)
     cb = dict(vals[0])
@@ -297,11 +333,13 @@ def run_reference(args, rank, ws):
     step_bytes = wl.step_bytes_alg(*{"tinyllama_int4": (wl.tinyllama_step(fused=True), wl.FMT_INT4_G64),
                                      "tinyllama_int4_unfused": (wl.tinyllama_step(), wl.FMT_INT4_G64),
                                      "qwen_bf16": (wl.qwen25_7b_step(), wl.FMT_BF16),
-                                     "bf16_2048": ([wl.Mat("c", 2048, 2048)] * 64, wl.FMT_BF16)}[args.workload])
+                                     "qwen_awq": (wl.qwen25_7b_step(), wl.FMT_INT4_AWQ_G128),
+                                     "bf16_2048": ([wl.Mat("c", 2048, 2048)] * 64, wl.FMT_BF16)}[args.workload],
+                                   args.batch)
     line = {"impl": "reference", "metric": metric_name(args.workload), "value": v, "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_bytes / (v * 1e9) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(args.workload)}, "cpu_baseline": cb,
+            "config": {"workload": workload_desc(args.workload, args.batch)}, "cpu_baseline": cb,
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -310,11 +348,13 @@ def metric_name(workload):
     return "decode GEMV achieved HBM GB/s (% of GB300 peak); weight-stream ms/token"
 
 
-def workload_desc(workload):
+def workload_desc(workload, batch=1):
     return {"tinyllama_int4": "TinyLlama-1.1B-shaped INT4 group-64 decode step, batch 1, q/k/v and gate/up fused "
                               "(89 GEMVs)",
             "tinyllama_int4_unfused": "TinyLlama-1.1B-shaped INT4 group-64 decode step, batch 1 (155 GEMVs)",
             "qwen_bf16": "Qwen2.5-7B-shaped BF16 decode step, batch 1 (141 GEMVs)",
+            "qwen_awq": f"Qwen2.5-7B-shaped AWQ-style INT4 decode step (group 128, fp16 scale, uint4 zero point, LM head "
+                        f"included), batch {batch} (141 GEMMs)",
             "bf16_2048": "BF16 GEMV 2048x2048, batch 1, 64 rotating copies"}[workload]
 
 
@@ -341,25 +381,26 @@ def main():
     barrier(ws)
     import memory_bound_weight_gb300 as mbw
 
-    step = make_step(args.workload, seed=0, device=device)
+    step = make_step(args.workload, seed=0, device=device, M=args.batch)
+    Mb = step.M
     if args.plans_from:
         with open(args.plans_from) as f:
             saved = json.load(f)
         for N, K in step.shapes():
-            mbw.plan_select(step.op, 1, N, K, int(saved[f"{N}x{K}"]))
+            mbw.plan_select(step.op, Mb, N, K, int(saved[f"{N}x{K}"]))
     else:
         for N, K in step.shapes():
-            mbw.autotune(step.op, 1, N, K)
+            mbw.autotune(step.op, Mb, N, K)
         if args.tune == "step":
             from memory_bound_weight_gb300.tune import tune_sequence
 
-            res = tune_sequence(step.run, [(step.op, 1, N, K) for N, K in step.shapes()],
+            res = tune_sequence(step.run, [(step.op, Mb, N, K) for N, K in step.shapes()],
                                 log=(lambda m: print("[tune]", m, file=sys.stderr)))
             print(f"[tune] step {res['_ms'][0]:.4f} -> {res['_ms'][1]:.4f} ms", file=sys.stderr)
     if args.plans_out and rank == 0:
         with open(args.plans_out, "w") as f:
-            json.dump({f"{N}x{K}": mbw.plan_index(step.op, 1, N, K) for N, K in step.shapes()}, f)
-    plans = {f"{N}x{K}": mbw.plan_describe(step.op, 1, N, K) for N, K in step.shapes()}
+            json.dump({f"{N}x{K}": mbw.plan_index(step.op, Mb, N, K) for N, K in step.shapes()}, f)
+    plans = {f"{N}x{K}": mbw.plan_describe(step.op, Mb, N, K) for N, K in step.shapes()}
     step.run()
     torch.cuda.synchronize()
 
@@ -442,7 +483,7 @@ def main():
         return
     cb = None
     if ws == 1 and not args.no_cpu_baseline:
-        cb = cpu_baseline(args.workload)
+        cb = cpu_baseline(args.workload, M=step.M)
     line = {
         "metric": metric_name(args.workload),
         "value": value,
@@ -456,19 +497,13 @@ def main():
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": workload_desc(args.workload), "matrices": len(step.mats),
-                   "bytes_alg_per_step": step.bytes_alg, "batch": 1, "parallelism": f"replicas{ws}",
+        "config": {"workload": workload_desc(args.workload, step.M), "matrices": len(step.mats),
+                   "bytes_alg_per_step": step.bytes_alg, "batch": step.M, "parallelism": f"replicas{ws}",
                    "l2": "inputs larger than L2: each step streams %.3f GB of distinct weights" % (step.bytes_alg / 1e9),
                    "plans": plans},
         "weight_stream_ms_per_token": ms_step,
         "frac_of_peak": gbs_rank / peak,
-        "roofline": {"bound": "hbm", "achieved": gbs_rank, "peak": peak, "unit": "GB/s", "frac": gbs_rank / peak,
-                     "traffic": traffic, "peak_source": peak_src,
-                     "kernel": "libmbw GEMV launches of the step (plan per shape: %s)" % "; ".join(
-                         f"{k}: {v.split(' ')[0]}" for k, v in plans.items()),
-                     "note": "every launch in the timed region is one of this library's GEMV kernels (%d per "
-                             "step); achieved = algorithmic bytes per launch / (timed region / launches), launch "
-                             "gaps included; per-shape steady-state numbers are in per_matrix" % launches_per_step},
+        "roofline": roofline_fields(step, ms_step, gbs_rank, peak, peak_src, traffic, plans, launches_per_step),
         "cpu_baseline": cb,
         "e2e": e2e,
         "clocks": clocks,
@@ -481,11 +516,38 @@ def main():
     print(json.dumps(line), flush=True)
 
 
+def roofline_fields(step, ms_step, gbs, peak, peak_src, traffic, plans, launches_per_step):
+    """HBM roofline of the step's GEMV launches; with a batch, the tensor-core
+    roofline too, and the one whose time is longer is the bound."""
+    kernel = "libmbw launches of the step (plan per shape: %s)" % "; ".join(
+        f"{k}: {v.split(' ')[0]}" for k, v in plans.items())
+    note = ("every launch in the timed region is one of this library's kernels (%d per step); achieved = "
+            "algorithmic bytes (or flops) per launch / (timed region / launches), launch gaps included; "
+            "per-shape steady-state numbers are in per_matrix" % launches_per_step)
+    r = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak, "traffic": traffic,
+         "peak_source": peak_src, "kernel": kernel, "note": note}
+    if step.M > 1:
+        tc, tc_src = tensor_peak()
+        tflops = step.flops / (ms_step * 1e-3) / 1e12
+        t_hbm = step.bytes_alg / (peak * 1e9)
+        t_tc = step.flops / (tc * 1e12)
+        r["hbm_frac"] = gbs / peak
+        r["tensor_frac"] = tflops / tc
+        r["tensor_peak"] = tc
+        r["tensor_peak_source"] = tc_src
+        if t_tc > t_hbm:
+            r.update({"bound": "tensor", "achieved": tflops, "peak": tc, "unit": "TFLOP/s", "frac": tflops / tc,
+                      "peak_source": tc_src})
+    return r
+
+
 def named_shapes(fmt):
     """The shapes the per-matrix figures are quoted on, besides the step's own:
     tinyinfer's four TinyLlama INT4 matrices, and the 2048x2048 BF16 GEMV."""
     if fmt == wl.FMT_INT4_G64:
         return [(m.N, m.K) for m in wl.TINYLLAMA_TABLE_SHAPES]
+    if fmt == wl.FMT_INT4_AWQ_G128:
+        return [(m.N, m.K) for m in wl.SKINNY_SHAPES]
     return [(2048, 2048)]
 
 
@@ -503,22 +565,29 @@ def time_per_shape(step, device, reps=5):
     peak, _ = hbm_peak()
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     shapes = sorted(set(step.shapes()) | set(named_shapes(step.fmt)))
+    M = step.M
     for N, K in shapes:
-        b = wl.bytes_alg(step.fmt, 1, N, K)
+        b = wl.bytes_alg(step.fmt, M, N, K)
         copies = int(min(512, max(8, -(-4 * l2 // b))))
-        x = torch.empty((copies, K), dtype=torch.bfloat16, device=device)
-        y = torch.empty((copies, N), dtype=torch.bfloat16, device=device)
+        x = torch.empty((copies, M, K), dtype=torch.bfloat16, device=device)
+        y = torch.empty((copies, M, N), dtype=torch.bfloat16, device=device)
         inputs_gpu.bf16_normal_(x.view(-1), 0, 7, 1.0)
         calls = []
         for i in range(copies):
+            xi, yi = (x[i, 0], y[i, 0]) if M == 1 else (x[i], y[i])
             if step.fmt == wl.FMT_INT4_G64:
                 c = inputs_gpu.int4_codes(0, 1000 + i, N, K, device)
                 sc = inputs_gpu.f16_group_scales(0, 1000 + i, N, K // 64, device)
-                calls.append((mbw.gemv_int4_g64, (c, sc, x[i]), y[i]))
+                calls.append((mbw.gemv_int4_g64, (c, sc, xi), yi))
+            elif step.fmt == wl.FMT_INT4_AWQ_G128:
+                c = inputs_gpu.int4_codes(0, 1000 + i, N, K, device)
+                sc = inputs_gpu.f16_group_scales(0, 1000 + i, N, K // 128, device)
+                z = inputs_gpu.u4_zero_points(0, 1000 + i, N, K // 128, device)
+                calls.append((mbw.gemv_int4_awq_g128, (c, sc, z, xi), yi))
             else:
                 W = inputs_gpu.bf16_weights(0, 1000 + i, N, K, device)
-                calls.append((mbw.gemv_bf16, (W, x[i]), y[i]))
-        mbw.autotune(step.op, 1, N, K)
+                calls.append((mbw.gemv_bf16, (W, xi), yi))
+        mbw.autotune(step.op, M, N, K)
         for fn, a, o in calls:
             fn(*a, out=o)
         torch.cuda.synchronize()
@@ -541,7 +610,8 @@ def time_per_shape(step, device, reps=5):
             ts.append(e0.elapsed_time(e1) / copies)
         us = statistics.median(ts) * 1e3
         out[f"{N}x{K}"] = {"us": us, "GB/s": b / (us * 1e-6) / 1e9, "frac": b / (us * 1e-6) / 1e9 / peak,
-                           "copies": copies, "plan": mbw.plan_describe(step.op, 1, N, K)}
+                           "TFLOP/s": wl.flops(M, N, K) / (us * 1e-6) / 1e12,
+                           "copies": copies, "plan": mbw.plan_describe(step.op, M, N, K)}
         del calls, g
         torch.cuda.empty_cache()
     return out

@@ -93,11 +93,39 @@ __host__ __device__ constexpr uint32_t tc_idesc(int m, int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-template <int NT>  // batch tile (MMA N): 16 .. 256, multiple of 16
+// INT4 helpers of the AWQ path: the nibbles at bits 0-3 and 16-19 of v as the
+// bf16 pair (128 + n_lo, 128 + n_hi); an exact bf16x2 subtract; the x chunk
+// permutation (0,4) (1,5) (2,6) (3,7) that matches the unpack's k order.
+__device__ __forceinline__ uint32_t tc_nib(uint32_t v) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(0x000F000Fu), "r"(0x43004300u));
+    return r;
+}
+__device__ __forceinline__ uint32_t tc_sub(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint4 tc_perm(uint4 v) {
+    uint4 o;
+    o.x = __byte_perm(v.x, v.z, 0x5410);
+    o.y = __byte_perm(v.x, v.z, 0x7632);
+    o.z = __byte_perm(v.y, v.w, 0x5410);
+    o.w = __byte_perm(v.y, v.w, 0x7632);
+    return o;
+}
+
+// NT: batch tile (MMA N), 16 .. 256, multiple of 16. C: independent TMEM
+// accumulators the k-steps rotate over -- consecutive MMAs into one
+// accumulator wait for each other, so a single chain runs at the MMA latency
+// instead of the tensor pipe's rate; the epilogue adds the C partial sums.
+template <int NT, int C>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX,
                    const TcArgs a, const int S, const int D) {
-    constexpr int TMEM_COLS = NT <= 32 ? 32 : NT <= 64 ? 64 : NT <= 128 ? 128 : 256;
+    constexpr int NTP = NT <= 32 ? 32 : NT <= 64 ? 64 : NT <= 128 ? 128 : 256;  // columns per accumulator
+    constexpr int TMEM_COLS = NTP * C;
+    static_assert(TMEM_COLS <= 512, "");
     constexpr uint32_t A_BYTES = 128 * 128;   // 128 rows x 64 bf16
     constexpr uint32_t B_BYTES = NT * 128;    // NT rows x 64 bf16
     constexpr uint32_t STAGE = A_BYTES + B_BYTES;
@@ -181,12 +209,14 @@ __global__ void __launch_bounds__(192, 1)
                     const uint64_t da = tc_desc(sa), db = tc_desc(sa + A_BYTES);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
+                        const int t = i * 4 + k;  // k-step; accumulator t % C
+                        const uint32_t acc = (t >= C) ? 1u : 0u;
                         // advance 16 k (32 bytes) inside the swizzle atom: +2 in the address field
                         asm volatile(
                             "{\n\t.reg .pred p;\n\t"
                             "setp.ne.b32 p, %4, 0;\n\t"
-                            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+                            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+                                tmem + (uint32_t)((t % C) * NTP)),
                             "l"(da + 2 * k), "l"(db + 2 * k), "r"(idesc), "r"(acc)
                             : "memory");
                     }
@@ -210,19 +240,30 @@ __global__ void __launch_bounds__(192, 1)
         float* part = reinterpret_cast<float*>(smem);  // [NT][128] fp32 partials (ring reused)
 #pragma unroll 1
         for (int c = 0; c < NT; c += 16) {
-            uint32_t v[16];
-            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c;
-            asm volatile(
-                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
-                "[%16];"
-                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                  "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-                  "=r"(v[15])
-                : "r"(taddr));
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            float fs[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) fs[j] = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < C; ++ch) {
+                uint32_t v[16];
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ch * NTP + c);
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+                    "[%16];"
+                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+                      "=r"(v[15])
+                    : "r"(taddr));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                // an accumulator no k-step reached holds no data
+                if (ch < nks * 4) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) fs[j] += __uint_as_float(v[j]);
+                }
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const float f = (ok && nks > 0) ? __uint_as_float(v[j]) : 0.f;
+                const float f = (ok && nks > 0) ? fs[j] : 0.f;
                 const int m = c + j;
                 if (S == 1) {
                     if (a.m0 + m < a.M && row0 + lrow < a.N)
@@ -256,6 +297,358 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
+// ----------------------------------------------------------------------------
+// AWQ-style INT4 (group 128, uint4 zero point, fp16 scale) batched GEMM.
+//
+// Every group of 128 k has its own scale per weight row, so the scale cannot
+// ride inside one exact tensor-core accumulation over K, and folding it into
+// bf16 weights would round them. Here each 128-k stage is one group, and four
+// roles run concurrently, decoupled by mbarriers:
+//   * warp 0 (one thread) streams the packed codes (128 rows x 64 bytes) and
+//     the X tile (two 64-k halves, 128-byte swizzle) with TMA into a deep ring
+//     (the codes are the HBM stream; the ring holds no converted operand);
+//   * warps 2..9 (one thread per weight row and k-half) unpack their row's
+//     codes to exact bf16 (q - z) and store them with tcgen05.st into one of
+//     two A operands held in TMEM (lane = weight row; column c of a 16-k step
+//     = the bf16 pair of k 2c, 2c+1 -- measured), so the 4x wider converted
+//     operand never touches shared memory; they also permute the X tile's
+//     16-byte chunks in place to the same k order (pairs (0,4) (1,5) (2,6)
+//     (3,7), the order the nibble unpack produces); the products are exact
+//     and the tensor core adds in fp32;
+//   * warp 1 (one thread) issues the stage's 8 MMAs (A from TMEM, X from
+//     shared memory) into one of four TMEM accumulators;
+//   * warps 10..13 (one thread per weight row) read each accumulator back,
+//     multiply by the row's fp32 group scale and accumulate in registers.
+// A cluster splits K for short, wide shapes (partials summed through
+// distributed shared memory in rank order). Every wait is bounded; on expiry
+// the kernel records the fault flag and skips the remaining work.
+struct TcAwqArgs {
+    const uint16_t* scales;  // fp16 [N][G]
+    const uint8_t* zeros;    // uint4 [N][zstride], low nibble = even group
+    void* y;
+    int M, N, K, G, zstride;
+    int m0;       // first batch row of this launch
+    int kstages;  // groups per cluster rank
+    int out_f32;
+    const void* xpf;  // the launch's X rows, prefetched into L2 before the wait
+    size_t xpf_bytes;
+};
+
+// A ring slot holds GS groups: the codes of 128 rows x GS*64 bytes as GS/2
+// TMA boxes of 128-byte rows in 128-byte-swizzled atoms (a thread per row
+// then reads its row without bank conflicts), and the X tile of each group
+// (two 64-k halves).
+template <int NT>
+struct TcAwqLayout {
+    static constexpr int GS = 4;                      // groups per ring slot
+    static constexpr uint32_t X_HALF = NT * 128;      // NT rows x 64 bf16 (SW128 atoms)
+    static constexpr uint32_t X_GROUP = 2 * X_HALF;
+    static constexpr uint32_t Q_ROW = GS * 64;        // code bytes of one row per slot
+    static constexpr uint32_t Q_BOX = 128 * 128;      // one box: 128 rows x 2 groups
+    static constexpr uint32_t OFF_Q = GS * X_GROUP;   // inside a ring slot
+    static constexpr uint32_t SLOT = OFF_Q + 128 * Q_ROW;
+    static constexpr uint32_t TX = 128 * Q_ROW + GS * X_GROUP;  // bytes TMA delivers per slot
+    static constexpr int NA = 4;                      // TMEM A operands
+    static constexpr int A_COLS = 64;                 // TMEM columns of one 128-k A operand
+    static constexpr int D_COL0 = NA * A_COLS;        // accumulators follow the A operands
+    // a group's 8 MMAs rotate over C independent accumulators (one chain of
+    // dependent MMAs runs at the MMA latency); NB groups in flight
+    static constexpr int C = (NT == 16) ? 4 : 2;
+    static constexpr int NB = (NT == 64) ? 2 : 4;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(D_COL0 + NB * C * NT <= TMEM_COLS, "");
+};
+
+template <int NT>  // batch tile: 16, 32 or 64
+__global__ void __launch_bounds__(448, 1)
+    gemm_tc_awq_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapX,
+                       const TcAwqArgs a, const int S, const int D) {
+    using L = TcAwqLayout<NT>;
+    constexpr int NB = L::NB;
+    constexpr int TMEM_COLS = L::TMEM_COLS;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    pdl_launch_dependents();
+    prefetch_l2_grid_share(a.xpf, a.xpf_bytes);
+
+    const int rank = (S > 1) ? (int)cg::this_cluster().block_rank() : 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x / S;
+    const int row0 = tile * 128;
+    const int ks0 = rank * a.kstages;
+    const int nks = max(0, min(a.G, ks0 + a.kstages) - ks0);
+
+    constexpr int GS = L::GS, NA = L::NA;
+    uint8_t* ring = smem;
+    uint64_t* qfull = reinterpret_cast<uint64_t*>(ring + (size_t)D * L::SLOT);
+    uint64_t* empty = qfull + D;
+    uint64_t* aready = empty + D;
+    uint64_t* afree = aready + NA;
+    uint64_t* dfull = afree + NA;
+    uint64_t* dempty = dfull + NB;
+    uint64_t* done = dempty + NB;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    // this CTA's scales (fp16) and zero points (one byte each) of its rows and
+    // groups, loaded once: a per-group global load would put an L2 round trip
+    // on every group's critical path
+    uint16_t* s_tab = reinterpret_cast<uint16_t*>(done + 2);               // [kstages][128]
+    uint8_t* z_tab = reinterpret_cast<uint8_t*>(s_tab + 128 * a.kstages);  // [kstages][128]
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < D; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&qfull[s])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&empty[s])));
+        }
+        for (int b = 0; b < NA; ++b) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(tc_smem(&aready[b])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&afree[b])));
+        }
+        for (int b = 0; b < NB; ++b) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&dfull[b])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(tc_smem(&dempty[b])));
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(done)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tc_smem(tmem_slot)),
+                     "n"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // start the code stream before anything else (codes do not depend on the previous kernel)
+        const int npre = min(D, (nks + GS - 1) / GS);
+        for (int j = 0; j < npre; ++j) {
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc_smem(&qfull[j])), "r"(L::TX)
+                         : "memory");
+            for (int q = 0; q < GS / 2; ++q)
+                tc_tma_2d(ring + (size_t)j * L::SLOT + L::OFF_Q + q * L::Q_BOX, &mapQ, (ks0 + j * GS + 2 * q) * 64,
+                          row0, &qfull[j]);
+        }
+    }
+    // The CTA's scale and zero tables, [group][row], loaded by all threads at
+    // once (a per-group load, or a per-thread loop of dependent load/store
+    // pairs, puts an L2 round trip on every group of the critical path).
+    for (int e = threadIdx.x; e < nks * 128; e += 448) {
+        const int i = e >> 7, rr = e & 127;
+        const size_t row = (size_t)min(row0 + rr, a.N - 1);
+        s_tab[i * 128 + rr] = ld_ro_u16(a.scales + row * a.G + ks0 + i);
+        const uint32_t zb = ld_ro_u8(a.zeros + row * a.zstride + ((ks0 + i) >> 1));
+        z_tab[i * 128 + rr] = (uint8_t)(((ks0 + i) & 1) ? (zb >> 4) : (zb & 0xF));
+    }
+    __syncthreads();
+
+    float acc[NT];  // epilogue warps: this row's outputs for the launch's batch columns
+#pragma unroll
+    for (int c = 0; c < NT; ++c) acc[c] = 0.f;
+    bool ok = true;
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer ----
+        if (lane == 0) {
+            // a slot = GS groups; codes do not depend on the previous kernel:
+            // fill the ring with them first, then wait, then add the X tiles
+            const int nslots = (nks + GS - 1) / GS;
+            const int npre = min(D, nslots);  // slots whose codes are already on the way (issued above)
+            auto load_x = [&](uint8_t* st, int j, uint64_t* bar) {
+                for (int g = 0; g < GS; ++g) {
+                    const int kc = (ks0 + j * GS + g) * 128;
+                    tc_tma_2d(st + g * L::X_GROUP, &mapX, kc, a.m0, bar);
+                    tc_tma_2d(st + g * L::X_GROUP + L::X_HALF, &mapX, kc + 64, a.m0, bar);
+                }
+            };
+            pdl_wait();
+            for (int j = 0; j < npre; ++j) load_x(ring + (size_t)j * L::SLOT, j, &qfull[j]);
+            for (int j = npre; j < nslots; ++j) {
+                const int s = j % D;
+                if (!tc_wait(&empty[s], ((j / D) - 1) & 1)) break;
+                uint8_t* st = ring + (size_t)s * L::SLOT;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc_smem(&qfull[s])),
+                             "r"(L::TX)
+                             : "memory");
+                for (int q = 0; q < GS / 2; ++q)
+                    tc_tma_2d(st + L::OFF_Q + q * L::Q_BOX, &mapQ, (ks0 + j * GS + 2 * q) * 64, row0, &qfull[s]);
+                load_x(st, j, &qfull[s]);
+            }
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------- MMA issuer ----
+        if (lane == 0) {
+            const uint32_t idesc = tc_idesc(128, NT);
+            for (int i = 0; i < nks; ++i) {
+                const int j = i / GS, s = j % D, g = i - j * GS, b = i % NB, ab = i % NA;
+                if (ok) ok = tc_wait(&aready[ab], (i / NA) & 1);
+                if (ok && i >= NB) ok = tc_wait(&dempty[b], ((i / NB) - 1) & 1);
+                if (ok) {
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t ta = tmem + (uint32_t)(ab * L::A_COLS);
+                    const uint32_t sx = tc_smem(ring + (size_t)s * L::SLOT + g * L::X_GROUP);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint64_t db = tc_desc(sx + h * L::X_HALF);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int kk = h * 4 + k;  // k-step of the group; accumulator kk % C
+                            const uint32_t accf = (kk >= L::C) ? 1u : 0u;
+                            // A: 8 TMEM columns per 16 k; X: +32 bytes per 16 k inside the swizzle atom
+                            asm volatile(
+                                "{\n\t.reg .pred p;\n\t"
+                                "setp.ne.b32 p, %4, 0;\n\t"
+                                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+                                    tmem + (uint32_t)(L::D_COL0 + (b * L::C + kk % L::C) * NT)),
+                                "r"(ta + (uint32_t)((h * 4 + k) * 8)), "l"(db + 2 * k), "r"(idesc), "r"(accf)
+                                : "memory");
+                        }
+                    }
+                }
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                 tc_smem(&dfull[b]))
+                             : "memory");
+                if (g == GS - 1 || i == nks - 1)
+                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                     tc_smem(&empty[s]))
+                                 : "memory");
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                 tc_smem(&afree[ab]))
+                             : "memory");
+            }
+            // every MMA issued above has completed before TMEM is released
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                             tc_smem(done))
+                         : "memory");
+            tc_wait(done, 0);
+        }
+    } else if (warp < 10) {
+        // ------------------------------------------------------ unpack ----
+        const int cw = warp - 2;            // 0..7
+        const int h = cw >> 2;              // k-half of the group this warp unpacks
+        const int quarter = warp & 3;       // TMEM lanes 32*quarter .. +31 (the warp's accessible quarter)
+        const int r = quarter * 32 + lane;  // weight row of the tile
+        for (int i = 0; i < nks; ++i) {
+            const int j = i / GS, s = j % D, g = i - j * GS, ab = i % NA;
+            const uint32_t zc = z_tab[i * 128 + r];
+            ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&qfull[s], (j / D) & 1));
+            if (i >= NA) ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&afree[ab], ((i / NA) - 1) & 1));
+            // all lanes take part in the (warp-collective) TMEM store
+            uint8_t* st = ring + (size_t)s * L::SLOT;
+            uint32_t av[32];
+            {
+                // row r of box g/2; 16-byte chunk c of the row sits at chunk c ^ (r & 7)
+                const uint8_t* qrow = st + L::OFF_Q + (g >> 1) * L::Q_BOX + r * 128;
+                const int c0 = (g & 1) * 4 + h * 2;
+                uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
+                if (ok) {
+                    q0 = *reinterpret_cast<const uint4*>(qrow + ((c0 ^ (r & 7)) << 4));
+                    q1 = *reinterpret_cast<const uint4*>(qrow + (((c0 + 1) ^ (r & 7)) << 4));
+                }
+                const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                const uint32_t zz = (0x4300u | zc) * 0x00010001u;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    av[4 * c + 0] = tc_sub(tc_nib(wv[c]), zz);
+                    av[4 * c + 1] = tc_sub(tc_nib(wv[c] >> 4), zz);
+                    av[4 * c + 2] = tc_sub(tc_nib(wv[c] >> 8), zz);
+                    av[4 * c + 3] = tc_sub(tc_nib(wv[c] >> 12), zz);
+                }
+            }
+            const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * L::A_COLS + h * 32);
+            asm volatile(
+                "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+                "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(ta),
+                "r"(av[0]), "r"(av[1]), "r"(av[2]), "r"(av[3]), "r"(av[4]), "r"(av[5]), "r"(av[6]), "r"(av[7]),
+                "r"(av[8]), "r"(av[9]), "r"(av[10]), "r"(av[11]), "r"(av[12]), "r"(av[13]), "r"(av[14]),
+                "r"(av[15]), "r"(av[16]), "r"(av[17]), "r"(av[18]), "r"(av[19]), "r"(av[20]), "r"(av[21]),
+                "r"(av[22]), "r"(av[23]), "r"(av[24]), "r"(av[25]), "r"(av[26]), "r"(av[27]), "r"(av[28]),
+                "r"(av[29]), "r"(av[30]), "r"(av[31])
+                : "memory");
+            if (ok) {
+                uint4* xs = reinterpret_cast<uint4*>(st + g * L::X_GROUP);
+                for (int c = cw * 32 + lane; c < NT * 16; c += 256) xs[c] = tc_perm(xs[c]);
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc_smem(&aready[ab])) : "memory");
+        }
+    } else {
+        // ---------------------------------------------------- read back ----
+        const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+        const int r = quarter * 32 + lane;     // weight row of the tile
+        for (int j = 0; j < nks; ++j) {
+            const int b = j % NB;
+            const float sc = f16_bits_to_f32(s_tab[j * 128 + r]);
+            ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&dfull[b], (j / NB) & 1));
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+            for (int cc = 0; cc < NT; cc += 8) {
+                float gsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ch = 0; ch < L::C; ++ch) {
+                    uint32_t v[8];
+                    const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) +
+                                           (uint32_t)(L::D_COL0 + (b * L::C + ch) * NT + cc);
+                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                                   "=r"(v[7])
+                                 : "r"(taddr));
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) gsum[jj] += __uint_as_float(v[jj]);
+                }
+                // the group's partial sum, scaled once by the row's group scale
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) acc[cc + jj] = fmaf(sc, gsum[jj], acc[cc + jj]);
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc_smem(&dempty[b])) : "memory");
+        }
+        if (S == 1) {
+            // rows are the fast index of the stores: a warp writes 32 consecutive outputs per batch row
+#pragma unroll
+            for (int c = 0; c < NT; ++c) {
+                const int m = a.m0 + c;
+                if (m < a.M && row0 + r < a.N) store_out(a.y, (int64_t)m * a.N + row0 + r, ok ? acc[c] : 0.f, a.out_f32);
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+
+    if (S > 1) {
+        // every accumulator has been read back and every MMA is done: the ring is free for the partials
+        float* part = reinterpret_cast<float*>(smem);  // [NT][128]
+        if (warp >= 10) {
+            const int r = (warp & 3) * 32 + lane;
+#pragma unroll
+            for (int c = 0; c < NT; ++c) part[c * 128 + r] = ok ? acc[c] : 0.f;
+        }
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        const int total = NT * 128;
+        const int lo = rank * total / S, hi = (rank + 1) * total / S;
+        for (int e = lo + (int)threadIdx.x; e < hi; e += 448) {
+            const int m = e / 128, rr = e % 128;
+            float v = 0.f;
+            for (int s2 = 0; s2 < S; ++s2) v += *cluster.map_shared_rank(part + e, s2);
+            if (a.m0 + m < a.M && row0 + rr < a.N)
+                store_out(a.y, (int64_t)(a.m0 + m) * a.N + row0 + rr, v, a.out_f32);
+        }
+        cluster.sync();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(TMEM_COLS));
+    }
+}
+
 // ------------------------------------------------------------ host side ----
 // The tensor-map encoder lives in the driver; it is looked up through the
 // runtime at first use, so libmbw.so has no link-time dependency on libcuda.
@@ -274,17 +667,24 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-static bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                      uint32_t box_outer) {
+static bool encode_2d_typed(CUtensorMap* map, CUtensorMapDataType dt, uint32_t esize, const void* base,
+                            uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                            CUtensorMapSwizzle swz) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint64_t strides[1] = {inner * esize};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 [outer][inner] operand, 128-byte swizzle
+static bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                      uint32_t box_outer) {
+    return encode_2d_typed(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, outer, box_inner, box_outer,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 int tc_batch_tile(int64_t M) {
@@ -318,12 +718,13 @@ size_t tc_smem_bytes(int nt, int D, int split) {
     return 1024 + ring + (size_t)(2 * D + 1) * 8 + 16;
 }
 
-template <int NT>
+template <int NT, int C>
 static cudaError_t launch_nt(const CUtensorMap& mw, const CUtensorMap& mx, const TcArgs& a, int split, int ring,
                              int tiles, cudaStream_t s) {
     const int D = tc_stages(NT, ring);
     const size_t smem = tc_smem_bytes(NT, D, split);
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_kernel<NT, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(tiles * split), 1, 1);
@@ -345,7 +746,7 @@ static cudaError_t launch_nt(const CUtensorMap& mw, const CUtensorMap& mx, const
     cfg.attrs = attrs;
     cfg.numAttrs = na;
     count_launch();
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NT>, mw, mx, a, split, D);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NT, C>, mw, mx, a, split, D);
 }
 
 // Y[M][N] = X[M][K] . W[N][K]^T, bf16, in batch slices of up to 256 rows.
@@ -372,11 +773,119 @@ cudaError_t launch_gemm_tc(const uint16_t* X, const uint16_t* W, void* Y, int64_
         a.xpf_bytes = (size_t)((M - m0 < 256) ? (M - m0) : 256) * (size_t)K * 2;
         cudaError_t e;
         switch (nt) {
-            case 16: e = launch_nt<16>(mw, mx, a, split, ring, tiles, s); break;
-            case 32: e = launch_nt<32>(mw, mx, a, split, ring, tiles, s); break;
-            case 64: e = launch_nt<64>(mw, mx, a, split, ring, tiles, s); break;
-            case 128: e = launch_nt<128>(mw, mx, a, split, ring, tiles, s); break;
-            default: e = launch_nt<256>(mw, mx, a, split, ring, tiles, s); break;
+            // accumulator chains: all of TMEM with one CTA per SM (deep ring),
+            // half of it when the next launch's CTA shares the SM
+            case 16: e = launch_nt<16, 4>(mw, mx, a, split, ring, tiles, s); break;
+            case 32: e = launch_nt<32, 4>(mw, mx, a, split, ring, tiles, s); break;
+            case 64: e = ring == 0 ? launch_nt<64, 4>(mw, mx, a, split, ring, tiles, s)
+                                   : launch_nt<64, 2>(mw, mx, a, split, ring, tiles, s); break;
+            case 128: e = ring == 0 ? launch_nt<128, 4>(mw, mx, a, split, ring, tiles, s)
+                                    : launch_nt<128, 2>(mw, mx, a, split, ring, tiles, s); break;
+            default: e = ring == 0 ? launch_nt<256, 2>(mw, mx, a, split, ring, tiles, s)
+                                   : launch_nt<256, 1>(mw, mx, a, split, ring, tiles, s); break;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+// AWQ batch tile for a call of M rows (a launch covers up to 64 of them).
+int tc_awq_batch_tile(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
+
+// bytes after the ring: barriers, TMEM slot, then the scale and zero tables
+template <int NT>
+static size_t tc_awq_tail_bytes(int kstages) {
+    using L = TcAwqLayout<NT>;
+    return (size_t)(2 * 8 + 2 * L::NA + 2 * L::NB + 2) * 8 + (size_t)128 * kstages * 3 + 16;
+}
+
+template <int NT>
+static int tc_awq_stages(int kstages) {  // ring slots (of GS groups each); 0 if the tables leave no room
+    const size_t budget = 210 * 1024;
+    const size_t tail = tc_awq_tail_bytes<NT>(kstages);
+    if (tail + 2 * TcAwqLayout<NT>::SLOT > budget) return 0;
+    int d = (int)((budget - tail) / TcAwqLayout<NT>::SLOT);
+    return d > 8 ? 8 : d;
+}
+
+// Whether a K split leaves room for the per-CTA scale and zero tables.
+bool tc_awq_fits(int64_t M, int64_t K, int split) {
+    const int G = (int)(K / 128);
+    const int gs = TcAwqLayout<16>::GS;
+    if (split < 1) split = 1;
+    const int kst = ((G + split - 1) / split + gs - 1) / gs * gs;
+    const int nt = tc_awq_batch_tile(M);
+    return (nt == 16 ? tc_awq_stages<16>(kst) : nt == 32 ? tc_awq_stages<32>(kst) : tc_awq_stages<64>(kst)) >= 2;
+}
+
+template <int NT>
+static cudaError_t launch_awq_nt(const CUtensorMap& mq, const CUtensorMap& mx, const TcAwqArgs& a, int split,
+                                 int tiles, cudaStream_t s) {
+    const int D = tc_awq_stages<NT>(a.kstages);
+    if (D < 2) return cudaErrorInvalidValue;
+    const size_t smem = 1024 + (size_t)D * TcAwqLayout<NT>::SLOT + tc_awq_tail_bytes<NT>(a.kstages);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_awq_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(tiles * split), 1, 1);
+    cfg.blockDim = dim3(448, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (split > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)split;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    count_launch();
+    return cudaLaunchKernelEx(&cfg, gemm_tc_awq_kernel<NT>, mq, mx, a, split, D);
+}
+
+// Y[M][N] = X[M][K] . dequant(W)^T for AWQ-style INT4 weights, in batch
+// slices of up to 64 rows; K split over a cluster of `split` CTAs.
+cudaError_t launch_gemm_tc_awq(const uint8_t* Q, const uint16_t* scales, const uint8_t* zeros, const uint16_t* X,
+                               void* Y, int64_t M, int64_t N, int64_t K, int split, int out_f32, cudaStream_t s) {
+    const int nt = tc_awq_batch_tile(M);
+    CUtensorMap mq, mx;
+    if (!encode_2d_typed(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Q, (uint64_t)(K / 2), (uint64_t)N, 128, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (!encode_2d(&mx, X, (uint64_t)K, (uint64_t)M, 64, (uint32_t)nt)) return cudaErrorInvalidValue;
+    const int tiles = (int)((N + 127) / 128);
+    const int G = (int)(K / 128);
+    if (split < 1) split = 1;
+    if (split > G) split = G;
+    TcAwqArgs a;
+    a.scales = scales;
+    a.zeros = zeros;
+    a.y = Y;
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.G = G;
+    a.zstride = (G + 1) / 2;
+    // whole ring slots per cluster rank (only the last rank may end inside one)
+    const int gs = TcAwqLayout<16>::GS;
+    a.kstages = ((G + split - 1) / split + gs - 1) / gs * gs;
+    a.out_f32 = out_f32;
+    for (int64_t m0 = 0; m0 < M; m0 += 64) {
+        a.m0 = (int)m0;
+        a.xpf = X + m0 * K;
+        a.xpf_bytes = (size_t)((M - m0 < 64) ? (M - m0) : 64) * (size_t)K * 2;
+        cudaError_t e;
+        switch (nt) {
+            case 16: e = launch_awq_nt<16>(mq, mx, a, split, tiles, s); break;
+            case 32: e = launch_awq_nt<32>(mq, mx, a, split, tiles, s); break;
+            default: e = launch_awq_nt<64>(mq, mx, a, split, tiles, s); break;
         }
         if (e != cudaSuccess) return e;
     }

@@ -104,6 +104,11 @@ cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStrea
 cudaError_t launch_gemm_tc(const uint16_t* X, const uint16_t* W, void* Y, int64_t M, int64_t N, int64_t K, int split,
                            int ring, int out_f32, cudaStream_t s);
 int tc_batch_tile(int64_t M);
+// tcgen05 AWQ-style INT4 batched GEMM (gemm_tc.cu): whole batch M, slices of 64.
+cudaError_t launch_gemm_tc_awq(const uint8_t* Q, const uint16_t* scales, const uint8_t* zeros, const uint16_t* X,
+                               void* Y, int64_t M, int64_t N, int64_t K, int split, int out_f32, cudaStream_t s);
+int tc_awq_batch_tile(int64_t M);
+bool tc_awq_fits(int64_t M, int64_t K, int split);  // the split leaves room for the scale/zero tables
 int tc_take_fault();
 
 // Bulk-copy-fed kernel tables (gemv_tma.cu).

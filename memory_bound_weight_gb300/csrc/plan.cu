@@ -52,6 +52,7 @@ static int simt_want_mb(int64_t M) { return M <= 2 ? (int)M : M <= 4 ? 4 : 8; }
 
 static int batch_key(int op, int64_t M) {
     if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 8) return tc_batch_tile(M);
+    if (op == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4) return 1000 + tc_awq_batch_tile(M);
     return (int)std::min<int64_t>(M, 8);
 }
 
@@ -73,6 +74,13 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K) 
     if (p.split < 1 || p.split > 8) return false;
     if (p.kind == PLAN_TC) {
         // tensor-core skinny GEMM: BF16, batches above the GEMV column width
+        if (fmt == FMT_AWQ) {
+            // AWQ tensor-core GEMM: batches above the GEMV column width, one 128-k group per stage
+            const int64_t G = K / 128;
+            if (M <= 4 || K % 128 != 0 || p.cfg != 0 || p.occ != 1 || p.split > G) return false;
+            const int64_t per = ((G + p.split - 1) / p.split + 3) / 4 * 4;  // whole 4-group ring slots per rank
+            return per * (p.split - 1) < G && tc_awq_fits(M, K, p.split);
+        }
         const int64_t KS = (K + 63) / 64;
         if (fmt != FMT_BF16 || M <= 8 || p.cfg < 0 || p.cfg > 1 || p.occ != 1) return false;
         if (p.split > KS) return false;
@@ -138,6 +146,11 @@ static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
     std::vector<Plan> out;
     const int fmt = fmt_of_op(op);
     const int64_t Mb = std::min<int64_t>(M, 8);
+    if (op == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4)
+        for (int sp = 1; sp <= 8; ++sp) {
+            Plan p{PLAN_TC, 0, sp, 1};
+            if (plan_valid(fmt, p, M, N, K)) out.push_back(p);
+        }
     if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 8)
         for (int ring = 0; ring <= 1; ++ring)
             for (int sp = 1; sp <= 8; ++sp) {
@@ -181,7 +194,7 @@ Plan plan_default(int op, int64_t M, int64_t N, int64_t K) {
     const int fmt = fmt_of_op(op);
     const int64_t Mb = std::min<int64_t>(M, 8);
     const int sms = device_sm_count();
-    if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 8) {
+    if ((op == MBW_OP_GEMM_SKINNY_BF16 && M > 8) || (op == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4)) {
         // tcgen05 tiles of 128 weight rows; split K over a cluster until the
         // tiles cover the SMs
         const int64_t tiles = (N + 127) / 128;
@@ -242,8 +255,11 @@ std::string plan_to_string(int op, const Plan& p) {
     const char* fs = fmt == FMT_BF16 ? "bf16" : fmt == FMT_G64 ? "int4_g64" : "int4_awq_g128";
     char buf[192];
     if (p.kind == PLAN_TC) {
-        snprintf(buf, sizeof(buf), "tcgen05 fmt=%s tile=128xbatch k_stage=64 ring=%s split_k=%d", fs,
-                 p.cfg == 0 ? "deep" : "shared_sm", p.split);
+        if (fmt == FMT_AWQ)
+            snprintf(buf, sizeof(buf), "tcgen05 fmt=%s tile=128xbatch k_stage=128 (one group) split_k=%d", fs, p.split);
+        else
+            snprintf(buf, sizeof(buf), "tcgen05 fmt=%s tile=128xbatch k_stage=64 ring=%s split_k=%d", fs,
+                     p.cfg == 0 ? "deep" : "shared_sm", p.split);
     } else if (p.kind == PLAN_LAT) {
         const LatConfig c = lat_config(fmt, p.cfg);
         snprintf(buf, sizeof(buf),
@@ -272,6 +288,8 @@ std::string plan_to_string(int op, const Plan& p) {
 }
 
 cudaError_t launch_plan(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
+    if (p.kind == PLAN_TC && fmt == FMT_AWQ)
+        return launch_gemm_tc_awq(a.W, a.scales, a.zeros, a.x, a.y, a.M, a.N, a.K, p.split, a.out_f32, s);
     if (p.kind == PLAN_TC) return launch_gemm_tc(a.x, (const uint16_t*)a.W, a.y, a.M, a.N, a.K, p.split, p.cfg, a.out_f32, s);
     if (p.kind == PLAN_MMA2) return launch_gemv_mma2(fmt, p, a, s);
     if (p.kind == PLAN_LAT) return launch_gemv_lat(fmt, p, a, s);
@@ -363,7 +381,9 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
         return MBW_ERR_CUDA;
     }
     const int fmt = fmt_of_op(op);
-    const int64_t Mb = (op == MBW_OP_GEMM_SKINNY_BF16) ? M : std::min<int64_t>(M, 8);
+    // candidates are timed at the call's batch (a GEMV plan narrower than M
+    // is launched once per batch slice, as the call would)
+    const int64_t Mb = M;
     const size_t wb = weight_bytes(fmt, N, K);
     const size_t wstride = (wb + 255) / 256 * 256;
     const size_t target = (size_t)384 << 20;  // about three times the L2

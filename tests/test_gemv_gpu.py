@@ -319,3 +319,59 @@ def test_int4_g64_every_plan_at_step_shapes(orc, N, K):
     for i, desc in each_plan(mbw.OP_GEMV_INT4_G64, 1, N, K):
         y = mbw.gemv_int4_g64(cd, sd, xd[0])
         assert_parity(y[sel], Y[0], A[0], f"g64 {N}x{K} plan {desc}")
+
+
+# ------------------------------------------ AWQ batched tensor-core path ----
+@pytest.mark.parametrize("N,K,M", [(130, 256, 16), (128, 384, 5), (300, 1024, 33), (64, 3584, 64),
+                                   (257, 512, 100), (40, 1280, 17), (200, 640, 130)])
+def test_int4_awq_batched_all_plans(orc, N, K, M):
+    c, s, z, X = awq_case(800 + M, N, K, M)
+    Y, A = orc.gemm_int4_awq_g128(c, s, z, X)
+    cd, sd, zd, Xd = dev_u8(c), dev_f16(s), dev_u8(z), dev_bf16(X)
+    seen_tc = False
+    for i, desc in each_plan(mbw.OP_GEMV_INT4_AWQ_G128, M, N, K):
+        seen_tc |= desc.startswith("tcgen05")
+        y = mbw.gemv_int4_awq_g128(cd, sd, zd, Xd)
+        assert_parity(y, Y, A, f"awq {M}x{N}x{K} plan {desc}")
+    assert seen_tc
+
+
+def test_int4_awq_batched_one_hot_rows_exact(orc):
+    """Batch row m = e_{k_m}: with fp32 output every tensor-core plan returns
+    column k_m of the dequantized weights exactly (exact unpack, exact
+    products, the group scale applied in fp32 to a single nonzero term)."""
+    N, K, M = 200, 1024, 24
+    c, s, z, _ = awq_case(811, N, K, 1)
+    deq = orc.dequant_int4_awq_g128(c, s, z, N, K)
+    ks = [(37 * m + 5) % K for m in range(M)]
+    X = np.zeros((M, K), dtype=np.uint16)
+    for m, k in enumerate(ks):
+        X[m, k] = 0x3F80
+    cd, sd, zd, Xd = dev_u8(c), dev_f16(s), dev_u8(z), dev_bf16(X)
+    for i, desc in each_plan(mbw.OP_GEMV_INT4_AWQ_G128, M, N, K):
+        if not desc.startswith("tcgen05"):
+            continue
+        with mbw.output_fp32():
+            y = mbw.gemv_int4_awq_g128(cd, sd, zd, Xd)
+        got = host_f64(y)
+        for m, k in enumerate(ks):
+            assert np.array_equal(got[m], deq[:, k]), (desc, m, k)
+
+
+@pytest.mark.parametrize("M", [16, 64])
+@pytest.mark.parametrize("N,K", [(18944, 3584), (3584, 18944)])
+def test_int4_awq_batched_config_shapes_sampled_rows(orc, M, N, K):
+    G = K // 128
+    rows = np.unique(np.concatenate([np.arange(0, 8), np.arange(N - 8, N),
+                                     np.random.default_rng(N + M).integers(0, N, 48)]))
+    cd = inputs_gpu.int4_codes(0, 21, N, K)
+    sd = inputs_gpu.f16_group_scales(0, 21, N, G)
+    zd = inputs_gpu.u4_zero_points(0, 21, N, G)
+    Xd = inputs_gpu.bf16_activations(0, 22, M, K)
+    Y = mbw.gemv_int4_awq_g128(cd, sd, zd, Xd)
+    assert mbw.plan_describe(mbw.OP_GEMV_INT4_AWQ_G128, M, N, K).startswith("tcgen05")
+    c = np.stack([gen.int4_codes(0, 21, N, K, row0=int(r), rows=1)[0] for r in rows])
+    s = np.stack([gen.f16_group_scales(0, 21, N, G, row0=int(r), rows=1)[0] for r in rows])
+    z = np.stack([gen.u4_zero_points(0, 21, N, G, row0=int(r), rows=1)[0] for r in rows])
+    Yr, Ar = orc.gemm_int4_awq_g128(c, s, z, host_bits16(Xd))
+    assert_parity(Y[:, torch.from_numpy(rows).cuda()], Yr, Ar, f"awq M={M} {N}x{K} sampled")
