@@ -40,9 +40,14 @@ from memory_bound_weight_gb300 import workloads as wl  # noqa: E402
 FALLBACK_HBM_GBS = 6778.3  # the machine's measured copy bandwidth, recorded copy
 FALLBACK_BF16_TFLOPS = 1752.2  # the pool's measured sustained cuBLAS bf16, recorded copy
 # DRAM bytes (read + write) per launch of the step's dominant kernel from one
-# ncu capture, keyed by the sha256 of the kernel source it was taken on; a
-# changed kernel gets traffic = null until it is captured again.
-TRAFFIC = {}
+# ncu capture, keyed by (kernel source sha, shape); a changed kernel gets
+# traffic = null until it is captured again.
+TRAFFIC = {
+    # gemv_lat on the fused gate_up matrices (INT4 g64, 11264x2048): ncu --set full,
+    # 2 launches, dram__bytes_read.sum 12,322,048 + dram__bytes_write.sum 0 per launch
+    # (profiles/gemv_lat_int4_g64_11264x2048.md)
+    ("65175de089367b3b", "11264x2048"): 12322048,
+}
 
 
 def parse_args():
@@ -58,6 +63,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--per-matrix", action="store_true", help="also time each distinct shape on its own")
+    p.add_argument("--no-shape-timing", action="store_true",
+                   help="skip the per-shape timing behind the dominant-kernel roofline (e.g. under a profiler)")
     p.add_argument("--tune", default="step", choices=["step", "shape"],
                    help="step: per-shape autotune, then refine the plans on the whole step graph (default); "
                         "shape: per-shape autotune only")
@@ -174,9 +181,14 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "window": window}
 
 
-def kernel_source_sha():
+KERNEL_SOURCES = {"lat": ("gemv_lat.cu", "device.cuh"), "mma2": ("gemv_mma.cu", "device.cuh"),
+                  "mma": ("gemv_mma.cu", "device.cuh"), "simt": ("gemv_simt.cu", "device.cuh"),
+                  "tma": ("gemv_tma.cu", "device.cuh"), "tcgen05": ("gemm_tc.cu", "device.cuh")}
+
+
+def kernel_source_sha(family):
     h = hashlib.sha256()
-    for f in ("gemv_simt.cu", "device.cuh"):
+    for f in KERNEL_SOURCES.get(family, ("device.cuh",)):
         with open(os.path.join(ROOT, "memory_bound_weight_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -471,13 +483,28 @@ def main():
                "h2d_bytes_per_step": step.h2d_bytes, "d2h_bytes_per_step": step.d2h_bytes,
                "ms_per_step": ems, "steps": ke}
 
+    # per-shape steady state on the step's own plans: the dominant kernel is
+    # the shape with the largest share of the step (launches x time per launch)
+    step_plans = {(N, K): mbw.plan_index(step.op, Mb, N, K) for N, K in step.shapes()}
+    shape_times = {}
+    if rank == 0 and not args.no_shape_timing:
+        shape_times = time_per_shape(step, device, shapes=step.shapes(), plans=step_plans)
     per_matrix = None
     if args.per_matrix and rank == 0:
-        per_matrix = time_per_shape(step, device)
+        per_matrix = dict(shape_times)
+        per_matrix.update(time_per_shape(step, device, shapes=[sh for sh in named_shapes(step.fmt)
+                                                               if sh not in step_plans]))
 
     peak, peak_src = hbm_peak()
-    sha = kernel_source_sha()
-    traffic = TRAFFIC.get(sha)
+    counts = {}
+    for m in step.mats:
+        counts[(m.N, m.K)] = counts.get((m.N, m.K), 0) + 1
+    dominant = None
+    if shape_times:
+        dominant = max(step.shapes(), key=lambda sh: counts[sh] * shape_times[f"{sh[0]}x{sh[1]}"]["us"])
+    family = plans[f"{dominant[0]}x{dominant[1]}"].split(" ")[0] if dominant else "lat"
+    sha = kernel_source_sha(family)
+    traffic = TRAFFIC.get((sha, f"{dominant[0]}x{dominant[1]}")) if dominant else None
     clocks = sampler.summary(t0, t1)
     if rank != 0:
         return
@@ -503,39 +530,56 @@ def main():
                    "plans": plans},
         "weight_stream_ms_per_token": ms_step,
         "frac_of_peak": gbs_rank / peak,
-        "roofline": roofline_fields(step, ms_step, gbs_rank, peak, peak_src, traffic, plans, launches_per_step),
+        "roofline": roofline_fields(step, ms_step, gbs_rank, peak, peak_src, traffic, plans, launches_per_step,
+                                    dominant, counts, shape_times),
         "cpu_baseline": cb,
         "e2e": e2e,
         "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
         "launches_per_step": launches_per_step,
         "kernel_source_sha": sha,
+        "step_shapes": shape_times,
     }
     if per_matrix:
         line["per_matrix"] = per_matrix
     print(json.dumps(line), flush=True)
 
 
-def roofline_fields(step, ms_step, gbs, peak, peak_src, traffic, plans, launches_per_step):
-    """HBM roofline of the step's GEMV launches; with a batch, the tensor-core
-    roofline too, and the one whose time is longer is the bound."""
-    kernel = "libmbw launches of the step (plan per shape: %s)" % "; ".join(
-        f"{k}: {v.split(' ')[0]}" for k, v in plans.items())
-    note = ("every launch in the timed region is one of this library's kernels (%d per step); achieved = "
-            "algorithmic bytes (or flops) per launch / (timed region / launches), launch gaps included; "
-            "per-shape steady-state numbers are in per_matrix" % launches_per_step)
-    r = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak, "traffic": traffic,
-         "peak_source": peak_src, "kernel": kernel, "note": note}
-    if step.M > 1:
+def roofline_fields(step, ms_step, gbs, peak, peak_src, traffic, plans, launches_per_step, dominant, counts,
+                    shape_times):
+    """Roofline of the step's dominant kernel (the shape with the largest share
+    of the step: launches x steady-state time per launch). achieved = its
+    algorithmic bytes per launch / its average launch duration, timed with
+    CUDA events on the launching stream over a PDL-chained graph of its own
+    launches on the plan the step uses. With a batch, the tensor-core roofline
+    too, and the one whose time is longer is the bound."""
+    if dominant is None:  # not timed (other ranks)
+        return {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                "traffic": traffic, "peak_source": peak_src, "kernel": "step average"}
+    key = f"{dominant[0]}x{dominant[1]}"
+    st = shape_times[key]
+    tot = sum(counts[sh] * shape_times[f"{sh[0]}x{sh[1]}"]["us"] for sh in counts)
+    M = step.M
+    kb = wl.bytes_alg(step.fmt, M, *dominant)
+    kfl = wl.flops(M, *dominant)
+    achieved = kb / (st["us"] * 1e-6) / 1e9
+    r = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+         "traffic": traffic, "peak_source": peak_src,
+         "kernel": f"{plans[key]} on the {key} matrices ({counts[dominant]} per step)",
+         "bytes_alg_per_launch": kb, "us_per_launch": st["us"],
+         "share_of_step": counts[dominant] * st["us"] / tot,
+         "note": "per-launch time of the dominant kernel in a PDL-chained graph of its own launches over distinct "
+                 "weight copies >= 4x L2 (same plan as in the step); the step-level figure is value / "
+                 "frac_of_peak (every launch of the step is one of this library's kernels, %d per step)"
+                 % launches_per_step}
+    if M > 1:
         tc, tc_src = tensor_peak()
-        tflops = step.flops / (ms_step * 1e-3) / 1e12
-        t_hbm = step.bytes_alg / (peak * 1e9)
-        t_tc = step.flops / (tc * 1e12)
-        r["hbm_frac"] = gbs / peak
+        tflops = kfl / (st["us"] * 1e-6) / 1e12
+        r["hbm_frac"] = achieved / peak
         r["tensor_frac"] = tflops / tc
         r["tensor_peak"] = tc
         r["tensor_peak_source"] = tc_src
-        if t_tc > t_hbm:
+        if kfl / (tc * 1e12) > kb / (peak * 1e9):
             r.update({"bound": "tensor", "achieved": tflops, "peak": tc, "unit": "TFLOP/s", "frac": tflops / tc,
                       "peak_source": tc_src})
     return r
@@ -551,7 +595,7 @@ def named_shapes(fmt):
     return [(2048, 2048)]
 
 
-def time_per_shape(step, device, reps=5):
+def time_per_shape(step, device, reps=5, shapes=None, plans=None):
     """Steady-state time per matrix of each shape: a CUDA graph of back-to-back
     launches (programmatic dependent launch, as in the step) over distinct
     copies of the matrix totalling at least 4x the L2, so every launch reads
@@ -564,7 +608,7 @@ def time_per_shape(step, device, reps=5):
     out = {}
     peak, _ = hbm_peak()
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    shapes = sorted(set(step.shapes()) | set(named_shapes(step.fmt)))
+    shapes = sorted(set(step.shapes()) | set(named_shapes(step.fmt))) if shapes is None else list(shapes)
     M = step.M
     for N, K in shapes:
         b = wl.bytes_alg(step.fmt, M, N, K)
@@ -587,7 +631,10 @@ def time_per_shape(step, device, reps=5):
             else:
                 W = inputs_gpu.bf16_weights(0, 1000 + i, N, K, device)
                 calls.append((mbw.gemv_bf16, (W, xi), yi))
-        mbw.autotune(step.op, M, N, K)
+        if plans is not None and (N, K) in plans:
+            mbw.plan_select(step.op, M, N, K, plans[(N, K)])
+        else:
+            mbw.autotune(step.op, M, N, K)
         for fn, a, o in calls:
             fn(*a, out=o)
         torch.cuda.synchronize()
