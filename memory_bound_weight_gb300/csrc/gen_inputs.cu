@@ -54,6 +54,28 @@ __global__ void gen_scales(uint16_t* __restrict__ out, int64_t n, int64_t start,
     }
 }
 
+// int8 from a 65,536-entry code table, 4 values per hash (low 16 bits first).
+__global__ void gen_table8(int8_t* __restrict__ out, int64_t n, int64_t start, uint64_t key,
+                           const int8_t* __restrict__ table) {
+    for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n; j += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t e = start + j;
+        const uint64_t h = splitmix_at(key, (uint64_t)(e >> 2));
+        out[j] = table[(h >> (16 * (e & 3))) & 0xFFFF];
+    }
+}
+
+// fp32 ~ U(lo, lo + span): ((fp32(u) * 2^-24) * span) + lo, u = top 24 bits.
+__global__ void gen_f32_uniform(float* __restrict__ out, int64_t n, int64_t start, uint64_t key, float lo,
+                                float span) {
+    for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n; j += (int64_t)gridDim.x * blockDim.x) {
+        const uint64_t h = splitmix_at(key, (uint64_t)(start + j));
+        const float u = __uint2float_rn((unsigned)(h >> 40));
+        float s = __fmul_rn(u, 5.9604644775390625e-08f);  // 2^-24
+        s = __fmul_rn(s, span);
+        out[j] = __fadd_rn(s, lo);
+    }
+}
+
 int grid_for(int64_t n) {
     int64_t b = (n + 255) / 256;
     if (b > 152 * 32) b = 152 * 32;
@@ -78,5 +100,19 @@ extern "C" int mbw_gen_bytes(void* out, int64_t n, int64_t start, uint64_t key, 
 extern "C" int mbw_gen_f16_scales(void* out, int64_t n, int64_t start, uint64_t key, cudaStream_t s) {
     if (n <= 0) return 0;
     gen_scales<<<grid_for(n), 256, 0, s>>>((uint16_t*)out, n, start, key);
+    return (int)cudaGetLastError();
+}
+
+extern "C" int mbw_gen_i8_table(void* out, int64_t n, int64_t start, uint64_t key, const void* table,
+                                cudaStream_t s) {
+    if (n <= 0) return 0;
+    gen_table8<<<grid_for(n), 256, 0, s>>>((int8_t*)out, n, start, key, (const int8_t*)table);
+    return (int)cudaGetLastError();
+}
+
+extern "C" int mbw_gen_f32_uniform(void* out, int64_t n, int64_t start, uint64_t key, float lo, float span,
+                                   cudaStream_t s) {
+    if (n <= 0) return 0;
+    gen_f32_uniform<<<grid_for(n), 256, 0, s>>>((float*)out, n, start, key, lo, span);
     return (int)cudaGetLastError();
 }

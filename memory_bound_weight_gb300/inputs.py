@@ -24,6 +24,13 @@ Value maps (one hash = 64 bits):
   * fp16 ~ U(0.001, 0.01): 1 value per hash from its top 24 bits u:
     fp16_rne(((fp32(u) * 2^-24) * 0.009f) + 0.001f), every fp32 step rounded
     separately (no fused multiply-add).
+  * int8 codes in [-127, 127], shaped like a per-channel quantized Gaussian
+    row: 4 values per hash, 16 bits each, each an index into a 65,536-entry
+    table (entry j = clip(rint(32 * Phi^-1((j + 0.5) / 65536)), -127, 127)),
+    so codes spread over about +-4 sigma and a few saturate at +-127.
+  * fp32 ~ U(0.0002, 0.001) (per-channel INT8 scales, about max|w| / 127 for
+    N(0, 0.02^2) rows): 1 value per hash, ((fp32(u) * 2^-24) * 0.0008f) +
+    0.0002f, each fp32 step rounded separately.
 """
 from __future__ import annotations
 
@@ -46,6 +53,9 @@ W_SIGMA = 0.02
 X_SIGMA = 1.0
 SCALE_LO = 0.001
 SCALE_SPAN = 0.009
+I8_SIGMA = 32.0
+I8_SCALE_LO = np.float32(0.0002)
+I8_SCALE_SPAN = np.float32(0.0008)
 
 
 def stream_id(matrix_index: int, kind: int) -> int:
@@ -94,18 +104,48 @@ def normal_table(sigma: float) -> np.ndarray:
     return t
 
 
-def bf16_normal(seed: int, stream: int, n: int, sigma: float, start: int = 0) -> np.ndarray:
-    """n bf16 bit patterns (uint16) ~ N(0, sigma^2), elements start .. start+n-1."""
-    if n == 0:
-        return np.zeros(0, dtype=np.uint16)
+@functools.lru_cache(maxsize=4)
+def int8_table(sigma: float) -> np.ndarray:
+    """65,536 int8 codes: quantiles (j+0.5)/65536 of N(0, sigma^2), rounded, clipped to +-127."""
+    from scipy.special import ndtri
+
+    p = (np.arange(65536, dtype=np.float64) + 0.5) / 65536.0
+    t = np.clip(np.rint(sigma * ndtri(p)), -127, 127).astype(np.int8)
+    t.setflags(write=False)
+    return t
+
+
+def _table_indices(seed: int, stream: int, n: int, start: int) -> np.ndarray:
     h0 = start // 4
     h1 = (start + n + 3) // 4
     h = hashes(seed, stream, h0, h1 - h0)
     idx = h.view(np.uint16).reshape(-1)  # little-endian: low 16 bits first
-    if idx.dtype.byteorder == ">":  # pragma: no cover - both hosts are little-endian
-        raise RuntimeError("big-endian host")
     off = start - 4 * h0
-    return normal_table(sigma)[idx[off:off + n]]
+    return idx[off:off + n]
+
+
+def int8_normal(seed: int, stream: int, n: int, sigma: float, start: int = 0) -> np.ndarray:
+    """n int8 codes from the quantile table, elements start .. start+n-1."""
+    if n == 0:
+        return np.zeros(0, dtype=np.int8)
+    return int8_table(sigma)[_table_indices(seed, stream, n, start)]
+
+
+def f32_uniform(seed: int, stream: int, n: int, lo: np.float32, span: np.float32, start: int = 0) -> np.ndarray:
+    """n fp32 ~ U(lo, lo + span): ((fp32(u) * 2^-24) * span) + lo, u = top 24 bits of a hash."""
+    if n == 0:
+        return np.zeros(0, dtype=np.float32)
+    u = (hashes(seed, stream, start, n) >> np.uint64(40)).astype(np.float32)
+    s = u * np.float32(2.0 ** -24)
+    s = s * np.float32(span)
+    return s + np.float32(lo)
+
+
+def bf16_normal(seed: int, stream: int, n: int, sigma: float, start: int = 0) -> np.ndarray:
+    """n bf16 bit patterns (uint16) ~ N(0, sigma^2), elements start .. start+n-1."""
+    if n == 0:
+        return np.zeros(0, dtype=np.uint16)
+    return normal_table(sigma)[_table_indices(seed, stream, n, start)]
 
 
 def random_bytes(seed: int, stream: int, n: int, start: int = 0) -> np.ndarray:
@@ -163,3 +203,15 @@ def u4_zero_points(seed: int, mi: int, N: int, groups: int, row0: int = 0, rows:
     if groups % 2:  # the unused high nibble of the last byte is kept zero
         z[:, -1] &= 0x0F
     return z
+
+
+def int8_codes(seed: int, mi: int, N: int, K: int, row0: int = 0, rows: int | None = None) -> np.ndarray:
+    """Symmetric INT8 codes, shape (rows, K) int8, values in [-127, 127]."""
+    rows = N - row0 if rows is None else rows
+    return int8_normal(seed, stream_id(mi, KIND_W), rows * K, I8_SIGMA, start=row0 * K).reshape(rows, K)
+
+
+def f32_row_scales(seed: int, mi: int, N: int, row0: int = 0, rows: int | None = None) -> np.ndarray:
+    """Per-output-channel fp32 scales, shape (rows,)."""
+    rows = N - row0 if rows is None else rows
+    return f32_uniform(seed, stream_id(mi, KIND_SCALES), rows, I8_SCALE_LO, I8_SCALE_SPAN, start=row0)

@@ -32,7 +32,10 @@ def _L():
                 L.mbw_gen_bf16_table.argtypes = [P, I64, I64, U64, P, P]
                 L.mbw_gen_bytes.argtypes = [P, I64, I64, U64, P]
                 L.mbw_gen_f16_scales.argtypes = [P, I64, I64, U64, P]
-                for f in (L.mbw_gen_bf16_table, L.mbw_gen_bytes, L.mbw_gen_f16_scales):
+                L.mbw_gen_i8_table.argtypes = [P, I64, I64, U64, P, P]
+                L.mbw_gen_f32_uniform.argtypes = [P, I64, I64, U64, ctypes.c_float, ctypes.c_float, P]
+                for f in (L.mbw_gen_bf16_table, L.mbw_gen_bytes, L.mbw_gen_f16_scales, L.mbw_gen_i8_table,
+                          L.mbw_gen_f32_uniform):
                     f.restype = ctypes.c_int
                 _lib = L
     return _lib
@@ -51,6 +54,15 @@ def _table(sigma, dev):
     if key not in _tables:
         t = gen.normal_table(sigma).view("int16")
         _tables[key] = torch.from_numpy(t.copy()).to(dev)
+    return _tables[key]
+
+
+def _i8_table(sigma, dev):
+    import torch
+
+    key = ("i8", float(sigma), str(dev))
+    if key not in _tables:
+        _tables[key] = torch.from_numpy(gen.int8_table(sigma).copy()).to(dev)
     return _tables[key]
 
 
@@ -115,3 +127,23 @@ def u4_zero_points(seed: int, mi: int, N: int, groups: int, device="cuda"):
         raise ValueError("device fill of zero points needs an even group count")
     t = torch.empty((N, groups // 2), dtype=torch.uint8, device=device)
     return bytes_(t, seed, gen.stream_id(mi, gen.KIND_ZEROS))
+
+
+def int8_codes(seed: int, mi: int, N: int, K: int, device="cuda"):
+    import torch
+
+    t = torch.empty((N, K), dtype=torch.int8, device=device)
+    tab = _i8_table(gen.I8_SIGMA, t.device)
+    _ok(_L().mbw_gen_i8_table(t.data_ptr(), t.numel(), 0, gen.stream_key(seed, gen.stream_id(mi, gen.KIND_W)),
+                              tab.data_ptr(), _stream(t.device)), "mbw_gen_i8_table")
+    return t
+
+
+def f32_row_scales(seed: int, mi: int, N: int, device="cuda"):
+    import torch
+
+    t = torch.empty((N,), dtype=torch.float32, device=device)
+    _ok(_L().mbw_gen_f32_uniform(t.data_ptr(), N, 0, gen.stream_key(seed, gen.stream_id(mi, gen.KIND_SCALES)),
+                                 float(gen.I8_SCALE_LO), float(gen.I8_SCALE_SPAN), _stream(t.device)),
+        "mbw_gen_f32_uniform")
+    return t

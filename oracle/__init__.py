@@ -75,10 +75,13 @@ class Oracle:
         lib.oracle_gemm_bf16.argtypes = [_P, _P, _I64, _I64, _I64, _P, _P]
         lib.oracle_gemm_int4_g64.argtypes = [_P, _P, _P, _I64, _I64, _I64, _P, _P]
         lib.oracle_gemm_int4_awq_g128.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P]
+        lib.oracle_gemm_int8_pc.argtypes = [_P, _P, _P, _I64, _I64, _I64, _P, _P]
+        lib.oracle_quantize_int8_pc.argtypes = [_P, _I64, _I64, _P, _P]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         for f in ("oracle_dequant_int4_g64", "oracle_dequant_int4_awq_g128", "oracle_gemm_bf16",
-                  "oracle_gemm_int4_g64", "oracle_gemm_int4_awq_g128", "oracle_set_num_threads"):
+                  "oracle_gemm_int4_g64", "oracle_gemm_int4_awq_g128", "oracle_gemm_int8_pc",
+                  "oracle_quantize_int8_pc", "oracle_set_num_threads"):
             getattr(lib, f).restype = None
 
     # ---- scalar formats
@@ -154,3 +157,26 @@ class Oracle:
         self.lib.oracle_gemm_int4_awq_g128(_ptr(codes), _ptr(scales), _ptr(zeros), _ptr(X), M, N, K,
                                            _ptr(Y), _ptr(A))
         return Y, A
+
+    # ---- symmetric INT8, per-output-channel scale
+    def gemm_int8_pc(self, codes, scales, X: np.ndarray):
+        """codes int8 (N, K), scales float32 (N,), X bf16 bits (M, K) or (K,) -> (Y, Yabs), each (M, N)."""
+        codes = np.ascontiguousarray(codes, dtype=np.int8)
+        scales = np.ascontiguousarray(scales, dtype=np.float32)
+        X = np.ascontiguousarray(np.atleast_2d(X), dtype=np.uint16)
+        M, K = X.shape
+        N = codes.shape[0]
+        assert codes.shape == (N, K) and scales.shape == (N,)
+        Y = np.empty((M, N), dtype=np.float64)
+        A = np.empty((M, N), dtype=np.float64)
+        self.lib.oracle_gemm_int8_pc(_ptr(codes), _ptr(scales), _ptr(X), M, N, K, _ptr(Y), _ptr(A))
+        return Y, A
+
+    def quantize_int8_pc(self, W: np.ndarray):
+        """W bf16 bits (N, K) -> (codes int8 (N, K), scales float32 (N,))."""
+        W = np.ascontiguousarray(W, dtype=np.uint16)
+        N, K = W.shape
+        Q = np.empty((N, K), dtype=np.int8)
+        S = np.empty((N,), dtype=np.float32)
+        self.lib.oracle_quantize_int8_pc(_ptr(W), N, K, _ptr(Q), _ptr(S))
+        return Q, S

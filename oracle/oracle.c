@@ -22,6 +22,11 @@
  *     with z a 4-bit code.
  *   - Batched decode: the same weights used for M activation rows
  *     (llm-rs vs vLLM, sec. 3 "Batching moves decode from memory toward math").
+ *   - Symmetric INT8 weights with one Float32 scale per output channel
+ *     (TileInfer, "Pushing further with cheating: INT8 quantization"): codes
+ *     q in [-127, 127], w_ik = s_i * q_ik, and the load-time quantizer that
+ *     makes them, s_i = max_k |w_ik| / 127 and q_ik = w_ik / s_i rounded to the
+ *     nearest integer.
  *
  * Readings where the pages are silent (all recorded in the design notes):
  *   - nibble order: the low nibble of byte b holds code k = 2b (even k), the
@@ -29,10 +34,14 @@
  *   - a group is 64 (or 128) consecutive k within one row;
  *   - AWQ zero points are packed two per byte, low nibble = even group, with
  *     ceil(G/2) bytes per row (G = K/128 groups);
- *   - accumulation order: k = 0 .. K-1 sequentially in fp64 per output.
+ *   - accumulation order: k = 0 .. K-1 sequentially in fp64 per output;
+ *   - INT8 quantizer: the scale is computed in fp32 (the stored precision),
+ *     the quotient w / s in fp32 (IEEE division), rounded to the nearest
+ *     integer with ties to even; an all-zero row gets s = 0 and q = 0.
  *
- * Every product w*x is exact in fp64 (w has at most 15 significant bits,
- * x at most 8), so the only rounding is in the fp64 summation.
+ * Every product w*x is exact in fp64 (INT4: w has at most 15 significant
+ * bits; INT8: s * q has at most 32; x at most 8), so the only rounding is in
+ * the fp64 summation.
  *
  * Each GEMV also returns yabs[i] = sum_k |w_ik * x_k| in fp64, the quantity
  * the parity tolerance is stated against.
@@ -242,6 +251,71 @@ void oracle_gemm_int4_awq_g128(const uint8_t *codes, const uint16_t *scales,
             }
             Y[m * N + i] = acc;
             Yabs[m * N + i] = aabs;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Symmetric INT8, one fp32 scale per output channel.                        */
+/* ------------------------------------------------------------------------ */
+
+/* Y[m][i] = sum_k w_ik * X[m][k] with w_ik = S[i] * Q[i][k] (TileInfer,
+ * "Pushing further with cheating: INT8 quantization": one scale per output
+ * channel). The plain definition: dequantize each weight, multiply, add. The
+ * pages' kernel sums q * x and applies S[i] once at the end, which is the same
+ * value up to rounding order. Q int8 [N][K], S fp32 [N], X bf16 [M][K]. */
+void oracle_gemm_int8_pc(const int8_t *Q, const float *S, const uint16_t *X,
+                         int64_t M, int64_t N, int64_t K, double *Y,
+                         double *Yabs)
+{
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < N; i++) {
+        for (int64_t m = 0; m < M; m++) {
+            double acc = 0.0, aabs = 0.0;
+            for (int64_t k = 0; k < K; k++) {
+                double w = (double)S[i] * (double)Q[i * K + k];
+                double x = oracle_bf16_to_double(X[m * K + k]);
+                acc += w * x;
+                aabs += fabs(w * x);
+            }
+            Y[m * N + i] = acc;
+            Yabs[m * N + i] = aabs;
+        }
+    }
+}
+
+/* Load-time quantizer of one weight matrix (same section): for each row i,
+ * s_i = max_k |w_ik| / 127 in fp32, and q_ik = w_ik / s_i rounded to the
+ * nearest integer (fp32 quotient, ties to even), so the largest entry lands
+ * on +-127 and every entry is off by at most s_i / 2. W bf16 [N][K]. */
+void oracle_quantize_int8_pc(const uint16_t *W, int64_t N, int64_t K,
+                             int8_t *Q, float *S)
+{
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < N; i++) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; k++) {
+            float a = (float)fabs(oracle_bf16_to_double(W[i * K + k]));
+            if (a > amax)
+                amax = a;
+        }
+        float s = amax / 127.0f;                    /* fp32 division */
+        S[i] = s;
+        for (int64_t k = 0; k < K; k++) {
+            if (s == 0.0f) {
+                Q[i * K + k] = 0;
+                continue;
+            }
+            float w = (float)oracle_bf16_to_double(W[i * K + k]);
+            float t = w / s;                          /* fp32 division */
+            float r = rintf(t);                       /* nearest, ties to even */
+            if (r > 127.0f)
+                r = 127.0f;
+            if (r < -127.0f)
+                r = -127.0f;
+            Q[i * K + k] = (int8_t)r;
         }
     }
 }

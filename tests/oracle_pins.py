@@ -14,7 +14,12 @@ What each pin compares with:
     and numpy's fp64 matmul of the numpy dequant;
   * invariants: power-of-two scaling, identity / one-hot weights, one-hot x,
     consistent permutation of k, batch = separate calls, linearity on
-    disjoint supports.
+    disjoint supports;
+  * INT8 per-channel: hand-worked values in tests/golden/int8_pc_hand.txt
+    (GEMV and quantizer, including ties and a non-dyadic scale), exact
+    rational products, numpy's matmul, scale linearity, and the quantizer's
+    properties stated on the page (largest entry on +-127, every entry
+    within half a scale).
 """
 from __future__ import annotations
 
@@ -99,6 +104,37 @@ def small_awq_case(seed, N, K, M=1):
     z = gen.u4_zero_points(seed, 0, N, G)
     X = gen.bf16_activations(seed, 0, M, K)
     return c, s, z, X
+
+
+def small_int8_case(seed, N, K, M=1):
+    q = gen.int8_codes(seed, 0, N, K)
+    s = gen.f32_row_scales(seed, 0, N)
+    X = gen.bf16_activations(seed, 0, M, K)
+    return q, s, X
+
+
+def np_dequant_int8(q, s) -> np.ndarray:
+    return np.asarray(s, dtype=np.float32).astype(np.float64)[:, None] * np.asarray(q, dtype=np.int8).astype(np.float64)
+
+
+def load_int8_fixture():
+    gemv, quant = [], []
+    with open(os.path.join(GOLDEN, "int8_pc_hand.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            parts = line.split()
+            if parts[0] == "gemv":
+                _, N, K, codes, scales, x, row, expect = parts
+                gemv.append(dict(N=int(N), K=int(K), codes=[int(v) for v in codes.split(",")],
+                                 scales=[int(v, 16) for v in scales.split(",")],
+                                 x=[int(v, 16) for v in x.split(",")], row=int(row), expect=Fraction(expect)))
+            else:
+                _, K, w, scale, codes = parts
+                quant.append(dict(K=int(K), w=[int(v, 16) for v in w.split(",")], scale=int(scale, 16),
+                                  codes=[int(v) for v in codes.split(",")]))
+    return gemv, quant
 
 
 # --------------------------------------------------------------- pins ----
@@ -364,6 +400,96 @@ def pin_yabs_bounds(o):
     assert np.all(np.abs(y) <= ya) and np.all(ya > 0)
 
 
+def pin_int8_hand_worked(o):
+    gemv, quant = load_int8_fixture()
+    assert len(gemv) >= 5 and len(quant) >= 4
+    for c in gemv:
+        q = np.array(c["codes"], dtype=np.int8).reshape(c["N"], c["K"])
+        s = np.array(c["scales"], dtype=np.uint32).view(np.float32)
+        x = np.array(c["x"], dtype=np.uint16).reshape(1, c["K"])
+        y, _ = o.gemm_int8_pc(q, s, x)
+        assert Fraction(float(y[0, c["row"]])) == c["expect"], (c, y)
+    for c in quant:
+        w = np.array(c["w"], dtype=np.uint16).reshape(1, c["K"])
+        q, s = o.quantize_int8_pc(w)
+        assert int(s.view(np.uint32)[0]) == c["scale"], (c, hex(int(s.view(np.uint32)[0])))
+        assert q[0].tolist() == c["codes"], (c, q)
+
+
+def pin_int8_exact_and_numpy(o):
+    for seed, N, K, M in ((91, 3, 64, 1), (92, 2, 128, 2), (93, 5, 48, 1)):
+        q, s, X = small_int8_case(seed, N, K, M)
+        y, ya = o.gemm_int8_pc(q, s, X)
+        _exact_check(y, ya, np_dequant_int8(q, s), np_bf16_to_f64(X))
+    for seed, N, K, M in ((94, 37, 640, 1), (95, 9, 1024, 3)):
+        q, s, X = small_int8_case(seed, N, K, M)
+        y, ya = o.gemm_int8_pc(q, s, X)
+        Wd, Xf = np_dequant_int8(q, s), np_bf16_to_f64(X)
+        assert np.all(np.abs(y - Xf @ Wd.T) <= 2 * sum_bound(K, ya))
+        assert np.all(np.abs(ya - np.abs(Xf) @ np.abs(Wd).T) <= 2 * sum_bound(K, ya))
+
+
+def pin_int8_invariants(o):
+    N, K, M = 7, 256, 3
+    q, s, X = small_int8_case(101, N, K, M)
+    y, ya = o.gemm_int8_pc(q, s, X)
+    # a row's scale scales only that row's output (x2 is exact in fp32 and fp64)
+    s2 = s.copy()
+    s2[3] = s2[3] * np.float32(2.0)
+    y2, _ = o.gemm_int8_pc(q, s2, X)
+    assert np.array_equal(y2[:, 3], 2.0 * y[:, 3])
+    assert np.array_equal(np.delete(y2, 3, axis=1), np.delete(y, 3, axis=1))
+    # negating the codes negates the output
+    yn, _ = o.gemm_int8_pc(-q, s, X)
+    assert np.array_equal(yn, -y)
+    # one-hot x = e_k picks column k of the dequantized weights
+    for k in (0, 1, 127, 255):
+        e = np.zeros((1, K))
+        e[0, k] = 1.0
+        ye, _ = o.gemm_int8_pc(q, s, f64_to_bf16_exact(e))
+        assert np.array_equal(ye[0], np_dequant_int8(q, s)[:, k])
+    # identity codes with scale 1: y = x
+    eye = np.eye(K, dtype=np.int8)
+    yi, _ = o.gemm_int8_pc(eye, np.ones(K, dtype=np.float32), X[:1])
+    assert np.array_equal(yi[0], np_bf16_to_f64(X[0]))
+    # the batch equals separate calls
+    for m in range(M):
+        assert np.array_equal(y[m], o.gemm_int8_pc(q, s, X[m:m + 1])[0][0])
+    # power-of-two scaling of x
+    Xj = f64_to_bf16_exact(np_bf16_to_f64(X) * 2.0 ** -3)
+    assert np.array_equal(o.gemm_int8_pc(q, s, Xj)[0], y * 2.0 ** -3)
+    assert np.all(np.abs(y) <= ya)
+
+
+def pin_int8_quantizer_properties(o):
+    """The page's rule: the largest entry of a row lands on +-127 and every
+    entry is within half a scale of scale * code (up to the fp32 quotient)."""
+    N, K = 12, 300
+    W = gen.bf16_weights(111, 0, N, K)
+    W[5] = 0          # an all-zero row
+    W[6, :] = W[6, :] & 0x807F  # tiny (subnormal) bf16 values
+    W[7, 17] = 0xC2FE  # a negative maximum, -127
+    q, s = o.quantize_int8_pc(W)
+    Wf = np_bf16_to_f64(W)
+    for i in range(N):
+        amax = float(np.max(np.abs(Wf[i])))
+        if amax == 0.0:
+            assert s[i] == 0 and not q[i].any()
+            continue
+        si = Fraction(float(s[i]))
+        # s is amax / 127 correctly rounded to fp32 (half an ulp; fixed ulp 2^-149 below 2^-126)
+        half_ulp = max(si * Fraction(2) ** -24, Fraction(2) ** -150)
+        assert abs(si * 127 - Fraction(amax)) <= 127 * half_ulp
+        j = int(np.argmax(np.abs(Wf[i])))
+        assert int(q[i, j]) == (127 if Wf[i, j] > 0 else -127), (i, j, q[i, j])
+        assert np.all(np.abs(q[i].astype(np.int64)) <= 127)
+        for k in range(K):
+            t = Fraction(float(Wf[i, k])) / si
+            assert abs(t - int(q[i, k])) <= Fraction(1, 2) + Fraction(1, 2 ** 16), (i, k)
+            if Wf[i, k] == 0:
+                assert q[i, k] == 0
+
+
 PINS = [
     pin_f16_decoder_exhaustive,
     pin_bf16_decoder_exhaustive,
@@ -378,6 +504,10 @@ PINS = [
     pin_batch_equals_separate,
     pin_linearity_disjoint,
     pin_yabs_bounds,
+    pin_int8_hand_worked,
+    pin_int8_exact_and_numpy,
+    pin_int8_invariants,
+    pin_int8_quantizer_properties,
 ]
 
 

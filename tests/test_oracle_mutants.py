@@ -41,6 +41,17 @@ MUTANTS = [
     ("awq_acc_sign", "acc += w * x;", "acc -= w * x;", 3),
     ("output_transposed", "Y[m * N + i] = acc;", "Y[i * M + m] = acc;", 1),
     ("batch_row_of_x", "X[m * K + k]", "X[0 * K + k]", 1),
+    ("int8_scale_of_row_0", "(double)S[i] * (double)Q[i * K + k]", "(double)S[0] * (double)Q[i * K + k]", 1),
+    ("int8_scale_dropped", "(double)S[i] * (double)Q[i * K + k]", "(double)Q[i * K + k]", 1),
+    ("int8_codes_unsigned", "(double)S[i] * (double)Q[i * K + k]", "(double)S[i] * (double)(uint8_t)Q[i * K + k]", 1),
+    ("int8_code_row_stride", "(double)S[i] * (double)Q[i * K + k]", "(double)S[i] * (double)Q[i * (K - 1) + k]", 1),
+    ("int8_dropped_last_term", "for (int64_t k = 0; k < K; k++) {", "for (int64_t k = 0; k < K - 1; k++) {", 4),
+    ("int8_acc_sign", "acc += w * x;", "acc -= w * x;", 4),
+    ("quant_divisor_128", "amax / 127.0f", "amax / 128.0f", 1),
+    ("quant_ties_away", "rintf(t)", "roundf(t)", 1),
+    ("quant_truncate", "rintf(t)", "truncf(t)", 1),
+    ("quant_signed_max", "(float)fabs(oracle_bf16_to_double(W[i * K + k]))", "(float)oracle_bf16_to_double(W[i * K + k])", 1),
+    ("quant_first_entry_skipped", "for (int64_t k = 0; k < K; k++) {", "for (int64_t k = 1; k < K; k++) {", 5),
 ]
 
 

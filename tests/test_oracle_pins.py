@@ -23,3 +23,13 @@ def test_fixture_is_hand_worked_not_generated():
     head = open(path).read(2000)
     assert "tinyinfer" in head and "llm-rs vs vLLM" in head
     assert len(oracle_pins.load_dequant_fixture()) >= 30
+
+
+def test_int8_fixture_is_hand_worked():
+    """The INT8 table is read as text and carries its citation header."""
+    import os
+
+    head = open(os.path.join(oracle_pins.GOLDEN, "int8_pc_hand.txt")).read(1500)
+    assert "TileInfer" in head and "INT8 quantization" in head
+    gemv, quant = oracle_pins.load_int8_fixture()
+    assert len(gemv) >= 5 and len(quant) >= 4
