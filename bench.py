@@ -57,7 +57,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="mbw", choices=["mbw", "reference"])
     p.add_argument("--workload", default="tinyllama_int4",
-                   choices=["tinyllama_int4", "tinyllama_int4_unfused", "qwen_bf16", "qwen_awq", "bf16_2048"])
+                   choices=["tinyllama_int4", "tinyllama_int4_unfused", "qwen_bf16", "qwen_awq", "qwen3_int8",
+                            "bf16_2048"])
     p.add_argument("--batch", type=int, default=1,
                    help="activation rows per GEMV (qwen_awq: AWQ-style INT4 decode at batch M)")
     p.add_argument("--no-e2e", action="store_true")
@@ -220,24 +221,11 @@ class Step:
             inputs_gpu.bf16_normal_(xv, seed, gen.stream_id(mi, gen.KIND_X), gen.X_SIGMA)
             xa = xv if M == 1 else xv.view(M, m.K)
             ya = yv if M == 1 else yv.view(M, m.N)
-            if fmt == wl.FMT_INT4_G64:
-                c = inputs_gpu.int4_codes(seed, mi, m.N, m.K, device)
-                s = inputs_gpu.f16_group_scales(seed, mi, m.N, m.K // 64, device)
-                self.calls.append((mbw.gemv_int4_g64, (c, s, xa), ya))
-            elif fmt == wl.FMT_INT4_AWQ_G128:
-                c = inputs_gpu.int4_codes(seed, mi, m.N, m.K, device)
-                s = inputs_gpu.f16_group_scales(seed, mi, m.N, m.K // 128, device)
-                z = inputs_gpu.u4_zero_points(seed, mi, m.N, m.K // 128, device)
-                self.calls.append((mbw.gemv_int4_awq_g128, (c, s, z, xa), ya))
-            elif fmt == wl.FMT_BF16:
-                W = inputs_gpu.bf16_weights(seed, mi, m.N, m.K, device)
-                self.calls.append((mbw.gemv_bf16, (W, xa), ya))
-            else:
-                raise ValueError(fmt)
+            self.calls.append(device_call(fmt, seed, mi, m.N, m.K, xa, ya, device))
             ko += M * m.K
             no += M * m.N
         self.op = {wl.FMT_INT4_G64: mbw.OP_GEMV_INT4_G64, wl.FMT_INT4_AWQ_G128: mbw.OP_GEMV_INT4_AWQ_G128,
-                   wl.FMT_BF16: mbw.OP_GEMV_BF16}[fmt]
+                   wl.FMT_BF16: mbw.OP_GEMV_BF16, wl.FMT_INT8_PC: mbw.OP_GEMV_INT8_PC}[fmt]
         self.bytes_alg = wl.step_bytes_alg(mats, fmt, M)
         self.flops = sum(wl.flops(M, m.N, m.K) for m in mats)
         self.h2d_bytes = 2 * M * sumK
@@ -251,6 +239,40 @@ class Step:
             fn(*args, out=out)
 
 
+def device_call(fmt, seed, mi, N, K, x, y, device):
+    """(C-ABI call, its inputs, its output) for matrix `mi` of a workload, with
+    the matrix generated on the device."""
+    import memory_bound_weight_gb300 as mbw
+    from memory_bound_weight_gb300 import inputs_gpu
+
+    if fmt == wl.FMT_INT4_G64:
+        c = inputs_gpu.int4_codes(seed, mi, N, K, device)
+        s = inputs_gpu.f16_group_scales(seed, mi, N, K // 64, device)
+        return mbw.gemv_int4_g64, (c, s, x), y
+    if fmt == wl.FMT_INT4_AWQ_G128:
+        c = inputs_gpu.int4_codes(seed, mi, N, K, device)
+        s = inputs_gpu.f16_group_scales(seed, mi, N, K // 128, device)
+        z = inputs_gpu.u4_zero_points(seed, mi, N, K // 128, device)
+        return mbw.gemv_int4_awq_g128, (c, s, z, x), y
+    if fmt == wl.FMT_INT8_PC:
+        q = inputs_gpu.int8_codes(seed, mi, N, K, device)
+        s = inputs_gpu.f32_row_scales(seed, mi, N, device)
+        return mbw.gemv_int8_pc, (q, s, x), y
+    if fmt == wl.FMT_BF16:
+        return mbw.gemv_bf16, (inputs_gpu.bf16_weights(seed, mi, N, K, device), x), y
+    raise ValueError(fmt)
+
+
+WORKLOAD_MATS = {
+    "tinyllama_int4": (lambda: wl.tinyllama_step(fused=True), wl.FMT_INT4_G64),
+    "tinyllama_int4_unfused": (lambda: wl.tinyllama_step(), wl.FMT_INT4_G64),
+    "qwen_bf16": (wl.qwen25_7b_step, wl.FMT_BF16),
+    "qwen_awq": (wl.qwen25_7b_step, wl.FMT_INT4_AWQ_G128),
+    "qwen3_int8": (wl.qwen3_4b_step, wl.FMT_INT8_PC),
+    "bf16_2048": (lambda: [wl.Mat(f"copy{i}", 2048, 2048) for i in range(64)], wl.FMT_BF16),
+}
+
+
 def make_step(workload, seed, device, M=1):
     if workload in ("tinyllama_int4", "tinyllama_int4_unfused"):
         return Step("TinyLlama-1.1B-shaped INT4 g64 decode step, batch 1", wl.FMT_INT4_G64,
@@ -260,6 +282,9 @@ def make_step(workload, seed, device, M=1):
     if workload == "qwen_awq":
         return Step(f"Qwen2.5-7B-shaped AWQ-style INT4 decode step, batch {M}", wl.FMT_INT4_AWQ_G128,
                     wl.qwen25_7b_step(), seed, device, M)
+    if workload == "qwen3_int8":
+        return Step(f"Qwen3-4B-shaped symmetric INT8 per-channel decode step, batch {M}", wl.FMT_INT8_PC,
+                    wl.qwen3_4b_step(), seed, device, M)
     if workload == "bf16_2048":
         # 2048x2048 BF16 GEMV; 64 distinct copies (537 MB) so that each is evicted before it recurs
         mats = [wl.Mat(f"copy{i}", 2048, 2048) for i in range(64)]
@@ -278,14 +303,11 @@ def cpu_baseline(workload, budget_s=10.0, M=1):
     from memory_bound_weight_gb300 import inputs as gen
 
     o = oracle.load()
-    if workload in ("tinyllama_int4", "tinyllama_int4_unfused"):
-        mats, fmt = wl.tinyllama_step(fused=(workload == "tinyllama_int4")), wl.FMT_INT4_G64
-    elif workload == "qwen_bf16":
-        mats, fmt = wl.qwen25_7b_step(), wl.FMT_BF16
-    elif workload == "qwen_awq":
-        mats, fmt = wl.qwen25_7b_step(), wl.FMT_INT4_AWQ_G128
-    else:
+    if workload == "bf16_2048":
         mats, fmt = [wl.Mat("copy0", 2048, 2048)] * 64, wl.FMT_BF16
+    else:
+        mk, fmt = WORKLOAD_MATS[workload]
+        mats = mk()
     done_bytes = 0
     spent = 0.0
     n = 0
@@ -300,6 +322,8 @@ def cpu_baseline(workload, budget_s=10.0, M=1):
             Z = None
             if fmt == wl.FMT_INT4_G64:
                 A, B = gen.int4_codes(0, mi, m.N, m.K), gen.f16_group_scales(0, mi, m.N, m.K // 64)
+            elif fmt == wl.FMT_INT8_PC:
+                A, B = gen.int8_codes(0, mi, m.N, m.K), gen.f32_row_scales(0, mi, m.N)
             elif fmt == wl.FMT_INT4_AWQ_G128:
                 G = m.K // 128
                 A, B = gen.int4_codes(0, mi, m.N, m.K), gen.f16_group_scales(0, mi, m.N, G)
@@ -311,6 +335,8 @@ def cpu_baseline(workload, budget_s=10.0, M=1):
         t = time.perf_counter()
         if fmt == wl.FMT_INT4_G64:
             o.gemm_int4_g64(A, B, X)
+        elif fmt == wl.FMT_INT8_PC:
+            o.gemm_int8_pc(A, B, X)
         elif fmt == wl.FMT_INT4_AWQ_G128:
             o.gemm_int4_awq_g128(A, B, Z, X)
         else:
@@ -342,12 +368,8 @@ def run_reference(args, rank, ws):
     cb["value"] = v
     cb["sample"] = f"each step: {per_step:.1f} s of oracle time over the step's matrices in order; first step: " \
                    + vals[0]["sample"]
-    step_bytes = wl.step_bytes_alg(*{"tinyllama_int4": (wl.tinyllama_step(fused=True), wl.FMT_INT4_G64),
-                                     "tinyllama_int4_unfused": (wl.tinyllama_step(), wl.FMT_INT4_G64),
-                                     "qwen_bf16": (wl.qwen25_7b_step(), wl.FMT_BF16),
-                                     "qwen_awq": (wl.qwen25_7b_step(), wl.FMT_INT4_AWQ_G128),
-                                     "bf16_2048": ([wl.Mat("c", 2048, 2048)] * 64, wl.FMT_BF16)}[args.workload],
-                                   args.batch)
+    mk, fmt = WORKLOAD_MATS[args.workload]
+    step_bytes = wl.step_bytes_alg(mk(), fmt, args.batch)
     line = {"impl": "reference", "metric": metric_name(args.workload), "value": v, "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_bytes / (v * 1e9) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -367,6 +389,8 @@ def workload_desc(workload, batch=1):
             "qwen_bf16": "Qwen2.5-7B-shaped BF16 decode step, batch 1 (141 GEMVs)",
             "qwen_awq": f"Qwen2.5-7B-shaped AWQ-style INT4 decode step (group 128, fp16 scale, uint4 zero point, LM head "
                         f"included), batch {batch} (141 GEMMs)",
+            "qwen3_int8": f"Qwen3-4B-shaped symmetric INT8 decode step (one fp32 scale per output channel, every "
+                          f"linear layer and the LM head, q/k/v and gate/up fused), batch {batch} (145 GEMVs)",
             "bf16_2048": "BF16 GEMV 2048x2048, batch 1, 64 rotating copies"}[workload]
 
 
@@ -592,6 +616,8 @@ def named_shapes(fmt):
         return [(m.N, m.K) for m in wl.TINYLLAMA_TABLE_SHAPES]
     if fmt == wl.FMT_INT4_AWQ_G128:
         return [(m.N, m.K) for m in wl.SKINNY_SHAPES]
+    if fmt == wl.FMT_INT8_PC:
+        return []
     return [(2048, 2048)]
 
 
@@ -619,18 +645,7 @@ def time_per_shape(step, device, reps=5, shapes=None, plans=None):
         calls = []
         for i in range(copies):
             xi, yi = (x[i, 0], y[i, 0]) if M == 1 else (x[i], y[i])
-            if step.fmt == wl.FMT_INT4_G64:
-                c = inputs_gpu.int4_codes(0, 1000 + i, N, K, device)
-                sc = inputs_gpu.f16_group_scales(0, 1000 + i, N, K // 64, device)
-                calls.append((mbw.gemv_int4_g64, (c, sc, xi), yi))
-            elif step.fmt == wl.FMT_INT4_AWQ_G128:
-                c = inputs_gpu.int4_codes(0, 1000 + i, N, K, device)
-                sc = inputs_gpu.f16_group_scales(0, 1000 + i, N, K // 128, device)
-                z = inputs_gpu.u4_zero_points(0, 1000 + i, N, K // 128, device)
-                calls.append((mbw.gemv_int4_awq_g128, (c, sc, z, xi), yi))
-            else:
-                W = inputs_gpu.bf16_weights(0, 1000 + i, N, K, device)
-                calls.append((mbw.gemv_bf16, (W, xi), yi))
+            calls.append(device_call(step.fmt, 0, 1000 + i, N, K, xi, yi, device))
         if plans is not None and (N, K) in plans:
             mbw.plan_select(step.op, M, N, K, plans[(N, K)])
         else:

@@ -70,6 +70,7 @@ typedef int mbw_status;
 #define MBW_OP_GEMV_INT4_G64 2
 #define MBW_OP_GEMV_INT4_AWQ_G128 3
 #define MBW_OP_GEMM_SKINNY_BF16 4
+#define MBW_OP_GEMV_INT8_PC 5
 
 /*
  * gemv_bf16 -- y = W . x with BF16 weights (16 bits per weight; llm-rs vs
@@ -118,6 +119,34 @@ mbw_status gemv_int4_awq_g128(const uint8_t *Wq, const void *scales, const uint8
  */
 mbw_status gemm_skinny_bf16(const void *X, const void *W, void *Y, int64_t M, int64_t N,
                             int64_t K, void *workspace, size_t ws_bytes, mbw_stream_t stream);
+
+/*
+ * gemv_int8_pc -- Y = X . W^T with symmetric INT8 weights and one fp32 scale
+ * per output channel (TileInfer, "Pushing further with cheating: INT8
+ * quantization"): w_ik = scales[i] * Wq[i][k], codes in [-127, 127]. The
+ * kernel multiplies the codes in (exactly, as bf16 on the tensor core, fp32
+ * accumulation) and applies the row's scale once to the finished sum. M = 1
+ * is the decode GEMV; batches above 8 run in slices of 8 rows.
+ *   Wq     : int8 [N][K]     scales : fp32 [N]
+ *   X      : bf16 [M][K]     Y      : bf16 [M][N] (fp32 under the fp32 hook)
+ *   Requires K % 128 == 0. `scales` needs 4-byte alignment. The code -128 is
+ *   outside the format; the kernels read it as -128.
+ */
+mbw_status gemv_int8_pc(const int8_t *Wq, const float *scales, const void *X, void *Y, int64_t M,
+                        int64_t N, int64_t K, void *workspace, size_t ws_bytes, mbw_stream_t stream);
+
+/*
+ * mbw_quantize_int8_pc -- the load-time step that makes gemv_int8_pc's
+ * weights from BF16 ones (same section): per row i, scales[i] = max_k |W[i][k]|
+ * / 127 and Wq[i][k] = W[i][k] / scales[i] rounded to the nearest integer, so
+ * the row's largest entry lands on +-127 and every entry is off by at most
+ * half a scale. Both divisions are IEEE fp32; ties round to even; an all-zero
+ * row gets scale 0 and codes 0. W must be finite.
+ *   W : bf16 [N][K] (2-byte aligned)   Wq : int8 [N][K]   scales : fp32 [N]
+ *   Any K >= 0.
+ */
+mbw_status mbw_quantize_int8_pc(const void *W, int8_t *Wq, float *scales, int64_t N, int64_t K,
+                                mbw_stream_t stream);
 
 /* Bytes of workspace the largest plan of `op` may use for this shape (0 if none). */
 size_t mbw_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);

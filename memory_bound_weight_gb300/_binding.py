@@ -19,6 +19,7 @@ OP_GEMV_BF16 = 1
 OP_GEMV_INT4_G64 = 2
 OP_GEMV_INT4_AWQ_G128 = 3
 OP_GEMM_SKINNY_BF16 = 4
+OP_GEMV_INT8_PC = 5
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -34,6 +35,8 @@ SIGNATURES = {
     "gemv_int4_g64": ([_P, _P, _P, _P, _I64, _I64, _P, _SZ, _P], _ST),
     "gemv_int4_awq_g128": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _ST),
     "gemm_skinny_bf16": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _ST),
+    "gemv_int8_pc": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _ST),
+    "mbw_quantize_int8_pc": ([_P, _P, _P, _I64, _I64, _P], _ST),
     "mbw_workspace_bytes": ([ctypes.c_int, _I64, _I64, _I64], _SZ),
     "mbw_dequant_int4_g64": ([_P, _P, _P, _I64, _I64, _P], _ST),
     "mbw_dequant_int4_awq_g128": ([_P, _P, _P, _P, _I64, _I64, _P], _ST),
@@ -215,6 +218,37 @@ def gemm_skinny_bf16(X, W, out=None, workspace=None):
     check("gemm_skinny_bf16", lib().gemm_skinny_bf16(X.data_ptr(), W.data_ptr(), Y.data_ptr(), M, N, K, wp, wn,
                                                      _stream_ptr(W.device)))
     return Y
+
+
+def gemv_int8_pc(Wq, scales, X, out=None, workspace=None):
+    """Y = X . W^T; Wq int8 (N, K), scales fp32 (N,), X bf16 (M, K) or (K,) -> Y (M, N) or (N,)."""
+    torch = _torch()
+    vec = X.dim() == 1
+    X2 = X.unsqueeze(0) if vec else X
+    _need(Wq, "Wq", torch.int8, 2)
+    _need(scales, "scales", torch.float32, 1)
+    _need(X2, "X", torch.bfloat16, 2)
+    M, K = X2.shape
+    N = Wq.shape[0]
+    if Wq.shape[1] != K or scales.shape[0] != N:
+        raise ValueError("shapes: Wq (N, K), scales (N,), X (M, K)")
+    Y = _alloc_out((M, N), Wq, None if out is None else (out.unsqueeze(0) if vec else out))
+    wp, wn = _ws(workspace)
+    check("gemv_int8_pc", lib().gemv_int8_pc(Wq.data_ptr(), scales.data_ptr(), X2.data_ptr(), Y.data_ptr(), M, N, K,
+                                             wp, wn, _stream_ptr(Wq.device)))
+    return Y[0] if vec else Y
+
+
+def quantize_int8_pc(W):
+    """BF16 W (N, K) -> (Wq int8 (N, K), scales fp32 (N,)), scale = max|w| / 127 per row."""
+    torch = _torch()
+    _need(W, "W", torch.bfloat16, 2)
+    N, K = W.shape
+    Wq = torch.empty((N, K), dtype=torch.int8, device=W.device)
+    sc = torch.empty((N,), dtype=torch.float32, device=W.device)
+    check("mbw_quantize_int8_pc", lib().mbw_quantize_int8_pc(W.data_ptr(), Wq.data_ptr(), sc.data_ptr(), N, K,
+                                                             _stream_ptr(W.device)))
+    return Wq, sc
 
 
 def dequant_int4_g64(Wq, scales):

@@ -58,7 +58,8 @@ static mbw_status zero_output(void* y, int64_t M, int64_t N, cudaStream_t s) {
 // Run a CUDA-core streaming GEMV over M activation rows, in slices of the
 // planned kernel's batch width.
 static mbw_status run_simt(int fmt, int op, const uint8_t* W, const uint16_t* scales, const uint8_t* zeros,
-                           const uint16_t* X, void* Y, int64_t M, int64_t N, int64_t K, cudaStream_t s) {
+                           const uint16_t* X, void* Y, int64_t M, int64_t N, int64_t K, cudaStream_t s,
+                           const float* rscale = nullptr) {
     const Plan p = plan_lookup(op, M, N, K, s);
     const int width = plan_batch_width(fmt, p);
     GemvArgs a;
@@ -67,11 +68,12 @@ static mbw_status run_simt(int fmt, int op, const uint8_t* W, const uint16_t* sc
     a.zeros = zeros;
     a.N = (int)N;
     a.K = (int)K;
-    a.chunks = (int)(fmt == FMT_BF16 ? K / 8 : K / 32);
+    a.chunks = (int)(fmt == FMT_BF16 ? K / 8 : fmt == FMT_I8 ? K / 16 : K / 32);
     a.split_chunks = (a.chunks + p.split - 1) / p.split;
     a.groups = (int)(fmt == FMT_G64 ? K / 64 : fmt == FMT_AWQ ? K / 128 : 0);
     a.zstride = (a.groups + 1) / 2;
     a.out_f32 = g_out_f32;
+    a.rscale = rscale;
     const size_t ybytes = g_out_f32 ? 4 : 2;
     for (int64_t m0 = 0; m0 < M; m0 += width) {
         a.x = X + m0 * K;
@@ -134,6 +136,33 @@ mbw_status gemv_int4_awq_g128(const uint8_t* Wq, const void* scales, const uint8
     if (K == 0) return zero_output(Y, M, N, (cudaStream_t)stream);
     return run_simt(FMT_AWQ, MBW_OP_GEMV_INT4_AWQ_G128, Wq, (const uint16_t*)scales, zeros, (const uint16_t*)X, Y,
                     M, N, K, (cudaStream_t)stream);
+}
+
+mbw_status gemv_int8_pc(const int8_t* Wq, const float* scales, const void* X, void* Y, int64_t M, int64_t N,
+                        int64_t K, void* workspace, size_t ws_bytes, mbw_stream_t stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    mbw_status st = check_sizes("gemv_int8_pc", M, N, K, 128);
+    if (st != MBW_OK) return st;
+    if (N == 0 || M == 0) return MBW_OK;
+    if (!Y || (K > 0 && (!Wq || !scales || !X))) return fail(MBW_ERR_INVALID_ARG, "gemv_int8_pc: NULL pointer");
+    if (!aligned(Wq, 16) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(scales, 4))
+        return fail(MBW_ERR_MISALIGNED, "gemv_int8_pc: Wq, X and Y must be 16-byte aligned, scales 4-byte");
+    if (K == 0) return zero_output(Y, M, N, (cudaStream_t)stream);
+    return run_simt(FMT_I8, MBW_OP_GEMV_INT8_PC, (const uint8_t*)Wq, nullptr, nullptr, (const uint16_t*)X, Y, M, N,
+                    K, (cudaStream_t)stream, scales);
+}
+
+mbw_status mbw_quantize_int8_pc(const void* W, int8_t* Wq, float* scales, int64_t N, int64_t K,
+                                mbw_stream_t stream) {
+    mbw_status st = check_sizes("mbw_quantize_int8_pc", 1, N, K, 1);
+    if (st != MBW_OK) return st;
+    if (N == 0) return MBW_OK;
+    if (!scales || (K > 0 && (!W || !Wq))) return fail(MBW_ERR_INVALID_ARG, "mbw_quantize_int8_pc: NULL pointer");
+    if (!aligned(W, 2) || !aligned(scales, 4))
+        return fail(MBW_ERR_MISALIGNED, "mbw_quantize_int8_pc: W must be 2-byte aligned, scales 4-byte");
+    cudaError_t e = launch_quantize_int8_pc((const uint16_t*)W, Wq, scales, N, K, (cudaStream_t)stream);
+    return e == cudaSuccess ? MBW_OK : cuda_fail(e, "quantize launch");
 }
 
 mbw_status gemm_skinny_bf16(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,

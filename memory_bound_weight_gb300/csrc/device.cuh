@@ -112,6 +112,35 @@ __device__ __forceinline__ float code_minus(uint32_t n, float zf) {
     return __uint_as_float(0x4B000000u | n) - zf;
 }
 
+// Symmetric INT8 codes (TileInfer, "Pushing further with cheating: INT8
+// quantization") as exact bf16 pairs for the tensor core. A two's-complement
+// byte b is q = (b & 0x7F) - 128 * (b >> 7), so the bf16 pair
+// (0x4300 | (b & 0x7F)) = 128 + (b & 0x7F) minus (0x4300 | (b & 0x80)) = 128
+// or 256 is q exactly: two LOP3 and one bf16 subtract per two codes. Bytes 0
+// and 2 of v become p02, bytes 1 and 3 become p13 (the x operand is permuted
+// to match).
+__device__ __forceinline__ void i8_pairs(uint32_t v, uint32_t& p02, uint32_t& p13) {
+    const uint32_t u = v >> 8;
+    uint32_t a, b, c, d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(a) : "r"(v), "r"(0x007F007Fu), "r"(0x43004300u));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(b) : "r"(v), "r"(0x00800080u), "r"(0x43004300u));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(c) : "r"(u), "r"(0x007F007Fu), "r"(0x43004300u));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(u), "r"(0x00800080u), "r"(0x43004300u));
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(p02) : "r"(a), "r"(b));
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(p13) : "r"(c), "r"(d));
+}
+
+// 8 bf16 x[8w..8w+7] -> pairs (0,2) (1,3) (4,6) (5,7): the order of the INT8
+// pairs above (word u of the codes multiplies x pairs 2u' and 2u'+1 of its 8-x word).
+__device__ __forceinline__ uint4 perm_i8(uint4 v) {
+    uint4 o;
+    o.x = __byte_perm(v.x, v.y, 0x5410);  // x0 | x2 << 16
+    o.y = __byte_perm(v.x, v.y, 0x7632);  // x1 | x3 << 16
+    o.z = __byte_perm(v.z, v.w, 0x5410);  // x4 | x6 << 16
+    o.w = __byte_perm(v.z, v.w, 0x7632);  // x5 | x7 << 16
+    return o;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);

@@ -1,5 +1,5 @@
 // gemv_lat.cu -- latency-oriented GEMV for the small matrices of a decode
-// chain (batch 1..8), INT4 group-64 and BF16.
+// chain (batch 1..8), INT4 group-64, symmetric per-channel INT8 and BF16.
 //
 // In a decode step every GEMV waits for the one before it (its x is the
 // previous kernel's output), so a small matrix costs the chain's release
@@ -27,7 +27,9 @@
 // Arithmetic is that of the mma2 family: codes become exact bf16 (128 + n) -
 // (128 + 8) pairs, products with bf16 x are exact, the tensor core
 // accumulates in fp32 and the group scale multiplies each group's fp32
-// partial. BF16 weights go to the tensor core unchanged.
+// partial. INT8 codes become exact bf16 pairs the same way and the row's
+// fp32 scale multiplies the row's finished sum. BF16 weights go to the
+// tensor core unchanged.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -74,6 +76,16 @@ __device__ __forceinline__ uint4 lat_perm(uint4 v) {
     return o;
 }
 
+// INT8 fragments of one item for one lane: word w of rows g and g+8 -> the A
+// registers of the one MMA of word w (codes 0, 2 | 1, 3 of the word).
+__device__ __forceinline__ void lat_unpack_i8(const u32x8& ra, const u32x8& rb, uint32_t (&A)[8][8]) {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        i8_pairs(ra.v[w], A[w][0], A[w][2]);
+        i8_pairs(rb.v[w], A[w][1], A[w][3]);
+    }
+}
+
 // INT4 fragments of one item for one lane: word w of rows g (wa) and g+8 (wb)
 // -> the A registers of the two MMAs of word w, (q - 8) exact in bf16.
 __device__ __forceinline__ void lat_unpack(const u32x8& ra, const u32x8& rb, uint32_t (&A)[8][8]) {
@@ -97,16 +109,18 @@ __device__ __forceinline__ void lat_unpack(const u32x8& ra, const u32x8& rb, uin
 // Shared memory: per-warp partials [ntmax][WK][16][M], per-CTA sums
 // [ntmax][16][M] (read by the other ranks of a split-K cluster), then one
 // x slot per warp: 72 words (64 + 8 pad words of 16 bytes) per super-block
-// of the warp's k-slice (xsb = min(NI, k-slice length)); then, for the staged
-// variants, the item ring (W x NI x 2 KB).
+// of the warp's k-slice (xsb = min(NI, k-slice length)); then the INT8 row
+// scales of the CTA ([ntmax][16] fp32, `scf` floats, 0 for other formats);
+// then, for the staged variants, the item ring (W x NI x 2 KB).
 __host__ __device__ inline size_t lat_red_floats(int ntmax, int WK, int M) {
     return ((size_t)ntmax * (WK + 1) * 16 * M + 3) / 4 * 4;  // 16-byte aligned end
 }
-__host__ __device__ inline size_t lat_smem_floats(int ntmax, int W, int WK, int M, int xsb) {
-    return lat_red_floats(ntmax, WK, M) + (size_t)W * 72 * 4 * xsb;
+__host__ __device__ inline size_t lat_sc_floats(int fmt, int ntmax) { return fmt == FMT_I8 ? (size_t)ntmax * 16 : 0; }
+__host__ __device__ inline size_t lat_smem_floats(int ntmax, int W, int WK, int M, int xsb, size_t scf) {
+    return lat_red_floats(ntmax, WK, M) + (size_t)W * 72 * 4 * xsb + scf;
 }
-__host__ __device__ inline size_t lat_ring_off(int ntmax, int W, int WK, int M, int xsb) {
-    return (lat_smem_floats(ntmax, W, WK, M, xsb) * 4 + 127) / 128 * 128;
+__host__ __device__ inline size_t lat_ring_off(int ntmax, int W, int WK, int M, int xsb, size_t scf) {
+    return (lat_smem_floats(ntmax, W, WK, M, xsb, scf) * 4 + 127) / 128 * 128;
 }
 
 // W warps = WK along K x WT along the CTA's row tiles. Warp (wk, wt) owns
@@ -119,13 +133,14 @@ __host__ __device__ inline size_t lat_ring_off(int ntmax, int W, int WK, int M, 
 template <int FMT, int W, int WT, int NI, int NPRE, int STG, int LEAN>
 __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     gemv_lat_kernel(const GemvArgs a, const int S) {
-    static_assert(FMT == FMT_G64 || FMT == FMT_BF16, "INT4 group-64 and BF16 only");
-    static_assert(FMT == FMT_G64 || (NPRE == 0 && LEAN == 0), "BF16 needs no unpack");
+    static_assert(FMT == FMT_G64 || FMT == FMT_BF16 || FMT == FMT_I8, "INT4 group-64, INT8 and BF16 only");
+    static_assert(FMT != FMT_BF16 || NPRE == 0, "BF16 needs no unpack");
+    static_assert(FMT == FMT_G64 || LEAN == 0, "the lean path is INT4 only");
     static_assert(NPRE <= NI, "");
     static_assert(!LEAN || (STG && NPRE == 0), "the lean path reads staged items");
     static_assert(W % WT == 0, "");
     constexpr int WK = W / WT;
-    constexpr int BK = (FMT == FMT_BF16) ? 64 : 256;  // k per 128-byte row super-block
+    constexpr int BK = (FMT == FMT_BF16) ? 64 : (FMT == FMT_I8) ? 128 : 256;  // k per 128-byte row super-block
     extern __shared__ float lat_smem[];
 
     pdl_launch_dependents();
@@ -147,8 +162,9 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     const int nb = max(0, min(KB, b0 + BS) - b0);
     const int ntw = (nt > wt) ? (nt - wt + WT - 1) / WT : 0;  // tiles of this warp
     const int total = ntw * nb;  // items of this warp; the plan guarantees total <= NI
-    const size_t rowbytes = (FMT == FMT_BF16) ? (size_t)a.K * 2 : (size_t)a.K / 2;
+    const size_t rowbytes = (FMT == FMT_BF16) ? (size_t)a.K * 2 : (FMT == FMT_I8) ? (size_t)a.K : (size_t)a.K / 2;
     const int xsb = min(NI, BS);  // x super-blocks per warp slot
+    const size_t scf = lat_sc_floats(FMT, ntmax);
 
     // ---------------------------------------------- before the wait ----
     // Items live in registers (STG = 0), or -- past the first NPRE, which are
@@ -157,7 +173,7 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     // so every lane reads back exactly the bytes it copied.
     u32x8 ra[NI], rb[NI];  // 32 bytes of rows g and g+8 per register-held item
     uint32_t rs[NI][2];    // group-64: the 2 fp16 scales of this lane's columns, rows g and g+8
-    uint8_t* ring = reinterpret_cast<uint8_t*>(lat_smem) + lat_ring_off(ntmax, W, WK, mb, xsb) +
+    uint8_t* ring = reinterpret_cast<uint8_t*>(lat_smem) + lat_ring_off(ntmax, W, WK, mb, xsb, scf) +
                     (size_t)warp * NI * 2048 + lane * 16;
 #pragma unroll
     for (int j = 0; j < NI; ++j) {
@@ -190,8 +206,18 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     if (STG) cp_async_commit();
     uint32_t A[NPRE > 0 ? NPRE : 1][8][8];
 #pragma unroll
-    for (int j = 0; j < NPRE; ++j)
-        if (j < total) lat_unpack(ra[j], rb[j], A[j]);
+    for (int j = 0; j < NPRE; ++j) {
+        if (j < total) {
+            if (FMT == FMT_I8)
+                lat_unpack_i8(ra[j], rb[j], A[j]);
+            else
+                lat_unpack(ra[j], rb[j], A[j]);
+        }
+    }
+    // INT8: the fp32 scales of the CTA's rows (weights: read before the wait)
+    float* rsc = lat_smem + lat_red_floats(ntmax, WK, mb) + (size_t)W * 72 * 4 * xsb;
+    if (FMT == FMT_I8)
+        for (int i = threadIdx.x; i < nt * 16; i += W * 32) rsc[i] = __ldg(a.rscale + min(t0 * 16 + i, a.N - 1));
 
     // Addresses of the x words this lane reads after the wait: word i of the
     // warp's x (super-block i / (M * words per row), batch row, word) is
@@ -223,7 +249,8 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     // B fragment of this lane: column n = g.
     //   group-64: n = 4m + j carries batch m, group j of the super-block; lane
     //             (g, q) supplies it only when j == q (x words 8q .. 8q+7);
-    //   BF16:     n = m; x words 2q, 2q+1 of the super-block.
+    //   BF16:     n = m; x words 2q, 2q+1 of the super-block;
+    //   INT8:     n = m; x words 4q .. 4q+3 of the super-block.
     int xm;
     bool xon;
     if (FMT == FMT_G64) {
@@ -233,7 +260,7 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
         xm = g;
         xon = xm < mb;
     }
-    constexpr int XWL = (FMT == FMT_G64) ? 8 : 2;  // x words per B-fragment lane per super-block
+    constexpr int XWL = (FMT == FMT_G64) ? 8 : (FMT == FMT_I8) ? 4 : 2;  // x words per B-fragment lane per super-block
     // The warp reads all the x it needs in one round of 16-byte loads and
     // hands each B-fragment lane its words through a per-warp shared-memory
     // slot (one pad word per 8 keeps those reads conflict-free). Loading per
@@ -251,13 +278,14 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
 #pragma unroll
         for (int r = 0; r < XLD; ++r) {
             const int wi = lane + 32 * r;
-            if (wi < nxw) xslot[wi + (wi >> 3)] = (FMT == FMT_G64) ? lat_perm(v[r]) : v[r];
+            if (wi < nxw)
+                xslot[wi + (wi >> 3)] = (FMT == FMT_G64) ? lat_perm(v[r]) : (FMT == FMT_I8) ? perm_i8(v[r]) : v[r];
         }
     }
     __syncwarp();
     // slot index of this lane's first x word of super-block sb of its k-slice
     auto xword0 = [&](int sb) {
-        return sb * sbw + ((FMT == FMT_G64) ? (min(xm, 1) * 32 + 8 * q) : (g * 8 + 2 * q));
+        return sb * sbw + ((FMT == FMT_G64) ? (min(xm, 1) * 32 + 8 * q) : (FMT == FMT_I8) ? (g * 16 + 4 * q) : (g * 8 + 2 * q));
     };
     uint4 xv[LEAN ? 1 : XWL];
     auto load_x = [&](int sb) {
@@ -349,6 +377,26 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
                     acc[0] = fmaf(f0.y, ds[1], acc[0]);
                     acc[2] = fmaf(f1.x, ds[2], acc[2]);
                     acc[2] = fmaf(f1.y, ds[3], acc[2]);
+                } else if (FMT == FMT_I8) {
+                    uint32_t Aj[8][8];
+                    if (j < NPRE) {
+#pragma unroll
+                        for (int w = 0; w < 8; ++w)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) Aj[w][i] = A[j < NPRE ? j : 0][w][i];
+                    } else {
+                        lat_unpack_i8(ra[j], rb[j], Aj);
+                    }
+                    // four independent accumulator chains of two MMAs each
+                    float d[4][4] = {};
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const uint4 x4 = xv[w >> 1];
+                        lat_mma(d[w & 3], Aj[w][0], Aj[w][1], Aj[w][2], Aj[w][3], (w & 1) ? x4.z : x4.x,
+                                (w & 1) ? x4.w : x4.y);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i] += (d[0][i] + d[1][i]) + (d[2][i] + d[3][i]);
                 } else {
                     const u32x8& wa = ra[j];
                     const u32x8& wb = rb[j];
@@ -406,6 +454,7 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
                 float v = 0.f;
 #pragma unroll
                 for (int w = 0; w < WK; ++w) v += rp[w * 16];
+                if (FMT == FMT_I8) v *= rsc[i];
                 if (row0 + i < a.N) store_out(a.y, row0 + i, v, a.out_f32);
             }
             return;
@@ -420,6 +469,7 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
 #pragma unroll
             for (int w = 0; w < WK; ++w) v += rp[(size_t)w * 16 * mb];
             const int row = row0 + t * 16 + r;
+            if (FMT == FMT_I8) v *= rsc[t * 16 + r];
             if (row < a.N) store_out(a.y, (int64_t)m * a.N + row, v, a.out_f32);
         }
         return;
@@ -445,6 +495,7 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
         const int m = i - (i / mb) * mb;
         float v = 0.f;
         for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(fin + lr * mb + m, s);
+        if (FMT == FMT_I8) v *= rsc[lr];
         if (row0 + lr < a.N) store_out(a.y, (int64_t)m * a.N + row0 + lr, v, a.out_f32);
     }
     cluster.sync();
@@ -465,6 +516,9 @@ const LatEntry kLatG64[] = {
     MBW_L(FMT_G64, 8, 1, 4, 1, 1, 0), MBW_L(FMT_G64, 8, 1, 6, 0, 1, 0), MBW_L(FMT_G64, 16, 2, 2, 0, 1, 1),
     MBW_L(FMT_G64, 16, 2, 3, 0, 1, 1), MBW_L(FMT_G64, 16, 1, 2, 0, 1, 1), MBW_L(FMT_G64, 8, 1, 3, 0, 1, 1),
     MBW_L(FMT_G64, 8, 1, 5, 0, 1, 1)};
+const LatEntry kLatI8[] = {MBW_L(FMT_I8, 8, 1, 1, 1, 0, 0), MBW_L(FMT_I8, 8, 1, 2, 1, 0, 0), MBW_L(FMT_I8, 8, 1, 2, 0, 0, 0),
+                           MBW_L(FMT_I8, 8, 1, 3, 0, 0, 0), MBW_L(FMT_I8, 8, 1, 4, 0, 1, 0), MBW_L(FMT_I8, 8, 1, 6, 0, 1, 0),
+                           MBW_L(FMT_I8, 16, 1, 2, 0, 0, 0), MBW_L(FMT_I8, 4, 1, 2, 1, 0, 0)};
 const LatEntry kLatBf16[] = {MBW_L(FMT_BF16, 8, 1, 2, 0, 0, 0), MBW_L(FMT_BF16, 8, 1, 4, 0, 0, 0),
                              MBW_L(FMT_BF16, 4, 1, 4, 0, 0, 0), MBW_L(FMT_BF16, 16, 1, 2, 0, 0, 0),
                              MBW_L(FMT_BF16, 16, 2, 2, 0, 0, 0), MBW_L(FMT_BF16, 8, 1, 4, 0, 1, 0),
@@ -479,6 +533,10 @@ const LatEntry* lat_table(int fmt, int* n) {
     if (fmt == FMT_BF16) {
         *n = (int)(sizeof(kLatBf16) / sizeof(kLatBf16[0]));
         return kLatBf16;
+    }
+    if (fmt == FMT_I8) {
+        *n = (int)(sizeof(kLatI8) / sizeof(kLatI8[0]));
+        return kLatI8;
     }
     *n = 0;
     return nullptr;
@@ -496,8 +554,9 @@ LatConfig lat_config(int fmt, int idx) {
     return lat_table(fmt, &n)[idx].cfg;
 }
 
-int lat_max_batch(int fmt) { return fmt == FMT_G64 ? 2 : 8; }
-int lat_block_k(int fmt) { return fmt == FMT_BF16 ? 64 : 256; }
+// the per-warp x slot holds 64 words per super-block: M * (x words per row per super-block) <= 64
+int lat_max_batch(int fmt) { return fmt == FMT_G64 ? 2 : fmt == FMT_I8 ? 4 : 8; }
+int lat_block_k(int fmt) { return fmt == FMT_BF16 ? 64 : fmt == FMT_I8 ? 128 : 256; }
 
 // Most items any warp owns under this split (0 if the shape does not fit the family).
 int lat_items_per_warp(int fmt, const LatConfig& c, int64_t N, int64_t K, int split, int occ) {
@@ -521,8 +580,9 @@ size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, 
     const int64_t KB = K / lat_block_k(fmt);
     const int64_t BS = (KB + (int64_t)split * WK - 1) / ((int64_t)split * WK);
     const int xsb = (int)std::min<int64_t>(c.ni, BS);
-    if (c.staged) return lat_ring_off(ntmax, c.warps, WK, M, xsb) + (size_t)c.warps * c.ni * 2048;
-    return lat_smem_floats(ntmax, c.warps, WK, M, xsb) * sizeof(float);
+    const size_t scf = lat_sc_floats(fmt, ntmax);
+    if (c.staged) return lat_ring_off(ntmax, c.warps, WK, M, xsb, scf) + (size_t)c.warps * c.ni * 2048;
+    return lat_smem_floats(ntmax, c.warps, WK, M, xsb, scf) * sizeof(float);
 }
 
 cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {

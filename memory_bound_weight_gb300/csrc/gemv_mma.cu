@@ -1,8 +1,9 @@
 // gemv_mma.cu -- weight-streaming GEMV for sm_103a with the tensor core as the
 // multiply-add unit.
 //
-// Y[m][i] = sum_k X[m][k] * w(i, k) for BF16, INT4 group-64 and AWQ-style INT4
-// group-128 weights and a small batch M (1..8; 1..4 for group-64).
+// Y[m][i] = sum_k X[m][k] * w(i, k) for BF16, INT4 group-64, AWQ-style INT4
+// group-128 and symmetric per-channel INT8 weights (the last in the "mma2"
+// family only) and a small batch M (1..8; 1..4 for group-64).
 //
 // Why mma here: at batch 1 every weight is used for one multiply-add (llm-rs
 // vs vLLM, sec. 2), so at GB300's HBM rate the kernel must retire ~41 INT4
@@ -381,11 +382,16 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
 //   AWQ      : column n = 2m + j, j = group within the super-block, M <= 4;
 //              lane (g,q) holds both groups of batch q.
 //   BF16     : column n = m (M <= 8); lane q's 16 weights feed 4 MMAs.
+//   INT8     : column n = m (M <= 8); a lane's 32 bytes of a row are 32
+//              codes, 8 MMAs per super-block (one per 32-bit word of rows g
+//              and g+8); every code of a row shares the row's fp32 scale,
+//              which multiplies the row's finished sum in the store (TileInfer,
+//              "Pushing further with cheating: INT8 quantization").
 template <int FMT, int W, int U, int ASYNC>
 __global__ void __launch_bounds__(W * 32, 16 / W)
     gemv_mma2_kernel(const GemvArgs a, const int S) {
-    constexpr int BK = (FMT == FMT_BF16) ? 64 : 256;  // k per 128-byte row super-block
-    constexpr int XW = BK / 8;                        // 16-byte x words per super-block
+    constexpr int BK = (FMT == FMT_BF16) ? 64 : (FMT == FMT_I8) ? 128 : 256;  // k per 128-byte row super-block
+    constexpr int XW = BK / 8;                                              // 16-byte x words per super-block
     extern __shared__ uint4 smem_u4[];
 
     pdl_launch_dependents();
@@ -407,7 +413,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     const int b0 = cb0 + warp * BS;
     const int nb = max(0, min(KB, b0 + BS) - b0);
     const int total = nt * nb;
-    const size_t rowbytes = (FMT == FMT_BF16) ? (size_t)a.K * 2 : (size_t)a.K / 2;
+    const size_t rowbytes = (FMT == FMT_BF16) ? (size_t)a.K * 2 : (FMT == FMT_I8) ? (size_t)a.K : (size_t)a.K / 2;
 
     // load cursor (rows g, g+8 of the tile being loaded)
     int lb = 0, lt = 0;
@@ -438,7 +444,10 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     // cp.async ring (ASYNC): slot u of this warp holds chunk c of lane l at
     // ((warp * U + u) * 4 + c) * 512 + l * 16, so 8-lane phases touch 128
     // contiguous bytes; each lane reads back only the bytes it copied.
-    uint8_t* aring = reinterpret_cast<uint8_t*>(smem_u4) + (L.total + 127) / 128 * 128 +
+    // INT8: the fp32 scales of the CTA's rows, read before the wait (they are weights)
+    float* rsc = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.total);
+    const size_t sc_bytes = (FMT == FMT_I8) ? (size_t)L.ntmax * 16 * 4 : 0;
+    uint8_t* aring = reinterpret_cast<uint8_t*>(smem_u4) + (L.total + sc_bytes + 127) / 128 * 128 +
                      (size_t)warp * U * 4 * 512 + lane * 16;
     uint32_t rs[U][2];   // group-64: 2 fp16 scales per row; AWQ: 2 fp16 scales per row
     uint32_t rz[U];      // AWQ: zero-point byte of rows g (bits 0-7) and g+8 (bits 8-15)
@@ -456,7 +465,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
             rw[u][2] = ld_stream16(wp1);
             rw[u][3] = ld_stream16(wp1 + 16);
         }
-        if (FMT != FMT_BF16) {
+        if (FMT == FMT_G64 || FMT == FMT_AWQ) {
             rs[u][0] = (uint32_t)ld_ro_u16(sp0) | ((uint32_t)ld_ro_u16(sp0 + 1) << 16);
             rs[u][1] = (uint32_t)ld_ro_u16(sp1) | ((uint32_t)ld_ro_u16(sp1 + 1) << 16);
         }
@@ -479,6 +488,9 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
         if (ASYNC) cp_async_commit();  // one group per step, empty past the end
     }
 
+    if (FMT == FMT_I8)
+        for (int i = threadIdx.x; i < nt * 16; i += W * 32) rsc[i] = __ldg(a.rscale + min(t0 * 16 + i, a.N - 1));
+
     prefetch_l2_grid_share(a.x, (size_t)a.M * a.K * 2);
     pdl_wait();
 
@@ -490,7 +502,10 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
             const int m = i / L.xwords;
             const int wi = i - m * L.xwords;
             if (wi < cwords) v = ld_ro16(a.x + (size_t)m * a.K + (size_t)cb0 * BK + (size_t)wi * 8);
-            if (FMT != FMT_BF16) v = perm_pairs(v);
+            if (FMT == FMT_I8)
+                v = perm_i8(v);
+            else if (FMT != FMT_BF16)
+                v = perm_pairs(v);
         }
         xs[i] = v;
     }
@@ -509,8 +524,8 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
         xm = g;
         xon = xm < mb;
     }
-    // lane's x words of a super-block: INT4 words 8q .. 8q+7, BF16 words 2q, 2q+1
-    const int xoff = (FMT == FMT_BF16) ? 2 * q : 8 * q;
+    // lane's x words of a super-block: INT4 words 8q .. 8q+7, INT8 4q .. 4q+3, BF16 2q, 2q+1
+    const int xoff = (FMT == FMT_BF16) ? 2 * q : (FMT == FMT_I8) ? 4 * q : 8 * q;
     const uint4* xbase = xon ? xs + (size_t)xm * L.xwords + (size_t)(b0 - cb0) * XW + xoff : xs + (size_t)mb * L.xwords;
     const int xstep = xon ? XW : 0;
     const uint4* xp = xbase;
@@ -547,6 +562,20 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
                     mma_bf16_16816(acc2, a0.z, c0.z, a0.w, c0.w, x0.z, x0.w);
                     mma_bf16_16816(acc, a1.x, c1.x, a1.y, c1.y, x1.x, x1.y);
                     mma_bf16_16816(acc2, a1.z, c1.z, a1.w, c1.w, x1.z, x1.w);
+                } else if (FMT == FMT_I8) {
+                    const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                    const uint32_t wb[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        uint32_t p0, p1, p2, p3;
+                        i8_pairs(wa[w], p0, p2);
+                        i8_pairs(wb[w], p1, p3);
+                        const uint4 xv = xp[w >> 1];
+                        if (w & 1)
+                            mma_bf16_16816(acc2, p0, p1, p2, p3, xv.z, xv.w);
+                        else
+                            mma_bf16_16816(acc, p0, p1, p2, p3, xv.x, xv.y);
+                    }
                 } else {
                     uint32_t zz0, zz1;
                     if (FMT == FMT_G64) {
@@ -593,7 +622,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
                 xp += xstep;
                 if (++cb == nb) {
                     float* rp = red + ((size_t)(ct * W + warp) * 16) * mb;
-                    if (FMT == FMT_BF16) {
+                    if (FMT == FMT_BF16 || FMT == FMT_I8) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
                         if (2 * q < mb) {
@@ -650,7 +679,9 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
         __syncthreads();
         for (int i = threadIdx.x; i < nout; i += W * 32) {
             const int m = i / (nt * 16), lr = i - m * nt * 16;
-            if (row0 + lr < a.N) store_out(a.y, (int64_t)m * a.N + row0 + lr, fin[lr * mb + m], a.out_f32);
+            if (row0 + lr < a.N)
+                store_out(a.y, (int64_t)m * a.N + row0 + lr, (FMT == FMT_I8) ? fin[lr * mb + m] * rsc[lr] : fin[lr * mb + m],
+                          a.out_f32);
         }
         return;
     }
@@ -663,6 +694,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
         const int m = i / span, lr = lo + (i - m * span);
         float v = 0.f;
         for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(fin + lr * mb + m, s);
+        if (FMT == FMT_I8) v *= rsc[lr];
         if (row0 + lr < a.N) store_out(a.y, (int64_t)m * a.N + row0 + lr, v, a.out_f32);
     }
     cluster.sync();
@@ -697,6 +729,8 @@ static const MmaEntry kMma2G64[] = {MBW_M2(FMT_G64, 8, 2, 0), MBW_M2(FMT_G64, 8,
                                     MBW_M2(FMT_G64, 4, 6, 1)};
 static const MmaEntry kMma2Awq[] = {MBW_M2(FMT_AWQ, 8, 2, 0), MBW_M2(FMT_AWQ, 8, 3, 0), MBW_M2(FMT_AWQ, 4, 2, 0),
                                     MBW_M2(FMT_AWQ, 8, 4, 1), MBW_M2(FMT_AWQ, 8, 6, 1)};
+static const MmaEntry kMma2I8[] = {MBW_M2(FMT_I8, 8, 2, 0), MBW_M2(FMT_I8, 8, 3, 0), MBW_M2(FMT_I8, 4, 3, 0),
+                                   MBW_M2(FMT_I8, 8, 4, 1), MBW_M2(FMT_I8, 8, 6, 1), MBW_M2(FMT_I8, 4, 8, 1)};
 #undef MBW_M2
 
 static const MmaEntry* mma2_table(int fmt, int* n) {
@@ -707,9 +741,15 @@ static const MmaEntry* mma2_table(int fmt, int* n) {
         case FMT_G64:
             *n = (int)(sizeof(kMma2G64) / sizeof(kMma2G64[0]));
             return kMma2G64;
-        default:
+        case FMT_AWQ:
             *n = (int)(sizeof(kMma2Awq) / sizeof(kMma2Awq[0]));
             return kMma2Awq;
+        case FMT_I8:
+            *n = (int)(sizeof(kMma2I8) / sizeof(kMma2I8[0]));
+            return kMma2I8;
+        default:
+            *n = 0;
+            return nullptr;
     }
 }
 
@@ -725,11 +765,12 @@ MmaConfig mma2_config(int fmt, int idx) {
 }
 
 int mma2_max_batch(int fmt) { return fmt == FMT_G64 ? 2 : fmt == FMT_AWQ ? 4 : 8; }
-int mma2_block_k(int fmt) { return fmt == FMT_BF16 ? 64 : 256; }
+int mma2_block_k(int fmt) { return fmt == FMT_BF16 ? 64 : fmt == FMT_I8 ? 128 : 256; }
 
 size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
     const int G = mma_row_groups(N, split, occ);
-    const size_t base = mma_smem_layout(mma2_block_k(fmt), K, (int)N, M, c.warps, split, G).total;
+    const MmaSmem L = mma_smem_layout(mma2_block_k(fmt), K, (int)N, M, c.warps, split, G);
+    const size_t base = L.total + (fmt == FMT_I8 ? (size_t)L.ntmax * 16 * 4 : 0);  // + INT8 row scales
     if (!c.async) return base;
     return (base + 127) / 128 * 128 + (size_t)c.warps * c.u * 4 * 512;
 }
@@ -737,7 +778,7 @@ size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M,
 cudaError_t launch_gemv_mma2(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
     int n;
     const MmaEntry* t = mma2_table(fmt, &n);
-    if (p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > mma2_max_batch(fmt)) return cudaErrorInvalidValue;
+    if (t == nullptr || p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > mma2_max_batch(fmt)) return cudaErrorInvalidValue;
     const MmaEntry& e = t[p.cfg];
     const int G = mma_row_groups(a.N, p.split, p.occ);
     const size_t smem = mma2_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
@@ -776,9 +817,12 @@ static const MmaEntry* mma_table(int fmt, int* n) {
         case FMT_G64:
             *n = (int)(sizeof(kMmaG64) / sizeof(kMmaG64[0]));
             return kMmaG64;
-        default:
+        case FMT_AWQ:
             *n = (int)(sizeof(kMmaAwq) / sizeof(kMmaAwq[0]));
             return kMmaAwq;
+        default:
+            *n = 0;
+            return nullptr;
     }
 }
 

@@ -289,9 +289,12 @@ static const Entry* table(int fmt, int* n) {
         case FMT_G64:
             *n = (int)(sizeof(kG64) / sizeof(kG64[0]));
             return kG64;
-        default:
+        case FMT_AWQ:
             *n = (int)(sizeof(kAwq) / sizeof(kAwq[0]));
             return kAwq;
+        default:
+            *n = 0;
+            return nullptr;
     }
 }
 

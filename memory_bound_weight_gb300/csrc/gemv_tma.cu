@@ -438,9 +438,12 @@ static const TmaEntry* tma_table(int fmt, int* n) {
         case FMT_G64:
             *n = (int)(sizeof(kTmaG64) / sizeof(kTmaG64[0]));
             return kTmaG64;
-        default:
+        case FMT_AWQ:
             *n = (int)(sizeof(kTmaAwq) / sizeof(kTmaAwq[0]));
             return kTmaAwq;
+        default:
+            *n = 0;
+            return nullptr;
     }
 }
 

@@ -10,10 +10,10 @@
 
 namespace mbw {
 
-enum Fmt : int { FMT_BF16 = 0, FMT_G64 = 1, FMT_AWQ = 2 };
+enum Fmt : int { FMT_BF16 = 0, FMT_G64 = 1, FMT_AWQ = 2, FMT_I8 = 3 };
 
 // Arguments of one weight-streaming GEMV launch. A "chunk" is 16 bytes of one
-// weight row: 8 bf16 weights or 32 INT4 codes.
+// weight row: 8 bf16 weights, 32 INT4 codes or 16 INT8 codes.
 struct GemvArgs {
     const uint8_t* W;        // weight rows, `chunks` 16-byte chunks each
     const uint16_t* scales;  // fp16 group scales [N][groups] (INT4 only)
@@ -26,6 +26,7 @@ struct GemvArgs {
     int groups;        // scale groups per row
     int zstride;       // zero-point bytes per row
     int out_f32;       // 1: write fp32 y
+    const float* rscale;  // fp32 scale per weight row [N] (INT8 only)
 };
 
 // One instantiation of the CUDA-core streaming kernel.
@@ -120,6 +121,9 @@ int tma_take_fault();  // 1 if a bounded device wait expired since the last call
 
 cudaError_t launch_dequant(int fmt, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zeros,
                            float* out, int64_t N, int64_t K, cudaStream_t s);
+// INT8 load-time quantizer (quantize.cu).
+cudaError_t launch_quantize_int8_pc(const uint16_t* W, int8_t* Wq, float* scales, int64_t N, int64_t K,
+                                    cudaStream_t s);
 
 // Plan cache (plan.cu).
 Plan plan_lookup(int op, int64_t M, int64_t N, int64_t K, cudaStream_t s);

@@ -34,11 +34,12 @@ static int fmt_of_op(int op) {
     switch (op) {
         case MBW_OP_GEMV_INT4_G64: return FMT_G64;
         case MBW_OP_GEMV_INT4_AWQ_G128: return FMT_AWQ;
+        case MBW_OP_GEMV_INT8_PC: return FMT_I8;
         default: return FMT_BF16;
     }
 }
 
-static int chunks_of(int fmt, int64_t K) { return (int)(fmt == FMT_BF16 ? K / 8 : K / 32); }
+static int chunks_of(int fmt, int64_t K) { return (int)(fmt == FMT_BF16 ? K / 8 : fmt == FMT_I8 ? K / 16 : K / 32); }
 
 static size_t simt_smem(int fmt, const SimtConfig& c, int64_t K, int split) {
     GemvArgs a{};
@@ -204,6 +205,19 @@ Plan plan_default(int op, int64_t M, int64_t N, int64_t K) {
         while (!plan_valid(fmt, p, M, N, K) && p.split > 1) --p.split;
         return p;
     }
+    if (fmt == FMT_I8) {
+        // INT8 runs on the "mma2" and latency families only: 8 warps, 3
+        // super-blocks in flight in registers, one CTA per SM; split K over a
+        // cluster while there are fewer 16-row tiles than SMs.
+        const int64_t tiles = (N + 15) / 16;
+        Plan p{PLAN_MMA2, 1, 1, 1};
+        while (p.split < 8 && tiles * p.split < sms && (int64_t)8 * p.split * 2 <= K / 128) p.split *= 2;
+        while (!plan_valid(fmt, p, Mb, N, K) && p.split > 1) p.split /= 2;
+        if (plan_valid(fmt, p, Mb, N, K)) return p;
+        const std::vector<Plan> c = candidates(op, M, N, K);
+        if (!c.empty()) return c.front();
+        return p;
+    }
     // Tensor-core family: 8 warps, 4 blocks in flight, one CTA per SM; split K
     // over a cluster while there are fewer 16-row tiles than SMs.
     int cfg = 0;
@@ -252,7 +266,7 @@ Plan plan_lookup(int op, int64_t M, int64_t N, int64_t K, cudaStream_t s) {
 
 std::string plan_to_string(int op, const Plan& p) {
     const int fmt = fmt_of_op(op);
-    const char* fs = fmt == FMT_BF16 ? "bf16" : fmt == FMT_G64 ? "int4_g64" : "int4_awq_g128";
+    const char* fs = fmt == FMT_BF16 ? "bf16" : fmt == FMT_G64 ? "int4_g64" : fmt == FMT_I8 ? "int8_pc" : "int4_awq_g128";
     char buf[192];
     if (p.kind == PLAN_TC) {
         if (fmt == FMT_AWQ)
@@ -301,16 +315,17 @@ cudaError_t launch_plan(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t 
 static size_t weight_bytes(int fmt, int64_t N, int64_t K) {
     if (fmt == FMT_BF16) return (size_t)N * K * 2;
     if (fmt == FMT_G64) return (size_t)N * K / 2 + (size_t)N * (K / 64) * 2;
+    if (fmt == FMT_I8) return (size_t)N * K + (size_t)N * 4;
     const int64_t G = K / 128;
     return (size_t)N * K / 2 + (size_t)N * G * 2 + (size_t)N * ((G + 1) / 2);
 }
 
 static bool shape_ok(int op, int64_t M, int64_t N, int64_t K) {
-    if (op < MBW_OP_GEMV_BF16 || op > MBW_OP_GEMM_SKINNY_BF16) return false;
+    if (op < MBW_OP_GEMV_BF16 || op > MBW_OP_GEMV_INT8_PC) return false;
     if (M < 1 || N < 1 || K < 1 || N > 0x7FFFFFFF || K > 0x7FFFFFFF || M > 0x7FFFFFFF) return false;
     if (op == MBW_OP_GEMV_INT4_G64 && M != 1) return false;
     const int fmt = fmt_of_op(op);
-    const int64_t kunit = fmt == FMT_BF16 ? 8 : fmt == FMT_G64 ? 64 : 128;
+    const int64_t kunit = fmt == FMT_BF16 ? 8 : fmt == FMT_G64 ? 64 : 128;  // AWQ and INT8: 128
     return K % kunit == 0;
 }
 
@@ -418,7 +433,7 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
         a.groups = (int)(fmt == FMT_G64 ? K / 64 : fmt == FMT_AWQ ? K / 128 : 0);
         a.zstride = (a.groups + 1) / 2;
         a.out_f32 = 0;
-        const size_t codes = fmt == FMT_BF16 ? (size_t)N * K * 2 : (size_t)N * K / 2;
+        const size_t codes = fmt == FMT_BF16 ? (size_t)N * K * 2 : fmt == FMT_I8 ? (size_t)N * K : (size_t)N * K / 2;
         const int slices = (int)((Mb + a.M - 1) / a.M);  // launches per call at this batch
         cudaGraph_t g = nullptr;
         cudaGraphExec_t ge = nullptr;
@@ -429,6 +444,7 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
             a.W = wbuf + (size_t)i * wstride;
             a.scales = (const uint16_t*)(a.W + codes);
             a.zeros = (const uint8_t*)(a.W + codes + (size_t)N * a.groups * 2);
+            a.rscale = (const float*)(a.W + codes);
             for (int sl = 0; sl < slices && le == cudaSuccess; ++sl) le = launch_plan(fmt, p, a, stream);
         }
         e = cudaStreamEndCapture(stream, &g);

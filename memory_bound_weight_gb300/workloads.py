@@ -16,6 +16,7 @@ from dataclasses import dataclass
 FMT_BF16 = "bf16"
 FMT_INT4_G64 = "int4_g64"
 FMT_INT4_AWQ_G128 = "int4_awq_g128"
+FMT_INT8_PC = "int8_pc"
 
 
 @dataclass(frozen=True)
@@ -39,6 +40,8 @@ def weight_bytes(fmt: str, N: int, K: int) -> int:
     if fmt == FMT_INT4_AWQ_G128:
         G = K // 128
         return N * K // 2 + 2 * N * G + N * ((G + 1) // 2)
+    if fmt == FMT_INT8_PC:
+        return N * K + 4 * N
     raise ValueError(fmt)
 
 
@@ -83,6 +86,18 @@ QWEN25_7B_LAYER = (
 QWEN25_7B_LAYERS = 28
 QWEN25_7B_HEAD = Mat("lm_head", 152064, 3584)
 
+# Qwen3-4B: hidden 2560, MLP 9728, 36 layers, 32 query heads and 8 KV heads
+# of 128 dims, vocabulary 151936 (the model of TileInfer's INT8 measurements:
+# every linear layer and the lm_head in INT8, about 4 GB per token). The
+# projections that share an input are concatenated: [Wq; Wk; Wv] = 6144 rows,
+# [Wgate; Wup] = 19456 rows.
+QWEN3_4B_LAYER_FUSED = (
+    Mat("qkv", 4096 + 1024 + 1024, 2560), Mat("o", 2560, 4096), Mat("gate_up", 2 * 9728, 2560),
+    Mat("down", 2560, 9728),
+)
+QWEN3_4B_LAYERS = 36
+QWEN3_4B_HEAD = Mat("lm_head", 151936, 2560)
+
 # The four TinyLlama-shaped INT4 matrices of tinyinfer's per-matrix bandwidth table.
 TINYLLAMA_TABLE_SHAPES = (
     Mat("q/o", 2048, 2048), Mat("gate/up", 5632, 2048), Mat("down", 2048, 5632),
@@ -111,6 +126,10 @@ def tinyllama_step(fused: bool = False) -> list[Mat]:
 
 def qwen25_7b_step() -> list[Mat]:
     return decode_step(QWEN25_7B_LAYER, QWEN25_7B_LAYERS, QWEN25_7B_HEAD)
+
+
+def qwen3_4b_step() -> list[Mat]:
+    return decode_step(QWEN3_4B_LAYER_FUSED, QWEN3_4B_LAYERS, QWEN3_4B_HEAD)
 
 
 def step_weight_bytes(mats, fmt: str, head_fmt: str | None = None) -> int:

@@ -84,6 +84,16 @@ A16c = 0x30000
     (lambda L: L.gemm_skinny_bf16(A16, A16b, A16c, 4, 8, 12, None, 0, None), 3),
     (lambda L: L.gemm_skinny_bf16(A16, A16b, A16c + 4, 4, 8, 16, None, 0, None), 2),
     (lambda L: L.gemm_skinny_bf16(A16, A16b, A16c, 0, 8, 16, None, 0, None), 0),
+    (lambda L: L.gemv_int8_pc(A16, A16b, A16c, A16, 1, 8, 192, None, 0, None), 3),
+    (lambda L: L.gemv_int8_pc(A16, A16b + 2, A16c, A16, 1, 8, 256, None, 0, None), 2),
+    (lambda L: L.gemv_int8_pc(A16 + 8, A16b, A16c, A16, 1, 8, 256, None, 0, None), 2),
+    (lambda L: L.gemv_int8_pc(A16, None, A16c, A16, 1, 8, 256, None, 0, None), 1),
+    (lambda L: L.gemv_int8_pc(A16, A16b, A16c, A16, 0, 8, 256, None, 0, None), 0),
+    (lambda L: L.gemv_int8_pc(A16, A16b, A16c, A16, 1, -8, 256, None, 0, None), 1),
+    (lambda L: L.mbw_quantize_int8_pc(A16, A16b, None, 8, 64, None), 1),
+    (lambda L: L.mbw_quantize_int8_pc(A16 + 1, A16b, A16c, 8, 64, None), 2),
+    (lambda L: L.mbw_quantize_int8_pc(A16, A16b, A16c + 2, 8, 64, None), 2),
+    (lambda L: L.mbw_quantize_int8_pc(A16, A16b, A16c, 0, 64, None), 0),
     (lambda L: L.mbw_dequant_int4_g64(A16, A16b, A16c, 4, 100, None), 3),
     (lambda L: L.mbw_dequant_int4_awq_g128(A16, A16b, None, A16c, 4, 128, None), 1),
     (lambda L: L.mbw_set_output_fp32(2), 1),
@@ -98,7 +108,8 @@ def test_argument_errors_without_cuda(L, call, expect):
 
 def test_planner_host_logic(L):
     # candidate enumeration and plan description run on the host
-    for op, M, N, K in [(1, 1, 2048, 2048), (2, 1, 2048, 5632), (3, 16, 3584, 18944), (4, 8, 18944, 3584)]:
+    for op, M, N, K in [(1, 1, 2048, 2048), (2, 1, 2048, 5632), (3, 16, 3584, 18944), (4, 8, 18944, 3584),
+                        (5, 1, 9728, 2560), (5, 8, 2560, 9728)]:
         n = L.mbw_plan_candidates(op, M, N, K)
         assert n >= 1
         buf = ctypes.create_string_buffer(256)
@@ -106,6 +117,9 @@ def test_planner_host_logic(L):
         assert b"split_k=" in buf.value
     assert L.mbw_plan_candidates(2, 1, 8, 96) == 0  # K not a multiple of 64
     assert L.mbw_plan_candidates(7, 1, 8, 64) == 0
+    assert L.mbw_plan_candidates(5, 1, 8, 192) == 0  # INT8: K not a multiple of 128
+    buf = ctypes.create_string_buffer(256)
+    assert L.mbw_plan_describe(5, 1, 9728, 2560, buf, 256) == 0 and b"int8_pc" in buf.value
     assert L.mbw_workspace_bytes(1, 1, 2048, 2048) == 0
 
 

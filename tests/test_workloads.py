@@ -74,3 +74,16 @@ def test_fused_tinyllama_step_streams_the_same_weights():
     for fmt in (wl.FMT_BF16, wl.FMT_INT4_G64, wl.FMT_INT4_AWQ_G128):
         assert wl.step_weight_bytes(a, fmt) == wl.step_weight_bytes(b, fmt)
     assert wl.step_params(a) == wl.step_params(b)
+
+
+def test_qwen3_4b_int8_step_is_about_4_gb():
+    """TileInfer, 'Pushing further with cheating: INT8 quantization': INT8
+    weights halve the Qwen3-4B step from ~8 GB of BF16 weights to ~4 GB."""
+    mats = wl.qwen3_4b_step()
+    assert len(mats) == 4 * 36 + 1
+    b8 = wl.step_weight_bytes(mats, wl.FMT_INT8_PC)
+    b16 = wl.step_weight_bytes(mats, wl.FMT_BF16)
+    assert 3.9e9 < b8 < 4.1e9 and 7.9e9 < b16 < 8.1e9
+    # the per-channel scales add 4 bytes per output row
+    assert b8 - sum(m.N * m.K for m in mats) == 4 * sum(m.N for m in mats)
+    assert abs(b8 / b16 - 0.5) < 1e-3
