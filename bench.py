@@ -47,6 +47,10 @@ TRAFFIC = {
     # 2 launches, dram__bytes_read.sum 12,322,048 + dram__bytes_write.sum 0 per launch
     # (profiles/gemv_lat_int4_g64_11264x2048.md)
     ("65175de089367b3b", "11264x2048"): 12322048,
+    # gemv_mma2 on the fused gate_up matrices (symmetric INT8, 19456x2560): ncu --set full,
+    # 1 launch, dram__bytes_read.sum 49,944,064 + dram__bytes_write.sum 2,048
+    # (profiles/gemv_mma2_int8_19456x2560.md)
+    ("7fbf9c1f6e5275d3", "19456x2560"): 49946112,
 }
 
 

@@ -16,8 +16,10 @@
  *
  * Conventions shared by every call below:
  *   - Pointers are device pointers on the current CUDA device, row-major and
- *     contiguous, 16-byte aligned (MBW_ERR_MISALIGNED otherwise). The caller
- *     owns every buffer; the library never allocates on a call path.
+ *     contiguous, 16-byte aligned (MBW_ERR_MISALIGNED otherwise); the weight
+ *     (code) pointer W / Wq must be 32-byte aligned, because the kernels read
+ *     weights with 256-bit loads. The caller owns every buffer; the library
+ *     never allocates on a call path.
  *   - bf16 = IEEE bfloat16, fp16 = IEEE binary16, passed as raw bits.
  *   - Accumulation is fp32; the output is rounded to bf16 (round to nearest
  *     even) unless mbw_set_output_fp32(1) is in effect on the calling thread.

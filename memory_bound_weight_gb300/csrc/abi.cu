@@ -99,8 +99,8 @@ mbw_status gemv_bf16(const void* W, const void* x, void* y, int64_t N, int64_t K
     if (st != MBW_OK) return st;
     if (N == 0) return MBW_OK;
     if (!y || (K > 0 && (!W || !x))) return fail(MBW_ERR_INVALID_ARG, "gemv_bf16: NULL pointer");
-    if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 16))
-        return fail(MBW_ERR_MISALIGNED, "gemv_bf16: W, x and y must be 16-byte aligned");
+    if (!aligned(W, 32) || !aligned(x, 16) || !aligned(y, 16))
+        return fail(MBW_ERR_MISALIGNED, "gemv_bf16: W must be 32-byte aligned, x and y 16-byte");
     if (K == 0) return zero_output(y, 1, N, (cudaStream_t)stream);
     return run_simt(FMT_BF16, MBW_OP_GEMV_BF16, (const uint8_t*)W, nullptr, nullptr, (const uint16_t*)x, y, 1, N,
                     K, (cudaStream_t)stream);
@@ -114,8 +114,8 @@ mbw_status gemv_int4_g64(const uint8_t* Wq, const void* scales, const void* x, v
     if (st != MBW_OK) return st;
     if (N == 0) return MBW_OK;
     if (!y || (K > 0 && (!Wq || !scales || !x))) return fail(MBW_ERR_INVALID_ARG, "gemv_int4_g64: NULL pointer");
-    if (!aligned(Wq, 16) || !aligned(x, 16) || !aligned(y, 16) || !aligned(scales, 2))
-        return fail(MBW_ERR_MISALIGNED, "gemv_int4_g64: Wq, x and y must be 16-byte aligned, scales 2-byte");
+    if (!aligned(Wq, 32) || !aligned(x, 16) || !aligned(y, 16) || !aligned(scales, 2))
+        return fail(MBW_ERR_MISALIGNED, "gemv_int4_g64: Wq must be 32-byte aligned, x and y 16-byte, scales 2-byte");
     if (K == 0) return zero_output(y, 1, N, (cudaStream_t)stream);
     return run_simt(FMT_G64, MBW_OP_GEMV_INT4_G64, Wq, (const uint16_t*)scales, nullptr, (const uint16_t*)x, y, 1,
                     N, K, (cudaStream_t)stream);
@@ -131,8 +131,9 @@ mbw_status gemv_int4_awq_g128(const uint8_t* Wq, const void* scales, const uint8
     if (N == 0 || M == 0) return MBW_OK;
     if (!Y || (K > 0 && (!Wq || !scales || !zeros || !X)))
         return fail(MBW_ERR_INVALID_ARG, "gemv_int4_awq_g128: NULL pointer");
-    if (!aligned(Wq, 16) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(scales, 2))
-        return fail(MBW_ERR_MISALIGNED, "gemv_int4_awq_g128: Wq, X and Y must be 16-byte aligned, scales 2-byte");
+    if (!aligned(Wq, 32) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(scales, 2))
+        return fail(MBW_ERR_MISALIGNED,
+                    "gemv_int4_awq_g128: Wq must be 32-byte aligned, X and Y 16-byte, scales 2-byte");
     if (K == 0) return zero_output(Y, M, N, (cudaStream_t)stream);
     return run_simt(FMT_AWQ, MBW_OP_GEMV_INT4_AWQ_G128, Wq, (const uint16_t*)scales, zeros, (const uint16_t*)X, Y,
                     M, N, K, (cudaStream_t)stream);
@@ -146,8 +147,8 @@ mbw_status gemv_int8_pc(const int8_t* Wq, const float* scales, const void* X, vo
     if (st != MBW_OK) return st;
     if (N == 0 || M == 0) return MBW_OK;
     if (!Y || (K > 0 && (!Wq || !scales || !X))) return fail(MBW_ERR_INVALID_ARG, "gemv_int8_pc: NULL pointer");
-    if (!aligned(Wq, 16) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(scales, 4))
-        return fail(MBW_ERR_MISALIGNED, "gemv_int8_pc: Wq, X and Y must be 16-byte aligned, scales 4-byte");
+    if (!aligned(Wq, 32) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(scales, 4))
+        return fail(MBW_ERR_MISALIGNED, "gemv_int8_pc: Wq must be 32-byte aligned, X and Y 16-byte, scales 4-byte");
     if (K == 0) return zero_output(Y, M, N, (cudaStream_t)stream);
     return run_simt(FMT_I8, MBW_OP_GEMV_INT8_PC, (const uint8_t*)Wq, nullptr, nullptr, (const uint16_t*)X, Y, M, N,
                     K, (cudaStream_t)stream, scales);
@@ -173,8 +174,8 @@ mbw_status gemm_skinny_bf16(const void* X, const void* W, void* Y, int64_t M, in
     if (st != MBW_OK) return st;
     if (N == 0 || M == 0) return MBW_OK;
     if (!Y || (K > 0 && (!W || !X))) return fail(MBW_ERR_INVALID_ARG, "gemm_skinny_bf16: NULL pointer");
-    if (!aligned(W, 16) || !aligned(X, 16) || !aligned(Y, 16))
-        return fail(MBW_ERR_MISALIGNED, "gemm_skinny_bf16: X, W and Y must be 16-byte aligned");
+    if (!aligned(W, 32) || !aligned(X, 16) || !aligned(Y, 16))
+        return fail(MBW_ERR_MISALIGNED, "gemm_skinny_bf16: W must be 32-byte aligned, X and Y 16-byte");
     if (K == 0) return zero_output(Y, M, N, (cudaStream_t)stream);
     return run_simt(FMT_BF16, MBW_OP_GEMM_SKINNY_BF16, (const uint8_t*)W, nullptr, nullptr, (const uint16_t*)X, Y,
                     M, N, K, (cudaStream_t)stream);

@@ -98,6 +98,24 @@ __device__ __forceinline__ void prefetch_l2_grid_share(const void* base, size_t 
     }
 }
 
+// Shared-memory ring slots of 16 rows x 128 bytes (one row super-block of a
+// 16-row tile). Fragment lane L = 4g + q uses bytes 32q .. 32q+31 of rows g
+// and g+8; its 16-byte chunk c (0, 1: row g; 2, 3: row g+8) sits at
+// c * 512 + L * 16, so its reads are conflict-free. The copies are
+// sector-complete instead: copy instruction j (0..3) moves rows 4j .. 4j+3
+// whole, lane l taking 16-byte chunk l % 8 of row 4j + l / 8, so each 32-byte
+// DRAM sector is requested once (two 16-byte copies per lane of its own 32
+// bytes split every sector over two requests). A lane then reads chunks other
+// lanes copied: __syncwarp after the copies have landed, and before a slot is
+// refilled.
+__device__ __forceinline__ uint32_t ring_copy_dst(int lane, int j) {
+    const int r = 4 * j + (lane >> 3), cc = lane & 7;
+    return (uint32_t)(((r >> 3) * 2 + (cc & 1)) * 512 + (4 * (r & 7) + (cc >> 1)) * 16);
+}
+// Source row (within the tile) and byte offset (within the super-block) of copy j of `lane`.
+__device__ __forceinline__ int ring_copy_row(int lane, int j) { return 4 * j + (lane >> 3); }
+__device__ __forceinline__ int ring_copy_byte(int lane) { return (lane & 7) * 16; }
+
 // ------------------------------------------------------------- formats ----
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -169,12 +169,13 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     // ---------------------------------------------- before the wait ----
     // Items live in registers (STG = 0), or -- past the first NPRE, which are
     // unpacked early -- in a per-warp shared-memory ring filled with cp.async
-    // (STG = 1): 2 KB per item, lane l's 16-byte chunk c at c * 512 + l * 16,
-    // so every lane reads back exactly the bytes it copied.
+    // (STG = 1): one 2 KB ring slot per item (device.cuh: fragment lane L's
+    // chunk c at c * 512 + L * 16, filled by sector-complete copies).
     u32x8 ra[NI], rb[NI];  // 32 bytes of rows g and g+8 per register-held item
     uint32_t rs[NI][2];    // group-64: the 2 fp16 scales of this lane's columns, rows g and g+8
-    uint8_t* ring = reinterpret_cast<uint8_t*>(lat_smem) + lat_ring_off(ntmax, W, WK, mb, xsb, scf) +
-                    (size_t)warp * NI * 2048 + lane * 16;
+    uint8_t* ringw = reinterpret_cast<uint8_t*>(lat_smem) + lat_ring_off(ntmax, W, WK, mb, xsb, scf) +
+                     (size_t)warp * NI * 2048;
+    uint8_t* ring = ringw + lane * 16;
 #pragma unroll
     for (int j = 0; j < NI; ++j) {
         if (j < total) {
@@ -189,11 +190,12 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
                 ra[j] = ld_stream32(p0);
                 rb[j] = ld_stream32(p1);
             } else {
-                uint8_t* d = ring + (size_t)j * 2048;
-                cp_async16(d, p0);
-                cp_async16(d + 512, p0 + 16);
-                cp_async16(d + 1024, p1);
-                cp_async16(d + 1536, p1 + 16);
+                uint8_t* d = ringw + (size_t)j * 2048;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    cp_async16(d + ring_copy_dst(lane, c),
+                               a.W + (size_t)min(tile * 16 + ring_copy_row(lane, c), a.N - 1) * rowbytes +
+                                   (size_t)b * 128 + ring_copy_byte(lane));
             }
             if (FMT == FMT_G64) {
                 const uint16_t* s0 = a.scales + (size_t)r0 * a.groups + (size_t)b * 4 + 2 * (q & 1);
@@ -296,7 +298,10 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
         }
     };
     if (!LEAN && total > 0) load_x(0);
-    if (STG) cp_async_wait<0>();  // this lane's ring bytes have landed (it reads only those)
+    if (STG) {
+        cp_async_wait<0>();  // this lane's copies have landed
+        __syncwarp();        // and so have the other lanes'
+    }
 
     float* red = lat_smem;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};

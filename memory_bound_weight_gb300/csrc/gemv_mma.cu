@@ -423,11 +423,19 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     const uint16_t* sp1 = nullptr;
     const uint8_t* zp0 = nullptr;
     const uint8_t* zp1 = nullptr;
+    const uint8_t* ap[4] = {nullptr, nullptr, nullptr, nullptr};  // ASYNC: sources of this lane's 4 copies
     auto set_rows = [&](int t) {
         const int r0 = min((t0 + t) * 16 + g, a.N - 1);
         const int r1 = min((t0 + t) * 16 + g + 8, a.N - 1);
-        wp0 = a.W + (size_t)r0 * rowbytes + (size_t)b0 * 128 + q * 32;
-        wp1 = a.W + (size_t)r1 * rowbytes + (size_t)b0 * 128 + q * 32;
+        if (ASYNC) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                ap[j] = a.W + (size_t)min((t0 + t) * 16 + ring_copy_row(lane, j), a.N - 1) * rowbytes +
+                        (size_t)b0 * 128 + ring_copy_byte(lane);
+        } else {
+            wp0 = a.W + (size_t)r0 * rowbytes + (size_t)b0 * 128 + q * 32;
+            wp1 = a.W + (size_t)r1 * rowbytes + (size_t)b0 * 128 + q * 32;
+        }
         if (FMT == FMT_G64) {
             sp0 = a.scales + (size_t)r0 * a.groups + (size_t)b0 * 4 + 2 * (q & 1);
             sp1 = a.scales + (size_t)r1 * a.groups + (size_t)b0 * 4 + 2 * (q & 1);
@@ -441,29 +449,33 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     if (nt > 0) set_rows(0);
 
     uint4 rw[U][4];      // [u][0..1] row g (32 bytes), [u][2..3] row g+8 (register ring)
-    // cp.async ring (ASYNC): slot u of this warp holds chunk c of lane l at
-    // ((warp * U + u) * 4 + c) * 512 + l * 16, so 8-lane phases touch 128
-    // contiguous bytes; each lane reads back only the bytes it copied.
+    // cp.async ring (ASYNC): slot u of this warp is one ring slot of 2 KB
+    // (device.cuh: fragment lane L's chunk c at c * 512 + L * 16, filled by
+    // sector-complete copies).
     // INT8: the fp32 scales of the CTA's rows, read before the wait (they are weights)
     float* rsc = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.total);
     const size_t sc_bytes = (FMT == FMT_I8) ? (size_t)L.ntmax * 16 * 4 : 0;
-    uint8_t* aring = reinterpret_cast<uint8_t*>(smem_u4) + (L.total + sc_bytes + 127) / 128 * 128 +
-                     (size_t)warp * U * 4 * 512 + lane * 16;
+    uint8_t* abase = reinterpret_cast<uint8_t*>(smem_u4) + (L.total + sc_bytes + 127) / 128 * 128 +
+                     (size_t)warp * U * 4 * 512;
+    const uint8_t* aring = abase + lane * 16;
     uint32_t rs[U][2];   // group-64: 2 fp16 scales per row; AWQ: 2 fp16 scales per row
     uint32_t rz[U];      // AWQ: zero-point byte of rows g (bits 0-7) and g+8 (bits 8-15)
 
     auto load = [&](int u) {
         if (ASYNC) {
-            uint8_t* d = aring + (size_t)u * 4 * 512;
-            cp_async16(d, wp0);
-            cp_async16(d + 512, wp0 + 16);
-            cp_async16(d + 1024, wp1);
-            cp_async16(d + 1536, wp1 + 16);
+            uint8_t* d = abase + (size_t)u * 4 * 512;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                cp_async16(d + ring_copy_dst(lane, j), ap[j]);
+                ap[j] += 128;
+            }
         } else {
-            rw[u][0] = ld_stream16(wp0);
-            rw[u][1] = ld_stream16(wp0 + 16);
-            rw[u][2] = ld_stream16(wp1);
-            rw[u][3] = ld_stream16(wp1 + 16);
+            const u32x8 v0 = ld_stream32(wp0);  // one 256-bit load per row: whole sectors
+            const u32x8 v1 = ld_stream32(wp1);
+            rw[u][0] = make_uint4(v0.v[0], v0.v[1], v0.v[2], v0.v[3]);
+            rw[u][1] = make_uint4(v0.v[4], v0.v[5], v0.v[6], v0.v[7]);
+            rw[u][2] = make_uint4(v1.v[0], v1.v[1], v1.v[2], v1.v[3]);
+            rw[u][3] = make_uint4(v1.v[4], v1.v[5], v1.v[6], v1.v[7]);
         }
         if (FMT == FMT_G64 || FMT == FMT_AWQ) {
             rs[u][0] = (uint32_t)ld_ro_u16(sp0) | ((uint32_t)ld_ro_u16(sp0 + 1) << 16);
@@ -541,7 +553,8 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
             if (j0 + u < total) {
                 uint4 a0, a1, c0, c1;
                 if (ASYNC) {
-                    cp_async_wait<U - 1>();  // step j0 + u has landed (one group per step)
+                    cp_async_wait<U - 1>();  // this lane's copies of step j0 + u have landed
+                    __syncwarp();            // and so have the other lanes'
                     const uint8_t* d = aring + (size_t)u * 4 * 512;
                     a0 = *reinterpret_cast<const uint4*>(d);
                     a1 = *reinterpret_cast<const uint4*>(d + 512);
@@ -616,6 +629,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
                     }
                 }
                 if (ASYNC) {
+                    __syncwarp();  // every lane has read slot u before it is refilled
                     if (j0 + u + U < total) load(u);
                     cp_async_commit();
                 }

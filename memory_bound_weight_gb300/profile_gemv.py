@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import argparse
 
-OPS = {"bf16": 1, "int4_g64": 2, "int4_awq_g128": 3, "skinny_bf16": 4}
+OPS = {"bf16": 1, "int4_g64": 2, "int4_awq_g128": 3, "skinny_bf16": 4, "int8_pc": 5}
 
 
 def main():
@@ -51,6 +51,10 @@ def main():
         c = ig.int4_codes(0, 0, N, K)
         s = ig.f16_group_scales(0, 0, N, K // 64)
         call = lambda: mbw.gemv_int4_g64(c, s, X[0])  # noqa: E731
+    elif op == 5:
+        q = ig.int8_codes(0, 0, N, K)
+        s = ig.f32_row_scales(0, 0, N)
+        call = lambda: mbw.gemv_int8_pc(q, s, X)  # noqa: E731
     else:
         c = ig.int4_codes(0, 0, N, K)
         s = ig.f16_group_scales(0, 0, N, K // 128)

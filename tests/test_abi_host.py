@@ -84,6 +84,11 @@ A16c = 0x30000
     (lambda L: L.gemm_skinny_bf16(A16, A16b, A16c, 4, 8, 12, None, 0, None), 3),
     (lambda L: L.gemm_skinny_bf16(A16, A16b, A16c + 4, 4, 8, 16, None, 0, None), 2),
     (lambda L: L.gemm_skinny_bf16(A16, A16b, A16c, 0, 8, 16, None, 0, None), 0),
+    (lambda L: L.gemv_bf16(A16 + 16, A16b, A16c, 8, 64, None, 0, None), 2),  # weights need 32 bytes
+    (lambda L: L.gemv_int4_g64(A16 + 16, A16b, A16c, A16c, 8, 128, None, 0, None), 2),
+    (lambda L: L.gemv_int4_awq_g128(A16 + 16, A16b, A16c, A16c, A16, 1, 8, 256, None, 0, None), 2),
+    (lambda L: L.gemm_skinny_bf16(A16, A16b + 16, A16c, 4, 8, 16, None, 0, None), 2),
+    (lambda L: L.gemv_int8_pc(A16 + 16, A16b, A16c, A16, 1, 8, 256, None, 0, None), 2),
     (lambda L: L.gemv_int8_pc(A16, A16b, A16c, A16, 1, 8, 192, None, 0, None), 3),
     (lambda L: L.gemv_int8_pc(A16, A16b + 2, A16c, A16, 1, 8, 256, None, 0, None), 2),
     (lambda L: L.gemv_int8_pc(A16 + 8, A16b, A16c, A16, 1, 8, 256, None, 0, None), 2),

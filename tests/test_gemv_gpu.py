@@ -375,3 +375,38 @@ def test_int4_awq_batched_config_shapes_sampled_rows(orc, M, N, K):
     z = np.stack([gen.u4_zero_points(0, 21, N, G, row0=int(r), rows=1)[0] for r in rows])
     Yr, Ar = orc.gemm_int4_awq_g128(c, s, z, host_bits16(Xd))
     assert_parity(Y[:, torch.from_numpy(rows).cuda()], Yr, Ar, f"awq M={M} {N}x{K} sampled")
+
+
+def test_weights_at_a_32_byte_offset_every_plan(orc):
+    """The weight pointer only has to be 32-byte aligned: every plan of every
+    format runs on weights that start 32 bytes into a larger allocation."""
+    N, K = 300, 1024
+    W, X = bf16_case(1201, N, K)
+    big = torch.empty(N * K + 64, dtype=torch.bfloat16, device="cuda")
+    Wd = big[16:16 + N * K].view(N, K)
+    Wd.copy_(dev_bf16(W))
+    assert Wd.data_ptr() % 64 == 32
+    Y, A = orc.gemm_bf16(W, X)
+    for _, desc in each_plan(mbw.OP_GEMV_BF16, 1, N, K):
+        assert_parity(mbw.gemv_bf16(Wd, dev_bf16(X[0])), Y[0], A[0], f"bf16 offset plan {desc}")
+
+    c, s, X1 = g64_case(1202, N, K)
+    bigc = torch.empty(N * K // 2 + 64, dtype=torch.uint8, device="cuda")
+    cd = bigc[32:32 + N * K // 2].view(N, K // 2)
+    cd.copy_(dev_u8(c))
+    Y, A = orc.gemm_int4_g64(c, s, X1)
+    for _, desc in each_plan(mbw.OP_GEMV_INT4_G64, 1, N, K):
+        assert_parity(mbw.gemv_int4_g64(cd, dev_f16(s), dev_bf16(X1[0])), Y[0], A[0], f"g64 offset plan {desc}")
+
+    q = gen.int8_codes(1203, 0, N, K)
+    sq = gen.f32_row_scales(1203, 0, N)
+    bigq = torch.empty(N * K + 64, dtype=torch.int8, device="cuda")
+    qd = bigq[32:32 + N * K].view(N, K)
+    qd.copy_(torch.from_numpy(q).cuda())
+    Y, A = orc.gemm_int8_pc(q, sq, X)
+    for _, desc in each_plan(mbw.OP_GEMV_INT8_PC, 1, N, K):
+        assert_parity(mbw.gemv_int8_pc(qd, torch.from_numpy(sq).cuda(), dev_bf16(X[0])), Y[0], A[0],
+                      f"int8 offset plan {desc}")
+    # 16 bytes is not enough
+    with pytest.raises(mbw.MbwError):
+        mbw.gemv_int8_pc(bigq[16:16 + N * K].view(N, K), torch.from_numpy(sq).cuda(), dev_bf16(X[0]))
