@@ -77,11 +77,15 @@ class Oracle:
         lib.oracle_gemm_int4_awq_g128.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P]
         lib.oracle_gemm_int8_pc.argtypes = [_P, _P, _P, _I64, _I64, _I64, _P, _P]
         lib.oracle_quantize_int8_pc.argtypes = [_P, _I64, _I64, _P, _P]
+        lib.oracle_rmsnorm_bf16.argtypes = [_P, _P, _I64, _I64, ctypes.c_double, _P]
+        lib.oracle_swiglu.argtypes = [_P, _P, _I64, _P]
+        lib.oracle_add_residual.argtypes = [_P, _P, _I64, _P]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         for f in ("oracle_dequant_int4_g64", "oracle_dequant_int4_awq_g128", "oracle_gemm_bf16",
                   "oracle_gemm_int4_g64", "oracle_gemm_int4_awq_g128", "oracle_gemm_int8_pc",
-                  "oracle_quantize_int8_pc", "oracle_set_num_threads"):
+                  "oracle_quantize_int8_pc", "oracle_rmsnorm_bf16", "oracle_swiglu", "oracle_add_residual",
+                  "oracle_set_num_threads"):
             getattr(lib, f).restype = None
 
     # ---- scalar formats
@@ -180,3 +184,34 @@ class Oracle:
         S = np.empty((N,), dtype=np.float32)
         self.lib.oracle_quantize_int8_pc(_ptr(W), N, K, _ptr(Q), _ptr(S))
         return Q, S
+
+    # ---- fusions around the GEMV
+    def rmsnorm_bf16(self, X: np.ndarray, G: np.ndarray, eps: float):
+        """X bf16 bits (M, K) or (K,), G bf16 bits (K,) -> Xn bf16 bits, same shape as X."""
+        X = np.ascontiguousarray(X, dtype=np.uint16)
+        shape = X.shape
+        X2 = np.atleast_2d(X)
+        M, K = X2.shape
+        G = np.ascontiguousarray(G, dtype=np.uint16)
+        assert G.shape == (K,)
+        out = np.empty((M, K), dtype=np.uint16)
+        self.lib.oracle_rmsnorm_bf16(_ptr(X2), _ptr(G), M, K, float(eps), _ptr(out))
+        return out.reshape(shape)
+
+    def swiglu(self, A: np.ndarray, B: np.ndarray):
+        """silu(A) * B elementwise (float64 arrays of one shape)."""
+        A = np.ascontiguousarray(A, dtype=np.float64)
+        B = np.ascontiguousarray(B, dtype=np.float64)
+        assert A.shape == B.shape
+        out = np.empty_like(A)
+        self.lib.oracle_swiglu(_ptr(A), _ptr(B), A.size, _ptr(out))
+        return out
+
+    def add_residual(self, Y: np.ndarray, R: np.ndarray):
+        """Y (float64) + R (bf16 bits), elementwise."""
+        Y = np.ascontiguousarray(Y, dtype=np.float64)
+        R = np.ascontiguousarray(R, dtype=np.uint16)
+        assert Y.shape == R.shape
+        out = np.empty_like(Y)
+        self.lib.oracle_add_residual(_ptr(Y), _ptr(R), Y.size, _ptr(out))
+        return out

@@ -22,6 +22,12 @@
  *     with z a 4-bit code.
  *   - Batched decode: the same weights used for M activation rows
  *     (llm-rs vs vLLM, sec. 3 "Batching moves decode from memory toward math").
+ *   - Fusions around a GEMV: RMSNorm of x folded into the projection
+ *     (llm-rs vs vLLM, "Decode: from ~35% to ~70% of the ceiling": norms folded
+ *     into the projections), the residual add and the gated SiLU product
+ *     silu(W1.x) * (W3.x) fused into the matmul that produces them (yalm,
+ *     sec. 3.3 "Fusion and a better matmul"; TileInfer: SwiGLU in the GEMV
+ *     epilogue).
  *   - Symmetric INT8 weights with one Float32 scale per output channel
  *     (TileInfer, "Pushing further with cheating: INT8 quantization"): codes
  *     q in [-127, 127], w_ik = s_i * q_ik, and the load-time quantizer that
@@ -35,6 +41,11 @@
  *   - AWQ zero points are packed two per byte, low nibble = even group, with
  *     ceil(G/2) bytes per row (G = K/128 groups);
  *   - accumulation order: k = 0 .. K-1 sequentially in fp64 per output;
+ *   - RMSNorm: xn_k = x_k * g_k / sqrt(mean_k(x_k^2) + eps), computed in fp64 and
+ *     rounded to bf16 (round to nearest even), since the normalised vector is
+ *     the bf16 activation the projection consumes;
+ *   - SiLU(a) = a / (1 + exp(-a)); the fused output is silu(gate) * up, and the
+ *     residual add is y + r, both on the fp64 GEMV results;
  *   - INT8 quantizer: the scale is computed in fp32 (the stored precision),
  *     the quotient w / s in fp32 (IEEE division), rounded to the nearest
  *     integer with ties to even; an all-zero row gets s = 0 and q = 0.
@@ -318,6 +329,47 @@ void oracle_quantize_int8_pc(const uint16_t *W, int64_t N, int64_t K,
             Q[i * K + k] = (int8_t)r;
         }
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Fusions around the GEMV.                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* RMSNorm of each row of X with weight G (the prologue folded into a
+ * projection): Xn[m][k] = bf16(X[m][k] * G[k] / sqrt(mean_k X[m][k]^2 + eps)).
+ * X bf16 [M][K], G bf16 [K], Xn bf16 [M][K]. */
+void oracle_rmsnorm_bf16(const uint16_t *X, const uint16_t *G, int64_t M,
+                         int64_t K, double eps, uint16_t *Xn)
+{
+    for (int64_t m = 0; m < M; m++) {
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; k++) {
+            double x = oracle_bf16_to_double(X[m * K + k]);
+            ss += x * x;
+        }
+        double inv = 1.0 / sqrt(ss / (double)K + eps);
+        for (int64_t k = 0; k < K; k++) {
+            double x = oracle_bf16_to_double(X[m * K + k]);
+            double g = oracle_bf16_to_double(G[k]);
+            Xn[m * K + k] = oracle_double_to_bf16_rne(x * inv * g);
+        }
+    }
+}
+
+/* Gated SiLU of two GEMV results of the same shape: out = silu(A) * B with
+ * silu(a) = a / (1 + exp(-a)) (yalm: F.silu(w1(x)) * w3(x)). */
+void oracle_swiglu(const double *A, const double *B, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = A[i] / (1.0 + exp(-A[i])) * B[i];
+}
+
+/* Residual add: out = Y + R (R bf16), the result written back into the
+ * residual stream (yalm: fused matmul + add_residuals). */
+void oracle_add_residual(const double *Y, const uint16_t *R, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = Y[i] + oracle_bf16_to_double(R[i]);
 }
 
 /* Threads the OpenMP loops above will use (for reporting the CPU baseline). */

@@ -137,6 +137,24 @@ def load_int8_fixture():
     return gemv, quant
 
 
+def load_fusion_fixture():
+    norm, glu, res = [], [], []
+    with open(os.path.join(GOLDEN, "fusion_hand.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            p = line.split()
+            if p[0] == "rmsnorm":
+                norm.append(dict(K=int(p[1]), eps=float(p[2]), x=[int(v, 16) for v in p[3].split(",")],
+                                 g=[int(v, 16) for v in p[4].split(",")], expect=[int(v, 16) for v in p[5].split(",")]))
+            elif p[0] == "swiglu":
+                glu.append((float(p[1]), float(p[2]), float(p[3])))
+            else:
+                res.append((float(p[1]), int(p[2], 16), float(p[3])))
+    return norm, glu, res
+
+
 # --------------------------------------------------------------- pins ----
 def pin_f16_decoder_exhaustive(o):
     bits = np.arange(65536, dtype=np.uint16)
@@ -490,6 +508,57 @@ def pin_int8_quantizer_properties(o):
                 assert q[i, k] == 0
 
 
+def pin_fusions_hand_worked(o):
+    norm, glu, res = load_fusion_fixture()
+    assert len(norm) >= 5 and len(glu) >= 5 and len(res) >= 3
+    for c in norm:
+        got = o.rmsnorm_bf16(np.array([c["x"]], dtype=np.uint16), np.array(c["g"], dtype=np.uint16), c["eps"])
+        assert got[0].tolist() == c["expect"], (c, [hex(v) for v in got[0]])
+    out = o.swiglu(np.array([a for a, _, _ in glu]), np.array([b for _, b, _ in glu]))
+    for (a, b, e), v in zip(glu, out):
+        assert abs(v - e) <= 1e-15 * max(1.0, abs(e)), (a, b, v, e)
+    out = o.add_residual(np.array([y for y, _, _ in res]), np.array([r for _, r, _ in res], dtype=np.uint16))
+    assert out.tolist() == [e for _, _, e in res]
+
+
+def pin_rmsnorm_invariants(o):
+    K = 640
+    X = gen.bf16_activations(131, 0, 3, K)
+    G = gen.bf16_weights(131, 1, 1, K)[0]
+    ones = np.full(K, 0x3F80, dtype=np.uint16)
+    xn = o.rmsnorm_bf16(X, G, 0.0)
+    # scale invariance without eps: x * 2^j has the same norm-scaled values exactly
+    for j in (-3, 4):
+        Xj = f64_to_bf16_exact(np_bf16_to_f64(X) * 2.0 ** j)
+        assert np.array_equal(o.rmsnorm_bf16(Xj, G, 0.0), xn)
+    # g * 2 doubles every output exactly; -x negates it
+    G2 = f64_to_bf16_exact(np_bf16_to_f64(G) * 2.0)
+    assert np.array_equal(np_bf16_to_f64(o.rmsnorm_bf16(X, G2, 0.0)), 2.0 * np_bf16_to_f64(xn))
+    Xneg = X ^ np.uint16(0x8000)
+    assert np.array_equal(np_bf16_to_f64(o.rmsnorm_bf16(Xneg, G, 0.0)), -np_bf16_to_f64(xn))
+    # unit weight: the normalised row has mean square 1 (up to bf16 rounding)
+    u = np_bf16_to_f64(o.rmsnorm_bf16(X, ones, 0.0))
+    assert np.all(np.abs(np.mean(u * u, axis=1) - 1.0) < 2.0 ** -7)
+    # a large eps shrinks the outputs toward zero
+    big = np_bf16_to_f64(o.rmsnorm_bf16(X, ones, 1e6))
+    assert np.all(np.abs(big) <= np.abs(np_bf16_to_f64(X)) / 990.0)  # 1/sqrt(1e6 + ~1), then bf16 rounding
+    # batch rows are independent
+    for m in range(3):
+        assert np.array_equal(o.rmsnorm_bf16(X[m], G, 1e-6), o.rmsnorm_bf16(X, G, 1e-6)[m])
+
+
+def pin_swiglu_identities(o):
+    a = np.random.default_rng(5).standard_normal(2000) * 6.0
+    ones = np.ones_like(a)
+    s = o.swiglu(a, ones)
+    # silu(a) - silu(-a) = a, and silu(a) = a (1 + tanh(a / 2)) / 2 (another closed form)
+    assert np.all(np.abs(s - o.swiglu(-a, ones) - a) <= 1e-14 * (1 + np.abs(a)))
+    assert np.all(np.abs(s - a * (1.0 + np.tanh(a / 2.0)) / 2.0) <= 1e-14 * (1 + np.abs(a)))
+    # linear in the up operand
+    b = np.random.default_rng(6).standard_normal(2000)
+    assert np.allclose(o.swiglu(a, b), s * b, rtol=0, atol=1e-13)
+
+
 PINS = [
     pin_f16_decoder_exhaustive,
     pin_bf16_decoder_exhaustive,
@@ -508,6 +577,9 @@ PINS = [
     pin_int8_exact_and_numpy,
     pin_int8_invariants,
     pin_int8_quantizer_properties,
+    pin_fusions_hand_worked,
+    pin_rmsnorm_invariants,
+    pin_swiglu_identities,
 ]
 
 

@@ -51,6 +51,14 @@ MUTANTS = [
     ("quant_ties_away", "rintf(t)", "roundf(t)", 1),
     ("quant_truncate", "rintf(t)", "truncf(t)", 1),
     ("quant_signed_max", "(float)fabs(oracle_bf16_to_double(W[i * K + k]))", "(float)oracle_bf16_to_double(W[i * K + k])", 1),
+    ("rmsnorm_mean_over_k_minus_1", "ss / (double)K + eps", "ss / (double)(K - 1) + eps", 1),
+    ("rmsnorm_eps_dropped", "ss / (double)K + eps", "ss / (double)K", 1),
+    ("rmsnorm_no_sqrt", "1.0 / sqrt(ss / (double)K + eps)", "1.0 / (ss / (double)K + eps)", 1),
+    ("rmsnorm_weight_dropped", "x * inv * g", "x * inv", 1),
+    ("rmsnorm_abs_sum", "ss += x * x;", "ss += fabs(x);", 1),
+    ("swiglu_exp_sign", "exp(-A[i])", "exp(A[i])", 1),
+    ("swiglu_gate_up_swapped", "A[i] / (1.0 + exp(-A[i])) * B[i]", "B[i] / (1.0 + exp(-B[i])) * A[i]", 1),
+    ("residual_subtracted", "Y[i] + oracle_bf16_to_double(R[i])", "Y[i] - oracle_bf16_to_double(R[i])", 1),
     ("quant_first_entry_skipped", "for (int64_t k = 0; k < K; k++) {", "for (int64_t k = 1; k < K; k++) {", 5),
 ]
 

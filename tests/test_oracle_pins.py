@@ -33,3 +33,12 @@ def test_int8_fixture_is_hand_worked():
     assert "TileInfer" in head and "INT8 quantization" in head
     gemv, quant = oracle_pins.load_int8_fixture()
     assert len(gemv) >= 5 and len(quant) >= 4
+
+
+def test_fusion_fixture_is_hand_worked():
+    import os
+
+    head = open(os.path.join(oracle_pins.GOLDEN, "fusion_hand.txt")).read(1200)
+    assert "llm-rs vs vLLM" in head and "yalm" in head and "TileInfer" in head
+    norm, glu, res = oracle_pins.load_fusion_fixture()
+    assert len(norm) >= 5 and len(glu) >= 5 and len(res) >= 3
