@@ -73,6 +73,13 @@ typedef int mbw_status;
 #define MBW_OP_GEMV_INT4_AWQ_G128 3
 #define MBW_OP_GEMM_SKINNY_BF16 4
 #define MBW_OP_GEMV_INT8_PC 5
+/* Fusion bits, or-ed into an op id for the plan queries of gemv_fused calls
+ * (the bits follow the mbw_fusion fields that are set). */
+#define MBW_OP_BASE_MASK 0xFF
+#define MBW_FUSE_NORM 0x100     /* RMSNorm prologue */
+#define MBW_FUSE_GLU 0x200      /* gated SiLU epilogue */
+#define MBW_FUSE_RESIDUAL 0x400 /* residual-add epilogue */
+#define MBW_FUSE_MASK 0x700
 
 /*
  * gemv_bf16 -- y = W . x with BF16 weights (16 bits per weight; llm-rs vs
@@ -149,6 +156,50 @@ mbw_status gemv_int8_pc(const int8_t *Wq, const float *scales, const void *X, vo
  */
 mbw_status mbw_quantize_int8_pc(const void *W, int8_t *Wq, float *scales, int64_t N, int64_t K,
                                 mbw_stream_t stream);
+
+/*
+ * Optional fusions around one GEMV (all fields zero / NULL = none).
+ *   norm_weight : bf16 [K] or NULL. RMSNorm prologue (llm-rs vs vLLM, "Decode:
+ *                 from ~35% to ~70% of the ceiling": norms folded into the
+ *                 projections): each batch row of X is replaced by
+ *                 bf16(x * norm_weight / sqrt(mean(x^2) + norm_eps)) before the
+ *                 product. Every CTA computes mean(x^2) over all of K itself
+ *                 (fp32, fixed order), so the result is deterministic.
+ *   norm_eps    : the epsilon under the square root.
+ *   residual    : bf16 [M][N] or NULL. Residual epilogue (yalm, sec. 3.3:
+ *                 matmul fused with add_residuals): Y = W.x + residual, rounded
+ *                 once. It may be Y itself (in-place accumulation into the
+ *                 residual stream).
+ *   up_weights  : NULL, or a second weight matrix of the same format and shape
+ *                 (with up_scales). Gated epilogue (yalm, sec. 3.3:
+ *                 F.silu(w1(x)) * w3(x); TileInfer: SwiGLU in the GEMV
+ *                 epilogue): Y = silu(W.x) * (U.x), silu(a) = a / (1 + e^-a),
+ *                 both sums in fp32; the call streams both matrices. With a
+ *                 residual too, the residual is added after the product.
+ *   up_scales   : the up matrix's scales (INT4 g64: fp16 [N][K/64]; INT8:
+ *                 fp32 [N]; BF16: unused).
+ */
+typedef struct mbw_fusion {
+    const void *norm_weight;
+    float norm_eps;
+    const void *residual;
+    const void *up_weights;
+    const void *up_scales;
+} mbw_fusion;
+
+/*
+ * gemv_fused -- one GEMV with the fusions of `fusion` (NULL: none), for
+ * op = MBW_OP_GEMV_BF16, MBW_OP_GEMV_INT4_G64 (M = 1) or MBW_OP_GEMV_INT8_PC.
+ * W / scales / X / Y and their layouts are those of the op's own call
+ * (gemv_bf16: scales unused; gemv_int4_g64; gemv_int8_pc). Requires K > 0 and
+ * the op's K multiple; norm_weight 16-byte aligned, up_weights 32-byte aligned,
+ * residual 2-byte aligned. Y must not alias any input other than `residual`.
+ * Fused calls run on the mma2 and latency kernel families; their plans are
+ * keyed by op | MBW_FUSE_* (e.g. for mbw_autotune).
+ */
+mbw_status gemv_fused(int op, const void *W, const void *scales, const void *X, void *Y, int64_t M,
+                      int64_t N, int64_t K, const mbw_fusion *fusion, void *workspace, size_t ws_bytes,
+                      mbw_stream_t stream);
 
 /* Bytes of workspace the largest plan of `op` may use for this shape (0 if none). */
 size_t mbw_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);

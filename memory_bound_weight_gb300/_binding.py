@@ -20,6 +20,9 @@ OP_GEMV_INT4_G64 = 2
 OP_GEMV_INT4_AWQ_G128 = 3
 OP_GEMM_SKINNY_BF16 = 4
 OP_GEMV_INT8_PC = 5
+FUSE_NORM = 0x100
+FUSE_GLU = 0x200
+FUSE_RESIDUAL = 0x400
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -29,6 +32,12 @@ _ST = ctypes.c_int
 _lock = threading.Lock()
 _lib = None
 
+
+class MbwFusion(ctypes.Structure):
+    """struct mbw_fusion of include/mbw.h."""
+    _fields_ = [("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float), ("residual", ctypes.c_void_p),
+                ("up_weights", ctypes.c_void_p), ("up_scales", ctypes.c_void_p)]
+
 # name -> (argtypes, restype)
 SIGNATURES = {
     "gemv_bf16": ([_P, _P, _P, _I64, _I64, _P, _SZ, _P], _ST),
@@ -37,6 +46,7 @@ SIGNATURES = {
     "gemm_skinny_bf16": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _ST),
     "gemv_int8_pc": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _ST),
     "mbw_quantize_int8_pc": ([_P, _P, _P, _I64, _I64, _P], _ST),
+    "gemv_fused": ([ctypes.c_int, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.POINTER(MbwFusion), _P, _SZ, _P], _ST),
     "mbw_workspace_bytes": ([ctypes.c_int, _I64, _I64, _I64], _SZ),
     "mbw_dequant_int4_g64": ([_P, _P, _P, _I64, _I64, _P], _ST),
     "mbw_dequant_int4_awq_g128": ([_P, _P, _P, _P, _I64, _I64, _P], _ST),
@@ -236,6 +246,54 @@ def gemv_int8_pc(Wq, scales, X, out=None, workspace=None):
     wp, wn = _ws(workspace)
     check("gemv_int8_pc", lib().gemv_int8_pc(Wq.data_ptr(), scales.data_ptr(), X2.data_ptr(), Y.data_ptr(), M, N, K,
                                              wp, wn, _stream_ptr(Wq.device)))
+    return Y[0] if vec else Y
+
+
+def gemv_fused(op, W, scales, X, out=None, norm_weight=None, norm_eps=1e-6, residual=None, up_weights=None,
+               up_scales=None, workspace=None):
+    """One GEMV of format `op` (OP_GEMV_BF16 / _INT4_G64 / _INT8_PC) with optional fusions:
+    RMSNorm prologue (norm_weight bf16 (K,)), gated SiLU epilogue (up_weights / up_scales, same
+    layout as W / scales), residual add (residual bf16 shaped like the output; may be `out`).
+    X bf16 (M, K) or (K,) -> Y (M, N) or (N,)."""
+    torch = _torch()
+    vec = X.dim() == 1
+    X2 = X.unsqueeze(0) if vec else X
+    _need(X2, "X", torch.bfloat16, 2)
+    M, K = X2.shape
+    N = W.shape[0]
+    wdt, sdt, kdiv = {OP_GEMV_BF16: (torch.bfloat16, None, 1), OP_GEMV_INT4_G64: (torch.uint8, torch.float16, 2),
+                      OP_GEMV_INT8_PC: (torch.int8, torch.float32, 1)}[op]
+    _need(W, "W", wdt, 2)
+    if W.shape[1] * kdiv != K:
+        raise ValueError("W does not match K")
+    if sdt is not None:
+        _need(scales, "scales", sdt, scales.dim())
+    f = MbwFusion()
+    if norm_weight is not None:
+        _need(norm_weight, "norm_weight", torch.bfloat16, 1)
+        if norm_weight.shape[0] != K:
+            raise ValueError("norm_weight must have length K")
+        f.norm_weight = norm_weight.data_ptr()
+        f.norm_eps = float(norm_eps)
+    if up_weights is not None:
+        _need(up_weights, "up_weights", wdt, 2)
+        if tuple(up_weights.shape) != tuple(W.shape):
+            raise ValueError("up_weights must have W's shape")
+        f.up_weights = up_weights.data_ptr()
+        if sdt is not None:
+            _need(up_scales, "up_scales", sdt, up_scales.dim())
+            f.up_scales = up_scales.data_ptr()
+    Y = _alloc_out((M, N), X2, None if out is None else (out.unsqueeze(0) if vec else out))
+    if residual is not None:
+        r2 = residual.unsqueeze(0) if residual.dim() == 1 else residual
+        _need(r2, "residual", torch.bfloat16, 2)
+        if tuple(r2.shape) != (M, N):
+            raise ValueError("residual must be shaped like the output")
+        f.residual = r2.data_ptr()
+    wp, wn = _ws(workspace)
+    check("gemv_fused", lib().gemv_fused(op, W.data_ptr(), None if scales is None else scales.data_ptr(),
+                                         X2.data_ptr(), Y.data_ptr(), M, N, K, ctypes.byref(f), wp, wn,
+                                         _stream_ptr(X2.device)))
     return Y[0] if vec else Y
 
 

@@ -57,12 +57,13 @@ static mbw_status zero_output(void* y, int64_t M, int64_t N, cudaStream_t s) {
 
 // Run a CUDA-core streaming GEMV over M activation rows, in slices of the
 // planned kernel's batch width.
+// `op` may carry MBW_FUSE_* bits; `fz` then holds the fusion pointers.
 static mbw_status run_simt(int fmt, int op, const uint8_t* W, const uint16_t* scales, const uint8_t* zeros,
                            const uint16_t* X, void* Y, int64_t M, int64_t N, int64_t K, cudaStream_t s,
-                           const float* rscale = nullptr) {
+                           const float* rscale = nullptr, const mbw_fusion* fz = nullptr) {
     const Plan p = plan_lookup(op, M, N, K, s);
     const int width = plan_batch_width(fmt, p);
-    GemvArgs a;
+    GemvArgs a{};
     a.W = W;
     a.scales = scales;
     a.zeros = zeros;
@@ -74,10 +75,21 @@ static mbw_status run_simt(int fmt, int op, const uint8_t* W, const uint16_t* sc
     a.zstride = (a.groups + 1) / 2;
     a.out_f32 = g_out_f32;
     a.rscale = rscale;
+    if (fz) {
+        a.norm_w = static_cast<const uint16_t*>(fz->norm_weight);
+        a.norm_eps = fz->norm_eps;
+        if (fz->up_weights) {
+            a.glu = 1;
+            a.W2 = static_cast<const uint8_t*>(fz->up_weights);
+            a.scales2 = static_cast<const uint16_t*>(fz->up_scales);
+            a.rscale2 = static_cast<const float*>(fz->up_scales);
+        }
+    }
     const size_t ybytes = g_out_f32 ? 4 : 2;
     for (int64_t m0 = 0; m0 < M; m0 += width) {
         a.x = X + m0 * K;
         a.y = static_cast<char*>(Y) + (size_t)m0 * (size_t)N * ybytes;
+        if (fz && fz->residual) a.residual = static_cast<const uint16_t*>(fz->residual) + (size_t)m0 * (size_t)N;
         a.M = (int)((M - m0) < width ? (M - m0) : width);
         cudaError_t e = launch_plan(fmt, p, a, s);
         if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
@@ -164,6 +176,61 @@ mbw_status mbw_quantize_int8_pc(const void* W, int8_t* Wq, float* scales, int64_
         return fail(MBW_ERR_MISALIGNED, "mbw_quantize_int8_pc: W must be 2-byte aligned, scales 4-byte");
     cudaError_t e = launch_quantize_int8_pc((const uint16_t*)W, Wq, scales, N, K, (cudaStream_t)stream);
     return e == cudaSuccess ? MBW_OK : cuda_fail(e, "quantize launch");
+}
+
+mbw_status gemv_fused(int op, const void* W, const void* scales, const void* X, void* Y, int64_t M, int64_t N,
+                      int64_t K, const mbw_fusion* fusion, void* workspace, size_t ws_bytes, mbw_stream_t stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    int fmt;
+    switch (op) {
+        case MBW_OP_GEMV_BF16: fmt = FMT_BF16; break;
+        case MBW_OP_GEMV_INT4_G64: fmt = FMT_G64; break;
+        case MBW_OP_GEMV_INT8_PC: fmt = FMT_I8; break;
+        default: return fail(MBW_ERR_INVALID_ARG, "gemv_fused: op must be MBW_OP_GEMV_BF16, _INT4_G64 or _INT8_PC");
+    }
+    const int64_t kmul = (fmt == FMT_BF16) ? 8 : (fmt == FMT_G64) ? 64 : 128;
+    mbw_status st = check_sizes("gemv_fused", M, N, K, kmul);
+    if (st != MBW_OK) return st;
+    if (N == 0 || M == 0) return MBW_OK;
+    if (K == 0) return fail(MBW_ERR_BAD_SHAPE, "gemv_fused: K must be positive");
+    if (fmt == FMT_G64 && M != 1) return fail(MBW_ERR_BAD_SHAPE, "gemv_fused: INT4 g64 takes M = 1");
+    if (!W || !X || !Y || (fmt != FMT_BF16 && !scales)) return fail(MBW_ERR_INVALID_ARG, "gemv_fused: NULL pointer");
+    const size_t salign = (fmt == FMT_I8) ? 4 : 2;
+    if (!aligned(W, 32) || !aligned(X, 16) || !aligned(Y, 16) || (scales && !aligned(scales, salign)))
+        return fail(MBW_ERR_MISALIGNED, "gemv_fused: W must be 32-byte aligned, X and Y 16-byte, scales 2 or 4 bytes");
+    int fop = op;
+    if (fusion) {
+        if (fusion->norm_weight) {
+            if (!aligned(fusion->norm_weight, 16))
+                return fail(MBW_ERR_MISALIGNED, "gemv_fused: norm_weight must be 16-byte aligned");
+            if (!(fusion->norm_eps >= 0.0f)) return fail(MBW_ERR_INVALID_ARG, "gemv_fused: norm_eps must be >= 0");
+            fop |= MBW_FUSE_NORM;
+        }
+        if (fusion->up_weights) {
+            if (!aligned(fusion->up_weights, 32))
+                return fail(MBW_ERR_MISALIGNED, "gemv_fused: up_weights must be 32-byte aligned");
+            if (fmt != FMT_BF16 && (!fusion->up_scales || !aligned(fusion->up_scales, salign)))
+                return fail(MBW_ERR_INVALID_ARG, "gemv_fused: up_scales missing or misaligned");
+            fop |= MBW_FUSE_GLU;
+        }
+        if (fusion->residual) {
+            if (!aligned(fusion->residual, 2))
+                return fail(MBW_ERR_MISALIGNED, "gemv_fused: residual must be 2-byte aligned");
+            fop |= MBW_FUSE_RESIDUAL;
+        }
+    }
+    if (fmt == FMT_G64 || fmt == FMT_I8) {
+        if (fmt == FMT_G64 && K % 256 != 0 && (fop & MBW_FUSE_MASK))
+            return fail(MBW_ERR_BAD_SHAPE, "gemv_fused: fused INT4 g64 needs K % 256 == 0");
+    } else if ((fop & MBW_FUSE_MASK) && K % 64 != 0) {
+        return fail(MBW_ERR_BAD_SHAPE, "gemv_fused: fused BF16 needs K % 64 == 0");
+    }
+    if (mbw_plan_candidates(fop, M, N, K) == 0)
+        return fail(MBW_ERR_UNSUPPORTED, "gemv_fused: no kernel for this shape and fusion");
+    return run_simt(fmt, fop, (const uint8_t*)W, (const uint16_t*)scales, nullptr, (const uint16_t*)X, Y, M, N, K,
+                    (cudaStream_t)stream, fmt == FMT_I8 ? (const float*)scales : nullptr,
+                    (fop & MBW_FUSE_MASK) ? fusion : nullptr);
 }
 
 mbw_status gemm_skinny_bf16(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,

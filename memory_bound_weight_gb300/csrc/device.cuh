@@ -7,6 +7,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "internal.h"
+
 namespace mbw {
 
 // ---------------------------------------------------------------- loads ----
@@ -170,6 +172,92 @@ __device__ __forceinline__ void store_out(void* y, int64_t idx, float v, int out
         static_cast<float*>(y)[idx] = v;
     else
         static_cast<__nv_bfloat16*>(y)[idx] = __float2bfloat16_rn(v);
+}
+
+// ------------------------------------------------------------- fusions ----
+// Which matrix and physical 16-row tile a logical tile t reads: under the
+// gated epilogue logical tiles alternate between W (gate) and W2 (up).
+__device__ __forceinline__ const uint8_t* tile_weights(const GemvArgs& a, int t) {
+    return (a.glu && (t & 1)) ? a.W2 : a.W;
+}
+__device__ __forceinline__ int tile_row0(const GemvArgs& a, int t) { return (a.glu ? (t >> 1) : t) * 16; }
+__device__ __forceinline__ const uint16_t* tile_scales(const GemvArgs& a, int t) {
+    return (a.glu && (t & 1)) ? a.scales2 : a.scales;
+}
+__device__ __forceinline__ const float* tile_rscale(const GemvArgs& a, int t) {
+    return (a.glu && (t & 1)) ? a.rscale2 : a.rscale;
+}
+
+// The CTA's logical tile range [t0, t0 + nt) of row-group `cg` of `G`: whole
+// output tiles, and whole gate/up pairs under the gated epilogue.
+__device__ __forceinline__ void cta_tile_range(const GemvArgs& a, int G, int cg, int& t0, int& nt) {
+    const int T = (a.N + 15) / 16;
+    const int f = a.glu ? 2 : 1;
+    const int p0 = (int)(((long long)T * cg) / G);
+    const int p1 = (int)(((long long)T * (cg + 1)) / G);
+    t0 = p0 * f;
+    nt = (p1 - p0) * f;
+}
+
+// RMSNorm prologue (llm-rs vs vLLM, "norms folded into the projections"):
+// 1 / sqrt(mean_k x[m][k]^2 + eps) for every batch row m, summed by the whole
+// CTA in a fixed order (deterministic). `scratch` needs (warps + 1) * M
+// floats; the factor of row m is left in scratch[warps * M + m]. Contains two
+// __syncthreads: every thread of the CTA must call it.
+__device__ __forceinline__ void norm_factors(const GemvArgs& a, float* scratch, int nthreads) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = nthreads >> 5;
+    const int words = a.K / 8;
+    for (int m = 0; m < a.M; ++m) {
+        float s = 0.f;
+        for (int i = threadIdx.x; i < words; i += nthreads) {
+            const uint4 v = ld_ro16(a.x + (size_t)m * a.K + (size_t)i * 8);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float lo = bf16lo_to_f32(w[j]), hi = bf16hi_to_f32(w[j]);
+                s = fmaf(lo, lo, s);
+                s = fmaf(hi, hi, s);
+            }
+        }
+        s = warp_sum(s);
+        if (lane == 0) scratch[m * nw + warp] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x < a.M) {
+        float t = 0.f;
+        for (int w = 0; w < nw; ++w) t += scratch[threadIdx.x * nw + w];
+        scratch[nw * a.M + threadIdx.x] = 1.0f / sqrtf(t / (float)a.K + a.norm_eps);
+    }
+    __syncthreads();
+}
+
+// x word (8 bf16 at k .. k+7 of batch row m) -> bf16(x * r * g), rounded to nearest even.
+__device__ __forceinline__ uint4 norm_word(uint4 v, float r, const uint16_t* g) {
+    const uint4 gv = ld_ro16(g);
+    const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float lo = bf16lo_to_f32(xw[j]) * r * bf16lo_to_f32(gw[j]);
+        const float hi = bf16hi_to_f32(xw[j]) * r * bf16hi_to_f32(gw[j]);
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        o[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float silu_f32(float v) { return v / (1.0f + expf(-v)); }
+
+// Store output (m, row) of a finished row sum (INT8 scales already applied):
+// v is the sum of W's row, v2 that of W2's row under the gated epilogue;
+// SwiGLU (yalm sec. 3.3, TileInfer: SwiGLU in the GEMV epilogue), then the
+// residual add (yalm: fused matmul + add_residuals), then the bf16 store.
+__device__ __forceinline__ void store_fused(const GemvArgs& a, int m, int row, float v, float v2) {
+    if (a.glu) v = silu_f32(v) * v2;
+    const int64_t idx = (int64_t)m * a.N + row;
+    if (a.residual) v += bf16lo_to_f32(a.residual[idx]);
+    store_out(a.y, idx, v, a.out_f32);
 }
 
 }  // namespace mbw

@@ -111,13 +111,19 @@ __device__ __forceinline__ void lat_unpack(const u32x8& ra, const u32x8& rb, uin
 // x slot per warp: 72 words (64 + 8 pad words of 16 bytes) per super-block
 // of the warp's k-slice (xsb = min(NI, k-slice length)); then the INT8 row
 // scales of the CTA ([ntmax][16] fp32, `scf` floats, 0 for other formats);
-// then, for the staged variants, the item ring (W x NI x 2 KB).
+// then the RMSNorm prologue's scratch ((16 + 1) x 8 floats, its own area: warps
+// write their partials while others may still read the factors); then, for the
+// staged variants, the item ring (W x NI x 2 KB).
+constexpr int kLatNormFloats = (16 + 1) * 8;
 __host__ __device__ inline size_t lat_red_floats(int ntmax, int WK, int M) {
     return ((size_t)ntmax * (WK + 1) * 16 * M + 3) / 4 * 4;  // 16-byte aligned end
 }
 __host__ __device__ inline size_t lat_sc_floats(int fmt, int ntmax) { return fmt == FMT_I8 ? (size_t)ntmax * 16 : 0; }
-__host__ __device__ inline size_t lat_smem_floats(int ntmax, int W, int WK, int M, int xsb, size_t scf) {
+__host__ __device__ inline size_t lat_norm_off(int ntmax, int W, int WK, int M, int xsb, size_t scf) {
     return lat_red_floats(ntmax, WK, M) + (size_t)W * 72 * 4 * xsb + scf;
+}
+__host__ __device__ inline size_t lat_smem_floats(int ntmax, int W, int WK, int M, int xsb, size_t scf) {
+    return lat_norm_off(ntmax, W, WK, M, xsb, scf) + kLatNormFloats;
 }
 __host__ __device__ inline size_t lat_ring_off(int ntmax, int W, int WK, int M, int xsb, size_t scf) {
     return (lat_smem_floats(ntmax, W, WK, M, xsb, scf) * 4 + 127) / 128 * 128;
@@ -151,10 +157,9 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     const int g = lane >> 2, q = lane & 3;
     const int G = gridDim.x / S;
     const int cgid = blockIdx.x / S;
-    const int T = (a.N + 15) / 16;
-    const int t0 = (int)(((long long)T * cgid) / G);
-    const int nt = (int)(((long long)T * (cgid + 1)) / G) - t0;
-    const int ntmax = (T + G - 1) / G;
+    int t0, nt;  // the CTA's logical tiles (gate/up pairs under the gated epilogue)
+    cta_tile_range(a, G, cgid, t0, nt);
+    const int ntmax = ((a.N + 15) / 16 + G - 1) / G * (a.glu ? 2 : 1);
     const int mb = a.M;
     const int KB = a.K / BK;  // the plan guarantees K % BK == 0
     const int BS = (KB + S * WK - 1) / (S * WK);
@@ -182,10 +187,12 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
             const int tt = j / nb;
             const int b = b0 + (j - tt * nb);
             const int tile = t0 + wt + tt * WT;
-            const int r0 = min(tile * 16 + g, a.N - 1);
-            const int r1 = min(tile * 16 + g + 8, a.N - 1);
-            const uint8_t* p0 = a.W + (size_t)r0 * rowbytes + (size_t)b * 128 + q * 32;
-            const uint8_t* p1 = a.W + (size_t)r1 * rowbytes + (size_t)b * 128 + q * 32;
+            const uint8_t* Wt = tile_weights(a, tile);
+            const int trow = tile_row0(a, tile);
+            const int r0 = min(trow + g, a.N - 1);
+            const int r1 = min(trow + g + 8, a.N - 1);
+            const uint8_t* p0 = Wt + (size_t)r0 * rowbytes + (size_t)b * 128 + q * 32;
+            const uint8_t* p1 = Wt + (size_t)r1 * rowbytes + (size_t)b * 128 + q * 32;
             if (!STG || j < NPRE) {
                 ra[j] = ld_stream32(p0);
                 rb[j] = ld_stream32(p1);
@@ -194,12 +201,13 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     cp_async16(d + ring_copy_dst(lane, c),
-                               a.W + (size_t)min(tile * 16 + ring_copy_row(lane, c), a.N - 1) * rowbytes +
+                               Wt + (size_t)min(trow + ring_copy_row(lane, c), a.N - 1) * rowbytes +
                                    (size_t)b * 128 + ring_copy_byte(lane));
             }
             if (FMT == FMT_G64) {
-                const uint16_t* s0 = a.scales + (size_t)r0 * a.groups + (size_t)b * 4 + 2 * (q & 1);
-                const uint16_t* s1 = a.scales + (size_t)r1 * a.groups + (size_t)b * 4 + 2 * (q & 1);
+                const uint16_t* st = tile_scales(a, tile);
+                const uint16_t* s0 = st + (size_t)r0 * a.groups + (size_t)b * 4 + 2 * (q & 1);
+                const uint16_t* s1 = st + (size_t)r1 * a.groups + (size_t)b * 4 + 2 * (q & 1);
                 rs[j][0] = (uint32_t)ld_ro_u16(s0) | ((uint32_t)ld_ro_u16(s0 + 1) << 16);
                 rs[j][1] = (uint32_t)ld_ro_u16(s1) | ((uint32_t)ld_ro_u16(s1 + 1) << 16);
             }
@@ -219,7 +227,10 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     // INT8: the fp32 scales of the CTA's rows (weights: read before the wait)
     float* rsc = lat_smem + lat_red_floats(ntmax, WK, mb) + (size_t)W * 72 * 4 * xsb;
     if (FMT == FMT_I8)
-        for (int i = threadIdx.x; i < nt * 16; i += W * 32) rsc[i] = __ldg(a.rscale + min(t0 * 16 + i, a.N - 1));
+        for (int i = threadIdx.x; i < nt * 16; i += W * 32) {
+            const int tl = t0 + (i >> 4);
+            rsc[i] = __ldg(tile_rscale(a, tl) + min(tile_row0(a, tl) + (i & 15), a.N - 1));
+        }
 
     // Addresses of the x words this lane reads after the wait: word i of the
     // warp's x (super-block i / (M * words per row), batch row, word) is
@@ -269,6 +280,9 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     // item, a lane issuing eight loads itself, or eight rounds of shuffles
     // each cost more latency.
     uint4* xslot = reinterpret_cast<uint4*>(lat_smem + lat_red_floats(ntmax, WK, mb)) + (size_t)warp * (72 * xsb);
+    // RMSNorm prologue: the CTA's factor per batch row
+    float* nscr = lat_smem + lat_norm_off(ntmax, W, WK, mb, xsb, scf);
+    if (a.norm_w) norm_factors(a, nscr, W * 32);
     {
         uint4 v[XLD];
 #pragma unroll
@@ -280,6 +294,11 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
 #pragma unroll
         for (int r = 0; r < XLD; ++r) {
             const int wi = lane + 32 * r;
+            if (wi < nxw && a.norm_w) {
+                const int sb = wi / sbw, rem = wi - sb * sbw;
+                const int m = rem / XWSB, w = rem - m * XWSB;
+                v[r] = norm_word(v[r], nscr[W * mb + m], a.norm_w + (size_t)(b0 + sb) * BK + w * 8);
+            }
             if (wi < nxw)
                 xslot[wi + (wi >> 3)] = (FMT == FMT_G64) ? lat_perm(v[r]) : (FMT == FMT_I8) ? perm_i8(v[r]) : v[r];
         }
@@ -449,59 +468,55 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     }
     __syncthreads();
 
-    // each output: the sum over the K-warps in order
-    const int nout = nt * 16 * mb;
-    const int row0 = t0 * 16;
+    // each output: the sum over the K-warps in order. Local logical row lr
+    // (tile lr / 16) of batch row m; under the gated epilogue output row o
+    // pairs gate row gate_row(o) with up row gate_row(o) + 16.
+    const int nto = a.glu ? nt / 2 : nt;
+    const int orow0 = (a.glu ? t0 / 2 : t0) * 16;
+    auto gate_row = [&](int o) { return a.glu ? (o >> 4) * 32 + (o & 15) : o; };
+    auto wsum = [&](int lr, int m) -> float {
+        const float* rp = red + ((size_t)(lr >> 4) * WK * 16 + (lr & 15)) * mb + m;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < WK; ++w) v += rp[(size_t)w * 16 * mb];
+        return v;
+    };
     if (S == 1) {
-        if (mb == 1) {
-            for (int i = threadIdx.x; i < nout; i += W * 32) {
-                const float* rp = red + (i >> 4) * (WK * 16) + (i & 15);
-                float v = 0.f;
-#pragma unroll
-                for (int w = 0; w < WK; ++w) v += rp[w * 16];
-                if (FMT == FMT_I8) v *= rsc[i];
-                if (row0 + i < a.N) store_out(a.y, row0 + i, v, a.out_f32);
+        for (int i = threadIdx.x; i < nto * 16 * mb; i += W * 32) {
+            const int o = (mb == 1) ? i : i / mb;
+            const int m = (mb == 1) ? 0 : i - o * mb;
+            if (orow0 + o >= a.N) continue;
+            const int lr = gate_row(o);
+            float v = wsum(lr, m), v2 = 0.f;
+            if (FMT == FMT_I8) v *= rsc[lr];
+            if (a.glu) {
+                v2 = wsum(lr + 16, m);
+                if (FMT == FMT_I8) v2 *= rsc[lr + 16];
             }
-            return;
-        }
-        for (int i = threadIdx.x; i < nout; i += W * 32) {
-            const int t = i / (16 * mb);
-            const int rm = i - t * 16 * mb;
-            const int r = rm / mb;
-            const int m = rm - r * mb;
-            float v = 0.f;
-            const float* rp = red + (size_t)t * WK * 16 * mb + rm;
-#pragma unroll
-            for (int w = 0; w < WK; ++w) v += rp[(size_t)w * 16 * mb];
-            const int row = row0 + t * 16 + r;
-            if (FMT == FMT_I8) v *= rsc[t * 16 + r];
-            if (row < a.N) store_out(a.y, (int64_t)m * a.N + row, v, a.out_f32);
+            store_fused(a, m, orow0 + o, v, v2);
         }
         return;
     }
-    float* fin = red + (size_t)ntmax * WK * 16 * mb;  // [tile*16 + row][m]
-    for (int i = threadIdx.x; i < nout; i += W * 32) {
-        const int t = i / (16 * mb);
-        const int rm = i - t * 16 * mb;
-        float v = 0.f;
-        const float* rp = red + (size_t)t * WK * 16 * mb + rm;
-#pragma unroll
-        for (int w = 0; w < WK; ++w) v += rp[(size_t)w * 16 * mb];
-        fin[i] = v;
-    }
+    float* fin = red + (size_t)ntmax * WK * 16 * mb;  // [lr][m]: this rank's sums
+    for (int i = threadIdx.x; i < nt * 16 * mb; i += W * 32) fin[i] = wsum(i / mb, i - (i / mb) * mb);
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
-    // rank s writes rows [s * R / S, (s + 1) * R / S) of the CTA group's R rows
-    const int R = nt * 16;
-    const int lo = rank * R / S, hi = (rank + 1) * R / S;
+    // rank s writes output rows [s * Ro / S, (s + 1) * Ro / S) of the CTA group's Ro rows
+    const int Ro = nto * 16;
+    const int lo = rank * Ro / S, hi = (rank + 1) * Ro / S;
     const int span = hi - lo;
     for (int i = threadIdx.x; i < span * mb; i += W * 32) {
-        const int lr = lo + i / mb;
+        const int o = lo + i / mb;
         const int m = i - (i / mb) * mb;
-        float v = 0.f;
+        const int lr = gate_row(o);
+        float v = 0.f, v2 = 0.f;
         for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(fin + lr * mb + m, s);
         if (FMT == FMT_I8) v *= rsc[lr];
-        if (row0 + lr < a.N) store_out(a.y, (int64_t)m * a.N + row0 + lr, v, a.out_f32);
+        if (a.glu) {
+            for (int s = 0; s < S; ++s) v2 += *cluster.map_shared_rank(fin + (lr + 16) * mb + m, s);
+            if (FMT == FMT_I8) v2 *= rsc[lr + 16];
+        }
+        if (orow0 + o < a.N) store_fused(a, m, orow0 + o, v, v2);
     }
     cluster.sync();
 }
@@ -564,7 +579,7 @@ int lat_max_batch(int fmt) { return fmt == FMT_G64 ? 2 : fmt == FMT_I8 ? 4 : 8; 
 int lat_block_k(int fmt) { return fmt == FMT_BF16 ? 64 : fmt == FMT_I8 ? 128 : 256; }
 
 // Most items any warp owns under this split (0 if the shape does not fit the family).
-int lat_items_per_warp(int fmt, const LatConfig& c, int64_t N, int64_t K, int split, int occ) {
+int lat_items_per_warp(int fmt, const LatConfig& c, int64_t N, int64_t K, int split, int occ, int glu) {
     const int BK = lat_block_k(fmt);
     if (K % BK != 0) return 0;
     const int WK = c.warps / c.wt;
@@ -573,14 +588,14 @@ int lat_items_per_warp(int fmt, const LatConfig& c, int64_t N, int64_t K, int sp
     if ((int64_t)(split - 1) * WK * BS >= KB) return 0;  // a cluster rank without k-range
     const int G = mma_row_groups(N, split, occ);
     const int64_t T = (N + 15) / 16;
-    const int64_t ntmax = (T + G - 1) / G;
+    const int64_t ntmax = (T + G - 1) / G * (glu ? 2 : 1);
     return (int)((ntmax + c.wt - 1) / c.wt * BS);
 }
 
-size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
+size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu) {
     const int G = mma_row_groups(N, split, occ);
     const int64_t T = (N + 15) / 16;
-    const int ntmax = (int)((T + G - 1) / G);
+    const int ntmax = (int)((T + G - 1) / G) * (glu ? 2 : 1);
     const int WK = c.warps / c.wt;
     const int64_t KB = K / lat_block_k(fmt);
     const int64_t BS = (KB + (int64_t)split * WK - 1) / ((int64_t)split * WK);
@@ -595,10 +610,10 @@ cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStrea
     const LatEntry* t = lat_table(fmt, &n);
     if (t == nullptr || p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > lat_max_batch(fmt)) return cudaErrorInvalidValue;
     const LatEntry& e = t[p.cfg];
-    const int items = lat_items_per_warp(fmt, e.cfg, a.N, a.K, p.split, p.occ);
+    const int items = lat_items_per_warp(fmt, e.cfg, a.N, a.K, p.split, p.occ, a.glu);
     if (items < 1 || items > e.cfg.ni) return cudaErrorInvalidValue;
     const int G = mma_row_groups(a.N, p.split, p.occ);
-    const size_t smem = lat_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
+    const size_t smem = lat_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ, a.glu);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;

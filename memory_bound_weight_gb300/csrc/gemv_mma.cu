@@ -107,13 +107,13 @@ struct MmaSmem {
     size_t x_bytes, red_off, red_bytes, total;
 };
 
-__host__ __device__ inline MmaSmem mma_smem_layout(int BK, int64_t K, int N, int M, int W, int S, int G) {
+__host__ __device__ inline MmaSmem mma_smem_layout(int BK, int64_t K, int N, int M, int W, int S, int G, int glu = 0) {
     MmaSmem L;
     const int64_t KB = (K + BK - 1) / BK;
     const int64_t BS = (KB + (int64_t)S * W - 1) / ((int64_t)S * W);
     L.xwords = (int)(W * BS * (BK / 8));
     const int T = (N + 15) / 16;
-    L.ntmax = (T + G - 1) / G;
+    L.ntmax = (T + G - 1) / G * (glu ? 2 : 1);  // logical tiles (gate/up pairs under the gated epilogue)
     L.x_bytes = ((size_t)M * L.xwords + BK / 8) * 16;  // + one block of zero words
     const size_t fin_bytes = (size_t)L.ntmax * 16 * M * 4;
     L.red_off = ((L.x_bytes > fin_bytes ? L.x_bytes : fin_bytes) + 15) / 16 * 16;
@@ -401,11 +401,10 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     const int g = lane >> 2, q = lane & 3;
     const int G = gridDim.x / S;
     const int cgid = blockIdx.x / S;
-    const int T = (a.N + 15) / 16;
-    const int t0 = (int)(((long long)T * cgid) / G);
-    const int nt = (int)(((long long)T * (cgid + 1)) / G) - t0;
+    int t0, nt;  // the CTA's logical tiles (gate/up pairs under the gated epilogue)
+    cta_tile_range(a, G, cgid, t0, nt);
     const int mb = a.M;
-    const MmaSmem L = mma_smem_layout(BK, a.K, a.N, mb, W, S, G);
+    const MmaSmem L = mma_smem_layout(BK, a.K, a.N, mb, W, S, G, a.glu);
 
     const int KB = a.K / BK;  // the plan guarantees K % BK == 0
     const int BS = (KB + S * W - 1) / (S * W);
@@ -425,23 +424,27 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     const uint8_t* zp1 = nullptr;
     const uint8_t* ap[4] = {nullptr, nullptr, nullptr, nullptr};  // ASYNC: sources of this lane's 4 copies
     auto set_rows = [&](int t) {
-        const int r0 = min((t0 + t) * 16 + g, a.N - 1);
-        const int r1 = min((t0 + t) * 16 + g + 8, a.N - 1);
+        const int tl = t0 + t;
+        const uint8_t* Wt = tile_weights(a, tl);
+        const uint16_t* St = tile_scales(a, tl);
+        const int trow = tile_row0(a, tl);
+        const int r0 = min(trow + g, a.N - 1);
+        const int r1 = min(trow + g + 8, a.N - 1);
         if (ASYNC) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                ap[j] = a.W + (size_t)min((t0 + t) * 16 + ring_copy_row(lane, j), a.N - 1) * rowbytes +
-                        (size_t)b0 * 128 + ring_copy_byte(lane);
+                ap[j] = Wt + (size_t)min(trow + ring_copy_row(lane, j), a.N - 1) * rowbytes + (size_t)b0 * 128 +
+                        ring_copy_byte(lane);
         } else {
-            wp0 = a.W + (size_t)r0 * rowbytes + (size_t)b0 * 128 + q * 32;
-            wp1 = a.W + (size_t)r1 * rowbytes + (size_t)b0 * 128 + q * 32;
+            wp0 = Wt + (size_t)r0 * rowbytes + (size_t)b0 * 128 + q * 32;
+            wp1 = Wt + (size_t)r1 * rowbytes + (size_t)b0 * 128 + q * 32;
         }
         if (FMT == FMT_G64) {
-            sp0 = a.scales + (size_t)r0 * a.groups + (size_t)b0 * 4 + 2 * (q & 1);
-            sp1 = a.scales + (size_t)r1 * a.groups + (size_t)b0 * 4 + 2 * (q & 1);
+            sp0 = St + (size_t)r0 * a.groups + (size_t)b0 * 4 + 2 * (q & 1);
+            sp1 = St + (size_t)r1 * a.groups + (size_t)b0 * 4 + 2 * (q & 1);
         } else if (FMT == FMT_AWQ) {
-            sp0 = a.scales + (size_t)r0 * a.groups + (size_t)b0 * 2;
-            sp1 = a.scales + (size_t)r1 * a.groups + (size_t)b0 * 2;
+            sp0 = St + (size_t)r0 * a.groups + (size_t)b0 * 2;
+            sp1 = St + (size_t)r1 * a.groups + (size_t)b0 * 2;
             zp0 = a.zeros + (size_t)r0 * a.zstride + b0;
             zp1 = a.zeros + (size_t)r1 * a.zstride + b0;
         }
@@ -501,10 +504,17 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     }
 
     if (FMT == FMT_I8)
-        for (int i = threadIdx.x; i < nt * 16; i += W * 32) rsc[i] = __ldg(a.rscale + min(t0 * 16 + i, a.N - 1));
+        for (int i = threadIdx.x; i < nt * 16; i += W * 32) {
+            const int tl = t0 + (i >> 4);
+            rsc[i] = __ldg(tile_rscale(a, tl) + min(tile_row0(a, tl) + (i & 15), a.N - 1));
+        }
 
     prefetch_l2_grid_share(a.x, (size_t)a.M * a.K * 2);
     pdl_wait();
+
+    // RMSNorm prologue: factor per batch row into the (still unused) partial-sum area
+    float* nscr = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.red_off);
+    if (a.norm_w) norm_factors(a, nscr, W * 32);
 
     uint4* xs = smem_u4;
     const int cwords = max(0, min(KB, cb0 + W * BS) - cb0) * XW;
@@ -513,7 +523,10 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
         if (i < mb * L.xwords) {
             const int m = i / L.xwords;
             const int wi = i - m * L.xwords;
-            if (wi < cwords) v = ld_ro16(a.x + (size_t)m * a.K + (size_t)cb0 * BK + (size_t)wi * 8);
+            if (wi < cwords) {
+                v = ld_ro16(a.x + (size_t)m * a.K + (size_t)cb0 * BK + (size_t)wi * 8);
+                if (a.norm_w) v = norm_word(v, nscr[W * mb + m], a.norm_w + (size_t)cb0 * BK + (size_t)wi * 8);
+            }
             if (FMT == FMT_I8)
                 v = perm_i8(v);
             else if (FMT != FMT_BF16)
@@ -679,7 +692,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     }
     __syncthreads();
 
-    float* fin = reinterpret_cast<float*>(smem_u4);
+    float* fin = reinterpret_cast<float*>(smem_u4);  // [lr][m]: sums over the CTA's warps
     const int nout = nt * 16 * mb;
     for (int i = threadIdx.x; i < nout; i += W * 32) {
         const int t = i / (16 * mb);
@@ -688,28 +701,44 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
         for (int w = 0; w < W; ++w) v += red[((size_t)(t * W + w) * 16) * mb + rm];
         fin[i] = v;
     }
-    const int row0 = t0 * 16;
+    // output row o of the CTA; under the gated epilogue it pairs gate row
+    // gate_row(o) with up row gate_row(o) + 16 (local logical rows)
+    const int nto = a.glu ? nt / 2 : nt;
+    const int orow0 = (a.glu ? t0 / 2 : t0) * 16;
+    auto gate_row = [&](int o) { return a.glu ? (o >> 4) * 32 + (o & 15) : o; };
     if (S == 1) {
         __syncthreads();
-        for (int i = threadIdx.x; i < nout; i += W * 32) {
-            const int m = i / (nt * 16), lr = i - m * nt * 16;
-            if (row0 + lr < a.N)
-                store_out(a.y, (int64_t)m * a.N + row0 + lr, (FMT == FMT_I8) ? fin[lr * mb + m] * rsc[lr] : fin[lr * mb + m],
-                          a.out_f32);
+        for (int i = threadIdx.x; i < nto * 16 * mb; i += W * 32) {
+            const int m = i / (nto * 16), o = i - m * nto * 16;
+            if (orow0 + o >= a.N) continue;
+            const int lr = gate_row(o);
+            float v = fin[lr * mb + m], v2 = 0.f;
+            if (FMT == FMT_I8) v *= rsc[lr];
+            if (a.glu) {
+                v2 = fin[(lr + 16) * mb + m];
+                if (FMT == FMT_I8) v2 *= rsc[lr + 16];
+            }
+            store_fused(a, m, orow0 + o, v, v2);
         }
         return;
     }
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
-    const int R = nt * 16;
-    const int lo = rank * R / S, hi = (rank + 1) * R / S;
+    // rank s writes output rows [s * Ro / S, (s + 1) * Ro / S) of the CTA group's Ro rows, every batch row
+    const int Ro = nto * 16;
+    const int lo = rank * Ro / S, hi = (rank + 1) * Ro / S;
     const int span = hi - lo;
     for (int i = threadIdx.x; i < span * mb; i += W * 32) {
-        const int m = i / span, lr = lo + (i - m * span);
-        float v = 0.f;
+        const int m = i / span, o = lo + (i - m * span);
+        const int lr = gate_row(o);
+        float v = 0.f, v2 = 0.f;
         for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(fin + lr * mb + m, s);
         if (FMT == FMT_I8) v *= rsc[lr];
-        if (row0 + lr < a.N) store_out(a.y, (int64_t)m * a.N + row0 + lr, v, a.out_f32);
+        if (a.glu) {
+            for (int s = 0; s < S; ++s) v2 += *cluster.map_shared_rank(fin + (lr + 16) * mb + m, s);
+            if (FMT == FMT_I8) v2 *= rsc[lr + 16];
+        }
+        if (orow0 + o < a.N) store_fused(a, m, orow0 + o, v, v2);
     }
     cluster.sync();
 }
@@ -781,9 +810,9 @@ MmaConfig mma2_config(int fmt, int idx) {
 int mma2_max_batch(int fmt) { return fmt == FMT_G64 ? 2 : fmt == FMT_AWQ ? 4 : 8; }
 int mma2_block_k(int fmt) { return fmt == FMT_BF16 ? 64 : fmt == FMT_I8 ? 128 : 256; }
 
-size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
+size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu) {
     const int G = mma_row_groups(N, split, occ);
-    const MmaSmem L = mma_smem_layout(mma2_block_k(fmt), K, (int)N, M, c.warps, split, G);
+    const MmaSmem L = mma_smem_layout(mma2_block_k(fmt), K, (int)N, M, c.warps, split, G, glu);
     const size_t base = L.total + (fmt == FMT_I8 ? (size_t)L.ntmax * 16 * 4 : 0);  // + INT8 row scales
     if (!c.async) return base;
     return (base + 127) / 128 * 128 + (size_t)c.warps * c.u * 4 * 512;
@@ -795,7 +824,7 @@ cudaError_t launch_gemv_mma2(int fmt, const Plan& p, const GemvArgs& a, cudaStre
     if (t == nullptr || p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > mma2_max_batch(fmt)) return cudaErrorInvalidValue;
     const MmaEntry& e = t[p.cfg];
     const int G = mma_row_groups(a.N, p.split, p.occ);
-    const size_t smem = mma2_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
+    const size_t smem = mma2_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ, a.glu);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;

@@ -27,7 +27,21 @@ struct GemvArgs {
     int zstride;       // zero-point bytes per row
     int out_f32;       // 1: write fp32 y
     const float* rscale;  // fp32 scale per weight row [N] (INT8 only)
+    // Fusions (NULL / 0 = none). RMSNorm prologue: x <- bf16(x * norm_w / sqrt(mean(x^2) + eps)).
+    const uint16_t* norm_w;  // bf16 [K]
+    float norm_eps;
+    // Residual epilogue: y <- y + residual (bf16 [M][N]; may be y itself).
+    const uint16_t* residual;
+    // Gated epilogue: W2 (+ scales2 / rscale2) is the "up" matrix of the same shape and format;
+    // y <- silu(W.x) * (W2.x). Its tiles interleave with W's: logical tile 2p is W's tile p, 2p+1 is W2's.
+    int glu;
+    const uint8_t* W2;
+    const uint16_t* scales2;
+    const float* rscale2;
 };
+
+// Logical 16-row tiles of a launch (twice the output tiles under the gated epilogue).
+inline int64_t gemv_tiles(int64_t N, int glu) { return (N + 15) / 16 * (glu ? 2 : 1); }
 
 // One instantiation of the CUDA-core streaming kernel.
 struct SimtConfig {
@@ -89,7 +103,7 @@ int mma2_num_configs(int fmt);
 MmaConfig mma2_config(int fmt, int idx);
 int mma2_max_batch(int fmt);
 int mma2_block_k(int fmt);
-size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ);
+size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu = 0);
 cudaError_t launch_gemv_mma2(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
 
 // Latency-oriented kernel tables (gemv_lat.cu).
@@ -97,8 +111,8 @@ int lat_num_configs(int fmt);
 LatConfig lat_config(int fmt, int idx);
 int lat_max_batch(int fmt);
 int lat_block_k(int fmt);
-int lat_items_per_warp(int fmt, const LatConfig& c, int64_t N, int64_t K, int split, int occ);
-size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, int split, int occ);
+int lat_items_per_warp(int fmt, const LatConfig& c, int64_t N, int64_t K, int split, int occ, int glu = 0);
+size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu = 0);
 cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
 
 // tcgen05 skinny GEMM (gemm_tc.cu): Y = X . W^T for the whole batch M.

@@ -31,7 +31,7 @@ static std::map<std::tuple<int, int, int64_t, int64_t, int64_t>, Plan> g_plans;
 static const size_t kSmemLimit = 200 * 1024;
 
 static int fmt_of_op(int op) {
-    switch (op) {
+    switch (op & MBW_OP_BASE_MASK) {
         case MBW_OP_GEMV_INT4_G64: return FMT_G64;
         case MBW_OP_GEMV_INT4_AWQ_G128: return FMT_AWQ;
         case MBW_OP_GEMV_INT8_PC: return FMT_I8;
@@ -70,9 +70,12 @@ static int64_t kblocks(int fmt, int64_t K) {
     return (K + BK - 1) / BK;
 }
 
-static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K) {
-    (void)N;
+// `fuse`: the MBW_FUSE_* bits of the call. Fused calls run on the "mma2" and
+// latency families only (the kernels with the prologue and epilogue hooks).
+static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K, int fuse = 0) {
     if (p.split < 1 || p.split > 8) return false;
+    const int glu = (fuse & MBW_FUSE_GLU) ? 1 : 0;
+    if (fuse && p.kind != PLAN_MMA2 && p.kind != PLAN_LAT) return false;
     if (p.kind == PLAN_TC) {
         // tensor-core skinny GEMM: BF16, batches above the GEMV column width
         if (fmt == FMT_AWQ) {
@@ -116,7 +119,7 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K) 
         if (K % bk != 0) return false;
         const int mb = (int)std::min<int64_t>(M, mma2_max_batch(fmt));
         if ((int64_t)p.split * c.warps > K / bk) return false;
-        if (mma2_smem_bytes(fmt, c, N, K, mb, p.split, p.occ) > kSmemLimit) return false;
+        if (mma2_smem_bytes(fmt, c, N, K, mb, p.split, p.occ, glu) > kSmemLimit) return false;
         return true;
     }
     if (p.kind == PLAN_LAT) {
@@ -124,10 +127,10 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K) 
         const LatConfig c = lat_config(fmt, p.cfg);
         if (p.occ < 1 || p.occ > 2) return false;
         const int mb = (int)std::min<int64_t>(M, lat_max_batch(fmt));
-        const int items = lat_items_per_warp(fmt, c, N, K, p.split, p.occ);
+        const int items = lat_items_per_warp(fmt, c, N, K, p.split, p.occ, glu);
         if (items < 1 || items > c.ni) return false;
         if (c.ni > items + 1) return false;  // a smaller instantiation holds this share
-        if (lat_smem_bytes(fmt, c, N, K, mb, p.split, p.occ) > kSmemLimit) return false;
+        if (lat_smem_bytes(fmt, c, N, K, mb, p.split, p.occ, glu) > kSmemLimit) return false;
         return true;
     }
     if (p.kind == PLAN_TMA) {
@@ -146,53 +149,55 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K) 
 static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
     std::vector<Plan> out;
     const int fmt = fmt_of_op(op);
+    const int fuse = op & MBW_FUSE_MASK;
     const int64_t Mb = std::min<int64_t>(M, 8);
     if (op == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4)
         for (int sp = 1; sp <= 8; ++sp) {
             Plan p{PLAN_TC, 0, sp, 1};
-            if (plan_valid(fmt, p, M, N, K)) out.push_back(p);
+            if (plan_valid(fmt, p, M, N, K, fuse)) out.push_back(p);
         }
     if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 8)
         for (int ring = 0; ring <= 1; ++ring)
             for (int sp = 1; sp <= 8; ++sp) {
                 Plan p{PLAN_TC, ring, sp, 1};
-                if (plan_valid(fmt, p, M, N, K)) out.push_back(p);
+                if (plan_valid(fmt, p, M, N, K, fuse)) out.push_back(p);
             }
     const int splits[4] = {1, 2, 4, 8};
     for (int cfg = 0; cfg < mma_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si)
             for (int occ = 1; occ <= 2; ++occ) {
                 Plan p{PLAN_MMA, cfg, splits[si], occ};
-                if (plan_valid(fmt, p, Mb, N, K)) out.push_back(p);
+                if (plan_valid(fmt, p, Mb, N, K, fuse)) out.push_back(p);
             }
     for (int cfg = 0; cfg < mma2_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si)
             for (int occ = 1; occ <= 2; ++occ) {
                 Plan p{PLAN_MMA2, cfg, splits[si], occ};
-                if (plan_valid(fmt, p, Mb, N, K)) out.push_back(p);
+                if (plan_valid(fmt, p, Mb, N, K, fuse)) out.push_back(p);
             }
     for (int cfg = 0; cfg < lat_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si)
             for (int occ = 1; occ <= 2; ++occ) {
                 Plan p{PLAN_LAT, cfg, splits[si], occ};
-                if (plan_valid(fmt, p, Mb, N, K)) out.push_back(p);
+                if (plan_valid(fmt, p, Mb, N, K, fuse)) out.push_back(p);
             }
     for (int cfg = 0; cfg < tma_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si)
             for (int occ = 1; occ <= 2; ++occ) {
                 Plan p{PLAN_TMA, cfg, splits[si], occ};
-                if (plan_valid(fmt, p, Mb, N, K)) out.push_back(p);
+                if (plan_valid(fmt, p, Mb, N, K, fuse)) out.push_back(p);
             }
     for (int cfg = 0; cfg < simt_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si) {
             Plan p{PLAN_SIMT, cfg, splits[si], 1};
-            if (plan_valid(fmt, p, Mb, N, K)) out.push_back(p);
+            if (plan_valid(fmt, p, Mb, N, K, fuse)) out.push_back(p);
         }
     return out;
 }
 
 Plan plan_default(int op, int64_t M, int64_t N, int64_t K) {
     const int fmt = fmt_of_op(op);
+    const int fuse = op & MBW_FUSE_MASK;
     const int64_t Mb = std::min<int64_t>(M, 8);
     const int sms = device_sm_count();
     if ((op == MBW_OP_GEMM_SKINNY_BF16 && M > 8) || (op == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4)) {
@@ -202,18 +207,18 @@ Plan plan_default(int op, int64_t M, int64_t N, int64_t K) {
         int split = 1;
         while (split < 8 && tiles * (split + 1) <= sms) ++split;
         Plan p{PLAN_TC, 0, split, 1};
-        while (!plan_valid(fmt, p, M, N, K) && p.split > 1) --p.split;
+        while (!plan_valid(fmt, p, M, N, K, fuse) && p.split > 1) --p.split;
         return p;
     }
-    if (fmt == FMT_I8) {
-        // INT8 runs on the "mma2" and latency families only: 8 warps, 3
-        // super-blocks in flight in registers, one CTA per SM; split K over a
-        // cluster while there are fewer 16-row tiles than SMs.
+    if (fmt == FMT_I8 || fuse) {
+        // INT8 and fused calls run on the "mma2" and latency families only: 8
+        // warps, 3 super-blocks in flight in registers, one CTA per SM; split K
+        // over a cluster while there are fewer 16-row tiles than SMs.
         const int64_t tiles = (N + 15) / 16;
         Plan p{PLAN_MMA2, 1, 1, 1};
         while (p.split < 8 && tiles * p.split < sms && (int64_t)8 * p.split * 2 <= K / 128) p.split *= 2;
-        while (!plan_valid(fmt, p, Mb, N, K) && p.split > 1) p.split /= 2;
-        if (plan_valid(fmt, p, Mb, N, K)) return p;
+        while (!plan_valid(fmt, p, Mb, N, K, fuse) && p.split > 1) p.split /= 2;
+        if (plan_valid(fmt, p, Mb, N, K, fuse)) return p;
         const std::vector<Plan> c = candidates(op, M, N, K);
         if (!c.empty()) return c.front();
         return p;
@@ -233,8 +238,8 @@ Plan plan_default(int op, int64_t M, int64_t N, int64_t K) {
     int split = 1;
     while (split < 8 && tiles * split < sms && (int64_t)8 * split * 2 <= KB) split *= 2;
     Plan p{PLAN_MMA, cfg, split, 1};
-    while (!plan_valid(fmt, p, Mb, N, K) && p.split < 8) p.split *= 2;
-    if (plan_valid(fmt, p, Mb, N, K)) return p;
+    while (!plan_valid(fmt, p, Mb, N, K, fuse) && p.split < 8) p.split *= 2;
+    if (plan_valid(fmt, p, Mb, N, K, fuse)) return p;
     const std::vector<Plan> c = candidates(op, M, N, K);
     if (!c.empty()) return c.front();
     return Plan{PLAN_MMA, cfg, 8, 1};
@@ -298,7 +303,11 @@ std::string plan_to_string(int op, const Plan& p) {
         snprintf(buf, sizeof(buf), "simt fmt=%s warps=%d rows_per_warp=%d chunks_in_flight=%d batch=%d split_k=%d",
                  fs, c.warps, c.r, c.u, c.mb, p.split);
     }
-    return buf;
+    std::string out = buf;
+    if (op & MBW_FUSE_NORM) out += " +rmsnorm";
+    if (op & MBW_FUSE_GLU) out += " +swiglu";
+    if (op & MBW_FUSE_RESIDUAL) out += " +residual";
+    return out;
 }
 
 cudaError_t launch_plan(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
@@ -321,9 +330,12 @@ static size_t weight_bytes(int fmt, int64_t N, int64_t K) {
 }
 
 static bool shape_ok(int op, int64_t M, int64_t N, int64_t K) {
-    if (op < MBW_OP_GEMV_BF16 || op > MBW_OP_GEMV_INT8_PC) return false;
+    const int base = op & MBW_OP_BASE_MASK, fuse = op & ~MBW_OP_BASE_MASK;
+    if (base < MBW_OP_GEMV_BF16 || base > MBW_OP_GEMV_INT8_PC) return false;
+    if (fuse & ~MBW_FUSE_MASK) return false;
+    if (fuse && base != MBW_OP_GEMV_BF16 && base != MBW_OP_GEMV_INT4_G64 && base != MBW_OP_GEMV_INT8_PC) return false;
     if (M < 1 || N < 1 || K < 1 || N > 0x7FFFFFFF || K > 0x7FFFFFFF || M > 0x7FFFFFFF) return false;
-    if (op == MBW_OP_GEMV_INT4_G64 && M != 1) return false;
+    if (base == MBW_OP_GEMV_INT4_G64 && M != 1) return false;
     const int fmt = fmt_of_op(op);
     const int64_t kunit = fmt == FMT_BF16 ? 8 : fmt == FMT_G64 ? 64 : 128;  // AWQ and INT8: 128
     return K % kunit == 0;
@@ -399,7 +411,11 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
     // candidates are timed at the call's batch (a GEMV plan narrower than M
     // is launched once per batch slice, as the call would)
     const int64_t Mb = M;
-    const size_t wb = weight_bytes(fmt, N, K);
+    const int fuse = op & MBW_FUSE_MASK;
+    const int glu = (fuse & MBW_FUSE_GLU) ? 1 : 0;
+    const size_t wb1 = weight_bytes(fmt, N, K);
+    const size_t wstride1 = (wb1 + 255) / 256 * 256;
+    const size_t wb = glu ? 2 * wstride1 : wb1;  // gated calls stream the gate and the up matrix
     const size_t wstride = (wb + 255) / 256 * 256;
     const size_t target = (size_t)384 << 20;  // about three times the L2
     int copies = (int)std::max<size_t>(2, (target + wb - 1) / wb);
@@ -408,11 +424,17 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
     uint8_t* wbuf = nullptr;
     uint16_t* xbuf = nullptr;
     void* ybuf = nullptr;
+    uint16_t* nbuf = nullptr;  // RMSNorm weight
+    uint16_t* rbuf = nullptr;  // residual
     e = cudaMalloc(&wbuf, wstride * copies);
     if (e == cudaSuccess) e = cudaMalloc(&xbuf, (size_t)Mb * K * 2);
     if (e == cudaSuccess) e = cudaMalloc(&ybuf, (size_t)Mb * N * 4);
+    if (e == cudaSuccess && (fuse & MBW_FUSE_NORM)) e = cudaMalloc(&nbuf, (size_t)K * 2);
+    if (e == cudaSuccess && (fuse & MBW_FUSE_RESIDUAL)) e = cudaMalloc(&rbuf, (size_t)Mb * N * 2);
     if (e == cudaSuccess) e = cudaMemsetAsync(wbuf, 0x37, wstride * copies, stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(xbuf, 0x37, (size_t)Mb * K * 2, stream);
+    if (e == cudaSuccess && nbuf) e = cudaMemsetAsync(nbuf, 0x37, (size_t)K * 2, stream);
+    if (e == cudaSuccess && rbuf) e = cudaMemsetAsync(rbuf, 0x37, (size_t)Mb * N * 2, stream);
     cudaEvent_t t0 = nullptr, t1 = nullptr;
     if (e == cudaSuccess) e = cudaEventCreate(&t0);
     if (e == cudaSuccess) e = cudaEventCreate(&t1);
@@ -433,6 +455,10 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
         a.groups = (int)(fmt == FMT_G64 ? K / 64 : fmt == FMT_AWQ ? K / 128 : 0);
         a.zstride = (a.groups + 1) / 2;
         a.out_f32 = 0;
+        a.norm_w = nbuf;
+        a.norm_eps = 1e-6f;
+        a.residual = rbuf;
+        a.glu = glu;
         const size_t codes = fmt == FMT_BF16 ? (size_t)N * K * 2 : fmt == FMT_I8 ? (size_t)N * K : (size_t)N * K / 2;
         const int slices = (int)((Mb + a.M - 1) / a.M);  // launches per call at this batch
         cudaGraph_t g = nullptr;
@@ -445,6 +471,11 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
             a.scales = (const uint16_t*)(a.W + codes);
             a.zeros = (const uint8_t*)(a.W + codes + (size_t)N * a.groups * 2);
             a.rscale = (const float*)(a.W + codes);
+            if (glu) {
+                a.W2 = a.W + wstride1;
+                a.scales2 = (const uint16_t*)(a.W2 + codes);
+                a.rscale2 = (const float*)(a.W2 + codes);
+            }
             for (int sl = 0; sl < slices && le == cudaSuccess; ++sl) le = launch_plan(fmt, p, a, stream);
         }
         e = cudaStreamEndCapture(stream, &g);
@@ -492,6 +523,8 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
     if (wbuf) cudaFree(wbuf);
     if (xbuf) cudaFree(xbuf);
     if (ybuf) cudaFree(ybuf);
+    if (nbuf) cudaFree(nbuf);
+    if (rbuf) cudaFree(rbuf);
     if (e != cudaSuccess) {
         set_last_error(std::string("mbw_autotune: ") + cudaGetErrorString(e));
         return MBW_ERR_CUDA;

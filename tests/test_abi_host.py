@@ -61,6 +61,12 @@ def test_status_strings(L):
         assert L.mbw_status_string(code).decode() == name
 
 
+def _fusion(norm=None, eps=1e-6, res=None, up=None, ups=None):
+    f = B.MbwFusion()
+    f.norm_weight, f.norm_eps, f.residual, f.up_weights, f.up_scales = norm, eps, res, up, ups
+    return ctypes.byref(f)
+
+
 A16 = 0x10000  # fake, 16-byte aligned addresses: never dereferenced on these paths
 A16b = 0x20000
 A16c = 0x30000
@@ -90,6 +96,16 @@ A16c = 0x30000
     (lambda L: L.gemm_skinny_bf16(A16, A16b + 16, A16c, 4, 8, 16, None, 0, None), 2),
     (lambda L: L.gemv_int8_pc(A16 + 16, A16b, A16c, A16, 1, 8, 256, None, 0, None), 2),
     (lambda L: L.gemv_int8_pc(A16, A16b, A16c, A16, 1, 8, 192, None, 0, None), 3),
+    (lambda L: L.gemv_fused(3, A16, A16b, A16c, A16, 1, 8, 256, None, None, 0, None), 1),  # AWQ: no fused path
+    (lambda L: L.gemv_fused(1, A16, None, A16c, A16, 1, 8, 0, None, None, 0, None), 3),     # K = 0
+    (lambda L: L.gemv_fused(2, A16, A16b, A16c, A16, 2, 8, 256, None, None, 0, None), 3),   # g64 takes M = 1
+    (lambda L: L.gemv_fused(5, A16 + 16, A16b, A16c, A16, 1, 8, 256, None, None, 0, None), 2),
+    (lambda L: L.gemv_fused(5, A16, None, A16c, A16, 1, 8, 256, None, None, 0, None), 1),
+    (lambda L: L.gemv_fused(1, A16, None, A16c, A16, 1, 8, 256, _fusion(norm=A16b + 8), None, 0, None), 2),
+    (lambda L: L.gemv_fused(1, A16, None, A16c, A16, 1, 8, 256, _fusion(norm=A16b, eps=-1.0), None, 0, None), 1),
+    (lambda L: L.gemv_fused(5, A16, A16b, A16c, A16, 1, 8, 256, _fusion(up=A16c), None, 0, None), 1),  # no up_scales
+    (lambda L: L.gemv_fused(5, A16, A16b, A16c, A16, 1, 8, 256, _fusion(up=A16c + 16, ups=A16b), None, 0, None), 2),
+    (lambda L: L.gemv_fused(1, A16, None, A16c, A16, 1, 8, 96, _fusion(res=A16b), None, 0, None), 3),  # fused BF16: K % 64
     (lambda L: L.gemv_int8_pc(A16, A16b + 2, A16c, A16, 1, 8, 256, None, 0, None), 2),
     (lambda L: L.gemv_int8_pc(A16 + 8, A16b, A16c, A16, 1, 8, 256, None, 0, None), 2),
     (lambda L: L.gemv_int8_pc(A16, None, A16c, A16, 1, 8, 256, None, 0, None), 1),
@@ -123,6 +139,16 @@ def test_planner_host_logic(L):
     assert L.mbw_plan_candidates(2, 1, 8, 96) == 0  # K not a multiple of 64
     assert L.mbw_plan_candidates(7, 1, 8, 64) == 0
     assert L.mbw_plan_candidates(5, 1, 8, 192) == 0  # INT8: K not a multiple of 128
+    # fused ops: only the mma2 and latency families, described with their fusions
+    for op in (1 | 0x100, 2 | 0x300, 5 | 0x700):
+        n = L.mbw_plan_candidates(op, 1, 2048, 2048)
+        assert 1 <= n < L.mbw_plan_candidates(op & 0xFF, 1, 2048, 2048) or (op & 0xFF) == 5
+        for i in range(n):
+            assert L.mbw_plan_select(op, 1, 2048, 2048, i) == 0
+            assert L.mbw_plan_describe(op, 1, 2048, 2048, buf, 256) == 0
+            assert buf.value.split()[0] in (b"mma2", b"lat") and b"+" in buf.value
+    assert L.mbw_plan_candidates(3 | 0x100, 1, 2048, 2048) == 0  # no fused AWQ
+    assert L.mbw_plan_candidates(5 | 0x800, 1, 2048, 2048) == 0  # unknown fusion bit
     buf = ctypes.create_string_buffer(256)
     assert L.mbw_plan_describe(5, 1, 9728, 2560, buf, 256) == 0 and b"int8_pc" in buf.value
     assert L.mbw_workspace_bytes(1, 1, 2048, 2048) == 0

@@ -1,0 +1,173 @@
+"""GPU parity of the fused GEMV calls (gemv_fused) against the fp64 oracle.
+
+The fusions follow the pages: an RMSNorm prologue folded into the projection
+(llm-rs vs vLLM, "norms folded into the projections"), the gated SiLU product
+silu(W1.x) * (W3.x) and the residual add in the GEMV epilogue (yalm, sec. 3.3;
+TileInfer: SwiGLU in the GEMV epilogue). Every combination runs every
+candidate plan (mma2 and latency families) on ragged shapes of each format.
+
+Tolerance (derived from the arithmetic; the kernels accumulate in fp32):
+  with A = sum_k |w_ik xn_k| of each product and v the oracle's value,
+  e = (1e-4 + 2^-7 [prologue]) * A bounds the error of each fp32 row sum (the
+  kernel's bf16 xn may differ from the oracle's by one bf16 ulp, at most 2^-7
+  relative); the gated product propagates it as 1.1 |up| e_gate + |silu(gate)| e_up
+  (|silu'| <= 1.1); the bf16 store adds 2^-8 |v| + 1e-5.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_util import dev_bf16, dev_f16, dev_u8, host_f64
+from memory_bound_weight_gb300 import inputs as gen
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - the marker keeps these off CPU runs
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+import memory_bound_weight_gb300 as mbw  # noqa: E402
+
+COMBOS = {"norm": (1, 0, 0), "glu": (0, 1, 0), "res": (0, 0, 1), "norm+glu": (1, 1, 0), "norm+res": (1, 0, 1),
+          "glu+res": (0, 1, 1), "all": (1, 1, 1)}
+SHAPES = [("bf16", 33, 512, 1), ("bf16", 130, 1024, 3), ("g64", 45, 512, 1), ("g64", 300, 2048, 1),
+          ("i8", 77, 640, 1), ("i8", 257, 2560, 2)]
+OPS = {"bf16": mbw.OP_GEMV_BF16, "g64": mbw.OP_GEMV_INT4_G64, "i8": mbw.OP_GEMV_INT8_PC}
+EPS = 1e-5
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load()
+
+
+def weights(fmt, seed, mi, N, K):
+    """Host arrays and device tensors of one weight matrix."""
+    if fmt == "bf16":
+        W = gen.bf16_weights(seed, mi, N, K)
+        return (W, None), (dev_bf16(W), None)
+    if fmt == "g64":
+        c, s = gen.int4_codes(seed, mi, N, K), gen.f16_group_scales(seed, mi, N, K // 64)
+        return (c, s), (dev_u8(c), dev_f16(s))
+    q, s = gen.int8_codes(seed, mi, N, K), gen.f32_row_scales(seed, mi, N)
+    return (q, s), (torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda())
+
+
+def ogemm(orc, fmt, w, X):
+    if fmt == "bf16":
+        return orc.gemm_bf16(w[0], X)
+    if fmt == "g64":
+        return orc.gemm_int4_g64(w[0], w[1], X)
+    return orc.gemm_int8_pc(w[0], w[1], X)
+
+
+def reference(orc, fmt, w, wu, X, g, R):
+    """Oracle value and tolerance of the fused output."""
+    Xn = orc.rmsnorm_bf16(X, g, EPS) if g is not None else X
+    yg, ag = ogemm(orc, fmt, w, Xn)
+    e_rel = 1e-4 + (2.0 ** -7 if g is not None else 0.0)
+    if wu is not None:
+        yu, au = ogemm(orc, fmt, wu, Xn)
+        v = orc.swiglu(yg, yu)
+        sg = np.abs(orc.swiglu(yg, np.ones_like(yg)))
+        err = 1.1 * np.abs(yu) * e_rel * ag + sg * e_rel * au + 1.1 * (e_rel * ag) * (e_rel * au)
+    else:
+        v, err = yg, e_rel * ag
+    if R is not None:
+        v = orc.add_residual(v, R)
+    return v, err + 2.0 ** -8 * np.abs(v) + 1e-5
+
+
+def check(y, v, tol, what):
+    got = host_f64(y).reshape(v.shape)
+    bad = np.abs(got - v) > tol
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} out of tolerance; first {i}: got {got[i]!r} "
+                             f"want {v[i]!r} tol {tol[i]!r}")
+
+
+def fused_op(op, norm, glu, res):
+    return op | (mbw.FUSE_NORM if norm else 0) | (mbw.FUSE_GLU if glu else 0) | (mbw.FUSE_RESIDUAL if res else 0)
+
+
+@pytest.mark.parametrize("combo", sorted(COMBOS))
+@pytest.mark.parametrize("fmt,N,K,M", SHAPES, ids=[f"{s[0]}-{s[1]}x{s[2]}-M{s[3]}" for s in SHAPES])
+def test_fused_every_plan(orc, fmt, N, K, M, combo):
+    norm, glu, res = COMBOS[combo]
+    seed = 1300 + N + K
+    w, wd = weights(fmt, seed, 0, N, K)
+    wu, wud = weights(fmt, seed, 1, N, K) if glu else ((None, None), (None, None))
+    X = gen.bf16_activations(seed, 2, M, K)
+    g = gen.bf16_activations(seed, 3, 1, K)[0] if norm else None
+    R = gen.bf16_activations(seed, 4, M, N) if res else None
+    v, tol = reference(orc, fmt, w, wu if glu else None, X, g, R)
+    Xd = dev_bf16(X)
+    gd = dev_bf16(g) if norm else None
+    Rd = dev_bf16(R) if res else None
+    op = fused_op(OPS[fmt], norm, glu, res)
+    n = mbw.plan_candidates(op, M, N, K)
+    assert n >= 1
+    for i in range(n):
+        mbw.plan_select(op, M, N, K, i)
+        desc = mbw.plan_describe(op, M, N, K)
+        y = mbw.gemv_fused(OPS[fmt], wd[0], wd[1], Xd, norm_weight=gd, norm_eps=EPS, residual=Rd,
+                           up_weights=wud[0], up_scales=wud[1])
+        check(y, v, tol, f"{fmt} {combo} {M}x{N}x{K} plan {desc}")
+
+
+def test_rmsnorm_prologue_matches_the_oracle_bf16(orc):
+    """W = identity (BF16), fp32 output: y is the kernel's own normalised bf16
+    x. It equals the oracle's RMSNorm except where the fp32 factor rounds to
+    the other bf16 neighbour (at most one ulp, and rarely)."""
+    K = 1024
+    X = gen.bf16_activations(1401, 0, 4, K)
+    g = gen.bf16_activations(1401, 1, 1, K)[0]
+    ref = orc.rmsnorm_bf16(X, g, EPS)
+    eye = torch.eye(K, dtype=torch.bfloat16, device="cuda")
+    op = fused_op(mbw.OP_GEMV_BF16, 1, 0, 0)
+    for i in range(mbw.plan_candidates(op, 4, K, K)):
+        mbw.plan_select(op, 4, K, K, i)
+        with mbw.output_fp32():
+            y = mbw.gemv_fused(mbw.OP_GEMV_BF16, eye, None, dev_bf16(X), norm_weight=dev_bf16(g), norm_eps=EPS)
+        got = y.to(torch.bfloat16).cpu().view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(host_f64(y), host_f64(y.to(torch.bfloat16)))  # y is a bf16 value
+        diff = np.abs(got.astype(np.int32) - ref.astype(np.int32))
+        assert diff.max() <= 1 and (diff > 0).mean() < 0.01, (mbw.plan_describe(op, 4, K, K), int((diff > 0).sum()))
+
+
+def test_residual_in_place_and_determinism(orc):
+    N, K, M = 2560, 2048, 2
+    w, wd = weights("i8", 1411, 0, N, K)
+    X = gen.bf16_activations(1411, 2, M, K)
+    R = gen.bf16_activations(1411, 4, M, N)
+    v, tol = reference(orc, "i8", w, None, X, None, R)
+    Y = dev_bf16(R).clone()
+    mbw.gemv_fused(mbw.OP_GEMV_INT8_PC, wd[0], wd[1], dev_bf16(X), out=Y, residual=Y)  # y += W.x in place
+    check(Y, v, tol, "in-place residual")
+    # the same call twice gives bitwise the same result
+    a = mbw.gemv_fused(mbw.OP_GEMV_INT8_PC, wd[0], wd[1], dev_bf16(X), residual=dev_bf16(R))
+    b = mbw.gemv_fused(mbw.OP_GEMV_INT8_PC, wd[0], wd[1], dev_bf16(X), residual=dev_bf16(R))
+    assert torch.equal(a, b)
+
+
+def test_fused_tinyllama_shapes_sampled_rows(orc):
+    """The TinyLlama decode step's fused calls: q/k/v with the attention
+    RMSNorm, gate/up (5632 + 5632 rows) with the MLP RMSNorm and SwiGLU, down
+    and o with the residual add; every row compared."""
+    K = 2048
+    X = gen.bf16_activations(1421, 0, 1, K)
+    g = gen.bf16_activations(1421, 1, 1, K)[0]
+    cases = [("qkv", 2560, 2048, (1, 0, 0)), ("gate_up", 5632, 2048, (1, 1, 0)), ("o", 2048, 2048, (0, 0, 1)),
+             ("down", 2048, 5632, (0, 0, 1))]
+    for name, N, Kc, (norm, glu, res) in cases:
+        Xc = X if Kc == K else gen.bf16_activations(1421, 5, 1, Kc)
+        w, wd = weights("g64", 1421, 10, N, Kc)
+        wu, wud = weights("g64", 1421, 11, N, Kc) if glu else ((None, None), (None, None))
+        R = gen.bf16_activations(1421, 6, 1, N) if res else None
+        v, tol = reference(orc, "g64", w, wu if glu else None, Xc, g if norm else None, R)
+        mbw.autotune(fused_op(mbw.OP_GEMV_INT4_G64, norm, glu, res), 1, N, Kc)
+        y = mbw.gemv_fused(mbw.OP_GEMV_INT4_G64, wd[0], wd[1], dev_bf16(Xc[0]),
+                           norm_weight=dev_bf16(g) if norm else None, norm_eps=EPS,
+                           residual=dev_bf16(R[0]) if res else None, up_weights=wud[0], up_scales=wud[1])
+        check(y, v[0], tol[0], f"tinyllama {name}")
