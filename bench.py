@@ -61,8 +61,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="mbw", choices=["mbw", "reference"])
     p.add_argument("--workload", default="tinyllama_int4",
-                   choices=["tinyllama_int4", "tinyllama_int4_unfused", "qwen_bf16", "qwen_awq", "qwen3_int8",
-                            "bf16_2048"])
+                   choices=["tinyllama_int4", "tinyllama_int4_fusedops", "tinyllama_int4_unfused", "qwen_bf16",
+                            "qwen_awq", "qwen3_int8", "bf16_2048"])
     p.add_argument("--batch", type=int, default=1,
                    help="activation rows per GEMV (qwen_awq: AWQ-style INT4 decode at batch M)")
     p.add_argument("--no-e2e", action="store_true")
@@ -225,29 +225,64 @@ class Step:
             inputs_gpu.bf16_normal_(xv, seed, gen.stream_id(mi, gen.KIND_X), gen.X_SIGMA)
             xa = xv if M == 1 else xv.view(M, m.K)
             ya = yv if M == 1 else yv.view(M, m.N)
-            self.calls.append(device_call(fmt, seed, mi, m.N, m.K, xa, ya, device))
+            self.calls.append(device_call(fmt, seed, mi, m.N, m.K, xa, ya, device, m.fuse, M))
             ko += M * m.K
             no += M * m.N
-        self.op = {wl.FMT_INT4_G64: mbw.OP_GEMV_INT4_G64, wl.FMT_INT4_AWQ_G128: mbw.OP_GEMV_INT4_AWQ_G128,
-                   wl.FMT_BF16: mbw.OP_GEMV_BF16, wl.FMT_INT8_PC: mbw.OP_GEMV_INT8_PC}[fmt]
+        self.op = op_of_fmt(fmt)
         self.bytes_alg = wl.step_bytes_alg(mats, fmt, M)
-        self.flops = sum(wl.flops(M, m.N, m.K) for m in mats)
-        self.h2d_bytes = 2 * M * sumK
+        self.flops = sum(wl.call_flops(M, m) for m in mats)
+        # e2e: the x vectors and the residuals the calls read come from the host
+        self.h2d_bytes = 2 * M * sumK + sum(2 * M * m.N for m in mats if m.fuse & wl.FUSE_RESIDUAL)
         self.d2h_bytes = 2 * M * sumN
 
     def shapes(self):
-        return sorted({(m.N, m.K) for m in self.mats})
+        """Distinct call kinds (fusion bits, N, K)."""
+        return sorted({(m.fuse, m.N, m.K) for m in self.mats})
 
     def run(self):
         for fn, args, out in self.calls:
             fn(*args, out=out)
 
 
-def device_call(fmt, seed, mi, N, K, x, y, device):
-    """(C-ABI call, its inputs, its output) for matrix `mi` of a workload, with
-    the matrix generated on the device."""
+def op_of_fmt(fmt):
     import memory_bound_weight_gb300 as mbw
+
+    return {wl.FMT_INT4_G64: mbw.OP_GEMV_INT4_G64, wl.FMT_INT4_AWQ_G128: mbw.OP_GEMV_INT4_AWQ_G128,
+            wl.FMT_BF16: mbw.OP_GEMV_BF16, wl.FMT_INT8_PC: mbw.OP_GEMV_INT8_PC}[fmt]
+
+
+def skey(kind):
+    """String key of a call kind (fusion bits, N, K): "NxK" plus its fusions."""
+    fz, N, K = kind
+    return f"{N}x{K}" + ("+norm" if fz & wl.FUSE_NORM else "") + ("+glu" if fz & wl.FUSE_GLU else "") + \
+        ("+res" if fz & wl.FUSE_RESIDUAL else "")
+
+
+def device_call(fmt, seed, mi, N, K, x, y, device, fuse=0, M=1):
+    """(C-ABI call, its inputs, its output) for matrix `mi` of a workload, with
+    the matrix generated on the device. A fused call also gets its up matrix,
+    norm weight and residual (seeded like the rest)."""
+    import functools
+
+    import memory_bound_weight_gb300 as mbw
+    from memory_bound_weight_gb300 import inputs as gen
     from memory_bound_weight_gb300 import inputs_gpu
+
+    if fuse:
+        base = op_of_fmt(fmt)
+        W, sc = device_weights(fmt, seed, mi, N, K, device)
+        kw = {}
+        if fuse & wl.FUSE_GLU:
+            kw["up_weights"], kw["up_scales"] = device_weights(fmt, seed, 50000 + mi, N, K, device)
+        if fuse & wl.FUSE_NORM:
+            g = torch_empty((K,), device)
+            inputs_gpu.bf16_normal_(g, seed, gen.stream_id(60000 + mi, gen.KIND_X), gen.X_SIGMA)
+            kw["norm_weight"], kw["norm_eps"] = g, 1e-6
+        if fuse & wl.FUSE_RESIDUAL:
+            r = torch_empty((M, N) if M > 1 else (N,), device)
+            inputs_gpu.bf16_normal_(r.view(-1), seed, gen.stream_id(70000 + mi, gen.KIND_X), gen.X_SIGMA)
+            kw["residual"] = r
+        return functools.partial(mbw.gemv_fused, base, W, sc, x, **kw), (), y
 
     if fmt == wl.FMT_INT4_G64:
         c = inputs_gpu.int4_codes(seed, mi, N, K, device)
@@ -267,8 +302,28 @@ def device_call(fmt, seed, mi, N, K, x, y, device):
     raise ValueError(fmt)
 
 
+def torch_empty(shape, device):
+    import torch
+
+    return torch.empty(shape, dtype=torch.bfloat16, device=device)
+
+
+def device_weights(fmt, seed, mi, N, K, device):
+    """(weights, scales) of matrix `mi`, generated on the device (scales None for BF16)."""
+    from memory_bound_weight_gb300 import inputs_gpu
+
+    if fmt == wl.FMT_INT4_G64:
+        return inputs_gpu.int4_codes(seed, mi, N, K, device), inputs_gpu.f16_group_scales(seed, mi, N, K // 64, device)
+    if fmt == wl.FMT_INT8_PC:
+        return inputs_gpu.int8_codes(seed, mi, N, K, device), inputs_gpu.f32_row_scales(seed, mi, N, device)
+    if fmt == wl.FMT_BF16:
+        return inputs_gpu.bf16_weights(seed, mi, N, K, device), None
+    raise ValueError(fmt)
+
+
 WORKLOAD_MATS = {
     "tinyllama_int4": (lambda: wl.tinyllama_step(fused=True), wl.FMT_INT4_G64),
+    "tinyllama_int4_fusedops": (lambda: wl.tinyllama_step(fusedops=True), wl.FMT_INT4_G64),
     "tinyllama_int4_unfused": (lambda: wl.tinyllama_step(), wl.FMT_INT4_G64),
     "qwen_bf16": (wl.qwen25_7b_step, wl.FMT_BF16),
     "qwen_awq": (wl.qwen25_7b_step, wl.FMT_INT4_AWQ_G128),
@@ -278,9 +333,9 @@ WORKLOAD_MATS = {
 
 
 def make_step(workload, seed, device, M=1):
-    if workload in ("tinyllama_int4", "tinyllama_int4_unfused"):
+    if workload in ("tinyllama_int4", "tinyllama_int4_unfused", "tinyllama_int4_fusedops"):
         return Step("TinyLlama-1.1B-shaped INT4 g64 decode step, batch 1", wl.FMT_INT4_G64,
-                    wl.tinyllama_step(fused=(workload == "tinyllama_int4")), seed, device)
+                    WORKLOAD_MATS[workload][0](), seed, device)
     if workload == "qwen_bf16":
         return Step("Qwen2.5-7B-shaped BF16 decode step, batch 1", wl.FMT_BF16, wl.qwen25_7b_step(), seed, device)
     if workload == "qwen_awq":
@@ -312,6 +367,27 @@ def cpu_baseline(workload, budget_s=10.0, M=1):
     else:
         mk, fmt = WORKLOAD_MATS[workload]
         mats = mk()
+
+    def host_weights(mi, m):
+        if fmt == wl.FMT_INT4_G64:
+            return gen.int4_codes(0, mi, m.N, m.K), gen.f16_group_scales(0, mi, m.N, m.K // 64), None
+        if fmt == wl.FMT_INT8_PC:
+            return gen.int8_codes(0, mi, m.N, m.K), gen.f32_row_scales(0, mi, m.N), None
+        if fmt == wl.FMT_INT4_AWQ_G128:
+            G = m.K // 128
+            return (gen.int4_codes(0, mi, m.N, m.K), gen.f16_group_scales(0, mi, m.N, G),
+                    gen.u4_zero_points(0, mi, m.N, G))
+        return gen.bf16_weights(0, mi, m.N, m.K), None, None
+
+    def gemm(w, X):
+        A, B, Z = w
+        if fmt == wl.FMT_INT4_G64:
+            return o.gemm_int4_g64(A, B, X)[0]
+        if fmt == wl.FMT_INT8_PC:
+            return o.gemm_int8_pc(A, B, X)[0]
+        if fmt == wl.FMT_INT4_AWQ_G128:
+            return o.gemm_int4_awq_g128(A, B, Z, X)[0]
+        return o.gemm_bf16(A, X)[0]
     done_bytes = 0
     spent = 0.0
     n = 0
@@ -320,33 +396,26 @@ def cpu_baseline(workload, budget_s=10.0, M=1):
     cacheable = wl.step_weight_bytes(mats, fmt) < 2e9
     for mi, m in order:
         if mi in cache:
-            X, A, B, Z = cache[mi]
+            X, w, wu, G, R = cache[mi]
         else:
             X = gen.bf16_activations(0, mi, M, m.K)
-            Z = None
-            if fmt == wl.FMT_INT4_G64:
-                A, B = gen.int4_codes(0, mi, m.N, m.K), gen.f16_group_scales(0, mi, m.N, m.K // 64)
-            elif fmt == wl.FMT_INT8_PC:
-                A, B = gen.int8_codes(0, mi, m.N, m.K), gen.f32_row_scales(0, mi, m.N)
-            elif fmt == wl.FMT_INT4_AWQ_G128:
-                G = m.K // 128
-                A, B = gen.int4_codes(0, mi, m.N, m.K), gen.f16_group_scales(0, mi, m.N, G)
-                Z = gen.u4_zero_points(0, mi, m.N, G)
-            else:
-                A, B = gen.bf16_weights(0, mi, m.N, m.K), None
+            w = host_weights(mi, m)
+            wu = host_weights(50000 + mi, m) if m.fuse & wl.FUSE_GLU else None
+            G = gen.bf16_normal(0, gen.stream_id(60000 + mi, gen.KIND_X), m.K, gen.X_SIGMA) \
+                if m.fuse & wl.FUSE_NORM else None
+            R = gen.bf16_normal(0, gen.stream_id(70000 + mi, gen.KIND_X), M * m.N, gen.X_SIGMA).reshape(M, m.N) \
+                if m.fuse & wl.FUSE_RESIDUAL else None
             if cacheable:
-                cache[mi] = (X, A, B, Z)
+                cache[mi] = (X, w, wu, G, R)
         t = time.perf_counter()
-        if fmt == wl.FMT_INT4_G64:
-            o.gemm_int4_g64(A, B, X)
-        elif fmt == wl.FMT_INT8_PC:
-            o.gemm_int8_pc(A, B, X)
-        elif fmt == wl.FMT_INT4_AWQ_G128:
-            o.gemm_int4_awq_g128(A, B, Z, X)
-        else:
-            o.gemm_bf16(A, X)
+        Xn = o.rmsnorm_bf16(X, G, 1e-6) if G is not None else X
+        Y = gemm(w, Xn)
+        if wu is not None:
+            Y = o.swiglu(Y, gemm(wu, Xn))
+        if R is not None:
+            Y = o.add_residual(Y, R)
         spent += time.perf_counter() - t
-        done_bytes += wl.bytes_alg(fmt, M, m.N, m.K)
+        done_bytes += wl.call_bytes(fmt, M, m)
         n += 1
         if spent >= budget_s:
             break
@@ -390,6 +459,10 @@ def workload_desc(workload, batch=1):
     return {"tinyllama_int4": "TinyLlama-1.1B-shaped INT4 group-64 decode step, batch 1, q/k/v and gate/up fused "
                               "(89 GEMVs)",
             "tinyllama_int4_unfused": "TinyLlama-1.1B-shaped INT4 group-64 decode step, batch 1 (155 GEMVs)",
+            "tinyllama_int4_fusedops": "TinyLlama-1.1B-shaped INT4 group-64 decode step, batch 1, q/k/v and gate/up "
+                                       "fused, with the layer's small ops folded into the GEMVs: RMSNorm prologues "
+                                       "(q/k/v, gate/up, head), SwiGLU epilogue (gate/up), residual-add epilogues (o, "
+                                       "down) (89 GEMVs)",
             "qwen_bf16": "Qwen2.5-7B-shaped BF16 decode step, batch 1 (141 GEMVs)",
             "qwen_awq": f"Qwen2.5-7B-shaped AWQ-style INT4 decode step (group 128, fp16 scale, uint4 zero point, LM head "
                         f"included), batch {batch} (141 GEMMs)",
@@ -426,21 +499,21 @@ def main():
     if args.plans_from:
         with open(args.plans_from) as f:
             saved = json.load(f)
-        for N, K in step.shapes():
-            mbw.plan_select(step.op, Mb, N, K, int(saved[f"{N}x{K}"]))
+        for fz, N, K in step.shapes():
+            mbw.plan_select(step.op | fz, Mb, N, K, int(saved[skey((fz, N, K))]))
     else:
-        for N, K in step.shapes():
-            mbw.autotune(step.op, Mb, N, K)
+        for fz, N, K in step.shapes():
+            mbw.autotune(step.op | fz, Mb, N, K)
         if args.tune == "step":
             from memory_bound_weight_gb300.tune import tune_sequence
 
-            res = tune_sequence(step.run, [(step.op, Mb, N, K) for N, K in step.shapes()],
+            res = tune_sequence(step.run, [(step.op | fz, Mb, N, K) for fz, N, K in step.shapes()],
                                 log=(lambda m: print("[tune]", m, file=sys.stderr)))
             print(f"[tune] step {res['_ms'][0]:.4f} -> {res['_ms'][1]:.4f} ms", file=sys.stderr)
     if args.plans_out and rank == 0:
         with open(args.plans_out, "w") as f:
-            json.dump({f"{N}x{K}": mbw.plan_index(step.op, Mb, N, K) for N, K in step.shapes()}, f)
-    plans = {f"{N}x{K}": mbw.plan_describe(step.op, Mb, N, K) for N, K in step.shapes()}
+            json.dump({skey(sh): mbw.plan_index(step.op | sh[0], Mb, sh[1], sh[2]) for sh in step.shapes()}, f)
+    plans = {skey(sh): mbw.plan_describe(step.op | sh[0], Mb, sh[1], sh[2]) for sh in step.shapes()}
     step.run()
     torch.cuda.synchronize()
 
@@ -513,7 +586,7 @@ def main():
 
     # per-shape steady state on the step's own plans: the dominant kernel is
     # the shape with the largest share of the step (launches x time per launch)
-    step_plans = {(N, K): mbw.plan_index(step.op, Mb, N, K) for N, K in step.shapes()}
+    step_plans = {sh: mbw.plan_index(step.op | sh[0], Mb, sh[1], sh[2]) for sh in step.shapes()}
     shape_times = {}
     if rank == 0 and not args.no_shape_timing:
         shape_times = time_per_shape(step, device, shapes=step.shapes(), plans=step_plans)
@@ -526,13 +599,13 @@ def main():
     peak, peak_src = hbm_peak()
     counts = {}
     for m in step.mats:
-        counts[(m.N, m.K)] = counts.get((m.N, m.K), 0) + 1
+        counts[(m.fuse, m.N, m.K)] = counts.get((m.fuse, m.N, m.K), 0) + 1
     dominant = None
     if shape_times:
-        dominant = max(step.shapes(), key=lambda sh: counts[sh] * shape_times[f"{sh[0]}x{sh[1]}"]["us"])
-    family = plans[f"{dominant[0]}x{dominant[1]}"].split(" ")[0] if dominant else "lat"
+        dominant = max(step.shapes(), key=lambda sh: counts[sh] * shape_times[skey(sh)]["us"])
+    family = plans[skey(dominant)].split(" ")[0] if dominant else "lat"
     sha = kernel_source_sha(family)
-    traffic = TRAFFIC.get((sha, f"{dominant[0]}x{dominant[1]}")) if dominant else None
+    traffic = TRAFFIC.get((sha, skey(dominant))) if dominant else None
     clocks = sampler.summary(t0, t1)
     if rank != 0:
         return
@@ -584,12 +657,13 @@ def roofline_fields(step, ms_step, gbs, peak, peak_src, traffic, plans, launches
     if dominant is None:  # not timed (other ranks)
         return {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                 "traffic": traffic, "peak_source": peak_src, "kernel": "step average"}
-    key = f"{dominant[0]}x{dominant[1]}"
+    key = skey(dominant)
     st = shape_times[key]
-    tot = sum(counts[sh] * shape_times[f"{sh[0]}x{sh[1]}"]["us"] for sh in counts)
+    tot = sum(counts[sh] * shape_times[skey(sh)]["us"] for sh in counts)
     M = step.M
-    kb = wl.bytes_alg(step.fmt, M, *dominant)
-    kfl = wl.flops(M, *dominant)
+    dm = wl.Mat(key, dominant[1], dominant[2], dominant[0])
+    kb = wl.call_bytes(step.fmt, M, dm)
+    kfl = wl.call_flops(M, dm)
     achieved = kb / (st["us"] * 1e-6) / 1e9
     r = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
          "traffic": traffic, "peak_source": peak_src,
@@ -617,12 +691,12 @@ def named_shapes(fmt):
     """The shapes the per-matrix figures are quoted on, besides the step's own:
     tinyinfer's four TinyLlama INT4 matrices, and the 2048x2048 BF16 GEMV."""
     if fmt == wl.FMT_INT4_G64:
-        return [(m.N, m.K) for m in wl.TINYLLAMA_TABLE_SHAPES]
+        return [(0, m.N, m.K) for m in wl.TINYLLAMA_TABLE_SHAPES]
     if fmt == wl.FMT_INT4_AWQ_G128:
-        return [(m.N, m.K) for m in wl.SKINNY_SHAPES]
+        return [(0, m.N, m.K) for m in wl.SKINNY_SHAPES]
     if fmt == wl.FMT_INT8_PC:
         return []
-    return [(2048, 2048)]
+    return [(0, 2048, 2048)]
 
 
 def time_per_shape(step, device, reps=5, shapes=None, plans=None):
@@ -640,8 +714,8 @@ def time_per_shape(step, device, reps=5, shapes=None, plans=None):
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     shapes = sorted(set(step.shapes()) | set(named_shapes(step.fmt))) if shapes is None else list(shapes)
     M = step.M
-    for N, K in shapes:
-        b = wl.bytes_alg(step.fmt, M, N, K)
+    for fz, N, K in shapes:
+        b = wl.call_bytes(step.fmt, M, wl.Mat("", N, K, fz))
         copies = int(min(512, max(8, -(-4 * l2 // b))))
         x = torch.empty((copies, M, K), dtype=torch.bfloat16, device=device)
         y = torch.empty((copies, M, N), dtype=torch.bfloat16, device=device)
@@ -649,11 +723,11 @@ def time_per_shape(step, device, reps=5, shapes=None, plans=None):
         calls = []
         for i in range(copies):
             xi, yi = (x[i, 0], y[i, 0]) if M == 1 else (x[i], y[i])
-            calls.append(device_call(step.fmt, 0, 1000 + i, N, K, xi, yi, device))
-        if plans is not None and (N, K) in plans:
-            mbw.plan_select(step.op, M, N, K, plans[(N, K)])
+            calls.append(device_call(step.fmt, 0, 1000 + i, N, K, xi, yi, device, fz, M))
+        if plans is not None and (fz, N, K) in plans:
+            mbw.plan_select(step.op | fz, M, N, K, plans[(fz, N, K)])
         else:
-            mbw.autotune(step.op, M, N, K)
+            mbw.autotune(step.op | fz, M, N, K)
         for fn, a, o in calls:
             fn(*a, out=o)
         torch.cuda.synchronize()
@@ -675,9 +749,9 @@ def time_per_shape(step, device, reps=5, shapes=None, plans=None):
             torch.cuda.synchronize()
             ts.append(e0.elapsed_time(e1) / copies)
         us = statistics.median(ts) * 1e3
-        out[f"{N}x{K}"] = {"us": us, "GB/s": b / (us * 1e-6) / 1e9, "frac": b / (us * 1e-6) / 1e9 / peak,
-                           "TFLOP/s": wl.flops(M, N, K) / (us * 1e-6) / 1e12,
-                           "copies": copies, "plan": mbw.plan_describe(step.op, M, N, K)}
+        out[skey((fz, N, K))] = {"us": us, "GB/s": b / (us * 1e-6) / 1e9, "frac": b / (us * 1e-6) / 1e9 / peak,
+                                 "TFLOP/s": wl.call_flops(M, wl.Mat("", N, K, fz)) / (us * 1e-6) / 1e12,
+                                 "copies": copies, "plan": mbw.plan_describe(step.op | fz, M, N, K)}
         del calls, g
         torch.cuda.empty_cache()
     return out

@@ -175,24 +175,34 @@ __device__ __forceinline__ void store_out(void* y, int64_t idx, float v, int out
 }
 
 // ------------------------------------------------------------- fusions ----
+// The helpers below take FZ = 1 in the kernels instantiated for fused calls;
+// with FZ = 0 every fusion branch compiles away.
+//
 // Which matrix and physical 16-row tile a logical tile t reads: under the
 // gated epilogue logical tiles alternate between W (gate) and W2 (up).
+template <int FZ>
+__device__ __forceinline__ bool gated(const GemvArgs& a) { return FZ && a.glu; }
+template <int FZ>
 __device__ __forceinline__ const uint8_t* tile_weights(const GemvArgs& a, int t) {
-    return (a.glu && (t & 1)) ? a.W2 : a.W;
+    return (gated<FZ>(a) && (t & 1)) ? a.W2 : a.W;
 }
-__device__ __forceinline__ int tile_row0(const GemvArgs& a, int t) { return (a.glu ? (t >> 1) : t) * 16; }
+template <int FZ>
+__device__ __forceinline__ int tile_row0(const GemvArgs& a, int t) { return (gated<FZ>(a) ? (t >> 1) : t) * 16; }
+template <int FZ>
 __device__ __forceinline__ const uint16_t* tile_scales(const GemvArgs& a, int t) {
-    return (a.glu && (t & 1)) ? a.scales2 : a.scales;
+    return (gated<FZ>(a) && (t & 1)) ? a.scales2 : a.scales;
 }
+template <int FZ>
 __device__ __forceinline__ const float* tile_rscale(const GemvArgs& a, int t) {
-    return (a.glu && (t & 1)) ? a.rscale2 : a.rscale;
+    return (gated<FZ>(a) && (t & 1)) ? a.rscale2 : a.rscale;
 }
 
 // The CTA's logical tile range [t0, t0 + nt) of row-group `cg` of `G`: whole
 // output tiles, and whole gate/up pairs under the gated epilogue.
+template <int FZ>
 __device__ __forceinline__ void cta_tile_range(const GemvArgs& a, int G, int cg, int& t0, int& nt) {
     const int T = (a.N + 15) / 16;
-    const int f = a.glu ? 2 : 1;
+    const int f = gated<FZ>(a) ? 2 : 1;
     const int p0 = (int)(((long long)T * cg) / G);
     const int p1 = (int)(((long long)T * (cg + 1)) / G);
     t0 = p0 * f;
@@ -253,10 +263,11 @@ __device__ __forceinline__ float silu_f32(float v) { return v / (1.0f + expf(-v)
 // v is the sum of W's row, v2 that of W2's row under the gated epilogue;
 // SwiGLU (yalm sec. 3.3, TileInfer: SwiGLU in the GEMV epilogue), then the
 // residual add (yalm: fused matmul + add_residuals), then the bf16 store.
+template <int FZ>
 __device__ __forceinline__ void store_fused(const GemvArgs& a, int m, int row, float v, float v2) {
-    if (a.glu) v = silu_f32(v) * v2;
+    if (gated<FZ>(a)) v = silu_f32(v) * v2;
     const int64_t idx = (int64_t)m * a.N + row;
-    if (a.residual) v += bf16lo_to_f32(a.residual[idx]);
+    if (FZ && a.residual) v += bf16lo_to_f32(a.residual[idx]);
     store_out(a.y, idx, v, a.out_f32);
 }
 

@@ -122,11 +122,12 @@ __host__ __device__ inline size_t lat_sc_floats(int fmt, int ntmax) { return fmt
 __host__ __device__ inline size_t lat_norm_off(int ntmax, int W, int WK, int M, int xsb, size_t scf) {
     return lat_red_floats(ntmax, WK, M) + (size_t)W * 72 * 4 * xsb + scf;
 }
-__host__ __device__ inline size_t lat_smem_floats(int ntmax, int W, int WK, int M, int xsb, size_t scf) {
-    return lat_norm_off(ntmax, W, WK, M, xsb, scf) + kLatNormFloats;
+// (`fz`: the instantiation is the fused one, which alone has the norm area)
+__host__ __device__ inline size_t lat_smem_floats(int ntmax, int W, int WK, int M, int xsb, size_t scf, int fz) {
+    return lat_norm_off(ntmax, W, WK, M, xsb, scf) + (fz ? kLatNormFloats : 0);
 }
-__host__ __device__ inline size_t lat_ring_off(int ntmax, int W, int WK, int M, int xsb, size_t scf) {
-    return (lat_smem_floats(ntmax, W, WK, M, xsb, scf) * 4 + 127) / 128 * 128;
+__host__ __device__ inline size_t lat_ring_off(int ntmax, int W, int WK, int M, int xsb, size_t scf, int fz) {
+    return (lat_smem_floats(ntmax, W, WK, M, xsb, scf, fz) * 4 + 127) / 128 * 128;
 }
 
 // W warps = WK along K x WT along the CTA's row tiles. Warp (wk, wt) owns
@@ -136,7 +137,9 @@ __host__ __device__ inline size_t lat_ring_off(int ntmax, int W, int WK, int M, 
 // INT4 unpack and MMAs stream one 32-bit word at a time from the ring, with
 // x read from the slot per word, so a warp needs few registers and 16 warps
 // fit beside the next launch.
-template <int FMT, int W, int WT, int NI, int NPRE, int STG, int LEAN>
+// FZ: 1 in the twin instantiated for fused calls (RMSNorm prologue, gated
+// and residual epilogues); 0 compiles the fusions out.
+template <int FMT, int W, int WT, int NI, int NPRE, int STG, int LEAN, int FZ>
 __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     gemv_lat_kernel(const GemvArgs a, const int S) {
     static_assert(FMT == FMT_G64 || FMT == FMT_BF16 || FMT == FMT_I8, "INT4 group-64, INT8 and BF16 only");
@@ -158,8 +161,8 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     const int G = gridDim.x / S;
     const int cgid = blockIdx.x / S;
     int t0, nt;  // the CTA's logical tiles (gate/up pairs under the gated epilogue)
-    cta_tile_range(a, G, cgid, t0, nt);
-    const int ntmax = ((a.N + 15) / 16 + G - 1) / G * (a.glu ? 2 : 1);
+    cta_tile_range<FZ>(a, G, cgid, t0, nt);
+    const int ntmax = ((a.N + 15) / 16 + G - 1) / G * (gated<FZ>(a) ? 2 : 1);
     const int mb = a.M;
     const int KB = a.K / BK;  // the plan guarantees K % BK == 0
     const int BS = (KB + S * WK - 1) / (S * WK);
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     // chunk c at c * 512 + L * 16, filled by sector-complete copies).
     u32x8 ra[NI], rb[NI];  // 32 bytes of rows g and g+8 per register-held item
     uint32_t rs[NI][2];    // group-64: the 2 fp16 scales of this lane's columns, rows g and g+8
-    uint8_t* ringw = reinterpret_cast<uint8_t*>(lat_smem) + lat_ring_off(ntmax, W, WK, mb, xsb, scf) +
+    uint8_t* ringw = reinterpret_cast<uint8_t*>(lat_smem) + lat_ring_off(ntmax, W, WK, mb, xsb, scf, FZ) +
                      (size_t)warp * NI * 2048;
     uint8_t* ring = ringw + lane * 16;
 #pragma unroll
@@ -187,8 +190,8 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
             const int tt = j / nb;
             const int b = b0 + (j - tt * nb);
             const int tile = t0 + wt + tt * WT;
-            const uint8_t* Wt = tile_weights(a, tile);
-            const int trow = tile_row0(a, tile);
+            const uint8_t* Wt = tile_weights<FZ>(a, tile);
+            const int trow = tile_row0<FZ>(a, tile);
             const int r0 = min(trow + g, a.N - 1);
             const int r1 = min(trow + g + 8, a.N - 1);
             const uint8_t* p0 = Wt + (size_t)r0 * rowbytes + (size_t)b * 128 + q * 32;
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
                                    (size_t)b * 128 + ring_copy_byte(lane));
             }
             if (FMT == FMT_G64) {
-                const uint16_t* st = tile_scales(a, tile);
+                const uint16_t* st = tile_scales<FZ>(a, tile);
                 const uint16_t* s0 = st + (size_t)r0 * a.groups + (size_t)b * 4 + 2 * (q & 1);
                 const uint16_t* s1 = st + (size_t)r1 * a.groups + (size_t)b * 4 + 2 * (q & 1);
                 rs[j][0] = (uint32_t)ld_ro_u16(s0) | ((uint32_t)ld_ro_u16(s0 + 1) << 16);
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     if (FMT == FMT_I8)
         for (int i = threadIdx.x; i < nt * 16; i += W * 32) {
             const int tl = t0 + (i >> 4);
-            rsc[i] = __ldg(tile_rscale(a, tl) + min(tile_row0(a, tl) + (i & 15), a.N - 1));
+            rsc[i] = __ldg(tile_rscale<FZ>(a, tl) + min(tile_row0<FZ>(a, tl) + (i & 15), a.N - 1));
         }
 
     // Addresses of the x words this lane reads after the wait: word i of the
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     uint4* xslot = reinterpret_cast<uint4*>(lat_smem + lat_red_floats(ntmax, WK, mb)) + (size_t)warp * (72 * xsb);
     // RMSNorm prologue: the CTA's factor per batch row
     float* nscr = lat_smem + lat_norm_off(ntmax, W, WK, mb, xsb, scf);
-    if (a.norm_w) norm_factors(a, nscr, W * 32);
+    if (FZ && a.norm_w) norm_factors(a, nscr, W * 32);
     {
         uint4 v[XLD];
 #pragma unroll
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
 #pragma unroll
         for (int r = 0; r < XLD; ++r) {
             const int wi = lane + 32 * r;
-            if (wi < nxw && a.norm_w) {
+            if (FZ && wi < nxw && a.norm_w) {
                 const int sb = wi / sbw, rem = wi - sb * sbw;
                 const int m = rem / XWSB, w = rem - m * XWSB;
                 v[r] = norm_word(v[r], nscr[W * mb + m], a.norm_w + (size_t)(b0 + sb) * BK + w * 8);
@@ -471,9 +474,9 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
     // each output: the sum over the K-warps in order. Local logical row lr
     // (tile lr / 16) of batch row m; under the gated epilogue output row o
     // pairs gate row gate_row(o) with up row gate_row(o) + 16.
-    const int nto = a.glu ? nt / 2 : nt;
-    const int orow0 = (a.glu ? t0 / 2 : t0) * 16;
-    auto gate_row = [&](int o) { return a.glu ? (o >> 4) * 32 + (o & 15) : o; };
+    const int nto = gated<FZ>(a) ? nt / 2 : nt;
+    const int orow0 = (gated<FZ>(a) ? t0 / 2 : t0) * 16;
+    auto gate_row = [&](int o) { return gated<FZ>(a) ? (o >> 4) * 32 + (o & 15) : o; };
     auto wsum = [&](int lr, int m) -> float {
         const float* rp = red + ((size_t)(lr >> 4) * WK * 16 + (lr & 15)) * mb + m;
         float v = 0.f;
@@ -489,11 +492,11 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
             const int lr = gate_row(o);
             float v = wsum(lr, m), v2 = 0.f;
             if (FMT == FMT_I8) v *= rsc[lr];
-            if (a.glu) {
+            if (gated<FZ>(a)) {
                 v2 = wsum(lr + 16, m);
                 if (FMT == FMT_I8) v2 *= rsc[lr + 16];
             }
-            store_fused(a, m, orow0 + o, v, v2);
+            store_fused<FZ>(a, m, orow0 + o, v, v2);
         }
         return;
     }
@@ -512,11 +515,11 @@ __global__ void __launch_bounds__(W * 32, (16 / W) > 2 ? (16 / W) : 2)
         float v = 0.f, v2 = 0.f;
         for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(fin + lr * mb + m, s);
         if (FMT == FMT_I8) v *= rsc[lr];
-        if (a.glu) {
+        if (gated<FZ>(a)) {
             for (int s = 0; s < S; ++s) v2 += *cluster.map_shared_rank(fin + (lr + 16) * mb + m, s);
             if (FMT == FMT_I8) v2 *= rsc[lr + 16];
         }
-        if (orow0 + o < a.N) store_fused(a, m, orow0 + o, v, v2);
+        if (orow0 + o < a.N) store_fused<FZ>(a, m, orow0 + o, v, v2);
     }
     cluster.sync();
 }
@@ -526,10 +529,11 @@ namespace {
 using LatFn = void (*)(const GemvArgs, const int);
 struct LatEntry {
     LatConfig cfg;
-    LatFn fn;
+    LatFn fn;   // plain calls
+    LatFn fnf;  // fused calls (the FZ = 1 twin)
 };
 #define MBW_L(F, W, WT, NI, NP, ST, LN) \
-    { {W, WT, NI, NP, ST, LN}, gemv_lat_kernel<F, W, WT, NI, NP, ST, LN> }
+    { {W, WT, NI, NP, ST, LN}, gemv_lat_kernel<F, W, WT, NI, NP, ST, LN, 0>, gemv_lat_kernel<F, W, WT, NI, NP, ST, LN, 1> }
 const LatEntry kLatG64[] = {
     MBW_L(FMT_G64, 8, 1, 1, 1, 0, 0), MBW_L(FMT_G64, 8, 1, 1, 0, 0, 0), MBW_L(FMT_G64, 8, 1, 2, 0, 0, 0),
     MBW_L(FMT_G64, 8, 1, 3, 0, 0, 0), MBW_L(FMT_G64, 4, 1, 1, 1, 0, 0), MBW_L(FMT_G64, 8, 1, 2, 1, 1, 0),
@@ -592,7 +596,7 @@ int lat_items_per_warp(int fmt, const LatConfig& c, int64_t N, int64_t K, int sp
     return (int)((ntmax + c.wt - 1) / c.wt * BS);
 }
 
-size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu) {
+size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu, int fz) {
     const int G = mma_row_groups(N, split, occ);
     const int64_t T = (N + 15) / 16;
     const int ntmax = (int)((T + G - 1) / G) * (glu ? 2 : 1);
@@ -601,8 +605,8 @@ size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, 
     const int64_t BS = (KB + (int64_t)split * WK - 1) / ((int64_t)split * WK);
     const int xsb = (int)std::min<int64_t>(c.ni, BS);
     const size_t scf = lat_sc_floats(fmt, ntmax);
-    if (c.staged) return lat_ring_off(ntmax, c.warps, WK, M, xsb, scf) + (size_t)c.warps * c.ni * 2048;
-    return lat_smem_floats(ntmax, c.warps, WK, M, xsb, scf) * sizeof(float);
+    if (c.staged) return lat_ring_off(ntmax, c.warps, WK, M, xsb, scf, fz) + (size_t)c.warps * c.ni * 2048;
+    return lat_smem_floats(ntmax, c.warps, WK, M, xsb, scf, fz) * sizeof(float);
 }
 
 cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
@@ -613,9 +617,11 @@ cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStrea
     const int items = lat_items_per_warp(fmt, e.cfg, a.N, a.K, p.split, p.occ, a.glu);
     if (items < 1 || items > e.cfg.ni) return cudaErrorInvalidValue;
     const int G = mma_row_groups(a.N, p.split, p.occ);
-    const size_t smem = lat_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ, a.glu);
+    const int fz = gemv_fused_args(a);
+    const size_t smem = lat_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ, a.glu, fz);
+    const LatFn fn = fz ? e.fnf : e.fn;
     if (smem > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
     }
     cudaLaunchConfig_t cfg = {};
@@ -638,7 +644,7 @@ cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStrea
     cfg.attrs = attrs;
     cfg.numAttrs = na;
     count_launch();
-    return cudaLaunchKernelEx(&cfg, e.fn, a, p.split);
+    return cudaLaunchKernelEx(&cfg, fn, a, p.split);
 }
 
 }  // namespace mbw

@@ -387,7 +387,9 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
 //              and g+8); every code of a row shares the row's fp32 scale,
 //              which multiplies the row's finished sum in the store (TileInfer,
 //              "Pushing further with cheating: INT8 quantization").
-template <int FMT, int W, int U, int ASYNC>
+// FZ: 1 in the twin instantiated for fused calls (RMSNorm prologue, gated
+// and residual epilogues); 0 compiles the fusions out.
+template <int FMT, int W, int U, int ASYNC, int FZ>
 __global__ void __launch_bounds__(W * 32, 16 / W)
     gemv_mma2_kernel(const GemvArgs a, const int S) {
     constexpr int BK = (FMT == FMT_BF16) ? 64 : (FMT == FMT_I8) ? 128 : 256;  // k per 128-byte row super-block
@@ -402,9 +404,9 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     const int G = gridDim.x / S;
     const int cgid = blockIdx.x / S;
     int t0, nt;  // the CTA's logical tiles (gate/up pairs under the gated epilogue)
-    cta_tile_range(a, G, cgid, t0, nt);
+    cta_tile_range<FZ>(a, G, cgid, t0, nt);
     const int mb = a.M;
-    const MmaSmem L = mma_smem_layout(BK, a.K, a.N, mb, W, S, G, a.glu);
+    const MmaSmem L = mma_smem_layout(BK, a.K, a.N, mb, W, S, G, gated<FZ>(a) ? 1 : 0);
 
     const int KB = a.K / BK;  // the plan guarantees K % BK == 0
     const int BS = (KB + S * W - 1) / (S * W);
@@ -425,9 +427,9 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     const uint8_t* ap[4] = {nullptr, nullptr, nullptr, nullptr};  // ASYNC: sources of this lane's 4 copies
     auto set_rows = [&](int t) {
         const int tl = t0 + t;
-        const uint8_t* Wt = tile_weights(a, tl);
-        const uint16_t* St = tile_scales(a, tl);
-        const int trow = tile_row0(a, tl);
+        const uint8_t* Wt = tile_weights<FZ>(a, tl);
+        const uint16_t* St = tile_scales<FZ>(a, tl);
+        const int trow = tile_row0<FZ>(a, tl);
         const int r0 = min(trow + g, a.N - 1);
         const int r1 = min(trow + g + 8, a.N - 1);
         if (ASYNC) {
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     if (FMT == FMT_I8)
         for (int i = threadIdx.x; i < nt * 16; i += W * 32) {
             const int tl = t0 + (i >> 4);
-            rsc[i] = __ldg(tile_rscale(a, tl) + min(tile_row0(a, tl) + (i & 15), a.N - 1));
+            rsc[i] = __ldg(tile_rscale<FZ>(a, tl) + min(tile_row0<FZ>(a, tl) + (i & 15), a.N - 1));
         }
 
     prefetch_l2_grid_share(a.x, (size_t)a.M * a.K * 2);
@@ -514,7 +516,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
 
     // RMSNorm prologue: factor per batch row into the (still unused) partial-sum area
     float* nscr = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.red_off);
-    if (a.norm_w) norm_factors(a, nscr, W * 32);
+    if (FZ && a.norm_w) norm_factors(a, nscr, W * 32);
 
     uint4* xs = smem_u4;
     const int cwords = max(0, min(KB, cb0 + W * BS) - cb0) * XW;
@@ -525,7 +527,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
             const int wi = i - m * L.xwords;
             if (wi < cwords) {
                 v = ld_ro16(a.x + (size_t)m * a.K + (size_t)cb0 * BK + (size_t)wi * 8);
-                if (a.norm_w) v = norm_word(v, nscr[W * mb + m], a.norm_w + (size_t)cb0 * BK + (size_t)wi * 8);
+                if (FZ && a.norm_w) v = norm_word(v, nscr[W * mb + m], a.norm_w + (size_t)cb0 * BK + (size_t)wi * 8);
             }
             if (FMT == FMT_I8)
                 v = perm_i8(v);
@@ -703,9 +705,9 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     }
     // output row o of the CTA; under the gated epilogue it pairs gate row
     // gate_row(o) with up row gate_row(o) + 16 (local logical rows)
-    const int nto = a.glu ? nt / 2 : nt;
-    const int orow0 = (a.glu ? t0 / 2 : t0) * 16;
-    auto gate_row = [&](int o) { return a.glu ? (o >> 4) * 32 + (o & 15) : o; };
+    const int nto = gated<FZ>(a) ? nt / 2 : nt;
+    const int orow0 = (gated<FZ>(a) ? t0 / 2 : t0) * 16;
+    auto gate_row = [&](int o) { return gated<FZ>(a) ? (o >> 4) * 32 + (o & 15) : o; };
     if (S == 1) {
         __syncthreads();
         for (int i = threadIdx.x; i < nto * 16 * mb; i += W * 32) {
@@ -714,11 +716,11 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
             const int lr = gate_row(o);
             float v = fin[lr * mb + m], v2 = 0.f;
             if (FMT == FMT_I8) v *= rsc[lr];
-            if (a.glu) {
+            if (gated<FZ>(a)) {
                 v2 = fin[(lr + 16) * mb + m];
                 if (FMT == FMT_I8) v2 *= rsc[lr + 16];
             }
-            store_fused(a, m, orow0 + o, v, v2);
+            store_fused<FZ>(a, m, orow0 + o, v, v2);
         }
         return;
     }
@@ -734,11 +736,11 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
         float v = 0.f, v2 = 0.f;
         for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(fin + lr * mb + m, s);
         if (FMT == FMT_I8) v *= rsc[lr];
-        if (a.glu) {
+        if (gated<FZ>(a)) {
             for (int s = 0; s < S; ++s) v2 += *cluster.map_shared_rank(fin + (lr + 16) * mb + m, s);
             if (FMT == FMT_I8) v2 *= rsc[lr + 16];
         }
-        if (orow0 + o < a.N) store_fused(a, m, orow0 + o, v, v2);
+        if (orow0 + o < a.N) store_fused<FZ>(a, m, orow0 + o, v, v2);
     }
     cluster.sync();
 }
@@ -747,10 +749,11 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
 using MmaFn = void (*)(const GemvArgs, const int);
 struct MmaEntry {
     MmaConfig cfg;
-    MmaFn fn;
+    MmaFn fn;   // plain calls
+    MmaFn fnf;  // fused calls (mma2 FZ = 1 twin; null where the format has no fused path)
 };
 #define MBW_M(F, W, U) \
-    { {W, U, 0}, gemv_mma_kernel<F, W, U> }
+    { {W, U, 0}, gemv_mma_kernel<F, W, U>, nullptr }
 
 static const MmaEntry kMmaBf16[] = {
     MBW_M(FMT_BF16, 4, 4), MBW_M(FMT_BF16, 4, 8), MBW_M(FMT_BF16, 8, 4), MBW_M(FMT_BF16, 8, 8),
@@ -764,17 +767,20 @@ static const MmaEntry kMmaAwq[] = {
 #undef MBW_M
 
 #define MBW_M2(F, W, U, A) \
-    { {W, U, A}, gemv_mma2_kernel<F, W, U, A> }
+    { {W, U, A}, gemv_mma2_kernel<F, W, U, A, 0>, gemv_mma2_kernel<F, W, U, A, 1> }
+#define MBW_M2P(F, W, U, A) \
+    { {W, U, A}, gemv_mma2_kernel<F, W, U, A, 0>, nullptr }
 static const MmaEntry kMma2Bf16[] = {MBW_M2(FMT_BF16, 8, 2, 0), MBW_M2(FMT_BF16, 8, 4, 0), MBW_M2(FMT_BF16, 4, 4, 0),
                                      MBW_M2(FMT_BF16, 8, 4, 1), MBW_M2(FMT_BF16, 8, 6, 1)};
 static const MmaEntry kMma2G64[] = {MBW_M2(FMT_G64, 8, 2, 0), MBW_M2(FMT_G64, 8, 3, 0), MBW_M2(FMT_G64, 4, 2, 0),
                                     MBW_M2(FMT_G64, 4, 3, 0), MBW_M2(FMT_G64, 8, 4, 1), MBW_M2(FMT_G64, 8, 6, 1),
                                     MBW_M2(FMT_G64, 4, 6, 1)};
-static const MmaEntry kMma2Awq[] = {MBW_M2(FMT_AWQ, 8, 2, 0), MBW_M2(FMT_AWQ, 8, 3, 0), MBW_M2(FMT_AWQ, 4, 2, 0),
-                                    MBW_M2(FMT_AWQ, 8, 4, 1), MBW_M2(FMT_AWQ, 8, 6, 1)};
+static const MmaEntry kMma2Awq[] = {MBW_M2P(FMT_AWQ, 8, 2, 0), MBW_M2P(FMT_AWQ, 8, 3, 0), MBW_M2P(FMT_AWQ, 4, 2, 0),
+                                    MBW_M2P(FMT_AWQ, 8, 4, 1), MBW_M2P(FMT_AWQ, 8, 6, 1)};
 static const MmaEntry kMma2I8[] = {MBW_M2(FMT_I8, 8, 2, 0), MBW_M2(FMT_I8, 8, 3, 0), MBW_M2(FMT_I8, 4, 3, 0),
                                    MBW_M2(FMT_I8, 8, 4, 1), MBW_M2(FMT_I8, 8, 6, 1), MBW_M2(FMT_I8, 4, 8, 1)};
 #undef MBW_M2
+#undef MBW_M2P
 
 static const MmaEntry* mma2_table(int fmt, int* n) {
     switch (fmt) {
@@ -823,10 +829,12 @@ cudaError_t launch_gemv_mma2(int fmt, const Plan& p, const GemvArgs& a, cudaStre
     const MmaEntry* t = mma2_table(fmt, &n);
     if (t == nullptr || p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > mma2_max_batch(fmt)) return cudaErrorInvalidValue;
     const MmaEntry& e = t[p.cfg];
+    const MmaFn fn = gemv_fused_args(a) ? e.fnf : e.fn;
+    if (fn == nullptr) return cudaErrorInvalidValue;
     const int G = mma_row_groups(a.N, p.split, p.occ);
     const size_t smem = mma2_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ, a.glu);
     if (smem > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
     }
     cudaLaunchConfig_t cfg = {};
@@ -849,7 +857,7 @@ cudaError_t launch_gemv_mma2(int fmt, const Plan& p, const GemvArgs& a, cudaStre
     cfg.attrs = attrs;
     cfg.numAttrs = na;
     count_launch();
-    return cudaLaunchKernelEx(&cfg, e.fn, a, p.split);
+    return cudaLaunchKernelEx(&cfg, fn, a, p.split);
 }
 
 static const MmaEntry* mma_table(int fmt, int* n) {

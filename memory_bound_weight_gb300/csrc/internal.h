@@ -42,6 +42,8 @@ struct GemvArgs {
 
 // Logical 16-row tiles of a launch (twice the output tiles under the gated epilogue).
 inline int64_t gemv_tiles(int64_t N, int glu) { return (N + 15) / 16 * (glu ? 2 : 1); }
+// 1 if the launch uses a fusion (it then runs the kernels' FZ = 1 instantiations).
+inline int gemv_fused_args(const GemvArgs& a) { return (a.glu || a.norm_w || a.residual) ? 1 : 0; }
 
 // One instantiation of the CUDA-core streaming kernel.
 struct SimtConfig {
@@ -112,7 +114,8 @@ LatConfig lat_config(int fmt, int idx);
 int lat_max_batch(int fmt);
 int lat_block_k(int fmt);
 int lat_items_per_warp(int fmt, const LatConfig& c, int64_t N, int64_t K, int split, int occ, int glu = 0);
-size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu = 0);
+size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu = 0,
+                      int fz = 0);
 cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
 
 // tcgen05 skinny GEMM (gemm_tc.cu): Y = X . W^T for the whole batch M.

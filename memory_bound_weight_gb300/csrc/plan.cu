@@ -130,7 +130,7 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K, 
         const int items = lat_items_per_warp(fmt, c, N, K, p.split, p.occ, glu);
         if (items < 1 || items > c.ni) return false;
         if (c.ni > items + 1) return false;  // a smaller instantiation holds this share
-        if (lat_smem_bytes(fmt, c, N, K, mb, p.split, p.occ, glu) > kSmemLimit) return false;
+        if (lat_smem_bytes(fmt, c, N, K, mb, p.split, p.occ, glu, fuse ? 1 : 0) > kSmemLimit) return false;
         return true;
     }
     if (p.kind == PLAN_TMA) {

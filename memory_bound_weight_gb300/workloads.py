@@ -18,12 +18,18 @@ FMT_INT4_G64 = "int4_g64"
 FMT_INT4_AWQ_G128 = "int4_awq_g128"
 FMT_INT8_PC = "int8_pc"
 
+# Fusion bits of a call (the MBW_FUSE_* values of include/mbw.h).
+FUSE_NORM = 0x100      # RMSNorm prologue: reads a bf16 [K] norm weight
+FUSE_GLU = 0x200       # gated SiLU epilogue: streams a second (up) matrix of the same shape
+FUSE_RESIDUAL = 0x400  # residual add: reads a bf16 [M][N] residual
+
 
 @dataclass(frozen=True)
 class Mat:
     name: str
     N: int  # output rows
     K: int  # reduction length
+    fuse: int = 0  # FUSE_* bits of the call that streams it
 
 
 def bits_per_weight(code_bits: int, group: int, scale_bits: int, zero_bits: int) -> float:
@@ -48,6 +54,26 @@ def weight_bytes(fmt: str, N: int, K: int) -> int:
 def bytes_alg(fmt: str, M: int, N: int, K: int) -> int:
     """Algorithmic bytes of one call: weights (+ scales, zeros) + M activation rows (bf16)."""
     return weight_bytes(fmt, N, K) + 2 * M * K
+
+
+def call_weight_bytes(fmt: str, m: Mat) -> int:
+    """Weight bytes one call streams (both matrices of a gated call)."""
+    return weight_bytes(fmt, m.N, m.K) * (2 if m.fuse & FUSE_GLU else 1)
+
+
+def call_bytes(fmt: str, M: int, m: Mat) -> int:
+    """Algorithmic bytes of one call with its fusions: weights, x, and the
+    norm weight and residual it reads."""
+    b = call_weight_bytes(fmt, m) + 2 * M * m.K
+    if m.fuse & FUSE_NORM:
+        b += 2 * m.K
+    if m.fuse & FUSE_RESIDUAL:
+        b += 2 * M * m.N
+    return b
+
+
+def call_flops(M: int, m: Mat) -> int:
+    return flops(M, m.N, m.K) * (2 if m.fuse & FUSE_GLU else 1)
 
 
 def out_bytes(M: int, N: int) -> int:
@@ -75,6 +101,17 @@ TINYLLAMA_LAYER_FUSED = (
     Mat("qkv", 2048 + 256 + 256, 2048), Mat("o", 2048, 2048), Mat("gate_up", 2 * 5632, 2048),
     Mat("down", 2048, 5632),
 )
+
+# The fused-projection layer with the small ops of the layer folded into its
+# GEMVs (NEXT-1, NEXT-4): the attention RMSNorm into q/k/v, the residual adds
+# into o and down, and the MLP RMSNorm plus SwiGLU into the gate/up call, which
+# streams gate and up (5632 rows each) and writes silu(gate) * up. The head
+# takes the final RMSNorm. Same weights and launches as the fused layer.
+TINYLLAMA_LAYER_FUSEDOPS = (
+    Mat("qkv", 2048 + 256 + 256, 2048, FUSE_NORM), Mat("o", 2048, 2048, FUSE_RESIDUAL),
+    Mat("gate_up", 5632, 2048, FUSE_NORM | FUSE_GLU), Mat("down", 2048, 5632, FUSE_RESIDUAL),
+)
+TINYLLAMA_HEAD_NORM = Mat("lm_head", 32000, 2048, FUSE_NORM)
 
 # Qwen2.5-7B: hidden 3584, MLP 18944, 28 layers, 28 query heads and 4 KV heads
 # of 128 dims (Q, K, V concatenated to 4608 rows), vocabulary 152064
@@ -114,12 +151,14 @@ def decode_step(layer, layers: int, head: Mat) -> list[Mat]:
     mats = []
     for li in range(layers):
         for m in layer:
-            mats.append(Mat(f"L{li}.{m.name}", m.N, m.K))
+            mats.append(Mat(f"L{li}.{m.name}", m.N, m.K, m.fuse))
     mats.append(head)
     return mats
 
 
-def tinyllama_step(fused: bool = False) -> list[Mat]:
+def tinyllama_step(fused: bool = False, fusedops: bool = False) -> list[Mat]:
+    if fusedops:
+        return decode_step(TINYLLAMA_LAYER_FUSEDOPS, TINYLLAMA_LAYERS, TINYLLAMA_HEAD_NORM)
     layer = TINYLLAMA_LAYER_FUSED if fused else TINYLLAMA_LAYER
     return decode_step(layer, TINYLLAMA_LAYERS, TINYLLAMA_HEAD)
 
@@ -136,12 +175,13 @@ def step_weight_bytes(mats, fmt: str, head_fmt: str | None = None) -> int:
     total = 0
     for m in mats:
         f = head_fmt if (head_fmt is not None and m.name == "lm_head") else fmt
-        total += weight_bytes(f, m.N, m.K)
+        total += call_weight_bytes(f, m)
     return total
 
 
 def step_bytes_alg(mats, fmt: str, M: int = 1, head_fmt: str | None = None) -> int:
-    return step_weight_bytes(mats, fmt, head_fmt) + sum(2 * M * m.K for m in mats)
+    return step_weight_bytes(mats, fmt, head_fmt) + sum(call_bytes(fmt, M, m) - call_weight_bytes(fmt, m)
+                                                          for m in mats)
 
 
 def step_params(mats) -> int:
