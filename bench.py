@@ -44,13 +44,13 @@ FALLBACK_BF16_TFLOPS = 1752.2  # the pool's measured sustained cuBLAS bf16, reco
 # traffic = null until it is captured again.
 TRAFFIC = {
     # gemv_lat on the fused gate_up matrices (INT4 g64, 11264x2048): ncu --set full,
-    # 2 launches, dram__bytes_read.sum 12,322,048 + dram__bytes_write.sum 0 per launch
+    # 1 launch, dram__bytes_read.sum 12,316,160 + dram__bytes_write.sum 0
     # (profiles/gemv_lat_int4_g64_11264x2048.md)
-    ("65175de089367b3b", "11264x2048"): 12322048,
+    ("a49c5dc3ed8058bf", "11264x2048"): 12316160,
     # gemv_mma2 on the fused gate_up matrices (symmetric INT8, 19456x2560): ncu --set full,
-    # 1 launch, dram__bytes_read.sum 49,944,064 + dram__bytes_write.sum 2,048
+    # 1 launch, dram__bytes_read.sum 49,946,112 + dram__bytes_write.sum 2,304
     # (profiles/gemv_mma2_int8_19456x2560.md)
-    ("7fbf9c1f6e5275d3", "19456x2560"): 49946112,
+    ("762d3f116d2b1194", "19456x2560"): 49948416,
 }
 
 
