@@ -243,22 +243,27 @@ __global__ void __launch_bounds__(192, 1)
             float fs[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) fs[j] = 0.f;
+            // all C accumulators of this 16-column block, then one wait (a wait
+            // per load would put a TMEM round trip per accumulator on the epilogue)
+            uint32_t v[C][16];
 #pragma unroll
             for (int ch = 0; ch < C; ++ch) {
-                uint32_t v[16];
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ch * NTP + c);
                 asm volatile(
                     "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
                     "[%16];"
-                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-                      "=r"(v[15])
+                    : "=r"(v[ch][0]), "=r"(v[ch][1]), "=r"(v[ch][2]), "=r"(v[ch][3]), "=r"(v[ch][4]), "=r"(v[ch][5]),
+                      "=r"(v[ch][6]), "=r"(v[ch][7]), "=r"(v[ch][8]), "=r"(v[ch][9]), "=r"(v[ch][10]),
+                      "=r"(v[ch][11]), "=r"(v[ch][12]), "=r"(v[ch][13]), "=r"(v[ch][14]), "=r"(v[ch][15])
                     : "r"(taddr));
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            }
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int ch = 0; ch < C; ++ch) {
                 // an accumulator no k-step reached holds no data
                 if (ch < nks * 4) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) fs[j] += __uint_as_float(v[j]);
+                    for (int j = 0; j < 16; ++j) fs[j] += __uint_as_float(v[ch][j]);
                 }
             }
 #pragma unroll
@@ -319,6 +324,14 @@ __global__ void __launch_bounds__(192, 1)
 //     shared memory) into one of four TMEM accumulators;
 //   * warps 10..13 (one thread per weight row) read each accumulator back,
 //     multiply by the row's fp32 group scale and accumulate in registers.
+// The thread that issues MMAs is the serial role, and every mbarrier wait or
+// commit costs ~0.1 us there, so it does one commit per group (group done,
+// waited on by both the unpack and the read-back warps) and, when there are
+// as many accumulators as A operands, one wait (A ready): the unpack warps
+// then check that the accumulator is free, in parallel. With fewer
+// accumulators (batch tile 64) that check stays with the MMA thread, so the
+// unpack warps can still run NA groups ahead. The unpack warps wait for a
+// ring slot once per slot.
 // A cluster splits K for short, wide shapes (partials summed through
 // distributed shared memory in rank order). Every wait is bounded; on expiry
 // the kernel records the fault flag and skips the remaining work.
@@ -348,13 +361,17 @@ struct TcAwqLayout {
     static constexpr uint32_t OFF_Q = GS * X_GROUP;   // inside a ring slot
     static constexpr uint32_t SLOT = OFF_Q + 128 * Q_ROW;
     static constexpr uint32_t TX = 128 * Q_ROW + GS * X_GROUP;  // bytes TMA delivers per slot
-    static constexpr int NA = 4;                      // TMEM A operands
+    // The groups in flight (NA A operands, NB accumulator sets) bound the
+    // throughput: each group's unpack -> MMA -> read-back cycle is serial, so
+    // about NA groups complete per round trip. A batch tile of 16 affords a
+    // fifth A operand when its 8 MMAs rotate over 2 accumulators (chains of 4).
+    static constexpr int NA = (NT == 16) ? 5 : 4;     // TMEM A operands
     static constexpr int A_COLS = 64;                 // TMEM columns of one 128-k A operand
     static constexpr int D_COL0 = NA * A_COLS;        // accumulators follow the A operands
     // a group's 8 MMAs rotate over C independent accumulators (one chain of
     // dependent MMAs runs at the MMA latency); NB groups in flight
-    static constexpr int C = (NT == 16) ? 4 : 2;
-    static constexpr int NB = (NT == 64) ? 2 : 4;
+    static constexpr int C = 2;
+    static constexpr int NB = (NT == 64) ? 2 : NA;
     static constexpr int TMEM_COLS = 512;
     static_assert(D_COL0 + NB * C * NT <= TMEM_COLS, "");
 };
@@ -384,10 +401,10 @@ __global__ void __launch_bounds__(448, 1)
     uint64_t* qfull = reinterpret_cast<uint64_t*>(ring + (size_t)D * L::SLOT);
     uint64_t* empty = qfull + D;
     uint64_t* aready = empty + D;
-    uint64_t* afree = aready + NA;
-    uint64_t* dfull = afree + NA;
-    uint64_t* dempty = dfull + NB;
+    uint64_t* mdone = aready + NA;  // [NA]: group i's MMAs are done (i % NA); frees its A operand and fills its accumulator
+    uint64_t* dempty = mdone + NA;
     uint64_t* done = dempty + NB;
+    static_assert(NB <= NA, "a group's accumulator is reused no sooner than its A operand");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     // this CTA's scales (fp16) and zero points (one byte each) of its rows and
     // groups, loaded once: a per-group global load would put an L2 round trip
@@ -402,12 +419,10 @@ __global__ void __launch_bounds__(448, 1)
         }
         for (int b = 0; b < NA; ++b) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(tc_smem(&aready[b])));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&afree[b])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&mdone[b])));
         }
-        for (int b = 0; b < NB; ++b) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&dfull[b])));
+        for (int b = 0; b < NB; ++b)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(tc_smem(&dempty[b])));
-        }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(done)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -484,7 +499,8 @@ __global__ void __launch_bounds__(448, 1)
             for (int i = 0; i < nks; ++i) {
                 const int j = i / GS, s = j % D, g = i - j * GS, b = i % NB, ab = i % NA;
                 if (ok) ok = tc_wait(&aready[ab], (i / NA) & 1);
-                if (ok && i >= NB) ok = tc_wait(&dempty[b], ((i / NB) - 1) & 1);
+                // accumulator b free; with NB == NA the unpack warps checked it before aready
+                if (NB < NA && ok && i >= NB) ok = tc_wait(&dempty[b], ((i / NB) - 1) & 1);
                 if (ok) {
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     const uint32_t ta = tmem + (uint32_t)(ab * L::A_COLS);
@@ -508,15 +524,12 @@ __global__ void __launch_bounds__(448, 1)
                     }
                 }
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                 tc_smem(&dfull[b]))
+                                 tc_smem(&mdone[ab]))
                              : "memory");
                 if (g == GS - 1 || i == nks - 1)
                     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                                      tc_smem(&empty[s]))
                                  : "memory");
-                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                 tc_smem(&afree[ab]))
-                             : "memory");
             }
             // every MMA issued above has completed before TMEM is released
             asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -531,10 +544,13 @@ __global__ void __launch_bounds__(448, 1)
         const int quarter = warp & 3;       // TMEM lanes 32*quarter .. +31 (the warp's accessible quarter)
         const int r = quarter * 32 + lane;  // weight row of the tile
         for (int i = 0; i < nks; ++i) {
-            const int j = i / GS, s = j % D, g = i - j * GS, ab = i % NA;
+            const int j = i / GS, s = j % D, g = i - j * GS, ab = i % NA, b = i % NB;
             const uint32_t zc = z_tab[i * 128 + r];
-            ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&qfull[s], (j / D) & 1));
-            if (i >= NA) ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&afree[ab], ((i / NA) - 1) & 1));
+            if (g == 0) ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&qfull[s], (j / D) & 1));  // once per slot
+            // A operand ab free: group i - NA's MMAs are done
+            if (i >= NA) ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&mdone[ab], ((i / NA) - 1) & 1));
+            // accumulator b free: group i - NB has been read back (checked here, in parallel, for the MMA thread)
+            if (NB == NA && i >= NB) ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&dempty[b], ((i / NB) - 1) & 1));
             // all lanes take part in the (warp-collective) TMEM store
             uint8_t* st = ring + (size_t)s * L::SLOT;
             uint32_t av[32];
@@ -584,27 +600,37 @@ __global__ void __launch_bounds__(448, 1)
         for (int j = 0; j < nks; ++j) {
             const int b = j % NB;
             const float sc = f16_bits_to_f32(s_tab[j * 128 + r]);
-            ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&dfull[b], (j / NB) & 1));
+            ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&mdone[j % NA], (j / NA) & 1));
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            // Issue the TMEM loads of up to 64 columns (all C accumulators of CB
+            // 8-column blocks) before one wait: a wait after every load puts a
+            // TMEM round trip per block on this role's per-group time.
+            constexpr int CB = (64 / (8 * L::C)) < (NT / 8) ? (64 / (8 * L::C)) : (NT / 8);
 #pragma unroll
-            for (int cc = 0; cc < NT; cc += 8) {
-                float gsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int cc0 = 0; cc0 < NT; cc0 += 8 * CB) {
+                uint32_t v[CB][L::C][8];
 #pragma unroll
-                for (int ch = 0; ch < L::C; ++ch) {
-                    uint32_t v[8];
-                    const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) +
-                                           (uint32_t)(L::D_COL0 + (b * L::C + ch) * NT + cc);
-                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-                                   "=r"(v[7])
-                                 : "r"(taddr));
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                for (int cb = 0; cb < CB; ++cb)
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) gsum[jj] += __uint_as_float(v[jj]);
-                }
-                // the group's partial sum, scaled once by the row's group scale
+                    for (int ch = 0; ch < L::C; ++ch) {
+                        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) +
+                                               (uint32_t)(L::D_COL0 + (b * L::C + ch) * NT + cc0 + 8 * cb);
+                        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                                     : "=r"(v[cb][ch][0]), "=r"(v[cb][ch][1]), "=r"(v[cb][ch][2]), "=r"(v[cb][ch][3]),
+                                       "=r"(v[cb][ch][4]), "=r"(v[cb][ch][5]), "=r"(v[cb][ch][6]), "=r"(v[cb][ch][7])
+                                     : "r"(taddr));
+                    }
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) acc[cc + jj] = fmaf(sc, gsum[jj], acc[cc + jj]);
+                for (int cb = 0; cb < CB; ++cb)
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        float gsum = 0.f;
+#pragma unroll
+                        for (int ch = 0; ch < L::C; ++ch) gsum += __uint_as_float(v[cb][ch][jj]);
+                        // the group's partial sum, scaled once by the row's group scale
+                        acc[cc0 + 8 * cb + jj] = fmaf(sc, gsum, acc[cc0 + 8 * cb + jj]);
+                    }
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
