@@ -361,17 +361,20 @@ struct TcAwqLayout {
     static constexpr uint32_t OFF_Q = GS * X_GROUP;   // inside a ring slot
     static constexpr uint32_t SLOT = OFF_Q + 128 * Q_ROW;
     static constexpr uint32_t TX = 128 * Q_ROW + GS * X_GROUP;  // bytes TMA delivers per slot
-    // The groups in flight (NA A operands, NB accumulator sets) bound the
-    // throughput: each group's unpack -> MMA -> read-back cycle is serial, so
-    // about NA groups complete per round trip. A batch tile of 16 affords a
-    // fifth A operand when its 8 MMAs rotate over 2 accumulators (chains of 4).
-    static constexpr int NA = (NT == 16) ? 5 : 4;     // TMEM A operands
+    // Every step of a role (a barrier wait, a fence, an arrive, a commit)
+    // costs ~0.1-0.25 us whatever the work behind it, so the roles hand over
+    // GP groups per stage: one wait, commit and arrive per stage. Each group
+    // keeps its own accumulators (its scale differs).
+    static constexpr int GP = (NT == 64) ? 1 : 2;     // groups per stage
+    static constexpr int NA = 4;                      // TMEM A operands (groups)
     static constexpr int A_COLS = 64;                 // TMEM columns of one 128-k A operand
     static constexpr int D_COL0 = NA * A_COLS;        // accumulators follow the A operands
     // a group's 8 MMAs rotate over C independent accumulators (one chain of
-    // dependent MMAs runs at the MMA latency); NB groups in flight
+    // dependent MMAs runs at the MMA latency); NB groups' accumulators in flight
     static constexpr int C = 2;
-    static constexpr int NB = (NT == 64) ? 2 : NA;
+    static constexpr int NB = (NT == 64) ? 2 : 4;
+    static constexpr int NAS = NA / GP, NBS = NB / GP;  // stages in flight
+    static_assert(NA % GP == 0 && NB % GP == 0 && GS % GP == 0, "");
     static constexpr int TMEM_COLS = 512;
     static_assert(D_COL0 + NB * C * NT <= TMEM_COLS, "");
 };
@@ -396,15 +399,16 @@ __global__ void __launch_bounds__(448, 1)
     const int ks0 = rank * a.kstages;
     const int nks = max(0, min(a.G, ks0 + a.kstages) - ks0);
 
-    constexpr int GS = L::GS, NA = L::NA;
+    constexpr int GS = L::GS, GP = L::GP, NAS = L::NAS, NBS = L::NBS;
+    const int nst = (nks + GP - 1) / GP;  // stages of GP groups
     uint8_t* ring = smem;
     uint64_t* qfull = reinterpret_cast<uint64_t*>(ring + (size_t)D * L::SLOT);
     uint64_t* empty = qfull + D;
-    uint64_t* aready = empty + D;
-    uint64_t* mdone = aready + NA;  // [NA]: group i's MMAs are done (i % NA); frees its A operand and fills its accumulator
-    uint64_t* dempty = mdone + NA;
-    uint64_t* done = dempty + NB;
-    static_assert(NB <= NA, "a group's accumulator is reused no sooner than its A operand");
+    uint64_t* aready = empty + D;   // [NAS]: stage p's A operands are in TMEM (p % NAS)
+    uint64_t* mdone = aready + NAS;  // [NAS]: stage p's MMAs are done: frees its A operands, fills its accumulators
+    uint64_t* dempty = mdone + NAS;  // [NBS]: stage p's accumulators have been read back (p % NBS)
+    uint64_t* done = dempty + NBS;
+    static_assert(NBS <= NAS, "a stage's accumulators are reused no sooner than its A operands");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     // this CTA's scales (fp16) and zero points (one byte each) of its rows and
     // groups, loaded once: a per-group global load would put an L2 round trip
@@ -417,11 +421,11 @@ __global__ void __launch_bounds__(448, 1)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&qfull[s])));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&empty[s])));
         }
-        for (int b = 0; b < NA; ++b) {
+        for (int b = 0; b < NAS; ++b) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(tc_smem(&aready[b])));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&mdone[b])));
         }
-        for (int b = 0; b < NB; ++b)
+        for (int b = 0; b < NBS; ++b)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(tc_smem(&dempty[b])));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(done)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -496,39 +500,48 @@ __global__ void __launch_bounds__(448, 1)
         // --------------------------------------------------- MMA issuer ----
         if (lane == 0) {
             const uint32_t idesc = tc_idesc(128, NT);
-            for (int i = 0; i < nks; ++i) {
-                const int j = i / GS, s = j % D, g = i - j * GS, b = i % NB, ab = i % NA;
-                if (ok) ok = tc_wait(&aready[ab], (i / NA) & 1);
-                // accumulator b free; with NB == NA the unpack warps checked it before aready
-                if (NB < NA && ok && i >= NB) ok = tc_wait(&dempty[b], ((i / NB) - 1) & 1);
+            for (int p = 0; p < nst; ++p) {
+                const int pa = p % NAS, pb = p % NBS;
+                if (ok) ok = tc_wait(&aready[pa], (p / NAS) & 1);
+                // accumulators free; with NBS == NAS the unpack warps checked them before aready
+                if (NBS < NAS && ok && p >= NBS) ok = tc_wait(&dempty[pb], ((p / NBS) - 1) & 1);
                 if (ok) {
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint32_t ta = tmem + (uint32_t)(ab * L::A_COLS);
-                    const uint32_t sx = tc_smem(ring + (size_t)s * L::SLOT + g * L::X_GROUP);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint64_t db = tc_desc(sx + h * L::X_HALF);
+                    for (int gg = 0; gg < GP; ++gg) {
+                        const int i = p * GP + gg;
+                        if (i >= nks) break;
+                        const int j = i / GS, s = j % D, g = i - j * GS;
+                        const uint32_t ta = tmem + (uint32_t)((pa * GP + gg) * L::A_COLS);
+                        const uint32_t dcol = (uint32_t)(L::D_COL0 + (pb * GP + gg) * L::C * NT);
+                        const uint32_t sx = tc_smem(ring + (size_t)s * L::SLOT + g * L::X_GROUP);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int kk = h * 4 + k;  // k-step of the group; accumulator kk % C
-                            const uint32_t accf = (kk >= L::C) ? 1u : 0u;
-                            // A: 8 TMEM columns per 16 k; X: +32 bytes per 16 k inside the swizzle atom
-                            asm volatile(
-                                "{\n\t.reg .pred p;\n\t"
-                                "setp.ne.b32 p, %4, 0;\n\t"
-                                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
-                                    tmem + (uint32_t)(L::D_COL0 + (b * L::C + kk % L::C) * NT)),
-                                "r"(ta + (uint32_t)((h * 4 + k) * 8)), "l"(db + 2 * k), "r"(idesc), "r"(accf)
-                                : "memory");
+                        for (int h = 0; h < 2; ++h) {
+                            const uint64_t db = tc_desc(sx + h * L::X_HALF);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const int kk = h * 4 + k;  // k-step of the group; accumulator kk % C
+                                const uint32_t accf = (kk >= L::C) ? 1u : 0u;
+                                // A: 8 TMEM columns per 16 k; X: +32 bytes per 16 k inside the swizzle atom
+                                asm volatile(
+                                    "{\n\t.reg .pred p;\n\t"
+                                    "setp.ne.b32 p, %4, 0;\n\t"
+                                    "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+                                        tmem + dcol + (uint32_t)((kk % L::C) * NT)),
+                                    "r"(ta + (uint32_t)(kk * 8)), "l"(db + 2 * k), "r"(idesc), "r"(accf)
+                                    : "memory");
+                            }
                         }
                     }
                 }
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                 tc_smem(&mdone[ab]))
+                                 tc_smem(&mdone[pa]))
                              : "memory");
-                if (g == GS - 1 || i == nks - 1)
+                // ring slot free once the stage holding its last group is done
+                const int il = min(nks, (p + 1) * GP) - 1, jl = il / GS;
+                if (il - jl * GS == GS - 1 || il == nks - 1)
                     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                     tc_smem(&empty[s]))
+                                     tc_smem(&empty[jl % D]))
                                  : "memory");
             }
             // every MMA issued above has completed before TMEM is released
@@ -543,98 +556,115 @@ __global__ void __launch_bounds__(448, 1)
         const int h = cw >> 2;              // k-half of the group this warp unpacks
         const int quarter = warp & 3;       // TMEM lanes 32*quarter .. +31 (the warp's accessible quarter)
         const int r = quarter * 32 + lane;  // weight row of the tile
-        for (int i = 0; i < nks; ++i) {
-            const int j = i / GS, s = j % D, g = i - j * GS, ab = i % NA, b = i % NB;
-            const uint32_t zc = z_tab[i * 128 + r];
-            if (g == 0) ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&qfull[s], (j / D) & 1));  // once per slot
-            // A operand ab free: group i - NA's MMAs are done
-            if (i >= NA) ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&mdone[ab], ((i / NA) - 1) & 1));
-            // accumulator b free: group i - NB has been read back (checked here, in parallel, for the MMA thread)
-            if (NB == NA && i >= NB) ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&dempty[b], ((i / NB) - 1) & 1));
-            // all lanes take part in the (warp-collective) TMEM store
-            uint8_t* st = ring + (size_t)s * L::SLOT;
-            uint32_t av[32];
-            {
-                // row r of box g/2; 16-byte chunk c of the row sits at chunk c ^ (r & 7)
-                const uint8_t* qrow = st + L::OFF_Q + (g >> 1) * L::Q_BOX + r * 128;
-                const int c0 = (g & 1) * 4 + h * 2;
-                uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
-                if (ok) {
-                    q0 = *reinterpret_cast<const uint4*>(qrow + ((c0 ^ (r & 7)) << 4));
-                    q1 = *reinterpret_cast<const uint4*>(qrow + (((c0 + 1) ^ (r & 7)) << 4));
-                }
-                const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                const uint32_t zz = (0x4300u | zc) * 0x00010001u;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    av[4 * c + 0] = tc_sub(tc_nib(wv[c]), zz);
-                    av[4 * c + 1] = tc_sub(tc_nib(wv[c] >> 4), zz);
-                    av[4 * c + 2] = tc_sub(tc_nib(wv[c] >> 8), zz);
-                    av[4 * c + 3] = tc_sub(tc_nib(wv[c] >> 12), zz);
-                }
+        for (int p = 0; p < nst; ++p) {
+            const int pa = p % NAS, pb = p % NBS;
+            const int i0 = p * GP, j = i0 / GS, s = j % D;
+            if (i0 % GS == 0) ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&qfull[s], (j / D) & 1));  // once per slot
+            if (NBS == NAS) {
+                // accumulators free (stage p - NBS read back, which also means its MMAs, the users of
+                // these A operands, are done): checked here, in parallel, for the MMA thread
+                if (p >= NBS) ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&dempty[pb], ((p / NBS) - 1) & 1));
+            } else if (p >= NAS) {
+                // A operands free: stage p - NAS's MMAs are done
+                ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&mdone[pa], ((p / NAS) - 1) & 1));
             }
-            const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * L::A_COLS + h * 32);
-            asm volatile(
-                "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-                "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(ta),
-                "r"(av[0]), "r"(av[1]), "r"(av[2]), "r"(av[3]), "r"(av[4]), "r"(av[5]), "r"(av[6]), "r"(av[7]),
-                "r"(av[8]), "r"(av[9]), "r"(av[10]), "r"(av[11]), "r"(av[12]), "r"(av[13]), "r"(av[14]),
-                "r"(av[15]), "r"(av[16]), "r"(av[17]), "r"(av[18]), "r"(av[19]), "r"(av[20]), "r"(av[21]),
-                "r"(av[22]), "r"(av[23]), "r"(av[24]), "r"(av[25]), "r"(av[26]), "r"(av[27]), "r"(av[28]),
-                "r"(av[29]), "r"(av[30]), "r"(av[31])
-                : "memory");
-            if (ok) {
-                uint4* xs = reinterpret_cast<uint4*>(st + g * L::X_GROUP);
-                for (int c = cw * 32 + lane; c < NT * 16; c += 256) xs[c] = tc_perm(xs[c]);
+            // all lanes take part in the (warp-collective) TMEM stores
+            uint8_t* st = ring + (size_t)s * L::SLOT;
+#pragma unroll
+            for (int gg = 0; gg < GP; ++gg) {
+                const int i = i0 + gg;
+                if (i >= nks) break;
+                const int g = i - j * GS;
+                const uint32_t zc = z_tab[i * 128 + r];
+                uint32_t av[32];
+                {
+                    // row r of box g/2; 16-byte chunk c of the row sits at chunk c ^ (r & 7)
+                    const uint8_t* qrow = st + L::OFF_Q + (g >> 1) * L::Q_BOX + r * 128;
+                    const int c0 = (g & 1) * 4 + h * 2;
+                    uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
+                    if (ok) {
+                        q0 = *reinterpret_cast<const uint4*>(qrow + ((c0 ^ (r & 7)) << 4));
+                        q1 = *reinterpret_cast<const uint4*>(qrow + (((c0 + 1) ^ (r & 7)) << 4));
+                    }
+                    const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    const uint32_t zz = (0x4300u | zc) * 0x00010001u;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        av[4 * c + 0] = tc_sub(tc_nib(wv[c]), zz);
+                        av[4 * c + 1] = tc_sub(tc_nib(wv[c] >> 4), zz);
+                        av[4 * c + 2] = tc_sub(tc_nib(wv[c] >> 8), zz);
+                        av[4 * c + 3] = tc_sub(tc_nib(wv[c] >> 12), zz);
+                    }
+                }
+                const uint32_t ta =
+                    tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((pa * GP + gg) * L::A_COLS + h * 32);
+                asm volatile(
+                    "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                    "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(ta),
+                    "r"(av[0]), "r"(av[1]), "r"(av[2]), "r"(av[3]), "r"(av[4]), "r"(av[5]), "r"(av[6]), "r"(av[7]),
+                    "r"(av[8]), "r"(av[9]), "r"(av[10]), "r"(av[11]), "r"(av[12]), "r"(av[13]), "r"(av[14]),
+                    "r"(av[15]), "r"(av[16]), "r"(av[17]), "r"(av[18]), "r"(av[19]), "r"(av[20]), "r"(av[21]),
+                    "r"(av[22]), "r"(av[23]), "r"(av[24]), "r"(av[25]), "r"(av[26]), "r"(av[27]), "r"(av[28]),
+                    "r"(av[29]), "r"(av[30]), "r"(av[31])
+                    : "memory");
+                if (ok) {
+                    uint4* xs = reinterpret_cast<uint4*>(st + g * L::X_GROUP);
+                    for (int c = cw * 32 + lane; c < NT * 16; c += 256) xs[c] = tc_perm(xs[c]);
+                }
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
-            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc_smem(&aready[ab])) : "memory");
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc_smem(&aready[pa])) : "memory");
         }
     } else {
         // ---------------------------------------------------- read back ----
         const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
         const int r = quarter * 32 + lane;     // weight row of the tile
-        for (int j = 0; j < nks; ++j) {
-            const int b = j % NB;
-            const float sc = f16_bits_to_f32(s_tab[j * 128 + r]);
-            ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&mdone[j % NA], (j / NA) & 1));
+        for (int p = 0; p < nst; ++p) {
+            const int pa = p % NAS, pb = p % NBS;
+            ok = __all_sync(0xFFFFFFFFu, ok && tc_wait(&mdone[pa], (p / NAS) & 1));
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            // Issue the TMEM loads of up to 64 columns (all C accumulators of CB
-            // 8-column blocks) before one wait: a wait after every load puts a
-            // TMEM round trip per block on this role's per-group time.
-            constexpr int CB = (64 / (8 * L::C)) < (NT / 8) ? (64 / (8 * L::C)) : (NT / 8);
 #pragma unroll
-            for (int cc0 = 0; cc0 < NT; cc0 += 8 * CB) {
-                uint32_t v[CB][L::C][8];
+            for (int gg = 0; gg < GP; ++gg) {
+                const int i = p * GP + gg;
+                if (i >= nks) break;
+                const float sc = f16_bits_to_f32(s_tab[i * 128 + r]);
+                // Issue the TMEM loads of up to 64 columns (all C accumulators of CB
+                // 8-column blocks) before one wait: a wait after every load puts a
+                // TMEM round trip per block on this role's per-group time.
+                constexpr int CB = (64 / (8 * L::C)) < (NT / 8) ? (64 / (8 * L::C)) : (NT / 8);
 #pragma unroll
-                for (int cb = 0; cb < CB; ++cb)
+                for (int cc0 = 0; cc0 < NT; cc0 += 8 * CB) {
+                    uint32_t v[CB][L::C][8];
 #pragma unroll
-                    for (int ch = 0; ch < L::C; ++ch) {
-                        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) +
-                                               (uint32_t)(L::D_COL0 + (b * L::C + ch) * NT + cc0 + 8 * cb);
-                        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                                     : "=r"(v[cb][ch][0]), "=r"(v[cb][ch][1]), "=r"(v[cb][ch][2]), "=r"(v[cb][ch][3]),
-                                       "=r"(v[cb][ch][4]), "=r"(v[cb][ch][5]), "=r"(v[cb][ch][6]), "=r"(v[cb][ch][7])
-                                     : "r"(taddr));
-                    }
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    for (int cb = 0; cb < CB; ++cb)
 #pragma unroll
-                for (int cb = 0; cb < CB; ++cb)
+                        for (int ch = 0; ch < L::C; ++ch) {
+                            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) +
+                                                   (uint32_t)(L::D_COL0 + ((pb * GP + gg) * L::C + ch) * NT + cc0 + 8 * cb);
+                            asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                                         : "=r"(v[cb][ch][0]), "=r"(v[cb][ch][1]), "=r"(v[cb][ch][2]), "=r"(v[cb][ch][3]),
+                                           "=r"(v[cb][ch][4]), "=r"(v[cb][ch][5]), "=r"(v[cb][ch][6]), "=r"(v[cb][ch][7])
+                                         : "r"(taddr));
+                        }
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        float gsum = 0.f;
+                    for (int cb = 0; cb < CB; ++cb)
 #pragma unroll
-                        for (int ch = 0; ch < L::C; ++ch) gsum += __uint_as_float(v[cb][ch][jj]);
-                        // the group's partial sum, scaled once by the row's group scale
-                        acc[cc0 + 8 * cb + jj] = fmaf(sc, gsum, acc[cc0 + 8 * cb + jj]);
-                    }
+                        for (int jj = 0; jj < 8; ++jj) {
+                            float gsum = 0.f;
+#pragma unroll
+                            for (int ch = 0; ch < L::C; ++ch) gsum += __uint_as_float(v[cb][ch][jj]);
+                            // the group's partial sum, scaled once by the row's group scale
+                            acc[cc0 + 8 * cb + jj] = fmaf(sc, gsum, acc[cc0 + 8 * cb + jj]);
+                        }
+                }
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
-            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc_smem(&dempty[b])) : "memory");
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc_smem(&dempty[pb])) : "memory");
         }
         if (S == 1) {
             // rows are the fast index of the stores: a warp writes 32 consecutive outputs per batch row
