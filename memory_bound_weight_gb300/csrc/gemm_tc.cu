@@ -119,16 +119,20 @@ __device__ __forceinline__ uint4 tc_perm(uint4 v) {
 // accumulators the k-steps rotate over -- consecutive MMAs into one
 // accumulator wait for each other, so a single chain runs at the MMA latency
 // instead of the tensor pipe's rate; the epilogue adds the C partial sums.
-template <int NT, int C>
+// BPS: 64-k boxes per ring stage. Every barrier step costs ~0.1-0.25 us in
+// the thread that issues MMAs whatever the work behind it, so two boxes per
+// stage (one wait and one commit per 8 MMAs) stream closer to the HBM rate at
+// small batch; a one-box stage keeps more stages in a small ring.
+template <int NT, int C, int BPS>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX,
                    const TcArgs a, const int S, const int D) {
     constexpr int NTP = NT <= 32 ? 32 : NT <= 64 ? 64 : NT <= 128 ? 128 : 256;  // columns per accumulator
     constexpr int TMEM_COLS = NTP * C;
     static_assert(TMEM_COLS <= 512, "");
-    constexpr uint32_t A_BYTES = 128 * 128;   // 128 rows x 64 bf16
-    constexpr uint32_t B_BYTES = NT * 128;    // NT rows x 64 bf16
-    constexpr uint32_t STAGE = A_BYTES + B_BYTES;
+    constexpr uint32_t A_BYTES = 128 * 128;   // 128 rows x 64 bf16 (one box)
+    constexpr uint32_t B_BYTES = NT * 128;    // NT rows x 64 bf16 (one box)
+    constexpr uint32_t STAGE = BPS * (A_BYTES + B_BYTES);  // W boxes, then X boxes
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -140,7 +144,7 @@ __global__ void __launch_bounds__(192, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x / S;
     const int row0 = tile * 128;
-    const int KS = (a.K + 63) / 64;
+    const int KS = (a.K + 64 * BPS - 1) / (64 * BPS);  // stages (boxes past K read zeros)
     const int ks0 = rank * a.kstages;
     const int nks = max(0, min(KS, ks0 + a.kstages) - ks0);
 
@@ -178,11 +182,15 @@ __global__ void __launch_bounds__(192, 1)
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc_smem(&full[i])),
                              "r"(STAGE)
                              : "memory");
-                tc_tma_2d(smem + (size_t)i * STAGE, &mapW, (ks0 + i) * 64, row0, &full[i]);
+                for (int bb = 0; bb < BPS; ++bb)
+                    tc_tma_2d(smem + (size_t)i * STAGE + bb * A_BYTES, &mapW, ((ks0 + i) * BPS + bb) * 64, row0,
+                              &full[i]);
             }
             pdl_wait();
             for (int i = 0; i < npre; ++i)
-                tc_tma_2d(smem + (size_t)i * STAGE + A_BYTES, &mapX, (ks0 + i) * 64, a.m0, &full[i]);
+                for (int bb = 0; bb < BPS; ++bb)
+                    tc_tma_2d(smem + (size_t)i * STAGE + BPS * A_BYTES + bb * B_BYTES, &mapX,
+                              ((ks0 + i) * BPS + bb) * 64, a.m0, &full[i]);
             for (int i = npre; i < nks; ++i) {
                 const int s = i % D;
                 if (!tc_wait(&empty[s], ((i / D) - 1) & 1)) break;
@@ -190,9 +198,11 @@ __global__ void __launch_bounds__(192, 1)
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc_smem(&full[s])),
                              "r"(STAGE)
                              : "memory");
-                const int kc = (ks0 + i) * 64;
-                tc_tma_2d(st, &mapW, kc, row0, &full[s]);
-                tc_tma_2d(st + A_BYTES, &mapX, kc, a.m0, &full[s]);
+                for (int bb = 0; bb < BPS; ++bb) {
+                    const int kc = ((ks0 + i) * BPS + bb) * 64;
+                    tc_tma_2d(st + bb * A_BYTES, &mapW, kc, row0, &full[s]);
+                    tc_tma_2d(st + BPS * A_BYTES + bb * B_BYTES, &mapX, kc, a.m0, &full[s]);
+                }
             }
         }
     } else if (warp == 1) {
@@ -206,19 +216,22 @@ __global__ void __launch_bounds__(192, 1)
                 if (ok) {
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     const uint32_t sa = tc_smem(smem + (size_t)s * STAGE);
-                    const uint64_t da = tc_desc(sa), db = tc_desc(sa + A_BYTES);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int t = i * 4 + k;  // k-step; accumulator t % C
-                        const uint32_t acc = (t >= C) ? 1u : 0u;
-                        // advance 16 k (32 bytes) inside the swizzle atom: +2 in the address field
-                        asm volatile(
-                            "{\n\t.reg .pred p;\n\t"
-                            "setp.ne.b32 p, %4, 0;\n\t"
-                            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
-                                tmem + (uint32_t)((t % C) * NTP)),
-                            "l"(da + 2 * k), "l"(db + 2 * k), "r"(idesc), "r"(acc)
-                            : "memory");
+                    for (int bb = 0; bb < BPS; ++bb) {
+                        const uint64_t da = tc_desc(sa + bb * A_BYTES), db = tc_desc(sa + BPS * A_BYTES + bb * B_BYTES);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int t = (i * BPS + bb) * 4 + k;  // k-step; accumulator t % C
+                            const uint32_t acc = (t >= C) ? 1u : 0u;
+                            // advance 16 k (32 bytes) inside the swizzle atom: +2 in the address field
+                            asm volatile(
+                                "{\n\t.reg .pred p;\n\t"
+                                "setp.ne.b32 p, %4, 0;\n\t"
+                                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+                                    tmem + (uint32_t)((t % C) * NTP)),
+                                "l"(da + 2 * k), "l"(db + 2 * k), "r"(idesc), "r"(acc)
+                                : "memory");
+                        }
                     }
                 }
                 // release the stage once these MMAs have read it (also on error, so the producer can finish)
@@ -261,7 +274,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int ch = 0; ch < C; ++ch) {
                 // an accumulator no k-step reached holds no data
-                if (ch < nks * 4) {
+                if (ch < nks * 4 * BPS) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) fs[j] += __uint_as_float(v[ch][j]);
                 }
@@ -758,29 +771,29 @@ int tc_batch_tile(int64_t M) {
 // Ring depth for a shared-memory budget: ring 0 = deep (one CTA per SM),
 // ring 1 = about 100 KB, so that the next launch's CTA fits beside this one
 // and streams its first W tiles while this one finishes.
-static int tc_stages(int nt, int ring) {
-    const size_t stage = 128 * 128 + (size_t)nt * 128;
+static int tc_stages(int nt, int ring, int bps) {
+    const size_t stage = (128 * 128 + (size_t)nt * 128) * bps;
     int d = (int)(((ring == 0 ? 180 : 96) * 1024) / stage);
     if (d > 8) d = 8;
     if (d < 2) d = 2;
     return d;
 }
 
-size_t tc_smem_bytes(int nt, int D, int split) {
-    const size_t stage = 128 * 128 + (size_t)nt * 128;
+size_t tc_smem_bytes(int nt, int D, int split, int bps) {
+    const size_t stage = (128 * 128 + (size_t)nt * 128) * bps;
     size_t ring = (size_t)D * stage;
     const size_t part = (size_t)nt * 128 * 4;
     if (split > 1 && part > ring) ring = part;
     return 1024 + ring + (size_t)(2 * D + 1) * 8 + 16;
 }
 
-template <int NT, int C>
+template <int NT, int C, int BPS>
 static cudaError_t launch_nt(const CUtensorMap& mw, const CUtensorMap& mx, const TcArgs& a, int split, int ring,
                              int tiles, cudaStream_t s) {
-    const int D = tc_stages(NT, ring);
-    const size_t smem = tc_smem_bytes(NT, D, split);
+    const int D = tc_stages(NT, ring, BPS);
+    const size_t smem = tc_smem_bytes(NT, D, split, BPS);
     cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel<NT, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(gemm_tc_kernel<NT, C, BPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(tiles * split), 1, 1);
@@ -802,18 +815,20 @@ static cudaError_t launch_nt(const CUtensorMap& mw, const CUtensorMap& mx, const
     cfg.attrs = attrs;
     cfg.numAttrs = na;
     count_launch();
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NT, C>, mw, mx, a, split, D);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NT, C, BPS>, mw, mx, a, split, D);
 }
 
 // Y[M][N] = X[M][K] . W[N][K]^T, bf16, in batch slices of up to 256 rows.
+// cfg bit 0: ring (0 deep, 1 co-resident); bit 1: two 64-k boxes per stage.
 cudaError_t launch_gemm_tc(const uint16_t* X, const uint16_t* W, void* Y, int64_t M, int64_t N, int64_t K, int split,
-                           int ring, int out_f32, cudaStream_t s) {
+                           int cfg_, int out_f32, cudaStream_t s) {
+    const int ring = cfg_ & 1, bps = (cfg_ & 2) ? 2 : 1;
     const int nt = tc_batch_tile(M);
     CUtensorMap mw, mx;
     if (!encode_2d(&mw, W, (uint64_t)K, (uint64_t)N, 64, 128)) return cudaErrorInvalidValue;
     if (!encode_2d(&mx, X, (uint64_t)K, (uint64_t)M, 64, (uint32_t)nt)) return cudaErrorInvalidValue;
     const int tiles = (int)((N + 127) / 128);
-    const int KS = (int)((K + 63) / 64);
+    const int KS = (int)((K + 64 * bps - 1) / (64 * bps));
     if (split < 1) split = 1;
     if (split > KS) split = KS;
     TcArgs a;
@@ -828,18 +843,21 @@ cudaError_t launch_gemm_tc(const uint16_t* X, const uint16_t* W, void* Y, int64_
         a.xpf = X + m0 * K;
         a.xpf_bytes = (size_t)((M - m0 < 256) ? (M - m0) : 256) * (size_t)K * 2;
         cudaError_t e;
+        // accumulator chains: all of TMEM with one CTA per SM (deep ring),
+        // half of it when the next launch's CTA shares the SM
+#define MBW_TC(NT_, C0, C1)                                                                              \
+    e = ring == 0 ? (bps == 2 ? launch_nt<NT_, C0, 2>(mw, mx, a, split, ring, tiles, s)                  \
+                              : launch_nt<NT_, C0, 1>(mw, mx, a, split, ring, tiles, s))                 \
+                  : (bps == 2 ? launch_nt<NT_, C1, 2>(mw, mx, a, split, ring, tiles, s)                  \
+                              : launch_nt<NT_, C1, 1>(mw, mx, a, split, ring, tiles, s))
         switch (nt) {
-            // accumulator chains: all of TMEM with one CTA per SM (deep ring),
-            // half of it when the next launch's CTA shares the SM
-            case 16: e = launch_nt<16, 4>(mw, mx, a, split, ring, tiles, s); break;
-            case 32: e = launch_nt<32, 4>(mw, mx, a, split, ring, tiles, s); break;
-            case 64: e = ring == 0 ? launch_nt<64, 4>(mw, mx, a, split, ring, tiles, s)
-                                   : launch_nt<64, 2>(mw, mx, a, split, ring, tiles, s); break;
-            case 128: e = ring == 0 ? launch_nt<128, 4>(mw, mx, a, split, ring, tiles, s)
-                                    : launch_nt<128, 2>(mw, mx, a, split, ring, tiles, s); break;
-            default: e = ring == 0 ? launch_nt<256, 2>(mw, mx, a, split, ring, tiles, s)
-                                   : launch_nt<256, 1>(mw, mx, a, split, ring, tiles, s); break;
+            case 16: MBW_TC(16, 4, 4); break;
+            case 32: MBW_TC(32, 4, 4); break;
+            case 64: MBW_TC(64, 4, 2); break;
+            case 128: MBW_TC(128, 4, 2); break;
+            default: MBW_TC(256, 2, 1); break;
         }
+#undef MBW_TC
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

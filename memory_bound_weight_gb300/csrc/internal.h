@@ -119,8 +119,9 @@ size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, 
 cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
 
 // tcgen05 skinny GEMM (gemm_tc.cu): Y = X . W^T for the whole batch M.
+// cfg bit 0: ring (0 deep, 1 co-resident); bit 1: two 64-k boxes per stage
 cudaError_t launch_gemm_tc(const uint16_t* X, const uint16_t* W, void* Y, int64_t M, int64_t N, int64_t K, int split,
-                           int ring, int out_f32, cudaStream_t s);
+                           int cfg, int out_f32, cudaStream_t s);
 int tc_batch_tile(int64_t M);
 // tcgen05 AWQ-style INT4 batched GEMM (gemm_tc.cu): whole batch M, slices of 64.
 cudaError_t launch_gemm_tc_awq(const uint8_t* Q, const uint16_t* scales, const uint8_t* zeros, const uint16_t* X,

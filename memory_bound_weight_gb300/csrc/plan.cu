@@ -85,8 +85,10 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K, 
             const int64_t per = ((G + p.split - 1) / p.split + 3) / 4 * 4;  // whole 4-group ring slots per rank
             return per * (p.split - 1) < G && tc_awq_fits(M, K, p.split);
         }
-        const int64_t KS = (K + 63) / 64;
-        if (fmt != FMT_BF16 || M <= 8 || p.cfg < 0 || p.cfg > 1 || p.occ != 1) return false;
+        // cfg bit 0: ring (deep / co-resident), bit 1: two 64-k boxes per stage
+        if (fmt != FMT_BF16 || M <= 8 || p.cfg < 0 || p.cfg > 3 || p.occ != 1) return false;
+        const int64_t bk = (p.cfg & 2) ? 128 : 64;
+        const int64_t KS = (K + bk - 1) / bk;
         if (p.split > KS) return false;
         const int64_t per = (KS + p.split - 1) / p.split;
         return per * (p.split - 1) < KS;  // every cluster rank gets k-stages
@@ -157,9 +159,9 @@ static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
             if (plan_valid(fmt, p, M, N, K, fuse)) out.push_back(p);
         }
     if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 8)
-        for (int ring = 0; ring <= 1; ++ring)
+        for (int cfg = 0; cfg <= 3; ++cfg)
             for (int sp = 1; sp <= 8; ++sp) {
-                Plan p{PLAN_TC, ring, sp, 1};
+                Plan p{PLAN_TC, cfg, sp, 1};
                 if (plan_valid(fmt, p, M, N, K, fuse)) out.push_back(p);
             }
     const int splits[4] = {1, 2, 4, 8};
@@ -277,8 +279,8 @@ std::string plan_to_string(int op, const Plan& p) {
         if (fmt == FMT_AWQ)
             snprintf(buf, sizeof(buf), "tcgen05 fmt=%s tile=128xbatch k_stage=128 (one group) split_k=%d", fs, p.split);
         else
-            snprintf(buf, sizeof(buf), "tcgen05 fmt=%s tile=128xbatch k_stage=64 ring=%s split_k=%d", fs,
-                     p.cfg == 0 ? "deep" : "shared_sm", p.split);
+            snprintf(buf, sizeof(buf), "tcgen05 fmt=%s tile=128xbatch k_stage=%d ring=%s split_k=%d", fs,
+                     (p.cfg & 2) ? 128 : 64, (p.cfg & 1) ? "shared_sm" : "deep", p.split);
     } else if (p.kind == PLAN_LAT) {
         const LatConfig c = lat_config(fmt, p.cfg);
         snprintf(buf, sizeof(buf),
