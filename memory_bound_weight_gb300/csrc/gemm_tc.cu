@@ -378,14 +378,15 @@ struct TcAwqLayout {
     // costs ~0.1-0.25 us whatever the work behind it, so the roles hand over
     // GP groups per stage: one wait, commit and arrive per stage. Each group
     // keeps its own accumulators (its scale differs).
-    static constexpr int GP = (NT == 64) ? 1 : 2;     // groups per stage
+    static constexpr int GP = 2;                      // groups per stage
     static constexpr int NA = 4;                      // TMEM A operands (groups)
     static constexpr int A_COLS = 64;                 // TMEM columns of one 128-k A operand
     static constexpr int D_COL0 = NA * A_COLS;        // accumulators follow the A operands
     // a group's 8 MMAs rotate over C independent accumulators (one chain of
-    // dependent MMAs runs at the MMA latency); NB groups' accumulators in flight
-    static constexpr int C = 2;
-    static constexpr int NB = (NT == 64) ? 2 : 4;
+    // dependent MMAs runs at the MMA latency; the stage's two groups are two
+    // chains more); NB groups' accumulators in flight
+    static constexpr int C = (NT == 64) ? 1 : 2;
+    static constexpr int NB = 4;
     static constexpr int NAS = NA / GP, NBS = NB / GP;  // stages in flight
     static_assert(NA % GP == 0 && NB % GP == 0 && GS % GP == 0, "");
     static constexpr int TMEM_COLS = 512;
