@@ -10,8 +10,9 @@
 // K-major), so Y^T[128 x n] accumulates in TMEM (lane = weight row, column =
 // batch row).
 //
-// CTA = 6 warps: warp 0 issues TMA loads (one elected thread), warp 1 owns
-// TMEM and issues tcgen05.mma (one elected thread), warps 2..5 are the
+// CTA = 6 warps: warp 0 issues TMA loads and warp 1 owns TMEM and issues
+// tcgen05.mma (each runs its loop on the whole warp and issues from one
+// elected lane), warps 2..5 are the
 // epilogue (TMEM -> registers -> bf16 -> global, coalesced along weight rows).
 // Stages of 64 k (128-byte rows, 128-byte swizzle) flow through a ring of
 // mbarriers: full[s] completes when both TMA loads of stage s landed;
@@ -68,6 +69,21 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity) {
     return false;
 }
 
+// The roles that issue tcgen05.mma and TMA copies run their loops on the
+// whole warp and issue from one elected lane. With a lone active lane (the
+// rest of the warp parked at a barrier) tcgen05.mma issues ~3x slower, and
+// every later wait of that lane stalls until the MMAs in flight drain.
+__device__ __forceinline__ bool tc_elect() {
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e != 0;
+}
+
+// a bounded wait with one outcome for the whole warp
+__device__ __forceinline__ bool tc_wait_warp(uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xFFFFFFFFu, tc_wait(bar, parity));
+}
+
 __device__ __forceinline__ void tc_tma_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
@@ -119,10 +135,8 @@ __device__ __forceinline__ uint4 tc_perm(uint4 v) {
 // accumulators the k-steps rotate over -- consecutive MMAs into one
 // accumulator wait for each other, so a single chain runs at the MMA latency
 // instead of the tensor pipe's rate; the epilogue adds the C partial sums.
-// BPS: 64-k boxes per ring stage. Every barrier step costs ~0.1-0.25 us in
-// the thread that issues MMAs whatever the work behind it, so two boxes per
-// stage (one wait and one commit per 8 MMAs) stream closer to the HBM rate at
-// small batch; a one-box stage keeps more stages in a small ring.
+// BPS: 64-k boxes per ring stage: two boxes per stage mean one wait and one
+// commit per 8 MMAs; a one-box stage keeps more stages in a small ring.
 template <int NT, int C, int BPS>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX,
@@ -173,11 +187,12 @@ __global__ void __launch_bounds__(192, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer ----
-        if (lane == 0) {
-            // W tiles do not depend on the previous kernel: fill the whole
-            // ring with them first, then wait, then add the X tiles (X may be
-            // the previous kernel's output).
-            const int npre = min(D, nks);
+        const bool leader = tc_elect();
+        // W tiles do not depend on the previous kernel: fill the whole
+        // ring with them first, then wait, then add the X tiles (X may be
+        // the previous kernel's output).
+        const int npre = min(D, nks);
+        if (leader)
             for (int i = 0; i < npre; ++i) {
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc_smem(&full[i])),
                              "r"(STAGE)
@@ -186,15 +201,19 @@ __global__ void __launch_bounds__(192, 1)
                     tc_tma_2d(smem + (size_t)i * STAGE + bb * A_BYTES, &mapW, ((ks0 + i) * BPS + bb) * 64, row0,
                               &full[i]);
             }
-            pdl_wait();
+        __syncwarp();
+        pdl_wait();
+        if (leader)
             for (int i = 0; i < npre; ++i)
                 for (int bb = 0; bb < BPS; ++bb)
                     tc_tma_2d(smem + (size_t)i * STAGE + BPS * A_BYTES + bb * B_BYTES, &mapX,
                               ((ks0 + i) * BPS + bb) * 64, a.m0, &full[i]);
-            for (int i = npre; i < nks; ++i) {
-                const int s = i % D;
-                if (!tc_wait(&empty[s], ((i / D) - 1) & 1)) break;
-                uint8_t* st = smem + (size_t)s * STAGE;
+        __syncwarp();
+        for (int i = npre; i < nks; ++i) {
+            const int s = i % D;
+            if (!tc_wait_warp(&empty[s], ((i / D) - 1) & 1)) break;
+            uint8_t* st = smem + (size_t)s * STAGE;
+            if (leader) {
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc_smem(&full[s])),
                              "r"(STAGE)
                              : "memory");
@@ -204,17 +223,19 @@ __global__ void __launch_bounds__(192, 1)
                     tc_tma_2d(st + BPS * A_BYTES + bb * B_BYTES, &mapX, kc, a.m0, &full[s]);
                 }
             }
+            __syncwarp();
         }
     } else if (warp == 1) {
         // --------------------------------------------------- MMA issuer ----
-        if (lane == 0) {
+        {
+            const bool leader = tc_elect();
             bool ok = true;
             const uint32_t idesc = tc_idesc(128, NT);
             for (int i = 0; i < nks; ++i) {
                 const int s = i % D;
-                if (ok) ok = tc_wait(&full[s], (i / D) & 1);
-                if (ok) {
-                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (ok) ok = tc_wait_warp(&full[s], (i / D) & 1);
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (ok && leader) {
                     const uint32_t sa = tc_smem(smem + (size_t)s * STAGE);
 #pragma unroll
                     for (int bb = 0; bb < BPS; ++bb) {
@@ -235,14 +256,18 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
                 // release the stage once these MMAs have read it (also on error, so the producer can finish)
-                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                 tc_smem(&empty[s]))
-                             : "memory");
+                if (leader)
+                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                     tc_smem(&empty[s]))
+                                 : "memory");
+                __syncwarp();
             }
             // accumulator complete (or, after an error, no MMA left in flight)
-            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                             tc_smem(accum))
-                         : "memory");
+            if (leader)
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                 tc_smem(accum))
+                             : "memory");
+            __syncwarp();
         }
     } else {
         // ----------------------------------------------------- epilogue ----
@@ -322,7 +347,7 @@ __global__ void __launch_bounds__(192, 1)
 // ride inside one exact tensor-core accumulation over K, and folding it into
 // bf16 weights would round them. Here each 128-k stage is one group, and four
 // roles run concurrently, decoupled by mbarriers:
-//   * warp 0 (one thread) streams the packed codes (128 rows x 64 bytes) and
+//   * warp 0 (one elected lane) streams the packed codes (128 rows x 64 bytes) and
 //     the X tile (two 64-k halves, 128-byte swizzle) with TMA into a deep ring
 //     (the codes are the HBM stream; the ring holds no converted operand);
 //   * warps 2..9 (one thread per weight row and k-half) unpack their row's
@@ -333,18 +358,17 @@ __global__ void __launch_bounds__(192, 1)
 //     16-byte chunks in place to the same k order (pairs (0,4) (1,5) (2,6)
 //     (3,7), the order the nibble unpack produces); the products are exact
 //     and the tensor core adds in fp32;
-//   * warp 1 (one thread) issues the stage's 8 MMAs (A from TMEM, X from
-//     shared memory) into one of four TMEM accumulators;
+//   * warp 1 (one elected lane) issues the stage's MMAs (A from TMEM, X from
+//     shared memory) into the groups' TMEM accumulators;
 //   * warps 10..13 (one thread per weight row) read each accumulator back,
 //     multiply by the row's fp32 group scale and accumulate in registers.
-// The thread that issues MMAs is the serial role, and every mbarrier wait or
-// commit costs ~0.1 us there, so it does one commit per group (group done,
-// waited on by both the unpack and the read-back warps) and, when there are
-// as many accumulators as A operands, one wait (A ready): the unpack warps
-// then check that the accumulator is free, in parallel. With fewer
-// accumulators (batch tile 64) that check stays with the MMA thread, so the
-// unpack warps can still run NA groups ahead. The unpack warps wait for a
-// ring slot once per slot.
+// The MMA issuer is the serial role: it does one commit per stage (stage
+// done, waited on by both the unpack and the read-back warps) and, when there
+// are as many accumulators as A operands, one wait (A ready): the unpack
+// warps then check that the accumulator is free, in parallel. With fewer
+// accumulators that check stays with the MMA issuer, so the unpack warps can
+// still run NA groups ahead. The unpack warps wait for a ring slot once per
+// slot.
 // A cluster splits K for short, wide shapes (partials summed through
 // distributed shared memory in rank order). Every wait is bounded; on expiry
 // the kernel records the fault flag and skips the remaining work.
@@ -374,10 +398,8 @@ struct TcAwqLayout {
     static constexpr uint32_t OFF_Q = GS * X_GROUP;   // inside a ring slot
     static constexpr uint32_t SLOT = OFF_Q + 128 * Q_ROW;
     static constexpr uint32_t TX = 128 * Q_ROW + GS * X_GROUP;  // bytes TMA delivers per slot
-    // Every step of a role (a barrier wait, a fence, an arrive, a commit)
-    // costs ~0.1-0.25 us whatever the work behind it, so the roles hand over
-    // GP groups per stage: one wait, commit and arrive per stage. Each group
-    // keeps its own accumulators (its scale differs).
+    // The roles hand over GP groups per stage: one wait, commit and arrive
+    // per stage. Each group keeps its own accumulators (its scale differs).
     static constexpr int GP = 2;                      // groups per stage
     static constexpr int NA = 4;                      // TMEM A operands (groups)
     static constexpr int A_COLS = 64;                 // TMEM columns of one 128-k A operand
@@ -484,24 +506,27 @@ __global__ void __launch_bounds__(448, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer ----
-        if (lane == 0) {
-            // a slot = GS groups; codes do not depend on the previous kernel:
-            // fill the ring with them first, then wait, then add the X tiles
-            const int nslots = (nks + GS - 1) / GS;
-            const int npre = min(D, nslots);  // slots whose codes are already on the way (issued above)
-            auto load_x = [&](uint8_t* st, int j, uint64_t* bar) {
-                for (int g = 0; g < GS; ++g) {
-                    const int kc = (ks0 + j * GS + g) * 128;
-                    tc_tma_2d(st + g * L::X_GROUP, &mapX, kc, a.m0, bar);
-                    tc_tma_2d(st + g * L::X_GROUP + L::X_HALF, &mapX, kc + 64, a.m0, bar);
-                }
-            };
-            pdl_wait();
+        const bool leader = tc_elect();
+        // a slot = GS groups; codes do not depend on the previous kernel:
+        // fill the ring with them first, then wait, then add the X tiles
+        const int nslots = (nks + GS - 1) / GS;
+        const int npre = min(D, nslots);  // slots whose codes are already on the way (issued above)
+        auto load_x = [&](uint8_t* st, int j, uint64_t* bar) {
+            for (int g = 0; g < GS; ++g) {
+                const int kc = (ks0 + j * GS + g) * 128;
+                tc_tma_2d(st + g * L::X_GROUP, &mapX, kc, a.m0, bar);
+                tc_tma_2d(st + g * L::X_GROUP + L::X_HALF, &mapX, kc + 64, a.m0, bar);
+            }
+        };
+        pdl_wait();
+        if (leader)
             for (int j = 0; j < npre; ++j) load_x(ring + (size_t)j * L::SLOT, j, &qfull[j]);
-            for (int j = npre; j < nslots; ++j) {
-                const int s = j % D;
-                if (!tc_wait(&empty[s], ((j / D) - 1) & 1)) break;
-                uint8_t* st = ring + (size_t)s * L::SLOT;
+        __syncwarp();
+        for (int j = npre; j < nslots; ++j) {
+            const int s = j % D;
+            if (!tc_wait_warp(&empty[s], ((j / D) - 1) & 1)) break;
+            uint8_t* st = ring + (size_t)s * L::SLOT;
+            if (leader) {
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc_smem(&qfull[s])),
                              "r"(L::TX)
                              : "memory");
@@ -509,18 +534,20 @@ __global__ void __launch_bounds__(448, 1)
                     tc_tma_2d(st + L::OFF_Q + q * L::Q_BOX, &mapQ, (ks0 + j * GS + 2 * q) * 64, row0, &qfull[s]);
                 load_x(st, j, &qfull[s]);
             }
+            __syncwarp();
         }
     } else if (warp == 1) {
         // --------------------------------------------------- MMA issuer ----
-        if (lane == 0) {
+        {
+            const bool leader = tc_elect();
             const uint32_t idesc = tc_idesc(128, NT);
             for (int p = 0; p < nst; ++p) {
                 const int pa = p % NAS, pb = p % NBS;
-                if (ok) ok = tc_wait(&aready[pa], (p / NAS) & 1);
+                if (ok) ok = tc_wait_warp(&aready[pa], (p / NAS) & 1);
                 // accumulators free; with NBS == NAS the unpack warps checked them before aready
-                if (NBS < NAS && ok && p >= NBS) ok = tc_wait(&dempty[pb], ((p / NBS) - 1) & 1);
-                if (ok) {
-                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (NBS < NAS && ok && p >= NBS) ok = tc_wait_warp(&dempty[pb], ((p / NBS) - 1) & 1);
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (ok && leader) {
 #pragma unroll
                     for (int gg = 0; gg < GP; ++gg) {
                         const int i = p * GP + gg;
@@ -548,21 +575,27 @@ __global__ void __launch_bounds__(448, 1)
                         }
                     }
                 }
-                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                 tc_smem(&mdone[pa]))
-                             : "memory");
-                // ring slot free once the stage holding its last group is done
-                const int il = min(nks, (p + 1) * GP) - 1, jl = il / GS;
-                if (il - jl * GS == GS - 1 || il == nks - 1)
+                if (leader) {
                     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                     tc_smem(&empty[jl % D]))
+                                     tc_smem(&mdone[pa]))
                                  : "memory");
+                    // ring slot free once the stage holding its last group is done
+                    const int il = min(nks, (p + 1) * GP) - 1, jl = il / GS;
+                    if (il - jl * GS == GS - 1 || il == nks - 1)
+                        asm volatile(
+                            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                tc_smem(&empty[jl % D]))
+                            : "memory");
+                }
+                __syncwarp();
             }
             // every MMA issued above has completed before TMEM is released
-            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                             tc_smem(done))
-                         : "memory");
-            tc_wait(done, 0);
+            if (leader)
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                 tc_smem(done))
+                             : "memory");
+            __syncwarp();
+            tc_wait_warp(done, 0);
         }
     } else if (warp < 10) {
         // ------------------------------------------------------ unpack ----
