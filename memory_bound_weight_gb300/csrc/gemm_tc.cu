@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(192, 1)
 //   * warp 0 (one elected lane) streams the packed codes (128 rows x 64 bytes) and
 //     the X tile (two 64-k halves, 128-byte swizzle) with TMA into a deep ring
 //     (the codes are the HBM stream; the ring holds no converted operand);
-//   * warps 2..9 (one thread per weight row and k-half) unpack their row's
+//   * the next UW warps (one thread per weight row and k-part) unpack their row's
 //     codes to exact bf16 (q - z) and store them with tcgen05.st into one of
 //     two A operands held in TMEM (lane = weight row; column c of a 16-k step
 //     = the bf16 pair of k 2c, 2c+1 -- measured), so the 4x wider converted
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(192, 1)
 //     and the tensor core adds in fp32;
 //   * warp 1 (one elected lane) issues the stage's MMAs (A from TMEM, X from
 //     shared memory) into the groups' TMEM accumulators;
-//   * warps 10..13 (one thread per weight row) read each accumulator back,
+//   * the last 4 warps (one thread per weight row) read each accumulator back,
 //     multiply by the row's fp32 group scale and accumulate in registers.
 // The MMA issuer is the serial role: it does one commit per stage (stage
 // done, waited on by both the unpack and the read-back warps) and, when there
@@ -413,10 +413,17 @@ struct TcAwqLayout {
     static_assert(NA % GP == 0 && NB % GP == 0 && GS % GP == 0, "");
     static constexpr int TMEM_COLS = 512;
     static_assert(D_COL0 + NB * C * NT <= TMEM_COLS, "");
+    // Unpack warps: 4 row quarters x KH k-parts of a group. The unpack is
+    // latency-bound with two of these warps per scheduler; at batch tile 16
+    // the kernel's registers leave room for four.
+    static constexpr int UW = (NT == 16) ? 16 : 8;
+    static constexpr int KH = UW / 4;
+    static constexpr int NWD = 16 / KH;  // 32-bit code words per lane and group (8 or 4)
+    static constexpr int THREADS = 32 * (2 + UW + 4);
 };
 
 template <int NT>  // batch tile: 16, 32 or 64
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(TcAwqLayout<NT>::THREADS, 1)
     gemm_tc_awq_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapX,
                        const TcAwqArgs a, const int S, const int D) {
     using L = TcAwqLayout<NT>;
@@ -458,7 +465,7 @@ __global__ void __launch_bounds__(448, 1)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&empty[s])));
         }
         for (int b = 0; b < NAS; ++b) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(tc_smem(&aready[b])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(tc_smem(&aready[b])), "n"(L::UW));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&mdone[b])));
         }
         for (int b = 0; b < NBS; ++b)
@@ -490,7 +497,7 @@ __global__ void __launch_bounds__(448, 1)
     // The CTA's scale and zero tables, [group][row], loaded by all threads at
     // once (a per-group load, or a per-thread loop of dependent load/store
     // pairs, puts an L2 round trip on every group of the critical path).
-    for (int e = threadIdx.x; e < nks * 128; e += 448) {
+    for (int e = threadIdx.x; e < nks * 128; e += L::THREADS) {
         const int i = e >> 7, rr = e & 127;
         const size_t row = (size_t)min(row0 + rr, a.N - 1);
         s_tab[i * 128 + rr] = ld_ro_u16(a.scales + row * a.G + ks0 + i);
@@ -597,10 +604,11 @@ __global__ void __launch_bounds__(448, 1)
             __syncwarp();
             tc_wait_warp(done, 0);
         }
-    } else if (warp < 10) {
+    } else if (warp < 2 + L::UW) {
         // ------------------------------------------------------ unpack ----
-        const int cw = warp - 2;            // 0..7
-        const int h = cw >> 2;              // k-half of the group this warp unpacks
+        constexpr int NWD = L::NWD;
+        const int cw = warp - 2;            // 0 .. UW-1
+        const int h = cw >> 2;              // k-part of the group this warp unpacks
         const int quarter = warp & 3;       // TMEM lanes 32*quarter .. +31 (the warp's accessible quarter)
         const int r = quarter * 32 + lane;  // weight row of the tile
         for (int p = 0; p < nst; ++p) {
@@ -623,40 +631,54 @@ __global__ void __launch_bounds__(448, 1)
                 if (i >= nks) break;
                 const int g = i - j * GS;
                 const uint32_t zc = z_tab[i * 128 + r];
-                uint32_t av[32];
+                uint32_t av[4 * NWD];
                 {
                     // row r of box g/2; 16-byte chunk c of the row sits at chunk c ^ (r & 7)
                     const uint8_t* qrow = st + L::OFF_Q + (g >> 1) * L::Q_BOX + r * 128;
-                    const int c0 = (g & 1) * 4 + h * 2;
-                    uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
-                    if (ok) {
-                        q0 = *reinterpret_cast<const uint4*>(qrow + ((c0 ^ (r & 7)) << 4));
-                        q1 = *reinterpret_cast<const uint4*>(qrow + (((c0 + 1) ^ (r & 7)) << 4));
+                    const int c0 = (g & 1) * 4 + h * (NWD / 4);
+                    uint32_t wv[NWD];
+#pragma unroll
+                    for (int ch = 0; ch < NWD / 4; ++ch) {
+                        uint4 q = make_uint4(0, 0, 0, 0);
+                        if (ok) q = *reinterpret_cast<const uint4*>(qrow + (((c0 + ch) ^ (r & 7)) << 4));
+                        wv[4 * ch + 0] = q.x;
+                        wv[4 * ch + 1] = q.y;
+                        wv[4 * ch + 2] = q.z;
+                        wv[4 * ch + 3] = q.w;
                     }
-                    const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
                     const uint32_t zz = (0x4300u | zc) * 0x00010001u;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 0; c < NWD; ++c) {
                         av[4 * c + 0] = tc_sub(tc_nib(wv[c]), zz);
                         av[4 * c + 1] = tc_sub(tc_nib(wv[c] >> 4), zz);
                         av[4 * c + 2] = tc_sub(tc_nib(wv[c] >> 8), zz);
                         av[4 * c + 3] = tc_sub(tc_nib(wv[c] >> 12), zz);
                     }
                 }
-                const uint32_t ta =
-                    tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((pa * GP + gg) * L::A_COLS + h * 32);
-                asm volatile(
-                    "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                    "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(ta),
-                    "r"(av[0]), "r"(av[1]), "r"(av[2]), "r"(av[3]), "r"(av[4]), "r"(av[5]), "r"(av[6]), "r"(av[7]),
-                    "r"(av[8]), "r"(av[9]), "r"(av[10]), "r"(av[11]), "r"(av[12]), "r"(av[13]), "r"(av[14]),
-                    "r"(av[15]), "r"(av[16]), "r"(av[17]), "r"(av[18]), "r"(av[19]), "r"(av[20]), "r"(av[21]),
-                    "r"(av[22]), "r"(av[23]), "r"(av[24]), "r"(av[25]), "r"(av[26]), "r"(av[27]), "r"(av[28]),
-                    "r"(av[29]), "r"(av[30]), "r"(av[31])
-                    : "memory");
+                const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) +
+                                    (uint32_t)((pa * GP + gg) * L::A_COLS + h * 4 * NWD);
+                if constexpr (NWD == 8) {
+                    asm volatile(
+                        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+                        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(ta),
+                        "r"(av[0]), "r"(av[1]), "r"(av[2]), "r"(av[3]), "r"(av[4]), "r"(av[5]), "r"(av[6]),
+                        "r"(av[7]), "r"(av[8]), "r"(av[9]), "r"(av[10]), "r"(av[11]), "r"(av[12]), "r"(av[13]),
+                        "r"(av[14]), "r"(av[15]), "r"(av[16]), "r"(av[17]), "r"(av[18]), "r"(av[19]), "r"(av[20]),
+                        "r"(av[21]), "r"(av[22]), "r"(av[23]), "r"(av[24]), "r"(av[25]), "r"(av[26]), "r"(av[27]),
+                        "r"(av[28]), "r"(av[29]), "r"(av[30]), "r"(av[31])
+                        : "memory");
+                } else {
+                    asm volatile(
+                        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+                        "%15,%16};" ::"r"(ta),
+                        "r"(av[0]), "r"(av[1]), "r"(av[2]), "r"(av[3]), "r"(av[4]), "r"(av[5]), "r"(av[6]),
+                        "r"(av[7]), "r"(av[8]), "r"(av[9]), "r"(av[10]), "r"(av[11]), "r"(av[12]), "r"(av[13]),
+                        "r"(av[14]), "r"(av[15])
+                        : "memory");
+                }
                 if (ok) {
                     uint4* xs = reinterpret_cast<uint4*>(st + g * L::X_GROUP);
-                    for (int c = cw * 32 + lane; c < NT * 16; c += 256) xs[c] = tc_perm(xs[c]);
+                    for (int c = cw * 32 + lane; c < NT * 16; c += L::UW * 32) xs[c] = tc_perm(xs[c]);
                 }
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -728,7 +750,7 @@ __global__ void __launch_bounds__(448, 1)
     if (S > 1) {
         // every accumulator has been read back and every MMA is done: the ring is free for the partials
         float* part = reinterpret_cast<float*>(smem);  // [NT][128]
-        if (warp >= 10) {
+        if (warp >= 2 + L::UW) {
             const int r = (warp & 3) * 32 + lane;
 #pragma unroll
             for (int c = 0; c < NT; ++c) part[c * 128 + r] = ok ? acc[c] : 0.f;
@@ -737,7 +759,7 @@ __global__ void __launch_bounds__(448, 1)
         cluster.sync();
         const int total = NT * 128;
         const int lo = rank * total / S, hi = (rank + 1) * total / S;
-        for (int e = lo + (int)threadIdx.x; e < hi; e += 448) {
+        for (int e = lo + (int)threadIdx.x; e < hi; e += L::THREADS) {
             const int m = e / 128, rr = e % 128;
             float v = 0.f;
             for (int s2 = 0; s2 < S; ++s2) v += *cluster.map_shared_rank(part + e, s2);
@@ -937,7 +959,7 @@ static cudaError_t launch_awq_nt(const CUtensorMap& mq, const CUtensorMap& mx, c
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(tiles * split), 1, 1);
-    cfg.blockDim = dim3(448, 1, 1);
+    cfg.blockDim = dim3(TcAwqLayout<NT>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attrs[2];
