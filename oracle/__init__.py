@@ -75,6 +75,8 @@ class Oracle:
         lib.oracle_gemm_bf16.argtypes = [_P, _P, _I64, _I64, _I64, _P, _P]
         lib.oracle_gemm_int4_g64.argtypes = [_P, _P, _P, _I64, _I64, _I64, _P, _P]
         lib.oracle_gemm_int4_awq_g128.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P]
+        lib.oracle_gemm_int4_awq_g128_repacked.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P]
+        lib.oracle_repack_int4.argtypes = [_P, _I64, _I64, _P]
         lib.oracle_gemm_int8_pc.argtypes = [_P, _P, _P, _I64, _I64, _I64, _P, _P]
         lib.oracle_quantize_int8_pc.argtypes = [_P, _I64, _I64, _P, _P]
         lib.oracle_rmsnorm_bf16.argtypes = [_P, _P, _I64, _I64, ctypes.c_double, _P]
@@ -83,7 +85,8 @@ class Oracle:
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         for f in ("oracle_dequant_int4_g64", "oracle_dequant_int4_awq_g128", "oracle_gemm_bf16",
-                  "oracle_gemm_int4_g64", "oracle_gemm_int4_awq_g128", "oracle_gemm_int8_pc",
+                  "oracle_gemm_int4_g64", "oracle_gemm_int4_awq_g128", "oracle_gemm_int4_awq_g128_repacked",
+                  "oracle_repack_int4", "oracle_gemm_int8_pc",
                   "oracle_quantize_int8_pc", "oracle_rmsnorm_bf16", "oracle_swiglu", "oracle_add_residual",
                   "oracle_set_num_threads"):
             getattr(lib, f).restype = None
@@ -147,7 +150,10 @@ class Oracle:
         self.lib.oracle_gemm_int4_g64(_ptr(codes), _ptr(scales), _ptr(X), M, N, K, _ptr(Y), _ptr(A))
         return Y, A
 
-    def gemm_int4_awq_g128(self, codes, scales, zeros, X: np.ndarray):
+    def gemm_int4_awq_g128(self, codes, scales, zeros, X: np.ndarray, repacked: bool = False):
+        """codes uint8 (N, K/2) (canonical, or the load-time repacked layout when
+        `repacked`), scales fp16 bits (N, K/128), zeros uint8 (N, (K/128+1)/2),
+        X bf16 bits (M, K) or (K,) -> (Y, Yabs), each (M, N)."""
         codes = np.ascontiguousarray(codes, dtype=np.uint8)
         scales = np.ascontiguousarray(scales, dtype=np.uint16)
         zeros = np.ascontiguousarray(zeros, dtype=np.uint8)
@@ -158,9 +164,19 @@ class Oracle:
         assert codes.shape == (N, K // 2) and scales.shape == (N, G) and zeros.shape == (N, (G + 1) // 2)
         Y = np.empty((M, N), dtype=np.float64)
         A = np.empty((M, N), dtype=np.float64)
-        self.lib.oracle_gemm_int4_awq_g128(_ptr(codes), _ptr(scales), _ptr(zeros), _ptr(X), M, N, K,
-                                           _ptr(Y), _ptr(A))
+        fn = self.lib.oracle_gemm_int4_awq_g128_repacked if repacked else self.lib.oracle_gemm_int4_awq_g128
+        fn(_ptr(codes), _ptr(scales), _ptr(zeros), _ptr(X), M, N, K, _ptr(Y), _ptr(A))
         return Y, A
+
+    def repack_int4(self, codes: np.ndarray) -> np.ndarray:
+        """Canonical INT4 codes uint8 (N, K/2), K % 8 == 0 -> the load-time repacked layout."""
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        N, half = codes.shape
+        K = 2 * half
+        assert K % 8 == 0
+        out = np.empty_like(codes)
+        self.lib.oracle_repack_int4(_ptr(codes), N, K, _ptr(out))
+        return out
 
     # ---- symmetric INT8, per-output-channel scale
     def gemm_int8_pc(self, codes, scales, X: np.ndarray):

@@ -19,7 +19,9 @@
  *     symmetric reading w = (q - 8) * s.
  *   - AWQ-style INT4 weights: 4-bit codes with an fp16 scale and a zero point
  *     per 128 weights (llm-rs vs vLLM, sec. 6, format table); w = (q - z) * s
- *     with z a 4-bit code.
+ *     with z a 4-bit code. The same codes reordered once at load time (sec. 6
+ *     and sec. 7: Marlin-style reordered weights) give the same product; the
+ *     reorder is a fixed permutation of the 8 nibbles of each 4-byte word.
  *   - Batched decode: the same weights used for M activation rows
  *     (llm-rs vs vLLM, sec. 3 "Batching moves decode from memory toward math").
  *   - Fusions around a GEMV: RMSNorm of x folded into the projection
@@ -161,19 +163,58 @@ static double dequant_g64(const uint8_t *codes, const uint16_t *scales,
     return (double)(q - 8) * s;
 }
 
+/* Load-time repacked layout of the same codes (llm-rs vs vLLM, sec. 6
+ * "Quantization helps memory-bound work, and can hurt compute-bound work" and
+ * sec. 7 "Reading the scoreboard": 4-bit weights reordered once at load time,
+ * so that the kernel's unpack hands the multiply its operands in order). A
+ * row keeps its K/2 bytes; within each 4-byte word (weights k = 8w .. 8w+7,
+ * nibble slot t = bits 4t .. 4t+3 of the little-endian word) weight 8w + j
+ * sits in slot j/2 + 4*(j%2): the even k in slots 0-3, the odd k in 4-7. */
+static int repacked_slot(int j) { return j / 2 + 4 * (j % 2); }
+
+/* 4-bit code of weight (i, k) in the repacked layout. */
+static int repacked_code_at(const uint8_t *codes, int64_t K, int64_t i, int64_t k)
+{
+    int t = repacked_slot((int)(k % 8));
+    uint8_t b = codes[i * (K / 2) + (k / 8) * 4 + t / 2];
+    return (t % 2 == 0) ? (b & 0x0F) : (b >> 4);
+}
+
+/* out = the repacked layout of canonical codes [N][K/2] (K a multiple of 8). */
+void oracle_repack_int4(const uint8_t *codes, int64_t N, int64_t K, uint8_t *out)
+{
+    for (int64_t i = 0; i < N; i++) {
+        for (int64_t b = 0; b < K / 2; b++) out[i * (K / 2) + b] = 0;
+        for (int64_t k = 0; k < K; ++k) {
+            int q = code_at(codes, K, i, k);
+            int t = repacked_slot((int)(k % 8));
+            int64_t at = i * (K / 2) + (k / 8) * 4 + t / 2;
+            out[at] = (uint8_t)(out[at] | (t % 2 == 0 ? q : q << 4));
+        }
+    }
+}
+
 /* AWQ-style group-128: w = (q - z) * s with scale and zero point of group
- * g = k/128 of row i; zero points packed two per byte, low nibble = even g. */
-static double dequant_awq(const uint8_t *codes, const uint16_t *scales,
-                          const uint8_t *zeros, int64_t K, int64_t i, int64_t k)
+ * g = k/128 of row i; zero points packed two per byte, low nibble = even g.
+ * `repacked`: the codes are in the repacked layout above. */
+static double dequant_awq_any(const uint8_t *codes, const uint16_t *scales,
+                              const uint8_t *zeros, int64_t K, int64_t i, int64_t k,
+                              int repacked)
 {
     int64_t G = K / 128;
     int64_t zstride = (G + 1) / 2;
     int64_t g = k / 128;
-    int q = code_at(codes, K, i, k);
+    int q = repacked ? repacked_code_at(codes, K, i, k) : code_at(codes, K, i, k);
     uint8_t zb = zeros[i * zstride + g / 2];
     int z = (g % 2 == 0) ? (zb & 0x0F) : (zb >> 4);
     double s = oracle_f16_to_double(scales[i * G + g]);
     return (double)(q - z) * s;
+}
+
+static double dequant_awq(const uint8_t *codes, const uint16_t *scales,
+                          const uint8_t *zeros, int64_t K, int64_t i, int64_t k)
+{
+    return dequant_awq_any(codes, scales, zeros, K, i, k, 0);
 }
 
 void oracle_dequant_int4_g64(const uint8_t *codes, const uint16_t *scales,
@@ -244,10 +285,10 @@ void oracle_gemm_int4_g64(const uint8_t *codes, const uint16_t *scales,
     }
 }
 
-void oracle_gemm_int4_awq_g128(const uint8_t *codes, const uint16_t *scales,
-                               const uint8_t *zeros, const uint16_t *X,
-                               int64_t M, int64_t N, int64_t K, double *Y,
-                               double *Yabs)
+static void gemm_awq_any(const uint8_t *codes, const uint16_t *scales,
+                         const uint8_t *zeros, const uint16_t *X, int64_t M,
+                         int64_t N, int64_t K, double *Y, double *Yabs,
+                         int repacked)
 {
     int64_t i;
 #pragma omp parallel for schedule(static)
@@ -255,7 +296,7 @@ void oracle_gemm_int4_awq_g128(const uint8_t *codes, const uint16_t *scales,
         for (int64_t m = 0; m < M; m++) {
             double acc = 0.0, aabs = 0.0;
             for (int64_t k = 0; k < K; k++) {
-                double w = dequant_awq(codes, scales, zeros, K, i, k);
+                double w = dequant_awq_any(codes, scales, zeros, K, i, k, repacked);
                 double x = oracle_bf16_to_double(X[m * K + k]);
                 acc += w * x;
                 aabs += fabs(w * x);
@@ -264,6 +305,23 @@ void oracle_gemm_int4_awq_g128(const uint8_t *codes, const uint16_t *scales,
             Yabs[m * N + i] = aabs;
         }
     }
+}
+
+void oracle_gemm_int4_awq_g128(const uint8_t *codes, const uint16_t *scales,
+                               const uint8_t *zeros, const uint16_t *X,
+                               int64_t M, int64_t N, int64_t K, double *Y,
+                               double *Yabs)
+{
+    gemm_awq_any(codes, scales, zeros, X, M, N, K, Y, Yabs, 0);
+}
+
+/* The same product with the codes in the repacked layout. */
+void oracle_gemm_int4_awq_g128_repacked(const uint8_t *codes, const uint16_t *scales,
+                                        const uint8_t *zeros, const uint16_t *X,
+                                        int64_t M, int64_t N, int64_t K, double *Y,
+                                        double *Yabs)
+{
+    gemm_awq_any(codes, scales, zeros, X, M, N, K, Y, Yabs, 1);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -15,6 +15,9 @@ What each pin compares with:
   * invariants: power-of-two scaling, identity / one-hot weights, one-hot x,
     consistent permutation of k, batch = separate calls, linearity on
     disjoint supports;
+  * load-time INT4 repack: hand-worked words and one-hot products in
+    tests/golden/int4_repack_hand.txt, the permutation's order (three
+    applications are the identity), and equality with the canonical product;
   * INT8 per-channel: hand-worked values in tests/golden/int8_pc_hand.txt
     (GEMV and quantizer, including ties and a non-dyadic scale), exact
     rational products, numpy's matmul, scale linearity, and the quantizer's
@@ -559,6 +562,66 @@ def pin_swiglu_identities(o):
     assert np.allclose(o.swiglu(a, b), s * b, rtol=0, atol=1e-13)
 
 
+def load_repack_fixture():
+    rep, dots = [], []
+    with open(os.path.join(GOLDEN, "int4_repack_hand.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            parts = line.split()
+            if parts[0] == "repack":
+                rep.append((_parse_hex_list(parts[1]), _parse_hex_list(parts[2])))
+            else:
+                _, codes, scale, zb, k, expect = parts
+                dots.append(dict(codes=_parse_hex_list(codes), scale=int(scale, 16), zeros=int(zb, 16), k=int(k),
+                                 expect=Fraction(expect)))
+    return rep, dots
+
+
+def pin_repack_hand_worked(o):
+    """Hand-worked repacked words, and one-hot products over repacked codes
+    (tests/golden/int4_repack_hand.txt)."""
+    rep, dots = load_repack_fixture()
+    assert len(rep) >= 6 and len(dots) >= 8
+    for canon, packed in rep:
+        c = np.array(canon, dtype=np.uint8).reshape(1, -1)
+        got = o.repack_int4(c)
+        assert got.tolist() == [packed], (canon, [hex(v) for v in got[0]])
+    for d in dots:
+        K = 128
+        codes = np.array(d["codes"], dtype=np.uint8).reshape(1, K // 2)
+        X = np.zeros((1, K), dtype=np.uint16)
+        X[0, d["k"]] = 0x3F80
+        Y, _ = o.gemm_int4_awq_g128(codes, np.array([[d["scale"]]], dtype=np.uint16),
+                                    np.array([[d["zeros"]]], dtype=np.uint8), X, repacked=True)
+        assert Fraction(float(Y[0, 0])) == d["expect"], (d, Y[0, 0])
+
+
+def pin_repack_permutation(o):
+    """The repack is a fixed permutation of the 8 nibbles of a word with cycles
+    (0)(7)(1 4 2)(3 5 6): applied three times it is the identity, twice it is
+    the inverse; it maps the nibble-count histogram of every row onto itself;
+    and the product over repacked codes equals the product over the canonical
+    ones (the canonical product is pinned above), bit for bit."""
+    rng = np.random.default_rng(41)
+    c = rng.integers(0, 256, size=(7, 192), dtype=np.uint8)
+    r1 = o.repack_int4(c)
+    r3 = o.repack_int4(o.repack_int4(r1))
+    assert np.array_equal(r3, c)
+    assert not np.array_equal(r1, c)
+    assert np.array_equal(np.sort(np_unpack_codes(r1), axis=1), np.sort(np_unpack_codes(c), axis=1))
+    # bytes 4w .. 4w+3 hold exactly the codes of k = 8w .. 8w+7
+    q, qr = np_unpack_codes(c), np_unpack_codes(r1)
+    for w in range(q.shape[1] // 8):
+        assert np.array_equal(np.sort(q[:, 8 * w:8 * w + 8], axis=1), np.sort(qr[:, 8 * w:8 * w + 8], axis=1))
+    for seed, N, K, M in ((42, 5, 256, 2), (43, 3, 384, 1)):
+        cc, s, z, X = small_awq_case(seed, N, K, M)
+        Y0, A0 = o.gemm_int4_awq_g128(cc, s, z, X)
+        Y1, A1 = o.gemm_int4_awq_g128(o.repack_int4(cc), s, z, X, repacked=True)
+        assert np.array_equal(Y0, Y1) and np.array_equal(A0, A1)
+
+
 PINS = [
     pin_f16_decoder_exhaustive,
     pin_bf16_decoder_exhaustive,
@@ -580,6 +643,8 @@ PINS = [
     pin_fusions_hand_worked,
     pin_rmsnorm_invariants,
     pin_swiglu_identities,
+    pin_repack_hand_worked,
+    pin_repack_permutation,
 ]
 
 

@@ -60,6 +60,12 @@ MUTANTS = [
     ("swiglu_gate_up_swapped", "A[i] / (1.0 + exp(-A[i])) * B[i]", "B[i] / (1.0 + exp(-B[i])) * A[i]", 1),
     ("residual_subtracted", "Y[i] + oracle_bf16_to_double(R[i])", "Y[i] - oracle_bf16_to_double(R[i])", 1),
     ("quant_first_entry_skipped", "for (int64_t k = 0; k < K; k++) {", "for (int64_t k = 1; k < K; k++) {", 5),
+    ("repack_inverse_permutation", "return j / 2 + 4 * (j % 2);", "return (j % 4) * 2 + j / 4;", 1),
+    ("repack_nibble_halves_swapped", "(t % 2 == 0 ? q : q << 4)", "(t % 2 == 0 ? q << 4 : q)", 1),
+    ("repacked_decode_nibble_order", "(t % 2 == 0) ? (b & 0x0F) : (b >> 4)", "(t % 2 == 0) ? (b >> 4) : (b & 0x0F)", 1),
+    ("repacked_decode_word_stride", "(k / 8) * 4 + t / 2]", "(k / 8) * 8 + t / 2]", 1),
+    ("repacked_gemm_reads_canonical", "dequant_awq_any(codes, scales, zeros, K, i, k, repacked)",
+     "dequant_awq_any(codes, scales, zeros, K, i, k, 0)", 1),
 ]
 
 
