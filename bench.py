@@ -62,7 +62,7 @@ def parse_args():
     p.add_argument("--impl", default="mbw", choices=["mbw", "reference"])
     p.add_argument("--workload", default="tinyllama_int4",
                    choices=["tinyllama_int4", "tinyllama_int4_fusedops", "tinyllama_int4_unfused", "qwen_bf16",
-                            "qwen_awq", "qwen3_int8", "bf16_2048"])
+                            "qwen_awq", "qwen_awq_repacked", "qwen3_int8", "bf16_2048"])
     p.add_argument("--batch", type=int, default=1,
                    help="activation rows per GEMV (qwen_awq: AWQ-style INT4 decode at batch M)")
     p.add_argument("--no-e2e", action="store_true")
@@ -204,7 +204,7 @@ class Step:
     """All matrices of one decode step resident on the device, and the calls
     that stream them (each GEMV with its own activation rows X [M][K])."""
 
-    def __init__(self, name, fmt, mats, seed, device, M=1):
+    def __init__(self, name, fmt, mats, seed, device, M=1, repacked=False):
         import torch
 
         import memory_bound_weight_gb300 as mbw
@@ -212,6 +212,7 @@ class Step:
         from memory_bound_weight_gb300 import inputs_gpu
 
         self.name, self.fmt, self.mats, self.M = name, fmt, mats, M
+        self.repacked = repacked  # AWQ codes reordered at load time (mbw.repack_int4)
         self.device = device
         sumK = sum(m.K for m in mats)
         sumN = sum(m.N for m in mats)
@@ -225,10 +226,10 @@ class Step:
             inputs_gpu.bf16_normal_(xv, seed, gen.stream_id(mi, gen.KIND_X), gen.X_SIGMA)
             xa = xv if M == 1 else xv.view(M, m.K)
             ya = yv if M == 1 else yv.view(M, m.N)
-            self.calls.append(device_call(fmt, seed, mi, m.N, m.K, xa, ya, device, m.fuse, M))
+            self.calls.append(device_call(fmt, seed, mi, m.N, m.K, xa, ya, device, m.fuse, M, repacked))
             ko += M * m.K
             no += M * m.N
-        self.op = op_of_fmt(fmt)
+        self.op = op_of_fmt(fmt) | (mbw.REPACKED if repacked else 0)
         self.bytes_alg = wl.step_bytes_alg(mats, fmt, M)
         self.flops = sum(wl.call_flops(M, m) for m in mats)
         # e2e: the x vectors and the residuals the calls read come from the host
@@ -258,10 +259,12 @@ def skey(kind):
         ("+res" if fz & wl.FUSE_RESIDUAL else "")
 
 
-def device_call(fmt, seed, mi, N, K, x, y, device, fuse=0, M=1):
+def device_call(fmt, seed, mi, N, K, x, y, device, fuse=0, M=1, repacked=False):
     """(C-ABI call, its inputs, its output) for matrix `mi` of a workload, with
     the matrix generated on the device. A fused call also gets its up matrix,
-    norm weight and residual (seeded like the rest)."""
+    norm weight and residual (seeded like the rest). `repacked` (AWQ): the codes
+    are reordered once, in place, by the load-time repack, and the call is the
+    repacked one."""
     import functools
 
     import memory_bound_weight_gb300 as mbw
@@ -292,6 +295,9 @@ def device_call(fmt, seed, mi, N, K, x, y, device, fuse=0, M=1):
         c = inputs_gpu.int4_codes(seed, mi, N, K, device)
         s = inputs_gpu.f16_group_scales(seed, mi, N, K // 128, device)
         z = inputs_gpu.u4_zero_points(seed, mi, N, K // 128, device)
+        if repacked:
+            mbw.repack_int4(c, out=c)
+            return functools.partial(mbw.gemv_int4_awq_g128, repacked=True), (c, s, z, x), y
         return mbw.gemv_int4_awq_g128, (c, s, z, x), y
     if fmt == wl.FMT_INT8_PC:
         q = inputs_gpu.int8_codes(seed, mi, N, K, device)
@@ -327,6 +333,7 @@ WORKLOAD_MATS = {
     "tinyllama_int4_unfused": (lambda: wl.tinyllama_step(), wl.FMT_INT4_G64),
     "qwen_bf16": (wl.qwen25_7b_step, wl.FMT_BF16),
     "qwen_awq": (wl.qwen25_7b_step, wl.FMT_INT4_AWQ_G128),
+    "qwen_awq_repacked": (wl.qwen25_7b_step, wl.FMT_INT4_AWQ_G128),
     "qwen3_int8": (wl.qwen3_4b_step, wl.FMT_INT8_PC),
     "bf16_2048": (lambda: [wl.Mat(f"copy{i}", 2048, 2048) for i in range(64)], wl.FMT_BF16),
 }
@@ -338,9 +345,10 @@ def make_step(workload, seed, device, M=1):
                     WORKLOAD_MATS[workload][0](), seed, device)
     if workload == "qwen_bf16":
         return Step("Qwen2.5-7B-shaped BF16 decode step, batch 1", wl.FMT_BF16, wl.qwen25_7b_step(), seed, device)
-    if workload == "qwen_awq":
-        return Step(f"Qwen2.5-7B-shaped AWQ-style INT4 decode step, batch {M}", wl.FMT_INT4_AWQ_G128,
-                    wl.qwen25_7b_step(), seed, device, M)
+    if workload in ("qwen_awq", "qwen_awq_repacked"):
+        rp = workload == "qwen_awq_repacked"
+        return Step(f"Qwen2.5-7B-shaped AWQ-style INT4 decode step, batch {M}" + (", repacked codes" if rp else ""),
+                    wl.FMT_INT4_AWQ_G128, wl.qwen25_7b_step(), seed, device, M, repacked=rp)
     if workload == "qwen3_int8":
         return Step(f"Qwen3-4B-shaped symmetric INT8 per-channel decode step, batch {M}", wl.FMT_INT8_PC,
                     wl.qwen3_4b_step(), seed, device, M)
@@ -466,6 +474,9 @@ def workload_desc(workload, batch=1):
             "qwen_bf16": "Qwen2.5-7B-shaped BF16 decode step, batch 1 (141 GEMVs)",
             "qwen_awq": f"Qwen2.5-7B-shaped AWQ-style INT4 decode step (group 128, fp16 scale, uint4 zero point, LM head "
                         f"included), batch {batch} (141 GEMMs)",
+            "qwen_awq_repacked": f"Qwen2.5-7B-shaped AWQ-style INT4 decode step (group 128, fp16 scale, uint4 zero "
+                                 f"point, LM head included), codes reordered at load time (mbw_repack_int4), batch "
+                                 f"{batch} (141 GEMMs)",
             "qwen3_int8": f"Qwen3-4B-shaped symmetric INT8 decode step (one fp32 scale per output channel, every "
                           f"linear layer and the LM head, q/k/v and gate/up fused), batch {batch} (145 GEMVs)",
             "bf16_2048": "BF16 GEMV 2048x2048, batch 1, 64 rotating copies"}[workload]
@@ -723,7 +734,7 @@ def time_per_shape(step, device, reps=5, shapes=None, plans=None):
         calls = []
         for i in range(copies):
             xi, yi = (x[i, 0], y[i, 0]) if M == 1 else (x[i], y[i])
-            calls.append(device_call(step.fmt, 0, 1000 + i, N, K, xi, yi, device, fz, M))
+            calls.append(device_call(step.fmt, 0, 1000 + i, N, K, xi, yi, device, fz, M, step.repacked))
         if plans is not None and (fz, N, K) in plans:
             mbw.plan_select(step.op | fz, M, N, K, plans[(fz, N, K)])
         else:

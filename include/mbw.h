@@ -80,6 +80,8 @@ typedef int mbw_status;
 #define MBW_FUSE_GLU 0x200      /* gated SiLU epilogue */
 #define MBW_FUSE_RESIDUAL 0x400 /* residual-add epilogue */
 #define MBW_FUSE_MASK 0x700
+/* Plan-key flag of gemv_int4_awq_g128_repacked: codes in the repacked layout. */
+#define MBW_REPACKED 0x800
 
 /*
  * gemv_bf16 -- y = W . x with BF16 weights (16 bits per weight; llm-rs vs
@@ -117,6 +119,37 @@ mbw_status gemv_int4_g64(const uint8_t *Wq, const void *scales, const void *x, v
 mbw_status gemv_int4_awq_g128(const uint8_t *Wq, const void *scales, const uint8_t *zeros,
                               const void *X, void *Y, int64_t M, int64_t N, int64_t K,
                               void *workspace, size_t ws_bytes, mbw_stream_t stream);
+
+/*
+ * mbw_repack_int4 -- the load-time reorder of INT4 codes (llm-rs vs vLLM,
+ * sec. 6 "Quantization helps memory-bound work, and can hurt compute-bound
+ * work": Marlin reorders 4-bit weights once at load time so that the unpack
+ * hands each thread its operand directly; sec. 7 "Reading the scoreboard":
+ * reordered weights and bit-trick unpacking). A row keeps its K/2 bytes.
+ * Within each 4-byte word (codes of k = 8w .. 8w+7; nibble slot t = bits
+ * 4t .. 4t+3 of the little-endian word, which holds k = 8w + t in the
+ * canonical layout) code 8w + j moves to slot j/2 + 4*(j%2): the even k fill
+ * slots 0-3 and the odd k slots 4-7, each in k order. The kernels' bit-trick
+ * unpack (bits 0-3 with 16-19, then 4-7 with 20-23, ...) then yields the bf16
+ * pairs (k0, k1), (k2, k3), ... in order, so they use X as loaded; with the
+ * canonical layout they permute X on chip, per thread block. Applied three
+ * times the reorder is the identity.
+ *   Wq : uint8 [N][K/2], canonical (low nibble = even k)   Wr : uint8 [N][K/2]
+ *   Requires K % 8 == 0; Wq and Wr 4-byte aligned; Wr may equal Wq (in place).
+ */
+mbw_status mbw_repack_int4(const uint8_t *Wq, uint8_t *Wr, int64_t N, int64_t K, mbw_stream_t stream);
+
+/*
+ * gemv_int4_awq_g128_repacked -- gemv_int4_awq_g128 with the codes in the
+ * layout of mbw_repack_int4: same scales, zero points, X, Y and product (up to
+ * the order of the fp32 additions). Same requirements as gemv_int4_awq_g128.
+ * Its plans are keyed by MBW_OP_GEMV_INT4_AWQ_G128 | MBW_REPACKED and run on
+ * the tensor-core kernel families (not the CUDA-core ones, which read the
+ * canonical layout).
+ */
+mbw_status gemv_int4_awq_g128_repacked(const uint8_t *Wr, const void *scales, const uint8_t *zeros,
+                                       const void *X, void *Y, int64_t M, int64_t N, int64_t K,
+                                       void *workspace, size_t ws_bytes, mbw_stream_t stream);
 
 /*
  * gemm_skinny_bf16 -- Y = X . W^T with BF16 weights and a skinny batch M

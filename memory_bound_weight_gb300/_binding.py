@@ -23,6 +23,7 @@ OP_GEMV_INT8_PC = 5
 FUSE_NORM = 0x100
 FUSE_GLU = 0x200
 FUSE_RESIDUAL = 0x400
+REPACKED = 0x800
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -43,6 +44,8 @@ SIGNATURES = {
     "gemv_bf16": ([_P, _P, _P, _I64, _I64, _P, _SZ, _P], _ST),
     "gemv_int4_g64": ([_P, _P, _P, _P, _I64, _I64, _P, _SZ, _P], _ST),
     "gemv_int4_awq_g128": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _ST),
+    "gemv_int4_awq_g128_repacked": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _ST),
+    "mbw_repack_int4": ([_P, _P, _I64, _I64, _P], _ST),
     "gemm_skinny_bf16": ([_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _ST),
     "gemv_int8_pc": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _ST),
     "mbw_quantize_int8_pc": ([_P, _P, _P, _I64, _I64, _P], _ST),
@@ -191,9 +194,10 @@ def gemv_int4_g64(Wq, scales, x, out=None, workspace=None):
     return y
 
 
-def gemv_int4_awq_g128(Wq, scales, zeros, X, out=None, workspace=None):
+def gemv_int4_awq_g128(Wq, scales, zeros, X, out=None, workspace=None, repacked=False):
     """Y = X . W^T; Wq uint8 (N, K/2), scales fp16 (N, G), zeros uint8 (N, ceil(G/2)),
-    X bf16 (M, K) or (K,) -> Y (M, N) or (N,)."""
+    X bf16 (M, K) or (K,) -> Y (M, N) or (N,). `repacked`: Wq is in the layout of
+    repack_int4 (calls gemv_int4_awq_g128_repacked)."""
     torch = _torch()
     vec = X.dim() == 1
     X2 = X.unsqueeze(0) if vec else X
@@ -208,10 +212,24 @@ def gemv_int4_awq_g128(Wq, scales, zeros, X, out=None, workspace=None):
         raise ValueError("shapes: Wq (N, K/2), scales (N, K/128), zeros (N, ceil(K/256)), X (M, K)")
     Y = _alloc_out((M, N), Wq, None if out is None else (out.unsqueeze(0) if vec else out))
     wp, wn = _ws(workspace)
-    check("gemv_int4_awq_g128", lib().gemv_int4_awq_g128(
+    name = "gemv_int4_awq_g128_repacked" if repacked else "gemv_int4_awq_g128"
+    check(name, getattr(lib(), name)(
         Wq.data_ptr(), scales.data_ptr(), zeros.data_ptr(), X2.data_ptr(), Y.data_ptr(), M, N, K, wp, wn,
         _stream_ptr(Wq.device)))
     return Y[0] if vec else Y
+
+
+def repack_int4(Wq, out=None):
+    """Canonical INT4 codes uint8 (N, K/2) -> the load-time repacked layout (a new
+    tensor, or `out`, which may be Wq itself)."""
+    torch = _torch()
+    _need(Wq, "Wq", torch.uint8, 2)
+    N, half = Wq.shape
+    Wr = torch.empty_like(Wq) if out is None else out
+    if Wr.shape != Wq.shape or Wr.dtype != torch.uint8 or not Wr.is_contiguous():
+        raise ValueError("out must be a contiguous uint8 tensor of Wq's shape")
+    check("mbw_repack_int4", lib().mbw_repack_int4(Wq.data_ptr(), Wr.data_ptr(), N, 2 * half, _stream_ptr(Wq.device)))
+    return Wr
 
 
 def gemm_skinny_bf16(X, W, out=None, workspace=None):

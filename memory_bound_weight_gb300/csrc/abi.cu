@@ -75,6 +75,7 @@ static mbw_status run_simt(int fmt, int op, const uint8_t* W, const uint16_t* sc
     a.zstride = (a.groups + 1) / 2;
     a.out_f32 = g_out_f32;
     a.rscale = rscale;
+    a.x_natural = (op & MBW_REPACKED) ? 1 : 0;
     if (fz) {
         a.norm_w = static_cast<const uint16_t*>(fz->norm_weight);
         a.norm_eps = fz->norm_eps;
@@ -95,6 +96,21 @@ static mbw_status run_simt(int fmt, int op, const uint8_t* W, const uint16_t* sc
         if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
     }
     return MBW_OK;
+}
+
+// AWQ-style INT4 call (`op` may carry MBW_REPACKED): checks, then the planned launch.
+static mbw_status awq_call(const char* fn, int op, const uint8_t* Wq, const void* scales, const uint8_t* zeros,
+                           const void* X, void* Y, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    mbw_status st = check_sizes(fn, M, N, K, 128);
+    if (st != MBW_OK) return st;
+    if (N == 0 || M == 0) return MBW_OK;
+    if (!Y || (K > 0 && (!Wq || !scales || !zeros || !X)))
+        return fail(MBW_ERR_INVALID_ARG, std::string(fn) + ": NULL pointer");
+    if (!aligned(Wq, 32) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(scales, 2))
+        return fail(MBW_ERR_MISALIGNED,
+                    std::string(fn) + ": Wq must be 32-byte aligned, X and Y 16-byte, scales 2-byte");
+    if (K == 0) return zero_output(Y, M, N, stream);
+    return run_simt(FMT_AWQ, op, Wq, (const uint16_t*)scales, zeros, (const uint16_t*)X, Y, M, N, K, stream);
 }
 
 }  // namespace mbw
@@ -138,17 +154,28 @@ mbw_status gemv_int4_awq_g128(const uint8_t* Wq, const void* scales, const uint8
                               mbw_stream_t stream) {
     (void)workspace;
     (void)ws_bytes;
-    mbw_status st = check_sizes("gemv_int4_awq_g128", M, N, K, 128);
+    return awq_call("gemv_int4_awq_g128", MBW_OP_GEMV_INT4_AWQ_G128, Wq, scales, zeros, X, Y, M, N, K,
+                    (cudaStream_t)stream);
+}
+
+mbw_status gemv_int4_awq_g128_repacked(const uint8_t* Wr, const void* scales, const uint8_t* zeros, const void* X,
+                                       void* Y, int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes,
+                                       mbw_stream_t stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    return awq_call("gemv_int4_awq_g128_repacked", MBW_OP_GEMV_INT4_AWQ_G128 | MBW_REPACKED, Wr, scales, zeros, X,
+                    Y, M, N, K, (cudaStream_t)stream);
+}
+
+mbw_status mbw_repack_int4(const uint8_t* Wq, uint8_t* Wr, int64_t N, int64_t K, mbw_stream_t stream) {
+    mbw_status st = check_sizes("mbw_repack_int4", 1, N, K, 8);
     if (st != MBW_OK) return st;
-    if (N == 0 || M == 0) return MBW_OK;
-    if (!Y || (K > 0 && (!Wq || !scales || !zeros || !X)))
-        return fail(MBW_ERR_INVALID_ARG, "gemv_int4_awq_g128: NULL pointer");
-    if (!aligned(Wq, 32) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(scales, 2))
-        return fail(MBW_ERR_MISALIGNED,
-                    "gemv_int4_awq_g128: Wq must be 32-byte aligned, X and Y 16-byte, scales 2-byte");
-    if (K == 0) return zero_output(Y, M, N, (cudaStream_t)stream);
-    return run_simt(FMT_AWQ, MBW_OP_GEMV_INT4_AWQ_G128, Wq, (const uint16_t*)scales, zeros, (const uint16_t*)X, Y,
-                    M, N, K, (cudaStream_t)stream);
+    if (N == 0 || K == 0) return MBW_OK;
+    if (!Wq || !Wr) return fail(MBW_ERR_INVALID_ARG, "mbw_repack_int4: NULL pointer");
+    if (!aligned(Wq, 4) || !aligned(Wr, 4))
+        return fail(MBW_ERR_MISALIGNED, "mbw_repack_int4: Wq and Wr must be 4-byte aligned");
+    cudaError_t e = launch_repack_int4(Wq, Wr, N, K, (cudaStream_t)stream);
+    return e == cudaSuccess ? MBW_OK : cuda_fail(e, "repack launch");
 }
 
 mbw_status gemv_int8_pc(const int8_t* Wq, const float* scales, const void* X, void* Y, int64_t M, int64_t N,

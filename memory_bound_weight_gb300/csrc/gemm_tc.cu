@@ -356,8 +356,9 @@ __global__ void __launch_bounds__(192, 1)
 //     = the bf16 pair of k 2c, 2c+1 -- measured), so the 4x wider converted
 //     operand never touches shared memory; they also permute the X tile's
 //     16-byte chunks in place to the same k order (pairs (0,4) (1,5) (2,6)
-//     (3,7), the order the nibble unpack produces); the products are exact
-//     and the tensor core adds in fp32;
+//     (3,7), the order the nibble unpack produces; codes in the load-time
+//     repacked layout unpack in natural k order and X is used as loaded);
+//     the products are exact and the tensor core adds in fp32;
 //   * warp 1 (one elected lane) issues the stage's MMAs (A from TMEM, X from
 //     shared memory) into the groups' TMEM accumulators;
 //   * the last 4 warps (one thread per weight row) read each accumulator back,
@@ -382,6 +383,7 @@ struct TcAwqArgs {
     int out_f32;
     const void* xpf;  // the launch's X rows, prefetched into L2 before the wait
     size_t xpf_bytes;
+    int x_natural;    // codes in the repacked layout: X is used as loaded
 };
 
 // A ring slot holds GS groups: the codes of 128 rows x GS*64 bytes as GS/2
@@ -676,7 +678,7 @@ __global__ void __launch_bounds__(TcAwqLayout<NT>::THREADS, 1)
                         "r"(av[14]), "r"(av[15])
                         : "memory");
                 }
-                if (ok) {
+                if (ok && !a.x_natural) {
                     uint4* xs = reinterpret_cast<uint4*>(st + g * L::X_GROUP);
                     for (int c = cw * 32 + lane; c < NT * 16; c += L::UW * 32) xs[c] = tc_perm(xs[c]);
                 }
@@ -983,7 +985,8 @@ static cudaError_t launch_awq_nt(const CUtensorMap& mq, const CUtensorMap& mx, c
 // Y[M][N] = X[M][K] . dequant(W)^T for AWQ-style INT4 weights, in batch
 // slices of up to 64 rows; K split over a cluster of `split` CTAs.
 cudaError_t launch_gemm_tc_awq(const uint8_t* Q, const uint16_t* scales, const uint8_t* zeros, const uint16_t* X,
-                               void* Y, int64_t M, int64_t N, int64_t K, int split, int out_f32, cudaStream_t s) {
+                               void* Y, int64_t M, int64_t N, int64_t K, int split, int out_f32, int x_natural,
+                               cudaStream_t s) {
     const int nt = tc_awq_batch_tile(M);
     CUtensorMap mq, mx;
     if (!encode_2d_typed(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Q, (uint64_t)(K / 2), (uint64_t)N, 128, 128,
@@ -1007,6 +1010,7 @@ cudaError_t launch_gemm_tc_awq(const uint8_t* Q, const uint16_t* scales, const u
     const int gs = TcAwqLayout<16>::GS;
     a.kstages = ((G + split - 1) / split + gs - 1) / gs * gs;
     a.out_f32 = out_f32;
+    a.x_natural = x_natural;
     for (int64_t m0 = 0; m0 < M; m0 += 64) {
         a.m0 = (int)m0;
         a.xpf = X + m0 * K;

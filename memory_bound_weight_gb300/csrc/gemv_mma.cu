@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
             const int m = i / L.xwords;
             const int wi = i - m * L.xwords;
             if (wi < cwords) v = ld_ro16(a.x + (size_t)m * a.K + (size_t)cb0 * BK + (size_t)wi * 8);
-            if (FMT != FMT_BF16) v = perm_pairs(v);
+            if (FMT != FMT_BF16 && !a.x_natural) v = perm_pairs(v);
         }
         xs[i] = v;
     }
@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
             }
             if (FMT == FMT_I8)
                 v = perm_i8(v);
-            else if (FMT != FMT_BF16)
+            else if (FMT != FMT_BF16 && !a.x_natural)
                 v = perm_pairs(v);
         }
         xs[i] = v;

@@ -232,7 +232,7 @@ __global__ void __launch_bounds__((W + 1) * 32)
                 const int m = i / L.xwords;
                 const int wi = i - m * L.xwords;
                 if (wi < cwords) v = ld_ro16(a.x + (size_t)m * a.K + (size_t)cb0 * BK + (size_t)wi * 8);
-                if (FMT != FMT_BF16) v = pair_perm(v);
+                if (FMT != FMT_BF16 && !a.x_natural) v = pair_perm(v);
             }
             xs[i] = v;
         }

@@ -38,6 +38,10 @@ struct GemvArgs {
     const uint8_t* W2;
     const uint16_t* scales2;
     const float* rscale2;
+    // INT4 codes in the load-time repacked layout (mbw_repack_int4): the
+    // unpack then yields the k pairs in natural order, and x is staged as is
+    // instead of with the pair permutation.
+    int x_natural;
 };
 
 // Logical 16-row tiles of a launch (twice the output tiles under the gated epilogue).
@@ -124,8 +128,10 @@ cudaError_t launch_gemm_tc(const uint16_t* X, const uint16_t* W, void* Y, int64_
                            int cfg, int out_f32, cudaStream_t s);
 int tc_batch_tile(int64_t M);
 // tcgen05 AWQ-style INT4 batched GEMM (gemm_tc.cu): whole batch M, slices of 64.
+// x_natural: the codes are in the repacked layout (no X permutation).
 cudaError_t launch_gemm_tc_awq(const uint8_t* Q, const uint16_t* scales, const uint8_t* zeros, const uint16_t* X,
-                               void* Y, int64_t M, int64_t N, int64_t K, int split, int out_f32, cudaStream_t s);
+                               void* Y, int64_t M, int64_t N, int64_t K, int split, int out_f32, int x_natural,
+                               cudaStream_t s);
 int tc_awq_batch_tile(int64_t M);
 bool tc_awq_fits(int64_t M, int64_t K, int split);  // the split leaves room for the scale/zero tables
 int tc_take_fault();
@@ -142,6 +148,8 @@ cudaError_t launch_dequant(int fmt, const uint8_t* Wq, const uint16_t* scales, c
 // INT8 load-time quantizer (quantize.cu).
 cudaError_t launch_quantize_int8_pc(const uint16_t* W, int8_t* Wq, float* scales, int64_t N, int64_t K,
                                     cudaStream_t s);
+// Load-time INT4 repack (quantize.cu): N x K/8 words, in place allowed.
+cudaError_t launch_repack_int4(const uint8_t* Wq, uint8_t* Wr, int64_t N, int64_t K, cudaStream_t s);
 
 // Plan cache (plan.cu).
 Plan plan_lookup(int op, int64_t M, int64_t N, int64_t K, cudaStream_t s);

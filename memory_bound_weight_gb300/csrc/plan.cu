@@ -53,7 +53,7 @@ static int simt_want_mb(int64_t M) { return M <= 2 ? (int)M : M <= 4 ? 4 : 8; }
 
 static int batch_key(int op, int64_t M) {
     if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 8) return tc_batch_tile(M);
-    if (op == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4) return 1000 + tc_awq_batch_tile(M);
+    if ((op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4) return 1000 + tc_awq_batch_tile(M);
     return (int)std::min<int64_t>(M, 8);
 }
 
@@ -70,9 +70,13 @@ static int64_t kblocks(int fmt, int64_t K) {
     return (K + BK - 1) / BK;
 }
 
-// `fuse`: the MBW_FUSE_* bits of the call. Fused calls run on the "mma2" and
+// `flags`: the MBW_FUSE_* and MBW_REPACKED bits of the call. Repacked INT4
+// codes run on every pair-based tensor-core kernel (they stage x as loaded);
+// the SIMT kernels read canonical codes. Fused calls run on the "mma2" and
 // latency families only (the kernels with the prologue and epilogue hooks).
-static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K, int fuse = 0) {
+static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K, int flags = 0) {
+    const int fuse = flags & MBW_FUSE_MASK;
+    if ((flags & MBW_REPACKED) && p.kind == PLAN_SIMT) return false;
     if (p.split < 1 || p.split > 8) return false;
     const int glu = (fuse & MBW_FUSE_GLU) ? 1 : 0;
     if (fuse && p.kind != PLAN_MMA2 && p.kind != PLAN_LAT) return false;
@@ -151,65 +155,67 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K, 
 static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
     std::vector<Plan> out;
     const int fmt = fmt_of_op(op);
-    const int fuse = op & MBW_FUSE_MASK;
+    const int flags = op & (MBW_FUSE_MASK | MBW_REPACKED);
     const int64_t Mb = std::min<int64_t>(M, 8);
-    if (op == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4)
+    if ((op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4)
         for (int sp = 1; sp <= 8; ++sp) {
             Plan p{PLAN_TC, 0, sp, 1};
-            if (plan_valid(fmt, p, M, N, K, fuse)) out.push_back(p);
+            if (plan_valid(fmt, p, M, N, K, flags)) out.push_back(p);
         }
     if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 8)
         for (int cfg = 0; cfg <= 3; ++cfg)
             for (int sp = 1; sp <= 8; ++sp) {
                 Plan p{PLAN_TC, cfg, sp, 1};
-                if (plan_valid(fmt, p, M, N, K, fuse)) out.push_back(p);
+                if (plan_valid(fmt, p, M, N, K, flags)) out.push_back(p);
             }
     const int splits[4] = {1, 2, 4, 8};
     for (int cfg = 0; cfg < mma_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si)
             for (int occ = 1; occ <= 2; ++occ) {
                 Plan p{PLAN_MMA, cfg, splits[si], occ};
-                if (plan_valid(fmt, p, Mb, N, K, fuse)) out.push_back(p);
+                if (plan_valid(fmt, p, Mb, N, K, flags)) out.push_back(p);
             }
     for (int cfg = 0; cfg < mma2_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si)
             for (int occ = 1; occ <= 2; ++occ) {
                 Plan p{PLAN_MMA2, cfg, splits[si], occ};
-                if (plan_valid(fmt, p, Mb, N, K, fuse)) out.push_back(p);
+                if (plan_valid(fmt, p, Mb, N, K, flags)) out.push_back(p);
             }
     for (int cfg = 0; cfg < lat_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si)
             for (int occ = 1; occ <= 2; ++occ) {
                 Plan p{PLAN_LAT, cfg, splits[si], occ};
-                if (plan_valid(fmt, p, Mb, N, K, fuse)) out.push_back(p);
+                if (plan_valid(fmt, p, Mb, N, K, flags)) out.push_back(p);
             }
     for (int cfg = 0; cfg < tma_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si)
             for (int occ = 1; occ <= 2; ++occ) {
                 Plan p{PLAN_TMA, cfg, splits[si], occ};
-                if (plan_valid(fmt, p, Mb, N, K, fuse)) out.push_back(p);
+                if (plan_valid(fmt, p, Mb, N, K, flags)) out.push_back(p);
             }
     for (int cfg = 0; cfg < simt_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si) {
             Plan p{PLAN_SIMT, cfg, splits[si], 1};
-            if (plan_valid(fmt, p, Mb, N, K, fuse)) out.push_back(p);
+            if (plan_valid(fmt, p, Mb, N, K, flags)) out.push_back(p);
         }
     return out;
 }
 
 Plan plan_default(int op, int64_t M, int64_t N, int64_t K) {
     const int fmt = fmt_of_op(op);
+    const int flags = op & (MBW_FUSE_MASK | MBW_REPACKED);
     const int fuse = op & MBW_FUSE_MASK;
     const int64_t Mb = std::min<int64_t>(M, 8);
     const int sms = device_sm_count();
-    if ((op == MBW_OP_GEMM_SKINNY_BF16 && M > 8) || (op == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4)) {
+    if ((op == MBW_OP_GEMM_SKINNY_BF16 && M > 8) ||
+        ((op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4)) {
         // tcgen05 tiles of 128 weight rows; split K over a cluster until the
         // tiles cover the SMs
         const int64_t tiles = (N + 127) / 128;
         int split = 1;
         while (split < 8 && tiles * (split + 1) <= sms) ++split;
         Plan p{PLAN_TC, 0, split, 1};
-        while (!plan_valid(fmt, p, M, N, K, fuse) && p.split > 1) --p.split;
+        while (!plan_valid(fmt, p, M, N, K, flags) && p.split > 1) --p.split;
         return p;
     }
     if (fmt == FMT_I8 || fuse) {
@@ -219,8 +225,8 @@ Plan plan_default(int op, int64_t M, int64_t N, int64_t K) {
         const int64_t tiles = (N + 15) / 16;
         Plan p{PLAN_MMA2, 1, 1, 1};
         while (p.split < 8 && tiles * p.split < sms && (int64_t)8 * p.split * 2 <= K / 128) p.split *= 2;
-        while (!plan_valid(fmt, p, Mb, N, K, fuse) && p.split > 1) p.split /= 2;
-        if (plan_valid(fmt, p, Mb, N, K, fuse)) return p;
+        while (!plan_valid(fmt, p, Mb, N, K, flags) && p.split > 1) p.split /= 2;
+        if (plan_valid(fmt, p, Mb, N, K, flags)) return p;
         const std::vector<Plan> c = candidates(op, M, N, K);
         if (!c.empty()) return c.front();
         return p;
@@ -240,8 +246,8 @@ Plan plan_default(int op, int64_t M, int64_t N, int64_t K) {
     int split = 1;
     while (split < 8 && tiles * split < sms && (int64_t)8 * split * 2 <= KB) split *= 2;
     Plan p{PLAN_MMA, cfg, split, 1};
-    while (!plan_valid(fmt, p, Mb, N, K, fuse) && p.split < 8) p.split *= 2;
-    if (plan_valid(fmt, p, Mb, N, K, fuse)) return p;
+    while (!plan_valid(fmt, p, Mb, N, K, flags) && p.split < 8) p.split *= 2;
+    if (plan_valid(fmt, p, Mb, N, K, flags)) return p;
     const std::vector<Plan> c = candidates(op, M, N, K);
     if (!c.empty()) return c.front();
     return Plan{PLAN_MMA, cfg, 8, 1};
@@ -309,12 +315,14 @@ std::string plan_to_string(int op, const Plan& p) {
     if (op & MBW_FUSE_NORM) out += " +rmsnorm";
     if (op & MBW_FUSE_GLU) out += " +swiglu";
     if (op & MBW_FUSE_RESIDUAL) out += " +residual";
+    if (op & MBW_REPACKED) out += " codes=repacked";
     return out;
 }
 
 cudaError_t launch_plan(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
     if (p.kind == PLAN_TC && fmt == FMT_AWQ)
-        return launch_gemm_tc_awq(a.W, a.scales, a.zeros, a.x, a.y, a.M, a.N, a.K, p.split, a.out_f32, s);
+        return launch_gemm_tc_awq(a.W, a.scales, a.zeros, a.x, a.y, a.M, a.N, a.K, p.split, a.out_f32, a.x_natural,
+                                  s);
     if (p.kind == PLAN_TC) return launch_gemm_tc(a.x, (const uint16_t*)a.W, a.y, a.M, a.N, a.K, p.split, p.cfg, a.out_f32, s);
     if (p.kind == PLAN_MMA2) return launch_gemv_mma2(fmt, p, a, s);
     if (p.kind == PLAN_LAT) return launch_gemv_lat(fmt, p, a, s);
@@ -332,9 +340,11 @@ static size_t weight_bytes(int fmt, int64_t N, int64_t K) {
 }
 
 static bool shape_ok(int op, int64_t M, int64_t N, int64_t K) {
-    const int base = op & MBW_OP_BASE_MASK, fuse = op & ~MBW_OP_BASE_MASK;
+    const int base = op & MBW_OP_BASE_MASK, flags = op & ~MBW_OP_BASE_MASK;
     if (base < MBW_OP_GEMV_BF16 || base > MBW_OP_GEMV_INT8_PC) return false;
-    if (fuse & ~MBW_FUSE_MASK) return false;
+    if (flags & ~(MBW_FUSE_MASK | MBW_REPACKED)) return false;
+    const int fuse = flags & MBW_FUSE_MASK;
+    if ((flags & MBW_REPACKED) && (base != MBW_OP_GEMV_INT4_AWQ_G128 || fuse)) return false;
     if (fuse && base != MBW_OP_GEMV_BF16 && base != MBW_OP_GEMV_INT4_G64 && base != MBW_OP_GEMV_INT8_PC) return false;
     if (M < 1 || N < 1 || K < 1 || N > 0x7FFFFFFF || K > 0x7FFFFFFF || M > 0x7FFFFFFF) return false;
     if (base == MBW_OP_GEMV_INT4_G64 && M != 1) return false;
@@ -461,6 +471,7 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
         a.norm_eps = 1e-6f;
         a.residual = rbuf;
         a.glu = glu;
+        a.x_natural = (op & MBW_REPACKED) ? 1 : 0;
         const size_t codes = fmt == FMT_BF16 ? (size_t)N * K * 2 : fmt == FMT_I8 ? (size_t)N * K : (size_t)N * K / 2;
         const int slices = (int)((Mb + a.M - 1) / a.M);  // launches per call at this batch
         cudaGraph_t g = nullptr;

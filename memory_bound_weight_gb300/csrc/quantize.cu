@@ -1,4 +1,6 @@
-// quantize.cu -- load-time quantizer of BF16 weights to symmetric INT8 with
+// quantize.cu -- load-time weight transforms.
+//
+// Quantizer of BF16 weights to symmetric INT8 with
 // one fp32 scale per output channel (TileInfer, "Pushing further with
 // cheating: INT8 quantization": codes in [-127, 127], scale = max|w| / 127,
 // every entry rounded to the nearest multiple of the scale).
@@ -47,7 +49,41 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_int8_pc_kernel(const u
     }
 }
 
+// Load-time INT4 repack (llm-rs vs vLLM, sec. 6 on Marlin: 4-bit weights
+// reordered once at load time so the unpack hands the multiply its operands
+// directly). In each 32-bit word of 8 codes (k = 8w + j in nibble slot j) the
+// even-k nibbles move to slots 0-3 and the odd-k nibbles to slots 4-7, each in
+// k order; the unpack's masks (bits 0-3 with 16-19, then 4-7 with 20-23, ...)
+// then give the pairs (k0, k1), (k2, k3), ... in order.
+__device__ __forceinline__ uint32_t repack_word(uint32_t v) {
+    uint32_t e = v & 0x0F0F0F0Fu, o = (v >> 4) & 0x0F0F0F0Fu;  // even / odd k, one per byte
+    e = (e | (e >> 4)) & 0x00FF00FFu;
+    o = (o | (o >> 4)) & 0x00FF00FFu;
+    e = (e | (e >> 8)) & 0x0000FFFFu;
+    o = (o | (o >> 8)) & 0x0000FFFFu;
+    return e | (o << 16);
+}
+
+// One word per thread and step; in place is fine (each word is read before
+// the same thread writes it).
+__global__ void repack_int4_kernel(const uint32_t* in, uint32_t* out, int64_t nwords) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nwords;
+         i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = repack_word(in[i]);
+}
+
 }  // namespace
+
+cudaError_t launch_repack_int4(const uint8_t* Wq, uint8_t* Wr, int64_t N, int64_t K, cudaStream_t s) {
+    const int64_t nwords = N * (K / 8);
+    if (nwords <= 0) return cudaSuccess;
+    const int64_t blocks = (nwords + 255) / 256;
+    const int64_t cap = (int64_t)device_sm_count() * 16;
+    count_launch();
+    repack_int4_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(
+        reinterpret_cast<const uint32_t*>(Wq), reinterpret_cast<uint32_t*>(Wr), nwords);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_int8_pc(const uint16_t* W, int8_t* Wq, float* scales, int64_t N, int64_t K,
                                     cudaStream_t s) {

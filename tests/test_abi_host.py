@@ -117,6 +117,16 @@ A16c = 0x30000
     (lambda L: L.mbw_quantize_int8_pc(A16, A16b, A16c, 0, 64, None), 0),
     (lambda L: L.mbw_dequant_int4_g64(A16, A16b, A16c, 4, 100, None), 3),
     (lambda L: L.mbw_dequant_int4_awq_g128(A16, A16b, None, A16c, 4, 128, None), 1),
+    (lambda L: L.mbw_repack_int4(A16, A16b, 8, 60, None), 3),   # K % 8
+    (lambda L: L.mbw_repack_int4(None, A16b, 8, 64, None), 1),
+    (lambda L: L.mbw_repack_int4(A16 + 2, A16b, 8, 64, None), 2),
+    (lambda L: L.mbw_repack_int4(A16, A16b + 1, 8, 64, None), 2),
+    (lambda L: L.mbw_repack_int4(A16, A16b, 0, 64, None), 0),
+    (lambda L: L.mbw_repack_int4(A16, A16b, 8, -64, None), 1),
+    (lambda L: L.gemv_int4_awq_g128_repacked(A16 + 16, A16b, A16c, A16c, A16, 1, 8, 256, None, 0, None), 2),
+    (lambda L: L.gemv_int4_awq_g128_repacked(A16, A16b, A16c, A16c, A16, 1, 8, 192, None, 0, None), 3),
+    (lambda L: L.gemv_int4_awq_g128_repacked(A16, A16b, None, A16c, A16, 1, 8, 256, None, 0, None), 1),
+    (lambda L: L.gemv_int4_awq_g128_repacked(A16, A16b, A16c, A16c, A16, 0, 8, 256, None, 0, None), 0),
     (lambda L: L.mbw_set_output_fp32(2), 1),
     (lambda L: L.mbw_plan_select(9, 1, 8, 64, 0), 1),
     (lambda L: L.mbw_autotune(9, 1, 8, 64, None), 1),
@@ -148,7 +158,22 @@ def test_planner_host_logic(L):
             assert L.mbw_plan_describe(op, 1, 2048, 2048, buf, 256) == 0
             assert buf.value.split()[0] in (b"mma2", b"lat") and b"+" in buf.value
     assert L.mbw_plan_candidates(3 | 0x100, 1, 2048, 2048) == 0  # no fused AWQ
-    assert L.mbw_plan_candidates(5 | 0x800, 1, 2048, 2048) == 0  # unknown fusion bit
+    assert L.mbw_plan_candidates(5 | 0x1000, 1, 2048, 2048) == 0  # unknown flag bit
+    # repacked INT4 codes (AWQ only): the tensor-core families, never the SIMT ones
+    assert L.mbw_plan_candidates(5 | 0x800, 1, 2048, 2048) == 0
+    assert L.mbw_plan_candidates(2 | 0x800, 1, 2048, 2048) == 0
+    assert L.mbw_plan_candidates(3 | 0x800 | 0x100, 1, 2048, 2048) == 0
+    for M, N, K in ((1, 3584, 18944), (3, 4608, 3584), (16, 18944, 3584), (64, 3584, 3584)):
+        n = L.mbw_plan_candidates(3 | 0x800, M, N, K)
+        assert 1 <= n < L.mbw_plan_candidates(3, M, N, K)
+        kinds = set()
+        for i in range(n):
+            assert L.mbw_plan_select(3 | 0x800, M, N, K, i) == 0
+            assert L.mbw_plan_describe(3 | 0x800, M, N, K, buf, 256) == 0
+            assert buf.value.endswith(b" codes=repacked")
+            kinds.add(buf.value.split()[0])
+        assert b"simt" not in kinds
+        assert (b"tcgen05" in kinds) == (M > 4)
     buf = ctypes.create_string_buffer(256)
     assert L.mbw_plan_describe(5, 1, 9728, 2560, buf, 256) == 0 and b"int8_pc" in buf.value
     assert L.mbw_workspace_bytes(1, 1, 2048, 2048) == 0
