@@ -10,7 +10,8 @@ from __future__ import annotations
 
 import argparse
 
-OPS = {"bf16": 1, "int4_g64": 2, "int4_awq_g128": 3, "skinny_bf16": 4, "int8_pc": 5}
+OPS = {"bf16": 1, "int4_g64": 2, "int4_awq_g128": 3, "skinny_bf16": 4, "int8_pc": 5,
+       "int4_awq_g128_repacked": 3 | 0x800}
 
 
 def main():
@@ -59,7 +60,10 @@ def main():
         c = ig.int4_codes(0, 0, N, K)
         s = ig.f16_group_scales(0, 0, N, K // 128)
         z = ig.u4_zero_points(0, 0, N, K // 128)
-        call = lambda: mbw.gemv_int4_awq_g128(c, s, z, X)  # noqa: E731
+        rp = bool(op & mbw.REPACKED)
+        if rp:
+            mbw.repack_int4(c, out=c)  # the load-time reorder, once
+        call = lambda: mbw.gemv_int4_awq_g128(c, s, z, X, repacked=rp)  # noqa: E731
     for _ in range(a.warmup + a.reps):
         call()
     torch.cuda.synchronize()
