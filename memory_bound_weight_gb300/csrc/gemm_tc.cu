@@ -162,7 +162,10 @@ __global__ void __launch_bounds__(192, 1)
     const int ks0 = rank * a.kstages;
     const int nks = max(0, min(KS, ks0 + a.kstages) - ks0);
 
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)D * STAGE);
+    // barriers after the ring and after the split-K partial tile that reuses it
+    // (a commit may still land on a ring barrier while the epilogue writes partials)
+    const size_t ring_bytes = max((size_t)D * STAGE, S > 1 ? (size_t)NT * 128 * 4 : (size_t)0);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + ring_bytes);
     uint64_t* empty = full + D;
     uint64_t* accum = empty + D;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
@@ -337,6 +340,251 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 1) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(TMEM_COLS));
+    }
+}
+
+// ----------------------------------------------------------------------------
+// CTA-pair variant for batch tiles of 128 and 256 (tcgen05.mma cta_group::2:
+// M = 256 across the two SMs of a pair). Each CTA of the pair stages its own
+// 128 weight rows and its half of the batch tile's X rows; the even CTA
+// issues one MMA for the pair, which reads A (W) from each CTA's own shared
+// memory and B (X) split by batch halves, and leaves each CTA's 128 rows x NT
+// outputs in that CTA's TMEM. At large batch X is two thirds of a one-CTA
+// stage; halving it fits more stages of the weight stream in the ring and
+// halves the X traffic out of L2.
+// Cluster rank r: member r & 1 of the pair, split-K rank r >> 1 (clusters of
+// 2 S CTAs). Both CTAs' loads of a stage complete on the even CTA's full
+// barrier; the even CTA's commits release both CTAs' ring slots and
+// accumulators (multicast). Every wait is bounded.
+__device__ __forceinline__ uint32_t tc_cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void tc_cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int NT, int C, int BPS>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX,
+                    const TcArgs a, const int S, const int D) {
+    constexpr int NH = NT / 2;  // X rows this CTA stages
+    constexpr int NTP = NT <= 128 ? 128 : 256;
+    constexpr int TMEM_COLS = NTP * C;
+    static_assert(TMEM_COLS <= 512 && (NT == 128 || NT == 256), "");
+    constexpr uint32_t A_BYTES = 128 * 128;  // 128 rows x 64 bf16 (one box)
+    constexpr uint32_t B_BYTES = NH * 128;   // NH rows x 64 bf16 (one box)
+    constexpr uint32_t STAGE = BPS * (A_BYTES + B_BYTES);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    pdl_launch_dependents();
+    prefetch_l2_grid_share(a.xpf, a.xpf_bytes);
+
+    const uint32_t crank = tc_cluster_rank();
+    const int member = (int)(crank & 1u), krank = (int)(crank >> 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = (blockIdx.x / (2 * S)) * 256 + member * 128;
+    const int KS = (a.K + 64 * BPS - 1) / (64 * BPS);
+    const int ks0 = krank * a.kstages;
+    const int nks = max(0, min(KS, ks0 + a.kstages) - ks0);
+    const uint16_t pair_mask = (uint16_t)(3u << (2 * krank));
+
+    // barriers after the ring and after the split-K partial tile that reuses it
+    const size_t ring_bytes = max((size_t)D * STAGE, S > 1 ? (size_t)NT * 128 * 4 : (size_t)0);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + ring_bytes);  // the even CTA's count both halves
+    uint64_t* empty = full + D;
+    uint64_t* accum = empty + D;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < D; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&full[s])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&empty[s])));
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(accum)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        // one warp of each CTA of the pair, collectively
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tc_smem(tmem_slot)),
+                     "n"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    // the peer's barriers exist before any remote arrive or multicast commit reaches them
+    tc_cluster_sync_all();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer ----
+        // Both CTAs' loads complete on the even CTA's full barriers (the
+        // .cta_group::2 form may name the peer's barrier); the even CTA
+        // expects the bytes of both halves of a stage.
+        const bool leader = tc_elect();
+        const int xrow = a.m0 + member * NH;
+        const int npre = min(D, nks);
+        uint32_t fbar0;  // full[0] of the even CTA
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(fbar0) : "r"(tc_smem(full)), "r"(crank & ~1u));
+        auto tma2 = [&](void* dst, const CUtensorMap* map, int c0, int c1, int s) {
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, "
+                "{%2, %3}], [%4];" ::"r"(tc_smem(dst)),
+                "l"(map), "r"(c0), "r"(c1), "r"(fbar0 + 8u * s)
+                : "memory");
+        };
+        if (leader)
+            for (int i = 0; i < npre; ++i) {
+                if (member == 0)
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc_smem(&full[i])),
+                                 "r"(2 * STAGE)
+                                 : "memory");
+                for (int bb = 0; bb < BPS; ++bb)
+                    tma2(smem + (size_t)i * STAGE + bb * A_BYTES, &mapW, ((ks0 + i) * BPS + bb) * 64, row0, i);
+            }
+        __syncwarp();
+        pdl_wait();
+        if (leader)
+            for (int i = 0; i < npre; ++i)
+                for (int bb = 0; bb < BPS; ++bb)
+                    tma2(smem + (size_t)i * STAGE + BPS * A_BYTES + bb * B_BYTES, &mapX, ((ks0 + i) * BPS + bb) * 64,
+                         xrow, i);
+        __syncwarp();
+        for (int i = npre; i < nks; ++i) {
+            const int s = i % D;
+            if (!tc_wait_warp(&empty[s], ((i / D) - 1) & 1)) break;
+            uint8_t* st = smem + (size_t)s * STAGE;
+            if (leader) {
+                if (member == 0)
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc_smem(&full[s])),
+                                 "r"(2 * STAGE)
+                                 : "memory");
+                for (int bb = 0; bb < BPS; ++bb) {
+                    const int kc = ((ks0 + i) * BPS + bb) * 64;
+                    tma2(st + bb * A_BYTES, &mapW, kc, row0, s);
+                    tma2(st + BPS * A_BYTES + bb * B_BYTES, &mapX, kc, xrow, s);
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------- MMA issuer (even CTA) ----
+        const bool leader = tc_elect();
+        if (member == 0) {
+            bool ok = true;
+            const uint32_t idesc = tc_idesc(256, NT);
+            for (int i = 0; i < nks; ++i) {
+                const int s = i % D;
+                if (ok) ok = tc_wait_warp(&full[s], (i / D) & 1);
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (ok && leader) {
+                    const uint32_t sa = tc_smem(smem + (size_t)s * STAGE);
+#pragma unroll
+                    for (int bb = 0; bb < BPS; ++bb) {
+                        const uint64_t da = tc_desc(sa + bb * A_BYTES), db = tc_desc(sa + BPS * A_BYTES + bb * B_BYTES);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int t = (i * BPS + bb) * 4 + k;  // k-step; accumulator t % C
+                            asm volatile(
+                                "{\n\t.reg .pred p;\n\t"
+                                "setp.ne.b32 p, %4, 0;\n\t"
+                                "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+                                    tmem + (uint32_t)((t % C) * NTP)),
+                                "l"(da + 2 * k), "l"(db + 2 * k), "r"(idesc), "r"((t >= C) ? 1u : 0u)
+                                : "memory");
+                        }
+                    }
+                }
+                // release the stage in both CTAs once these MMAs have read it (also on error)
+                if (leader)
+                    asm volatile(
+                        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+                        "[%0], %1;" ::"r"(tc_smem(&empty[s])),
+                        "h"(pair_mask)
+                        : "memory");
+                __syncwarp();
+            }
+            if (leader)
+                asm volatile(
+                    "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+                    "[%0], %1;" ::"r"(tc_smem(accum)),
+                    "h"(pair_mask)
+                    : "memory");
+            __syncwarp();
+        }
+    } else {
+        // ----------------------------------------------------- epilogue ----
+        const bool ok = tc_wait(accum, 0);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        const int lrow = quarter * 32 + lane;
+        float* part = reinterpret_cast<float*>(smem);  // [NT][128] fp32 partials (ring reused)
+#pragma unroll 1
+        for (int c = 0; c < NT; c += 16) {
+            float fs[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) fs[j] = 0.f;
+            uint32_t v[C][16];
+#pragma unroll
+            for (int ch = 0; ch < C; ++ch) {
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ch * NTP + c);
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+                    "[%16];"
+                    : "=r"(v[ch][0]), "=r"(v[ch][1]), "=r"(v[ch][2]), "=r"(v[ch][3]), "=r"(v[ch][4]), "=r"(v[ch][5]),
+                      "=r"(v[ch][6]), "=r"(v[ch][7]), "=r"(v[ch][8]), "=r"(v[ch][9]), "=r"(v[ch][10]),
+                      "=r"(v[ch][11]), "=r"(v[ch][12]), "=r"(v[ch][13]), "=r"(v[ch][14]), "=r"(v[ch][15])
+                    : "r"(taddr));
+            }
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int ch = 0; ch < C; ++ch) {
+                if (ch < nks * 4 * BPS) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) fs[j] += __uint_as_float(v[ch][j]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float f = (ok && nks > 0) ? fs[j] : 0.f;
+                const int m = c + j;
+                if (S == 1) {
+                    if (a.m0 + m < a.M && row0 + lrow < a.N)
+                        store_out(a.y, (int64_t)(a.m0 + m) * a.N + row0 + lrow, f, a.out_f32);
+                } else {
+                    part[m * 128 + lrow] = f;
+                }
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+
+    if (S > 1) {
+        // the split-K ranks of this CTA's rows are cluster ranks 2 kr + member
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        float* part = reinterpret_cast<float*>(smem);
+        const int total = NT * 128;
+        const int lo = krank * total / S, hi = (krank + 1) * total / S;
+        for (int e = lo + (int)threadIdx.x; e < hi; e += 192) {
+            const int m = e / 128, r = e % 128;
+            float v = 0.f;
+            for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(part + e, 2 * s + member);
+            if (a.m0 + m < a.M && row0 + r < a.N) store_out(a.y, (int64_t)(a.m0 + m) * a.N + row0 + r, v, a.out_f32);
+        }
+        cluster.sync();
+    } else {
+        // both CTAs are done with the pair's TMEM before it is released
+        tc_cluster_sync_all();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(TMEM_COLS));
     }
 }
 
@@ -845,6 +1093,49 @@ size_t tc_smem_bytes(int nt, int D, int split, int bps) {
     return 1024 + ring + (size_t)(2 * D + 1) * 8 + 16;
 }
 
+// CTA-pair kernel: a CTA stages 128 W rows and nt/2 X rows per box.
+static int tc2_stages(int nt, int ring, int bps) {
+    const size_t stage = (128 * 128 + (size_t)(nt / 2) * 128) * bps;
+    int d = (int)(((ring == 0 ? 180 : 96) * 1024) / stage);
+    if (d > 8) d = 8;
+    if (d < 2) d = 2;
+    return d;
+}
+
+static size_t tc2_smem_bytes(int nt, int D, int split, int bps) {
+    const size_t stage = (128 * 128 + (size_t)(nt / 2) * 128) * bps;
+    size_t ring = (size_t)D * stage;
+    const size_t part = (size_t)nt * 128 * 4;
+    if (split > 1 && part > ring) ring = part;
+    return 1024 + ring + (size_t)(2 * D + 1) * 8 + 16;
+}
+
+template <int NT, int C, int BPS>
+static cudaError_t launch_nt2(const CUtensorMap& mw, const CUtensorMap& mx, const TcArgs& a, int split, int ring,
+                              int tiles, cudaStream_t s) {
+    const int D = tc2_stages(NT, ring, BPS);
+    const size_t smem = tc2_smem_bytes(NT, D, split, BPS);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc2_kernel<NT, C, BPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((tiles + 1) / 2 * 2 * split), 1, 1);
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = (unsigned)(2 * split);
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 2;
+    count_launch();
+    return cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<NT, C, BPS>, mw, mx, a, split, D);
+}
+
 template <int NT, int C, int BPS>
 static cudaError_t launch_nt(const CUtensorMap& mw, const CUtensorMap& mx, const TcArgs& a, int split, int ring,
                              int tiles, cudaStream_t s) {
@@ -877,14 +1168,16 @@ static cudaError_t launch_nt(const CUtensorMap& mw, const CUtensorMap& mx, const
 }
 
 // Y[M][N] = X[M][K] . W[N][K]^T, bf16, in batch slices of up to 256 rows.
-// cfg bit 0: ring (0 deep, 1 co-resident); bit 1: two 64-k boxes per stage.
+// cfg bit 0: ring (0 deep, 1 co-resident); bit 1: two 64-k boxes per stage;
+// bit 2: CTA pairs (batch tiles 128 and 256, split_k <= 4).
 cudaError_t launch_gemm_tc(const uint16_t* X, const uint16_t* W, void* Y, int64_t M, int64_t N, int64_t K, int split,
                            int cfg_, int out_f32, cudaStream_t s) {
-    const int ring = cfg_ & 1, bps = (cfg_ & 2) ? 2 : 1;
+    const int ring = cfg_ & 1, bps = (cfg_ & 2) ? 2 : 1, pair = (cfg_ & 4) ? 1 : 0;
     const int nt = tc_batch_tile(M);
+    if (pair && (nt < 128 || split > 4)) return cudaErrorInvalidValue;
     CUtensorMap mw, mx;
     if (!encode_2d(&mw, W, (uint64_t)K, (uint64_t)N, 64, 128)) return cudaErrorInvalidValue;
-    if (!encode_2d(&mx, X, (uint64_t)K, (uint64_t)M, 64, (uint32_t)nt)) return cudaErrorInvalidValue;
+    if (!encode_2d(&mx, X, (uint64_t)K, (uint64_t)M, 64, (uint32_t)(pair ? nt / 2 : nt))) return cudaErrorInvalidValue;
     const int tiles = (int)((N + 127) / 128);
     const int KS = (int)((K + 64 * bps - 1) / (64 * bps));
     if (split < 1) split = 1;
@@ -908,13 +1201,26 @@ cudaError_t launch_gemm_tc(const uint16_t* X, const uint16_t* W, void* Y, int64_
                               : launch_nt<NT_, C0, 1>(mw, mx, a, split, ring, tiles, s))                 \
                   : (bps == 2 ? launch_nt<NT_, C1, 2>(mw, mx, a, split, ring, tiles, s)                  \
                               : launch_nt<NT_, C1, 1>(mw, mx, a, split, ring, tiles, s))
-        switch (nt) {
-            case 16: MBW_TC(16, 4, 4); break;
-            case 32: MBW_TC(32, 4, 4); break;
-            case 64: MBW_TC(64, 4, 2); break;
-            case 128: MBW_TC(128, 4, 2); break;
-            default: MBW_TC(256, 2, 1); break;
+#define MBW_TC2(NT_, C0, C1)                                                                             \
+    e = ring == 0 ? (bps == 2 ? launch_nt2<NT_, C0, 2>(mw, mx, a, split, ring, tiles, s)                 \
+                              : launch_nt2<NT_, C0, 1>(mw, mx, a, split, ring, tiles, s))                \
+                  : (bps == 2 ? launch_nt2<NT_, C1, 2>(mw, mx, a, split, ring, tiles, s)                 \
+                              : launch_nt2<NT_, C1, 1>(mw, mx, a, split, ring, tiles, s))
+        if (pair) {
+            if (nt == 128)
+                MBW_TC2(128, 4, 2);
+            else
+                MBW_TC2(256, 2, 1);
+        } else {
+            switch (nt) {
+                case 16: MBW_TC(16, 4, 4); break;
+                case 32: MBW_TC(32, 4, 4); break;
+                case 64: MBW_TC(64, 4, 2); break;
+                case 128: MBW_TC(128, 4, 2); break;
+                default: MBW_TC(256, 2, 1); break;
+            }
         }
+#undef MBW_TC2
 #undef MBW_TC
         if (e != cudaSuccess) return e;
     }

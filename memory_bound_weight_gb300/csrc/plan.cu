@@ -89,8 +89,10 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K, 
             const int64_t per = ((G + p.split - 1) / p.split + 3) / 4 * 4;  // whole 4-group ring slots per rank
             return per * (p.split - 1) < G && tc_awq_fits(M, K, p.split);
         }
-        // cfg bit 0: ring (deep / co-resident), bit 1: two 64-k boxes per stage
-        if (fmt != FMT_BF16 || M <= 8 || p.cfg < 0 || p.cfg > 3 || p.occ != 1) return false;
+        // cfg bit 0: ring (deep / co-resident), bit 1: two 64-k boxes per stage, bit 2: CTA pairs
+        // (batches 5 .. 8 run in a 16-wide tile: the tensor-core kernel can still beat the GEMVs)
+        if (fmt != FMT_BF16 || M <= 4 || p.cfg < 0 || p.cfg > 7 || p.occ != 1) return false;
+        if ((p.cfg & 4) && (tc_batch_tile(M) < 128 || p.split > 4)) return false;
         const int64_t bk = (p.cfg & 2) ? 128 : 64;
         const int64_t KS = (K + bk - 1) / bk;
         if (p.split > KS) return false;
@@ -162,8 +164,8 @@ static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
             Plan p{PLAN_TC, 0, sp, 1};
             if (plan_valid(fmt, p, M, N, K, flags)) out.push_back(p);
         }
-    if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 8)
-        for (int cfg = 0; cfg <= 3; ++cfg)
+    if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 4)
+        for (int cfg = 0; cfg <= 7; ++cfg)
             for (int sp = 1; sp <= 8; ++sp) {
                 Plan p{PLAN_TC, cfg, sp, 1};
                 if (plan_valid(fmt, p, M, N, K, flags)) out.push_back(p);
@@ -285,8 +287,9 @@ std::string plan_to_string(int op, const Plan& p) {
         if (fmt == FMT_AWQ)
             snprintf(buf, sizeof(buf), "tcgen05 fmt=%s tile=128xbatch k_stage=128 (one group) split_k=%d", fs, p.split);
         else
-            snprintf(buf, sizeof(buf), "tcgen05 fmt=%s tile=128xbatch k_stage=%d ring=%s split_k=%d", fs,
-                     (p.cfg & 2) ? 128 : 64, (p.cfg & 1) ? "shared_sm" : "deep", p.split);
+            snprintf(buf, sizeof(buf), "tcgen05 fmt=%s tile=%sxbatch k_stage=%d ring=%s split_k=%d", fs,
+                     (p.cfg & 4) ? "256 (cta pair)" : "128", (p.cfg & 2) ? 128 : 64,
+                     (p.cfg & 1) ? "shared_sm" : "deep", p.split);
     } else if (p.kind == PLAN_LAT) {
         const LatConfig c = lat_config(fmt, p.cfg);
         snprintf(buf, sizeof(buf),

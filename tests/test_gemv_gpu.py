@@ -273,6 +273,50 @@ def test_skinny_tcgen05_all_plans(orc, M, N, K):
     assert seen_tc
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 640, 3584), (128, 300, 2048), (200, 1000, 4096), (256, 128, 18944),
+                                   (129, 257, 1024)])
+def test_skinny_tcgen05_cta_pair_plans(orc, M, N, K):
+    """The CTA-pair kernel (cta_group::2 MMAs across two SMs): every pair plan,
+    including split-K clusters of up to 4 pairs, an odd number of 128-row tiles
+    (the last pair's second CTA reads rows past N) and partial batch tiles."""
+    W, X = bf16_case(960 + M + N, N, K, M)
+    Y, A = orc.gemm_bf16(W, X)
+    Wd, Xd = dev_bf16(W), dev_bf16(X)
+    seen = 0
+    for i, desc in each_plan(mbw.OP_GEMM_SKINNY_BF16, M, N, K):
+        if "cta pair" not in desc:
+            continue
+        seen += 1
+        y = mbw.gemm_skinny_bf16(Xd, Wd)
+        assert_parity(y, Y, A, f"skinny pair {M}x{N}x{K} plan {desc}")
+        with mbw.output_fp32():
+            y1 = mbw.gemm_skinny_bf16(Xd, Wd)
+            y2 = mbw.gemm_skinny_bf16(Xd, Wd)
+        assert torch.equal(y1, y2), desc
+    assert seen >= 4
+
+
+@pytest.mark.parametrize("N,K", [(18944, 3584), (3584, 18944)])
+def test_skinny_cta_pair_config_shapes_sampled_rows(orc, N, K):
+    """Every CTA-pair plan at the Qwen2.5-7B MLP shapes, batch 256, sampled rows."""
+    M = 256
+    rows = np.unique(np.concatenate([np.arange(0, 8), np.arange(N - 8, N),
+                                     np.random.default_rng(N + 5).integers(0, N, 48)]))
+    Wd = inputs_gpu.bf16_weights(0, 9, N, K)
+    Xd = inputs_gpu.bf16_activations(0, 10, M, K)
+    Wr = np.stack([gen.bf16_weights(0, 9, N, K, row0=int(r), rows=1)[0] for r in rows])
+    Yr, Ar = orc.gemm_bf16(Wr, host_bits16(Xd))
+    sel = torch.from_numpy(rows).cuda()
+    seen = 0
+    for i, desc in each_plan(mbw.OP_GEMM_SKINNY_BF16, M, N, K):
+        if "cta pair" not in desc:
+            continue
+        seen += 1
+        Y = mbw.gemm_skinny_bf16(Xd, Wd)
+        assert_parity(Y[:, sel], Yr, Ar, f"skinny pair M={M} {N}x{K} plan {desc}")
+    assert seen >= 4
+
+
 def test_skinny_tcgen05_deterministic_and_scaling():
     M, N, K = 64, 1024, 2048
     W, X = bf16_case(950, N, K, M)
