@@ -66,6 +66,8 @@ def parse_args():
     p.add_argument("--batch", type=int, default=1,
                    help="activation rows per GEMV (qwen_awq: AWQ-style INT4 decode at batch M)")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--ref-budget", type=float, default=None,
+                   help="--impl reference: oracle seconds per step (default: about 20 s over the whole run)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--per-matrix", action="store_true", help="also time each distinct shape on its own")
     p.add_argument("--no-shape-timing", action="store_true",
@@ -436,7 +438,7 @@ def run_reference(args, rank, ws):
     """--impl reference: the oracle, as it stands, on the host cores."""
     if rank != 0:
         return
-    per_step = max(0.5, 20.0 / max(1, args.steps + args.warmup))
+    per_step = args.ref_budget if args.ref_budget else max(0.5, 20.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         cpu_baseline(args.workload, budget_s=per_step, M=args.batch)
     t0 = time.perf_counter()
