@@ -67,6 +67,13 @@ typedef int mbw_status;
 #define MBW_ERR_CUDA 6                /* a CUDA runtime call failed */
 #define MBW_ERR_DEVICE_TIMEOUT 7      /* a device-side bounded wait gave up */
 
+/* Rounds of mbarrier.try_wait a kernel's wait makes before it gives up, sets
+ * the device fault flag and leaves its loop (the waits of the bulk-copy and
+ * tcgen05 kernels). A round that does not complete suspends for ~3.8 us on a
+ * GB300, so a stalled wait gives up after about 1 s of running time; a wait
+ * the pipeline satisfies lasts microseconds. */
+#define MBW_WAIT_LIMIT (1LL << 18)
+
 /* Operation ids for the plan / workspace queries. */
 #define MBW_OP_GEMV_BF16 1
 #define MBW_OP_GEMV_INT4_G64 2
@@ -280,6 +287,16 @@ mbw_status mbw_plan_describe(int op, int64_t M, int64_t N, int64_t K, char *buf,
 /* Read and clear the device-side error flag set by bounded waits inside
  * kernels (synchronizes the current device). MBW_OK or MBW_ERR_DEVICE_TIMEOUT. */
 mbw_status mbw_check_device_error(void);
+
+/* Self-test of the failure path above. Launches two one-thread kernels on
+ * `stream`, one per family of bounded waits (bulk-copy GEMV, tcgen05 GEMM);
+ * each waits on a shared-memory mbarrier that nothing arrives at, gives up
+ * after `tries` rounds (1 <= tries <= MBW_WAIT_LIMIT) and sets the fault flag
+ * as a stalled kernel would. It touches no memory outside the kernels' own
+ * shared memory and returns without synchronizing; the next
+ * mbw_check_device_error() then reports MBW_ERR_DEVICE_TIMEOUT and clears the
+ * flag. tries out of range: MBW_ERR_INVALID_ARG, nothing launched. */
+mbw_status mbw_selftest_wait_expiry(int64_t tries, mbw_stream_t stream);
 
 /* Number of kernel launches this library has issued on the calling thread. */
 uint64_t mbw_launch_count(void);

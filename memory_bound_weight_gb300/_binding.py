@@ -60,6 +60,7 @@ SIGNATURES = {
     "mbw_plan_index": ([ctypes.c_int, _I64, _I64, _I64], ctypes.c_int),
     "mbw_plan_describe": ([ctypes.c_int, _I64, _I64, _I64, ctypes.c_char_p, _SZ], _ST),
     "mbw_check_device_error": ([], _ST),
+    "mbw_selftest_wait_expiry": ([_I64, _P], _ST),
     "mbw_launch_count": ([], ctypes.c_uint64),
     "mbw_status_string": ([_ST], ctypes.c_char_p),
     "mbw_last_error": ([], ctypes.c_char_p),
@@ -383,3 +384,10 @@ def launch_count() -> int:
 
 def check_device_error() -> None:
     check("mbw_check_device_error", lib().mbw_check_device_error())
+
+
+def selftest_wait_expiry(tries: int) -> None:
+    """Launch, on the current stream, the two one-thread kernels whose bounded
+    waits expire after `tries` rounds; the next check_device_error() raises
+    MbwError with MBW_ERR_DEVICE_TIMEOUT."""
+    check("mbw_selftest_wait_expiry", lib().mbw_selftest_wait_expiry(int(tries), _stream_ptr(None)))

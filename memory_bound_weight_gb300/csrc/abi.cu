@@ -323,6 +323,15 @@ mbw_status mbw_check_device_error(void) {
     return MBW_OK;
 }
 
+mbw_status mbw_selftest_wait_expiry(int64_t tries, mbw_stream_t stream) {
+    if (tries < 1 || tries > MBW_WAIT_LIMIT)
+        return fail(MBW_ERR_INVALID_ARG, "mbw_selftest_wait_expiry: tries must be in [1, MBW_WAIT_LIMIT]");
+    cudaError_t e = launch_tma_wait_expiry((long long)tries, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "wait-expiry launch");
+    e = launch_tc_wait_expiry((long long)tries, (cudaStream_t)stream);
+    return e == cudaSuccess ? MBW_OK : cuda_fail(e, "wait-expiry launch");
+}
+
 uint64_t mbw_launch_count(void) { return g_launches; }
 
 const char* mbw_status_string(mbw_status s) {

@@ -36,7 +36,7 @@ namespace cg = cooperative_groups;
 namespace mbw {
 
 __device__ int g_tc_fault;
-static constexpr long long kTcSpin = 1ll << 22;
+static constexpr long long kTcSpin = MBW_WAIT_LIMIT;
 
 struct TcArgs {
     void* y;
@@ -62,8 +62,8 @@ __device__ __forceinline__ bool tc_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity) {
-    for (long long i = 0; i < kTcSpin; ++i)
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, long long limit = kTcSpin) {
+    for (long long i = 0; i < limit; ++i)
         if (tc_try_wait(bar, parity)) return true;
     atomicExch(&g_tc_fault, 1);
     return false;
@@ -1330,6 +1330,23 @@ cudaError_t launch_gemm_tc_awq(const uint8_t* Q, const uint16_t* scales, const u
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+// The expiry path of the bounded wait, run on purpose: one thread waits on an
+// mbarrier that expects one arrival that never comes. The wait gives up after
+// `tries` rounds and raises the fault flag exactly as a stalled pipeline would;
+// the kernel touches nothing outside its own shared memory.
+__global__ void tc_wait_expiry_kernel(long long tries) {
+    __shared__ __align__(8) uint64_t bar;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem(&bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    (void)tc_wait(&bar, 0, tries);
+}
+
+cudaError_t launch_tc_wait_expiry(long long tries, cudaStream_t s) {
+    tc_wait_expiry_kernel<<<1, 1, 0, s>>>(tries);
+    count_launch();
+    return cudaGetLastError();
 }
 
 int tc_take_fault() {

@@ -41,7 +41,7 @@ namespace mbw {
 
 __device__ int g_tma_fault;  // set by a bounded wait that expired
 
-static constexpr long long kSpinLimit = 1ll << 22;  // try_wait rounds before giving up
+static constexpr long long kSpinLimit = MBW_WAIT_LIMIT;  // try_wait rounds before giving up
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -64,8 +64,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait; returns false (and records the fault) if the phase never completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    for (long long i = 0; i < kSpinLimit; ++i)
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit = kSpinLimit) {
+    for (long long i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     atomicExch(&g_tma_fault, 1);
     return false;
@@ -495,6 +495,22 @@ cudaError_t launch_gemv_tma(int fmt, const Plan& p, const GemvArgs& a, cudaStrea
     cfg.numAttrs = na;
     count_launch();
     return cudaLaunchKernelEx(&cfg, e.fn, a, p.split);
+}
+
+// The expiry path of the bounded wait, run on purpose: one thread waits on an
+// mbarrier whose single expected arrival never comes, gives up after `tries`
+// rounds and raises the fault flag; nothing outside its shared memory is touched.
+__global__ void tma_wait_expiry_kernel(long long tries) {
+    __shared__ __align__(8) uint64_t bar;
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    (void)mbar_wait(&bar, 0, tries);
+}
+
+cudaError_t launch_tma_wait_expiry(long long tries, cudaStream_t s) {
+    tma_wait_expiry_kernel<<<1, 1, 0, s>>>(tries);
+    count_launch();
+    return cudaGetLastError();
 }
 
 // Read and clear the fault flag of the bounded waits (host side).

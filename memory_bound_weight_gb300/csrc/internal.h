@@ -135,6 +135,7 @@ cudaError_t launch_gemm_tc_awq(const uint8_t* Q, const uint16_t* scales, const u
 int tc_awq_batch_tile(int64_t M);
 bool tc_awq_fits(int64_t M, int64_t K, int split);  // the split leaves room for the scale/zero tables
 int tc_take_fault();
+cudaError_t launch_tc_wait_expiry(long long tries, cudaStream_t s);  // a bounded wait that expires
 
 // Bulk-copy-fed kernel tables (gemv_tma.cu).
 int tma_num_configs(int fmt);
@@ -142,6 +143,7 @@ TmaConfig tma_config(int fmt, int idx);
 size_t tma_smem_bytes(int fmt, const TmaConfig& c, int64_t N, int64_t K, int M, int split, int occ);
 cudaError_t launch_gemv_tma(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
 int tma_take_fault();  // 1 if a bounded device wait expired since the last call (and clear it)
+cudaError_t launch_tma_wait_expiry(long long tries, cudaStream_t s);  // a bounded wait that expires
 
 cudaError_t launch_dequant(int fmt, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zeros,
                            float* out, int64_t N, int64_t K, cudaStream_t s);

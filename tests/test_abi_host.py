@@ -130,6 +130,8 @@ A16c = 0x30000
     (lambda L: L.mbw_set_output_fp32(2), 1),
     (lambda L: L.mbw_plan_select(9, 1, 8, 64, 0), 1),
     (lambda L: L.mbw_autotune(9, 1, 8, 64, None), 1),
+    (lambda L: L.mbw_selftest_wait_expiry(0, None), 1),              # tries below 1
+    (lambda L: L.mbw_selftest_wait_expiry((1 << 18) + 1, None), 1),  # above the kernels' own limit
 ])
 def test_argument_errors_without_cuda(L, call, expect):
     assert call(L) == expect
