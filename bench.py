@@ -69,7 +69,8 @@ def parse_args():
     p.add_argument("--ref-budget", type=float, default=None,
                    help="--impl reference: oracle seconds per step (default: about 20 s over the whole run)")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--per-matrix", action="store_true", help="also time each distinct shape on its own")
+    p.add_argument("--per-matrix", action="store_true",
+                   help="also time each distinct shape on its own: steady state and cold (L2 flushed per call)")
     p.add_argument("--no-shape-timing", action="store_true",
                    help="skip the per-shape timing behind the dominant-kernel roofline (e.g. under a profiler)")
     p.add_argument("--tune", default="step", choices=["step", "shape"],
@@ -605,9 +606,11 @@ def main():
         shape_times = time_per_shape(step, device, shapes=step.shapes(), plans=step_plans)
     per_matrix = None
     if args.per_matrix and rank == 0:
-        per_matrix = dict(shape_times)
-        per_matrix.update(time_per_shape(step, device, shapes=[sh for sh in named_shapes(step.fmt)
-                                                               if sh not in step_plans]))
+        # steady state and cold (L2 flushed before every call), step's own plans
+        # for its shapes, autotuned plans for the named extra shapes
+        per_matrix = time_per_shape(step, device, plans=step_plans, cold_iters=100,
+                                    shapes=list(step_plans) + [sh for sh in named_shapes(step.fmt)
+                                                               if sh not in step_plans])
 
     peak, peak_src = hbm_peak()
     counts = {}
@@ -712,11 +715,16 @@ def named_shapes(fmt):
     return [(0, 2048, 2048)]
 
 
-def time_per_shape(step, device, reps=5, shapes=None, plans=None):
+def time_per_shape(step, device, reps=5, shapes=None, plans=None, cold_iters=0):
     """Steady-state time per matrix of each shape: a CUDA graph of back-to-back
     launches (programmatic dependent launch, as in the step) over distinct
     copies of the matrix totalling at least 4x the L2, so every launch reads
-    its weights from HBM; per-matrix time = graph time / launches."""
+    its weights from HBM; per-matrix time = graph time / launches.
+
+    With cold_iters > 0, also the cold figure: that many single calls, each
+    after a write of twice the L2 that evicts the matrix, each timed with CUDA
+    events on the calling stream (launch latency included, nothing overlaps);
+    median and interquartile range."""
     import torch
 
     import memory_bound_weight_gb300 as mbw
@@ -765,9 +773,37 @@ def time_per_shape(step, device, reps=5, shapes=None, plans=None):
         out[skey((fz, N, K))] = {"us": us, "GB/s": b / (us * 1e-6) / 1e9, "frac": b / (us * 1e-6) / 1e9 / peak,
                                  "TFLOP/s": wl.call_flops(M, wl.Mat("", N, K, fz)) / (us * 1e-6) / 1e12,
                                  "copies": copies, "plan": mbw.plan_describe(step.op | fz, M, N, K)}
+        if cold_iters > 0:
+            out[skey((fz, N, K))].update(time_cold(calls[0], b, peak, l2, device, cold_iters))
         del calls, g
         torch.cuda.empty_cache()
     return out
+
+
+def time_cold(call, nbytes, peak, l2, device, iters, warmup=3):
+    """Cold time of one call: before each timed call, 2x the L2 is written so
+    that the call reads its matrix from HBM."""
+    import torch
+
+    fn, a, o = call
+    flush = torch.empty((2 * l2) // 4 + 1, dtype=torch.int32, device=device)
+    ev = []
+    for it in range(warmup + iters):
+        flush.fill_(it)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn(*a, out=o)
+        e1.record()
+        if it >= warmup:
+            ev.append((e0, e1))
+    torch.cuda.synchronize()
+    ts = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev)
+    q = statistics.quantiles(ts, n=4)
+    med = statistics.median(ts)
+    del flush
+    return {"cold_us": med, "cold_iqr_us": [q[0], q[2]], "cold_frac": nbytes / (med * 1e-6) / 1e9 / peak,
+            "cold_iters": iters}
 
 
 if __name__ == "__main__":
