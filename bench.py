@@ -38,6 +38,7 @@ sys.path.insert(0, ROOT)
 from memory_bound_weight_gb300 import workloads as wl  # noqa: E402
 
 FALLBACK_HBM_GBS = 6778.3  # the machine's measured copy bandwidth, recorded copy
+NOMINAL_HBM_GBS = 7900.0  # the GB300's nominal HBM3e bandwidth (context only; fractions use the measured peak)
 FALLBACK_BF16_TFLOPS = 1752.2  # the pool's measured sustained cuBLAS bf16, recorded copy
 # DRAM bytes (read + write) per launch of the step's dominant kernel from one
 # ncu capture, keyed by (kernel source sha, shape); a changed kernel gets
@@ -684,6 +685,7 @@ def roofline_fields(step, ms_step, gbs, peak, peak_src, traffic, plans, launches
     r = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
          "traffic": traffic, "peak_source": peak_src,
          "kernel": f"{plans[key]} on the {key} matrices ({counts[dominant]} per step)",
+         "frac_of_nominal_hbm": achieved / NOMINAL_HBM_GBS, "nominal_hbm_gbs": NOMINAL_HBM_GBS,
          "bytes_alg_per_launch": kb, "us_per_launch": st["us"],
          "share_of_step": counts[dominant] * st["us"] / tot,
          "note": "per-launch time of the dominant kernel in a PDL-chained graph of its own launches over distinct "
