@@ -436,6 +436,21 @@ def cpu_baseline(workload, budget_s=10.0, M=1):
                       f"{done_bytes / 1e9:.3f} GB), fp64 C oracle, OpenMP over rows, {spent:.1f} s"}
 
 
+def cpu_baseline_single_thread(workload, M=1, budget_s=3.0):
+    """The same oracle sample on one host thread (the row loop unparallelised)."""
+    import oracle
+
+    o = oracle.load()
+    n = o.num_threads()
+    o.set_num_threads(1)
+    try:
+        r = cpu_baseline(workload, budget_s=budget_s, M=M)
+    finally:
+        o.set_num_threads(n)
+    return {"value": r["value"], "unit": r["unit"], "cores": 1, "sample": r["sample"].replace("OpenMP over rows",
+                                                                                             "one thread")}
+
+
 def run_reference(args, rank, ws):
     """--impl reference: the oracle, as it stands, on the host cores."""
     if rank != 0:
@@ -629,6 +644,7 @@ def main():
     cb = None
     if ws == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(args.workload, M=step.M)
+        cb["single_thread"] = cpu_baseline_single_thread(args.workload, M=step.M)
     line = {
         "metric": metric_name(args.workload),
         "value": value,
