@@ -125,6 +125,31 @@ def _need(t, name, dtype, ndim):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _common_device(*ts):
+    """The one device all given tensors (None skipped) are on."""
+    devs = {t.device for t in ts if t is not None}
+    if len(devs) != 1:
+        raise ValueError(f"all tensors must be on one device, got {sorted(str(d) for d in devs)}")
+    return devs.pop()
+
+
+def _on_current_device(*ts):
+    """All tensors on one CUDA device, the current one: the library plans and
+    launches on the current device, and a kernel given another device's memory
+    would fault."""
+    torch = _torch()
+    d = _common_device(*ts)
+    cur = torch.cuda.current_device()
+    if d.index != cur:
+        raise ValueError(f"tensors are on {d} but the current CUDA device is cuda:{cur} (torch.cuda.set_device)")
+    return d
+
+
+def _need_shape(t, name, shape):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
 _tls = threading.local()
 
 
@@ -172,6 +197,7 @@ def gemv_bf16(W, x, out=None, workspace=None):
     if x.shape[0] != K:
         raise ValueError("x must have length K")
     y = _alloc_out((N,), W, out)
+    _on_current_device(W, x, y, workspace)
     wp, wn = _ws(workspace)
     check("gemv_bf16", lib().gemv_bf16(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K, wp, wn,
                                        _stream_ptr(W.device)))
@@ -189,6 +215,7 @@ def gemv_int4_g64(Wq, scales, x, out=None, workspace=None):
     if Wq.shape[1] * 2 != K or tuple(scales.shape) != (N, K // 64):
         raise ValueError("shapes: Wq (N, K/2), scales (N, K/64), x (K,)")
     y = _alloc_out((N,), Wq, out)
+    _on_current_device(Wq, scales, x, y, workspace)
     wp, wn = _ws(workspace)
     check("gemv_int4_g64", lib().gemv_int4_g64(Wq.data_ptr(), scales.data_ptr(), x.data_ptr(), y.data_ptr(),
                                                N, K, wp, wn, _stream_ptr(Wq.device)))
@@ -212,6 +239,7 @@ def gemv_int4_awq_g128(Wq, scales, zeros, X, out=None, workspace=None, repacked=
     if Wq.shape[1] * 2 != K or tuple(scales.shape) != (N, G) or tuple(zeros.shape) != (N, (G + 1) // 2):
         raise ValueError("shapes: Wq (N, K/2), scales (N, K/128), zeros (N, ceil(K/256)), X (M, K)")
     Y = _alloc_out((M, N), Wq, None if out is None else (out.unsqueeze(0) if vec else out))
+    _on_current_device(Wq, scales, zeros, X2, Y, workspace)
     wp, wn = _ws(workspace)
     name = "gemv_int4_awq_g128_repacked" if repacked else "gemv_int4_awq_g128"
     check(name, getattr(lib(), name)(
@@ -229,6 +257,7 @@ def repack_int4(Wq, out=None):
     Wr = torch.empty_like(Wq) if out is None else out
     if Wr.shape != Wq.shape or Wr.dtype != torch.uint8 or not Wr.is_contiguous():
         raise ValueError("out must be a contiguous uint8 tensor of Wq's shape")
+    _on_current_device(Wq, Wr)
     check("mbw_repack_int4", lib().mbw_repack_int4(Wq.data_ptr(), Wr.data_ptr(), N, 2 * half, _stream_ptr(Wq.device)))
     return Wr
 
@@ -243,6 +272,7 @@ def gemm_skinny_bf16(X, W, out=None, workspace=None):
     if W.shape[1] != K:
         raise ValueError("W must be (N, K)")
     Y = _alloc_out((M, N), W, out)
+    _on_current_device(X, W, Y, workspace)
     wp, wn = _ws(workspace)
     check("gemm_skinny_bf16", lib().gemm_skinny_bf16(X.data_ptr(), W.data_ptr(), Y.data_ptr(), M, N, K, wp, wn,
                                                      _stream_ptr(W.device)))
@@ -262,6 +292,7 @@ def gemv_int8_pc(Wq, scales, X, out=None, workspace=None):
     if Wq.shape[1] != K or scales.shape[0] != N:
         raise ValueError("shapes: Wq (N, K), scales (N,), X (M, K)")
     Y = _alloc_out((M, N), Wq, None if out is None else (out.unsqueeze(0) if vec else out))
+    _on_current_device(Wq, scales, X2, Y, workspace)
     wp, wn = _ws(workspace)
     check("gemv_int8_pc", lib().gemv_int8_pc(Wq.data_ptr(), scales.data_ptr(), X2.data_ptr(), Y.data_ptr(), M, N, K,
                                              wp, wn, _stream_ptr(Wq.device)))
@@ -285,8 +316,10 @@ def gemv_fused(op, W, scales, X, out=None, norm_weight=None, norm_eps=1e-6, resi
     _need(W, "W", wdt, 2)
     if W.shape[1] * kdiv != K:
         raise ValueError("W does not match K")
+    sshape = None if sdt is None else ((N, K // 64) if op == OP_GEMV_INT4_G64 else (N,))
     if sdt is not None:
-        _need(scales, "scales", sdt, scales.dim())
+        _need(scales, "scales", sdt, len(sshape))
+        _need_shape(scales, "scales", sshape)
     f = MbwFusion()
     if norm_weight is not None:
         _need(norm_weight, "norm_weight", torch.bfloat16, 1)
@@ -300,7 +333,8 @@ def gemv_fused(op, W, scales, X, out=None, norm_weight=None, norm_eps=1e-6, resi
             raise ValueError("up_weights must have W's shape")
         f.up_weights = up_weights.data_ptr()
         if sdt is not None:
-            _need(up_scales, "up_scales", sdt, up_scales.dim())
+            _need(up_scales, "up_scales", sdt, len(sshape))
+            _need_shape(up_scales, "up_scales", sshape)
             f.up_scales = up_scales.data_ptr()
     Y = _alloc_out((M, N), X2, None if out is None else (out.unsqueeze(0) if vec else out))
     if residual is not None:
@@ -309,6 +343,8 @@ def gemv_fused(op, W, scales, X, out=None, norm_weight=None, norm_eps=1e-6, resi
         if tuple(r2.shape) != (M, N):
             raise ValueError("residual must be shaped like the output")
         f.residual = r2.data_ptr()
+    _on_current_device(W, scales if sdt is not None else None, X2, Y, norm_weight, residual, up_weights,
+                       up_scales if (up_weights is not None and sdt is not None) else None, workspace)
     wp, wn = _ws(workspace)
     check("gemv_fused", lib().gemv_fused(op, W.data_ptr(), None if scales is None else scales.data_ptr(),
                                          X2.data_ptr(), Y.data_ptr(), M, N, K, ctypes.byref(f), wp, wn,
@@ -321,6 +357,7 @@ def quantize_int8_pc(W):
     torch = _torch()
     _need(W, "W", torch.bfloat16, 2)
     N, K = W.shape
+    _on_current_device(W)
     Wq = torch.empty((N, K), dtype=torch.int8, device=W.device)
     sc = torch.empty((N,), dtype=torch.float32, device=W.device)
     check("mbw_quantize_int8_pc", lib().mbw_quantize_int8_pc(W.data_ptr(), Wq.data_ptr(), sc.data_ptr(), N, K,
@@ -333,6 +370,8 @@ def dequant_int4_g64(Wq, scales):
     _need(Wq, "Wq", torch.uint8, 2)
     _need(scales, "scales", torch.float16, 2)
     N, K = Wq.shape[0], Wq.shape[1] * 2
+    _need_shape(scales, "scales", (N, K // 64))
+    _on_current_device(Wq, scales)
     out = torch.empty((N, K), dtype=torch.float32, device=Wq.device)
     check("mbw_dequant_int4_g64", lib().mbw_dequant_int4_g64(Wq.data_ptr(), scales.data_ptr(), out.data_ptr(),
                                                              N, K, _stream_ptr(Wq.device)))
@@ -345,6 +384,10 @@ def dequant_int4_awq_g128(Wq, scales, zeros):
     _need(scales, "scales", torch.float16, 2)
     _need(zeros, "zeros", torch.uint8, 2)
     N, K = Wq.shape[0], Wq.shape[1] * 2
+    G = K // 128
+    _need_shape(scales, "scales", (N, G))
+    _need_shape(zeros, "zeros", (N, (G + 1) // 2))
+    _on_current_device(Wq, scales, zeros)
     out = torch.empty((N, K), dtype=torch.float32, device=Wq.device)
     check("mbw_dequant_int4_awq_g128", lib().mbw_dequant_int4_awq_g128(
         Wq.data_ptr(), scales.data_ptr(), zeros.data_ptr(), out.data_ptr(), N, K, _stream_ptr(Wq.device)))
