@@ -16,9 +16,16 @@ _EXPORTS = (
 )
 
 
+_PLAN_FILES = ("save_plans", "load_plans")
+
+
 def __getattr__(name):
     if name in _EXPORTS:
         from . import _binding
 
         return getattr(_binding, name)
+    if name in _PLAN_FILES:
+        from . import plans
+
+        return getattr(plans, name)
     raise AttributeError(name)
