@@ -298,6 +298,14 @@ mbw_status mbw_check_device_error(void);
  * flag. tries out of range: MBW_ERR_INVALID_ARG, nothing launched. */
 mbw_status mbw_selftest_wait_expiry(int64_t tries, mbw_stream_t stream);
 
+/* Host-side fault injection (test hook). The next `count` calls on the
+ * calling thread that pass their argument checks and would launch a kernel
+ * (the GEMV/GEMM entry points, mbw_repack_int4, mbw_quantize_int8_pc and the
+ * dequant helpers) launch nothing and return MBW_ERR_CUDA, as a failed launch
+ * would, with mbw_last_error() naming the injection. count = 0 (the default)
+ * turns it off; a negative count is MBW_ERR_INVALID_ARG. */
+mbw_status mbw_inject_launch_failures(int count);
+
 /* Number of kernel launches this library has issued on the calling thread. */
 uint64_t mbw_launch_count(void);
 

@@ -61,6 +61,7 @@ SIGNATURES = {
     "mbw_plan_describe": ([ctypes.c_int, _I64, _I64, _I64, ctypes.c_char_p, _SZ], _ST),
     "mbw_check_device_error": ([], _ST),
     "mbw_selftest_wait_expiry": ([_I64, _P], _ST),
+    "mbw_inject_launch_failures": ([ctypes.c_int], _ST),
     "mbw_launch_count": ([], ctypes.c_uint64),
     "mbw_status_string": ([_ST], ctypes.c_char_p),
     "mbw_last_error": ([], ctypes.c_char_p),
@@ -427,6 +428,12 @@ def launch_count() -> int:
 
 def check_device_error() -> None:
     check("mbw_check_device_error", lib().mbw_check_device_error())
+
+
+def inject_launch_failures(count: int) -> None:
+    """The next `count` launching calls on this thread raise MbwError with
+    MBW_ERR_CUDA and launch nothing (host-side fault injection; 0 turns it off)."""
+    check("mbw_inject_launch_failures", lib().mbw_inject_launch_failures(int(count)))
 
 
 def selftest_wait_expiry(tries: int) -> None:

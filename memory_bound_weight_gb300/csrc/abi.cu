@@ -16,6 +16,7 @@ namespace mbw {
 static thread_local std::string g_last_error;
 static thread_local int g_out_f32 = 0;
 static thread_local uint64_t g_launches = 0;
+static thread_local int g_injected_failures = 0;  // mbw_inject_launch_failures
 
 void set_last_error(const std::string& msg) { g_last_error = msg; }
 void count_launch() { ++g_launches; }
@@ -39,6 +40,14 @@ static mbw_status cuda_fail(cudaError_t e, const char* where) {
 
 static bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
 
+// The test hook's failure, taken at the point where a call would launch.
+static bool take_injected_failure(const char* where) {
+    if (g_injected_failures <= 0) return false;
+    --g_injected_failures;
+    g_last_error = std::string(where) + ": injected launch failure (mbw_inject_launch_failures)";
+    return true;
+}
+
 // Common size checks. Returns MBW_OK, or an error with the detail set.
 static mbw_status check_sizes(const char* fn, int64_t M, int64_t N, int64_t K, int64_t kunit) {
     if (M < 0 || N < 0 || K < 0) return fail(MBW_ERR_INVALID_ARG, std::string(fn) + ": negative size");
@@ -61,6 +70,7 @@ static mbw_status zero_output(void* y, int64_t M, int64_t N, cudaStream_t s) {
 static mbw_status run_simt(int fmt, int op, const uint8_t* W, const uint16_t* scales, const uint8_t* zeros,
                            const uint16_t* X, void* Y, int64_t M, int64_t N, int64_t K, cudaStream_t s,
                            const float* rscale = nullptr, const mbw_fusion* fz = nullptr) {
+    if (take_injected_failure("GEMV launch")) return MBW_ERR_CUDA;
     const Plan p = plan_lookup(op, M, N, K, s);
     const int width = plan_batch_width(fmt, p);
     GemvArgs a{};
@@ -174,6 +184,7 @@ mbw_status mbw_repack_int4(const uint8_t* Wq, uint8_t* Wr, int64_t N, int64_t K,
     if (!Wq || !Wr) return fail(MBW_ERR_INVALID_ARG, "mbw_repack_int4: NULL pointer");
     if (!aligned(Wq, 4) || !aligned(Wr, 4))
         return fail(MBW_ERR_MISALIGNED, "mbw_repack_int4: Wq and Wr must be 4-byte aligned");
+    if (take_injected_failure("repack launch")) return MBW_ERR_CUDA;
     cudaError_t e = launch_repack_int4(Wq, Wr, N, K, (cudaStream_t)stream);
     return e == cudaSuccess ? MBW_OK : cuda_fail(e, "repack launch");
 }
@@ -201,6 +212,7 @@ mbw_status mbw_quantize_int8_pc(const void* W, int8_t* Wq, float* scales, int64_
     if (!scales || (K > 0 && (!W || !Wq))) return fail(MBW_ERR_INVALID_ARG, "mbw_quantize_int8_pc: NULL pointer");
     if (!aligned(W, 2) || !aligned(scales, 4))
         return fail(MBW_ERR_MISALIGNED, "mbw_quantize_int8_pc: W must be 2-byte aligned, scales 4-byte");
+    if (take_injected_failure("quantize launch")) return MBW_ERR_CUDA;
     cudaError_t e = launch_quantize_int8_pc((const uint16_t*)W, Wq, scales, N, K, (cudaStream_t)stream);
     return e == cudaSuccess ? MBW_OK : cuda_fail(e, "quantize launch");
 }
@@ -290,6 +302,7 @@ mbw_status mbw_dequant_int4_g64(const uint8_t* Wq, const void* scales, float* ou
     if (N == 0 || K == 0) return MBW_OK;
     if (!Wq || !scales || !out) return fail(MBW_ERR_INVALID_ARG, "mbw_dequant_int4_g64: NULL pointer");
     if (!aligned(scales, 2) || !aligned(out, 4)) return fail(MBW_ERR_MISALIGNED, "mbw_dequant_int4_g64: alignment");
+    if (take_injected_failure("dequant launch")) return MBW_ERR_CUDA;
     cudaError_t e = launch_dequant(FMT_G64, Wq, (const uint16_t*)scales, nullptr, out, N, K, (cudaStream_t)stream);
     return e == cudaSuccess ? MBW_OK : cuda_fail(e, "dequant launch");
 }
@@ -303,6 +316,7 @@ mbw_status mbw_dequant_int4_awq_g128(const uint8_t* Wq, const void* scales, cons
         return fail(MBW_ERR_INVALID_ARG, "mbw_dequant_int4_awq_g128: NULL pointer");
     if (!aligned(scales, 2) || !aligned(out, 4))
         return fail(MBW_ERR_MISALIGNED, "mbw_dequant_int4_awq_g128: alignment");
+    if (take_injected_failure("dequant launch")) return MBW_ERR_CUDA;
     cudaError_t e = launch_dequant(FMT_AWQ, Wq, (const uint16_t*)scales, zeros, out, N, K, (cudaStream_t)stream);
     return e == cudaSuccess ? MBW_OK : cuda_fail(e, "dequant launch");
 }
@@ -330,6 +344,12 @@ mbw_status mbw_selftest_wait_expiry(int64_t tries, mbw_stream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "wait-expiry launch");
     e = launch_tc_wait_expiry((long long)tries, (cudaStream_t)stream);
     return e == cudaSuccess ? MBW_OK : cuda_fail(e, "wait-expiry launch");
+}
+
+mbw_status mbw_inject_launch_failures(int count) {
+    if (count < 0) return fail(MBW_ERR_INVALID_ARG, "mbw_inject_launch_failures: count must be >= 0");
+    g_injected_failures = count;
+    return MBW_OK;
 }
 
 uint64_t mbw_launch_count(void) { return g_launches; }

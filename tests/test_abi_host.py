@@ -196,3 +196,46 @@ def test_output_hook_is_thread_local(L):
     t.join()
     assert seen == [0]
     assert L.mbw_set_output_fp32(0) == 0
+
+
+def _gpu_present():
+    try:
+        import torch
+
+        return torch.cuda.is_available()
+    except ImportError:  # pragma: no cover
+        return False
+
+
+@pytest.mark.skipif(_gpu_present(), reason="valid-looking fake addresses must never reach a real GPU")
+def test_injected_launch_failures(L):
+    """Host-side fault injection: every launching call, given arguments that pass
+    its checks, fails with MBW_ERR_CUDA at its launch and launches nothing."""
+    calls = {
+        "gemv_bf16": lambda: L.gemv_bf16(A16, A16b, A16c, 8, 64, None, 0, None),
+        "gemv_int4_g64": lambda: L.gemv_int4_g64(A16, A16b, A16c, A16c, 8, 128, None, 0, None),
+        "gemv_int4_awq_g128": lambda: L.gemv_int4_awq_g128(A16, A16b, A16c, A16c, A16, 1, 8, 256, None, 0, None),
+        "gemv_int4_awq_g128_repacked":
+            lambda: L.gemv_int4_awq_g128_repacked(A16, A16b, A16c, A16c, A16, 20, 8, 256, None, 0, None),
+        "gemm_skinny_bf16": lambda: L.gemm_skinny_bf16(A16, A16b, A16c, 4, 8, 16, None, 0, None),
+        "gemv_int8_pc": lambda: L.gemv_int8_pc(A16, A16b, A16c, A16, 1, 8, 256, None, 0, None),
+        "gemv_fused": lambda: L.gemv_fused(1, A16, None, A16c, A16, 1, 8, 256, _fusion(norm=A16b), None, 0, None),
+        "mbw_repack_int4": lambda: L.mbw_repack_int4(A16, A16b, 8, 64, None),
+        "mbw_quantize_int8_pc": lambda: L.mbw_quantize_int8_pc(A16, A16b, A16c, 8, 64, None),
+        "mbw_dequant_int4_g64": lambda: L.mbw_dequant_int4_g64(A16, A16b, A16c, 4, 128, None),
+        "mbw_dequant_int4_awq_g128": lambda: L.mbw_dequant_int4_awq_g128(A16, A16b, A16c, A16c, 4, 128, None),
+    }
+    assert L.mbw_inject_launch_failures(-1) == 1
+    n0 = L.mbw_launch_count()
+    try:
+        for name, call in calls.items():
+            assert L.mbw_inject_launch_failures(1) == 0
+            assert call() == 6, name
+            assert "injected launch failure" in L.mbw_last_error().decode(), name
+        # a call stopped by its argument checks does not use up an injection
+        assert L.mbw_inject_launch_failures(1) == 0
+        assert L.gemv_bf16(A16, A16b, A16c, 8, 60, None, 0, None) == 3
+        assert calls["gemv_bf16"]() == 6
+    finally:
+        L.mbw_inject_launch_failures(0)
+    assert L.mbw_launch_count() == n0
