@@ -67,6 +67,12 @@ typedef int mbw_status;
 #define MBW_ERR_CUDA 6                /* a CUDA runtime call failed */
 #define MBW_ERR_DEVICE_TIMEOUT 7      /* a device-side bounded wait gave up */
 
+/* Largest N, K or M a call accepts (MBW_ERR_BAD_SHAPE above it). The kernels
+ * index rows and columns in 32-bit integers, and a tile may run up to 256 rows
+ * past N before its clamp; the 2^16 of headroom keeps every such index
+ * positive. */
+#define MBW_MAX_DIM ((1LL << 31) - (1LL << 16))
+
 /* Rounds of mbarrier.try_wait a kernel's wait makes before it gives up, sets
  * the device fault flag and leaves its loop (the waits of the bulk-copy and
  * tcgen05 kernels). A round that does not complete suspends for ~3.8 us on a
@@ -94,7 +100,7 @@ typedef int mbw_status;
  * gemv_bf16 -- y = W . x with BF16 weights (16 bits per weight; llm-rs vs
  * vLLM, sec. 6 format table, "BF16 16").
  *   W : bf16 [N][K]      x : bf16 [K]      y : bf16 [N] (fp32 [N] under the fp32 hook)
- *   Requires K % 8 == 0 (16-byte rows). N, K < 2^31.
+ *   Requires K % 8 == 0 (16-byte rows). N, K <= MBW_MAX_DIM.
  */
 mbw_status gemv_bf16(const void *W, const void *x, void *y, int64_t N, int64_t K,
                      void *workspace, size_t ws_bytes, mbw_stream_t stream);

@@ -4,7 +4,6 @@
 #include <stdint.h>
 #include <stdio.h>
 
-#include <climits>
 #include <cstring>
 #include <string>
 
@@ -51,8 +50,8 @@ static bool take_injected_failure(const char* where) {
 // Common size checks. Returns MBW_OK, or an error with the detail set.
 static mbw_status check_sizes(const char* fn, int64_t M, int64_t N, int64_t K, int64_t kunit) {
     if (M < 0 || N < 0 || K < 0) return fail(MBW_ERR_INVALID_ARG, std::string(fn) + ": negative size");
-    if (N > INT_MAX || K > INT_MAX || M > INT_MAX)
-        return fail(MBW_ERR_BAD_SHAPE, std::string(fn) + ": N, K and M must be below 2^31");
+    if (N > MBW_MAX_DIM || K > MBW_MAX_DIM || M > MBW_MAX_DIM)
+        return fail(MBW_ERR_BAD_SHAPE, std::string(fn) + ": N, K and M must be at most MBW_MAX_DIM (2^31 - 2^16)");
     if (K % kunit != 0)
         return fail(MBW_ERR_BAD_SHAPE, std::string(fn) + ": K must be a multiple of " + std::to_string(kunit));
     return MBW_OK;

@@ -349,7 +349,7 @@ static bool shape_ok(int op, int64_t M, int64_t N, int64_t K) {
     const int fuse = flags & MBW_FUSE_MASK;
     if ((flags & MBW_REPACKED) && (base != MBW_OP_GEMV_INT4_AWQ_G128 || fuse)) return false;
     if (fuse && base != MBW_OP_GEMV_BF16 && base != MBW_OP_GEMV_INT4_G64 && base != MBW_OP_GEMV_INT8_PC) return false;
-    if (M < 1 || N < 1 || K < 1 || N > 0x7FFFFFFF || K > 0x7FFFFFFF || M > 0x7FFFFFFF) return false;
+    if (M < 1 || N < 1 || K < 1 || N > MBW_MAX_DIM || K > MBW_MAX_DIM || M > MBW_MAX_DIM) return false;
     if (base == MBW_OP_GEMV_INT4_G64 && M != 1) return false;
     const int fmt = fmt_of_op(op);
     const int64_t kunit = fmt == FMT_BF16 ? 8 : fmt == FMT_G64 ? 64 : 128;  // AWQ and INT8: 128

@@ -35,6 +35,8 @@ int main(void) {
     expect("gemv_bf16 negative N", gemv_bf16(a, b, c, -1, 64, NULL, 0, NULL), MBW_ERR_INVALID_ARG);
     expect("gemv_bf16 K % 8", gemv_bf16(a, b, c, 8, 60, NULL, 0, NULL), MBW_ERR_BAD_SHAPE);
     expect("gemv_bf16 N == 0", gemv_bf16(NULL, NULL, NULL, 0, 64, NULL, 0, NULL), MBW_OK);
+    expect("gemv_bf16 N above MBW_MAX_DIM", gemv_bf16(a, b, c, MBW_MAX_DIM + 1, 64, NULL, 0, NULL),
+           MBW_ERR_BAD_SHAPE);
     expect("gemv_int4_g64 K % 64", gemv_int4_g64(a, b, c, c, 8, 96, NULL, 0, NULL), MBW_ERR_BAD_SHAPE);
     expect("gemv_int4_awq_g128 misaligned codes",
            gemv_int4_awq_g128((const uint8_t *)a + 16, b, c, c, a, 1, 8, 256, NULL, 0, NULL), MBW_ERR_MISALIGNED);

@@ -79,6 +79,8 @@ A16c = 0x30000
     (lambda L: L.gemv_bf16(A16, A16b + 8, A16c, 8, 64, None, 0, None), 2),
     (lambda L: L.gemv_bf16(None, A16b, A16c, 8, 64, None, 0, None), 1),
     (lambda L: L.gemv_bf16(A16, A16b, A16c, 1 << 31, 64, None, 0, None), 3),
+    (lambda L: L.gemv_bf16(A16, A16b, A16c, (1 << 31) - (1 << 16) + 1, 64, None, 0, None), 3),  # above MBW_MAX_DIM
+    (lambda L: L.gemm_skinny_bf16(A16, A16b, A16c, (1 << 31) - (1 << 16) + 1, 8, 16, None, 0, None), 3),
     (lambda L: L.gemv_bf16(None, None, None, 0, 64, None, 0, None), 0),  # N == 0: no-op
     (lambda L: L.gemv_int4_g64(A16, A16b, A16c, A16c, 8, 96, None, 0, None), 3),
     (lambda L: L.gemv_int4_g64(A16, A16b + 1, A16c, A16c, 8, 128, None, 0, None), 2),
@@ -151,6 +153,8 @@ def test_planner_host_logic(L):
     assert L.mbw_plan_candidates(2, 1, 8, 96) == 0  # K not a multiple of 64
     assert L.mbw_plan_candidates(7, 1, 8, 64) == 0
     assert L.mbw_plan_candidates(5, 1, 8, 192) == 0  # INT8: K not a multiple of 128
+    assert L.mbw_plan_candidates(1, 1, (1 << 31) - (1 << 16) + 1, 64) == 0  # N above MBW_MAX_DIM
+    assert L.mbw_plan_candidates(1, 1, (1 << 31) - (1 << 16), 64) >= 1  # N at MBW_MAX_DIM
     # fused ops: only the mma2 and latency families, described with their fusions
     for op in (1 | 0x100, 2 | 0x300, 5 | 0x700):
         n = L.mbw_plan_candidates(op, 1, 2048, 2048)
