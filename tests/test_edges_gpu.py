@@ -3,8 +3,8 @@ batch (GPU).
 
 K = 0 is the empty sum (outputs set to zero); N = 0 or M = 0 launches
 nothing. Ragged shapes on the tensor-core paths (partial 128-row tiles,
-partial batch tiles, a CTA pair whose second tile lies past N) must not write
-outside Y: a sentinel band before and after Y stays untouched, and Y matches
+partial batch tiles, a CTA pair whose second tile lies past N, batches past
+256 that the library runs in slices) must not write outside Y: a sentinel band before and after Y stays untouched, and Y matches
 the oracle.
 """
 import numpy as np
@@ -80,7 +80,7 @@ def bands_intact(buf, M, N):
     return bool(torch.all(buf[:64] == -7.0)) and bool(torch.all(buf[64 + M * N:] == -7.0))
 
 
-@pytest.mark.parametrize("M,N,K", [(20, 130, 384), (16, 1, 128), (64, 257, 1024), (100, 129, 256)])
+@pytest.mark.parametrize("M,N,K", [(20, 130, 384), (16, 1, 128), (64, 257, 1024), (100, 129, 256), (300, 130, 256)])
 def test_awq_tensor_core_guard_bands(orc, M, N, K):
     G = K // 128
     c, s, z = gen.int4_codes(1800 + N, 0, N, K), gen.f16_group_scales(1800 + N, 0, N, G), gen.u4_zero_points(1800 + N, 0, N, G)
@@ -98,7 +98,8 @@ def test_awq_tensor_core_guard_bands(orc, M, N, K):
             assert_parity(y, Y, A, f"awq guard {M}x{N}x{K} {desc}")
 
 
-@pytest.mark.parametrize("M,N,K", [(130, 300, 512), (256, 129, 256), (9, 200, 192), (200, 1, 64)])
+@pytest.mark.parametrize("M,N,K", [(130, 300, 512), (256, 129, 256), (9, 200, 192), (200, 1, 64),
+                                   (300, 200, 256), (520, 130, 128)])  # batches past 256: 2 and 3 slices
 def test_skinny_tensor_core_guard_bands(orc, M, N, K):
     W = gen.bf16_weights(1900 + N, 0, N, K)
     X = gen.bf16_activations(1900 + N, 0, M, K)
