@@ -4,14 +4,20 @@
 A step is one pass of the whole hot path over one decode token: every weight
 matrix of the model streamed once by the library's GEMV kernels, each GEMV
 with its own activation vector (all calls through the C ABI, captured once
-into a CUDA graph and replayed). Default workload (--workload tinyllama_int4):
-TinyLlama-1.1B-shaped INT4 group-64 weights at batch 1 with the projections
-that share an input fused, as an engine runs them -- 22 layers x (qkv
-2560x2048, o 2048x2048, gate_up 11264x2048, down 2048x5632) + LM head
-32000x2048 = 89 GEMVs and 0.5495 GB of codes + scales per step (4.4x the L2,
-so no matrix is still cached when the step reaches it again);
---workload tinyllama_int4_unfused streams the same bytes as 155 GEMVs (q, k,
-v, gate and up separately). Synthetic seeded data (no checkpoint).
+into a CUDA graph and replayed).
+
+Default workload (--workload qwen_bf16): the Qwen2.5-7B-shaped BF16 decode
+step at batch 1 -- 28 layers x (qkv 4608x3584, o 3584x3584, gate and up
+18944x3584, down 3584x18944) + LM head 152064x3584 = 141 GEMVs and 14.14 GB
+of weights per step (about 110x the L2, so no matrix is still cached when the
+step reaches it again). Synthetic seeded data (no checkpoint).
+
+The same JSON line carries, under "configs", the other configurations the
+metric is quoted on, each on its autotuned plans: the BF16 2048x2048 GEMV,
+the four TinyLlama-shaped INT4 group-64 matrices (and the TinyLlama INT4
+step), the skinny BF16 GEMM over the Qwen2.5-7B MLP shapes at M = 1 ... 256,
+and the AWQ-style INT4 Qwen2.5-7B step at M = 1, 16 and 64 (codes repacked at
+load time). --no-extras leaves them out.
 
 Metric: achieved HBM GB/s = algorithmic bytes of the step (weights + scales
 + x) / step time, and the weight-stream ms per token.
@@ -61,7 +67,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=10000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="mbw", choices=["mbw", "reference"])
-    p.add_argument("--workload", default="tinyllama_int4",
+    p.add_argument("--workload", default="qwen_bf16",
                    choices=["tinyllama_int4", "tinyllama_int4_fusedops", "tinyllama_int4_unfused", "qwen_bf16",
                             "qwen_awq", "qwen_awq_repacked", "qwen3_int8", "bf16_2048"])
     p.add_argument("--batch", type=int, default=1,
@@ -79,6 +85,11 @@ def parse_args():
                         "shape: per-shape autotune only")
     p.add_argument("--plans-out", default=None, help="write the tuned plan index of every shape to this JSON file")
     p.add_argument("--plans-from", default=None, help="restore plans from a --plans-out file instead of tuning")
+    p.add_argument("--no-extras", action="store_true",
+                   help="leave out the other configurations' figures (configs key of the JSON line)")
+    p.add_argument("--extras-tune", default="shape", choices=["step", "shape"],
+                   help="plan tuning of the extra decode steps (TinyLlama INT4, AWQ): per shape (default) or "
+                        "refined on the whole step")
     p.add_argument("--profile-range", action="store_true",
                    help="bracket the timed region with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     return p.parse_args()
@@ -379,6 +390,14 @@ def cpu_baseline(workload, budget_s=10.0, M=1):
     else:
         mk, fmt = WORKLOAD_MATS[workload]
         mats = mk()
+    what = f"the step's {len(mats)} matrices"
+    if wl.step_weight_bytes(mats, fmt) > 2e9:
+        # a multi-GB step: the oracle cycles over the first layer's matrices (the
+        # same GEMVs, byte for byte; generating every matrix on the host would
+        # take minutes and hold the whole step in host memory)
+        nl = sum(1 for m in mats if m.name.startswith("L0."))
+        what = f"the first layer's {nl} matrices of the {len(mats)}-matrix step"
+        mats = mats[:nl]
 
     def host_weights(mi, m):
         if fmt == wl.FMT_INT4_G64:
@@ -432,7 +451,7 @@ def cpu_baseline(workload, budget_s=10.0, M=1):
         if spent >= budget_s:
             break
     return {"value": done_bytes / spent / 1e9, "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
-            "sample": f"{n} matrix GEMVs ({n / len(mats):.2f} passes over the step's {len(mats)} matrices, "
+            "sample": f"{n} matrix GEMVs ({n / len(mats):.2f} passes over {what}, "
                       f"{done_bytes / 1e9:.3f} GB), fp64 C oracle, OpenMP over rows, {spent:.1f} s"}
 
 
@@ -499,6 +518,171 @@ def workload_desc(workload, batch=1):
             "qwen3_int8": f"Qwen3-4B-shaped symmetric INT8 decode step (one fp32 scale per output channel, every "
                           f"linear layer and the LM head, q/k/v and gate/up fused), batch {batch} (145 GEMVs)",
             "bf16_2048": "BF16 GEMV 2048x2048, batch 1, 64 rotating copies"}[workload]
+
+
+# ------------------------------------------------------- other configs ----
+class CallKind:
+    """What time_per_shape needs of a step (format, op, batch, code layout),
+    for shapes timed without a resident step."""
+
+    def __init__(self, fmt, M=1, repacked=False):
+        import memory_bound_weight_gb300 as mbw
+
+        self.fmt, self.M, self.repacked = fmt, M, repacked
+        self.op = op_of_fmt(fmt) | (mbw.REPACKED if repacked else 0)
+
+    def shapes(self):
+        return []
+
+
+def hbm_roofline(nbytes, us, peak):
+    """HBM roofline fields of one launch: algorithmic bytes / its time."""
+    a = nbytes / (us * 1e-6) / 1e9
+    return {"bound": "hbm", "achieved": a, "peak": peak, "unit": "GB/s", "frac": a / peak,
+            "bytes_alg_per_launch": nbytes, "us_per_launch": us}
+
+
+def per_matrix_figures(fmt, shapes, device, cold_iters=100):
+    """Steady state (PDL chain over copies >= 4x L2) and cold (L2 flushed)
+    time of each shape on its autotuned plan, with its roofline."""
+    peak, _ = hbm_peak()
+    out = time_per_shape(CallKind(fmt), device, shapes=shapes, plans=None, cold_iters=cold_iters)
+    for (fz, N, K) in shapes:
+        r = out[skey((fz, N, K))]
+        r["roofline"] = hbm_roofline(wl.call_bytes(fmt, 1, wl.Mat("", N, K, fz)), r["us"], peak)
+    return out
+
+
+def step_figure(workload, M, device, tune="shape", steps=20):
+    """One decode step of `workload` at batch M: plans tuned per shape (or on
+    the whole step), one CUDA graph per step, device time of `steps` replays;
+    the dominant kernel's roofline as in the headline line."""
+    import torch
+
+    import memory_bound_weight_gb300 as mbw
+
+    step = make_step(workload, seed=0, device=device, M=M)
+    for fz, N, K in step.shapes():
+        mbw.autotune(step.op | fz, M, N, K)
+    if tune == "step":
+        from memory_bound_weight_gb300.tune import tune_sequence
+
+        tune_sequence(step.run, [(step.op | fz, M, N, K) for fz, N, K in step.shapes()])
+    plans = {skey(sh): mbw.plan_describe(step.op | sh[0], M, sh[1], sh[2]) for sh in step.shapes()}
+    step_plans = {sh: mbw.plan_index(step.op | sh[0], M, sh[1], sh[2]) for sh in step.shapes()}
+    step.run()
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        step.run()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream(device)
+    e0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    peak, peak_src = hbm_peak()
+    gbs = step.bytes_alg / (ms * 1e-3) / 1e9
+    shape_times = time_per_shape(step, device, shapes=step.shapes(), plans=step_plans)
+    counts = {}
+    for m in step.mats:
+        counts[(m.fuse, m.N, m.K)] = counts.get((m.fuse, m.N, m.K), 0) + 1
+    dominant = max(step.shapes(), key=lambda sh: counts[sh] * shape_times[skey(sh)]["us"])
+    roof = roofline_fields(step, ms, gbs, peak, peak_src, None, plans, len(step.mats), dominant, counts,
+                           shape_times)
+    out = {"workload": workload_desc(workload, M), "ms_per_step": ms, "GB/s": gbs, "frac_of_peak": gbs / peak,
+           "bytes_alg_per_step": step.bytes_alg, "steps": steps, "tune": tune, "plans": plans, "roofline": roof,
+           "step_shapes": shape_times}
+    del g, step
+    torch.cuda.empty_cache()
+    return out
+
+
+def skinny_figures(device, Ms=wl.SKINNY_M, reps=7):
+    """gemm_skinny_bf16 over the Qwen2.5-7B MLP shapes at each batch M, on the
+    autotuned plan: a CUDA graph of calls over distinct copies of W >= 4x L2,
+    median of `reps` replays; HBM and tensor rooflines, the longer the bound."""
+    import torch
+
+    import memory_bound_weight_gb300 as mbw
+    from memory_bound_weight_gb300 import inputs_gpu
+
+    peak, _ = hbm_peak()
+    tc, tc_src = tensor_peak()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    op = mbw.OP_GEMM_SKINNY_BF16
+    out = {}
+    for m in wl.SKINNY_SHAPES:
+        N, K = m.N, m.K
+        row = {}
+        for M in Ms:
+            b = wl.bytes_alg(wl.FMT_BF16, M, N, K)
+            fl = wl.flops(M, N, K)
+            copies = int(max(4, -(-4 * l2 // b)))
+            Ws = [inputs_gpu.bf16_weights(0, 2000 + i, N, K, device) for i in range(copies)]
+            X = inputs_gpu.bf16_activations(0, 7, M, K, device)
+            Ys = [torch.empty((M, N), dtype=torch.bfloat16, device=device) for _ in range(copies)]
+            mbw.autotune(op, M, N, K)
+            for i in range(copies):
+                mbw.gemm_skinny_bf16(X, Ws[i], out=Ys[i])
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=torch.cuda.Stream(device)):
+                for i in range(copies):
+                    mbw.gemm_skinny_bf16(X, Ws[i], out=Ys[i])
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(reps):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) / copies)
+            us = statistics.median(ts) * 1e3
+            r = hbm_roofline(b, us, peak)
+            tflops = fl / (us * 1e-6) / 1e12
+            r.update({"hbm_frac": r["frac"], "tensor_frac": tflops / tc, "tensor_peak": tc,
+                      "tensor_peak_source": tc_src})
+            if fl / (tc * 1e12) > b / (peak * 1e9):
+                r.update({"bound": "tensor", "achieved": tflops, "peak": tc, "unit": "TFLOP/s", "frac": tflops / tc})
+            row[f"M={M}"] = {"us": us, "GB/s": b / (us * 1e-6) / 1e9, "frac_of_peak": b / (us * 1e-6) / 1e9 / peak,
+                             "TFLOP/s": tflops, "copies": copies, "plan": mbw.plan_describe(op, M, N, K),
+                             "roofline": r}
+            del Ws, Ys, g
+            torch.cuda.empty_cache()
+        out[f"{N}x{K}"] = row
+    return out
+
+
+def extra_configs(device, main_workload, tune="shape"):
+    """The other configurations the metric is quoted on, after the headline
+    step (N = 1 only): BF16 GEMV 2048x2048; the four TinyLlama-shaped INT4
+    group-64 matrices and the TinyLlama INT4 step; the skinny BF16 GEMM sweep;
+    the AWQ-style INT4 step at M = 1, 16, 64 with repacked codes."""
+    t0 = time.time()
+    out = {}
+    out["bf16_gemv_2048x2048"] = per_matrix_figures(wl.FMT_BF16, [(0, 2048, 2048)], device)
+    out["int4_g64_tinyllama_matrices"] = per_matrix_figures(
+        wl.FMT_INT4_G64, [(0, m.N, m.K) for m in wl.TINYLLAMA_TABLE_SHAPES], device)
+    if main_workload != "tinyllama_int4":
+        out["int4_g64_tinyllama_step"] = step_figure("tinyllama_int4", 1, device, tune)
+    if main_workload != "qwen_bf16":
+        out["bf16_qwen_step"] = step_figure("qwen_bf16", 1, device, tune)
+    out["skinny_bf16_qwen_mlp"] = skinny_figures(device)
+    out["awq_qwen_step_repacked"] = {f"M={M}": step_figure("qwen_awq_repacked", M, device, tune) for M in wl.AWQ_M}
+    out["seconds"] = time.time() - t0
+    return out
 
 
 # ------------------------------------------------------------------- main ----
@@ -676,6 +860,11 @@ def main():
     }
     if per_matrix:
         line["per_matrix"] = per_matrix
+    if ws == 1 and not args.no_extras:
+        # the other configurations, after the headline step's memory is released
+        del g, step
+        torch.cuda.empty_cache()
+        line["configs"] = extra_configs(device, args.workload, args.extras_tune)
     print(json.dumps(line), flush=True)
 
 

@@ -29,12 +29,16 @@
  *     errors are returned as MBW_ERR_CUDA (detail in mbw_last_error()).
  *   - y must not alias an input. Results are deterministic: the same inputs
  *     give bitwise the same outputs, run after run.
- *   - Kernels use programmatic dependent launch: each one starts streaming
- *     W (and scales, zero points) before it waits for the previous kernel in
- *     the stream, and reads x only after that wait. So x may be produced by the
- *     preceding kernel; the weights must not be written by a preceding kernel
- *     that lets its dependents launch early (none of this library's kernels
- *     writes weights).
+ *   - Kernels use programmatic dependent launch: each GEMV/GEMM starts
+ *     streaming W (and scales, zero points) before it waits for the previous
+ *     kernel in the stream, and reads x only after that wait. So x may be
+ *     produced by the preceding kernel, but the weights must not be: a kernel
+ *     that writes weights must have completed before the GEMV is launched
+ *     behind it. The library's own weight writers (mbw_quantize_int8_pc,
+ *     mbw_repack_int4) see to this themselves: each ends with an empty kernel
+ *     launched with plain stream ordering, which starts only after the writer
+ *     has completed, so a GEMV queued next on the same stream reads the
+ *     finished weights without a host synchronization.
  *   - `workspace` / `ws_bytes` are accepted for split-K plans that need global
  *     scratch; a NULL or short workspace never fails a call (the plan falls
  *     back to a variant that needs none). mbw_workspace_bytes() gives the size.

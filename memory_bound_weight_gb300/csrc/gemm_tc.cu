@@ -84,6 +84,15 @@ __device__ __forceinline__ bool tc_wait_warp(uint64_t* bar, uint32_t parity) {
     return __all_sync(0xFFFFFFFFu, tc_wait(bar, parity));
 }
 
+// After a producer's slot wait gave up at stage `stop` (< n), wait (bounded,
+// whole warp) for the bulk copies of the stages it issued that may still be in
+// flight: the last D before `stop`, whose slots are not reused. Then no copy
+// lands in shared memory after the ring is reused or the CTA exits.
+__device__ __forceinline__ void tc_drain_issued(uint64_t* full, int stop, int n, int D) {
+    if (stop >= n) return;
+    for (int j = max(0, stop - D); j < stop; ++j) tc_wait_warp(&full[j % D], (j / D) & 1);
+}
+
 __device__ __forceinline__ void tc_tma_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
@@ -212,7 +221,8 @@ __global__ void __launch_bounds__(192, 1)
                     tc_tma_2d(smem + (size_t)i * STAGE + BPS * A_BYTES + bb * B_BYTES, &mapX,
                               ((ks0 + i) * BPS + bb) * 64, a.m0, &full[i]);
         __syncwarp();
-        for (int i = npre; i < nks; ++i) {
+        int i = npre;
+        for (; i < nks; ++i) {
             const int s = i % D;
             if (!tc_wait_warp(&empty[s], ((i / D) - 1) & 1)) break;
             uint8_t* st = smem + (size_t)s * STAGE;
@@ -228,6 +238,8 @@ __global__ void __launch_bounds__(192, 1)
             }
             __syncwarp();
         }
+        tc_drain_issued(full, i, nks, D);
+        if (S > 1) asm volatile("bar.arrive 1, 160;" ::: "memory");  // the ring may now hold the partials
     } else if (warp == 1) {
         // --------------------------------------------------- MMA issuer ----
         {
@@ -276,6 +288,9 @@ __global__ void __launch_bounds__(192, 1)
         // ----------------------------------------------------- epilogue ----
         const bool ok = tc_wait(accum, 0);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        // split-K: the partials reuse the ring, which the producer may still be
+        // draining after a failed wait; it arrives here once no copy is in flight
+        if (S > 1) asm volatile("bar.sync 1, 160;" ::: "memory");
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
         const int lrow = quarter * 32 + lane;
         float* part = reinterpret_cast<float*>(smem);  // [NT][128] fp32 partials (ring reused)
@@ -454,7 +469,8 @@ __global__ void __launch_bounds__(192, 1)
                     tma2(smem + (size_t)i * STAGE + BPS * A_BYTES + bb * B_BYTES, &mapX, ((ks0 + i) * BPS + bb) * 64,
                          xrow, i);
         __syncwarp();
-        for (int i = npre; i < nks; ++i) {
+        int i = npre;
+        for (; i < nks; ++i) {
             const int s = i % D;
             if (!tc_wait_warp(&empty[s], ((i / D) - 1) & 1)) break;
             uint8_t* st = smem + (size_t)s * STAGE;
@@ -471,6 +487,11 @@ __global__ void __launch_bounds__(192, 1)
             }
             __syncwarp();
         }
+        // both CTAs' copies complete on the even CTA's barriers, so the even CTA
+        // drains for the pair; the cluster barrier at the end keeps the odd CTA
+        // resident until it has
+        if (member == 0) tc_drain_issued(full, i, nks, D);
+        if (S > 1) asm volatile("bar.arrive 1, 160;" ::: "memory");  // the ring may now hold the partials
     } else if (warp == 1) {
         // ----------------------------------------- MMA issuer (even CTA) ----
         const bool leader = tc_elect();
@@ -520,6 +541,9 @@ __global__ void __launch_bounds__(192, 1)
         // ----------------------------------------------------- epilogue ----
         const bool ok = tc_wait(accum, 0);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        // split-K: the partials reuse the ring, which the producer may still be
+        // draining after a failed wait; it arrives here once no copy is in flight
+        if (S > 1) asm volatile("bar.sync 1, 160;" ::: "memory");
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
         const int lrow = quarter * 32 + lane;
         float* part = reinterpret_cast<float*>(smem);  // [NT][128] fp32 partials (ring reused)
@@ -779,7 +803,8 @@ __global__ void __launch_bounds__(TcAwqLayout<NT>::THREADS, 1)
         if (leader)
             for (int j = 0; j < npre; ++j) load_x(ring + (size_t)j * L::SLOT, j, &qfull[j]);
         __syncwarp();
-        for (int j = npre; j < nslots; ++j) {
+        int j = npre;
+        for (; j < nslots; ++j) {
             const int s = j % D;
             if (!tc_wait_warp(&empty[s], ((j / D) - 1) & 1)) break;
             uint8_t* st = ring + (size_t)s * L::SLOT;
@@ -793,6 +818,7 @@ __global__ void __launch_bounds__(TcAwqLayout<NT>::THREADS, 1)
             }
             __syncwarp();
         }
+        tc_drain_issued(qfull, j, nslots, D);  // before the __syncthreads after which the ring holds partials
     } else if (warp == 1) {
         // --------------------------------------------------- MMA issuer ----
         {

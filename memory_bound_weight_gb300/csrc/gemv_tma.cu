@@ -215,8 +215,9 @@ __global__ void __launch_bounds__((W + 1) * 32)
                 }
             }
             if (!ok) {
-                // drain: wait (bounded) for the copies already issued
-                for (int j = max(0, i - 1 - D); j < i - 1; ++j) mbar_wait(&full[j % D], (j / D) & 1);
+                // drain: wait (bounded) for the copies that may still be in flight,
+                // stages i - D .. i - 1 (every earlier slot was released, so its copy landed)
+                for (int j = max(0, i - D); j < i; ++j) mbar_wait(&full[j % D], (j / D) & 1);
             }
         }
     } else {

@@ -72,6 +72,19 @@ __global__ void repack_int4_kernel(const uint32_t* in, uint32_t* out, int64_t nw
         out[i] = repack_word(in[i]);
 }
 
+// Launched after each weight writer above, without the programmatic-
+// serialization attribute, so it starts only once the writer has completed
+// and its stores are visible. The library's GEMVs read weights before their
+// griddepcontrol.wait and may start early relative to the kernel in front of
+// them; with this kernel in between, that kernel wrote nothing they read.
+__global__ void weights_written_fence_kernel() {}
+
+cudaError_t launch_weights_fence(cudaStream_t s) {
+    count_launch();
+    weights_written_fence_kernel<<<1, 32, 0, s>>>();
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_repack_int4(const uint8_t* Wq, uint8_t* Wr, int64_t N, int64_t K, cudaStream_t s) {
@@ -82,7 +95,8 @@ cudaError_t launch_repack_int4(const uint8_t* Wq, uint8_t* Wr, int64_t N, int64_
     count_launch();
     repack_int4_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(
         reinterpret_cast<const uint32_t*>(Wq), reinterpret_cast<uint32_t*>(Wr), nwords);
-    return cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
+    return e != cudaSuccess ? e : launch_weights_fence(s);
 }
 
 cudaError_t launch_quantize_int8_pc(const uint16_t* W, int8_t* Wq, float* scales, int64_t N, int64_t K,
@@ -91,7 +105,8 @@ cudaError_t launch_quantize_int8_pc(const uint16_t* W, int8_t* Wq, float* scales
     const int64_t grid = N < (int64_t)device_sm_count() * 8 ? N : (int64_t)device_sm_count() * 8;
     count_launch();
     quantize_int8_pc_kernel<<<(unsigned)grid, kQuantThreads, 0, s>>>(W, Wq, scales, N, K);
-    return cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
+    return e != cudaSuccess ? e : launch_weights_fence(s);
 }
 
 }  // namespace mbw

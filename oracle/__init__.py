@@ -80,6 +80,7 @@ class Oracle:
         lib.oracle_gemm_int8_pc.argtypes = [_P, _P, _P, _I64, _I64, _I64, _P, _P]
         lib.oracle_quantize_int8_pc.argtypes = [_P, _I64, _I64, _P, _P]
         lib.oracle_rmsnorm_bf16.argtypes = [_P, _P, _I64, _I64, ctypes.c_double, _P]
+        lib.oracle_rmsnorm_f64.argtypes = [_P, _P, _I64, _I64, ctypes.c_double, _P]
         lib.oracle_swiglu.argtypes = [_P, _P, _I64, _P]
         lib.oracle_add_residual.argtypes = [_P, _P, _I64, _P]
         lib.oracle_num_threads.restype = ctypes.c_int
@@ -87,7 +88,7 @@ class Oracle:
         for f in ("oracle_dequant_int4_g64", "oracle_dequant_int4_awq_g128", "oracle_gemm_bf16",
                   "oracle_gemm_int4_g64", "oracle_gemm_int4_awq_g128", "oracle_gemm_int4_awq_g128_repacked",
                   "oracle_repack_int4", "oracle_gemm_int8_pc",
-                  "oracle_quantize_int8_pc", "oracle_rmsnorm_bf16", "oracle_swiglu", "oracle_add_residual",
+                  "oracle_quantize_int8_pc", "oracle_rmsnorm_bf16", "oracle_rmsnorm_f64", "oracle_swiglu", "oracle_add_residual",
                   "oracle_set_num_threads"):
             getattr(lib, f).restype = None
 
@@ -212,6 +213,19 @@ class Oracle:
         assert G.shape == (K,)
         out = np.empty((M, K), dtype=np.uint16)
         self.lib.oracle_rmsnorm_bf16(_ptr(X2), _ptr(G), M, K, float(eps), _ptr(out))
+        return out.reshape(shape)
+
+    def rmsnorm_f64(self, X: np.ndarray, G: np.ndarray, eps: float):
+        """X bf16 bits (M, K) or (K,), G bf16 bits (K,) -> the normalised values
+        x * g / sqrt(mean(x^2) + eps) in float64, before the bf16 rounding."""
+        X = np.ascontiguousarray(X, dtype=np.uint16)
+        shape = X.shape
+        X2 = np.atleast_2d(X)
+        M, K = X2.shape
+        G = np.ascontiguousarray(G, dtype=np.uint16)
+        assert G.shape == (K,)
+        out = np.empty((M, K), dtype=np.float64)
+        self.lib.oracle_rmsnorm_f64(_ptr(X2), _ptr(G), M, K, float(eps), _ptr(out))
         return out.reshape(shape)
 
     def swiglu(self, A: np.ndarray, B: np.ndarray):

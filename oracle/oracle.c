@@ -394,10 +394,11 @@ void oracle_quantize_int8_pc(const uint16_t *W, int64_t N, int64_t K,
 /* ------------------------------------------------------------------------ */
 
 /* RMSNorm of each row of X with weight G (the prologue folded into a
- * projection): Xn[m][k] = bf16(X[m][k] * G[k] / sqrt(mean_k X[m][k]^2 + eps)).
- * X bf16 [M][K], G bf16 [K], Xn bf16 [M][K]. */
-void oracle_rmsnorm_bf16(const uint16_t *X, const uint16_t *G, int64_t M,
-                         int64_t K, double eps, uint16_t *Xn)
+ * projection), before the activation is rounded to bf16:
+ * V[m][k] = X[m][k] * G[k] / sqrt(mean_k X[m][k]^2 + eps), in fp64.
+ * X bf16 [M][K], G bf16 [K], V double [M][K]. */
+void oracle_rmsnorm_f64(const uint16_t *X, const uint16_t *G, int64_t M,
+                        int64_t K, double eps, double *V)
 {
     for (int64_t m = 0; m < M; m++) {
         double ss = 0.0;
@@ -409,9 +410,24 @@ void oracle_rmsnorm_bf16(const uint16_t *X, const uint16_t *G, int64_t M,
         for (int64_t k = 0; k < K; k++) {
             double x = oracle_bf16_to_double(X[m * K + k]);
             double g = oracle_bf16_to_double(G[k]);
-            Xn[m * K + k] = oracle_double_to_bf16_rne(x * inv * g);
+            V[m * K + k] = x * inv * g;
         }
     }
+}
+
+/* The normalised activation the projection consumes:
+ * Xn[m][k] = bf16(V[m][k]) (round to nearest even) with V as above.
+ * Xn bf16 [M][K]. */
+void oracle_rmsnorm_bf16(const uint16_t *X, const uint16_t *G, int64_t M,
+                         int64_t K, double eps, uint16_t *Xn)
+{
+    double *row = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+    for (int64_t m = 0; m < M; m++) {
+        oracle_rmsnorm_f64(X + m * K, G, 1, K, eps, row);
+        for (int64_t k = 0; k < K; k++)
+            Xn[m * K + k] = oracle_double_to_bf16_rne(row[k]);
+    }
+    free(row);
 }
 
 /* Gated SiLU of two GEMV results of the same shape: out = silu(A) * B with

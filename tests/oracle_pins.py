@@ -82,6 +82,17 @@ def f64_to_bf16_exact(v: np.ndarray) -> np.ndarray:
     return (b >> 16).astype(np.uint16)
 
 
+def np_round_bf16(v: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bf16 value, ties to even, computed
+    exactly in float64 (8 significant bits; spacing 2^-133 below 2^-126).
+    Returns float64. Finite inputs inside the bf16 range only."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, e = np.frexp(a)  # a = f * 2^e, f in [0.5, 1)
+    spacing = np.ldexp(1.0, np.maximum(e - 8, -133))
+    return np.sign(v) * np.rint(a / spacing) * spacing
+
+
 def sum_bound(K: int, yabs: np.ndarray) -> np.ndarray:
     """Bound on the rounding error of a K-term fp64 sum with sum |terms| = yabs."""
     return K * 2.0 ** -53 * yabs + 1e-300
@@ -550,6 +561,36 @@ def pin_rmsnorm_invariants(o):
         assert np.array_equal(o.rmsnorm_bf16(X[m], G, 1e-6), o.rmsnorm_bf16(X, G, 1e-6)[m])
 
 
+def pin_rmsnorm_f64(o):
+    """The unrounded normalised activation: a worked case, an independent
+    50-digit decimal evaluation of x * g / sqrt(mean(x^2) + eps), the unit
+    mean square with g = 1, and its bf16 rounding equal to rmsnorm_bf16."""
+    import decimal
+
+    # x = (3, 4), g = 1, eps = 0: mean(x^2) = 12.5, so v = (3, 4) / sqrt(12.5)
+    v = o.rmsnorm_f64(np.array([0x4040, 0x4080], dtype=np.uint16), np.array([0x3F80, 0x3F80], dtype=np.uint16), 0.0)
+    assert abs(v[0] - 0.848528137423857) <= 1e-15 and abs(v[1] - 1.131370849898476) <= 1e-15, v
+    K = 96
+    X = gen.bf16_activations(133, 0, 3, K)
+    G = gen.bf16_weights(133, 1, 1, K)[0]
+    eps = 1e-5
+    V = o.rmsnorm_f64(X, G, eps)
+    ctx = decimal.Context(prec=50)
+    Xf, Gf = np_bf16_to_f64(X), np_bf16_to_f64(G)
+    for m in range(3):
+        ss = sum((ctx.multiply(decimal.Decimal(float(x)), decimal.Decimal(float(x))) for x in Xf[m]),
+                 decimal.Decimal(0))
+        root = ctx.sqrt(ctx.add(ctx.divide(ss, decimal.Decimal(K)), decimal.Decimal(eps)))
+        for k in range(K):
+            want = float(ctx.divide(ctx.multiply(decimal.Decimal(float(Xf[m, k])), decimal.Decimal(float(Gf[k]))),
+                                    root))
+            assert abs(V[m, k] - want) <= 4 * 2.0 ** -52 * abs(want), (m, k, V[m, k], want)
+    ones = np.full(K, 0x3F80, dtype=np.uint16)
+    U = o.rmsnorm_f64(X, ones, 0.0)
+    assert np.all(np.abs(np.mean(U * U, axis=1) - 1.0) < 1e-13)
+    assert np.array_equal(np_round_bf16(V), np_bf16_to_f64(o.rmsnorm_bf16(X, G, eps)))
+
+
 def pin_swiglu_identities(o):
     a = np.random.default_rng(5).standard_normal(2000) * 6.0
     ones = np.ones_like(a)
@@ -642,6 +683,7 @@ PINS = [
     pin_int8_quantizer_properties,
     pin_fusions_hand_worked,
     pin_rmsnorm_invariants,
+    pin_rmsnorm_f64,
     pin_swiglu_identities,
     pin_repack_hand_worked,
     pin_repack_permutation,

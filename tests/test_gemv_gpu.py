@@ -454,3 +454,45 @@ def test_weights_at_a_32_byte_offset_every_plan(orc):
     # 16 bytes is not enough
     with pytest.raises(mbw.MbwError):
         mbw.gemv_int8_pc(bigq[16:16 + N * K].view(N, K), torch.from_numpy(sq).cuda(), dev_bf16(X[0]))
+
+
+# ------------------------------------ every plan at the Qwen2.5-7B BF16 shapes ----
+@pytest.mark.parametrize("N,K", [(4608, 3584), (3584, 3584), (18944, 3584), (3584, 18944), (152064, 3584)])
+def test_bf16_every_plan_at_qwen_step_shapes(orc, N, K):
+    """Every candidate plan of the batch-1 BF16 GEMV (each family,
+    instantiation, split-K factor and CTAs per SM), then the autotuned plan,
+    at the shapes of the Qwen2.5-7B decode step; every row against the
+    oracle. The weights come from the device generator (bit-identical to the
+    host one, test_device_generator_matches_host) and are read back for the
+    oracle."""
+    op = mbw.OP_GEMV_BF16
+    Wd = inputs_gpu.bf16_weights(0, 11, N, K)
+    xd = inputs_gpu.bf16_activations(0, 12, 1, K)[0]
+    Y, A = orc.gemm_bf16(host_bits16(Wd).reshape(N, K), host_bits16(xd)[None, :])
+    for i, desc in each_plan(op, 1, N, K):
+        assert_parity(mbw.gemv_bf16(Wd, xd), Y[0], A[0], f"bf16 {N}x{K} plan {i}: {desc}")
+    mbw.autotune(op, 1, N, K)
+    assert 0 <= mbw.plan_index(op, 1, N, K) < mbw.plan_candidates(op, 1, N, K)
+    assert_parity(mbw.gemv_bf16(Wd, xd), Y[0], A[0], f"bf16 {N}x{K} autotuned: {mbw.plan_describe(op, 1, N, K)}")
+
+
+@pytest.mark.parametrize("M", [8, 32, 128])
+@pytest.mark.parametrize("N,K", [(18944, 3584), (3584, 18944)])
+def test_skinny_every_plan_at_qwen_mlp_shapes(orc, M, N, K):
+    """Every candidate plan of the skinny BF16 GEMM, then the autotuned plan,
+    at the Qwen2.5-7B MLP shapes and batches 8, 32 and 128: every batch row of
+    112 sampled weight rows (the first and last 16 and 80 at random)."""
+    op = mbw.OP_GEMM_SKINNY_BF16
+    rows = np.unique(np.concatenate([np.arange(0, 16), np.arange(N - 16, N),
+                                     np.random.default_rng(N + 7 * M).integers(0, N, 80)]))
+    Wd = inputs_gpu.bf16_weights(0, 13, N, K)
+    Xd = inputs_gpu.bf16_activations(0, 14, M, K)
+    Wr = np.stack([gen.bf16_weights(0, 13, N, K, row0=int(r), rows=1)[0] for r in rows])
+    Yr, Ar = orc.gemm_bf16(Wr, host_bits16(Xd))
+    sel = torch.from_numpy(rows).cuda()
+    for i, desc in each_plan(op, M, N, K):
+        Y = mbw.gemm_skinny_bf16(Xd, Wd)
+        assert_parity(Y[:, sel], Yr, Ar, f"skinny M={M} {N}x{K} plan {i}: {desc}")
+    mbw.autotune(op, M, N, K)
+    Y = mbw.gemm_skinny_bf16(Xd, Wd)
+    assert_parity(Y[:, sel], Yr, Ar, f"skinny M={M} {N}x{K} autotuned: {mbw.plan_describe(op, M, N, K)}")
