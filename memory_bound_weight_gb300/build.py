@@ -26,7 +26,7 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-
 
 # translation units of libmbw.so (the product) and of the input generator
 LIB_SOURCES = ["abi.cu", "plan.cu", "gemv_simt.cu", "gemv_mma.cu", "gemv_tma.cu", "gemv_lat.cu", "gemm_tc.cu",
-               "quantize.cu"]
+               "gemv_awq_batch.cu", "quantize.cu"]
 GEN_SOURCES = ["gen_inputs.cu"]
 
 

@@ -81,6 +81,16 @@ struct TmaConfig {
     int depth;  // shared-memory ring stages
 };
 
+// One instantiation of the batched AWQ mma.sync kernel (gemv_awq_batch.cu).
+struct AwqbConfig {
+    int nb;    // n-blocks of 8 batch rows (the launch covers up to 8 * nb rows)
+    int wt;    // warps along the CTA's tiles (warp (wt, wk) owns tiles wt, wt + WT, ...)
+    int wk;    // warps along the CTA's k-range (each an even share of its super-blocks)
+    int u;     // super-blocks (256 k) per lane in flight (register ring depth)
+    int minb;  // CTAs per SM its register budget allows (at most this many per SM)
+    int early; // 1: a ring slot is refilled before its super-block is computed
+};
+
 // Execution plan of one call shape.
 struct Plan {
     int kind;   // PLAN_SIMT or PLAN_MMA
@@ -88,7 +98,15 @@ struct Plan {
     int split;  // CTAs per cluster along K (1 = no split)
     int occ;    // MMA kernels: CTAs per SM in the persistent grid (1 for SIMT)
 };
-enum PlanKind : int { PLAN_SIMT = 0, PLAN_MMA = 1, PLAN_TMA = 2, PLAN_MMA2 = 3, PLAN_TC = 4, PLAN_LAT = 5 };
+enum PlanKind : int {
+    PLAN_SIMT = 0,
+    PLAN_MMA = 1,
+    PLAN_TMA = 2,
+    PLAN_MMA2 = 3,
+    PLAN_TC = 4,
+    PLAN_LAT = 5,
+    PLAN_AWQB = 6,
+};
 
 // Kernel tables (gemv_simt.cu).
 int simt_num_configs(int fmt);
@@ -121,6 +139,14 @@ int lat_items_per_warp(int fmt, const LatConfig& c, int64_t N, int64_t K, int sp
 size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu = 0,
                       int fz = 0);
 cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
+
+// Batched AWQ mma.sync kernel tables (gemv_awq_batch.cu): batches of 5 .. 64
+// rows per launch, K % 256 == 0.
+int awqb_num_configs();
+AwqbConfig awqb_config(int idx);
+int awqb_row_groups(int64_t N, int split, int occ);
+size_t awqb_smem_bytes(const AwqbConfig& c, int64_t N, int64_t K, int split, int occ);
+cudaError_t launch_gemv_awq_batch(const Plan& p, const GemvArgs& a, cudaStream_t s);
 
 // tcgen05 skinny GEMM (gemm_tc.cu): Y = X . W^T for the whole batch M.
 // cfg bit 0: ring (0 deep, 1 co-resident); bit 1: two 64-k boxes per stage

@@ -51,14 +51,24 @@ static size_t simt_smem(int fmt, const SimtConfig& c, int64_t K, int split) {
 // SIMT batch width for a call of M rows: the smallest kernel batch >= min(M, 8).
 static int simt_want_mb(int64_t M) { return M <= 2 ? (int)M : M <= 4 ? 4 : 8; }
 
+// n-blocks of 8 columns the batched AWQ mma.sync kernel runs for a call of M
+// rows: the fewest covering min(M, 64).
+static int awqb_want_nb(int64_t M) {
+    const int64_t m = std::min<int64_t>(M, 64);
+    return m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8;
+}
+
+// Plan-cache key of the batch: calls whose M share a key share a plan, so
+// every candidate valid for one M of a key must be valid for all of them.
 static int batch_key(int op, int64_t M) {
     if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 8) return tc_batch_tile(M);
-    if ((op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4) return 1000 + tc_awq_batch_tile(M);
+    if ((op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4) return 1000 + 8 * awqb_want_nb(M);
     return (int)std::min<int64_t>(M, 8);
 }
 
 int plan_batch_width(int fmt, const Plan& p) {
     if (p.kind == PLAN_TC) return 1 << 30;  // one launch covers the whole batch
+    if (p.kind == PLAN_AWQB) return 8 * awqb_config(p.cfg).nb;
     if (p.kind == PLAN_MMA2) return mma2_max_batch(fmt);
     if (p.kind == PLAN_LAT) return lat_max_batch(fmt);
     if (p.kind == PLAN_MMA || p.kind == PLAN_TMA) return mma_max_batch(fmt);
@@ -98,6 +108,22 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K, 
         if (p.split > KS) return false;
         const int64_t per = (KS + p.split - 1) / p.split;
         return per * (p.split - 1) < KS;  // every cluster rank gets k-stages
+    }
+    if (p.kind == PLAN_AWQB) {
+        // batched AWQ on mma.sync: batches above the GEMV column width, whole
+        // super-blocks of 256 k, at least one per cluster rank
+        if (fmt != FMT_AWQ || M <= 4 || p.cfg < 0 || p.cfg >= awqb_num_configs()) return false;
+        const AwqbConfig c = awqb_config(p.cfg);
+        // the fewest n-blocks covering the batch, or down to a quarter of them
+        // in slices (each slice streams the weights again; past 16 rows the
+        // kernel is bound by the MMA rate rather than the weight stream, and
+        // narrower slices stage less of X in shared memory)
+        const int want = awqb_want_nb(M);
+        if (c.nb > want || 4 * c.nb < want) return false;
+        if (K % 256 != 0 || p.occ < 1 || p.occ > c.minb || K / 256 < p.split) return false;
+        if ((uint64_t)N * (uint64_t)(K / 2) > 0xFFFFFFFFull) return false;  // 32-bit load offsets
+        const size_t sm = awqb_smem_bytes(c, N, K, p.split, p.occ);
+        return sm <= kSmemLimit && sm * p.occ <= (size_t)227 * 1024;
     }
     if (p.kind == PLAN_SIMT) {
         if (p.cfg < 0 || p.cfg >= simt_num_configs(fmt) || p.occ != 1) return false;
@@ -159,11 +185,18 @@ static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
     const int fmt = fmt_of_op(op);
     const int flags = op & (MBW_FUSE_MASK | MBW_REPACKED);
     const int64_t Mb = std::min<int64_t>(M, 8);
-    if ((op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4)
+    if ((op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4) {
         for (int sp = 1; sp <= 8; ++sp) {
             Plan p{PLAN_TC, 0, sp, 1};
             if (plan_valid(fmt, p, M, N, K, flags)) out.push_back(p);
         }
+        for (int cfg = 0; cfg < awqb_num_configs(); ++cfg)
+            for (int sp = 1; sp <= 8; sp *= 2)
+                for (int occ = 1; occ <= 2; ++occ) {
+                    Plan p{PLAN_AWQB, cfg, sp, occ};
+                    if (plan_valid(fmt, p, M, N, K, flags)) out.push_back(p);
+                }
+    }
     if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 4)
         for (int cfg = 0; cfg <= 7; ++cfg)
             for (int sp = 1; sp <= 8; ++sp) {
@@ -209,6 +242,25 @@ Plan plan_default(int op, int64_t M, int64_t N, int64_t K) {
     const int fuse = op & MBW_FUSE_MASK;
     const int64_t Mb = std::min<int64_t>(M, 8);
     const int sms = device_sm_count();
+    if ((op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4) {
+        // batched AWQ on mma.sync: 8 warps, 2 super-blocks in flight; split K
+        // over a cluster while the 16-row tiles do not cover the SMs
+        const int want = awqb_want_nb(M);
+        for (int i = 0; i < awqb_num_configs(); ++i) {
+            const AwqbConfig c = awqb_config(i);
+            if (c.nb != want || c.wt * c.wk != 8) continue;
+            const int64_t tiles = (N + 15) / 16;
+            for (int occ = c.minb; occ >= 1; --occ) {
+                // split while the tiles do not cover the SMs or X does not fit
+                Plan p{PLAN_AWQB, i, 1, occ};
+                while (p.split < 8 && K / 256 / (2 * p.split) >= c.wk &&
+                       (tiles * p.split < (int64_t)sms * occ || !plan_valid(fmt, p, M, N, K, flags)))
+                    p.split *= 2;
+                if (plan_valid(fmt, p, M, N, K, flags)) return p;
+            }
+            break;
+        }
+    }
     if ((op == MBW_OP_GEMM_SKINNY_BF16 && M > 8) ||
         ((op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4)) {
         // tcgen05 tiles of 128 weight rows; split K over a cluster until the
@@ -283,7 +335,13 @@ std::string plan_to_string(int op, const Plan& p) {
     const int fmt = fmt_of_op(op);
     const char* fs = fmt == FMT_BF16 ? "bf16" : fmt == FMT_G64 ? "int4_g64" : fmt == FMT_I8 ? "int8_pc" : "int4_awq_g128";
     char buf[192];
-    if (p.kind == PLAN_TC) {
+    if (p.kind == PLAN_AWQB) {
+        const AwqbConfig c = awqb_config(p.cfg);
+        snprintf(buf, sizeof(buf),
+                 "awq_mma fmt=%s batch_cols=%d warps=%d (tiles %d x k %d) superblocks_in_flight=%d refill=%s "
+                 "ctas_per_sm=%d split_k=%d",
+                 fs, 8 * c.nb, c.wt * c.wk, c.wt, c.wk, c.u, c.early ? "early" : "late", p.occ, p.split);
+    } else if (p.kind == PLAN_TC) {
         if (fmt == FMT_AWQ)
             snprintf(buf, sizeof(buf), "tcgen05 fmt=%s tile=128xbatch k_stage=128 (one group) split_k=%d", fs, p.split);
         else
@@ -323,6 +381,7 @@ std::string plan_to_string(int op, const Plan& p) {
 }
 
 cudaError_t launch_plan(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
+    if (p.kind == PLAN_AWQB) return launch_gemv_awq_batch(p, a, s);
     if (p.kind == PLAN_TC && fmt == FMT_AWQ)
         return launch_gemm_tc_awq(a.W, a.scales, a.zeros, a.x, a.y, a.M, a.N, a.K, p.split, a.out_f32, a.x_natural,
                                   s);

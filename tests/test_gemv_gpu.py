@@ -381,9 +381,10 @@ def test_int4_awq_batched_all_plans(orc, N, K, M):
 
 
 def test_int4_awq_batched_one_hot_rows_exact(orc):
-    """Batch row m = e_{k_m}: with fp32 output every tensor-core plan returns
-    column k_m of the dequantized weights exactly (exact unpack, exact
-    products, the group scale applied in fp32 to a single nonzero term)."""
+    """Batch row m = e_{k_m}: with fp32 output every tensor-core plan (tcgen05
+    and the batched mma.sync family) returns column k_m of the dequantized
+    weights exactly (exact unpack, exact products, the group scale applied in
+    fp32 to a single nonzero term)."""
     N, K, M = 200, 1024, 24
     c, s, z, _ = awq_case(811, N, K, 1)
     deq = orc.dequant_int4_awq_g128(c, s, z, N, K)
@@ -393,7 +394,7 @@ def test_int4_awq_batched_one_hot_rows_exact(orc):
         X[m, k] = 0x3F80
     cd, sd, zd, Xd = dev_u8(c), dev_f16(s), dev_u8(z), dev_bf16(X)
     for i, desc in each_plan(mbw.OP_GEMV_INT4_AWQ_G128, M, N, K):
-        if not desc.startswith("tcgen05"):
+        if not desc.startswith(("tcgen05", "awq_mma")):
             continue
         with mbw.output_fp32():
             y = mbw.gemv_int4_awq_g128(cd, sd, zd, Xd)
@@ -413,7 +414,7 @@ def test_int4_awq_batched_config_shapes_sampled_rows(orc, M, N, K):
     zd = inputs_gpu.u4_zero_points(0, 21, N, G)
     Xd = inputs_gpu.bf16_activations(0, 22, M, K)
     Y = mbw.gemv_int4_awq_g128(cd, sd, zd, Xd)
-    assert mbw.plan_describe(mbw.OP_GEMV_INT4_AWQ_G128, M, N, K).startswith("tcgen05")
+    assert mbw.plan_describe(mbw.OP_GEMV_INT4_AWQ_G128, M, N, K).startswith(("tcgen05", "awq_mma"))
     c = np.stack([gen.int4_codes(0, 21, N, K, row0=int(r), rows=1)[0] for r in rows])
     s = np.stack([gen.f16_group_scales(0, 21, N, G, row0=int(r), rows=1)[0] for r in rows])
     z = np.stack([gen.u4_zero_points(0, 21, N, G, row0=int(r), rows=1)[0] for r in rows])
