@@ -43,6 +43,7 @@ def main():
     elif a.plan != "default":
         mbw.plan_select(op, M, N, K, int(a.plan))
     print("plan:", mbw.plan_describe(op, M, N, K), flush=True)
+    print("plan index:", mbw.plan_index(op, M, N, K), flush=True)
 
     X = ig.bf16_activations(0, 1, M, K)
     if op in (1, 4):
