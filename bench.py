@@ -58,6 +58,12 @@ TRAFFIC = {
     # 1 launch, dram__bytes_read.sum 49,946,368 + dram__bytes_write.sum 768
     # (profiles/gemv_mma2_int8_19456x2560.md)
     ("48716c9f658135ec", "19456x2560"): 49947136,
+    # the Qwen2.5-7B gate/up matrices (BF16, 18944x3584), the default step's dominant kernel, on either of the
+    # two plans the tuner picks there: gemv_simt (4 warps, 4 rows per warp) dram__bytes_read.sum 135,820,032 +
+    # dram__bytes_write.sum 2,951,680; gemv_mma2 (8 warps, 2 super-blocks in registers) 135,848,192 + 2,951,936
+    # (profiles/gemv_simt_bf16_18944x3584.md)
+    ("ed306bd65499f91f", "18944x3584"): 138771712,
+    ("48716c9f658135ec", "18944x3584"): 138800128,
 }
 
 
