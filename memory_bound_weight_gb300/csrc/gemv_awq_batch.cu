@@ -87,24 +87,31 @@ __device__ __forceinline__ uint4 awqb_perm(uint4 v) {
 // Shared memory of one launch: staged X [Mp][pitch] 16-byte chunks, then the
 // warps' per-tile partials [ntmax][WK][16][Mp] fp32 (when WK > 1 or S > 1),
 // then (WK > 1 and S > 1) the CTA's tile sums [ntmax][16][Mp] fp32 for the
-// cluster's sum.
+// cluster's sum; with the shared-memory ring (async) also the warps' rings
+// [W][U][4][32][16 B] and the CTA's scale [ntmax][16][2 kbr] fp16 and zero-point
+// [ntmax][16][kbr] byte tables.
 struct AwqbSmem {
     int pitch;  // 16-byte chunks per staged X row
     int ntmax;  // most tiles any CTA owns
-    size_t red_off, fin_off, total;
+    int kbr;    // most super-blocks any cluster rank owns
+    size_t red_off, fin_off, ring_off, stab_off, ztab_off, total;
 };
 
-__host__ __device__ inline AwqbSmem awqb_smem_layout(int64_t K, int64_t N, int Mp, int WK, int S, int G) {
+__host__ __device__ inline AwqbSmem awqb_smem_layout(int64_t K, int64_t N, int Mp, int W, int WK, int U, int async,
+                                                     int S, int G) {
     AwqbSmem L;
     const int KB = (int)(K / 256);
-    const int kbr = (KB + S - 1) / S;
-    L.pitch = kbr * 32 + 4;
+    L.kbr = (KB + S - 1) / S;
+    L.pitch = L.kbr * 32 + 4;
     const int64_t T = (N + 15) / 16;
     L.ntmax = (int)((T + G - 1) / G);
     L.red_off = (size_t)Mp * L.pitch * 16;
     const size_t red = (WK > 1 || S > 1) ? (size_t)L.ntmax * WK * 16 * Mp * 4 : 0;
     L.fin_off = L.red_off + red;
-    L.total = L.fin_off + ((WK > 1 && S > 1) ? (size_t)L.ntmax * 16 * Mp * 4 : 0);
+    L.ring_off = L.fin_off + ((WK > 1 && S > 1) ? (size_t)L.ntmax * 16 * Mp * 4 : 0);
+    L.stab_off = L.ring_off + (async ? (size_t)W * U * 2048 : 0);
+    L.ztab_off = L.stab_off + (async ? (size_t)L.ntmax * 16 * 2 * L.kbr * 2 : 0);
+    L.total = L.ztab_off + (async ? ((size_t)L.ntmax * 16 * L.kbr + 15) / 16 * 16 : 0);
     return L;
 }
 
@@ -113,7 +120,11 @@ __host__ __device__ inline AwqbSmem awqb_smem_layout(int64_t K, int64_t N, int M
 // EARLY: 1 = a ring slot is copied out and refilled before its super-block is
 // computed (U super-blocks of loads in flight during the compute, 19 more
 // registers), 0 = refilled after (U - 1 in flight).
-template <int NB, int WT, int WK, int U, int MINB, int EARLY>
+// ASYNC: 1 = the ring is in shared memory, filled by each lane's own 16-byte
+// cp.async copies (a quad's four copies of a row's group are one 64-byte run:
+// whole sectors), U slots deep per warp, refilled after its super-block is
+// computed; scales and zero points come from per-CTA tables loaded once.
+template <int NB, int WT, int WK, int U, int MINB, int EARLY, int ASYNC>
 __global__ void __launch_bounds__(WT * WK * 32, MINB) gemv_awq_batch_kernel(const GemvArgs a, const int S) {
     constexpr int W = WT * WK;
     constexpr int MP = 8 * NB;  // batch rows of the launch, padded
@@ -130,7 +141,7 @@ __global__ void __launch_bounds__(WT * WK * 32, MINB) gemv_awq_batch_kernel(cons
     const int T = (a.N + 15) / 16;
     const int t0 = (int)(((long long)T * cgid) / G);
     const int nt = (int)(((long long)T * (cgid + 1)) / G) - t0;
-    const AwqbSmem L = awqb_smem_layout(a.K, a.N, MP, WK, S, G);
+    const AwqbSmem L = awqb_smem_layout(a.K, a.N, MP, W, WK, U, ASYNC, S, G);
 
     // super-blocks of this cluster rank, then of this warp's k-slice (may be none)
     const int KB = a.K / 256;
@@ -163,7 +174,22 @@ __global__ void __launch_bounds__(WT * WK * 32, MINB) gemv_awq_batch_kernel(cons
     uint4 rc[U][4];    // [u][0] row g group 0, [1] row g group 1, [2] row g+8 group 0, [3] row g+8 group 1
     uint32_t rs[U][2];  // fp16 scales of groups 0 | 1 << 16: row g, row g+8
     uint32_t rz[U];     // zero-point byte of row g (bits 0-7) and row g+8 (bits 8-15)
+    // async ring of this warp: slot u, chunk c (the rc[u][c] order) of lane L at (u * 4 + c) * 512 + L * 16
+    uint8_t* aring = reinterpret_cast<uint8_t*>(smem_u4) + L.ring_off + (size_t)warp * U * 2048 + lane * 16;
     auto load = [&](int u) {
+        if (ASYNC) {
+            cp_async16(aring + (size_t)(u * 4 + 0) * 512, a.W + wo0);
+            cp_async16(aring + (size_t)(u * 4 + 1) * 512, a.W + wo0 + 64);
+            cp_async16(aring + (size_t)(u * 4 + 2) * 512, a.W + wo1);
+            cp_async16(aring + (size_t)(u * 4 + 3) * 512, a.W + wo1 + 64);
+            wo0 += 128;
+            wo1 += 128;
+            if (++lb == nbw) {
+                lb = 0;
+                if (++lt < ntw) set_rows(lt);
+            }
+            return;
+        }
         rc[u][0] = ld_stream16(a.W + wo0);
         rc[u][1] = ld_stream16(a.W + wo0 + 64);
         rc[u][2] = ld_stream16(a.W + wo1);
@@ -183,8 +209,25 @@ __global__ void __launch_bounds__(WT * WK * 32, MINB) gemv_awq_batch_kernel(cons
         }
     };
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+    for (int u = 0; u < U; ++u) {
         if (u < total) load(u);
+        if (ASYNC) cp_async_commit();  // one group per step, empty past the end
+    }
+    uint16_t* stab = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(smem_u4) + L.stab_off);
+    uint8_t* ztab = reinterpret_cast<uint8_t*>(smem_u4) + L.ztab_off;
+    if (ASYNC) {
+        // the CTA's scales (2 per super-block) and zero-point bytes (1 per
+        // super-block) of its rows and this rank's super-blocks; weights-side
+        // data, read before the wait
+        for (int i = threadIdx.x; i < nt * 16 * nkb; i += W * 32) {
+            const int tr = i / nkb, sbl = i - tr * nkb;
+            const int row = min((t0 + tr / 16) * 16 + (tr & 15), a.N - 1);
+            const size_t gi = (size_t)row * a.groups + (size_t)(kb0 + sbl) * 2;
+            stab[((size_t)tr * L.kbr + sbl) * 2] = ld_ro_u16(a.scales + gi);
+            stab[((size_t)tr * L.kbr + sbl) * 2 + 1] = ld_ro_u16(a.scales + gi + 1);
+            ztab[(size_t)tr * L.kbr + sbl] = ld_ro_u8(a.zeros + (size_t)row * a.zstride + kb0 + sbl);
+        }
+    }
 
     prefetch_l2_grid_share(a.x, (size_t)a.M * a.K * 2);
     pdl_wait();
@@ -222,12 +265,23 @@ __global__ void __launch_bounds__(WT * WK * 32, MINB) gemv_awq_batch_kernel(cons
                 const uint4* xb = xl + j * 32;
                 uint4 cw[4];
                 uint32_t cs[2], cz;
+                if (ASYNC) {
+                    cp_async_wait<U - 1>();  // this lane's copies of the step have landed
 #pragma unroll
-                for (int e = 0; e < 4; ++e) cw[e] = rc[u][e];
-                cs[0] = rs[u][0];
-                cs[1] = rs[u][1];
-                cz = rz[u];
-                if (EARLY && s0 + u + U < total) load(u);
+                    for (int e = 0; e < 4; ++e) cw[e] = *reinterpret_cast<const uint4*>(aring + (size_t)(u * 4 + e) * 512);
+                    const int tr = (wt + lt2 * WT) * 16, sbl = wb0 - kb0 + j;
+                    cs[0] = *reinterpret_cast<const uint32_t*>(stab + ((size_t)(tr + g) * L.kbr + sbl) * 2);
+                    cs[1] = *reinterpret_cast<const uint32_t*>(stab + ((size_t)(tr + g + 8) * L.kbr + sbl) * 2);
+                    cz = (uint32_t)ztab[(size_t)(tr + g) * L.kbr + sbl] |
+                         ((uint32_t)ztab[(size_t)(tr + g + 8) * L.kbr + sbl] << 8);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) cw[e] = rc[u][e];
+                    cs[0] = rs[u][0];
+                    cs[1] = rs[u][1];
+                    cz = rz[u];
+                    if (EARLY && s0 + u + U < total) load(u);
+                }
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t zb = cz;
@@ -271,8 +325,9 @@ __global__ void __launch_bounds__(WT * WK * 32, MINB) gemv_awq_batch_kernel(cons
                         acc[nb][3] = fmaf(f1, dl[nb][3], acc[nb][3]);
                     }
                 }
-                // the slot's registers are consumed: refill it U super-blocks ahead
-                if (!EARLY && s0 + u + U < total) load(u);
+                // the slot is consumed (its values have fed the MMAs): refill it U super-blocks ahead
+                if ((ASYNC || !EARLY) && s0 + u + U < total) load(u);
+                if (ASYNC) cp_async_commit();
                 if (++j == nbw) {
                     // this warp's k-slice of tile t done: store it (one k-slice, no
                     // cluster) or keep the partial for the sums after the loop
@@ -360,14 +415,16 @@ struct AwqbEntry {
 };
 // WT x WK warps; MINB: CTAs per SM the instantiation is register-bounded for
 // (128 registers per thread at 16 warps per SM; up to 255 with fewer);
-// EARLY: refill before the compute (see the kernel)
-#define MBW_AB(NB, WT, WK, U, MINB, EARLY) \
-    { {NB, WT, WK, U, MINB, EARLY}, gemv_awq_batch_kernel<NB, WT, WK, U, MINB, EARLY> }
+// EARLY: refill before the compute; ASYNC: shared-memory ring (see the kernel)
+#define MBW_AB(NB, WT, WK, U, MINB, EARLY, ASYNC) \
+    { {NB, WT, WK, U, MINB, EARLY, ASYNC}, gemv_awq_batch_kernel<NB, WT, WK, U, MINB, EARLY, ASYNC> }
 static const AwqbEntry kAwqb[] = {
-    MBW_AB(1, 8, 1, 3, 2, 0), MBW_AB(1, 8, 2, 3, 1, 0), MBW_AB(1, 8, 2, 2, 1, 1), MBW_AB(1, 8, 1, 5, 1, 1),
-    MBW_AB(2, 8, 2, 2, 1, 0), MBW_AB(2, 8, 2, 2, 1, 1), MBW_AB(2, 8, 1, 4, 1, 1), MBW_AB(2, 8, 1, 6, 1, 0),
-    MBW_AB(2, 4, 2, 4, 1, 1), MBW_AB(4, 8, 1, 2, 1, 0), MBW_AB(4, 8, 1, 3, 1, 1), MBW_AB(4, 4, 2, 3, 1, 1),
-    MBW_AB(8, 8, 1, 2, 1, 0),
+    MBW_AB(1, 8, 1, 3, 2, 0, 0), MBW_AB(1, 8, 2, 3, 1, 0, 0), MBW_AB(1, 8, 2, 2, 1, 1, 0), MBW_AB(1, 8, 1, 5, 1, 1, 0),
+    MBW_AB(1, 8, 2, 4, 1, 0, 1), MBW_AB(1, 8, 1, 6, 2, 0, 1), MBW_AB(2, 8, 2, 2, 1, 0, 0), MBW_AB(2, 8, 2, 2, 1, 1, 0),
+    MBW_AB(2, 8, 1, 4, 1, 1, 0), MBW_AB(2, 8, 1, 6, 1, 0, 0), MBW_AB(2, 4, 2, 4, 1, 1, 0), MBW_AB(2, 8, 2, 4, 1, 0, 1),
+    MBW_AB(2, 8, 2, 6, 1, 0, 1), MBW_AB(2, 8, 1, 8, 2, 0, 1), MBW_AB(4, 8, 1, 2, 1, 0, 0), MBW_AB(4, 8, 1, 3, 1, 1, 0),
+    MBW_AB(4, 4, 2, 3, 1, 1, 0), MBW_AB(4, 8, 2, 4, 1, 0, 1), MBW_AB(4, 8, 1, 6, 1, 0, 1), MBW_AB(8, 8, 1, 2, 1, 0, 0),
+    MBW_AB(8, 8, 1, 4, 1, 0, 1),
 };
 #undef MBW_AB
 
@@ -385,7 +442,7 @@ int awqb_row_groups(int64_t N, int split, int occ) {
 
 size_t awqb_smem_bytes(const AwqbConfig& c, int64_t N, int64_t K, int split, int occ) {
     const int G = awqb_row_groups(N, split, occ);
-    return awqb_smem_layout(K, N, 8 * c.nb, c.wk, split, G).total;
+    return awqb_smem_layout(K, N, 8 * c.nb, c.wt * c.wk, c.wk, c.u, c.async, split, G).total;
 }
 
 cudaError_t launch_gemv_awq_batch(const Plan& p, const GemvArgs& a, cudaStream_t s) {

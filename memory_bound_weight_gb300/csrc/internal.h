@@ -89,6 +89,7 @@ struct AwqbConfig {
     int u;     // super-blocks (256 k) per lane in flight (register ring depth)
     int minb;  // CTAs per SM its register budget allows (at most this many per SM)
     int early; // 1: a ring slot is refilled before its super-block is computed
+    int async; // 1: the ring is in shared memory (cp.async), scales and zero points in per-CTA tables
 };
 
 // Execution plan of one call shape.

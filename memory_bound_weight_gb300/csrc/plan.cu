@@ -338,9 +338,10 @@ std::string plan_to_string(int op, const Plan& p) {
     if (p.kind == PLAN_AWQB) {
         const AwqbConfig c = awqb_config(p.cfg);
         snprintf(buf, sizeof(buf),
-                 "awq_mma fmt=%s batch_cols=%d warps=%d (tiles %d x k %d) superblocks_in_flight=%d refill=%s "
+                 "awq_mma fmt=%s batch_cols=%d warps=%d (tiles %d x k %d) superblocks_in_flight=%d ring=%s "
                  "ctas_per_sm=%d split_k=%d",
-                 fs, 8 * c.nb, c.wt * c.wk, c.wt, c.wk, c.u, c.early ? "early" : "late", p.occ, p.split);
+                 fs, 8 * c.nb, c.wt * c.wk, c.wt, c.wk, c.u,
+                 c.async ? "smem" : c.early ? "registers refill=early" : "registers refill=late", p.occ, p.split);
     } else if (p.kind == PLAN_TC) {
         if (fmt == FMT_AWQ)
             snprintf(buf, sizeof(buf), "tcgen05 fmt=%s tile=128xbatch k_stage=128 (one group) split_k=%d", fs, p.split);
