@@ -75,7 +75,7 @@ def parse_args():
     p.add_argument("--impl", default="mbw", choices=["mbw", "reference"])
     p.add_argument("--workload", default="qwen_bf16",
                    choices=["tinyllama_int4", "tinyllama_int4_fusedops", "tinyllama_int4_unfused", "qwen_bf16",
-                            "qwen_awq", "qwen_awq_repacked", "qwen3_int8", "bf16_2048"])
+                            "qwen_awq", "qwen_awq_repacked", "qwen_awq_fusedops", "qwen3_int8", "bf16_2048"])
     p.add_argument("--batch", type=int, default=1,
                    help="activation rows per GEMV (qwen_awq: AWQ-style INT4 decode at batch M)")
     p.add_argument("--no-e2e", action="store_true")
@@ -293,6 +293,27 @@ def device_call(fmt, seed, mi, N, K, x, y, device, fuse=0, M=1, repacked=False):
     from memory_bound_weight_gb300 import inputs as gen
     from memory_bound_weight_gb300 import inputs_gpu
 
+    if fuse and fmt == wl.FMT_INT4_AWQ_G128:
+        def awq(m):
+            c = inputs_gpu.int4_codes(seed, m, N, K, device)
+            if repacked:
+                mbw.repack_int4(c, out=c)
+            return (c, inputs_gpu.f16_group_scales(seed, m, N, K // 128, device),
+                    inputs_gpu.u4_zero_points(seed, m, N, K // 128, device))
+        c, s, z = awq(mi)
+        kw = {"repacked": repacked}
+        if fuse & wl.FUSE_GLU:
+            kw["up_weights"], kw["up_scales"], kw["up_zeros"] = awq(50000 + mi)
+        if fuse & wl.FUSE_NORM:
+            g = torch_empty((K,), device)
+            inputs_gpu.bf16_normal_(g, seed, gen.stream_id(60000 + mi, gen.KIND_X), gen.X_SIGMA)
+            kw["norm_weight"], kw["norm_eps"] = g, 1e-6
+        if fuse & wl.FUSE_RESIDUAL:
+            r = torch_empty((M, N) if M > 1 else (N,), device)
+            inputs_gpu.bf16_normal_(r.view(-1), seed, gen.stream_id(70000 + mi, gen.KIND_X), gen.X_SIGMA)
+            kw["residual"] = r
+        return functools.partial(mbw.gemv_fused_awq_g128, c, s, z, x, **kw), (), y
+
     if fuse:
         base = op_of_fmt(fmt)
         W, sc = device_weights(fmt, seed, mi, N, K, device)
@@ -356,6 +377,7 @@ WORKLOAD_MATS = {
     "qwen_bf16": (wl.qwen25_7b_step, wl.FMT_BF16),
     "qwen_awq": (wl.qwen25_7b_step, wl.FMT_INT4_AWQ_G128),
     "qwen_awq_repacked": (wl.qwen25_7b_step, wl.FMT_INT4_AWQ_G128),
+    "qwen_awq_fusedops": (lambda: wl.qwen25_7b_step(fusedops=True), wl.FMT_INT4_AWQ_G128),
     "qwen3_int8": (wl.qwen3_4b_step, wl.FMT_INT8_PC),
     "bf16_2048": (lambda: [wl.Mat(f"copy{i}", 2048, 2048) for i in range(64)], wl.FMT_BF16),
 }
@@ -367,10 +389,12 @@ def make_step(workload, seed, device, M=1):
                     WORKLOAD_MATS[workload][0](), seed, device)
     if workload == "qwen_bf16":
         return Step("Qwen2.5-7B-shaped BF16 decode step, batch 1", wl.FMT_BF16, wl.qwen25_7b_step(), seed, device)
-    if workload in ("qwen_awq", "qwen_awq_repacked"):
-        rp = workload == "qwen_awq_repacked"
-        return Step(f"Qwen2.5-7B-shaped AWQ-style INT4 decode step, batch {M}" + (", repacked codes" if rp else ""),
-                    wl.FMT_INT4_AWQ_G128, wl.qwen25_7b_step(), seed, device, M, repacked=rp)
+    if workload in ("qwen_awq", "qwen_awq_repacked", "qwen_awq_fusedops"):
+        rp = workload != "qwen_awq"
+        fo = workload == "qwen_awq_fusedops"
+        return Step(f"Qwen2.5-7B-shaped AWQ-style INT4 decode step, batch {M}" + (", repacked codes" if rp else "")
+                    + (", small ops fused" if fo else ""),
+                    wl.FMT_INT4_AWQ_G128, wl.qwen25_7b_step(fusedops=fo), seed, device, M, repacked=rp)
     if workload == "qwen3_int8":
         return Step(f"Qwen3-4B-shaped symmetric INT8 per-channel decode step, batch {M}", wl.FMT_INT8_PC,
                     wl.qwen3_4b_step(), seed, device, M)
@@ -522,6 +546,10 @@ def workload_desc(workload, batch=1):
             "qwen_awq_repacked": f"Qwen2.5-7B-shaped AWQ-style INT4 decode step (group 128, fp16 scale, uint4 zero "
                                  f"point, LM head included), codes reordered at load time (mbw_repack_int4), batch "
                                  f"{batch} (141 GEMMs)",
+            "qwen_awq_fusedops": f"Qwen2.5-7B-shaped AWQ-style INT4 decode step (group 128, fp16 scale, uint4 zero "
+                                 f"point), codes reordered at load time, with the layer's small ops folded into the "
+                                 f"GEMVs: RMSNorm prologues (q/k/v, gate/up, head), SwiGLU epilogue (gate/up), "
+                                 f"residual-add epilogues (o, down), batch {batch} (113 GEMVs)",
             "qwen3_int8": f"Qwen3-4B-shaped symmetric INT8 decode step (one fp32 scale per output channel, every "
                           f"linear layer and the LM head, q/k/v and gate/up fused), batch {batch} (145 GEMVs)",
             "bf16_2048": "BF16 GEMV 2048x2048, batch 1, 64 rotating copies"}[workload]

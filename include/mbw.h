@@ -227,7 +227,10 @@ mbw_status mbw_quantize_int8_pc(const void *W, int8_t *Wq, float *scales, int64_
  *                 both sums in fp32; the call streams both matrices. With a
  *                 residual too, the residual is added after the product.
  *   up_scales   : the up matrix's scales (INT4 g64: fp16 [N][K/64]; INT8:
- *                 fp32 [N]; BF16: unused).
+ *                 fp32 [N]; AWQ: fp16 [N][K/128]; BF16: unused).
+ *   up_zeros    : the up matrix's zero points (AWQ only: uint8 [N][(K/128+1)/2],
+ *                 as gemv_int4_awq_g128's zeros); read by gemv_fused_awq_g128
+ *                 alone, and only with up_weights set.
  */
 typedef struct mbw_fusion {
     const void *norm_weight;
@@ -235,11 +238,13 @@ typedef struct mbw_fusion {
     const void *residual;
     const void *up_weights;
     const void *up_scales;
+    const void *up_zeros;
 } mbw_fusion;
 
 /*
  * gemv_fused -- one GEMV with the fusions of `fusion` (NULL: none), for
- * op = MBW_OP_GEMV_BF16, MBW_OP_GEMV_INT4_G64 (M = 1) or MBW_OP_GEMV_INT8_PC.
+ * op = MBW_OP_GEMV_BF16, MBW_OP_GEMV_INT4_G64 (M = 1) or MBW_OP_GEMV_INT8_PC
+ * (AWQ: gemv_fused_awq_g128, which also takes the zero points).
  * W / scales / X / Y and their layouts are those of the op's own call
  * (gemv_bf16: scales unused; gemv_int4_g64; gemv_int8_pc). Requires K > 0 and
  * the op's K multiple; norm_weight 16-byte aligned, up_weights 32-byte aligned,
@@ -250,6 +255,24 @@ typedef struct mbw_fusion {
 mbw_status gemv_fused(int op, const void *W, const void *scales, const void *X, void *Y, int64_t M,
                       int64_t N, int64_t K, const mbw_fusion *fusion, void *workspace, size_t ws_bytes,
                       mbw_stream_t stream);
+
+/*
+ * gemv_fused_awq_g128 -- gemv_int4_awq_g128 (codes canonical, or in the
+ * load-time repacked layout when `repacked` is 1) with the fusions of
+ * `fusion` (NULL: none; the same prologue and epilogues as gemv_fused): the
+ * RMSNorm prologue, the gated SiLU epilogue with an up matrix of the same
+ * AWQ format (up_weights, up_scales, up_zeros; all three required together),
+ * the residual add. Wq / scales / zeros / X / Y as in gemv_int4_awq_g128.
+ * Requires K % 256 == 0 for a fused call (no fusion: K % 128 == 0); runs on
+ * the streaming tensor-core kernel 4 batch rows per launch (larger batches in
+ * slices of 4, each streaming the weights), whose smallest instantiation
+ * needs K >= 1024 (MBW_ERR_UNSUPPORTED below it); plans keyed by
+ * MBW_OP_GEMV_INT4_AWQ_G128 | MBW_FUSE_* (| MBW_REPACKED). Alignment as in
+ * gemv_fused; up_zeros needs none.
+ */
+mbw_status gemv_fused_awq_g128(const uint8_t *Wq, const void *scales, const uint8_t *zeros, const void *X, void *Y,
+                               int64_t M, int64_t N, int64_t K, int repacked, const mbw_fusion *fusion,
+                               void *workspace, size_t ws_bytes, mbw_stream_t stream);
 
 /* Bytes of workspace the largest plan of `op` may use for this shape (0 if none). */
 size_t mbw_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);

@@ -8,7 +8,7 @@ accounting) import without loading the CUDA library.
 """
 _EXPORTS = (
     "gemv_bf16", "gemv_int4_g64", "gemv_int4_awq_g128", "gemm_skinny_bf16", "gemv_int8_pc", "quantize_int8_pc",
-    "gemv_fused", "MbwFusion", "FUSE_NORM", "FUSE_GLU", "FUSE_RESIDUAL", "repack_int4", "REPACKED",
+    "gemv_fused", "gemv_fused_awq_g128", "MbwFusion", "FUSE_NORM", "FUSE_GLU", "FUSE_RESIDUAL", "repack_int4", "REPACKED",
     "dequant_int4_g64", "dequant_int4_awq_g128", "autotune", "plan_describe", "plan_candidates", "plan_select", "plan_index", "workspace_bytes",
     "launch_count", "check_device_error", "selftest_wait_expiry", "inject_launch_failures", "output_fp32", "MbwError",
     "OP_GEMV_BF16", "OP_GEMV_INT4_G64", "OP_GEMV_INT4_AWQ_G128", "OP_GEMM_SKINNY_BF16",

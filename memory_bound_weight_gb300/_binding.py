@@ -37,7 +37,7 @@ _lib = None
 class MbwFusion(ctypes.Structure):
     """struct mbw_fusion of include/mbw.h."""
     _fields_ = [("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float), ("residual", ctypes.c_void_p),
-                ("up_weights", ctypes.c_void_p), ("up_scales", ctypes.c_void_p)]
+                ("up_weights", ctypes.c_void_p), ("up_scales", ctypes.c_void_p), ("up_zeros", ctypes.c_void_p)]
 
 # name -> (argtypes, restype)
 SIGNATURES = {
@@ -50,6 +50,8 @@ SIGNATURES = {
     "gemv_int8_pc": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], _ST),
     "mbw_quantize_int8_pc": ([_P, _P, _P, _I64, _I64, _P], _ST),
     "gemv_fused": ([ctypes.c_int, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.POINTER(MbwFusion), _P, _SZ, _P], _ST),
+    "gemv_fused_awq_g128": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(MbwFusion), _P, _SZ,
+                             _P], _ST),
     "mbw_workspace_bytes": ([ctypes.c_int, _I64, _I64, _I64], _SZ),
     "mbw_dequant_int4_g64": ([_P, _P, _P, _I64, _I64, _P], _ST),
     "mbw_dequant_int4_awq_g128": ([_P, _P, _P, _P, _I64, _I64, _P], _ST),
@@ -350,6 +352,57 @@ def gemv_fused(op, W, scales, X, out=None, norm_weight=None, norm_eps=1e-6, resi
     check("gemv_fused", lib().gemv_fused(op, W.data_ptr(), None if scales is None else scales.data_ptr(),
                                          X2.data_ptr(), Y.data_ptr(), M, N, K, ctypes.byref(f), wp, wn,
                                          _stream_ptr(X2.device)))
+    return Y[0] if vec else Y
+
+
+def gemv_fused_awq_g128(Wq, scales, zeros, X, out=None, norm_weight=None, norm_eps=1e-6, residual=None,
+                        up_weights=None, up_scales=None, up_zeros=None, repacked=False, workspace=None):
+    """gemv_int4_awq_g128 (Wq uint8 (N, K/2), scales fp16 (N, K/128), zeros uint8 (N, (K/128+1)/2); codes
+    canonical or, with repacked=True, from repack_int4) with optional fusions: RMSNorm prologue
+    (norm_weight bf16 (K,)), gated SiLU epilogue (up_weights / up_scales / up_zeros, same layouts),
+    residual add (bf16 shaped like the output; may be `out`). X bf16 (M, K) or (K,) -> Y (M, N) or (N,)."""
+    torch = _torch()
+    vec = X.dim() == 1
+    X2 = X.unsqueeze(0) if vec else X
+    _need(X2, "X", torch.bfloat16, 2)
+    M, K = X2.shape
+    _need(Wq, "Wq", torch.uint8, 2)
+    N = Wq.shape[0]
+    if Wq.shape[1] * 2 != K:
+        raise ValueError("Wq does not match K")
+    G = K // 128
+    _need(scales, "scales", torch.float16, 2)
+    _need_shape(scales, "scales", (N, G))
+    _need(zeros, "zeros", torch.uint8, 2)
+    _need_shape(zeros, "zeros", (N, (G + 1) // 2))
+    f = MbwFusion()
+    if norm_weight is not None:
+        _need(norm_weight, "norm_weight", torch.bfloat16, 1)
+        if norm_weight.shape[0] != K:
+            raise ValueError("norm_weight must have length K")
+        f.norm_weight = norm_weight.data_ptr()
+        f.norm_eps = float(norm_eps)
+    if up_weights is not None:
+        _need(up_weights, "up_weights", torch.uint8, 2)
+        if tuple(up_weights.shape) != tuple(Wq.shape):
+            raise ValueError("up_weights must have Wq's shape")
+        _need(up_scales, "up_scales", torch.float16, 2)
+        _need_shape(up_scales, "up_scales", (N, G))
+        _need(up_zeros, "up_zeros", torch.uint8, 2)
+        _need_shape(up_zeros, "up_zeros", (N, (G + 1) // 2))
+        f.up_weights, f.up_scales, f.up_zeros = up_weights.data_ptr(), up_scales.data_ptr(), up_zeros.data_ptr()
+    Y = _alloc_out((M, N), X2, None if out is None else (out.unsqueeze(0) if vec else out))
+    if residual is not None:
+        r2 = residual.unsqueeze(0) if residual.dim() == 1 else residual
+        _need(r2, "residual", torch.bfloat16, 2)
+        if tuple(r2.shape) != (M, N):
+            raise ValueError("residual must be shaped like the output")
+        f.residual = r2.data_ptr()
+    _on_current_device(Wq, scales, zeros, X2, Y, norm_weight, residual, up_weights, up_scales, up_zeros, workspace)
+    wp, wn = _ws(workspace)
+    check("gemv_fused_awq_g128", lib().gemv_fused_awq_g128(Wq.data_ptr(), scales.data_ptr(), zeros.data_ptr(),
+                                                           X2.data_ptr(), Y.data_ptr(), M, N, K, int(bool(repacked)),
+                                                           ctypes.byref(f), wp, wn, _stream_ptr(X2.device)))
     return Y[0] if vec else Y
 
 

@@ -93,6 +93,7 @@ static mbw_status run_simt(int fmt, int op, const uint8_t* W, const uint16_t* sc
             a.W2 = static_cast<const uint8_t*>(fz->up_weights);
             a.scales2 = static_cast<const uint16_t*>(fz->up_scales);
             a.rscale2 = static_cast<const float*>(fz->up_scales);
+            if (fmt == FMT_AWQ) a.zeros2 = static_cast<const uint8_t*>(fz->up_zeros);
         }
     }
     const size_t ybytes = g_out_f32 ? 4 : 2;
@@ -269,6 +270,51 @@ mbw_status gemv_fused(int op, const void* W, const void* scales, const void* X, 
     return run_simt(fmt, fop, (const uint8_t*)W, (const uint16_t*)scales, nullptr, (const uint16_t*)X, Y, M, N, K,
                     (cudaStream_t)stream, fmt == FMT_I8 ? (const float*)scales : nullptr,
                     (fop & MBW_FUSE_MASK) ? fusion : nullptr);
+}
+
+mbw_status gemv_fused_awq_g128(const uint8_t* Wq, const void* scales, const uint8_t* zeros, const void* X, void* Y,
+                               int64_t M, int64_t N, int64_t K, int repacked, const mbw_fusion* fusion,
+                               void* workspace, size_t ws_bytes, mbw_stream_t stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    if (repacked != 0 && repacked != 1) return fail(MBW_ERR_INVALID_ARG, "gemv_fused_awq_g128: repacked must be 0 or 1");
+    const int op = MBW_OP_GEMV_INT4_AWQ_G128 | (repacked ? MBW_REPACKED : 0);
+    int fop = op;
+    if (fusion) {
+        if (fusion->norm_weight) {
+            if (!aligned(fusion->norm_weight, 16))
+                return fail(MBW_ERR_MISALIGNED, "gemv_fused_awq_g128: norm_weight must be 16-byte aligned");
+            if (!(fusion->norm_eps >= 0.0f))
+                return fail(MBW_ERR_INVALID_ARG, "gemv_fused_awq_g128: norm_eps must be >= 0");
+            fop |= MBW_FUSE_NORM;
+        }
+        if (fusion->up_weights) {
+            if (!aligned(fusion->up_weights, 32))
+                return fail(MBW_ERR_MISALIGNED, "gemv_fused_awq_g128: up_weights must be 32-byte aligned");
+            if (!fusion->up_scales || !aligned(fusion->up_scales, 2) || !fusion->up_zeros)
+                return fail(MBW_ERR_INVALID_ARG, "gemv_fused_awq_g128: up_scales or up_zeros missing or misaligned");
+            fop |= MBW_FUSE_GLU;
+        }
+        if (fusion->residual) {
+            if (!aligned(fusion->residual, 2))
+                return fail(MBW_ERR_MISALIGNED, "gemv_fused_awq_g128: residual must be 2-byte aligned");
+            fop |= MBW_FUSE_RESIDUAL;
+        }
+    }
+    if (!(fop & MBW_FUSE_MASK))
+        return awq_call("gemv_fused_awq_g128", op, Wq, scales, zeros, X, Y, M, N, K, (cudaStream_t)stream);
+    mbw_status st = check_sizes("gemv_fused_awq_g128", M, N, K, 256);
+    if (st != MBW_OK) return st;
+    if (N == 0 || M == 0) return MBW_OK;
+    if (K == 0) return fail(MBW_ERR_BAD_SHAPE, "gemv_fused_awq_g128: K must be positive");
+    if (!Wq || !scales || !zeros || !X || !Y) return fail(MBW_ERR_INVALID_ARG, "gemv_fused_awq_g128: NULL pointer");
+    if (!aligned(Wq, 32) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(scales, 2))
+        return fail(MBW_ERR_MISALIGNED,
+                    "gemv_fused_awq_g128: Wq must be 32-byte aligned, X and Y 16-byte, scales 2-byte");
+    if (mbw_plan_candidates(fop, M, N, K) == 0)
+        return fail(MBW_ERR_UNSUPPORTED, "gemv_fused_awq_g128: no kernel for this shape and fusion");
+    return run_simt(FMT_AWQ, fop, Wq, (const uint16_t*)scales, zeros, (const uint16_t*)X, Y, M, N, K,
+                    (cudaStream_t)stream, nullptr, fusion);
 }
 
 mbw_status gemm_skinny_bf16(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K,

@@ -610,6 +610,9 @@ size_t lat_smem_bytes(int fmt, const LatConfig& c, int64_t N, int64_t K, int M, 
 }
 
 cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
+    // a gated launch reads the up matrix's codes, scales (not BF16) and zero points (AWQ)
+    if (a.glu && (!a.W2 || (fmt != FMT_BF16 && !a.scales2) || (fmt == FMT_AWQ && !a.zeros2)))
+        return cudaErrorInvalidValue;
     int n;
     const LatEntry* t = lat_table(fmt, &n);
     if (t == nullptr || p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > lat_max_batch(fmt)) return cudaErrorInvalidValue;

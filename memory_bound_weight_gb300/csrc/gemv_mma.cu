@@ -447,8 +447,9 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
         } else if (FMT == FMT_AWQ) {
             sp0 = St + (size_t)r0 * a.groups + (size_t)b0 * 2;
             sp1 = St + (size_t)r1 * a.groups + (size_t)b0 * 2;
-            zp0 = a.zeros + (size_t)r0 * a.zstride + b0;
-            zp1 = a.zeros + (size_t)r1 * a.zstride + b0;
+            const uint8_t* Zt = (gated<FZ>(a) && (tl & 1)) ? a.zeros2 : a.zeros;  // up or gate tile
+            zp0 = Zt + (size_t)r0 * a.zstride + b0;
+            zp1 = Zt + (size_t)r1 * a.zstride + b0;
         }
     };
     if (nt > 0) set_rows(0);
@@ -768,19 +769,16 @@ static const MmaEntry kMmaAwq[] = {
 
 #define MBW_M2(F, W, U, A) \
     { {W, U, A}, gemv_mma2_kernel<F, W, U, A, 0>, gemv_mma2_kernel<F, W, U, A, 1> }
-#define MBW_M2P(F, W, U, A) \
-    { {W, U, A}, gemv_mma2_kernel<F, W, U, A, 0>, nullptr }
 static const MmaEntry kMma2Bf16[] = {MBW_M2(FMT_BF16, 8, 2, 0), MBW_M2(FMT_BF16, 8, 4, 0), MBW_M2(FMT_BF16, 4, 4, 0),
                                      MBW_M2(FMT_BF16, 8, 4, 1), MBW_M2(FMT_BF16, 8, 6, 1)};
 static const MmaEntry kMma2G64[] = {MBW_M2(FMT_G64, 8, 2, 0), MBW_M2(FMT_G64, 8, 3, 0), MBW_M2(FMT_G64, 4, 2, 0),
                                     MBW_M2(FMT_G64, 4, 3, 0), MBW_M2(FMT_G64, 8, 4, 1), MBW_M2(FMT_G64, 8, 6, 1),
                                     MBW_M2(FMT_G64, 4, 6, 1)};
-static const MmaEntry kMma2Awq[] = {MBW_M2P(FMT_AWQ, 8, 2, 0), MBW_M2P(FMT_AWQ, 8, 3, 0), MBW_M2P(FMT_AWQ, 4, 2, 0),
-                                    MBW_M2P(FMT_AWQ, 8, 4, 1), MBW_M2P(FMT_AWQ, 8, 6, 1)};
+static const MmaEntry kMma2Awq[] = {MBW_M2(FMT_AWQ, 8, 2, 0), MBW_M2(FMT_AWQ, 8, 3, 0), MBW_M2(FMT_AWQ, 4, 2, 0),
+                                    MBW_M2(FMT_AWQ, 8, 4, 1), MBW_M2(FMT_AWQ, 8, 6, 1)};
 static const MmaEntry kMma2I8[] = {MBW_M2(FMT_I8, 8, 2, 0), MBW_M2(FMT_I8, 8, 3, 0), MBW_M2(FMT_I8, 4, 3, 0),
                                    MBW_M2(FMT_I8, 8, 4, 1), MBW_M2(FMT_I8, 8, 6, 1), MBW_M2(FMT_I8, 4, 8, 1)};
 #undef MBW_M2
-#undef MBW_M2P
 
 static const MmaEntry* mma2_table(int fmt, int* n) {
     switch (fmt) {
@@ -825,6 +823,9 @@ size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M,
 }
 
 cudaError_t launch_gemv_mma2(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
+    // a gated launch reads the up matrix's codes, scales (not BF16) and zero points (AWQ)
+    if (a.glu && (!a.W2 || (fmt != FMT_BF16 && !a.scales2) || (fmt == FMT_AWQ && !a.zeros2)))
+        return cudaErrorInvalidValue;
     int n;
     const MmaEntry* t = mma2_table(fmt, &n);
     if (t == nullptr || p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > mma2_max_batch(fmt)) return cudaErrorInvalidValue;

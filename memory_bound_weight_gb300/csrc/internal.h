@@ -38,6 +38,7 @@ struct GemvArgs {
     const uint8_t* W2;
     const uint16_t* scales2;
     const float* rscale2;
+    const uint8_t* zeros2;  // the up matrix's zero points (AWQ)
     // INT4 codes in the load-time repacked layout (mbw_repack_int4): the
     // unpack then yields the k pairs in natural order, and x is staged as is
     // instead of with the pair permutation.

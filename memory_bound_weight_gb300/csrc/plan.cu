@@ -407,8 +407,8 @@ static bool shape_ok(int op, int64_t M, int64_t N, int64_t K) {
     if (base < MBW_OP_GEMV_BF16 || base > MBW_OP_GEMV_INT8_PC) return false;
     if (flags & ~(MBW_FUSE_MASK | MBW_REPACKED)) return false;
     const int fuse = flags & MBW_FUSE_MASK;
-    if ((flags & MBW_REPACKED) && (base != MBW_OP_GEMV_INT4_AWQ_G128 || fuse)) return false;
-    if (fuse && base != MBW_OP_GEMV_BF16 && base != MBW_OP_GEMV_INT4_G64 && base != MBW_OP_GEMV_INT8_PC) return false;
+    if ((flags & MBW_REPACKED) && base != MBW_OP_GEMV_INT4_AWQ_G128) return false;
+    if (fuse && base == MBW_OP_GEMM_SKINNY_BF16) return false;
     if (M < 1 || N < 1 || K < 1 || N > MBW_MAX_DIM || K > MBW_MAX_DIM || M > MBW_MAX_DIM) return false;
     if (base == MBW_OP_GEMV_INT4_G64 && M != 1) return false;
     const int fmt = fmt_of_op(op);
@@ -551,6 +551,7 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
                 a.W2 = a.W + wstride1;
                 a.scales2 = (const uint16_t*)(a.W2 + codes);
                 a.rscale2 = (const float*)(a.W2 + codes);
+                a.zeros2 = (const uint8_t*)(a.W2 + codes + (size_t)N * a.groups * 2);
             }
             for (int sl = 0; sl < slices && le == cudaSuccess; ++sl) le = launch_plan(fmt, p, a, stream);
         }

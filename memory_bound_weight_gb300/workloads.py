@@ -122,6 +122,15 @@ QWEN25_7B_LAYER = (
 )
 QWEN25_7B_LAYERS = 28
 QWEN25_7B_HEAD = Mat("lm_head", 152064, 3584)
+# The same layer with the small ops folded into its GEMVs (NEXT-1, NEXT-4 on
+# the AWQ path): the attention RMSNorm into q/k/v, the residual adds into o and
+# down, the MLP RMSNorm and SwiGLU into one gate/up call (gate and up streamed
+# together, 18944 output rows); the head takes the final RMSNorm.
+QWEN25_7B_LAYER_FUSEDOPS = (
+    Mat("qkv", 4608, 3584, FUSE_NORM), Mat("o", 3584, 3584, FUSE_RESIDUAL),
+    Mat("gate_up", 18944, 3584, FUSE_NORM | FUSE_GLU), Mat("down", 3584, 18944, FUSE_RESIDUAL),
+)
+QWEN25_7B_HEAD_NORM = Mat("lm_head", 152064, 3584, FUSE_NORM)
 
 # Qwen3-4B: hidden 2560, MLP 9728, 36 layers, 32 query heads and 8 KV heads
 # of 128 dims, vocabulary 151936 (the model of TileInfer's INT8 measurements:
@@ -163,7 +172,9 @@ def tinyllama_step(fused: bool = False, fusedops: bool = False) -> list[Mat]:
     return decode_step(layer, TINYLLAMA_LAYERS, TINYLLAMA_HEAD)
 
 
-def qwen25_7b_step() -> list[Mat]:
+def qwen25_7b_step(fusedops: bool = False) -> list[Mat]:
+    if fusedops:
+        return decode_step(QWEN25_7B_LAYER_FUSEDOPS, QWEN25_7B_LAYERS, QWEN25_7B_HEAD_NORM)
     return decode_step(QWEN25_7B_LAYER, QWEN25_7B_LAYERS, QWEN25_7B_HEAD)
 
 

@@ -59,12 +59,15 @@ def near_tie_gap(orc, X, g, eps):
 
 
 def abs_weights(orc, fmt, w):
-    """|dequantized W| (N, K) in float64 for fmt in bf16 / g64 / i8."""
+    """|dequantized W| (N, K) in float64 for fmt in bf16 / g64 / i8 / awq (w = (codes, scales, zeros))."""
     if fmt == "bf16":
         return np.abs(np_bf16_to_f64(w[0]))
     if fmt == "g64":
         N, K = w[0].shape[0], w[0].shape[1] * 2
         return np.abs(orc.dequant_int4_g64(w[0], w[1], N, K))
+    if fmt == "awq":
+        N, K = w[0].shape[0], w[0].shape[1] * 2
+        return np.abs(orc.dequant_int4_awq_g128(w[0], w[1], w[2], N, K))
     return np.abs(w[0].astype(np.float64)) * np.abs(w[1].astype(np.float64))[:, None]
 
 
@@ -73,6 +76,8 @@ def ogemm(orc, fmt, w, X):
         return orc.gemm_bf16(w[0], X)
     if fmt == "g64":
         return orc.gemm_int4_g64(w[0], w[1], X)
+    if fmt == "awq":
+        return orc.gemm_int4_awq_g128(w[0], w[1], w[2], X)
     return orc.gemm_int8_pc(w[0], w[1], X)
 
 

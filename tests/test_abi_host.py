@@ -163,12 +163,21 @@ def test_planner_host_logic(L):
             assert L.mbw_plan_select(op, 1, 2048, 2048, i) == 0
             assert L.mbw_plan_describe(op, 1, 2048, 2048, buf, 256) == 0
             assert buf.value.split()[0] in (b"mma2", b"lat") and b"+" in buf.value
-    assert L.mbw_plan_candidates(3 | 0x100, 1, 2048, 2048) == 0  # no fused AWQ
+    # fused AWQ (canonical or repacked codes): the streaming tensor-core kernel, 4 batch rows per launch
+    for op in (3 | 0x100, 3 | 0x700, 3 | 0x800 | 0x300):
+        for M in (1, 9):
+            n = L.mbw_plan_candidates(op, M, 2048, 2048)
+            assert n >= 1
+            for i in range(n):
+                assert L.mbw_plan_select(op, M, 2048, 2048, i) == 0
+                assert L.mbw_plan_describe(op, M, 2048, 2048, buf, 256) == 0
+                assert buf.value.startswith(b"mma2") and b"+" in buf.value
+                assert buf.value.endswith(b" codes=repacked") == bool(op & 0x800)
+    assert L.mbw_plan_candidates(4 | 0x100, 8, 2048, 2048) == 0  # no fused skinny GEMM
     assert L.mbw_plan_candidates(5 | 0x1000, 1, 2048, 2048) == 0  # unknown flag bit
     # repacked INT4 codes (AWQ only): the tensor-core families, never the SIMT ones
     assert L.mbw_plan_candidates(5 | 0x800, 1, 2048, 2048) == 0
     assert L.mbw_plan_candidates(2 | 0x800, 1, 2048, 2048) == 0
-    assert L.mbw_plan_candidates(3 | 0x800 | 0x100, 1, 2048, 2048) == 0
     for M, N, K in ((1, 3584, 18944), (3, 4608, 3584), (16, 18944, 3584), (64, 3584, 3584)):
         n = L.mbw_plan_candidates(3 | 0x800, M, N, K)
         assert 1 <= n < L.mbw_plan_candidates(3, M, N, K)

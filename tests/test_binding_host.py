@@ -105,13 +105,17 @@ def test_every_call_marshals_valid_arguments(host_marshalling):
                           up_weights=W).shape == (N,)
     assert mbw.gemv_fused(mbw.OP_GEMV_INT4_G64, q4, s64, x, up_weights=q4, up_scales=s64).shape == (N,)
     assert mbw.gemv_fused(mbw.OP_GEMV_INT8_PC, q8, s8, X, residual=torch.zeros(M, N, dtype=bf)).shape == (M, N)
+    assert mbw.gemv_fused_awq_g128(q4, s128, z128, x, norm_weight=x, up_weights=q4, up_scales=s128,
+                                   up_zeros=z128, residual=torch.zeros(N, dtype=bf)).shape == (N,)
+    assert mbw.gemv_fused_awq_g128(q4, s128, z128, X, repacked=True).shape == (M, N)
     assert mbw.quantize_int8_pc(W)[0].shape == (N, K)
     assert mbw.dequant_int4_g64(q4, s64).shape == (N, K)
     assert mbw.dequant_int4_awq_g128(q4, s128, z128).shape == (N, K)
     names = [c[0] for c in host_marshalling.calls]
     assert names == ["gemv_bf16", "gemv_int4_g64", "gemv_int4_awq_g128", "gemv_int4_awq_g128_repacked",
                      "mbw_repack_int4", "gemm_skinny_bf16", "gemv_int8_pc", "gemv_fused", "gemv_fused",
-                     "gemv_fused", "mbw_quantize_int8_pc", "mbw_dequant_int4_g64", "mbw_dequant_int4_awq_g128"]
+                     "gemv_fused", "gemv_fused_awq_g128", "gemv_fused_awq_g128", "mbw_quantize_int8_pc",
+                     "mbw_dequant_int4_g64", "mbw_dequant_int4_awq_g128"]
     for name, nargs in host_marshalling.calls:
         assert nargs == len(B.SIGNATURES[name][0]), name
 
@@ -132,6 +136,12 @@ def test_bad_scale_and_zero_shapes_never_reach_the_library(host_marshalling):
         mbw.dequant_int4_g64(q4, torch.zeros(N, 1, dtype=torch.float16))
     with pytest.raises(ValueError, match="zeros"):
         mbw.dequant_int4_awq_g128(q4, torch.zeros(N, 2, dtype=torch.float16), torch.zeros(N, 2, dtype=torch.uint8))
+    s128 = torch.zeros(N, K // 128, dtype=torch.float16)
+    z128 = torch.zeros(N, 1, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="up_zeros"):
+        mbw.gemv_fused_awq_g128(q4, s128, z128, x, up_weights=q4, up_scales=s128, up_zeros=z128[:2].contiguous())
+    with pytest.raises(ValueError, match="zeros"):
+        mbw.gemv_fused_awq_g128(q4, s128, torch.zeros(N, 3, dtype=torch.uint8), x)
     with pytest.raises(ValueError, match="one device"):
         mbw.gemv_bf16(torch.zeros(N, K, dtype=torch.bfloat16), torch.zeros(K, dtype=torch.bfloat16, device="meta"))
     assert host_marshalling.calls == []

@@ -199,3 +199,109 @@ def positive_weights(fmt, seed, mi, N, K):
     q = np.abs(gen.int8_codes(seed, mi, N, K).astype(np.int16)).astype(np.int8)
     s = gen.f32_row_scales(seed, mi, N)
     return (q, s), (torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda())
+
+
+# ------------------------------------------------ AWQ-style INT4 (group 128) ----
+def awq_weights(seed, mi, N, K, repacked):
+    G = K // 128
+    c = gen.int4_codes(seed, mi, N, K)
+    s, z = gen.f16_group_scales(seed, mi, N, G), gen.u4_zero_points(seed, mi, N, G)
+    cd = mbw.repack_int4(dev_u8(c)) if repacked else dev_u8(c)
+    return (c, s, z), (cd, dev_f16(s), dev_u8(z))
+
+
+AWQ_SHAPES = [(45, 1024, 1), (300, 2048, 1), (130, 1280, 3), (77, 1024, 4), (40, 2048, 9)]
+
+
+def test_fused_awq_needs_a_super_block_per_warp():
+    """The fused AWQ calls run on the streaming tensor-core kernel, whose
+    smallest instantiation has 4 warps along K, each needing a 256-k
+    super-block: below K = 1024 a fused call is refused as unsupported (a
+    plain call still runs)."""
+    N, K = 40, 512
+    _, wd = awq_weights(1971, 0, N, K, False)
+    x = dev_bf16(gen.bf16_activations(1971, 2, 1, K)[0])
+    g = dev_bf16(gen.bf16_activations(1971, 3, 1, K)[0])
+    with pytest.raises(mbw.MbwError) as e:
+        mbw.gemv_fused_awq_g128(wd[0], wd[1], wd[2], x, norm_weight=g)
+    assert e.value.status == 5  # MBW_ERR_UNSUPPORTED
+    assert mbw.gemv_fused_awq_g128(wd[0], wd[1], wd[2], x).shape == (N,)
+
+
+@pytest.mark.parametrize("repacked", [False, True])
+@pytest.mark.parametrize("combo", sorted(COMBOS))
+@pytest.mark.parametrize("N,K,M", AWQ_SHAPES, ids=[f"{n}x{k}-M{m}" for n, k, m in AWQ_SHAPES])
+def test_fused_awq_every_plan(orc, N, K, M, combo, repacked):
+    """gemv_fused_awq_g128, every fusion combination, every plan (the streaming
+    tensor-core kernel; batches above 4 in slices of 4), canonical and repacked
+    codes, against the oracle under the fused tolerance."""
+    norm, glu, res = COMBOS[combo]
+    seed = 1900 + N + K
+    w, wd = awq_weights(seed, 0, N, K, repacked)
+    wu, wud = awq_weights(seed, 1, N, K, repacked) if glu else (None, (None, None, None))
+    X = gen.bf16_activations(seed, 2, M, K)
+    g = gen.bf16_activations(seed, 3, 1, K)[0] if norm else None
+    R = gen.bf16_activations(seed, 4, M, N) if res else None
+    v, tol, _ = fused_reference(orc, "awq", w, wu, X, g, R, EPS)
+    Xd = dev_bf16(X)
+    gd = dev_bf16(g) if norm else None
+    Rd = dev_bf16(R) if res else None
+    op = fused_op(mbw.OP_GEMV_INT4_AWQ_G128, norm, glu, res) | (mbw.REPACKED if repacked else 0)
+    n = mbw.plan_candidates(op, M, N, K)
+    assert n >= 1
+    for i in range(n):
+        mbw.plan_select(op, M, N, K, i)
+        desc = mbw.plan_describe(op, M, N, K)
+        y = mbw.gemv_fused_awq_g128(wd[0], wd[1], wd[2], Xd, norm_weight=gd, norm_eps=EPS, residual=Rd,
+                                    up_weights=wud[0], up_scales=wud[1], up_zeros=wud[2], repacked=repacked)
+        check(y, v, tol, f"awq {combo} rp={repacked} {M}x{N}x{K} plan {desc}")
+
+
+def test_fused_awq_same_sign_norm(orc):
+    """Same-sign AWQ data (codes >= 8 > zero points, so every dequantized
+    weight is > 0), fp32 output: the tolerance is below 0.25% of |y| and every
+    plan meets it, so a 0.3% norm-factor error would fail."""
+    N, K = 300, 2048
+    G = K // 128
+    c = gen.int4_codes(1951, 0, N, K) | np.uint8(0x88)  # codes 8 .. 15
+    s = gen.f16_group_scales(1951, 0, N, G)
+    z = gen.u4_zero_points(1951, 0, N, G) & np.uint8(0x77)  # zero points 0 .. 7
+    X = gen.bf16_activations(1951, 2, 1, K) & np.uint16(0x7FFF)
+    g = gen.bf16_activations(1951, 3, 1, K)[0] & np.uint16(0x7FFF)
+    v, tol, allow = fused_reference(orc, "awq", (c, s, z), None, X, g, None, EPS, out_fp32=True)
+    assert np.all(v > 0) and np.max((tol - 1e-5) / v) < 2.5e-3 and allow.max() < 5e-4
+    op = fused_op(mbw.OP_GEMV_INT4_AWQ_G128, 1, 0, 0)
+    for i in range(mbw.plan_candidates(op, 1, N, K)):
+        mbw.plan_select(op, 1, N, K, i)
+        with mbw.output_fp32():
+            y = mbw.gemv_fused_awq_g128(dev_u8(c), dev_f16(s), dev_u8(z), dev_bf16(X[0]), norm_weight=dev_bf16(g),
+                                        norm_eps=EPS)
+        check(y, v[0], tol[0], f"same-sign awq plan {mbw.plan_describe(op, 1, N, K)}")
+
+
+def test_fused_awq_qwen_shapes_sampled_rows(orc):
+    """The Qwen2.5-7B decode layer's fused AWQ calls at batch 1 on the
+    autotuned plans, codes repacked at load time: q/k/v with the RMSNorm,
+    gate/up (18944 + 18944 rows) with the RMSNorm and SwiGLU, o and down with
+    the residual add; sampled rows."""
+    K0 = 3584
+    X = gen.bf16_activations(1961, 0, 1, K0)
+    g = gen.bf16_activations(1961, 1, 1, K0)[0]
+    cases = [("qkv", 4608, K0, (1, 0, 0)), ("gate_up", 18944, K0, (1, 1, 0)), ("o", 3584, K0, (0, 0, 1)),
+             ("down", 3584, 18944, (0, 0, 1))]
+    for name, N, K, (norm, glu, res) in cases:
+        Xc = X if K == K0 else gen.bf16_activations(1961, 5, 1, K)
+        rows = np.unique(np.concatenate([np.arange(0, 16), np.arange(N - 16, N),
+                                         np.random.default_rng(N + K).integers(0, N, 48)]))
+        w, wd = awq_weights(1961, 10, N, K, True)
+        wu, wud = awq_weights(1961, 11, N, K, True) if glu else (None, (None, None, None))
+        R = gen.bf16_activations(1961, 6, 1, N) if res else None
+        wr = tuple(a[rows] for a in w)
+        wur = tuple(a[rows] for a in wu) if glu else None
+        v, tol, _ = fused_reference(orc, "awq", wr, wur, Xc, g if norm else None, R[:, rows] if res else None, EPS)
+        op = fused_op(mbw.OP_GEMV_INT4_AWQ_G128, norm, glu, res) | mbw.REPACKED
+        mbw.autotune(op, 1, N, K)
+        y = mbw.gemv_fused_awq_g128(wd[0], wd[1], wd[2], dev_bf16(Xc[0]), norm_weight=dev_bf16(g) if norm else None,
+                                    norm_eps=EPS, residual=dev_bf16(R[0]) if res else None, up_weights=wud[0],
+                                    up_scales=wud[1], up_zeros=wud[2], repacked=True)
+        check(y[torch.from_numpy(rows).cuda()], v[0], tol[0], f"qwen awq {name} ({mbw.plan_describe(op, 1, N, K)})")

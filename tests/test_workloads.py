@@ -87,3 +87,17 @@ def test_qwen3_4b_int8_step_is_about_4_gb():
     # the per-channel scales add 4 bytes per output row
     assert b8 - sum(m.N * m.K for m in mats) == 4 * sum(m.N for m in mats)
     assert abs(b8 / b16 - 0.5) < 1e-3
+
+
+def test_fused_qwen_awq_step_streams_the_same_weights():
+    """The AWQ step with the small ops fused streams the same weight bytes in 113 calls instead of 141 (gate and up
+    in one gated call per layer); the fusions add only the norm weights and the residuals read."""
+    plain, fused = wl.qwen25_7b_step(), wl.qwen25_7b_step(fusedops=True)
+    fmt = wl.FMT_INT4_AWQ_G128
+    assert len(plain) == 141 and len(fused) == 113
+    assert wl.step_weight_bytes(plain, fmt) == wl.step_weight_bytes(fused, fmt)
+    extra = wl.step_bytes_alg(fused, fmt) - wl.step_bytes_alg(plain, fmt)
+    norms = 28 * 2 * 3584 * 2 + 3584 * 2          # q/k/v and gate/up norm weights per layer, the head's
+    residuals = 28 * 2 * 3584 * 2                   # o and down
+    x_saved = 28 * 3584 * 2                         # up no longer reads its own x
+    assert extra == norms + residuals - x_saved
