@@ -210,7 +210,7 @@ class ClockSampler:
 KERNEL_SOURCES = {"lat": ("gemv_lat.cu", "device.cuh"), "mma2": ("gemv_mma.cu", "device.cuh"),
                   "mma": ("gemv_mma.cu", "device.cuh"), "simt": ("gemv_simt.cu", "device.cuh"),
                   "tma": ("gemv_tma.cu", "device.cuh"), "tcgen05": ("gemm_tc.cu", "device.cuh"),
-                  "awq_mma": ("gemv_awq_batch.cu", "device.cuh")}
+                  "awq_mma": ("gemv_awq_batch.cu", "device.cuh"), "rows": ("gemv_tma.cu", "device.cuh")}
 
 
 def kernel_source_sha(family):
@@ -642,8 +642,9 @@ def step_figure(workload, M, device, tune="shape", steps=20):
 
 def skinny_figures(device, Ms=wl.SKINNY_M, reps=7):
     """gemm_skinny_bf16 over the Qwen2.5-7B MLP shapes at each batch M, on the
-    autotuned plan: a CUDA graph of calls over distinct copies of W >= 4x L2,
-    median of `reps` replays; HBM and tensor rooflines, the longer the bound."""
+    autotuned plan: a CUDA graph of at least 40 calls over distinct copies of
+    W >= 4x L2 taken in turn, median of `reps` replays; HBM and tensor
+    rooflines, the longer the bound."""
     import torch
 
     import memory_bound_weight_gb300 as mbw
@@ -669,9 +670,10 @@ def skinny_figures(device, Ms=wl.SKINNY_M, reps=7):
                 mbw.gemm_skinny_bf16(X, Ws[i], out=Ys[i])
             torch.cuda.synchronize()
             g = torch.cuda.CUDAGraph()
+            launches = max(copies, 40)  # the copies in turn
             with torch.cuda.graph(g, stream=torch.cuda.Stream(device)):
-                for i in range(copies):
-                    mbw.gemm_skinny_bf16(X, Ws[i], out=Ys[i])
+                for i in range(launches):
+                    mbw.gemm_skinny_bf16(X, Ws[i % copies], out=Ys[i % copies])
             for _ in range(3):
                 g.replay()
             torch.cuda.synchronize()
@@ -683,7 +685,7 @@ def skinny_figures(device, Ms=wl.SKINNY_M, reps=7):
                 g.replay()
                 e1.record()
                 torch.cuda.synchronize()
-                ts.append(e0.elapsed_time(e1) / copies)
+                ts.append(e0.elapsed_time(e1) / launches)
             us = statistics.median(ts) * 1e3
             r = hbm_roofline(b, us, peak)
             tflops = fl / (us * 1e-6) / 1e12
@@ -928,10 +930,11 @@ def roofline_fields(step, ms_step, gbs, peak, peak_src, traffic, plans, launches
          "frac_of_nominal_hbm": achieved / NOMINAL_HBM_GBS, "nominal_hbm_gbs": NOMINAL_HBM_GBS,
          "bytes_alg_per_launch": kb, "us_per_launch": st["us"],
          "share_of_step": counts[dominant] * st["us"] / tot,
-         "note": "per-launch time of the dominant kernel in a PDL-chained graph of its own launches over distinct "
-                 "weight copies >= 4x L2 (same plan as in the step); the step-level figure is value / "
+         "note": "per-launch time of the dominant kernel in a PDL-chained graph of %d of its own launches over "
+                 "%d distinct weight copies >= 4x L2 taken in turn (same plan as in the step); the step-level "
+                 "figure is value / "
                  "frac_of_peak (every launch of the step is one of this library's kernels, %d per step)"
-                 % launches_per_step}
+                 % (st["launches"], st["copies"], launches_per_step)}
     if M > 1:
         tc, tc_src = tensor_peak()
         tflops = kfl / (st["us"] * 1e-6) / 1e12
@@ -960,8 +963,9 @@ def named_shapes(fmt):
 def time_per_shape(step, device, reps=5, shapes=None, plans=None, cold_iters=0):
     """Steady-state time per matrix of each shape: a CUDA graph of back-to-back
     launches (programmatic dependent launch, as in the step) over distinct
-    copies of the matrix totalling at least 4x the L2, so every launch reads
-    its weights from HBM; per-matrix time = graph time / launches.
+    copies of the matrix totalling at least 4x the L2, taken in turn for at
+    least 40 launches, so every launch reads its weights from HBM and the
+    graph's own start weighs little; per-matrix time = graph time / launches.
 
     With cold_iters > 0, also the cold figure: that many single calls, each
     after a write of twice the L2 that evicts the matrix, each timed with CUDA
@@ -996,8 +1000,10 @@ def time_per_shape(step, device, reps=5, shapes=None, plans=None, cold_iters=0):
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream(device)
+        launches = max(copies, 40)
         with torch.cuda.graph(g, stream=s):
-            for fn, a, o in calls:
+            for i in range(launches):
+                fn, a, o = calls[i % copies]
                 fn(*a, out=o)
         for _ in range(3):
             g.replay()
@@ -1010,11 +1016,12 @@ def time_per_shape(step, device, reps=5, shapes=None, plans=None, cold_iters=0):
             g.replay()
             e1.record()
             torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1) / copies)
+            ts.append(e0.elapsed_time(e1) / launches)
         us = statistics.median(ts) * 1e3
         out[skey((fz, N, K))] = {"us": us, "GB/s": b / (us * 1e-6) / 1e9, "frac": b / (us * 1e-6) / 1e9 / peak,
                                  "TFLOP/s": wl.call_flops(M, wl.Mat("", N, K, fz)) / (us * 1e-6) / 1e12,
-                                 "copies": copies, "plan": mbw.plan_describe(step.op | fz, M, N, K)}
+                                 "copies": copies, "launches": launches,
+                                 "plan": mbw.plan_describe(step.op | fz, M, N, K)}
         if cold_iters > 0:
             out[skey((fz, N, K))].update(time_cold(calls[0], b, peak, l2, device, cold_iters))
         del calls, g

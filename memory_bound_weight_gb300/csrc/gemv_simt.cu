@@ -256,6 +256,240 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     cluster.sync();
 }
 
+// BF16 at batch 1 with 32-byte lane loads: a lane reads 16 weights of a row per
+// load (ld.global v8), so one warp instruction covers 1 KB of the row, twice
+// the run of the 16-byte kernel above; the matrix is then read as long
+// contiguous runs, which the DRAM serves at nearly the rate of a linear sweep
+// (measured on 18944 x 3584 BF16: 512-byte runs per row cost ~2.5 us more per
+// launch than a grid-stride read, 1 KB runs ~0.5 us). Same row ownership, x
+// staging (fp32, plane-major, 4 planes per chunk), double buffer, reduction and
+// split-K cluster sum as above; chunk = 32 bytes, K % 16 == 0.
+template <int WARPS, int R, int U>
+__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) gemv_simt_bf16w_kernel(const GemvArgs a, const int S) {
+    constexpr int PL = 4;  // float4 planes per 32-byte chunk (16 weights)
+    extern __shared__ float4 smem[];
+
+    pdl_launch_dependents();
+
+    const int rank = (S > 1) ? (int)cg::this_cluster().block_rank() : 0;
+    const int rowblock = blockIdx.x / S;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int chunks = a.chunks / 2;  // 32-byte chunks per row (a.chunks counts 16-byte ones)
+    const int split = (chunks + S - 1) / S;
+    const int c0 = rank * split;
+    const int c1 = min(chunks, c0 + split);
+    const int nc = max(c1 - c0, 0);
+    const int iters = (nc + 32 * U - 1) / (32 * U);
+
+    const int row_base = rowblock * (WARPS * R) + warp * R;
+    const uint8_t* wrow[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) wrow[r] = a.W + (size_t)min(row_base + r, a.N - 1) * (size_t)chunks * 32;
+
+    u32x8 cur[R][U];
+    auto load = [&](u32x8 (&buf)[R][U], int it) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + it * 32 * U + u * 32 + lane;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                if (c < c1) {
+                    buf[r][u] = ld_stream32(wrow[r] + (size_t)c * 32);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) buf[r][u].v[e] = 0;
+                }
+            }
+        }
+    };
+    if (iters > 0) load(cur, 0);
+
+    prefetch_l2_grid_share(a.x, (size_t)a.K * 2);
+    pdl_wait();
+
+    // x of this CTA's k-slice as fp32: smem[p * nc + lc] = x[(c0 + lc) * 16 + 4p .. +4]
+    for (int i = threadIdx.x; i < nc * 2; i += WARPS * 32) {
+        const int lc = i >> 1, p0 = (i & 1) * 2;
+        const uint4 v = ld_ro16(a.x + (size_t)(c0 + lc) * 16 + (size_t)p0 * 4);
+        smem[p0 * nc + lc] = make_float4(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x), bf16lo_to_f32(v.y), bf16hi_to_f32(v.y));
+        smem[(p0 + 1) * nc + lc] =
+            make_float4(bf16lo_to_f32(v.z), bf16hi_to_f32(v.z), bf16lo_to_f32(v.w), bf16hi_to_f32(v.w));
+    }
+    __syncthreads();
+
+    float acc[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = 0.f;
+
+    for (int it = 0; it < iters; ++it) {
+        u32x8 nxt[R][U];
+        if (it + 1 < iters) load(nxt, it + 1);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + it * 32 * U + u * 32 + lane;
+            if (c < c1) {
+                const int lc = c - c0;
+#pragma unroll
+                for (int p = 0; p < PL; ++p) {
+                    const float4 xv = smem[p * nc + lc];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint32_t w0 = cur[r][u].v[2 * p], w1 = cur[r][u].v[2 * p + 1];
+                        float t = acc[r];
+                        t = fmaf(bf16lo_to_f32(w0), xv.x, t);
+                        t = fmaf(bf16hi_to_f32(w0), xv.y, t);
+                        t = fmaf(bf16lo_to_f32(w1), xv.z, t);
+                        t = fmaf(bf16hi_to_f32(w1), xv.w, t);
+                        acc[r] = t;
+                    }
+                }
+            }
+        }
+        if (it + 1 < iters) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int u = 0; u < U; ++u) cur[r][u] = nxt[r][u];
+        }
+    }
+
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = warp_sum(acc[r]);
+
+    if (S == 1) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if (lane == (r & 31) && row_base + r < a.N) store_out(a.y, row_base + r, acc[r], a.out_f32);
+        return;
+    }
+
+    // split K: partials of this CTA's rows -> shared memory, then rank 0 sums the
+    // S partials in rank order through distributed shared memory
+    float* red = reinterpret_cast<float*>(smem) + (size_t)PL * split * 4;
+    if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) red[warp * R + r] = acc[r];
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (rank == 0) {
+        for (int t = threadIdx.x; t < WARPS * R; t += WARPS * 32) {
+            float v = 0.f;
+            for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(red + t, s);
+            const int row = rowblock * (WARPS * R) + t;
+            if (row < a.N) store_out(a.y, row, v, a.out_f32);
+        }
+    }
+    cluster.sync();
+}
+
+// Persistent form of the 32-byte kernel (batch 1, no split): a grid of
+// `occ` CTAs per SM, each staging the whole of x once; warp w of the grid takes
+// the R-row groups w, w + TW, w + 2 TW, ... (TW = warps in the grid), and its
+// register double buffer runs across group boundaries, so a warp's next rows
+// are in flight while it finishes the current ones. A non-persistent grid
+// instead restarts cold in every CTA of its second wave (x staged again, one
+// chunk per row in flight until the staging ends).
+template <int WARPS, int R, int U>
+__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) gemv_simt_bf16p_kernel(const GemvArgs a, const int) {
+    constexpr int PL = 4;
+    extern __shared__ float4 smem[];
+
+    pdl_launch_dependents();
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int chunks = a.chunks / 2;
+    const int iters = (chunks + 32 * U - 1) / (32 * U);
+    const int ngroups = (a.N + R - 1) / R;
+    const int TW = gridDim.x * WARPS;
+    int g = blockIdx.x * WARPS + warp;
+    int it = 0;
+
+    auto load = [&](u32x8 (&buf)[R][U], int grp, int itn) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint8_t* wr = a.W + (size_t)min(grp * R + r, a.N - 1) * (size_t)chunks * 32;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = itn * 32 * U + u * 32 + lane;
+                if (c < chunks) {
+                    buf[r][u] = ld_stream32(wr + (size_t)c * 32);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) buf[r][u].v[e] = 0;
+                }
+            }
+        }
+    };
+    u32x8 cur[R][U];
+    if (g < ngroups) load(cur, g, 0);
+
+    prefetch_l2_grid_share(a.x, (size_t)a.K * 2);
+    pdl_wait();
+
+    // the whole of x as fp32: smem[p * chunks + c] = x[c * 16 + 4p .. +4]
+    for (int i = threadIdx.x; i < chunks * 2; i += WARPS * 32) {
+        const int c = i >> 1, p0 = (i & 1) * 2;
+        const uint4 v = ld_ro16(a.x + (size_t)c * 16 + (size_t)p0 * 4);
+        smem[p0 * chunks + c] = make_float4(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x), bf16lo_to_f32(v.y), bf16hi_to_f32(v.y));
+        smem[(p0 + 1) * chunks + c] =
+            make_float4(bf16lo_to_f32(v.z), bf16hi_to_f32(v.z), bf16lo_to_f32(v.w), bf16hi_to_f32(v.w));
+    }
+    __syncthreads();
+
+    float acc[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = 0.f;
+
+    while (g < ngroups) {
+        int ng = g, nit = it + 1;
+        if (nit == iters) {
+            nit = 0;
+            ng = g + TW;
+        }
+        u32x8 nxt[R][U];
+        if (ng < ngroups) load(nxt, ng, nit);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = it * 32 * U + u * 32 + lane;
+            if (c < chunks) {
+#pragma unroll
+                for (int p = 0; p < PL; ++p) {
+                    const float4 xv = smem[p * chunks + c];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint32_t w0 = cur[r][u].v[2 * p], w1 = cur[r][u].v[2 * p + 1];
+                        float t = acc[r];
+                        t = fmaf(bf16lo_to_f32(w0), xv.x, t);
+                        t = fmaf(bf16hi_to_f32(w0), xv.y, t);
+                        t = fmaf(bf16lo_to_f32(w1), xv.z, t);
+                        t = fmaf(bf16hi_to_f32(w1), xv.w, t);
+                        acc[r] = t;
+                    }
+                }
+            }
+        }
+        if (nit == 0) {  // the group's last chunks: reduce over the warp and store its rows
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float v = warp_sum(acc[r]);
+                if (lane == (r & 31) && g * R + r < a.N) store_out(a.y, g * R + r, v, a.out_f32);
+                acc[r] = 0.f;
+            }
+        }
+        if (ng < ngroups) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int u = 0; u < U; ++u) cur[r][u] = nxt[r][u];
+        }
+        g = ng;
+        it = nit;
+    }
+}
+
 // ------------------------------------------------------------- tables ----
 using KernFn = void (*)(const GemvArgs, const int);
 struct Entry {
@@ -263,12 +497,19 @@ struct Entry {
     KernFn fn;
 };
 #define MBW_E(F, W, R, U, MB) \
-    { {W, R, U, MB}, gemv_simt_kernel<F, W, R, U, MB> }
+    { {W, R, U, MB, 16}, gemv_simt_kernel<F, W, R, U, MB> }
+#define MBW_EW(W, R, U) \
+    { {W, R, U, 1, 32}, gemv_simt_bf16w_kernel<W, R, U> }
+#define MBW_EP(W, R, U) \
+    { {W, R, U, 1, 32, 1}, gemv_simt_bf16p_kernel<W, R, U> }
 
 static const Entry kBf16[] = {
     MBW_E(FMT_BF16, 4, 1, 4, 1), MBW_E(FMT_BF16, 4, 2, 4, 1), MBW_E(FMT_BF16, 8, 1, 8, 1),
     MBW_E(FMT_BF16, 4, 4, 2, 1), MBW_E(FMT_BF16, 8, 2, 2, 1), MBW_E(FMT_BF16, 8, 1, 4, 1),
     MBW_E(FMT_BF16, 4, 2, 2, 2), MBW_E(FMT_BF16, 4, 2, 2, 4), MBW_E(FMT_BF16, 4, 1, 2, 8),
+    MBW_EW(4, 2, 2), MBW_EW(4, 4, 1), MBW_EW(4, 1, 4), MBW_EW(8, 2, 2), MBW_EW(8, 1, 4),
+    MBW_EW(8, 1, 2),  MBW_EP(4, 4, 1), MBW_EP(4, 2, 2), MBW_EP(4, 2, 1), MBW_EP(8, 2, 1), MBW_EP(8, 1, 2),
+    MBW_EP(4, 1, 2),
 };
 static const Entry kG64[] = {
     MBW_E(FMT_G64, 4, 1, 2, 1), MBW_E(FMT_G64, 4, 2, 2, 1), MBW_E(FMT_G64, 4, 4, 1, 1),
@@ -280,6 +521,8 @@ static const Entry kAwq[] = {
     MBW_E(FMT_AWQ, 4, 2, 1, 4), MBW_E(FMT_AWQ, 4, 1, 1, 8),
 };
 #undef MBW_E
+#undef MBW_EW
+#undef MBW_EP
 
 static const Entry* table(int fmt, int* n) {
     switch (fmt) {
@@ -311,6 +554,11 @@ SimtConfig simt_config(int fmt, int idx) {
 }
 
 size_t simt_smem_bytes(int fmt, const SimtConfig& c, const GemvArgs& a, int split) {
+    if (c.persist) return (size_t)(a.chunks / 2) * 16 * sizeof(float);  // the whole of x, fp32
+    if (c.cb == 32) {  // BF16, 32-byte chunks of 16 weights: the x slice of the widest rank, then the partials
+        const size_t split32 = (size_t)(a.chunks / 2 + split - 1) / split;
+        return split32 * 16 * sizeof(float) + ((split > 1) ? (size_t)c.warps * c.r * sizeof(float) : 0);
+    }
     const int cw = (fmt == FMT_BF16) ? 8 : 32;
     const size_t xs = (size_t)c.mb * a.split_chunks * cw * sizeof(float);
     const size_t red = (split > 1) ? (size_t)c.warps * c.r * c.mb * sizeof(float) : 0;
@@ -323,7 +571,11 @@ cudaError_t launch_gemv_simt(int fmt, const Plan& p, const GemvArgs& a, cudaStre
     if (p.cfg < 0 || p.cfg >= n) return cudaErrorInvalidValue;
     const Entry& e = t[p.cfg];
     const int rows_per_cta = e.cfg.warps * e.cfg.r;
-    const int rowblocks = (a.N + rows_per_cta - 1) / rows_per_cta;
+    int rowblocks = (a.N + rows_per_cta - 1) / rows_per_cta;
+    if (e.cfg.persist) {
+        if (p.split != 1 || p.occ < 1) return cudaErrorInvalidValue;
+        rowblocks = std::min(rowblocks, device_sm_count() * p.occ);
+    }
     const size_t smem = simt_smem_bytes(fmt, e.cfg, a, p.split);
 
     if (smem > 48 * 1024) {

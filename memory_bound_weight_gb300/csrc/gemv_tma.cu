@@ -32,6 +32,8 @@
 // order: deterministic, no global scratch.
 #include <cooperative_groups.h>
 
+#include <algorithm>
+
 #include "device.cuh"
 #include "internal.h"
 
@@ -496,6 +498,194 @@ cudaError_t launch_gemv_tma(int fmt, const Plan& p, const GemvArgs& a, cudaStrea
     cfg.numAttrs = na;
     count_launch();
     return cudaLaunchKernelEx(&cfg, e.fn, a, p.split);
+}
+
+// ---------------------------------------------------------- row stream ----
+// BF16 weights at batch 1, fed by per-warp bulk-copy rings over whole rows.
+//
+// CTA c of G owns the rows [N c / G, N (c + 1) / G); with row-major weights
+// those rows are one contiguous byte range, cut into stages of SEG bytes (the
+// last one shorter). Stage s belongs to warp s % W, whose lane 0 copies it with
+// one cp.async.bulk into one of the warp's D ring slots and refills the slot as
+// soon as the warp has read it. Each SM thus keeps about W * D * SEG bytes in
+// flight with a few large copies, the ring rather than the register file
+// setting the depth, and the weights stream as long contiguous runs (the
+// pattern a plain linear read sweeps at full HBM rate).
+//
+// Rows are 16-byte multiples, so a stage holds whole 16-byte chunks of one or
+// more rows: the warp sums each row piece over its lanes (fp32) and stores the
+// piece's partial in shared memory; after the stream, row i's pieces (stages
+// floor(2K i / SEG) .. floor((2K (i + 1) - 1) / SEG), at most ceil(2K / SEG) + 1
+// of them) are summed in stage order: deterministic, no global scratch.
+//
+// x is staged once per CTA as bf16 and widened at use (each 16-byte chunk of a
+// row meets the matching 16 bytes of x). PDL: every warp issues its first D
+// copies before waiting for the previous grid. Every wait is bounded; on
+// expiry the warp stops consuming, raises the fault flag, and lane 0 waits
+// (bounded) for the copies it still has in flight before the CTA exits.
+struct RowsSmem {
+    int P;        // partial slots per row
+    int rows_max; // rows of the largest CTA share
+    size_t ring_off, bar_off, x_off, part_off, total;
+};
+
+__host__ __device__ inline RowsSmem rows_smem_layout(int64_t K, int64_t N, int G, int W, int D, int SEG) {
+    RowsSmem L;
+    const int64_t rb = 2 * K;
+    L.P = (int)((rb + SEG - 1) / SEG) + 1;
+    L.rows_max = (int)((N + G - 1) / G);
+    L.ring_off = 0;
+    L.bar_off = (size_t)W * D * SEG;
+    L.x_off = (L.bar_off + (size_t)W * D * 8 + 127) / 128 * 128;
+    L.part_off = (L.x_off + (size_t)rb + 15) / 16 * 16;
+    L.total = L.part_off + (size_t)L.rows_max * L.P * sizeof(float);
+    return L;
+}
+
+template <int W, int D, int SEG>
+__global__ void __launch_bounds__(W * 32, 2) gemv_rows_bf16_kernel(const GemvArgs a, const int G) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const RowsSmem L = rows_smem_layout(a.K, a.N, G, W, D, SEG);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+    const uint8_t* xs = smem + L.x_off;
+    float* part = reinterpret_cast<float*>(smem + L.part_off);
+
+    pdl_launch_dependents();
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rb = 2 * (int)a.K;  // bytes per row
+    const int r0 = (int)((int64_t)a.N * blockIdx.x / G);
+    const int r1 = (int)((int64_t)a.N * (blockIdx.x + 1) / G);
+    const int64_t nbytes = (int64_t)(r1 - r0) * rb;
+    const int nst = (int)((nbytes + SEG - 1) / SEG);
+    const uint8_t* src = a.W + (size_t)r0 * (size_t)rb;
+    uint64_t* wfull = full + warp * D;
+    uint8_t* wring = smem + L.ring_off + (size_t)warp * D * SEG;
+
+    uint64_t policy = 0;
+    if (lane == 0) {
+        for (int j = 0; j < D; ++j) mbar_init(&wfull[j], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    }
+    // lane 0: the warp's j-th stage (stage warp + j W) into slot j % D
+    auto issue = [&](int j) {
+        const int st = warp + j * W;
+        if (st >= nst) return;
+        const int64_t off = (int64_t)st * SEG;
+        const uint32_t len = (uint32_t)min((int64_t)SEG, nbytes - off);
+        uint64_t* bar = &wfull[j % D];
+        mbar_expect_tx(bar, len);
+        bulk_g2s(wring + (size_t)(j % D) * SEG, src + off, len, bar, policy);
+    };
+    if (lane == 0)
+        for (int j = 0; j < D; ++j) issue(j);
+    __syncwarp();
+
+    prefetch_l2_grid_share(a.x, (size_t)rb);
+    pdl_wait();
+    for (int i = threadIdx.x; i < rb / 16; i += W * 32)
+        reinterpret_cast<uint4*>(smem + L.x_off)[i] = ld_ro16(a.x + (size_t)i * 8);
+    __syncthreads();
+
+    bool ok = true;
+    int j = 0;
+    for (; warp + j * W < nst; ++j) {
+        const int st = warp + j * W;
+        ok = __all_sync(0xffffffffu, mbar_wait(&wfull[j % D], (j / D) & 1));
+        if (!ok) break;
+        const int64_t b0 = (int64_t)st * SEG;
+        const int64_t b1 = min(b0 + SEG, nbytes);
+        const uint8_t* stage = wring + (size_t)(j % D) * SEG;
+        int i = (int)(b0 / rb);  // CTA-local row of the stage's first byte
+        int64_t rs = (int64_t)i * rb;
+        while (rs < b1) {
+            const int p0 = (int)(max(b0, rs) - b0);  // piece in stage bytes
+            const int p1 = (int)(min(b1, rs + rb) - b0);
+            const uint8_t* xp = xs + (b0 - rs);      // x byte for stage byte o: xp + o
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 4
+            for (int o = p0 + lane * 16; o < p1; o += 512) {
+                const uint4 w = *reinterpret_cast<const uint4*>(stage + o);
+                const uint4 xv = *reinterpret_cast<const uint4*>(xp + o);
+                acc0 = fmaf(bf16lo_to_f32(w.x), bf16lo_to_f32(xv.x), acc0);
+                acc1 = fmaf(bf16hi_to_f32(w.x), bf16hi_to_f32(xv.x), acc1);
+                acc0 = fmaf(bf16lo_to_f32(w.y), bf16lo_to_f32(xv.y), acc0);
+                acc1 = fmaf(bf16hi_to_f32(w.y), bf16hi_to_f32(xv.y), acc1);
+                acc0 = fmaf(bf16lo_to_f32(w.z), bf16lo_to_f32(xv.z), acc0);
+                acc1 = fmaf(bf16hi_to_f32(w.z), bf16hi_to_f32(xv.z), acc1);
+                acc0 = fmaf(bf16lo_to_f32(w.w), bf16lo_to_f32(xv.w), acc0);
+                acc1 = fmaf(bf16hi_to_f32(w.w), bf16hi_to_f32(xv.w), acc1);
+            }
+            const float v = warp_sum(acc0 + acc1);
+            if (lane == 0) part[i * L.P + (st - (int)(rs / SEG))] = v;
+            ++i;
+            rs += rb;
+        }
+        __syncwarp();  // every lane has read the slot
+        if (lane == 0) issue(j + D);
+    }
+    if (!ok && lane == 0) {
+        // drain: the copies issued and not yet waited for, stages j .. j + D - 1
+        for (int jj = j; jj < j + D && warp + jj * W < nst; ++jj) mbar_wait(&wfull[jj % D], (jj / D) & 1);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < r1 - r0; i += W * 32) {
+        const int64_t rs = (int64_t)i * rb;
+        const int f = (int)(rs / SEG), l = (int)((rs + rb - 1) / SEG);
+        float v = 0.f;
+        for (int st = f; st <= l; ++st) v += part[i * L.P + (st - f)];
+        store_out(a.y, r0 + i, v, a.out_f32);
+    }
+}
+
+struct RowsEntry {
+    RowsConfig cfg;
+    TmaFn fn;
+};
+#define MBW_R(W, D, SEG) \
+    { {W, D, SEG}, gemv_rows_bf16_kernel<W, D, SEG> }
+static const RowsEntry kRows[] = {
+    MBW_R(8, 3, 8192), MBW_R(8, 2, 8192), MBW_R(4, 6, 8192), MBW_R(4, 4, 8192), MBW_R(4, 3, 16384),
+    MBW_R(16, 2, 4096), MBW_R(8, 4, 4096), MBW_R(8, 2, 4096), MBW_R(4, 4, 4096), MBW_R(12, 2, 8192),
+    MBW_R(8, 3, 4096), MBW_R(4, 3, 8192), MBW_R(12, 2, 4096), MBW_R(8, 2, 6144), MBW_R(16, 2, 3072),
+    MBW_R(4, 2, 8192), MBW_R(8, 1, 8192),
+};
+#undef MBW_R
+
+int rows_num_configs() { return (int)(sizeof(kRows) / sizeof(kRows[0])); }
+
+RowsConfig rows_config(int idx) { return kRows[idx].cfg; }
+
+int rows_ctas(int64_t N, int occ) { return (int)std::min<int64_t>(N, (int64_t)device_sm_count() * occ); }
+
+size_t rows_smem_bytes(const RowsConfig& c, int64_t N, int64_t K, int occ) {
+    return rows_smem_layout(K, N, rows_ctas(N, occ), c.warps, c.depth, c.seg).total;
+}
+
+cudaError_t launch_gemv_rows(const Plan& p, const GemvArgs& a, cudaStream_t s) {
+    if (p.cfg < 0 || p.cfg >= rows_num_configs() || a.M != 1 || p.split != 1 || p.occ < 1 || a.N < 1)
+        return cudaErrorInvalidValue;
+    const RowsEntry& e = kRows[p.cfg];
+    const int G = rows_ctas(a.N, p.occ);
+    const size_t smem = rows_smem_bytes(e.cfg, a.N, a.K, p.occ);
+    if (smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)G, 1, 1);
+    cfg.blockDim = dim3((unsigned)(e.cfg.warps * 32), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
+    count_launch();
+    return cudaLaunchKernelEx(&cfg, e.fn, a, G);
 }
 
 // The expiry path of the bounded wait, run on purpose: one thread waits on an

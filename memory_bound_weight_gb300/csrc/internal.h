@@ -54,8 +54,10 @@ inline int gemv_fused_args(const GemvArgs& a) { return (a.glu || a.norm_w || a.r
 struct SimtConfig {
     int warps;  // warps per CTA, each owning its own rows
     int r;      // rows per warp, streamed together
-    int u;      // 16-byte chunks per lane per row in flight
+    int u;      // chunks per lane per row in flight
     int mb;     // activation rows (batch) per launch
+    int cb;     // bytes per lane per load: 16, or 32 (BF16 batch 1: a warp reads 1 KB of a row per load)
+    int persist = 0;  // 32-byte BF16 only: occ CTAs per SM loop over the row groups (no split)
 };
 
 // One instantiation of the tensor-core (mma.sync) streaming kernel.
@@ -80,6 +82,14 @@ struct LatConfig {
 struct TmaConfig {
     int warps;  // consumer warps per CTA (plus one producer warp)
     int depth;  // shared-memory ring stages
+};
+
+// One instantiation of the BF16 row-stream kernel (gemv_tma.cu): per-warp
+// bulk-copy rings over the CTA's contiguous rows.
+struct RowsConfig {
+    int warps;  // warps per CTA, each with its own ring and copy-issuing lane
+    int depth;  // ring slots per warp
+    int seg;    // bytes per stage (one bulk copy)
 };
 
 // One instantiation of the batched AWQ mma.sync kernel (gemv_awq_batch.cu).
@@ -108,6 +118,7 @@ enum PlanKind : int {
     PLAN_TC = 4,
     PLAN_LAT = 5,
     PLAN_AWQB = 6,
+    PLAN_ROWS = 7,
 };
 
 // Kernel tables (gemv_simt.cu).
@@ -170,6 +181,11 @@ int tma_num_configs(int fmt);
 TmaConfig tma_config(int fmt, int idx);
 size_t tma_smem_bytes(int fmt, const TmaConfig& c, int64_t N, int64_t K, int M, int split, int occ);
 cudaError_t launch_gemv_tma(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
+int rows_num_configs();
+RowsConfig rows_config(int idx);
+int rows_ctas(int64_t N, int occ);
+size_t rows_smem_bytes(const RowsConfig& c, int64_t N, int64_t K, int occ);
+cudaError_t launch_gemv_rows(const Plan& p, const GemvArgs& a, cudaStream_t s);
 int tma_take_fault();  // 1 if a bounded device wait expired since the last call (and clear it)
 cudaError_t launch_tma_wait_expiry(long long tries, cudaStream_t s);  // a bounded wait that expires
 

@@ -72,6 +72,7 @@ int plan_batch_width(int fmt, const Plan& p) {
     if (p.kind == PLAN_MMA2) return mma2_max_batch(fmt);
     if (p.kind == PLAN_LAT) return lat_max_batch(fmt);
     if (p.kind == PLAN_MMA || p.kind == PLAN_TMA) return mma_max_batch(fmt);
+    if (p.kind == PLAN_ROWS) return 1;
     return simt_config(fmt, p.cfg).mb;
 }
 
@@ -126,11 +127,19 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K, 
         return sm <= kSmemLimit && sm * p.occ <= (size_t)227 * 1024;
     }
     if (p.kind == PLAN_SIMT) {
-        if (p.cfg < 0 || p.cfg >= simt_num_configs(fmt) || p.occ != 1) return false;
+        if (p.cfg < 0 || p.cfg >= simt_num_configs(fmt)) return false;
         const SimtConfig c = simt_config(fmt, p.cfg);
+        if (c.persist) {
+            // occ CTAs per SM, each holding the whole of x; at least one row group per warp
+            if (M != 1 || p.split != 1 || p.occ < 1 || p.occ * c.warps > 32 || K % 16 != 0) return false;
+            if ((int64_t)device_sm_count() * p.occ * c.warps * c.r > N) return false;
+            return simt_smem(fmt, c, K, 1) * p.occ <= (size_t)227 * 1024;
+        }
+        if (p.occ != 1) return false;
         if (c.mb != simt_want_mb(M)) return false;
+        if (c.cb == 32 && (fmt != FMT_BF16 || K % 16 != 0)) return false;  // whole 32-byte chunks per row
         if (simt_smem(fmt, c, K, p.split) > kSmemLimit) return false;
-        const int chunks = chunks_of(fmt, K);
+        const int chunks = chunks_of(fmt, K) / (c.cb / 16);
         if (p.split > 1 && (chunks + p.split - 1) / p.split < 16) return false;
         return true;
     }
@@ -166,6 +175,13 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K, 
         if (c.ni > items + 1) return false;  // a smaller instantiation holds this share
         if (lat_smem_bytes(fmt, c, N, K, mb, p.split, p.occ, glu, fuse ? 1 : 0) > kSmemLimit) return false;
         return true;
+    }
+    if (p.kind == PLAN_ROWS) {
+        // BF16 batch 1, one CTA row range per SM (or two), x staged whole
+        if (fmt != FMT_BF16 || M != 1 || p.split != 1 || p.cfg < 0 || p.cfg >= rows_num_configs()) return false;
+        if (p.occ < 1 || p.occ > 2 || 2 * K > 64 * 1024) return false;
+        const size_t sm = rows_smem_bytes(rows_config(p.cfg), N, K, p.occ);
+        return sm <= (size_t)227 * 1024 / p.occ && (p.occ == 1 || sm <= kSmemLimit);
     }
     if (p.kind == PLAN_TMA) {
         if (p.cfg < 0 || p.cfg >= tma_num_configs(fmt)) return false;
@@ -222,6 +238,11 @@ static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
                 Plan p{PLAN_LAT, cfg, splits[si], occ};
                 if (plan_valid(fmt, p, Mb, N, K, flags)) out.push_back(p);
             }
+    for (int cfg = 0; cfg < rows_num_configs(); ++cfg)
+        for (int occ = 1; occ <= 2; ++occ) {
+            Plan p{PLAN_ROWS, cfg, 1, occ};
+            if (plan_valid(fmt, p, Mb, N, K, flags)) out.push_back(p);
+        }
     for (int cfg = 0; cfg < tma_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si)
             for (int occ = 1; occ <= 2; ++occ) {
@@ -229,10 +250,11 @@ static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
                 if (plan_valid(fmt, p, Mb, N, K, flags)) out.push_back(p);
             }
     for (int cfg = 0; cfg < simt_num_configs(fmt); ++cfg)
-        for (int si = 0; si < 4; ++si) {
-            Plan p{PLAN_SIMT, cfg, splits[si], 1};
-            if (plan_valid(fmt, p, Mb, N, K, flags)) out.push_back(p);
-        }
+        for (int si = 0; si < 4; ++si)
+            for (int occ = 1; occ <= 8; ++occ) {
+                Plan p{PLAN_SIMT, cfg, splits[si], occ};
+                if (plan_valid(fmt, p, Mb, N, K, flags)) out.push_back(p);
+            }
     return out;
 }
 
@@ -364,14 +386,20 @@ std::string plan_to_string(int op, const Plan& p) {
         const TmaConfig c = tma_config(fmt, p.cfg);
         snprintf(buf, sizeof(buf), "tma fmt=%s consumer_warps=%d ring_stages=%d ctas_per_sm=%d split_k=%d", fs,
                  c.warps, c.depth, p.occ, p.split);
+    } else if (p.kind == PLAN_ROWS) {
+        const RowsConfig c = rows_config(p.cfg);
+        snprintf(buf, sizeof(buf), "rows fmt=%s warps=%d ring_slots_per_warp=%d stage_bytes=%d ctas_per_sm=%d split_k=%d",
+                 fs, c.warps, c.depth, c.seg, p.occ, p.split);
     } else if (p.kind == PLAN_MMA) {
         const MmaConfig c = mma_config(fmt, p.cfg);
         snprintf(buf, sizeof(buf), "mma fmt=%s warps=%d blocks_in_flight=%d ctas_per_sm=%d split_k=%d", fs, c.warps,
                  c.u, p.occ, p.split);
     } else {
         const SimtConfig c = simt_config(fmt, p.cfg);
-        snprintf(buf, sizeof(buf), "simt fmt=%s warps=%d rows_per_warp=%d chunks_in_flight=%d batch=%d split_k=%d",
-                 fs, c.warps, c.r, c.u, c.mb, p.split);
+        snprintf(buf, sizeof(buf),
+                 "simt fmt=%s warps=%d rows_per_warp=%d chunks_in_flight=%d chunk_bytes=%d batch=%d split_k=%d%s", fs,
+                 c.warps, c.r, c.u, c.cb, c.mb, p.split,
+                 c.persist ? (" persistent ctas_per_sm=" + std::to_string(p.occ)).c_str() : "");
     }
     std::string out = buf;
     if (op & MBW_FUSE_NORM) out += " +rmsnorm";
@@ -390,6 +418,7 @@ cudaError_t launch_plan(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t 
     if (p.kind == PLAN_MMA2) return launch_gemv_mma2(fmt, p, a, s);
     if (p.kind == PLAN_LAT) return launch_gemv_lat(fmt, p, a, s);
     if (p.kind == PLAN_TMA) return launch_gemv_tma(fmt, p, a, s);
+    if (p.kind == PLAN_ROWS) return launch_gemv_rows(p, a, s);
     if (p.kind == PLAN_MMA) return launch_gemv_mma(fmt, p, a, s);
     return launch_gemv_simt(fmt, p, a, s);
 }
@@ -495,6 +524,7 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
     const size_t target = (size_t)384 << 20;  // about three times the L2
     int copies = (int)std::max<size_t>(2, (target + wb - 1) / wb);
     copies = std::min(copies, 96);
+    const int launches = copies;  // one launch per copy: the first launch's ramp counts, as after a shape change
 
     uint8_t* wbuf = nullptr;
     uint16_t* xbuf = nullptr;
@@ -542,8 +572,8 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
         e = cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal);
         if (e != cudaSuccess) break;
         cudaError_t le = cudaSuccess;
-        for (int i = 0; i < copies && le == cudaSuccess; ++i) {
-            a.W = wbuf + (size_t)i * wstride;
+        for (int i = 0; i < launches && le == cudaSuccess; ++i) {
+            a.W = wbuf + (size_t)(i % copies) * wstride;
             a.scales = (const uint16_t*)(a.W + codes);
             a.zeros = (const uint8_t*)(a.W + codes + (size_t)N * a.groups * 2);
             a.rscale = (const float*)(a.W + codes);
@@ -583,7 +613,7 @@ extern "C" mbw_status mbw_autotune(int op, int64_t M, int64_t N, int64_t K, mbw_
         cudaGraphExecDestroy(ge);
         if (e != cudaSuccess) break;
         std::sort(times, times + 3);
-        const float per = times[1] / copies;
+        const float per = times[1] / launches;
         if (getenv("MBW_LOG") && atoi(getenv("MBW_LOG")) >= 2)
             fprintf(stderr, "[mbw]   candidate %zu %s: %.3f us\n", ci, plan_to_string(op, p).c_str(), per * 1e3f);
         if (per < best_ms) {

@@ -189,6 +189,37 @@ def test_planner_host_logic(L):
             kinds.add(buf.value.split()[0])
         assert b"simt" not in kinds
         assert (b"tcgen05" in kinds) == (M > 4)
+    # BF16 SIMT with 32-byte lane loads needs K % 16 == 0; its persistent form
+    # needs batch 1, no split, and at least one row group per warp of the grid
+    def simt_descs(M, N, K):
+        out = []
+        for i in range(L.mbw_plan_candidates(1, M, N, K)):
+            assert L.mbw_plan_select(1, M, N, K, i) == 0
+            assert L.mbw_plan_describe(1, M, N, K, buf, 256) == 0
+            if buf.value.startswith(b"simt"):
+                out.append(buf.value)
+        return out
+    big = simt_descs(1, 18944, 3584)
+    assert any(b"chunk_bytes=32" in d and b"persistent" not in d for d in big)
+    pers = [d for d in big if b"persistent" in d]
+    assert pers and all(b"split_k=1 " in d for d in pers)
+    assert {int(d.split(b"ctas_per_sm=")[1]) for d in pers} == set(range(1, 9))
+    assert not any(b"chunk_bytes=32" in d for d in simt_descs(1, 18944, 1032))  # K % 16 == 8
+    assert not any(b"persistent" in d for d in simt_descs(1, 300, 3584))  # fewer rows than warps
+    assert not any(b"chunk_bytes=32" in d for d in simt_descs(2, 18944, 3584))  # batch 2
+
+    # BF16 row stream: batch 1 only, x (2K bytes) at most 64 KB, no split
+    def kinds(M, N, K):
+        out = set()
+        for i in range(L.mbw_plan_candidates(1, M, N, K)):
+            assert L.mbw_plan_select(1, M, N, K, i) == 0
+            assert L.mbw_plan_describe(1, M, N, K, buf, 256) == 0
+            out.add(buf.value.split()[0])
+            if buf.value.startswith(b"rows"):
+                assert b"split_k=1" in buf.value
+        return out
+    assert b"rows" in kinds(1, 18944, 3584) and b"rows" in kinds(1, 3584, 18944) and b"rows" in kinds(1, 1, 8)
+    assert b"rows" not in kinds(2, 18944, 3584) and b"rows" not in kinds(1, 64, 32776)
     buf = ctypes.create_string_buffer(256)
     assert L.mbw_plan_describe(5, 1, 9728, 2560, buf, 256) == 0 and b"int8_pc" in buf.value
     assert L.mbw_workspace_bytes(1, 1, 2048, 2048) == 0

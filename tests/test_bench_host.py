@@ -36,7 +36,7 @@ def test_roofline_of_the_dominant_kernel_hbm_bound():
     peak = 6778.3
     shapes = {(0, 11264, 2048): 5.0, (0, 2048, 2048): 1.7}
     counts = {(0, 11264, 2048): 22, (0, 2048, 2048): 44}
-    times = {bench.skey(sh): {"us": us} for sh, us in shapes.items()}
+    times = {bench.skey(sh): {"us": us, "copies": 8, "launches": 40} for sh, us in shapes.items()}
     plans = {bench.skey(sh): "lat ..." for sh in shapes}
     r = bench.roofline_fields(FakeStep(wl.FMT_INT4_G64, 1), 0.29, 1900.0, peak, "measured", 123, plans, 89,
                               (0, 11264, 2048), counts, times)
@@ -52,7 +52,7 @@ def test_roofline_of_the_dominant_kernel_hbm_bound():
 def test_roofline_switches_to_the_tensor_bound_when_the_contraction_is_longer():
     tc, _ = bench.tensor_peak()
     sh = (0, 18944, 3584)
-    times = {bench.skey(sh): {"us": 100.0}}
+    times = {bench.skey(sh): {"us": 100.0, "copies": 8, "launches": 40}}
     for M, bound in ((16, "hbm"), (1024, "tensor")):
         r = bench.roofline_fields(FakeStep(wl.FMT_BF16, M), 1.0, 1.0, 6778.3, "measured", None,
                                   {bench.skey(sh): "tcgen05 ..."}, 1, sh, {sh: 1}, times)

@@ -53,7 +53,7 @@ def each_plan(op, M, N, K):
 
 
 # ------------------------------------------------------------ small shapes ----
-@pytest.mark.parametrize("N,K", [(1, 8), (7, 64), (33, 200), (257, 1032), (1000, 2048), (96, 5632)])
+@pytest.mark.parametrize("N,K", [(1, 8), (7, 64), (33, 200), (257, 1032), (1000, 2048), (96, 5632), (2501, 1040)])
 def test_bf16_all_plans(orc, N, K):
     W, X = bf16_case(100 + N, N, K)
     Y, A = orc.gemm_bf16(W, X)
