@@ -102,7 +102,7 @@ struct MmaTraits<FMT_AWQ> {
 // Shared memory layout of one launch (bytes): x words (later reused for the
 // per-CTA sums) at 0, per-warp partial sums at red_off.
 struct MmaSmem {
-    int xwords;  // 16-byte x words per batch row
+    int xwords;  // 16-byte x words per batch row (as laid out in shared memory)
     int ntmax;   // most tiles any CTA owns
     size_t x_bytes, red_off, red_bytes, total;
 };
@@ -111,10 +111,13 @@ __host__ __device__ inline MmaSmem mma_smem_layout(int BK, int64_t K, int N, int
     MmaSmem L;
     const int64_t KB = (K + BK - 1) / BK;
     const int64_t BS = (KB + (int64_t)S * W - 1) / ((int64_t)S * W);
-    L.xwords = (int)(W * BS * (BK / 8));
+    // 256-k super-blocks (INT4, "mma2"): the four 8-word quarters at word 10 q, so
+    // that the four quarters' lanes reading word w hit four different bank groups
+    const int xpb = (BK == 256) ? 40 : BK / 8;
+    L.xwords = (int)(W * BS * xpb);
     const int T = (N + 15) / 16;
     L.ntmax = (T + G - 1) / G * (glu ? 2 : 1);  // logical tiles (gate/up pairs under the gated epilogue)
-    L.x_bytes = ((size_t)M * L.xwords + BK / 8) * 16;  // + one block of zero words
+    L.x_bytes = ((size_t)M * L.xwords + xpb) * 16;  // + one block of zero words
     const size_t fin_bytes = (size_t)L.ntmax * 16 * M * 4;
     L.red_off = ((L.x_bytes > fin_bytes ? L.x_bytes : fin_bytes) + 15) / 16 * 16;
     L.red_bytes = (size_t)L.ntmax * W * 16 * M * 4;
@@ -460,7 +463,14 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     // sector-complete copies).
     // INT8: the fp32 scales of the CTA's rows, read before the wait (they are weights)
     float* rsc = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.total);
-    const size_t sc_bytes = (FMT == FMT_I8) ? (size_t)L.ntmax * 16 * 4 : 0;
+    // INT4: per-group sums of the staged x, [mb + 1][ngx] (row mb: zeros, for the unused batch columns)
+    constexpr bool ZF = (FMT == FMT_G64 || FMT == FMT_AWQ);
+    constexpr int GW = (FMT == FMT_AWQ) ? 16 : 8;  // 16-byte x words per quantization group
+    constexpr int XP = ZF ? 40 : XW;           // physical x words per super-block
+    const int lxw = L.xwords / XP * XW;       // logical x words per batch row
+    const int ngx = ZF ? lxw / GW : 0;
+    float* xsum = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.total);
+    const size_t sc_bytes = (FMT == FMT_I8) ? (size_t)L.ntmax * 16 * 4 : ZF ? (size_t)(mb + 1) * ngx * 4 : 0;
     uint8_t* abase = reinterpret_cast<uint8_t*>(smem_u4) + (L.total + sc_bytes + 127) / 128 * 128 +
                      (size_t)warp * U * 4 * 512;
     const uint8_t* aring = abase + lane * 16;
@@ -521,11 +531,16 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
 
     uint4* xs = smem_u4;
     const int cwords = max(0, min(KB, cb0 + W * BS) - cb0) * XW;
-    for (int i = threadIdx.x; i < mb * L.xwords + XW; i += W * 32) {
+    const int nxw = mb * lxw;  // logical words
+    // every thread runs the same number of rounds, so that (INT4) the group
+    // sums can be reduced over the group's consecutive lanes
+    for (int i0 = 0; i0 < nxw + XP; i0 += W * 32) {
+        const int i = i0 + threadIdx.x;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (i < mb * L.xwords) {
-            const int m = i / L.xwords;
-            const int wi = i - m * L.xwords;
+        int m = mb, wi = i - nxw;  // the zero block
+        if (i < nxw) {
+            m = i / lxw;
+            wi = i - m * lxw;
             if (wi < cwords) {
                 v = ld_ro16(a.x + (size_t)m * a.K + (size_t)cb0 * BK + (size_t)wi * 8);
                 if (FZ && a.norm_w) v = norm_word(v, nscr[W * mb + m], a.norm_w + (size_t)cb0 * BK + (size_t)wi * 8);
@@ -535,8 +550,23 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
             else if (FMT != FMT_BF16 && !a.x_natural)
                 v = perm_pairs(v);
         }
-        xs[i] = v;
+        if (i < nxw + XP) {
+            // INT4: logical word 32 b + 8 q + w of a batch row sits at 40 b + 10 q + w
+            // (the zero block, m = mb, is written as it is: XP zero words)
+            const int pw = (ZF && i < nxw) ? (wi >> 5) * 40 + ((wi & 31) >> 3) * 10 + (wi & 7) : wi;
+            xs[(size_t)m * L.xwords + pw] = v;
+        }
+        if (ZF) {
+            // sum of the group's x (the pair permutation stays inside a word)
+            float t = ((bf16lo_to_f32(v.x) + bf16hi_to_f32(v.x)) + (bf16lo_to_f32(v.y) + bf16hi_to_f32(v.y))) +
+                      ((bf16lo_to_f32(v.z) + bf16hi_to_f32(v.z)) + (bf16lo_to_f32(v.w) + bf16hi_to_f32(v.w)));
+#pragma unroll
+            for (int o = 1; o < GW; o <<= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+            if (i < nxw && (i & (GW - 1)) == 0) xsum[i / GW] = t;  // a batch row's words: a multiple of GW
+        }
     }
+    if (ZF)
+        for (int i = threadIdx.x; i < ngx; i += W * 32) xsum[mb * ngx + i] = 0.f;
     __syncthreads();
 
     // B fragment of this lane: column n = g
@@ -554,9 +584,18 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     }
     // lane's x words of a super-block: INT4 words 8q .. 8q+7, INT8 4q .. 4q+3, BF16 2q, 2q+1
     const int xoff = (FMT == FMT_BF16) ? 2 * q : (FMT == FMT_I8) ? 4 * q : 8 * q;
-    const uint4* xbase = xon ? xs + (size_t)xm * L.xwords + (size_t)(b0 - cb0) * XW + xoff : xs + (size_t)mb * L.xwords;
-    const int xstep = xon ? XW : 0;
+    // (INT4: the quarter at 10 q; the lanes without a column read zero words 1 .. 8,
+    // a bank group apart from the quarters' reads)
+    const int xq = ZF ? 10 * q : xoff;
+    const uint4* xbase = xon ? xs + (size_t)xm * L.xwords + (size_t)(b0 - cb0) * XP + xq
+                             : xs + (size_t)mb * L.xwords + (ZF ? 1 : 0);
+    const int xstep = xon ? XP : 0;
     const uint4* xp = xbase;
+    // INT4: x sums of the groups of this lane's two accumulator columns (AWQ: groups 0, 1 of batch q;
+    // group-64: groups 2(q&1), 2(q&1)+1 of batch q>>1), one super-block at a time
+    const int zm = (FMT == FMT_AWQ) ? min(q, mb) : min(q >> 1, mb);
+    const int xgbase = zm * ngx + (b0 - cb0) * (BK / (GW * 8)) + ((FMT == FMT_G64) ? 2 * (q & 1) : 0);
+    int xg = xgbase;
     float* red = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.red_off);
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -606,14 +645,10 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
                             mma_bf16_16816(acc, p0, p1, p2, p3, xv.x, xv.y);
                     }
                 } else {
-                    uint32_t zz0, zz1;
-                    if (FMT == FMT_G64) {
-                        zz0 = zz1 = 0x43084308u;
-                    } else {
-                        const uint32_t sh = (q >> 1) * 4;  // this lane's group: low or high nibble
-                        zz0 = (0x4300u | ((zb >> sh) & 0xF)) * 0x00010001u;
-                        zz1 = (0x4300u | ((zb >> (8 + sh)) & 0xF)) * 0x00010001u;
-                    }
+                    // the MMAs take each code as the bf16 value 128 + n (exact), so column j of row r
+                    // sums (128 + n) x over group j, and the zero point comes off once per group:
+                    // sum (n - z) x = D - (128 + z) X_j, X_j the group's x sum. Zero points of rows g,
+                    // g+8: AWQ bytes zb bits 0-7, 8-15, group 0 in the low nibble; group-64: z = 8.
                     float d0[4] = {0.f, 0.f, 0.f, 0.f};
                     float d1[4] = {0.f, 0.f, 0.f, 0.f};
                     const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
@@ -621,28 +656,28 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
 #pragma unroll
                     for (int w = 0; w < 8; ++w) {
                         const uint4 xv = xp[w];
-                        mma_bf16_16816(d0, bf16x2_sub(nib_pair(wa[w]), zz0), bf16x2_sub(nib_pair(wb[w]), zz1),
-                                       bf16x2_sub(nib_pair(wa[w] >> 4), zz0), bf16x2_sub(nib_pair(wb[w] >> 4), zz1),
-                                       xv.x, xv.y);
-                        mma_bf16_16816(d1, bf16x2_sub(nib_pair(wa[w] >> 8), zz0), bf16x2_sub(nib_pair(wb[w] >> 8), zz1),
-                                       bf16x2_sub(nib_pair(wa[w] >> 12), zz0),
-                                       bf16x2_sub(nib_pair(wb[w] >> 12), zz1), xv.z, xv.w);
+                        mma_bf16_16816(d0, nib_pair(wa[w]), nib_pair(wb[w]), nib_pair(wa[w] >> 4),
+                                       nib_pair(wb[w] >> 4), xv.x, xv.y);
+                        mma_bf16_16816(d1, nib_pair(wa[w] >> 8), nib_pair(wb[w] >> 8), nib_pair(wa[w] >> 12),
+                                       nib_pair(wb[w] >> 12), xv.z, xv.w);
                     }
                     const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&s0));
                     const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&s1));
+                    const float2 X = *reinterpret_cast<const float2*>(xsum + xg);
+                    float zg0, zg1, zh0, zh1;  // 128 + z of rows g and g+8 for the lane's two columns
                     if (FMT == FMT_G64) {
-                        // columns 2q, 2q+1 = groups 2(q&1), 2(q&1)+1 of batch q>>1
-                        acc[0] = fmaf(f0.x, d0[0] + d1[0], acc[0]);
-                        acc[0] = fmaf(f0.y, d0[1] + d1[1], acc[0]);
-                        acc[2] = fmaf(f1.x, d0[2] + d1[2], acc[2]);
-                        acc[2] = fmaf(f1.y, d0[3] + d1[3], acc[2]);
+                        zg0 = zg1 = zh0 = zh1 = 136.f;
                     } else {
-                        // columns 2q, 2q+1 = groups 0, 1 of batch q
-                        acc[0] = fmaf(f0.x, d0[0] + d1[0], acc[0]);
-                        acc[0] = fmaf(f0.y, d0[1] + d1[1], acc[0]);
-                        acc[2] = fmaf(f1.x, d0[2] + d1[2], acc[2]);
-                        acc[2] = fmaf(f1.y, d0[3] + d1[3], acc[2]);
+                        zg0 = __uint_as_float(0x43000000u | ((zb << 16) & 0x000F0000u));
+                        zg1 = __uint_as_float(0x43000000u | ((zb << 12) & 0x000F0000u));
+                        zh0 = __uint_as_float(0x43000000u | ((zb << 8) & 0x000F0000u));
+                        zh1 = __uint_as_float(0x43000000u | ((zb << 4) & 0x000F0000u));
                     }
+                    acc[0] = fmaf(f0.x, fmaf(-zg0, X.x, d0[0] + d1[0]), acc[0]);
+                    acc[0] = fmaf(f0.y, fmaf(-zg1, X.y, d0[1] + d1[1]), acc[0]);
+                    acc[2] = fmaf(f1.x, fmaf(-zh0, X.x, d0[2] + d1[2]), acc[2]);
+                    acc[2] = fmaf(f1.y, fmaf(-zh1, X.y, d0[3] + d1[3]), acc[2]);
+                    xg += BK / (GW * 8);
                 }
                 if (ASYNC) {
                     __syncwarp();  // every lane has read slot u before it is refilled
@@ -683,6 +718,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
                     cb = 0;
                     ++ct;
                     xp = xbase;
+                    xg = xgbase;
                 }
             }
         }
@@ -817,7 +853,10 @@ int mma2_block_k(int fmt) { return fmt == FMT_BF16 ? 64 : fmt == FMT_I8 ? 128 : 
 size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu) {
     const int G = mma_row_groups(N, split, occ);
     const MmaSmem L = mma_smem_layout(mma2_block_k(fmt), K, (int)N, M, c.warps, split, G, glu);
-    const size_t base = L.total + (fmt == FMT_I8 ? (size_t)L.ntmax * 16 * 4 : 0);  // + INT8 row scales
+    // + INT8 row scales, or the INT4 per-group x sums ([M + 1] rows of xwords / words-per-group)
+    const size_t base = L.total + (fmt == FMT_I8     ? (size_t)L.ntmax * 16 * 4
+                                   : fmt == FMT_BF16 ? 0
+                                                     : (size_t)(M + 1) * (L.xwords / 40 * 32 / (fmt == FMT_AWQ ? 16 : 8)) * 4);
     if (!c.async) return base;
     return (base + 127) / 128 * 128 + (size_t)c.warps * c.u * 4 * 512;
 }

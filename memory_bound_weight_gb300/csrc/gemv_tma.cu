@@ -688,6 +688,414 @@ cudaError_t launch_gemv_rows(const Plan& p, const GemvArgs& a, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, e.fn, a, G);
 }
 
+// ------------------------------------------------ bulk-fed INT4 GEMV ----
+// INT4 codes (group-64, or AWQ-style group-128 with zero points) at batch
+// 1 .. 4, with the arithmetic of the "mma2" kernels (gemv_mma.cu: each lane
+// takes 32 bytes of rows g and g+8 per 128-byte super-block, codes enter the
+// MMA as the exact bf16 values 128 + n, the zero point comes off once per group
+// against the group's x sum), but fed like the row stream above: one producer
+// lane copies, per stage, the 16 rows of a tile over a chunk of the CTA's
+// k-range, one cp.async.bulk per row, into a ring of D stages shared by the W
+// consumer warps. A register ring holds a few KB per warp; this ring holds up
+// to ~170 KB per SM, issued by one thread, so the consumers spend no issue
+// slots on load addresses and the stream keeps enough bytes in flight.
+//
+//   * stage i = (tile i / nch, chunk i % nch): rows at a stride of KC * 128 + 16
+//     bytes (rows g and g + 1 then fall in different bank groups for the
+//     16-byte fragment reads); consumer warp w takes super-blocks
+//     w BSC .. w BSC + BSC - 1 of the chunk;
+//   * full[s] (expect-tx) and empty[s] (one arrival per consumer warp); the
+//     producer never waits for the previous grid, the consumers wait before
+//     staging x;
+//   * group scales and zero points are loaded per lane from global memory
+//     one stage ahead (a few bytes per super-block);
+//   * x sits in shared memory with each 8-word quarter of a super-block at
+//     word 10 q (the four quarters' lanes reading word w hit four different
+//     bank groups; lanes without a batch column read zero words 1 .. 8);
+//   * per-tile partials are summed over warps (and cluster ranks, through
+//     distributed shared memory) once, in a fixed order.
+struct Q4bSmem {
+    int KR;         // super-blocks per cluster rank
+    int rowstride;  // bytes between rows of a stage
+    int xwords;     // 16-byte x words per batch row (the rank's k-range), as laid out: 40 per super-block
+    int ngx;        // quantization groups per batch row
+    int ntmax;      // most tiles any CTA owns
+    size_t stage_bytes, x_off, xsum_off, red_off, bar_off, total;
+};
+
+__host__ __device__ inline Q4bSmem q4b_smem_layout(int fmt, int64_t K, int64_t N, int M, int W, int D, int BSC, int S,
+                                                   int G) {
+    Q4bSmem L;
+    const int KB = (int)(K / 256);
+    L.KR = (KB + S - 1) / S;
+    L.rowstride = W * BSC * 128 + 16;
+    L.stage_bytes = (size_t)16 * L.rowstride;
+    L.xwords = L.KR * 40;
+    L.ngx = L.KR * 32 / (fmt == FMT_AWQ ? 16 : 8);
+    const int T = (int)((N + 15) / 16);
+    L.ntmax = (T + G - 1) / G;
+    L.x_off = (size_t)D * L.stage_bytes;
+    const size_t x_bytes = ((size_t)M * L.xwords + 40) * 16;  // + one super-block of zero words
+    const size_t fin_bytes = (size_t)L.ntmax * 16 * M * 4;    // the per-row sums, over x after the stream
+    L.xsum_off = L.x_off + ((x_bytes > fin_bytes ? x_bytes : fin_bytes) + 15) / 16 * 16;
+    L.red_off = L.xsum_off + ((size_t)(M + 1) * L.ngx * 4 + 15) / 16 * 16;
+    L.bar_off = (L.red_off + (size_t)L.ntmax * W * 16 * M * 4 + 7) / 8 * 8;
+    L.total = L.bar_off + (size_t)2 * D * 8;
+    return L;
+}
+
+template <int FMT, int W, int D, int BSC>
+__global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArgs a, const int S) {
+    constexpr int XW = 32;                         // 16-byte x words per 256-k super-block
+    constexpr int GW = (FMT == FMT_AWQ) ? 16 : 8;  // x words per quantization group
+    constexpr int GPB = 32 / GW;                   // groups per super-block
+    constexpr int KC = W * BSC;                    // super-blocks per stage
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    pdl_launch_dependents();
+
+    const int rank = (S > 1) ? (int)cg::this_cluster().block_rank() : 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int G = gridDim.x / S;
+    const int cgid = blockIdx.x / S;
+    const int T = (a.N + 15) / 16;
+    const int t0 = (int)(((long long)T * cgid) / G);
+    const int nt = (int)(((long long)T * (cgid + 1)) / G) - t0;
+    const int mb = a.M;
+    const Q4bSmem L = q4b_smem_layout(FMT, a.K, a.N, mb, W, D, BSC, S, G);
+    const int KB = (int)(a.K / 256);
+    const int kb0 = rank * L.KR;                        // the rank's first super-block
+    const int krb = max(0, min(KB, kb0 + L.KR) - kb0);  // and its count
+    const int nch = (krb + KC - 1) / KC;                // stages per tile
+    const int nst = nt * nch;
+    const size_t rowbytes = (size_t)a.K / 2;
+
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+    uint64_t* empty = full + D;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < D; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], W);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == W) {
+        // -------------------------------------------------------- producer ----
+        if (lane == 0 && nst > 0) {
+            uint64_t policy;
+            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+            bool ok = true;
+            int tl = 0, ch = 0, i = 0;
+            for (; i < nst; ++i) {
+                const int slot = i % D;
+                if (i >= D) ok = mbar_wait(&empty[slot], ((i / D) - 1) & 1);
+                if (!ok) break;
+                const int c0 = ch * KC;
+                const uint32_t bytes = (uint32_t)min(KC, krb - c0) * 128;
+                mbar_expect_tx(&full[slot], bytes * 16);
+                uint8_t* st = smem + (size_t)slot * L.stage_bytes;
+                const int row0 = (t0 + tl) * 16;
+                const uint8_t* src = a.W + (size_t)(kb0 + c0) * 128;
+                for (int r = 0; r < 16; ++r)
+                    bulk_g2s(st + (size_t)r * L.rowstride, src + (size_t)min(row0 + r, a.N - 1) * rowbytes, bytes,
+                             &full[slot], policy);
+                if (++ch == nch) {
+                    ch = 0;
+                    ++tl;
+                }
+            }
+            if (!ok) {
+                // drain: the stages issued last may still be landing (earlier slots were released)
+                for (int j = max(0, i - D); j < i; ++j) mbar_wait(&full[j % D], (j / D) & 1);
+            }
+        }
+        __syncwarp();  // the whole warp reaches the block-wide barriers below together
+    } else {
+        // ------------------------------------------------------- consumers ----
+        pdl_wait();
+        uint4* xs = reinterpret_cast<uint4*>(smem + L.x_off);
+        float* xsum = reinterpret_cast<float*>(smem + L.xsum_off);
+        const int cwords = krb * XW;
+        const int lxw = L.KR * XW;  // logical x words per batch row
+        const int nxw = mb * lxw;
+        for (int i0 = 0; i0 < nxw + 40; i0 += W * 32) {
+            const int i = i0 + threadIdx.x;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            int m = mb, wi = i - nxw;  // the zero block
+            if (i < nxw) {
+                m = i / lxw;
+                wi = i - m * lxw;
+                if (wi < cwords) v = ld_ro16(a.x + (size_t)m * a.K + (size_t)kb0 * 256 + (size_t)wi * 8);
+                if (!a.x_natural) v = pair_perm(v);
+            }
+            if (i < nxw + 40) {
+                const int pw = (i < nxw) ? (wi >> 5) * 40 + ((wi & 31) >> 3) * 10 + (wi & 7) : wi;
+                xs[(size_t)m * L.xwords + pw] = v;
+            }
+            // the group's x sum (the pair permutation stays inside a word)
+            float t = ((bf16lo_to_f32(v.x) + bf16hi_to_f32(v.x)) + (bf16lo_to_f32(v.y) + bf16hi_to_f32(v.y))) +
+                      ((bf16lo_to_f32(v.z) + bf16hi_to_f32(v.z)) + (bf16lo_to_f32(v.w) + bf16hi_to_f32(v.w)));
+#pragma unroll
+            for (int o = 1; o < GW; o <<= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+            if (i < nxw && (i & (GW - 1)) == 0) xsum[i / GW] = t;
+        }
+        for (int i = threadIdx.x; i < L.ngx; i += W * 32) xsum[mb * L.ngx + i] = 0.f;
+        asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
+
+        // B fragment of this lane (column n = g): group-64 n = 4m + j, AWQ n = 2m + j
+        int xm;
+        bool xon;
+        if (FMT == FMT_G64) {
+            xm = g >> 2;
+            xon = (xm < mb) && ((g & 3) == q);
+        } else {
+            xm = g >> 1;
+            xon = (xm < mb) && ((g & 1) == (q >> 1));
+        }
+        const uint4* xrow = xon ? xs + (size_t)xm * L.xwords + 10 * q : xs + (size_t)mb * L.xwords + 1;
+        const int xstep = xon ? 40 : 0;
+        // x sums of this lane's two accumulator columns (AWQ: groups 0, 1 of batch q;
+        // group-64: groups 2(q&1), 2(q&1)+1 of batch q>>1)
+        const int zm = (FMT == FMT_AWQ) ? min(q, mb) : min(q >> 1, mb);
+        const float* xgrow = xsum + (size_t)zm * L.ngx + ((FMT == FMT_G64) ? 2 * (q & 1) : 0);
+        float* red = reinterpret_cast<float*>(smem + L.red_off);
+        const uint16_t* sc = a.scales;
+
+        // scales and zero points of this warp's super-blocks of stage (tl, ch), for rows g and g+8
+        auto load_sc = [&](int tl, int ch, uint32_t (&s0)[BSC], uint32_t (&s1)[BSC], uint32_t (&zb)[BSC]) {
+            const int row0 = (t0 + tl) * 16;
+            const int r0 = min(row0 + g, a.N - 1), r1 = min(row0 + g + 8, a.N - 1);
+            const int cb = ch * KC + warp * BSC;
+#pragma unroll
+            for (int j = 0; j < BSC; ++j) {
+                const int gb = kb0 + min(cb + j, krb - 1);
+                if (FMT == FMT_G64) {
+                    const uint16_t* p0 = sc + (size_t)r0 * a.groups + (size_t)gb * 4 + 2 * (q & 1);
+                    const uint16_t* p1 = sc + (size_t)r1 * a.groups + (size_t)gb * 4 + 2 * (q & 1);
+                    s0[j] = (uint32_t)ld_ro_u16(p0) | ((uint32_t)ld_ro_u16(p0 + 1) << 16);
+                    s1[j] = (uint32_t)ld_ro_u16(p1) | ((uint32_t)ld_ro_u16(p1 + 1) << 16);
+                    zb[j] = 0;
+                } else {
+                    const uint16_t* p0 = sc + (size_t)r0 * a.groups + (size_t)gb * 2;
+                    const uint16_t* p1 = sc + (size_t)r1 * a.groups + (size_t)gb * 2;
+                    s0[j] = (uint32_t)ld_ro_u16(p0) | ((uint32_t)ld_ro_u16(p0 + 1) << 16);
+                    s1[j] = (uint32_t)ld_ro_u16(p1) | ((uint32_t)ld_ro_u16(p1 + 1) << 16);
+                    zb[j] = (uint32_t)ld_ro_u8(a.zeros + (size_t)r0 * a.zstride + gb) |
+                            ((uint32_t)ld_ro_u8(a.zeros + (size_t)r1 * a.zstride + gb) << 8);
+                }
+            }
+        };
+        uint32_t ns0[BSC], ns1[BSC], nzb[BSC];
+        if (nst > 0) load_sc(0, 0, ns0, ns1, nzb);
+
+        bool ok = true;
+        int i = 0;
+        for (int tl = 0; tl < nt && ok; ++tl) {
+            float acc0 = 0.f, acc2 = 0.f;
+            for (int ch = 0; ch < nch; ++ch, ++i) {
+                const int slot = i % D;
+                const int cb = ch * KC + warp * BSC;  // rank-local super-block of j = 0
+                uint32_t s0[BSC], s1[BSC], zb[BSC];
+#pragma unroll
+                for (int j = 0; j < BSC; ++j) {
+                    s0[j] = ns0[j];
+                    s1[j] = ns1[j];
+                    zb[j] = nzb[j];
+                }
+                if (i + 1 < nst) {
+                    if (ch + 1 < nch)
+                        load_sc(tl, ch + 1, ns0, ns1, nzb);
+                    else
+                        load_sc(tl + 1, 0, ns0, ns1, nzb);
+                }
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(&full[slot], (i / D) & 1));
+                if (!ok) break;
+                const uint8_t* st = smem + (size_t)slot * L.stage_bytes + (size_t)g * L.rowstride +
+                                    (size_t)(warp * BSC) * 128 + q * 32;
+#pragma unroll
+                for (int j = 0; j < BSC; ++j) {
+                    if (cb + j < krb) {
+                        const uint8_t* p = st + j * 128;
+                        const uint4 a0 = *reinterpret_cast<const uint4*>(p);
+                        const uint4 a1 = *reinterpret_cast<const uint4*>(p + 16);
+                        const uint4 c0 = *reinterpret_cast<const uint4*>(p + 8 * L.rowstride);
+                        const uint4 c1 = *reinterpret_cast<const uint4*>(p + 8 * L.rowstride + 16);
+                        const uint4* xp = xrow + (size_t)(cb + j) * xstep;
+                        // four accumulator sets: chains of 4 dependent MMAs instead of 8
+                        float d0[4] = {0.f, 0.f, 0.f, 0.f};
+                        float d1[4] = {0.f, 0.f, 0.f, 0.f};
+                        float e0[4] = {0.f, 0.f, 0.f, 0.f};
+                        float e1[4] = {0.f, 0.f, 0.f, 0.f};
+                        const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                        const uint32_t wb[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                        for (int w = 0; w < 8; w += 2) {
+                            const uint4 xv = xp[w], xu = xp[w + 1];
+                            mma_16816(d0, nibs(wa[w]), nibs(wb[w]), nibs(wa[w] >> 4), nibs(wb[w] >> 4), xv.x, xv.y);
+                            mma_16816(d1, nibs(wa[w] >> 8), nibs(wb[w] >> 8), nibs(wa[w] >> 12), nibs(wb[w] >> 12),
+                                      xv.z, xv.w);
+                            mma_16816(e0, nibs(wa[w + 1]), nibs(wb[w + 1]), nibs(wa[w + 1] >> 4), nibs(wb[w + 1] >> 4),
+                                      xu.x, xu.y);
+                            mma_16816(e1, nibs(wa[w + 1] >> 8), nibs(wb[w + 1] >> 8), nibs(wa[w + 1] >> 12),
+                                      nibs(wb[w + 1] >> 12), xu.z, xu.w);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            d0[e] += e0[e];
+                            d1[e] += e1[e];
+                        }
+                        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&s0[j]));
+                        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&s1[j]));
+                        const float2 X = *reinterpret_cast<const float2*>(xgrow + (size_t)(cb + j) * GPB);
+                        float zg0, zg1, zh0, zh1;  // 128 + z of rows g and g+8 for the lane's two columns
+                        if (FMT == FMT_G64) {
+                            zg0 = zg1 = zh0 = zh1 = 136.f;
+                        } else {
+                            zg0 = __uint_as_float(0x43000000u | ((zb[j] << 16) & 0x000F0000u));
+                            zg1 = __uint_as_float(0x43000000u | ((zb[j] << 12) & 0x000F0000u));
+                            zh0 = __uint_as_float(0x43000000u | ((zb[j] << 8) & 0x000F0000u));
+                            zh1 = __uint_as_float(0x43000000u | ((zb[j] << 4) & 0x000F0000u));
+                        }
+                        acc0 = fmaf(f0.x, fmaf(-zg0, X.x, d0[0] + d1[0]), acc0);
+                        acc0 = fmaf(f0.y, fmaf(-zg1, X.y, d0[1] + d1[1]), acc0);
+                        acc2 = fmaf(f1.x, fmaf(-zh0, X.x, d0[2] + d1[2]), acc2);
+                        acc2 = fmaf(f1.y, fmaf(-zh1, X.y, d0[3] + d1[3]), acc2);
+                    }
+                }
+                __syncwarp();  // every lane has read the stage
+                if (lane == 0) mbar_arrive(&empty[slot]);
+            }
+            if (!ok) break;
+            float* rp = red + ((size_t)(tl * W + warp) * 16) * mb;
+            if (FMT == FMT_G64) {
+                // lanes q and q^1 hold the other two groups of the same batch
+                const float v0 = acc0 + __shfl_xor_sync(0xFFFFFFFFu, acc0, 1);
+                const float v2 = acc2 + __shfl_xor_sync(0xFFFFFFFFu, acc2, 1);
+                const int m = q >> 1;
+                if ((q & 1) == 0 && m < mb) {
+                    rp[g * mb + m] = v0;
+                    rp[(g + 8) * mb + m] = v2;
+                }
+            } else if (q < mb) {
+                rp[g * mb + q] = acc0;
+                rp[(g + 8) * mb + q] = acc2;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
+        float* fin = reinterpret_cast<float*>(smem + L.x_off);  // [tile row][m]: sums over the warps
+        for (int k = threadIdx.x; k < nt * 16 * mb; k += W * 32) {
+            const int t = k / (16 * mb);
+            const int rm = k - t * 16 * mb;
+            float v = 0.f;
+            for (int w = 0; w < W; ++w) v += red[((size_t)(t * W + w) * 16) * mb + rm];
+            fin[k] = v;
+        }
+    }
+    float* fin = reinterpret_cast<float*>(smem + L.x_off);
+    if (S == 1) {
+        __syncthreads();
+        for (int k = threadIdx.x; k < nt * 16 * mb; k += (W + 1) * 32) {
+            const int m = k / (nt * 16), o = k - m * nt * 16;
+            if (t0 * 16 + o < a.N) store_out(a.y, (int64_t)m * a.N + t0 * 16 + o, fin[o * mb + m], a.out_f32);
+        }
+        return;
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    // rank s writes rows [s Ro / S, (s + 1) Ro / S) of the CTA group's Ro rows, every batch row
+    const int Ro = nt * 16;
+    const int lo = rank * Ro / S, hi = (rank + 1) * Ro / S;
+    const int span = hi - lo;
+    for (int k = threadIdx.x; k < span * mb; k += (W + 1) * 32) {
+        const int m = k / span, o = lo + (k - m * span);
+        float v = 0.f;
+        for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(fin + o * mb + m, s);
+        if (t0 * 16 + o < a.N) store_out(a.y, (int64_t)m * a.N + t0 * 16 + o, v, a.out_f32);
+    }
+    cluster.sync();
+}
+
+struct Q4bEntry {
+    Q4bConfig cfg;
+    TmaFn fn;
+};
+#define MBW_B(F, W, D, B) \
+    { {W, D, B}, gemv_q4b_kernel<F, W, D, B> }
+static const Q4bEntry kQ4bG64[] = {MBW_B(FMT_G64, 8, 4, 1),  MBW_B(FMT_G64, 8, 6, 1),  MBW_B(FMT_G64, 4, 6, 2),
+                                   MBW_B(FMT_G64, 7, 6, 2),  MBW_B(FMT_G64, 8, 4, 2),  MBW_B(FMT_G64, 4, 4, 2),
+                                   MBW_B(FMT_G64, 14, 6, 1), MBW_B(FMT_G64, 16, 5, 1), MBW_B(FMT_G64, 11, 4, 2)};
+static const Q4bEntry kQ4bAwq[] = {MBW_B(FMT_AWQ, 8, 4, 1),  MBW_B(FMT_AWQ, 8, 6, 1),  MBW_B(FMT_AWQ, 4, 6, 2),
+                                   MBW_B(FMT_AWQ, 7, 6, 2),  MBW_B(FMT_AWQ, 8, 4, 2),  MBW_B(FMT_AWQ, 4, 4, 2),
+                                   MBW_B(FMT_AWQ, 14, 6, 1), MBW_B(FMT_AWQ, 16, 5, 1), MBW_B(FMT_AWQ, 11, 4, 2)};
+#undef MBW_B
+
+static const Q4bEntry* q4b_table(int fmt, int* n) {
+    if (fmt == FMT_G64) {
+        *n = (int)(sizeof(kQ4bG64) / sizeof(kQ4bG64[0]));
+        return kQ4bG64;
+    }
+    if (fmt == FMT_AWQ) {
+        *n = (int)(sizeof(kQ4bAwq) / sizeof(kQ4bAwq[0]));
+        return kQ4bAwq;
+    }
+    *n = 0;
+    return nullptr;
+}
+
+int q4b_num_configs(int fmt) {
+    int n;
+    q4b_table(fmt, &n);
+    return n;
+}
+
+Q4bConfig q4b_config(int fmt, int idx) {
+    int n;
+    return q4b_table(fmt, &n)[idx].cfg;
+}
+
+size_t q4b_smem_bytes(int fmt, const Q4bConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
+    const int G = mma_row_groups(N, split, occ);
+    return q4b_smem_layout(fmt, K, N, M, c.warps, c.depth, c.bsc, split, G).total;
+}
+
+cudaError_t launch_gemv_q4b(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
+    int n;
+    const Q4bEntry* t = q4b_table(fmt, &n);
+    if (!t || p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > mma2_max_batch(fmt) || a.K % 256 != 0 || a.glu)
+        return cudaErrorInvalidValue;
+    const Q4bEntry& e = t[p.cfg];
+    const int G = mma_row_groups(a.N, p.split, p.occ);
+    const size_t smem = q4b_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
+    if (smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(G * p.split), 1, 1);
+    cfg.blockDim = dim3((unsigned)((e.cfg.warps + 1) * 32), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (p.split > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)p.split;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    count_launch();
+    return cudaLaunchKernelEx(&cfg, e.fn, a, p.split);
+}
+
 // The expiry path of the bounded wait, run on purpose: one thread waits on an
 // mbarrier whose single expected arrival never comes, gives up after `tries`
 // rounds and raises the fault flag; nothing outside its shared memory is touched.

@@ -220,6 +220,18 @@ def test_planner_host_logic(L):
         return out
     assert b"rows" in kinds(1, 18944, 3584) and b"rows" in kinds(1, 3584, 18944) and b"rows" in kinds(1, 1, 8)
     assert b"rows" not in kinds(2, 18944, 3584) and b"rows" not in kinds(1, 64, 32776)
+
+    # bulk-fed INT4: group-64 (batch 1), AWQ up to batch 4, whole super-blocks, no fusions
+    def int4_kinds(op, M, N, K):
+        out = set()
+        for i in range(L.mbw_plan_candidates(op, M, N, K)):
+            assert L.mbw_plan_select(op, M, N, K, i) == 0
+            assert L.mbw_plan_describe(op, M, N, K, buf, 256) == 0
+            out.add(buf.value.split()[0])
+        return out
+    assert b"bulk" in int4_kinds(2, 1, 11264, 2048) and b"bulk" in int4_kinds(2, 1, 32000, 2048)
+    assert b"bulk" in int4_kinds(3, 4, 18944, 3584) and b"bulk" in int4_kinds(3 | 0x800, 1, 3584, 18944)
+    assert b"bulk" not in int4_kinds(3, 1, 64, 384) and b"bulk" not in int4_kinds(3 | 0x100, 1, 2048, 2048)
     buf = ctypes.create_string_buffer(256)
     assert L.mbw_plan_describe(5, 1, 9728, 2560, buf, 256) == 0 and b"int8_pc" in buf.value
     assert L.mbw_workspace_bytes(1, 1, 2048, 2048) == 0

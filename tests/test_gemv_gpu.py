@@ -74,7 +74,8 @@ def test_int4_g64_all_plans(orc, N, K):
 
 
 @pytest.mark.parametrize("N,K,M", [(3, 128, 1), (45, 384, 1), (129, 1024, 3), (64, 256, 8), (33, 640, 9),
-                                   (70, 3584, 2), (17, 18944, 1), (40, 512, 5)])
+                                   (70, 3584, 2), (17, 18944, 1), (40, 512, 5), (300, 5632, 2), (2501, 3584, 1),
+                                   (77, 18944, 4)])
 def test_int4_awq_all_plans(orc, N, K, M):
     c, s, z, X = awq_case(300 + N, N, K, M)
     Y, A = orc.gemm_int4_awq_g128(c, s, z, X)
