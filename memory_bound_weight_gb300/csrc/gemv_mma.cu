@@ -463,14 +463,10 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     // sector-complete copies).
     // INT8: the fp32 scales of the CTA's rows, read before the wait (they are weights)
     float* rsc = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.total);
-    // INT4: per-group sums of the staged x, [mb + 1][ngx] (row mb: zeros, for the unused batch columns)
-    constexpr bool ZF = (FMT == FMT_G64 || FMT == FMT_AWQ);
-    constexpr int GW = (FMT == FMT_AWQ) ? 16 : 8;  // 16-byte x words per quantization group
-    constexpr int XP = ZF ? 40 : XW;           // physical x words per super-block
-    const int lxw = L.xwords / XP * XW;       // logical x words per batch row
-    const int ngx = ZF ? lxw / GW : 0;
-    float* xsum = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.total);
-    const size_t sc_bytes = (FMT == FMT_I8) ? (size_t)L.ntmax * 16 * 4 : ZF ? (size_t)(mb + 1) * ngx * 4 : 0;
+    constexpr bool ZF = (FMT == FMT_G64 || FMT == FMT_AWQ);  // INT4: padded x super-blocks
+    constexpr int XP = ZF ? 40 : XW;                          // physical x words per super-block
+    const int lxw = L.xwords / XP * XW;                       // logical x words per batch row
+    const size_t sc_bytes = (FMT == FMT_I8) ? (size_t)L.ntmax * 16 * 4 : 0;
     uint8_t* abase = reinterpret_cast<uint8_t*>(smem_u4) + (L.total + sc_bytes + 127) / 128 * 128 +
                      (size_t)warp * U * 4 * 512;
     const uint8_t* aring = abase + lane * 16;
@@ -532,8 +528,6 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     uint4* xs = smem_u4;
     const int cwords = max(0, min(KB, cb0 + W * BS) - cb0) * XW;
     const int nxw = mb * lxw;  // logical words
-    // every thread runs the same number of rounds, so that (INT4) the group
-    // sums can be reduced over the group's consecutive lanes
     for (int i0 = 0; i0 < nxw + XP; i0 += W * 32) {
         const int i = i0 + threadIdx.x;
         uint4 v = make_uint4(0, 0, 0, 0);
@@ -556,17 +550,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
             const int pw = (ZF && i < nxw) ? (wi >> 5) * 40 + ((wi & 31) >> 3) * 10 + (wi & 7) : wi;
             xs[(size_t)m * L.xwords + pw] = v;
         }
-        if (ZF) {
-            // sum of the group's x (the pair permutation stays inside a word)
-            float t = ((bf16lo_to_f32(v.x) + bf16hi_to_f32(v.x)) + (bf16lo_to_f32(v.y) + bf16hi_to_f32(v.y))) +
-                      ((bf16lo_to_f32(v.z) + bf16hi_to_f32(v.z)) + (bf16lo_to_f32(v.w) + bf16hi_to_f32(v.w)));
-#pragma unroll
-            for (int o = 1; o < GW; o <<= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
-            if (i < nxw && (i & (GW - 1)) == 0) xsum[i / GW] = t;  // a batch row's words: a multiple of GW
-        }
     }
-    if (ZF)
-        for (int i = threadIdx.x; i < ngx; i += W * 32) xsum[mb * ngx + i] = 0.f;
     __syncthreads();
 
     // B fragment of this lane: column n = g
@@ -591,11 +575,6 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
                              : xs + (size_t)mb * L.xwords + (ZF ? 1 : 0);
     const int xstep = xon ? XP : 0;
     const uint4* xp = xbase;
-    // INT4: x sums of the groups of this lane's two accumulator columns (AWQ: groups 0, 1 of batch q;
-    // group-64: groups 2(q&1), 2(q&1)+1 of batch q>>1), one super-block at a time
-    const int zm = (FMT == FMT_AWQ) ? min(q, mb) : min(q >> 1, mb);
-    const int xgbase = zm * ngx + (b0 - cb0) * (BK / (GW * 8)) + ((FMT == FMT_G64) ? 2 * (q & 1) : 0);
-    int xg = xgbase;
     float* red = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.red_off);
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -645,10 +624,15 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
                             mma_bf16_16816(acc, p0, p1, p2, p3, xv.x, xv.y);
                     }
                 } else {
-                    // the MMAs take each code as the bf16 value 128 + n (exact), so column j of row r
-                    // sums (128 + n) x over group j, and the zero point comes off once per group:
-                    // sum (n - z) x = D - (128 + z) X_j, X_j the group's x sum. Zero points of rows g,
-                    // g+8: AWQ bytes zb bits 0-7, 8-15, group 0 in the low nibble; group-64: z = 8.
+                    // codes n -> bf16 128 + n (exact), minus the bf16 128 + z (exact): n - z enters the MMA
+                    uint32_t zz0, zz1;
+                    if (FMT == FMT_G64) {
+                        zz0 = zz1 = 0x43084308u;
+                    } else {
+                        const uint32_t sh = (q >> 1) * 4;  // this lane's group: low or high nibble
+                        zz0 = (0x4300u | ((zb >> sh) & 0xF)) * 0x00010001u;
+                        zz1 = (0x4300u | ((zb >> (8 + sh)) & 0xF)) * 0x00010001u;
+                    }
                     float d0[4] = {0.f, 0.f, 0.f, 0.f};
                     float d1[4] = {0.f, 0.f, 0.f, 0.f};
                     const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
@@ -656,28 +640,20 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
 #pragma unroll
                     for (int w = 0; w < 8; ++w) {
                         const uint4 xv = xp[w];
-                        mma_bf16_16816(d0, nib_pair(wa[w]), nib_pair(wb[w]), nib_pair(wa[w] >> 4),
-                                       nib_pair(wb[w] >> 4), xv.x, xv.y);
-                        mma_bf16_16816(d1, nib_pair(wa[w] >> 8), nib_pair(wb[w] >> 8), nib_pair(wa[w] >> 12),
-                                       nib_pair(wb[w] >> 12), xv.z, xv.w);
+                        mma_bf16_16816(d0, bf16x2_sub(nib_pair(wa[w]), zz0), bf16x2_sub(nib_pair(wb[w]), zz1),
+                                       bf16x2_sub(nib_pair(wa[w] >> 4), zz0), bf16x2_sub(nib_pair(wb[w] >> 4), zz1),
+                                       xv.x, xv.y);
+                        mma_bf16_16816(d1, bf16x2_sub(nib_pair(wa[w] >> 8), zz0), bf16x2_sub(nib_pair(wb[w] >> 8), zz1),
+                                       bf16x2_sub(nib_pair(wa[w] >> 12), zz0),
+                                       bf16x2_sub(nib_pair(wb[w] >> 12), zz1), xv.z, xv.w);
                     }
                     const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&s0));
                     const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&s1));
-                    const float2 X = *reinterpret_cast<const float2*>(xsum + xg);
-                    float zg0, zg1, zh0, zh1;  // 128 + z of rows g and g+8 for the lane's two columns
-                    if (FMT == FMT_G64) {
-                        zg0 = zg1 = zh0 = zh1 = 136.f;
-                    } else {
-                        zg0 = __uint_as_float(0x43000000u | ((zb << 16) & 0x000F0000u));
-                        zg1 = __uint_as_float(0x43000000u | ((zb << 12) & 0x000F0000u));
-                        zh0 = __uint_as_float(0x43000000u | ((zb << 8) & 0x000F0000u));
-                        zh1 = __uint_as_float(0x43000000u | ((zb << 4) & 0x000F0000u));
-                    }
-                    acc[0] = fmaf(f0.x, fmaf(-zg0, X.x, d0[0] + d1[0]), acc[0]);
-                    acc[0] = fmaf(f0.y, fmaf(-zg1, X.y, d0[1] + d1[1]), acc[0]);
-                    acc[2] = fmaf(f1.x, fmaf(-zh0, X.x, d0[2] + d1[2]), acc[2]);
-                    acc[2] = fmaf(f1.y, fmaf(-zh1, X.y, d0[3] + d1[3]), acc[2]);
-                    xg += BK / (GW * 8);
+                    // columns 2q, 2q+1: AWQ groups 0, 1 of batch q; group-64 groups 2(q&1), 2(q&1)+1 of batch q>>1
+                    acc[0] = fmaf(f0.x, d0[0] + d1[0], acc[0]);
+                    acc[0] = fmaf(f0.y, d0[1] + d1[1], acc[0]);
+                    acc[2] = fmaf(f1.x, d0[2] + d1[2], acc[2]);
+                    acc[2] = fmaf(f1.y, d0[3] + d1[3], acc[2]);
                 }
                 if (ASYNC) {
                     __syncwarp();  // every lane has read slot u before it is refilled
@@ -718,7 +694,6 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
                     cb = 0;
                     ++ct;
                     xp = xbase;
-                    xg = xgbase;
                 }
             }
         }
@@ -853,10 +828,7 @@ int mma2_block_k(int fmt) { return fmt == FMT_BF16 ? 64 : fmt == FMT_I8 ? 128 : 
 size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu) {
     const int G = mma_row_groups(N, split, occ);
     const MmaSmem L = mma_smem_layout(mma2_block_k(fmt), K, (int)N, M, c.warps, split, G, glu);
-    // + INT8 row scales, or the INT4 per-group x sums ([M + 1] rows of xwords / words-per-group)
-    const size_t base = L.total + (fmt == FMT_I8     ? (size_t)L.ntmax * 16 * 4
-                                   : fmt == FMT_BF16 ? 0
-                                                     : (size_t)(M + 1) * (L.xwords / 40 * 32 / (fmt == FMT_AWQ ? 16 : 8)) * 4);
+    const size_t base = L.total + (fmt == FMT_I8 ? (size_t)L.ntmax * 16 * 4 : 0);  // + INT8 row scales
     if (!c.async) return base;
     return (base + 127) / 128 * 128 + (size_t)c.warps * c.u * 4 * 512;
 }

@@ -691,9 +691,8 @@ cudaError_t launch_gemv_rows(const Plan& p, const GemvArgs& a, cudaStream_t s) {
 // ------------------------------------------------ bulk-fed INT4 GEMV ----
 // INT4 codes (group-64, or AWQ-style group-128 with zero points) at batch
 // 1 .. 4, with the arithmetic of the "mma2" kernels (gemv_mma.cu: each lane
-// takes 32 bytes of rows g and g+8 per 128-byte super-block, codes enter the
-// MMA as the exact bf16 values 128 + n, the zero point comes off once per group
-// against the group's x sum), but fed like the row stream above: one producer
+// takes 32 bytes of rows g and g+8 per 128-byte super-block; n - z enters the
+// MMA exactly as a bf16 pair), but fed like the row stream above: one producer
 // lane copies, per stage, the 16 rows of a tile over a chunk of the CTA's
 // k-range, one cp.async.bulk per row, into a ring of D stages shared by the W
 // consumer warps. A register ring holds a few KB per warp; this ring holds up
@@ -718,9 +717,8 @@ struct Q4bSmem {
     int KR;         // super-blocks per cluster rank
     int rowstride;  // bytes between rows of a stage
     int xwords;     // 16-byte x words per batch row (the rank's k-range), as laid out: 40 per super-block
-    int ngx;        // quantization groups per batch row
     int ntmax;      // most tiles any CTA owns
-    size_t stage_bytes, x_off, xsum_off, red_off, bar_off, total;
+    size_t stage_bytes, x_off, red_off, bar_off, total;
 };
 
 __host__ __device__ inline Q4bSmem q4b_smem_layout(int fmt, int64_t K, int64_t N, int M, int W, int D, int BSC, int S,
@@ -731,14 +729,12 @@ __host__ __device__ inline Q4bSmem q4b_smem_layout(int fmt, int64_t K, int64_t N
     L.rowstride = W * BSC * 128 + 16;
     L.stage_bytes = (size_t)16 * L.rowstride;
     L.xwords = L.KR * 40;
-    L.ngx = L.KR * 32 / (fmt == FMT_AWQ ? 16 : 8);
     const int T = (int)((N + 15) / 16);
     L.ntmax = (T + G - 1) / G;
     L.x_off = (size_t)D * L.stage_bytes;
     const size_t x_bytes = ((size_t)M * L.xwords + 40) * 16;  // + one super-block of zero words
     const size_t fin_bytes = (size_t)L.ntmax * 16 * M * 4;    // the per-row sums, over x after the stream
-    L.xsum_off = L.x_off + ((x_bytes > fin_bytes ? x_bytes : fin_bytes) + 15) / 16 * 16;
-    L.red_off = L.xsum_off + ((size_t)(M + 1) * L.ngx * 4 + 15) / 16 * 16;
+    L.red_off = L.x_off + ((x_bytes > fin_bytes ? x_bytes : fin_bytes) + 15) / 16 * 16;
     L.bar_off = (L.red_off + (size_t)L.ntmax * W * 16 * M * 4 + 7) / 8 * 8;
     L.total = L.bar_off + (size_t)2 * D * 8;
     return L;
@@ -746,10 +742,8 @@ __host__ __device__ inline Q4bSmem q4b_smem_layout(int fmt, int64_t K, int64_t N
 
 template <int FMT, int W, int D, int BSC>
 __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArgs a, const int S) {
-    constexpr int XW = 32;                         // 16-byte x words per 256-k super-block
-    constexpr int GW = (FMT == FMT_AWQ) ? 16 : 8;  // x words per quantization group
-    constexpr int GPB = 32 / GW;                   // groups per super-block
-    constexpr int KC = W * BSC;                    // super-blocks per stage
+    constexpr int XW = 32;       // 16-byte x words per 256-k super-block
+    constexpr int KC = W * BSC;  // super-blocks per stage
     extern __shared__ __align__(128) uint8_t smem[];
 
     pdl_launch_dependents();
@@ -817,7 +811,6 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
         // ------------------------------------------------------- consumers ----
         pdl_wait();
         uint4* xs = reinterpret_cast<uint4*>(smem + L.x_off);
-        float* xsum = reinterpret_cast<float*>(smem + L.xsum_off);
         const int cwords = krb * XW;
         const int lxw = L.KR * XW;  // logical x words per batch row
         const int nxw = mb * lxw;
@@ -835,14 +828,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
                 const int pw = (i < nxw) ? (wi >> 5) * 40 + ((wi & 31) >> 3) * 10 + (wi & 7) : wi;
                 xs[(size_t)m * L.xwords + pw] = v;
             }
-            // the group's x sum (the pair permutation stays inside a word)
-            float t = ((bf16lo_to_f32(v.x) + bf16hi_to_f32(v.x)) + (bf16lo_to_f32(v.y) + bf16hi_to_f32(v.y))) +
-                      ((bf16lo_to_f32(v.z) + bf16hi_to_f32(v.z)) + (bf16lo_to_f32(v.w) + bf16hi_to_f32(v.w)));
-#pragma unroll
-            for (int o = 1; o < GW; o <<= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
-            if (i < nxw && (i & (GW - 1)) == 0) xsum[i / GW] = t;
         }
-        for (int i = threadIdx.x; i < L.ngx; i += W * 32) xsum[mb * L.ngx + i] = 0.f;
         asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
 
         // B fragment of this lane (column n = g): group-64 n = 4m + j, AWQ n = 2m + j
@@ -857,10 +843,6 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
         }
         const uint4* xrow = xon ? xs + (size_t)xm * L.xwords + 10 * q : xs + (size_t)mb * L.xwords + 1;
         const int xstep = xon ? 40 : 0;
-        // x sums of this lane's two accumulator columns (AWQ: groups 0, 1 of batch q;
-        // group-64: groups 2(q&1), 2(q&1)+1 of batch q>>1)
-        const int zm = (FMT == FMT_AWQ) ? min(q, mb) : min(q >> 1, mb);
-        const float* xgrow = xsum + (size_t)zm * L.ngx + ((FMT == FMT_G64) ? 2 * (q & 1) : 0);
         float* red = reinterpret_cast<float*>(smem + L.red_off);
         const uint16_t* sc = a.scales;
 
@@ -924,6 +906,16 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
                         const uint4 c0 = *reinterpret_cast<const uint4*>(p + 8 * L.rowstride);
                         const uint4 c1 = *reinterpret_cast<const uint4*>(p + 8 * L.rowstride + 16);
                         const uint4* xp = xrow + (size_t)(cb + j) * xstep;
+                        // n - z as exact bf16 pairs (128 + n minus 128 + z; AWQ: this lane's group
+                        // is q >> 1, low or high nibble of the zero byte; group-64: z = 8)
+                        uint32_t zz0, zz1;
+                        if (FMT == FMT_G64) {
+                            zz0 = zz1 = 0x43084308u;
+                        } else {
+                            const uint32_t sh = (q >> 1) * 4;
+                            zz0 = (0x4300u | ((zb[j] >> sh) & 0xF)) * 0x00010001u;
+                            zz1 = (0x4300u | ((zb[j] >> (8 + sh)) & 0xF)) * 0x00010001u;
+                        }
                         // four accumulator sets: chains of 4 dependent MMAs instead of 8
                         float d0[4] = {0.f, 0.f, 0.f, 0.f};
                         float d1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -934,13 +926,14 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
 #pragma unroll
                         for (int w = 0; w < 8; w += 2) {
                             const uint4 xv = xp[w], xu = xp[w + 1];
-                            mma_16816(d0, nibs(wa[w]), nibs(wb[w]), nibs(wa[w] >> 4), nibs(wb[w] >> 4), xv.x, xv.y);
-                            mma_16816(d1, nibs(wa[w] >> 8), nibs(wb[w] >> 8), nibs(wa[w] >> 12), nibs(wb[w] >> 12),
-                                      xv.z, xv.w);
-                            mma_16816(e0, nibs(wa[w + 1]), nibs(wb[w + 1]), nibs(wa[w + 1] >> 4), nibs(wb[w + 1] >> 4),
-                                      xu.x, xu.y);
-                            mma_16816(e1, nibs(wa[w + 1] >> 8), nibs(wb[w + 1] >> 8), nibs(wa[w + 1] >> 12),
-                                      nibs(wb[w + 1] >> 12), xu.z, xu.w);
+                            mma_16816(d0, bsub(nibs(wa[w]), zz0), bsub(nibs(wb[w]), zz1), bsub(nibs(wa[w] >> 4), zz0),
+                                      bsub(nibs(wb[w] >> 4), zz1), xv.x, xv.y);
+                            mma_16816(d1, bsub(nibs(wa[w] >> 8), zz0), bsub(nibs(wb[w] >> 8), zz1),
+                                      bsub(nibs(wa[w] >> 12), zz0), bsub(nibs(wb[w] >> 12), zz1), xv.z, xv.w);
+                            mma_16816(e0, bsub(nibs(wa[w + 1]), zz0), bsub(nibs(wb[w + 1]), zz1),
+                                      bsub(nibs(wa[w + 1] >> 4), zz0), bsub(nibs(wb[w + 1] >> 4), zz1), xu.x, xu.y);
+                            mma_16816(e1, bsub(nibs(wa[w + 1] >> 8), zz0), bsub(nibs(wb[w + 1] >> 8), zz1),
+                                      bsub(nibs(wa[w + 1] >> 12), zz0), bsub(nibs(wb[w + 1] >> 12), zz1), xu.z, xu.w);
                         }
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -949,20 +942,10 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
                         }
                         const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&s0[j]));
                         const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&s1[j]));
-                        const float2 X = *reinterpret_cast<const float2*>(xgrow + (size_t)(cb + j) * GPB);
-                        float zg0, zg1, zh0, zh1;  // 128 + z of rows g and g+8 for the lane's two columns
-                        if (FMT == FMT_G64) {
-                            zg0 = zg1 = zh0 = zh1 = 136.f;
-                        } else {
-                            zg0 = __uint_as_float(0x43000000u | ((zb[j] << 16) & 0x000F0000u));
-                            zg1 = __uint_as_float(0x43000000u | ((zb[j] << 12) & 0x000F0000u));
-                            zh0 = __uint_as_float(0x43000000u | ((zb[j] << 8) & 0x000F0000u));
-                            zh1 = __uint_as_float(0x43000000u | ((zb[j] << 4) & 0x000F0000u));
-                        }
-                        acc0 = fmaf(f0.x, fmaf(-zg0, X.x, d0[0] + d1[0]), acc0);
-                        acc0 = fmaf(f0.y, fmaf(-zg1, X.y, d0[1] + d1[1]), acc0);
-                        acc2 = fmaf(f1.x, fmaf(-zh0, X.x, d0[2] + d1[2]), acc2);
-                        acc2 = fmaf(f1.y, fmaf(-zh1, X.y, d0[3] + d1[3]), acc2);
+                        acc0 = fmaf(f0.x, d0[0] + d1[0], acc0);
+                        acc0 = fmaf(f0.y, d0[1] + d1[1], acc0);
+                        acc2 = fmaf(f1.x, d0[2] + d1[2], acc2);
+                        acc2 = fmaf(f1.y, d0[3] + d1[3], acc2);
                     }
                 }
                 __syncwarp();  // every lane has read the stage

@@ -164,13 +164,30 @@ def test_power_of_two_scaling_and_determinism():
 
 
 def test_zero_weights_give_exact_zero():
+    """Codes equal to the zero point are zero weights: every plan returns an
+    exact zero (n - z enters the products exactly, so nothing is left over
+    from cancellation)."""
     N, K = 513, 2048
     codes = torch.full((N, K // 2), 0x88, dtype=torch.uint8, device="cuda")  # q = 8 -> w = 0
     scales = torch.full((N, K // 64), 1.0, dtype=torch.float16, device="cuda")
     x = dev_bf16(gen.bf16_activations(7, 0, 1, K)[0])
-    with mbw.output_fp32():
-        y = mbw.gemv_int4_g64(codes, scales, x)
-    assert torch.count_nonzero(y).item() == 0
+    for _, desc in each_plan(mbw.OP_GEMV_INT4_G64, 1, N, K):
+        with mbw.output_fp32():
+            y = mbw.gemv_int4_g64(codes, scales, x)
+        assert torch.count_nonzero(y).item() == 0, desc
+    # AWQ: every code equal to its group's zero point (5), canonical and repacked codes
+    G = K // 128
+    codes = torch.full((N, K // 2), 0x55, dtype=torch.uint8, device="cuda")
+    zeros = torch.full((N, (G + 1) // 2), 0x55, dtype=torch.uint8, device="cuda")
+    scales = torch.full((N, G), 3.0, dtype=torch.float16, device="cuda")
+    for M in (1, 4, 16):
+        X = dev_bf16(gen.bf16_activations(8, 0, M, K))
+        for rp in (False, True):
+            op = mbw.OP_GEMV_INT4_AWQ_G128 | (mbw.REPACKED if rp else 0)
+            for _, desc in each_plan(op, M, N, K):
+                with mbw.output_fp32():
+                    y = mbw.gemv_int4_awq_g128(codes, scales, zeros, X, repacked=rp)
+                assert torch.count_nonzero(y).item() == 0, desc
 
 
 def test_edge_cases_and_canaries(orc):
