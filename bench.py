@@ -50,20 +50,11 @@ FALLBACK_BF16_TFLOPS = 1752.2  # the pool's measured sustained cuBLAS bf16, reco
 # ncu capture, keyed by (kernel source sha, shape); a changed kernel gets
 # traffic = null until it is captured again.
 TRAFFIC = {
-    # gemv_lat on the fused gate_up matrices (INT4 g64, 11264x2048): ncu --set full,
-    # 1 launch, dram__bytes_read.sum 12,316,160 + dram__bytes_write.sum 0
-    # (profiles/gemv_lat_int4_g64_11264x2048.md)
-    ("a49c5dc3ed8058bf", "11264x2048"): 12316160,
-    # gemv_mma2 on the fused gate_up matrices (symmetric INT8, 19456x2560): ncu --set full,
-    # 1 launch, dram__bytes_read.sum 49,946,368 + dram__bytes_write.sum 768
-    # (profiles/gemv_mma2_int8_19456x2560.md)
-    ("48716c9f658135ec", "19456x2560"): 49947136,
-    # the Qwen2.5-7B gate/up matrices (BF16, 18944x3584), the default step's dominant kernel, on either of the
-    # two plans the tuner picks there: gemv_simt (4 warps, 4 rows per warp) dram__bytes_read.sum 135,820,032 +
-    # dram__bytes_write.sum 2,951,680; gemv_mma2 (8 warps, 2 super-blocks in registers) 135,848,192 + 2,951,936
-    # (profiles/gemv_simt_bf16_18944x3584.md)
-    ("ed306bd65499f91f", "18944x3584"): 138771712,
-    ("48716c9f658135ec", "18944x3584"): 138800128,
+    # the Qwen2.5-7B gate/up matrices (BF16, 18944x3584), the default step's dominant kernel: gemv_rows
+    # (8 warps, 2 stages of 4 KB per warp, 2 CTAs per SM), ncu --set full, 1 launch, dram__bytes_read.sum
+    # 135,836,160 + dram__bytes_write.sum 3,280,128 (profiles/gemv_rows_bf16_18944x3584.md); the tuner's
+    # other row-stream instantiations on this shape stream the same rows through the same code
+    ("b447707bd52159b6", "18944x3584"): 139116288,
 }
 
 
