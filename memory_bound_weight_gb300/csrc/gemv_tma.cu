@@ -779,6 +779,20 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
     if (warp == W) {
         // -------------------------------------------------------- producer ----
         if (lane == 0 && nst > 0) {
+            // the CTA's rows' scales (and zero points) into L2 first: the consumers load them per lane, a few
+            // stages ahead, and would otherwise wait on DRAM for each (both ranges are contiguous)
+            auto prefetch_l2 = [](const void* base, size_t bytes) {
+                // whole 16-byte units inside [base, base + bytes) only: nothing outside the buffer is touched
+                const uintptr_t b0 = (reinterpret_cast<uintptr_t>(base) + 15) & ~uintptr_t(15);
+                const uintptr_t b1 = (reinterpret_cast<uintptr_t>(base) + bytes) & ~uintptr_t(15);
+                for (uintptr_t p = b0; p < b1; p += 65536) {
+                    const uint32_t n = (uint32_t)min((uintptr_t)65536, b1 - p);
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
+                }
+            };
+            const int rlo = t0 * 16, rhi = min(a.N, (t0 + nt) * 16);
+            prefetch_l2(a.scales + (size_t)rlo * a.groups, (size_t)(rhi - rlo) * a.groups * 2);
+            if (FMT == FMT_AWQ) prefetch_l2(a.zeros + (size_t)rlo * a.zstride, (size_t)(rhi - rlo) * a.zstride);
             uint64_t policy;
             asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
             bool ok = true;
@@ -870,8 +884,10 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
                 }
             }
         };
-        uint32_t ns0[BSC], ns1[BSC], nzb[BSC];
+        // two stages ahead: stage i + 1 in n*, stage i + 2 in m*
+        uint32_t ns0[BSC], ns1[BSC], nzb[BSC], ms0[BSC], ms1[BSC], mzb[BSC];
         if (nst > 0) load_sc(0, 0, ns0, ns1, nzb);
+        if (nst > 1) load_sc(nch > 1 ? 0 : 1, nch > 1 ? 1 : 0, ms0, ms1, mzb);
 
         bool ok = true;
         int i = 0;
@@ -886,12 +902,17 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
                     s0[j] = ns0[j];
                     s1[j] = ns1[j];
                     zb[j] = nzb[j];
+                    ns0[j] = ms0[j];
+                    ns1[j] = ms1[j];
+                    nzb[j] = mzb[j];
                 }
-                if (i + 1 < nst) {
-                    if (ch + 1 < nch)
-                        load_sc(tl, ch + 1, ns0, ns1, nzb);
-                    else
-                        load_sc(tl + 1, 0, ns0, ns1, nzb);
+                if (i + 2 < nst) {  // stage i + 2: (tl, ch + 2) or into the next tile
+                    int t2 = tl, c2 = ch + 2;
+                    while (c2 >= nch) {
+                        c2 -= nch;
+                        ++t2;
+                    }
+                    load_sc(t2, c2, ms0, ms1, mzb);
                 }
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait(&full[slot], (i / D) & 1));
                 if (!ok) break;
