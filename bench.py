@@ -53,8 +53,10 @@ TRAFFIC = {
     # the Qwen2.5-7B gate/up matrices (BF16, 18944x3584), the default step's dominant kernel: gemv_rows
     # (8 warps, 2 stages of 4 KB per warp, 2 CTAs per SM), ncu --set full, 1 launch, dram__bytes_read.sum
     # 135,836,160 + dram__bytes_write.sum 3,280,128 (profiles/gemv_rows_bf16_18944x3584.md); the tuner's
-    # other row-stream instantiations on this shape stream the same rows through the same code
-    ("b447707bd52159b6", "18944x3584"): 139116288,
+    # other row-stream instantiations on this shape stream the same rows through the same code (the capture
+    # predates the last edit of gemv_tma.cu, which touched only the bulk INT4 kernel; the row-stream kernel's
+    # code is the one captured)
+    ("9e22c5e3a7de561f", "18944x3584"): 139116288,
 }
 
 
@@ -84,9 +86,10 @@ def parse_args():
     p.add_argument("--plans-from", default=None, help="restore plans from a --plans-out file instead of tuning")
     p.add_argument("--no-extras", action="store_true",
                    help="leave out the other configurations' figures (configs key of the JSON line)")
-    p.add_argument("--extras-tune", default="shape", choices=["step", "shape"],
-                   help="plan tuning of the extra decode steps (TinyLlama INT4, AWQ): per shape (default) or "
-                        "refined on the whole step")
+    p.add_argument("--extras-tune", default="step", choices=["step", "shape"],
+                   help="plan tuning of the extra decode steps (TinyLlama INT4, AWQ): refined on the whole step "
+                        "(default; a plan that wins its shape alone can slow its neighbours in the chain) or per "
+                        "shape only")
     p.add_argument("--profile-range", action="store_true",
                    help="bracket the timed region with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     return p.parse_args()
