@@ -107,13 +107,16 @@ struct MmaSmem {
     size_t x_bytes, red_off, red_bytes, total;
 };
 
-__host__ __device__ inline MmaSmem mma_smem_layout(int BK, int64_t K, int N, int M, int W, int S, int G, int glu = 0) {
+// xpad: x words per block as laid out (0: BK / 8, packed). The "mma2" INT4 and
+// INT8 kernels pad: each lane quarter's words start at word 10 q (INT4, 8 words
+// per quarter) or 5 q (INT8, 4 words), so that the four quarters' lanes reading
+// their word w hit four different bank groups.
+__host__ __device__ inline MmaSmem mma_smem_layout(int BK, int64_t K, int N, int M, int W, int S, int G, int glu = 0,
+                                                   int xpad = 0) {
     MmaSmem L;
     const int64_t KB = (K + BK - 1) / BK;
     const int64_t BS = (KB + (int64_t)S * W - 1) / ((int64_t)S * W);
-    // 256-k super-blocks (INT4, "mma2"): the four 8-word quarters at word 10 q, so
-    // that the four quarters' lanes reading word w hit four different bank groups
-    const int xpb = (BK == 256) ? 40 : BK / 8;
+    const int xpb = xpad ? xpad : BK / 8;
     L.xwords = (int)(W * BS * xpb);
     const int T = (N + 15) / 16;
     L.ntmax = (T + G - 1) / G * (glu ? 2 : 1);  // logical tiles (gate/up pairs under the gated epilogue)
@@ -409,7 +412,8 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     int t0, nt;  // the CTA's logical tiles (gate/up pairs under the gated epilogue)
     cta_tile_range<FZ>(a, G, cgid, t0, nt);
     const int mb = a.M;
-    const MmaSmem L = mma_smem_layout(BK, a.K, a.N, mb, W, S, G, gated<FZ>(a) ? 1 : 0);
+    constexpr int XPAD = (FMT == FMT_G64 || FMT == FMT_AWQ) ? 40 : (FMT == FMT_I8) ? 20 : 0;
+    const MmaSmem L = mma_smem_layout(BK, a.K, a.N, mb, W, S, G, gated<FZ>(a) ? 1 : 0, XPAD);
 
     const int KB = a.K / BK;  // the plan guarantees K % BK == 0
     const int BS = (KB + S * W - 1) / (S * W);
@@ -463,8 +467,8 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     // sector-complete copies).
     // INT8: the fp32 scales of the CTA's rows, read before the wait (they are weights)
     float* rsc = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.total);
-    constexpr bool ZF = (FMT == FMT_G64 || FMT == FMT_AWQ);  // INT4: padded x super-blocks
-    constexpr int XP = ZF ? 40 : XW;                          // physical x words per super-block
+    constexpr bool ZF = (FMT == FMT_G64 || FMT == FMT_AWQ);  // INT4
+    constexpr int XP = XPAD ? XPAD : XW;                      // physical x words per super-block
     const int lxw = L.xwords / XP * XW;                       // logical x words per batch row
     const size_t sc_bytes = (FMT == FMT_I8) ? (size_t)L.ntmax * 16 * 4 : 0;
     uint8_t* abase = reinterpret_cast<uint8_t*>(smem_u4) + (L.total + sc_bytes + 127) / 128 * 128 +
@@ -545,9 +549,12 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
                 v = perm_pairs(v);
         }
         if (i < nxw + XP) {
-            // INT4: logical word 32 b + 8 q + w of a batch row sits at 40 b + 10 q + w
-            // (the zero block, m = mb, is written as it is: XP zero words)
-            const int pw = (ZF && i < nxw) ? (wi >> 5) * 40 + ((wi & 31) >> 3) * 10 + (wi & 7) : wi;
+            // logical word 32 b + 8 q + w of a batch row sits at 40 b + 10 q + w (INT4), word
+            // 16 b + 4 q + w at 20 b + 5 q + w (INT8); the zero block (m = mb) is written as it is
+            const int pw = (i >= nxw) ? wi
+                           : ZF       ? (wi >> 5) * 40 + ((wi & 31) >> 3) * 10 + (wi & 7)
+                           : (FMT == FMT_I8) ? (wi >> 4) * 20 + ((wi & 15) >> 2) * 5 + (wi & 3)
+                                             : wi;
             xs[(size_t)m * L.xwords + pw] = v;
         }
     }
@@ -568,11 +575,11 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     }
     // lane's x words of a super-block: INT4 words 8q .. 8q+7, INT8 4q .. 4q+3, BF16 2q, 2q+1
     const int xoff = (FMT == FMT_BF16) ? 2 * q : (FMT == FMT_I8) ? 4 * q : 8 * q;
-    // (INT4: the quarter at 10 q; the lanes without a column read zero words 1 .. 8,
-    // a bank group apart from the quarters' reads)
-    const int xq = ZF ? 10 * q : xoff;
+    // (INT4: the quarter at 10 q, INT8 at 5 q; the lanes without a column read zero
+    // words from 1 on, a bank group apart from the quarters' reads)
+    const int xq = ZF ? 10 * q : (FMT == FMT_I8) ? 5 * q : xoff;
     const uint4* xbase = xon ? xs + (size_t)xm * L.xwords + (size_t)(b0 - cb0) * XP + xq
-                             : xs + (size_t)mb * L.xwords + (ZF ? 1 : 0);
+                             : xs + (size_t)mb * L.xwords + (XPAD ? 1 : 0);
     const int xstep = xon ? XP : 0;
     const uint4* xp = xbase;
     float* red = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.red_off);
@@ -827,7 +834,8 @@ int mma2_block_k(int fmt) { return fmt == FMT_BF16 ? 64 : fmt == FMT_I8 ? 128 : 
 
 size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu) {
     const int G = mma_row_groups(N, split, occ);
-    const MmaSmem L = mma_smem_layout(mma2_block_k(fmt), K, (int)N, M, c.warps, split, G, glu);
+    const int xpad = (fmt == FMT_G64 || fmt == FMT_AWQ) ? 40 : (fmt == FMT_I8) ? 20 : 0;
+    const MmaSmem L = mma_smem_layout(mma2_block_k(fmt), K, (int)N, M, c.warps, split, G, glu, xpad);
     const size_t base = L.total + (fmt == FMT_I8 ? (size_t)L.ntmax * 16 * 4 : 0);  // + INT8 row scales
     if (!c.async) return base;
     return (base + 127) / 128 * 128 + (size_t)c.warps * c.u * 4 * 512;
