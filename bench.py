@@ -57,6 +57,15 @@ TRAFFIC = {
     # predates the last edit of gemv_tma.cu, which touched only the bulk INT4 kernel; the row-stream kernel's
     # code is the one captured)
     ("9e22c5e3a7de561f", "18944x3584"): 139116288,
+    # the TinyLlama INT4 step's dominant kernel: gemv_lat on the fused gate_up matrices (INT4 g64, 11264x2048),
+    # dram__bytes_read.sum 12,315,392 + dram__bytes_write.sum 0 (profiles/gemv_lat_int4_g64_11264x2048.md)
+    ("cf3bf3b20ec9aac8", "11264x2048"): 12315392,
+    # the qwen3_int8 step's dominant kernel: gemv_mma2 on the fused gate_up matrices (INT8, 19456x2560),
+    # 49,947,648 + 2,048 (profiles/gemv_mma2_int8_19456x2560.md)
+    ("ae20d984bdd059ad", "19456x2560"): 49949696,
+    # the AWQ batch-1 step's dominant kernel: gemv_mma2 on 18944x3584 (AWQ, repacked codes), 35,340,800 + 0
+    # (profiles/gemv_mma2_awq_g128_18944x3584_m1.md)
+    ("ae20d984bdd059ad", "18944x3584"): 35340800,
 }
 
 
