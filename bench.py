@@ -52,19 +52,19 @@ FALLBACK_BF16_TFLOPS = 1752.2  # the pool's measured sustained cuBLAS bf16, reco
 TRAFFIC = {
     # the Qwen2.5-7B gate/up matrices (BF16, 18944x3584), the default step's dominant kernel: gemv_rows
     # (8 warps, 2 stages of 4 KB per warp, 2 CTAs per SM), ncu --set full, 1 launch, dram__bytes_read.sum
-    # 135,836,160 + dram__bytes_write.sum 3,280,128 (profiles/gemv_rows_bf16_18944x3584.md); the tuner's
+    # 135,836,160 + dram__bytes_write.sum 3,280,128 (its ncu summary under profiles/); the tuner's
     # other row-stream instantiations on this shape stream the same rows through the same code (the capture
-    # predates the last edit of gemv_tma.cu, which touched only the bulk INT4 kernel; the row-stream kernel's
-    # code is the one captured)
-    ("9e22c5e3a7de561f", "18944x3584"): 139116288,
+    # predates the last edits of gemv_tma.cu, which touched the bulk INT4 kernel and comments only; the
+    # row-stream kernel's code is the one captured)
+    ("a303e31c0276df40", "18944x3584"): 139116288,
     # the TinyLlama INT4 step's dominant kernel: gemv_lat on the fused gate_up matrices (INT4 g64, 11264x2048),
-    # dram__bytes_read.sum 12,315,392 + dram__bytes_write.sum 0 (profiles/gemv_lat_int4_g64_11264x2048.md)
+    # dram__bytes_read.sum 12,315,392 + dram__bytes_write.sum 0 (its ncu summary under profiles/)
     ("cf3bf3b20ec9aac8", "11264x2048"): 12315392,
     # the qwen3_int8 step's dominant kernel: gemv_mma2 on the fused gate_up matrices (INT8, 19456x2560),
-    # 49,947,648 + 2,048 (profiles/gemv_mma2_int8_19456x2560.md)
+    # 49,947,648 + 2,048 (its ncu summary under profiles/)
     ("ae20d984bdd059ad", "19456x2560"): 49949696,
     # the AWQ batch-1 step's dominant kernel: gemv_mma2 on 18944x3584 (AWQ, repacked codes), 35,340,800 + 0
-    # (profiles/gemv_mma2_awq_g128_18944x3584_m1.md)
+    # (its ncu summary under profiles/)
     ("ae20d984bdd059ad", "18944x3584"): 35340800,
 }
 

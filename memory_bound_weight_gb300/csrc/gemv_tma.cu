@@ -502,6 +502,9 @@ cudaError_t launch_gemv_tma(int fmt, const Plan& p, const GemvArgs& a, cudaStrea
 
 // ---------------------------------------------------------- row stream ----
 // BF16 weights at batch 1, fed by per-warp bulk-copy rings over whole rows.
+// y[i] = sum_k W[i][k] x[k], every weight read once (llm-rs vs vLLM, sec. 2:
+// single-request decode is a weight stream; the kernel's job is to keep HBM
+// busy, which on this GPU means keeping ~100 KB or more in flight per SM).
 //
 // CTA c of G owns the rows [N c / G, N (c + 1) / G); with row-major weights
 // those rows are one contiguous byte range, cut into stages of SEG bytes (the
@@ -689,6 +692,9 @@ cudaError_t launch_gemv_rows(const Plan& p, const GemvArgs& a, cudaStream_t s) {
 }
 
 // ------------------------------------------------ bulk-fed INT4 GEMV ----
+// y[m][i] = sum_g s[i][g] sum_{k in g} (q[i][k] - z[i][g]) x[m][k] (tinyinfer,
+// INT4 group-64 with z = 8; llm-rs vs vLLM sec. 6, the AWQ-style group-128
+// layout with a zero point per group).
 // INT4 codes (group-64, or AWQ-style group-128 with zero points) at batch
 // 1 .. 4, with the arithmetic of the "mma2" kernels (gemv_mma.cu: each lane
 // takes 32 bytes of rows g and g+8 per 128-byte super-block; n - z enters the
