@@ -213,7 +213,8 @@ class ClockSampler:
 KERNEL_SOURCES = {"lat": ("gemv_lat.cu", "device.cuh"), "mma2": ("gemv_mma.cu", "device.cuh"),
                   "mma": ("gemv_mma.cu", "device.cuh"), "simt": ("gemv_simt.cu", "device.cuh"),
                   "tma": ("gemv_tma.cu", "device.cuh"), "tcgen05": ("gemm_tc.cu", "device.cuh"),
-                  "awq_mma": ("gemv_awq_batch.cu", "device.cuh"), "rows": ("gemv_tma.cu", "device.cuh")}
+                  "awq_mma": ("gemv_awq_batch.cu", "device.cuh"), "rows": ("gemv_tma.cu", "device.cuh"),
+                  "bulk": ("gemv_tma.cu", "device.cuh")}
 
 
 def kernel_source_sha(family):

@@ -691,7 +691,7 @@ cudaError_t launch_gemv_rows(const Plan& p, const GemvArgs& a, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, e.fn, a, G);
 }
 
-// ------------------------------------------------ bulk-fed INT4 GEMV ----
+// -------------------------------------------- bulk-fed INT4 / INT8 GEMV ----
 // y[m][i] = sum_g s[i][g] sum_{k in g} (q[i][k] - z[i][g]) x[m][k] (tinyinfer,
 // INT4 group-64 with z = 8; llm-rs vs vLLM sec. 6, the AWQ-style group-128
 // layout with a zero point per group).
@@ -704,6 +704,12 @@ cudaError_t launch_gemv_rows(const Plan& p, const GemvArgs& a, cudaStream_t s) {
 // consumer warps. A register ring holds a few KB per warp; this ring holds up
 // to ~170 KB per SM, issued by one thread, so the consumers spend no issue
 // slots on load addresses and the stream keeps enough bytes in flight.
+//
+// INT8 (symmetric, one fp32 scale per output channel; TileInfer, "Pushing
+// further with cheating: INT8 quantization") runs through the same ring: a
+// 128-byte super-block of a row is 128 codes (128 k), a lane's 32 bytes of rows
+// g and g+8 become exact bf16 pairs (i8_pairs), column n of the MMA is batch
+// row n (up to 8), and the row's scale multiplies its finished sum in the store.
 //
 //   * stage i = (tile i / nch, chunk i % nch): rows at a stride of KC * 128 + 16
 //     bytes (rows g and g + 1 then fall in different bank groups for the
@@ -719,7 +725,7 @@ cudaError_t launch_gemv_rows(const Plan& p, const GemvArgs& a, cudaStream_t s) {
 //     bank groups; lanes without a batch column read zero words 1 .. 8);
 //   * per-tile partials are summed over warps (and cluster ranks, through
 //     distributed shared memory) once, in a fixed order.
-struct Q4bSmem {
+struct QbulkSmem {
     int KR;         // super-blocks per cluster rank
     int rowstride;  // bytes between rows of a stage
     int xwords;     // 16-byte x words per batch row (the rank's k-range), as laid out: 40 per super-block
@@ -727,18 +733,19 @@ struct Q4bSmem {
     size_t stage_bytes, x_off, red_off, bar_off, total;
 };
 
-__host__ __device__ inline Q4bSmem q4b_smem_layout(int fmt, int64_t K, int64_t N, int M, int W, int D, int BSC, int S,
+__host__ __device__ inline QbulkSmem qbulk_smem_layout(int fmt, int64_t K, int64_t N, int M, int W, int D, int BSC, int S,
                                                    int G) {
-    Q4bSmem L;
-    const int KB = (int)(K / 256);
+    QbulkSmem L;
+    const int KB = (int)(K / (fmt == FMT_I8 ? 128 : 256));  // 128-byte super-blocks per row
+    const int xp = (fmt == FMT_I8) ? 20 : 40;                // x words per super-block, as laid out
     L.KR = (KB + S - 1) / S;
     L.rowstride = W * BSC * 128 + 16;
     L.stage_bytes = (size_t)16 * L.rowstride;
-    L.xwords = L.KR * 40;
+    L.xwords = L.KR * xp;
     const int T = (int)((N + 15) / 16);
     L.ntmax = (T + G - 1) / G;
     L.x_off = (size_t)D * L.stage_bytes;
-    const size_t x_bytes = ((size_t)M * L.xwords + 40) * 16;  // + one super-block of zero words
+    const size_t x_bytes = ((size_t)M * L.xwords + xp) * 16;  // + one super-block of zero words
     const size_t fin_bytes = (size_t)L.ntmax * 16 * M * 4;    // the per-row sums, over x after the stream
     L.red_off = L.x_off + ((x_bytes > fin_bytes ? x_bytes : fin_bytes) + 15) / 16 * 16;
     L.bar_off = (L.red_off + (size_t)L.ntmax * W * 16 * M * 4 + 7) / 8 * 8;
@@ -747,9 +754,13 @@ __host__ __device__ inline Q4bSmem q4b_smem_layout(int fmt, int64_t K, int64_t N
 }
 
 template <int FMT, int W, int D, int BSC>
-__global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArgs a, const int S) {
-    constexpr int XW = 32;       // 16-byte x words per 256-k super-block
-    constexpr int KC = W * BSC;  // super-blocks per stage
+__global__ void __launch_bounds__((W + 1) * 32, 1) gemv_qbulk_kernel(const GemvArgs a, const int S) {
+    constexpr bool I8 = (FMT == FMT_I8);
+    constexpr int BK = I8 ? 128 : 256;  // k per 128-byte row super-block
+    constexpr int XW = BK / 8;          // 16-byte x words per super-block (logical)
+    constexpr int XP = I8 ? 20 : 40;    // as laid out: each lane quarter's words at QW q
+    constexpr int QW = I8 ? 5 : 10;
+    constexpr int KC = W * BSC;         // super-blocks per stage
     extern __shared__ __align__(128) uint8_t smem[];
 
     pdl_launch_dependents();
@@ -763,13 +774,13 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
     const int t0 = (int)(((long long)T * cgid) / G);
     const int nt = (int)(((long long)T * (cgid + 1)) / G) - t0;
     const int mb = a.M;
-    const Q4bSmem L = q4b_smem_layout(FMT, a.K, a.N, mb, W, D, BSC, S, G);
-    const int KB = (int)(a.K / 256);
+    const QbulkSmem L = qbulk_smem_layout(FMT, a.K, a.N, mb, W, D, BSC, S, G);
+    const int KB = (int)(a.K / BK);
     const int kb0 = rank * L.KR;                        // the rank's first super-block
     const int krb = max(0, min(KB, kb0 + L.KR) - kb0);  // and its count
     const int nch = (krb + KC - 1) / KC;                // stages per tile
     const int nst = nt * nch;
-    const size_t rowbytes = (size_t)a.K / 2;
+    const size_t rowbytes = I8 ? (size_t)a.K : (size_t)a.K / 2;
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
     uint64_t* empty = full + D;
@@ -797,7 +808,10 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
                 }
             };
             const int rlo = t0 * 16, rhi = min(a.N, (t0 + nt) * 16);
-            prefetch_l2(a.scales + (size_t)rlo * a.groups, (size_t)(rhi - rlo) * a.groups * 2);
+            if (I8)
+                prefetch_l2(a.rscale + rlo, (size_t)(rhi - rlo) * 4);
+            else
+                prefetch_l2(a.scales + (size_t)rlo * a.groups, (size_t)(rhi - rlo) * a.groups * 2);
             if (FMT == FMT_AWQ) prefetch_l2(a.zeros + (size_t)rlo * a.zstride, (size_t)(rhi - rlo) * a.zstride);
             uint64_t policy;
             asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
@@ -834,35 +848,42 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
         const int cwords = krb * XW;
         const int lxw = L.KR * XW;  // logical x words per batch row
         const int nxw = mb * lxw;
-        for (int i0 = 0; i0 < nxw + 40; i0 += W * 32) {
+        for (int i0 = 0; i0 < nxw + XP; i0 += W * 32) {
             const int i = i0 + threadIdx.x;
             uint4 v = make_uint4(0, 0, 0, 0);
             int m = mb, wi = i - nxw;  // the zero block
             if (i < nxw) {
                 m = i / lxw;
                 wi = i - m * lxw;
-                if (wi < cwords) v = ld_ro16(a.x + (size_t)m * a.K + (size_t)kb0 * 256 + (size_t)wi * 8);
-                if (!a.x_natural) v = pair_perm(v);
+                if (wi < cwords) v = ld_ro16(a.x + (size_t)m * a.K + (size_t)kb0 * BK + (size_t)wi * 8);
+                if (I8)
+                    v = perm_i8(v);
+                else if (!a.x_natural)
+                    v = pair_perm(v);
             }
-            if (i < nxw + 40) {
-                const int pw = (i < nxw) ? (wi >> 5) * 40 + ((wi & 31) >> 3) * 10 + (wi & 7) : wi;
+            if (i < nxw + XP) {
+                // logical word XW b + (XW / 4) q + w of a batch row sits at XP b + QW q + w
+                const int pw = (i < nxw) ? (wi / XW) * XP + ((wi % XW) / (XW / 4)) * QW + wi % (XW / 4) : wi;
                 xs[(size_t)m * L.xwords + pw] = v;
             }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
 
-        // B fragment of this lane (column n = g): group-64 n = 4m + j, AWQ n = 2m + j
+        // B fragment of this lane (column n = g): group-64 n = 4m + j, AWQ n = 2m + j, INT8 n = m
         int xm;
         bool xon;
         if (FMT == FMT_G64) {
             xm = g >> 2;
             xon = (xm < mb) && ((g & 3) == q);
-        } else {
+        } else if (FMT == FMT_AWQ) {
             xm = g >> 1;
             xon = (xm < mb) && ((g & 1) == (q >> 1));
+        } else {
+            xm = g;
+            xon = xm < mb;
         }
-        const uint4* xrow = xon ? xs + (size_t)xm * L.xwords + 10 * q : xs + (size_t)mb * L.xwords + 1;
-        const int xstep = xon ? 40 : 0;
+        const uint4* xrow = xon ? xs + (size_t)xm * L.xwords + QW * q : xs + (size_t)mb * L.xwords + 1;
+        const int xstep = xon ? XP : 0;
         float* red = reinterpret_cast<float*>(smem + L.red_off);
         const uint16_t* sc = a.scales;
 
@@ -874,7 +895,9 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
 #pragma unroll
             for (int j = 0; j < BSC; ++j) {
                 const int gb = kb0 + min(cb + j, krb - 1);
-                if (FMT == FMT_G64) {
+                if (I8) {
+                    s0[j] = s1[j] = zb[j] = 0;  // INT8: one scale per row, applied in the store
+                } else if (FMT == FMT_G64) {
                     const uint16_t* p0 = sc + (size_t)r0 * a.groups + (size_t)gb * 4 + 2 * (q & 1);
                     const uint16_t* p1 = sc + (size_t)r1 * a.groups + (size_t)gb * 4 + 2 * (q & 1);
                     s0[j] = (uint32_t)ld_ro_u16(p0) | ((uint32_t)ld_ro_u16(p0 + 1) << 16);
@@ -899,6 +922,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
         int i = 0;
         for (int tl = 0; tl < nt && ok; ++tl) {
             float acc0 = 0.f, acc2 = 0.f;
+            float c8[4] = {0.f, 0.f, 0.f, 0.f}, e8[4] = {0.f, 0.f, 0.f, 0.f};  // INT8: rows g, g+8 x columns 2q, 2q+1
             for (int ch = 0; ch < nch; ++ch, ++i) {
                 const int slot = i % D;
                 const int cb = ch * KC + warp * BSC;  // rank-local super-block of j = 0
@@ -933,6 +957,24 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
                         const uint4 c0 = *reinterpret_cast<const uint4*>(p + 8 * L.rowstride);
                         const uint4 c1 = *reinterpret_cast<const uint4*>(p + 8 * L.rowstride + 16);
                         const uint4* xp = xrow + (size_t)(cb + j) * xstep;
+                        if (I8) {
+                            // word w of rows g and g+8: codes (0,2) and (1,3) as exact bf16 pairs, one MMA
+                            // per word; x is in the matching pair order (perm_i8), 4 words per lane
+                            const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                            const uint32_t wb[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                            for (int w = 0; w < 8; w += 2) {
+                                const uint4 xv = xp[w >> 1];
+                                uint32_t p0, p1, p2, p3;
+                                i8_pairs(wa[w], p0, p2);
+                                i8_pairs(wb[w], p1, p3);
+                                mma_16816(c8, p0, p1, p2, p3, xv.x, xv.y);
+                                i8_pairs(wa[w + 1], p0, p2);
+                                i8_pairs(wb[w + 1], p1, p3);
+                                mma_16816(e8, p0, p1, p2, p3, xv.z, xv.w);
+                            }
+                            continue;
+                        }
                         // n - z as exact bf16 pairs (128 + n minus 128 + z; AWQ: this lane's group
                         // is q >> 1, low or high nibble of the zero byte; group-64: z = 8)
                         uint32_t zz0, zz1;
@@ -980,7 +1022,16 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
             }
             if (!ok) break;
             float* rp = red + ((size_t)(tl * W + warp) * 16) * mb;
-            if (FMT == FMT_G64) {
+            if (I8) {
+                if (2 * q < mb) {
+                    rp[g * mb + 2 * q] = c8[0] + e8[0];
+                    rp[(g + 8) * mb + 2 * q] = c8[2] + e8[2];
+                }
+                if (2 * q + 1 < mb) {
+                    rp[g * mb + 2 * q + 1] = c8[1] + e8[1];
+                    rp[(g + 8) * mb + 2 * q + 1] = c8[3] + e8[3];
+                }
+            } else if (FMT == FMT_G64) {
                 // lanes q and q^1 hold the other two groups of the same batch
                 const float v0 = acc0 + __shfl_xor_sync(0xFFFFFFFFu, acc0, 1);
                 const float v2 = acc2 + __shfl_xor_sync(0xFFFFFFFFu, acc2, 1);
@@ -1009,7 +1060,12 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
         __syncthreads();
         for (int k = threadIdx.x; k < nt * 16 * mb; k += (W + 1) * 32) {
             const int m = k / (nt * 16), o = k - m * nt * 16;
-            if (t0 * 16 + o < a.N) store_out(a.y, (int64_t)m * a.N + t0 * 16 + o, fin[o * mb + m], a.out_f32);
+            const int row = t0 * 16 + o;
+            if (row < a.N) {
+                float v = fin[o * mb + m];
+                if (I8) v *= __ldg(a.rscale + row);
+                store_out(a.y, (int64_t)m * a.N + row, v, a.out_f32);
+            }
         }
         return;
     }
@@ -1023,62 +1079,75 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_q4b_kernel(const GemvArg
         const int m = k / span, o = lo + (k - m * span);
         float v = 0.f;
         for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(fin + o * mb + m, s);
-        if (t0 * 16 + o < a.N) store_out(a.y, (int64_t)m * a.N + t0 * 16 + o, v, a.out_f32);
+        const int row = t0 * 16 + o;
+        if (row < a.N) {
+            if (I8) v *= __ldg(a.rscale + row);
+            store_out(a.y, (int64_t)m * a.N + row, v, a.out_f32);
+        }
     }
     cluster.sync();
 }
 
-struct Q4bEntry {
-    Q4bConfig cfg;
+struct QbulkEntry {
+    QbulkConfig cfg;
     TmaFn fn;
 };
 #define MBW_B(F, W, D, B) \
-    { {W, D, B}, gemv_q4b_kernel<F, W, D, B> }
-static const Q4bEntry kQ4bG64[] = {MBW_B(FMT_G64, 8, 4, 1),  MBW_B(FMT_G64, 8, 6, 1),  MBW_B(FMT_G64, 4, 6, 2),
+    { {W, D, B}, gemv_qbulk_kernel<F, W, D, B> }
+static const QbulkEntry kQbulkG64[] = {MBW_B(FMT_G64, 8, 4, 1),  MBW_B(FMT_G64, 8, 6, 1),  MBW_B(FMT_G64, 4, 6, 2),
                                    MBW_B(FMT_G64, 7, 6, 2),  MBW_B(FMT_G64, 8, 4, 2),  MBW_B(FMT_G64, 4, 4, 2),
                                    MBW_B(FMT_G64, 14, 6, 1), MBW_B(FMT_G64, 16, 5, 1), MBW_B(FMT_G64, 11, 4, 2)};
-static const Q4bEntry kQ4bAwq[] = {MBW_B(FMT_AWQ, 8, 4, 1),  MBW_B(FMT_AWQ, 8, 6, 1),  MBW_B(FMT_AWQ, 4, 6, 2),
+static const QbulkEntry kQbulkAwq[] = {MBW_B(FMT_AWQ, 8, 4, 1),  MBW_B(FMT_AWQ, 8, 6, 1),  MBW_B(FMT_AWQ, 4, 6, 2),
                                    MBW_B(FMT_AWQ, 7, 6, 2),  MBW_B(FMT_AWQ, 8, 4, 2),  MBW_B(FMT_AWQ, 4, 4, 2),
                                    MBW_B(FMT_AWQ, 14, 6, 1), MBW_B(FMT_AWQ, 16, 5, 1), MBW_B(FMT_AWQ, 11, 4, 2)};
+
+static const QbulkEntry kQbulkI8[] = {MBW_B(FMT_I8, 10, 4, 2), MBW_B(FMT_I8, 5, 6, 4),  MBW_B(FMT_I8, 8, 6, 1),
+                                    MBW_B(FMT_I8, 16, 5, 1), MBW_B(FMT_I8, 16, 3, 2), MBW_B(FMT_I8, 4, 6, 2),
+                                    MBW_B(FMT_I8, 8, 4, 2)};
 #undef MBW_B
 
-static const Q4bEntry* q4b_table(int fmt, int* n) {
+static const QbulkEntry* qbulk_table(int fmt, int* n) {
     if (fmt == FMT_G64) {
-        *n = (int)(sizeof(kQ4bG64) / sizeof(kQ4bG64[0]));
-        return kQ4bG64;
+        *n = (int)(sizeof(kQbulkG64) / sizeof(kQbulkG64[0]));
+        return kQbulkG64;
     }
     if (fmt == FMT_AWQ) {
-        *n = (int)(sizeof(kQ4bAwq) / sizeof(kQ4bAwq[0]));
-        return kQ4bAwq;
+        *n = (int)(sizeof(kQbulkAwq) / sizeof(kQbulkAwq[0]));
+        return kQbulkAwq;
+    }
+    if (fmt == FMT_I8) {
+        *n = (int)(sizeof(kQbulkI8) / sizeof(kQbulkI8[0]));
+        return kQbulkI8;
     }
     *n = 0;
     return nullptr;
 }
 
-int q4b_num_configs(int fmt) {
+int qbulk_num_configs(int fmt) {
     int n;
-    q4b_table(fmt, &n);
+    qbulk_table(fmt, &n);
     return n;
 }
 
-Q4bConfig q4b_config(int fmt, int idx) {
+QbulkConfig qbulk_config(int fmt, int idx) {
     int n;
-    return q4b_table(fmt, &n)[idx].cfg;
+    return qbulk_table(fmt, &n)[idx].cfg;
 }
 
-size_t q4b_smem_bytes(int fmt, const Q4bConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
+size_t qbulk_smem_bytes(int fmt, const QbulkConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
     const int G = mma_row_groups(N, split, occ);
-    return q4b_smem_layout(fmt, K, N, M, c.warps, c.depth, c.bsc, split, G).total;
+    return qbulk_smem_layout(fmt, K, N, M, c.warps, c.depth, c.bsc, split, G).total;
 }
 
-cudaError_t launch_gemv_q4b(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
+cudaError_t launch_gemv_qbulk(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
     int n;
-    const Q4bEntry* t = q4b_table(fmt, &n);
-    if (!t || p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > mma2_max_batch(fmt) || a.K % 256 != 0 || a.glu)
+    const QbulkEntry* t = qbulk_table(fmt, &n);
+    if (!t || p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > mma2_max_batch(fmt) || a.K % (fmt == FMT_I8 ? 128 : 256) != 0 ||
+        a.glu)
         return cudaErrorInvalidValue;
-    const Q4bEntry& e = t[p.cfg];
+    const QbulkEntry& e = t[p.cfg];
     const int G = mma_row_groups(a.N, p.split, p.occ);
-    const size_t smem = q4b_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
+    const size_t smem = qbulk_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;

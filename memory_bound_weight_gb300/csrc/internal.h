@@ -94,7 +94,7 @@ struct RowsConfig {
 
 // One instantiation of the bulk-fed INT4 kernel (gemv_tma.cu): a producer
 // lane fills a CTA ring of 16-row stages for W consumer warps.
-struct Q4bConfig {
+struct QbulkConfig {
     int warps;  // consumer warps (plus one producer warp)
     int depth;  // ring stages
     int bsc;    // super-blocks per consumer warp per stage
@@ -127,7 +127,7 @@ enum PlanKind : int {
     PLAN_LAT = 5,
     PLAN_AWQB = 6,
     PLAN_ROWS = 7,
-    PLAN_Q4B = 8,
+    PLAN_QBULK = 8,
 };
 
 // Kernel tables (gemv_simt.cu).
@@ -195,10 +195,10 @@ RowsConfig rows_config(int idx);
 int rows_ctas(int64_t N, int occ);
 size_t rows_smem_bytes(const RowsConfig& c, int64_t N, int64_t K, int occ);
 cudaError_t launch_gemv_rows(const Plan& p, const GemvArgs& a, cudaStream_t s);
-int q4b_num_configs(int fmt);
-Q4bConfig q4b_config(int fmt, int idx);
-size_t q4b_smem_bytes(int fmt, const Q4bConfig& c, int64_t N, int64_t K, int M, int split, int occ);
-cudaError_t launch_gemv_q4b(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
+int qbulk_num_configs(int fmt);
+QbulkConfig qbulk_config(int fmt, int idx);
+size_t qbulk_smem_bytes(int fmt, const QbulkConfig& c, int64_t N, int64_t K, int M, int split, int occ);
+cudaError_t launch_gemv_qbulk(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
 int tma_take_fault();  // 1 if a bounded device wait expired since the last call (and clear it)
 cudaError_t launch_tma_wait_expiry(long long tries, cudaStream_t s);  // a bounded wait that expires
 

@@ -73,7 +73,7 @@ int plan_batch_width(int fmt, const Plan& p) {
     if (p.kind == PLAN_LAT) return lat_max_batch(fmt);
     if (p.kind == PLAN_MMA || p.kind == PLAN_TMA) return mma_max_batch(fmt);
     if (p.kind == PLAN_ROWS) return 1;
-    if (p.kind == PLAN_Q4B) return mma2_max_batch(fmt);
+    if (p.kind == PLAN_QBULK) return mma2_max_batch(fmt);
     return simt_config(fmt, p.cfg).mb;
 }
 
@@ -177,11 +177,13 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K, 
         if (lat_smem_bytes(fmt, c, N, K, mb, p.split, p.occ, glu, fuse ? 1 : 0) > kSmemLimit) return false;
         return true;
     }
-    if (p.kind == PLAN_Q4B) {
-        // INT4 (group-64, AWQ) at the "mma2" batch widths, whole super-blocks, no fusions
-        if ((fmt != FMT_G64 && fmt != FMT_AWQ) || p.cfg < 0 || p.cfg >= q4b_num_configs(fmt)) return false;
-        if (M > mma2_max_batch(fmt) || K % 256 != 0 || p.occ < 1 || p.occ > 2 || K / 256 < p.split) return false;
-        const size_t sm = q4b_smem_bytes(fmt, q4b_config(fmt, p.cfg), N, K, (int)M, p.split, p.occ);
+    if (p.kind == PLAN_QBULK) {
+        // INT4 (group-64, AWQ) and INT8 at the "mma2" batch widths, whole 128-byte super-blocks, no fusions
+        if ((fmt != FMT_G64 && fmt != FMT_AWQ && fmt != FMT_I8) || p.cfg < 0 || p.cfg >= qbulk_num_configs(fmt))
+            return false;
+        const int64_t bk = (fmt == FMT_I8) ? 128 : 256;
+        if (M > mma2_max_batch(fmt) || K % bk != 0 || p.occ < 1 || p.occ > 2 || K / bk < p.split) return false;
+        const size_t sm = qbulk_smem_bytes(fmt, qbulk_config(fmt, p.cfg), N, K, (int)M, p.split, p.occ);
         return sm * p.occ <= (size_t)227 * 1024;
     }
     if (p.kind == PLAN_ROWS) {
@@ -246,10 +248,10 @@ static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
                 Plan p{PLAN_LAT, cfg, splits[si], occ};
                 if (plan_valid(fmt, p, Mb, N, K, flags)) out.push_back(p);
             }
-    for (int cfg = 0; cfg < q4b_num_configs(fmt); ++cfg)
+    for (int cfg = 0; cfg < qbulk_num_configs(fmt); ++cfg)
         for (int si = 0; si < 4; ++si)
             for (int occ = 1; occ <= 2; ++occ) {
-                Plan p{PLAN_Q4B, cfg, splits[si], occ};
+                Plan p{PLAN_QBULK, cfg, splits[si], occ};
                 if (plan_valid(fmt, p, Mb, N, K, flags)) out.push_back(p);
             }
     for (int cfg = 0; cfg < rows_num_configs(); ++cfg)
@@ -400,8 +402,8 @@ std::string plan_to_string(int op, const Plan& p) {
         const TmaConfig c = tma_config(fmt, p.cfg);
         snprintf(buf, sizeof(buf), "tma fmt=%s consumer_warps=%d ring_stages=%d ctas_per_sm=%d split_k=%d", fs,
                  c.warps, c.depth, p.occ, p.split);
-    } else if (p.kind == PLAN_Q4B) {
-        const Q4bConfig c = q4b_config(fmt, p.cfg);
+    } else if (p.kind == PLAN_QBULK) {
+        const QbulkConfig c = qbulk_config(fmt, p.cfg);
         snprintf(buf, sizeof(buf),
                  "bulk fmt=%s consumer_warps=%d ring_stages=%d superblocks_per_warp=%d ctas_per_sm=%d split_k=%d", fs,
                  c.warps, c.depth, c.bsc, p.occ, p.split);
@@ -438,7 +440,7 @@ cudaError_t launch_plan(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t 
     if (p.kind == PLAN_LAT) return launch_gemv_lat(fmt, p, a, s);
     if (p.kind == PLAN_TMA) return launch_gemv_tma(fmt, p, a, s);
     if (p.kind == PLAN_ROWS) return launch_gemv_rows(p, a, s);
-    if (p.kind == PLAN_Q4B) return launch_gemv_q4b(fmt, p, a, s);
+    if (p.kind == PLAN_QBULK) return launch_gemv_qbulk(fmt, p, a, s);
     if (p.kind == PLAN_MMA) return launch_gemv_mma(fmt, p, a, s);
     return launch_gemv_simt(fmt, p, a, s);
 }
