@@ -31,6 +31,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -47,25 +48,26 @@ FALLBACK_HBM_GBS = 6778.3  # the machine's measured copy bandwidth, recorded copy
 NOMINAL_HBM_GBS = 7900.0  # the GB300's nominal HBM3e bandwidth (context only; fractions use the measured peak)
 FALLBACK_BF16_TFLOPS = 1752.2  # the pool's measured sustained cuBLAS bf16, recorded copy
 # DRAM bytes (read + write) per launch of the step's dominant kernel from one
-# ncu capture, keyed by (kernel source sha, shape); a changed kernel gets
-# traffic = null until it is captured again.
+# ncu capture, keyed by (kernel source sha, shape, weight format); a changed
+# kernel gets traffic = null until it is captured again.
 TRAFFIC = {
     # the Qwen2.5-7B gate/up matrices (BF16, 18944x3584), the default step's dominant kernel: gemv_rows
-    # (8 warps, 2 stages of 4 KB per warp, 2 CTAs per SM), ncu --set full, 1 launch, dram__bytes_read.sum
-    # 135,836,160 + dram__bytes_write.sum 3,280,128 (its ncu summary under profiles/); the tuner's
-    # other row-stream instantiations on this shape stream the same rows through the same code (the capture
-    # predates the last edits of gemv_tma.cu, which touched the bulk INT4 kernel and comments only; the
-    # row-stream kernel's code is the one captured)
-    ("a303e31c0276df40", "18944x3584"): 139116288,
+    # (8 warps, 3 stages of 4 KB per warp, 2 CTAs per SM), ncu --set full, 1 launch, dram__bytes_read.sum
+    # 135,828,480 + dram__bytes_write.sum 2,976,000 (its ncu summary under profiles/); the tuner's other
+    # row-stream instantiations on this shape stream the same rows through the same code
+    ("3924d15989828a16", "18944x3584", "bf16"): 138804480,
+    # the qwen3_int8 step's dominant kernel: the bulk-fed kernel on the fused gate_up matrices (INT8, 19456x2560),
+    # 49,933,056 + 768 (its ncu summary under profiles/)
+    ("3924d15989828a16", "19456x2560", "int8_pc"): 49933824,
     # the TinyLlama INT4 step's dominant kernel: gemv_lat on the fused gate_up matrices (INT4 g64, 11264x2048),
     # dram__bytes_read.sum 12,315,392 + dram__bytes_write.sum 0 (its ncu summary under profiles/)
-    ("cf3bf3b20ec9aac8", "11264x2048"): 12315392,
+    ("cf3bf3b20ec9aac8", "11264x2048", "int4_g64"): 12315392,
     # the qwen3_int8 step's dominant kernel: gemv_mma2 on the fused gate_up matrices (INT8, 19456x2560),
     # 49,947,648 + 2,048 (its ncu summary under profiles/)
-    ("ae20d984bdd059ad", "19456x2560"): 49949696,
+    ("ae20d984bdd059ad", "19456x2560", "int8_pc"): 49949696,
     # the AWQ batch-1 step's dominant kernel: gemv_mma2 on 18944x3584 (AWQ, repacked codes), 35,340,800 + 0
     # (its ncu summary under profiles/)
-    ("ae20d984bdd059ad", "18944x3584"): 35340800,
+    ("ae20d984bdd059ad", "18944x3584", "int4_awq_g128"): 35340800,
 }
 
 
@@ -862,7 +864,8 @@ def main():
         dominant = max(step.shapes(), key=lambda sh: counts[sh] * shape_times[skey(sh)]["us"])
     family = plans[skey(dominant)].split(" ")[0] if dominant else "lat"
     sha = kernel_source_sha(family)
-    traffic = TRAFFIC.get((sha, skey(dominant))) if dominant else None
+    fmt_tok = re.search(r"fmt=(\S+)", plans[skey(dominant)]) if dominant else None
+    traffic = TRAFFIC.get((sha, skey(dominant), fmt_tok.group(1))) if fmt_tok else None
     clocks = sampler.summary(t0, t1)
     if rank != 0:
         return
