@@ -154,9 +154,12 @@ def test_int8_every_plan_at_qwen3_4b_shapes(orc, N, K):
     s = np.concatenate([gen.f32_row_scales(0, 50, N, row0=int(r), rows=1) for r in rows])
     Y, A = orc.gemm_int8_pc(q, s, host_bits16(xd))
     sel = torch.from_numpy(rows).cuda()
+    families = set()
     for _, desc in each_plan(1, N, K):
+        families.add(desc.split()[0])
         y = mbw.gemv_int8_pc(qd, sd, xd[0])
         assert_parity(y[sel], Y[0], A[0], f"int8 {N}x{K} plan {desc}")
+    assert {"mma2", "bulk"} <= families  # the register-ring and the bulk-fed streaming kernels both ran
 
 
 def test_int8_lm_head_sampled_rows(orc):
