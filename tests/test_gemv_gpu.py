@@ -111,7 +111,7 @@ def test_dequant_bit_exact(orc):
 @pytest.mark.parametrize("fmt", ["bf16", "g64", "awq"])
 def test_one_hot_x_gives_the_exact_column(orc, fmt):
     """x = e_k: with fp32 output the GEMV returns column k of the weights
-    exactly -- the in-kernel unpack and dequant are bit-exact."""
+    exactly, on every plan -- the in-kernel unpack and dequant are bit-exact."""
     N, K = 200, 1024
     if fmt == "bf16":
         W, _ = bf16_case(601, N, K)
@@ -128,39 +128,51 @@ def test_one_hot_x_gives_the_exact_column(orc, fmt):
         c, s, z, _ = awq_case(603, N, K, 1)
         deq = orc.dequant_int4_awq_g128(c, s, z, N, K)
         cd, sd, zd = dev_u8(c), dev_f16(s), dev_u8(z)
+    op = {"bf16": mbw.OP_GEMV_BF16, "g64": mbw.OP_GEMV_INT4_G64, "awq": mbw.OP_GEMV_INT4_AWQ_G128}[fmt]
+    xs = {}
     for k in (0, 1, 63, 64, 127, 128, 511, 1023):
         e = np.zeros(K, dtype=np.uint16)
         e[k] = 0x3F80  # 1.0
-        xd = dev_bf16(e)
-        with mbw.output_fp32():
-            if fmt == "bf16":
-                y = mbw.gemv_bf16(Wd, xd)
-            elif fmt == "g64":
-                y = mbw.gemv_int4_g64(cd, sd, xd)
-            else:
-                y = mbw.gemv_int4_awq_g128(cd, sd, zd, xd)
-        assert np.array_equal(host_f64(y), deq[:, k]), (fmt, k)
+        xs[k] = dev_bf16(e)
+    for _, desc in each_plan(op, 1, N, K):  # every family and instantiation
+        for k, xd in xs.items():
+            with mbw.output_fp32():
+                if fmt == "bf16":
+                    y = mbw.gemv_bf16(Wd, xd)
+                elif fmt == "g64":
+                    y = mbw.gemv_int4_g64(cd, sd, xd)
+                else:
+                    y = mbw.gemv_int4_awq_g128(cd, sd, zd, xd)
+            assert np.array_equal(host_f64(y), deq[:, k]), (fmt, k, desc)
 
 
 def test_power_of_two_scaling_and_determinism():
+    """On every plan: a repeated call returns the same bits (fixed-order sums,
+    no atomics), and scaling x by a power of two scales the fp32 output
+    exactly."""
     N, K = 3000, 2048
     c, s, X = g64_case(700, N, K)
     cd, sd = dev_u8(c), dev_f16(s)
     x = dev_bf16(X[0])
     x2 = (x.float() * 4.0).to(torch.bfloat16)
-    with mbw.output_fp32():
-        y1 = mbw.gemv_int4_g64(cd, sd, x)
-        y1b = mbw.gemv_int4_g64(cd, sd, x)
-        y2 = mbw.gemv_int4_g64(cd, sd, x2)
-    assert torch.equal(y1, y1b)
-    assert torch.equal(y2, y1 * 4.0)
+    for _, desc in each_plan(mbw.OP_GEMV_INT4_G64, 1, N, K):
+        with mbw.output_fp32():
+            y1 = mbw.gemv_int4_g64(cd, sd, x)
+            y1b = mbw.gemv_int4_g64(cd, sd, x)
+            y2 = mbw.gemv_int4_g64(cd, sd, x2)
+        assert torch.equal(y1, y1b), desc
+        assert torch.equal(y2, y1 * 4.0), desc
     W, Xb = bf16_case(701, N, K)
     Wd = dev_bf16(W)
     xb = dev_bf16(Xb[0])
-    a = mbw.gemv_bf16(Wd, xb)
-    b = mbw.gemv_bf16(Wd, xb)
-    assert torch.equal(a, b)
-    assert torch.equal(mbw.gemv_bf16(Wd, (xb.float() * 0.5).to(torch.bfloat16)), (a.float() * 0.5).to(torch.bfloat16))
+    xh = (xb.float() * 0.5).to(torch.bfloat16)
+    for _, desc in each_plan(mbw.OP_GEMV_BF16, 1, N, K):
+        with mbw.output_fp32():
+            a = mbw.gemv_bf16(Wd, xb)
+            b = mbw.gemv_bf16(Wd, xb)
+            h = mbw.gemv_bf16(Wd, xh)
+        assert torch.equal(a, b), desc
+        assert torch.equal(h, a * 0.5), desc
 
 
 def test_zero_weights_give_exact_zero():
