@@ -1105,7 +1105,7 @@ int tc_batch_tile(int64_t M) {
 // and streams its first W tiles while this one finishes.
 static int tc_stages(int nt, int ring, int bps) {
     const size_t stage = (128 * 128 + (size_t)nt * 128) * bps;
-    int d = (int)(((ring == 0 ? 180 : 96) * 1024) / stage);
+    int d = (int)(((ring == 0 ? 200 : 96) * 1024) / stage);
     if (d > 8) d = 8;
     if (d < 2) d = 2;
     return d;
@@ -1122,7 +1122,7 @@ size_t tc_smem_bytes(int nt, int D, int split, int bps) {
 // CTA-pair kernel: a CTA stages 128 W rows and nt/2 X rows per box.
 static int tc2_stages(int nt, int ring, int bps) {
     const size_t stage = (128 * 128 + (size_t)(nt / 2) * 128) * bps;
-    int d = (int)(((ring == 0 ? 180 : 96) * 1024) / stage);
+    int d = (int)(((ring == 0 ? 200 : 96) * 1024) / stage);
     if (d > 8) d = 8;
     if (d < 2) d = 2;
     return d;
