@@ -52,22 +52,19 @@ FALLBACK_BF16_TFLOPS = 1752.2  # the pool's measured sustained cuBLAS bf16, reco
 # kernel gets traffic = null until it is captured again.
 TRAFFIC = {
     # the Qwen2.5-7B gate/up matrices (BF16, 18944x3584), the default step's dominant kernel: gemv_rows
-    # (8 warps, 3 stages of 4 KB per warp, 2 CTAs per SM), ncu --set full, 1 launch, dram__bytes_read.sum
-    # 135,828,480 + dram__bytes_write.sum 2,976,000 (its ncu summary under profiles/); the tuner's other
-    # row-stream instantiations on this shape stream the same rows through the same code
-    ("3924d15989828a16", "18944x3584", "bf16"): 138804480,
+    # (8 warps, 3 stages of 4 KB per warp, 2 CTAs per SM), ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,
+    # 1 launch: 135,827,712 + 2,765,568 (profiles/gemv_rows_bf16_18944x3584.md); the tuner's other row-stream
+    # instantiations on this shape stream the same rows through the same code
+    ("f5ed3ed01133743e", "18944x3584", "bf16"): 138593280,
     # the qwen3_int8 step's dominant kernel: the bulk-fed kernel on the fused gate_up matrices (INT8, 19456x2560),
-    # 49,933,056 + 768 (its ncu summary under profiles/)
-    ("3924d15989828a16", "19456x2560", "int8_pc"): 49933824,
+    # 49,933,824 + 0 (same capture; its ncu summary under profiles/)
+    ("f5ed3ed01133743e", "19456x2560", "int8_pc"): 49933824,
     # the TinyLlama INT4 step's dominant kernel: gemv_lat on the fused gate_up matrices (INT4 g64, 11264x2048),
     # dram__bytes_read.sum 12,315,392 + dram__bytes_write.sum 0 (its ncu summary under profiles/)
     ("cf3bf3b20ec9aac8", "11264x2048", "int4_g64"): 12315392,
-    # the qwen3_int8 step's dominant kernel: gemv_mma2 on the fused gate_up matrices (INT8, 19456x2560),
-    # 49,947,648 + 2,048 (its ncu summary under profiles/)
-    ("ae20d984bdd059ad", "19456x2560", "int8_pc"): 49949696,
-    # the AWQ batch-1 step's dominant kernel: gemv_mma2 on 18944x3584 (AWQ, repacked codes), 35,340,800 + 0
-    # (its ncu summary under profiles/)
-    ("ae20d984bdd059ad", "18944x3584", "int4_awq_g128"): 35340800,
+    # the AWQ batch-1 step's dominant kernel: gemv_mma2 on 18944x3584 (AWQ, repacked codes), 35,341,056 + 0
+    # (same capture; its ncu summary under profiles/)
+    ("fc44b33cdfecb3fc", "18944x3584", "int4_awq_g128"): 35341056,
 }
 
 

@@ -44,6 +44,8 @@
 // sum once.
 #include <cooperative_groups.h>
 
+#include <algorithm>
+
 #include "device.cuh"
 #include "internal.h"
 
@@ -431,17 +433,18 @@ static const AwqbEntry kAwqb[] = {
 int awqb_num_configs() { return (int)(sizeof(kAwqb) / sizeof(kAwqb[0])); }
 AwqbConfig awqb_config(int idx) { return kAwqb[idx].cfg; }
 
-int awqb_row_groups(int64_t N, int split, int occ) {
-    const int sms = device_sm_count();
-    const int64_t T = (N + 15) / 16;
-    int64_t G = ((int64_t)sms * occ) / split;
-    if (G > T) G = T;
-    if (G < 1) G = 1;
-    return (int)G;
+// CTA row-groups: one wave of occ CTAs per SM, or more groups (several waves)
+// where the per-tile partials and tables of one wave's share do not fit the
+// planner's limit (at most 227 KB over the occ CTAs of an SM).
+int awqb_row_groups(const AwqbConfig& c, int64_t N, int64_t K, int split, int occ) {
+    const size_t limit = std::min(kSmemFit, (size_t)227 * 1024 / occ);
+    return fitted_row_groups(N, split, occ, limit, [&](int G) {
+        return awqb_smem_layout(K, N, 8 * c.nb, c.wt * c.wk, c.wk, c.u, c.async, split, G).total;
+    });
 }
 
 size_t awqb_smem_bytes(const AwqbConfig& c, int64_t N, int64_t K, int split, int occ) {
-    const int G = awqb_row_groups(N, split, occ);
+    const int G = awqb_row_groups(c, N, K, split, occ);
     return awqb_smem_layout(K, N, 8 * c.nb, c.wt * c.wk, c.wk, c.u, c.async, split, G).total;
 }
 
@@ -450,7 +453,7 @@ cudaError_t launch_gemv_awq_batch(const Plan& p, const GemvArgs& a, cudaStream_t
     const AwqbEntry& e = kAwqb[p.cfg];
     if (a.M < 1 || a.M > 8 * e.cfg.nb || a.K % 256 != 0) return cudaErrorInvalidValue;
     if ((uint64_t)a.N * (uint64_t)(a.K / 2) > 0xFFFFFFFFull) return cudaErrorInvalidValue;  // 32-bit offsets
-    const int G = awqb_row_groups(a.N, p.split, p.occ);
+    const int G = awqb_row_groups(e.cfg, a.N, a.K, p.split, p.occ);
     const size_t smem = awqb_smem_bytes(e.cfg, a.N, a.K, p.split, p.occ);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

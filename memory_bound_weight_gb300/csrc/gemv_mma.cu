@@ -832,13 +832,21 @@ MmaConfig mma2_config(int fmt, int idx) {
 int mma2_max_batch(int fmt) { return fmt == FMT_G64 ? 2 : fmt == FMT_AWQ ? 4 : 8; }
 int mma2_block_k(int fmt) { return fmt == FMT_BF16 ? 64 : fmt == FMT_I8 ? 128 : 256; }
 
-size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu) {
-    const int G = mma_row_groups(N, split, occ);
+static size_t mma2_layout_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int G, int glu) {
     const int xpad = (fmt == FMT_G64 || fmt == FMT_AWQ) ? 40 : (fmt == FMT_I8) ? 20 : 0;
     const MmaSmem L = mma_smem_layout(mma2_block_k(fmt), K, (int)N, M, c.warps, split, G, glu, xpad);
     const size_t base = L.total + (fmt == FMT_I8 ? (size_t)L.ntmax * 16 * 4 : 0);  // + INT8 row scales
     if (!c.async) return base;
     return (base + 127) / 128 * 128 + (size_t)c.warps * c.u * 4 * 512;
+}
+
+static int mma2_groups(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu) {
+    return fitted_row_groups(N, split, occ, kSmemFit,
+                             [&](int G) { return mma2_layout_bytes(fmt, c, N, K, M, split, G, glu); });
+}
+
+size_t mma2_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ, int glu) {
+    return mma2_layout_bytes(fmt, c, N, K, M, split, mma2_groups(fmt, c, N, K, M, split, occ, glu), glu);
 }
 
 cudaError_t launch_gemv_mma2(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
@@ -851,8 +859,8 @@ cudaError_t launch_gemv_mma2(int fmt, const Plan& p, const GemvArgs& a, cudaStre
     const MmaEntry& e = t[p.cfg];
     const MmaFn fn = gemv_fused_args(a) ? e.fnf : e.fn;
     if (fn == nullptr) return cudaErrorInvalidValue;
-    const int G = mma_row_groups(a.N, p.split, p.occ);
-    const size_t smem = mma2_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ, a.glu);
+    const int G = mma2_groups(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ, a.glu);
+    const size_t smem = mma2_layout_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, G, a.glu);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
@@ -921,10 +929,15 @@ int mma_row_groups(int64_t N, int split, int occ) {
     return (int)G;
 }
 
+static int mma_groups(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
+    const int BK = (fmt == FMT_BF16) ? 32 : 128;
+    return fitted_row_groups(N, split, occ, kSmemFit,
+                             [&](int G) { return mma_smem_layout(BK, K, (int)N, M, c.warps, split, G).total; });
+}
+
 size_t mma_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
     const int BK = (fmt == FMT_BF16) ? 32 : 128;
-    const int G = mma_row_groups(N, split, occ);
-    return mma_smem_layout(BK, K, (int)N, M, c.warps, split, G).total;
+    return mma_smem_layout(BK, K, (int)N, M, c.warps, split, mma_groups(fmt, c, N, K, M, split, occ)).total;
 }
 
 cudaError_t launch_gemv_mma(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
@@ -932,7 +945,7 @@ cudaError_t launch_gemv_mma(int fmt, const Plan& p, const GemvArgs& a, cudaStrea
     const MmaEntry* t = mma_table(fmt, &n);
     if (p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > mma_max_batch(fmt)) return cudaErrorInvalidValue;
     const MmaEntry& e = t[p.cfg];
-    const int G = mma_row_groups(a.N, p.split, p.occ);
+    const int G = mma_groups(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
     const size_t smem = mma_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -461,9 +461,14 @@ TmaConfig tma_config(int fmt, int idx) {
     return tma_table(fmt, &n)[idx].cfg;
 }
 
+static int tma_groups(int fmt, const TmaConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
+    return fitted_row_groups(N, split, occ, kSmemFit, [&](int G) {
+        return tma_smem_layout(fmt, K, (int)N, M, c.warps, c.depth, split, G).total;
+    });
+}
+
 size_t tma_smem_bytes(int fmt, const TmaConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
-    const int G = mma_row_groups(N, split, occ);
-    return tma_smem_layout(fmt, K, (int)N, M, c.warps, c.depth, split, G).total;
+    return tma_smem_layout(fmt, K, (int)N, M, c.warps, c.depth, split, tma_groups(fmt, c, N, K, M, split, occ)).total;
 }
 
 cudaError_t launch_gemv_tma(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
@@ -471,7 +476,7 @@ cudaError_t launch_gemv_tma(int fmt, const Plan& p, const GemvArgs& a, cudaStrea
     const TmaEntry* t = tma_table(fmt, &n);
     if (p.cfg < 0 || p.cfg >= n || a.M < 1 || a.M > mma_max_batch(fmt)) return cudaErrorInvalidValue;
     const TmaEntry& e = t[p.cfg];
-    const int G = mma_row_groups(a.N, p.split, p.occ);
+    const int G = tma_groups(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
     const size_t smem = tma_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1134,9 +1139,16 @@ QbulkConfig qbulk_config(int fmt, int idx) {
     return qbulk_table(fmt, &n)[idx].cfg;
 }
 
+// (occ CTAs of this kernel share an SM's 227 KB)
+static int qbulk_groups(int fmt, const QbulkConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
+    return fitted_row_groups(N, split, occ, (size_t)227 * 1024 / occ, [&](int G) {
+        return qbulk_smem_layout(fmt, K, N, M, c.warps, c.depth, c.bsc, split, G).total;
+    });
+}
+
 size_t qbulk_smem_bytes(int fmt, const QbulkConfig& c, int64_t N, int64_t K, int M, int split, int occ) {
-    const int G = mma_row_groups(N, split, occ);
-    return qbulk_smem_layout(fmt, K, N, M, c.warps, c.depth, c.bsc, split, G).total;
+    return qbulk_smem_layout(fmt, K, N, M, c.warps, c.depth, c.bsc, split, qbulk_groups(fmt, c, N, K, M, split, occ))
+        .total;
 }
 
 cudaError_t launch_gemv_qbulk(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s) {
@@ -1146,7 +1158,7 @@ cudaError_t launch_gemv_qbulk(int fmt, const Plan& p, const GemvArgs& a, cudaStr
         a.glu)
         return cudaErrorInvalidValue;
     const QbulkEntry& e = t[p.cfg];
-    const int G = mma_row_groups(a.N, p.split, p.occ);
+    const int G = qbulk_groups(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
     const size_t smem = qbulk_smem_bytes(fmt, e.cfg, a.N, a.K, a.M, p.split, p.occ);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

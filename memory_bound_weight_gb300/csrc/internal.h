@@ -144,6 +144,32 @@ size_t mma_smem_bytes(int fmt, const MmaConfig& c, int64_t N, int64_t K, int M, 
 int mma_row_groups(int64_t N, int split, int occ);
 cudaError_t launch_gemv_mma(int fmt, const Plan& p, const GemvArgs& a, cudaStream_t s);
 
+// Shared memory a GEMV launch may ask for (the planner's limit).
+constexpr size_t kSmemFit = 200 * 1024;
+
+// CTA row-groups of a launch whose shared memory holds the partial sums of
+// every 16-row tile a CTA owns: the one-wave count of mma_row_groups when that
+// layout fits `limit` bytes, else the fewest groups whose layout does (a very
+// tall matrix then runs in several waves; its CTAs depend on no CTA outside
+// their own cluster). bytes(G), the layout's size for G groups, never grows
+// with G; when not even one tile per CTA fits, the one-wave count is returned
+// and the caller's size check refuses the plan.
+template <class F>
+int fitted_row_groups(int64_t N, int split, int occ, size_t limit, F bytes) {
+    const int64_t G = mma_row_groups(N, split, occ);
+    const int64_t T = (N + 15) / 16;
+    if (G >= T || bytes((int)G) <= limit || bytes((int)T) > limit) return (int)G;
+    int64_t lo = G + 1, hi = T;  // bytes(hi) fits
+    while (lo < hi) {
+        const int64_t mid = lo + (hi - lo) / 2;
+        if (bytes((int)mid) <= limit)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return (int)lo;
+}
+
 // 32-bytes-per-lane tensor-core kernel tables (gemv_mma.cu).
 int mma2_num_configs(int fmt);
 MmaConfig mma2_config(int fmt, int idx);
@@ -166,7 +192,7 @@ cudaError_t launch_gemv_lat(int fmt, const Plan& p, const GemvArgs& a, cudaStrea
 // rows per launch, K % 256 == 0.
 int awqb_num_configs();
 AwqbConfig awqb_config(int idx);
-int awqb_row_groups(int64_t N, int split, int occ);
+int awqb_row_groups(const AwqbConfig& c, int64_t N, int64_t K, int split, int occ);
 size_t awqb_smem_bytes(const AwqbConfig& c, int64_t N, int64_t K, int split, int occ);
 cudaError_t launch_gemv_awq_batch(const Plan& p, const GemvArgs& a, cudaStream_t s);
 

@@ -28,7 +28,7 @@ namespace mbw {
 static std::mutex g_plan_mu;
 static std::map<std::tuple<int, int, int64_t, int64_t, int64_t>, Plan> g_plans;
 
-static const size_t kSmemLimit = 200 * 1024;
+static const size_t kSmemLimit = kSmemFit;
 
 static int fmt_of_op(int op) {
     switch (op & MBW_OP_BASE_MASK) {

@@ -237,6 +237,30 @@ def test_planner_host_logic(L):
     assert L.mbw_workspace_bytes(1, 1, 2048, 2048) == 0
 
 
+def test_tall_matrices_have_a_plan_at_every_batch(L):
+    """The tensor-core GEMV families keep one partial sum per 16-row tile a CTA
+    owns in shared memory; past one wave's share of rows that fits, a launch
+    takes more CTAs (several waves) instead of refusing the shape. So every
+    call shape the header accepts has at least one plan, up to a few million
+    rows and K = 65536 (INT8 at batch 8 and the repacked AWQ codes at batch 4
+    had none on tall matrices before)."""
+    cases = [(1, (1, 2, 4, 8)), (2, (1,)), (3, (1, 2, 3, 4, 5, 8, 16, 64, 256)), (3 | 0x800, (1, 4, 16, 64)),
+             (4, (5, 8, 16, 64, 256)), (5, (1, 2, 3, 4, 5, 8, 16, 64))]
+    for op, Ms in cases:
+        for K in (1024, 4096, 16384, 65536):
+            for N in (16, 4096, 300000, 1000000, 4000000):
+                for M in Ms:
+                    assert L.mbw_plan_candidates(op, M, N, K) >= 1, (op, M, N, K)
+    # an INT8 batch of 8 on 300,000 rows: the tensor-core families run, in several waves
+    buf = ctypes.create_string_buffer(256)
+    kinds = set()
+    for i in range(L.mbw_plan_candidates(5, 8, 300000, 4096)):
+        assert L.mbw_plan_select(5, 8, 300000, 4096, i) == 0
+        assert L.mbw_plan_describe(5, 8, 300000, 4096, buf, 256) == 0
+        kinds.add(buf.value.split()[0])
+    assert b"mma2" in kinds
+
+
 def test_output_hook_is_thread_local(L):
     import threading
 
