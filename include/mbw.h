@@ -27,6 +27,15 @@
  *   - Calls are asynchronous on `stream`; arguments are checked on the host
  *     before any CUDA call and reported as a status, never thrown. Launch
  *     errors are returned as MBW_ERR_CUDA (detail in mbw_last_error()).
+ *   - Shapes no kernel fits return MBW_ERR_UNSUPPORTED before any launch:
+ *     the GEMV kernels stage the x of one CTA's k-range (split over at most
+ *     8 CTAs of a cluster) in shared memory, so very long rows have no plan
+ *     (batch 1: K above about 650,000 for INT8 and 800,000 for BF16 and INT4;
+ *     wider batches proportionally less). gemm_skinny_bf16 from M = 5 on
+ *     streams X through its tensor-core ring and takes any K.
+ *     mbw_plan_candidates() == 0 tells in advance. Tall matrices have no such
+ *     limit: a launch whose per-tile partial sums do not fit one wave of CTAs
+ *     runs in several.
  *   - y must not alias an input. Results are deterministic: the same inputs
  *     give bitwise the same outputs, run after run.
  *   - Kernels use programmatic dependent launch: each GEMV/GEMM starts

@@ -71,6 +71,9 @@ static mbw_status run_simt(int fmt, int op, const uint8_t* W, const uint16_t* sc
                            const float* rscale = nullptr, const mbw_fusion* fz = nullptr) {
     if (take_injected_failure("GEMV launch")) return MBW_ERR_CUDA;
     const Plan p = plan_lookup(op, M, N, K, s);
+    if (p.kind == PLAN_NONE)
+        return fail(MBW_ERR_UNSUPPORTED, "no kernel fits this shape: the x of one CTA's k-range (split over the "
+                                         "largest cluster) does not fit shared memory; see mbw_plan_candidates");
     const int width = plan_batch_width(fmt, p);
     GemvArgs a{};
     a.W = W;

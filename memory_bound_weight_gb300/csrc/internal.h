@@ -119,6 +119,7 @@ struct Plan {
     int occ;    // MMA kernels: CTAs per SM in the persistent grid (1 for SIMT)
 };
 enum PlanKind : int {
+    PLAN_NONE = -1,  // no kernel fits the shape (the call returns MBW_ERR_UNSUPPORTED)
     PLAN_SIMT = 0,
     PLAN_MMA = 1,
     PLAN_TMA = 2,

@@ -274,7 +274,7 @@ static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
     return out;
 }
 
-Plan plan_default(int op, int64_t M, int64_t N, int64_t K) {
+static Plan plan_heuristic(int op, int64_t M, int64_t N, int64_t K) {
     const int fmt = fmt_of_op(op);
     const int flags = op & (MBW_FUSE_MASK | MBW_REPACKED);
     const int fuse = op & MBW_FUSE_MASK;
@@ -345,6 +345,19 @@ Plan plan_default(int op, int64_t M, int64_t N, int64_t K) {
     return Plan{PLAN_MMA, cfg, 8, 1};
 }
 
+// The built-in plan of a shape: the heuristic's pick when it is one of the
+// shape's candidates, else the first candidate, else PLAN_NONE (no kernel
+// fits: x of one CTA's k-range, even split over the largest cluster, does not
+// fit shared memory).
+Plan plan_default(int op, int64_t M, int64_t N, int64_t K) {
+    const Plan h = plan_heuristic(op, M, N, K);
+    const std::vector<Plan> c = candidates(op, M, N, K);
+    for (const Plan& p : c)
+        if (p.kind == h.kind && p.cfg == h.cfg && p.split == h.split && p.occ == h.occ) return h;
+    if (!c.empty()) return c.front();
+    return Plan{PLAN_NONE, 0, 1, 1};
+}
+
 static int current_device() {
     int d = 0;
     cudaGetDevice(&d);
@@ -370,6 +383,7 @@ Plan plan_lookup(int op, int64_t M, int64_t N, int64_t K, cudaStream_t s) {
 }
 
 std::string plan_to_string(int op, const Plan& p) {
+    if (p.kind == PLAN_NONE) return "none (no kernel fits this shape)";
     const int fmt = fmt_of_op(op);
     const char* fs = fmt == FMT_BF16 ? "bf16" : fmt == FMT_G64 ? "int4_g64" : fmt == FMT_I8 ? "int8_pc" : "int4_awq_g128";
     char buf[192];

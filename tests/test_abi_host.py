@@ -129,6 +129,10 @@ A16c = 0x30000
     (lambda L: L.gemv_int4_awq_g128_repacked(A16, A16b, A16c, A16c, A16, 1, 8, 192, None, 0, None), 3),
     (lambda L: L.gemv_int4_awq_g128_repacked(A16, A16b, None, A16c, A16, 1, 8, 256, None, 0, None), 1),
     (lambda L: L.gemv_int4_awq_g128_repacked(A16, A16b, A16c, A16c, A16, 0, 8, 256, None, 0, None), 0),
+    # no kernel fits: x of one CTA's k-range, split over the largest cluster, exceeds shared memory
+    (lambda L: L.gemv_bf16(A16, A16b, A16c, 16, 1 << 20, None, 0, None), 5),
+    (lambda L: L.gemv_int8_pc(A16, A16b, A16c, A16, 8, 16, 1 << 17, None, 0, None), 5),
+    (lambda L: L.gemv_int4_awq_g128(A16, A16b, A16c, A16c, A16, 64, 16, 1 << 18, None, 0, None), 5),
     (lambda L: L.mbw_set_output_fp32(2), 1),
     (lambda L: L.mbw_plan_select(9, 1, 8, 64, 0), 1),
     (lambda L: L.mbw_autotune(9, 1, 8, 64, None), 1),
@@ -235,6 +239,11 @@ def test_planner_host_logic(L):
     buf = ctypes.create_string_buffer(256)
     assert L.mbw_plan_describe(5, 1, 9728, 2560, buf, 256) == 0 and b"int8_pc" in buf.value
     assert L.mbw_workspace_bytes(1, 1, 2048, 2048) == 0
+    # a shape no kernel fits has no candidate and describes its plan as none
+    assert L.mbw_plan_candidates(1, 1, 16, 1 << 20) == 0 and L.mbw_plan_index(1, 1, 16, 1 << 20) == -1
+    assert L.mbw_plan_describe(1, 1, 16, 1 << 20, buf, 256) == 0 and buf.value.startswith(b"none")
+    # the skinny GEMM streams X through the tensor-core ring: any K from batch 5 on
+    assert L.mbw_plan_candidates(4, 8, 16, 1 << 24) >= 1
 
 
 def test_tall_matrices_have_a_plan_at_every_batch(L):

@@ -174,3 +174,21 @@ def test_int8_past_4_gib_and_tall_batches(orc):
     Y, A = orc.gemm_int8_pc(qr, sr, host_bits16(Xd))
     mbw.autotune(op, 8, N, K)
     assert_parity(mbw.gemv_int8_pc(qd, sd, Xd)[:, sel], Y, A, f"int8 M=20 {N}x{K} autotuned")
+
+
+def test_rows_too_long_for_any_gemv_plan(orc):
+    """K = 2^20 at batch 1: no GEMV kernel can stage x, so the call is refused
+    with MBW_ERR_UNSUPPORTED before any launch and the context stays usable;
+    the skinny GEMM from batch 5 on streams X through its ring and computes
+    the same rows at batch 8 (every plan)."""
+    N, K = 16, 1 << 20
+    W, X = gen.bf16_weights(SEED, 6, N, K), gen.bf16_activations(SEED, 6, 8, K)
+    Wd = torch.from_numpy(W.view(np.int16)).view(torch.bfloat16).cuda()
+    Xd = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).cuda()
+    assert mbw.plan_candidates(mbw.OP_GEMV_BF16, 1, N, K) == 0
+    with pytest.raises(mbw.MbwError) as err:
+        mbw.gemv_bf16(Wd, Xd[0])
+    assert err.value.status == 5
+    Y, A = orc.gemm_bf16(W, X)
+    for i, desc in each_plan(mbw.OP_GEMM_SKINNY_BF16, 8, N, K):
+        assert_parity(mbw.gemm_skinny_bf16(Xd, Wd), Y, A, f"skinny M=8 {N}x{K} plan {i}: {desc}")
