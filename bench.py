@@ -76,7 +76,8 @@ def parse_args():
     p.add_argument("--impl", default="mbw", choices=["mbw", "reference"])
     p.add_argument("--workload", default="qwen_bf16",
                    choices=["tinyllama_int4", "tinyllama_int4_fusedops", "tinyllama_int4_unfused", "qwen_bf16",
-                            "qwen_awq", "qwen_awq_repacked", "qwen_awq_fusedops", "qwen3_int8", "bf16_2048"])
+                            "qwen_bf16_fused", "qwen_awq", "qwen_awq_repacked", "qwen_awq_fusedops", "qwen3_int8",
+                            "bf16_2048"])
     p.add_argument("--batch", type=int, default=1,
                    help="activation rows per GEMV (qwen_awq: AWQ-style INT4 decode at batch M)")
     p.add_argument("--no-e2e", action="store_true")
@@ -378,6 +379,7 @@ WORKLOAD_MATS = {
     "tinyllama_int4_fusedops": (lambda: wl.tinyllama_step(fusedops=True), wl.FMT_INT4_G64),
     "tinyllama_int4_unfused": (lambda: wl.tinyllama_step(), wl.FMT_INT4_G64),
     "qwen_bf16": (wl.qwen25_7b_step, wl.FMT_BF16),
+    "qwen_bf16_fused": (lambda: wl.qwen25_7b_step(fused=True), wl.FMT_BF16),
     "qwen_awq": (wl.qwen25_7b_step, wl.FMT_INT4_AWQ_G128),
     "qwen_awq_repacked": (wl.qwen25_7b_step, wl.FMT_INT4_AWQ_G128),
     "qwen_awq_fusedops": (lambda: wl.qwen25_7b_step(fusedops=True), wl.FMT_INT4_AWQ_G128),
@@ -392,6 +394,9 @@ def make_step(workload, seed, device, M=1):
                     WORKLOAD_MATS[workload][0](), seed, device)
     if workload == "qwen_bf16":
         return Step("Qwen2.5-7B-shaped BF16 decode step, batch 1", wl.FMT_BF16, wl.qwen25_7b_step(), seed, device)
+    if workload == "qwen_bf16_fused":
+        return Step("Qwen2.5-7B-shaped BF16 decode step, batch 1, gate and up fused", wl.FMT_BF16,
+                    wl.qwen25_7b_step(fused=True), seed, device)
     if workload in ("qwen_awq", "qwen_awq_repacked", "qwen_awq_fusedops"):
         rp = workload != "qwen_awq"
         fo = workload == "qwen_awq_fusedops"
@@ -544,6 +549,8 @@ def workload_desc(workload, batch=1):
                                        "(q/k/v, gate/up, head), SwiGLU epilogue (gate/up), residual-add epilogues (o, "
                                        "down) (89 GEMVs)",
             "qwen_bf16": "Qwen2.5-7B-shaped BF16 decode step, batch 1 (141 GEMVs)",
+            "qwen_bf16_fused": "Qwen2.5-7B-shaped BF16 decode step, batch 1, gate and up stored as one [Wgate; Wup] "
+                               "matrix and streamed by one GEMV per layer (113 GEMVs, the same weights)",
             "qwen_awq": f"Qwen2.5-7B-shaped AWQ-style INT4 decode step (group 128, fp16 scale, uint4 zero point, LM head "
                         f"included), batch {batch} (141 GEMMs)",
             "qwen_awq_repacked": f"Qwen2.5-7B-shaped AWQ-style INT4 decode step (group 128, fp16 scale, uint4 zero "
@@ -708,8 +715,9 @@ def skinny_figures(device, Ms=wl.SKINNY_M, reps=7):
 def extra_configs(device, main_workload, tune="shape"):
     """The other configurations the metric is quoted on, after the headline
     step (N = 1 only): BF16 GEMV 2048x2048; the four TinyLlama-shaped INT4
-    group-64 matrices and the TinyLlama INT4 step; the skinny BF16 GEMM sweep;
-    the AWQ-style INT4 step at M = 1, 16, 64 with repacked codes."""
+    group-64 matrices and the TinyLlama INT4 step; the Qwen2.5-7B BF16 step
+    with gate and up stored as one matrix; the skinny BF16 GEMM sweep; the
+    AWQ-style INT4 step at M = 1, 16, 64 with repacked codes."""
     t0 = time.time()
     out = {}
     out["bf16_gemv_2048x2048"] = per_matrix_figures(wl.FMT_BF16, [(0, 2048, 2048)], device)
@@ -719,6 +727,9 @@ def extra_configs(device, main_workload, tune="shape"):
         out["int4_g64_tinyllama_step"] = step_figure("tinyllama_int4", 1, device, tune)
     if main_workload != "qwen_bf16":
         out["bf16_qwen_step"] = step_figure("qwen_bf16", 1, device, tune)
+    if main_workload != "qwen_bf16_fused":
+        # the same weights with gate and up stored as one matrix: 113 GEMVs instead of 141
+        out["bf16_qwen_step_gate_up_fused"] = step_figure("qwen_bf16_fused", 1, device, tune)
     out["skinny_bf16_qwen_mlp"] = skinny_figures(device)
     out["awq_qwen_step_repacked"] = {f"M={M}": step_figure("qwen_awq_repacked", M, device, tune) for M in wl.AWQ_M}
     out["seconds"] = time.time() - t0

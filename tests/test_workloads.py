@@ -101,3 +101,13 @@ def test_fused_qwen_awq_step_streams_the_same_weights():
     residuals = 28 * 2 * 3584 * 2                   # o and down
     x_saved = 28 * 3584 * 2                         # up no longer reads its own x
     assert extra == norms + residuals - x_saved
+
+
+def test_fused_qwen_bf16_step_streams_the_same_weights():
+    """Gate and up stored as one [Wgate; Wup] matrix: the same weight bytes and
+    parameters in 113 GEMVs instead of 141."""
+    plain, fused = wl.qwen25_7b_step(), wl.qwen25_7b_step(fused=True)
+    assert len(plain) == 141 and len(fused) == 113
+    assert wl.step_weight_bytes(plain, wl.FMT_BF16) == wl.step_weight_bytes(fused, wl.FMT_BF16)
+    assert wl.step_params(plain) == wl.step_params(fused)
+    assert sum(m.N for m in fused if m.name.endswith("gate_up")) == 28 * 2 * 18944
