@@ -194,7 +194,9 @@ mbw_status gemm_skinny_bf16(const void *X, const void *W, void *Y, int64_t M, in
  * quantization"): w_ik = scales[i] * Wq[i][k], codes in [-127, 127]. The
  * kernel multiplies the codes in (exactly, as bf16 on the tensor core, fp32
  * accumulation) and applies the row's scale once to the finished sum. M = 1
- * is the decode GEMV; batches above 8 run in slices of 8 rows.
+ * is the decode GEMV; batches up to 8 run on the streaming GEMV kernels, and
+ * batches above 8 on a batched mma.sync kernel that reads every weight once
+ * per launch of 16, 32 or 64 rows.
  *   Wq     : int8 [N][K]     scales : fp32 [N]
  *   X      : bf16 [M][K]     Y      : bf16 [M][N] (fp32 under the fp32 hook)
  *   Requires K % 128 == 0. `scales` needs 4-byte alignment. The code -128 is

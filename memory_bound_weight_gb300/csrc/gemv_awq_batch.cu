@@ -1,6 +1,6 @@
 // gemv_awq_batch.cu -- AWQ-style INT4 (group 128) product for a batch of
-// 5 .. 64 activation rows on the mma.sync tensor-core path, every weight read
-// once per launch.
+// 5 .. 64 activation rows, and the symmetric INT8 one for 9 .. 64, on the
+// mma.sync tensor-core path, every weight read once per launch.
 //
 // Y[m][i] = sum_g s[i][g] * sum_{k in g} (q[i][k] - z[i][g]) * X[m][k]
 // (llm-rs vs vLLM, sec. 6 format table: 4-bit codes with an fp16 scale and a
@@ -42,6 +42,15 @@
 // bf16 pair 128 + z gives n - z exactly; (n - z) * x is exact in fp32 and the
 // tensor core accumulates in fp32; the group scale multiplies the group's fp32
 // sum once.
+//
+// Symmetric INT8 with one fp32 scale per output channel (TileInfer, "Pushing
+// further with cheating: INT8 quantization") runs through the same skeleton
+// at batches above the INT8 GEMVs' 8 rows: a 128-byte super-block of a row is
+// 128 codes (128 k), the lane's 16-byte chunks of rows g and g+8 become exact
+// bf16 pairs (i8_pairs: codes 0, 2 and 1, 3 of each word), X is staged with
+// the matching pair permutation (perm_i8) at an odd row pitch, the MMAs
+// accumulate over the warp's whole k-range, and the row's scale multiplies the
+// finished sum once in the store.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -99,21 +108,25 @@ struct AwqbSmem {
     size_t red_off, fin_off, ring_off, stab_off, ztab_off, total;
 };
 
-__host__ __device__ inline AwqbSmem awqb_smem_layout(int64_t K, int64_t N, int Mp, int W, int WK, int U, int async,
-                                                     int S, int G) {
+__host__ __device__ inline AwqbSmem awqb_smem_layout(int fmt, int64_t K, int64_t N, int Mp, int W, int WK, int U,
+                                                     int async, int S, int G) {
     AwqbSmem L;
-    const int KB = (int)(K / 256);
+    const bool i8 = fmt == FMT_I8;
+    const int KB = (int)(K / (i8 ? 128 : 256));
     L.kbr = (KB + S - 1) / S;
-    L.pitch = L.kbr * 32 + 4;
+    // INT8: 16 chunks per super-block and an odd pitch (each 8-lane phase of a
+    // B-fragment read then covers 8 bank groups)
+    L.pitch = i8 ? L.kbr * 16 + 1 : L.kbr * 32 + 4;
     const int64_t T = (N + 15) / 16;
     L.ntmax = (int)((T + G - 1) / G);
     L.red_off = (size_t)Mp * L.pitch * 16;
     const size_t red = (WK > 1 || S > 1) ? (size_t)L.ntmax * WK * 16 * Mp * 4 : 0;
     L.fin_off = L.red_off + red;
     L.ring_off = L.fin_off + ((WK > 1 && S > 1) ? (size_t)L.ntmax * 16 * Mp * 4 : 0);
+    const bool tabs = async && !i8;  // AWQ scale and zero-point tables
     L.stab_off = L.ring_off + (async ? (size_t)W * U * 2048 : 0);
-    L.ztab_off = L.stab_off + (async ? (size_t)L.ntmax * 16 * 2 * L.kbr * 2 : 0);
-    L.total = L.ztab_off + (async ? ((size_t)L.ntmax * 16 * L.kbr + 15) / 16 * 16 : 0);
+    L.ztab_off = L.stab_off + (tabs ? (size_t)L.ntmax * 16 * 2 * L.kbr * 2 : 0);
+    L.total = L.ztab_off + (tabs ? ((size_t)L.ntmax * 16 * L.kbr + 15) / 16 * 16 : 0);
     return L;
 }
 
@@ -126,8 +139,10 @@ __host__ __device__ inline AwqbSmem awqb_smem_layout(int64_t K, int64_t N, int M
 // cp.async copies (a quad's four copies of a row's group are one 64-byte run:
 // whole sectors), U slots deep per warp, refilled after its super-block is
 // computed; scales and zero points come from per-CTA tables loaded once.
-template <int NB, int WT, int WK, int U, int MINB, int EARLY, int ASYNC>
+template <int FMT, int NB, int WT, int WK, int U, int MINB, int EARLY, int ASYNC>
 __global__ void __launch_bounds__(WT * WK * 32, MINB) gemv_awq_batch_kernel(const GemvArgs a, const int S) {
+    constexpr bool I8 = (FMT == FMT_I8);
+    constexpr int BKS = I8 ? 128 : 256;  // k per 128-byte row super-block
     constexpr int W = WT * WK;
     constexpr int MP = 8 * NB;  // batch rows of the launch, padded
     extern __shared__ uint4 smem_u4[];
@@ -143,17 +158,17 @@ __global__ void __launch_bounds__(WT * WK * 32, MINB) gemv_awq_batch_kernel(cons
     const int T = (a.N + 15) / 16;
     const int t0 = (int)(((long long)T * cgid) / G);
     const int nt = (int)(((long long)T * (cgid + 1)) / G) - t0;
-    const AwqbSmem L = awqb_smem_layout(a.K, a.N, MP, W, WK, U, ASYNC, S, G);
+    const AwqbSmem L = awqb_smem_layout(FMT, a.K, a.N, MP, W, WK, U, ASYNC, S, G);
 
     // super-blocks of this cluster rank, then of this warp's k-slice (may be none)
-    const int KB = a.K / 256;
+    const int KB = a.K / BKS;
     const int kb0 = (int)(((long long)KB * rank) / S);
     const int nkb = (int)(((long long)KB * (rank + 1)) / S) - kb0;
     const int wb0 = kb0 + (nkb * wk) / WK;
     const int nbw = kb0 + (nkb * (wk + 1)) / WK - wb0;
     const int ntw = (nt > wt) ? (nt - wt + WT - 1) / WT : 0;  // tiles of this warp
     const int total = ntw * nbw;
-    const size_t rowbytes = (size_t)a.K / 2;
+    const size_t rowbytes = I8 ? (size_t)a.K : (size_t)a.K / 2;
 
     // load cursor: rows g and g + 8 of the tile being loaded, as 32-bit offsets
     // from the matrix (code bytes, scale and zero-point entries; the launch
@@ -196,9 +211,11 @@ __global__ void __launch_bounds__(WT * WK * 32, MINB) gemv_awq_batch_kernel(cons
         rc[u][1] = ld_stream16(a.W + wo0 + 64);
         rc[u][2] = ld_stream16(a.W + wo1);
         rc[u][3] = ld_stream16(a.W + wo1 + 64);
-        rs[u][0] = (uint32_t)ld_ro_u16(a.scales + so0) | ((uint32_t)ld_ro_u16(a.scales + so0 + 1) << 16);
-        rs[u][1] = (uint32_t)ld_ro_u16(a.scales + so1) | ((uint32_t)ld_ro_u16(a.scales + so1 + 1) << 16);
-        rz[u] = (uint32_t)ld_ro_u8(a.zeros + zo0) | ((uint32_t)ld_ro_u8(a.zeros + zo1) << 8);
+        if (!I8) {
+            rs[u][0] = (uint32_t)ld_ro_u16(a.scales + so0) | ((uint32_t)ld_ro_u16(a.scales + so0 + 1) << 16);
+            rs[u][1] = (uint32_t)ld_ro_u16(a.scales + so1) | ((uint32_t)ld_ro_u16(a.scales + so1 + 1) << 16);
+            rz[u] = (uint32_t)ld_ro_u8(a.zeros + zo0) | ((uint32_t)ld_ro_u8(a.zeros + zo1) << 8);
+        }
         wo0 += 128;
         wo1 += 128;
         so0 += 2;
@@ -217,7 +234,7 @@ __global__ void __launch_bounds__(WT * WK * 32, MINB) gemv_awq_batch_kernel(cons
     }
     uint16_t* stab = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(smem_u4) + L.stab_off);
     uint8_t* ztab = reinterpret_cast<uint8_t*>(smem_u4) + L.ztab_off;
-    if (ASYNC) {
+    if (ASYNC && !I8) {
         // the CTA's scales (2 per super-block) and zero-point bytes (1 per
         // super-block) of its rows and this rank's super-blocks; weights-side
         // data, read before the wait
@@ -234,58 +251,95 @@ __global__ void __launch_bounds__(WT * WK * 32, MINB) gemv_awq_batch_kernel(cons
     prefetch_l2_grid_share(a.x, (size_t)a.M * a.K * 2);
     pdl_wait();
 
-    // Stage X[:, kb0*256 .. (kb0 + nkb)*256) for MP rows (zeros past M):
-    // logical chunk c of a super-block = 16 h + 4 q' + w' goes to 16 h + 4 w' + q'.
+    // Stage X[:, kb0*BKS .. (kb0 + nkb)*BKS) for MP rows (zeros past M).
+    // AWQ: logical chunk c of a super-block = 16 h + 4 q' + w' goes to 16 h + 4 w' + q'.
+    // INT8: chunks in order, each 8-x chunk as the pairs (0,2) (1,3) (4,6) (5,7).
     uint4* xs = smem_u4;
-    const int cpr = nkb * 32;  // chunks per row
+    const int cpr = nkb * (BKS / 8);  // chunks per row
     for (int i = threadIdx.x; i < MP * cpr; i += W * 32) {
         const int m = i / cpr, c = i - m * cpr;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (m < a.M) {
-            v = ld_ro16(a.x + (size_t)m * a.K + (size_t)kb0 * 256 + (size_t)c * 8);
-            if (!a.x_natural) v = awqb_perm(v);
+            v = ld_ro16(a.x + (size_t)m * a.K + (size_t)kb0 * BKS + (size_t)c * 8);
+            if (I8)
+                v = perm_i8(v);
+            else if (!a.x_natural)
+                v = awqb_perm(v);
         }
-        const int c32 = c & 31;
-        const int phys = (c & ~31) | (c32 & 16) | ((c32 & 3) << 2) | ((c32 >> 2) & 3);
+        int phys = c;
+        if (!I8) {
+            const int c32 = c & 31;
+            phys = (c & ~31) | (c32 & 16) | ((c32 & 3) << 2) | ((c32 >> 2) & 3);
+        }
         xs[(size_t)m * L.pitch + phys] = v;
     }
     __syncthreads();
 
     float* red = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + L.red_off);
     float* fin = reinterpret_cast<float*>(reinterpret_cast<char*>(smem_u4) + ((WK > 1) ? L.fin_off : L.red_off));
-    // B fragments of this lane: batch row 8 nb + g, chunk 4 w' + q of each group
-    const uint4* xl = xs + (size_t)g * L.pitch + q + (size_t)(wb0 - kb0) * 32;
+    // B fragments of this lane: batch row 8 nb + g; AWQ: chunk 4 w' + q of each
+    // group; INT8: chunks 2q, 2q + 1 of each 64-byte half of the super-block
+    const uint4* xl = I8 ? xs + (size_t)g * L.pitch + 2 * q + (size_t)(wb0 - kb0) * 16
+                         : xs + (size_t)g * L.pitch + q + (size_t)(wb0 - kb0) * 32;
 
     float acc[NB][4];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
+    float acc1[1][4] = {{0.f, 0.f, 0.f, 0.f}};  // INT8 at one n-block: a second accumulator chain
     int j = 0, lt2 = 0;
     for (int s0 = 0; s0 < total; s0 += U) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (s0 + u < total) {
-                const uint4* xb = xl + j * 32;
+                const uint4* xb = xl + j * (BKS / 8);
                 uint4 cw[4];
                 uint32_t cs[2], cz;
                 if (ASYNC) {
                     cp_async_wait<U - 1>();  // this lane's copies of the step have landed
 #pragma unroll
                     for (int e = 0; e < 4; ++e) cw[e] = *reinterpret_cast<const uint4*>(aring + (size_t)(u * 4 + e) * 512);
-                    const int tr = (wt + lt2 * WT) * 16, sbl = wb0 - kb0 + j;
-                    cs[0] = *reinterpret_cast<const uint32_t*>(stab + ((size_t)(tr + g) * L.kbr + sbl) * 2);
-                    cs[1] = *reinterpret_cast<const uint32_t*>(stab + ((size_t)(tr + g + 8) * L.kbr + sbl) * 2);
-                    cz = (uint32_t)ztab[(size_t)(tr + g) * L.kbr + sbl] |
-                         ((uint32_t)ztab[(size_t)(tr + g + 8) * L.kbr + sbl] << 8);
+                    cs[0] = cs[1] = cz = 0;
+                    if (!I8) {
+                        const int tr = (wt + lt2 * WT) * 16, sbl = wb0 - kb0 + j;
+                        cs[0] = *reinterpret_cast<const uint32_t*>(stab + ((size_t)(tr + g) * L.kbr + sbl) * 2);
+                        cs[1] = *reinterpret_cast<const uint32_t*>(stab + ((size_t)(tr + g + 8) * L.kbr + sbl) * 2);
+                        cz = (uint32_t)ztab[(size_t)(tr + g) * L.kbr + sbl] |
+                             ((uint32_t)ztab[(size_t)(tr + g + 8) * L.kbr + sbl] << 8);
+                    }
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) cw[e] = rc[u][e];
-                    cs[0] = rs[u][0];
-                    cs[1] = rs[u][1];
-                    cz = rz[u];
+                    cs[0] = I8 ? 0u : rs[u][0];
+                    cs[1] = I8 ? 0u : rs[u][1];
+                    cz = I8 ? 0u : rz[u];
                     if (EARLY && s0 + u + U < total) load(u);
                 }
+                if (I8) {
+                    // word w of a lane's 16-byte chunk holds codes k0 .. k0 + 3: its pairs (0,2), (1,3)
+                    // meet the x pairs of the chunk's half (w & 1) of staged chunk 2q + (w >> 1)
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t wa[4] = {cw[h].x, cw[h].y, cw[h].z, cw[h].w};
+                        const uint32_t wb[4] = {cw[2 + h].x, cw[2 + h].y, cw[2 + h].z, cw[2 + h].w};
+#pragma unroll
+                        for (int wp = 0; wp < 2; ++wp) {
+                            uint32_t a02[2], a13[2], b02[2], b13[2];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                i8_pairs(wa[2 * wp + e], a02[e], a13[e]);
+                                i8_pairs(wb[2 * wp + e], b02[e], b13[e]);
+                            }
+#pragma unroll
+                            for (int nb = 0; nb < NB; ++nb) {
+                                const uint4 xv = xb[(size_t)nb * 8 * L.pitch + h * 8 + wp];
+                                awqb_mma(acc[nb], a02[0], b02[0], a13[0], b13[0], xv.x, xv.y);
+                                awqb_mma(NB == 1 ? acc1[0] : acc[nb], a02[1], b02[1], a13[1], b13[1], xv.z, xv.w);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2 && !I8; ++h) {
                     const uint32_t zb = cz;
                     const uint32_t zz0 = (0x4300u | ((zb >> (4 * h)) & 0xF)) * 0x00010001u;
                     const uint32_t zz1 = (0x4300u | ((zb >> (8 + 4 * h)) & 0xF)) * 0x00010001u;
@@ -335,20 +389,35 @@ __global__ void __launch_bounds__(WT * WK * 32, MINB) gemv_awq_batch_kernel(cons
                     // cluster) or keep the partial for the sums after the loop
                     const int t = wt + lt2 * WT;
                     const int row0 = (t0 + t) * 16;
+                    if (I8 && NB == 1) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            acc[0][e] += acc1[0][e];
+                            acc1[0][e] = 0.f;
+                        }
+                    }
+                    // INT8: the row scales of rows g and g + 8 (applied once, to the finished sum)
+                    float sg = 1.f, sg8 = 1.f;
+                    if (I8 && WK == 1 && S == 1) {
+                        sg = __ldg(a.rscale + min(row0 + g, a.N - 1));
+                        sg8 = __ldg(a.rscale + min(row0 + g + 8, a.N - 1));
+                    }
 #pragma unroll
                     for (int nb = 0; nb < NB; ++nb) {
                         const int m = 8 * nb + 2 * q;
                         if (WK == 1 && S == 1) {
                             if (m < a.M) {
-                                if (row0 + g < a.N) store_out(a.y, (int64_t)m * a.N + row0 + g, acc[nb][0], a.out_f32);
+                                if (row0 + g < a.N)
+                                    store_out(a.y, (int64_t)m * a.N + row0 + g, acc[nb][0] * sg, a.out_f32);
                                 if (row0 + g + 8 < a.N)
-                                    store_out(a.y, (int64_t)m * a.N + row0 + g + 8, acc[nb][2], a.out_f32);
+                                    store_out(a.y, (int64_t)m * a.N + row0 + g + 8, acc[nb][2] * sg8, a.out_f32);
                             }
                             if (m + 1 < a.M) {
                                 if (row0 + g < a.N)
-                                    store_out(a.y, (int64_t)(m + 1) * a.N + row0 + g, acc[nb][1], a.out_f32);
+                                    store_out(a.y, (int64_t)(m + 1) * a.N + row0 + g, acc[nb][1] * sg, a.out_f32);
                                 if (row0 + g + 8 < a.N)
-                                    store_out(a.y, (int64_t)(m + 1) * a.N + row0 + g + 8, acc[nb][3], a.out_f32);
+                                    store_out(a.y, (int64_t)(m + 1) * a.N + row0 + g + 8, acc[nb][3] * sg8,
+                                              a.out_f32);
                             }
                         } else {
                             float* rp = red + ((size_t)(t * WK + wk) * 16) * MP;
@@ -384,7 +453,7 @@ __global__ void __launch_bounds__(WT * WK * 32, MINB) gemv_awq_batch_kernel(cons
             for (int k2 = 0; k2 < WK; ++k2) v += red[((size_t)(t * WK + k2) * 16 + r) * MP + m];
             const int row = (t0 + t) * 16 + r;
             if (S == 1) {
-                if (row < a.N) store_out(a.y, (int64_t)m * a.N + row, v, a.out_f32);
+                if (row < a.N) store_out(a.y, (int64_t)m * a.N + row, I8 ? v * __ldg(a.rscale + row) : v, a.out_f32);
             } else {
                 fin[((size_t)t * 16 + r) * MP + m] = v;
             }
@@ -404,7 +473,7 @@ __global__ void __launch_bounds__(WT * WK * 32, MINB) gemv_awq_batch_kernel(cons
         float v = 0.f;
         for (int s = 0; s < S; ++s) v += *cluster.map_shared_rank(fin + (size_t)lr * MP + m, s);
         const int row = t0 * 16 + lr;
-        if (row < a.N) store_out(a.y, (int64_t)m * a.N + row, v, a.out_f32);
+        if (row < a.N) store_out(a.y, (int64_t)m * a.N + row, I8 ? v * __ldg(a.rscale + row) : v, a.out_f32);
     }
     cluster.sync();
 }
@@ -418,15 +487,21 @@ struct AwqbEntry {
 // WT x WK warps; MINB: CTAs per SM the instantiation is register-bounded for
 // (128 registers per thread at 16 warps per SM; up to 255 with fewer);
 // EARLY: refill before the compute; ASYNC: shared-memory ring (see the kernel)
-#define MBW_AB(NB, WT, WK, U, MINB, EARLY, ASYNC) \
-    { {NB, WT, WK, U, MINB, EARLY, ASYNC}, gemv_awq_batch_kernel<NB, WT, WK, U, MINB, EARLY, ASYNC> }
+#define MBW_AB(F, NB, WT, WK, U, MINB, EARLY, ASYNC) \
+    { {NB, WT, WK, U, MINB, EARLY, ASYNC, F}, gemv_awq_batch_kernel<F, NB, WT, WK, U, MINB, EARLY, ASYNC> }
 static const AwqbEntry kAwqb[] = {
-    MBW_AB(1, 8, 1, 3, 2, 0, 0), MBW_AB(1, 8, 2, 3, 1, 0, 0), MBW_AB(1, 8, 2, 2, 1, 1, 0), MBW_AB(1, 8, 1, 5, 1, 1, 0),
-    MBW_AB(1, 8, 2, 4, 1, 0, 1), MBW_AB(1, 8, 1, 6, 2, 0, 1), MBW_AB(2, 8, 2, 2, 1, 0, 0), MBW_AB(2, 8, 2, 2, 1, 1, 0),
-    MBW_AB(2, 8, 1, 4, 1, 1, 0), MBW_AB(2, 8, 1, 6, 1, 0, 0), MBW_AB(2, 4, 2, 4, 1, 1, 0), MBW_AB(2, 8, 2, 4, 1, 0, 1),
-    MBW_AB(2, 8, 2, 6, 1, 0, 1), MBW_AB(2, 8, 1, 8, 2, 0, 1), MBW_AB(4, 8, 1, 2, 1, 0, 0), MBW_AB(4, 8, 1, 3, 1, 1, 0),
-    MBW_AB(4, 4, 2, 3, 1, 1, 0), MBW_AB(4, 8, 2, 4, 1, 0, 1), MBW_AB(4, 8, 1, 6, 1, 0, 1), MBW_AB(8, 8, 1, 2, 1, 0, 0),
-    MBW_AB(8, 8, 1, 4, 1, 0, 1),
+    MBW_AB(FMT_AWQ, 1, 8, 1, 3, 2, 0, 0), MBW_AB(FMT_AWQ, 1, 8, 2, 3, 1, 0, 0), MBW_AB(FMT_AWQ, 1, 8, 2, 2, 1, 1, 0),
+    MBW_AB(FMT_AWQ, 1, 8, 1, 5, 1, 1, 0), MBW_AB(FMT_AWQ, 1, 8, 2, 4, 1, 0, 1), MBW_AB(FMT_AWQ, 1, 8, 1, 6, 2, 0, 1),
+    MBW_AB(FMT_AWQ, 2, 8, 2, 2, 1, 0, 0), MBW_AB(FMT_AWQ, 2, 8, 2, 2, 1, 1, 0), MBW_AB(FMT_AWQ, 2, 8, 1, 4, 1, 1, 0),
+    MBW_AB(FMT_AWQ, 2, 8, 1, 6, 1, 0, 0), MBW_AB(FMT_AWQ, 2, 4, 2, 4, 1, 1, 0), MBW_AB(FMT_AWQ, 2, 8, 2, 4, 1, 0, 1),
+    MBW_AB(FMT_AWQ, 2, 8, 2, 6, 1, 0, 1), MBW_AB(FMT_AWQ, 2, 8, 1, 8, 2, 0, 1), MBW_AB(FMT_AWQ, 4, 8, 1, 2, 1, 0, 0),
+    MBW_AB(FMT_AWQ, 4, 8, 1, 3, 1, 1, 0), MBW_AB(FMT_AWQ, 4, 4, 2, 3, 1, 1, 0), MBW_AB(FMT_AWQ, 4, 8, 2, 4, 1, 0, 1),
+    MBW_AB(FMT_AWQ, 4, 8, 1, 6, 1, 0, 1), MBW_AB(FMT_AWQ, 8, 8, 1, 2, 1, 0, 0), MBW_AB(FMT_AWQ, 8, 8, 1, 4, 1, 0, 1),
+    // INT8 at batches above 8 (9 .. 64 rows per launch)
+    MBW_AB(FMT_I8, 2, 8, 1, 4, 1, 0, 0), MBW_AB(FMT_I8, 2, 8, 2, 2, 1, 1, 0), MBW_AB(FMT_I8, 2, 8, 2, 4, 1, 0, 1),
+    MBW_AB(FMT_I8, 2, 8, 1, 6, 2, 0, 1), MBW_AB(FMT_I8, 4, 8, 1, 3, 1, 0, 0), MBW_AB(FMT_I8, 4, 8, 2, 2, 1, 1, 0),
+    MBW_AB(FMT_I8, 4, 8, 2, 4, 1, 0, 1), MBW_AB(FMT_I8, 8, 8, 1, 2, 1, 0, 0), MBW_AB(FMT_I8, 8, 8, 1, 4, 1, 0, 1),
+    MBW_AB(FMT_I8, 8, 4, 2, 3, 1, 0, 1),
 };
 #undef MBW_AB
 
@@ -439,20 +514,23 @@ AwqbConfig awqb_config(int idx) { return kAwqb[idx].cfg; }
 int awqb_row_groups(const AwqbConfig& c, int64_t N, int64_t K, int split, int occ) {
     const size_t limit = std::min(kSmemFit, (size_t)227 * 1024 / occ);
     return fitted_row_groups(N, split, occ, limit, [&](int G) {
-        return awqb_smem_layout(K, N, 8 * c.nb, c.wt * c.wk, c.wk, c.u, c.async, split, G).total;
+        return awqb_smem_layout(c.fmt, K, N, 8 * c.nb, c.wt * c.wk, c.wk, c.u, c.async, split, G).total;
     });
 }
 
 size_t awqb_smem_bytes(const AwqbConfig& c, int64_t N, int64_t K, int split, int occ) {
     const int G = awqb_row_groups(c, N, K, split, occ);
-    return awqb_smem_layout(K, N, 8 * c.nb, c.wt * c.wk, c.wk, c.u, c.async, split, G).total;
+    return awqb_smem_layout(c.fmt, K, N, 8 * c.nb, c.wt * c.wk, c.wk, c.u, c.async, split, G).total;
 }
 
 cudaError_t launch_gemv_awq_batch(const Plan& p, const GemvArgs& a, cudaStream_t s) {
     if (p.cfg < 0 || p.cfg >= awqb_num_configs()) return cudaErrorInvalidValue;
     const AwqbEntry& e = kAwqb[p.cfg];
-    if (a.M < 1 || a.M > 8 * e.cfg.nb || a.K % 256 != 0) return cudaErrorInvalidValue;
-    if ((uint64_t)a.N * (uint64_t)(a.K / 2) > 0xFFFFFFFFull) return cudaErrorInvalidValue;  // 32-bit offsets
+    const bool i8 = e.cfg.fmt == FMT_I8;
+    if (a.M < 1 || a.M > 8 * e.cfg.nb || a.K % (i8 ? 128 : 256) != 0) return cudaErrorInvalidValue;
+    if (i8 && !a.rscale) return cudaErrorInvalidValue;
+    const uint64_t rowbytes = i8 ? (uint64_t)a.K : (uint64_t)(a.K / 2);
+    if ((uint64_t)a.N * rowbytes > 0xFFFFFFFFull) return cudaErrorInvalidValue;  // 32-bit offsets
     const int G = awqb_row_groups(e.cfg, a.N, a.K, p.split, p.occ);
     const size_t smem = awqb_smem_bytes(e.cfg, a.N, a.K, p.split, p.occ);
     if (smem > 48 * 1024) {

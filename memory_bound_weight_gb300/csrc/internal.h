@@ -109,6 +109,7 @@ struct AwqbConfig {
     int minb;  // CTAs per SM its register budget allows (at most this many per SM)
     int early; // 1: a ring slot is refilled before its super-block is computed
     int async; // 1: the ring is in shared memory (cp.async), scales and zero points in per-CTA tables
+    int fmt;   // FMT_AWQ, or FMT_I8 (symmetric INT8 with a per-row scale, batches above 8)
 };
 
 // Execution plan of one call shape.

@@ -63,6 +63,7 @@ static int awqb_want_nb(int64_t M) {
 static int batch_key(int op, int64_t M) {
     if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 8) return tc_batch_tile(M);
     if ((op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4) return 1000 + 8 * awqb_want_nb(M);
+    if ((op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT8_PC && M > 8) return 1000 + 8 * awqb_want_nb(M);
     return (int)std::min<int64_t>(M, 8);
 }
 
@@ -114,16 +115,20 @@ static bool plan_valid(int fmt, const Plan& p, int64_t M, int64_t N, int64_t K, 
     if (p.kind == PLAN_AWQB) {
         // batched AWQ on mma.sync: batches above the GEMV column width, whole
         // super-blocks of 256 k, at least one per cluster rank
-        if (fmt != FMT_AWQ || M <= 4 || p.cfg < 0 || p.cfg >= awqb_num_configs()) return false;
+        // (INT8: batches above the INT8 GEMVs' 8 rows, whole 128-k super-blocks)
+        if ((fmt != FMT_AWQ && fmt != FMT_I8) || p.cfg < 0 || p.cfg >= awqb_num_configs()) return false;
+        if (M <= (fmt == FMT_I8 ? 8 : 4)) return false;
         const AwqbConfig c = awqb_config(p.cfg);
+        if (c.fmt != fmt) return false;
+        const int64_t bks = (fmt == FMT_I8) ? 128 : 256;
         // the fewest n-blocks covering the batch, or down to a quarter of them
         // in slices (each slice streams the weights again; past 16 rows the
         // kernel is bound by the MMA rate rather than the weight stream, and
         // narrower slices stage less of X in shared memory)
         const int want = awqb_want_nb(M);
         if (c.nb > want || 4 * c.nb < want) return false;
-        if (K % 256 != 0 || p.occ < 1 || p.occ > c.minb || K / 256 < p.split) return false;
-        if ((uint64_t)N * (uint64_t)(K / 2) > 0xFFFFFFFFull) return false;  // 32-bit load offsets
+        if (K % bks != 0 || p.occ < 1 || p.occ > c.minb || K / bks < p.split) return false;
+        if ((uint64_t)N * (uint64_t)(fmt == FMT_I8 ? K : K / 2) > 0xFFFFFFFFull) return false;  // 32-bit offsets
         const size_t sm = awqb_smem_bytes(c, N, K, p.split, p.occ);
         return sm <= kSmemLimit && sm * p.occ <= (size_t)227 * 1024;
     }
@@ -223,6 +228,13 @@ static std::vector<Plan> candidates(int op, int64_t M, int64_t N, int64_t K) {
                     if (plan_valid(fmt, p, M, N, K, flags)) out.push_back(p);
                 }
     }
+    if ((op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT8_PC && M > 8)
+        for (int cfg = 0; cfg < awqb_num_configs(); ++cfg)
+            for (int sp = 1; sp <= 8; sp *= 2)
+                for (int occ = 1; occ <= 2; ++occ) {
+                    Plan p{PLAN_AWQB, cfg, sp, occ};
+                    if (plan_valid(fmt, p, M, N, K, flags)) out.push_back(p);
+                }
     if (op == MBW_OP_GEMM_SKINNY_BF16 && M > 4)
         for (int cfg = 0; cfg <= 7; ++cfg)
             for (int sp = 1; sp <= 8; ++sp) {
@@ -280,18 +292,21 @@ static Plan plan_heuristic(int op, int64_t M, int64_t N, int64_t K) {
     const int fuse = op & MBW_FUSE_MASK;
     const int64_t Mb = std::min<int64_t>(M, 8);
     const int sms = device_sm_count();
-    if ((op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4) {
-        // batched AWQ on mma.sync: 8 warps, 2 super-blocks in flight; split K
-        // over a cluster while the 16-row tiles do not cover the SMs
+    const bool awq_batch = (op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT4_AWQ_G128 && M > 4;
+    const bool i8_batch = (op & MBW_OP_BASE_MASK) == MBW_OP_GEMV_INT8_PC && M > 8 && !fuse;
+    if (awq_batch || i8_batch) {
+        // batched AWQ / INT8 on mma.sync: 8 warps; split K over a cluster
+        // while the 16-row tiles do not cover the SMs or X does not fit
         const int want = awqb_want_nb(M);
+        const int bks = i8_batch ? 128 : 256;
         for (int i = 0; i < awqb_num_configs(); ++i) {
             const AwqbConfig c = awqb_config(i);
-            if (c.nb != want || c.wt * c.wk != 8) continue;
+            if (c.fmt != fmt || c.nb != want || c.wt * c.wk != 8) continue;
             const int64_t tiles = (N + 15) / 16;
             for (int occ = c.minb; occ >= 1; --occ) {
                 // split while the tiles do not cover the SMs or X does not fit
                 Plan p{PLAN_AWQB, i, 1, occ};
-                while (p.split < 8 && K / 256 / (2 * p.split) >= c.wk &&
+                while (p.split < 8 && K / bks / (2 * p.split) >= c.wk &&
                        (tiles * p.split < (int64_t)sms * occ || !plan_valid(fmt, p, M, N, K, flags)))
                     p.split *= 2;
                 if (plan_valid(fmt, p, M, N, K, flags)) return p;
@@ -390,9 +405,9 @@ std::string plan_to_string(int op, const Plan& p) {
     if (p.kind == PLAN_AWQB) {
         const AwqbConfig c = awqb_config(p.cfg);
         snprintf(buf, sizeof(buf),
-                 "awq_mma fmt=%s batch_cols=%d warps=%d (tiles %d x k %d) superblocks_in_flight=%d ring=%s "
+                 "%s fmt=%s batch_cols=%d warps=%d (tiles %d x k %d) superblocks_in_flight=%d ring=%s "
                  "ctas_per_sm=%d split_k=%d",
-                 fs, 8 * c.nb, c.wt * c.wk, c.wt, c.wk, c.u,
+                 c.fmt == FMT_I8 ? "int8_mma" : "awq_mma", fs, 8 * c.nb, c.wt * c.wk, c.wt, c.wk, c.u,
                  c.async ? "smem" : c.early ? "registers refill=early" : "registers refill=late", p.occ, p.split);
     } else if (p.kind == PLAN_TC) {
         if (fmt == FMT_AWQ)

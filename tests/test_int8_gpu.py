@@ -72,6 +72,59 @@ def test_int8_all_plans(orc, N, K, M):
         assert "mma2" in families
 
 
+@pytest.mark.parametrize("N,K,M", [(40, 256, 12), (257, 1024, 16), (130, 2560, 17), (300, 1280, 33), (64, 640, 64),
+                                   (33, 9728, 40), (520, 512, 100), (16, 128, 9)])
+def test_int8_batched_every_plan(orc, N, K, M):
+    """Batches above 8: every plan, the batched mma.sync family (one launch
+    per 16 .. 64 rows, every weight read once per launch) among them, against
+    the oracle; fp32 output leaves only accumulation rounding."""
+    q, s, X = int8_case(1300 + N + M, N, K, M)
+    Y, A = orc.gemm_int8_pc(q, s, X)
+    qd, sd, Xd = dev_i8(q), dev_f32(s), dev_bf16(X)
+    families = set()
+    for i, desc in each_plan(M, N, K):
+        families.add(desc.split()[0])
+        assert_parity(mbw.gemv_int8_pc(qd, sd, Xd), Y, A, f"int8 {M}x{N}x{K} plan {desc}")
+        with mbw.output_fp32():
+            y32 = mbw.gemv_int8_pc(qd, sd, Xd)
+        err = np.abs(host_f64(y32) - Y)
+        assert np.all(err <= 1e-4 * A + 1e-7), (desc, float(err.max()))
+    assert "int8_mma" in families
+
+
+def test_int8_batched_deterministic_and_default_plan(orc):
+    """The built-in plan of a batch above 8 is the batched family; two calls
+    give bitwise the same output."""
+    N, K, M = 1000, 2560, 24
+    q, s, X = int8_case(1400, N, K, M)
+    qd, sd, Xd = dev_i8(q), dev_f32(s), dev_bf16(X)
+    assert mbw.plan_describe(OP, M, N, K).startswith("int8_mma")
+    y1, y2 = mbw.gemv_int8_pc(qd, sd, Xd), mbw.gemv_int8_pc(qd, sd, Xd)
+    assert torch.equal(y1, y2)
+    Y, A = orc.gemm_int8_pc(q, s, X)
+    assert_parity(y1, Y, A, "int8 M=24 default plan")
+
+
+@pytest.mark.parametrize("M", [16, 64])
+@pytest.mark.parametrize("N,K", [(6144, 2560), (19456, 2560), (2560, 9728)])
+def test_int8_batched_every_plan_at_qwen3_4b_shapes(orc, N, K, M):
+    """Every plan at batch 16 and 64 on the Qwen3-4B shapes, then the autotuned
+    plan; sampled rows, every batch row."""
+    rows = np.unique(np.concatenate([np.arange(0, 16), np.arange(N - 16, N),
+                                     np.random.default_rng(N + K + M).integers(0, N, 48)]))
+    qd = inputs_gpu.int8_codes(0, 60, N, K)
+    sd = inputs_gpu.f32_row_scales(0, 60, N)
+    Xd = inputs_gpu.bf16_activations(0, 61, M, K)
+    q = np.stack([gen.int8_codes(0, 60, N, K, row0=int(r), rows=1)[0] for r in rows])
+    s = np.concatenate([gen.f32_row_scales(0, 60, N, row0=int(r), rows=1) for r in rows])
+    Y, A = orc.gemm_int8_pc(q, s, host_bits16(Xd))
+    sel = torch.from_numpy(rows).cuda()
+    for _, desc in each_plan(M, N, K):
+        assert_parity(mbw.gemv_int8_pc(qd, sd, Xd)[:, sel], Y, A, f"int8 M={M} {N}x{K} plan {desc}")
+    mbw.autotune(OP, M, N, K)
+    assert_parity(mbw.gemv_int8_pc(qd, sd, Xd)[:, sel], Y, A, f"int8 M={M} {N}x{K} autotuned")
+
+
 def test_int8_every_byte_value_exact(orc):
     """Codes q[i][k] = ((i + k) mod 256) - 128 cover all 256 byte values in
     every column; x = one-hot rows, scale 1: with fp32 output each batch row
