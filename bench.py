@@ -76,8 +76,8 @@ def parse_args():
     p.add_argument("--impl", default="mbw", choices=["mbw", "reference"])
     p.add_argument("--workload", default="qwen_bf16",
                    choices=["tinyllama_int4", "tinyllama_int4_fusedops", "tinyllama_int4_unfused", "qwen_bf16",
-                            "qwen_bf16_fused", "qwen_awq", "qwen_awq_repacked", "qwen_awq_fusedops", "qwen3_int8",
-                            "bf16_2048"])
+                            "qwen_bf16_fused", "qwen_awq", "qwen_awq_repacked", "qwen_awq_repacked_fused",
+                            "qwen_awq_fusedops", "qwen3_int8", "bf16_2048"])
     p.add_argument("--batch", type=int, default=1,
                    help="activation rows per GEMV (qwen_awq: AWQ-style INT4 decode at batch M)")
     p.add_argument("--no-e2e", action="store_true")
@@ -382,6 +382,7 @@ WORKLOAD_MATS = {
     "qwen_bf16_fused": (lambda: wl.qwen25_7b_step(fused=True), wl.FMT_BF16),
     "qwen_awq": (wl.qwen25_7b_step, wl.FMT_INT4_AWQ_G128),
     "qwen_awq_repacked": (wl.qwen25_7b_step, wl.FMT_INT4_AWQ_G128),
+    "qwen_awq_repacked_fused": (lambda: wl.qwen25_7b_step(fused=True), wl.FMT_INT4_AWQ_G128),
     "qwen_awq_fusedops": (lambda: wl.qwen25_7b_step(fusedops=True), wl.FMT_INT4_AWQ_G128),
     "qwen3_int8": (wl.qwen3_4b_step, wl.FMT_INT8_PC),
     "bf16_2048": (lambda: [wl.Mat(f"copy{i}", 2048, 2048) for i in range(64)], wl.FMT_BF16),
@@ -397,12 +398,13 @@ def make_step(workload, seed, device, M=1):
     if workload == "qwen_bf16_fused":
         return Step("Qwen2.5-7B-shaped BF16 decode step, batch 1, gate and up fused", wl.FMT_BF16,
                     wl.qwen25_7b_step(fused=True), seed, device)
-    if workload in ("qwen_awq", "qwen_awq_repacked", "qwen_awq_fusedops"):
+    if workload in ("qwen_awq", "qwen_awq_repacked", "qwen_awq_repacked_fused", "qwen_awq_fusedops"):
         rp = workload != "qwen_awq"
         fo = workload == "qwen_awq_fusedops"
+        fu = workload == "qwen_awq_repacked_fused"
         return Step(f"Qwen2.5-7B-shaped AWQ-style INT4 decode step, batch {M}" + (", repacked codes" if rp else "")
-                    + (", small ops fused" if fo else ""),
-                    wl.FMT_INT4_AWQ_G128, wl.qwen25_7b_step(fusedops=fo), seed, device, M, repacked=rp)
+                    + (", small ops fused" if fo else "") + (", gate and up fused" if fu else ""),
+                    wl.FMT_INT4_AWQ_G128, wl.qwen25_7b_step(fusedops=fo, fused=fu), seed, device, M, repacked=rp)
     if workload == "qwen3_int8":
         return Step(f"Qwen3-4B-shaped symmetric INT8 per-channel decode step, batch {M}", wl.FMT_INT8_PC,
                     wl.qwen3_4b_step(), seed, device, M)
@@ -556,6 +558,9 @@ def workload_desc(workload, batch=1):
             "qwen_awq_repacked": f"Qwen2.5-7B-shaped AWQ-style INT4 decode step (group 128, fp16 scale, uint4 zero "
                                  f"point, LM head included), codes reordered at load time (mbw_repack_int4), batch "
                                  f"{batch} (141 GEMMs)",
+            "qwen_awq_repacked_fused": f"Qwen2.5-7B-shaped AWQ-style INT4 decode step (group 128, fp16 scale, uint4 "
+                                       f"zero point, LM head included), codes reordered at load time, gate and up "
+                                       f"stored as one [Wgate; Wup] matrix, batch {batch} (113 GEMMs, the same weights)",
             "qwen_awq_fusedops": f"Qwen2.5-7B-shaped AWQ-style INT4 decode step (group 128, fp16 scale, uint4 zero "
                                  f"point), codes reordered at load time, with the layer's small ops folded into the "
                                  f"GEMVs: RMSNorm prologues (q/k/v, gate/up, head), SwiGLU epilogue (gate/up), "
@@ -717,7 +722,8 @@ def extra_configs(device, main_workload, tune="shape"):
     step (N = 1 only): BF16 GEMV 2048x2048; the four TinyLlama-shaped INT4
     group-64 matrices and the TinyLlama INT4 step; the Qwen2.5-7B BF16 step
     with gate and up stored as one matrix; the skinny BF16 GEMM sweep; the
-    AWQ-style INT4 step at M = 1, 16, 64 with repacked codes."""
+    AWQ-style INT4 step at M = 1, 16, 64 with repacked codes, and at M = 1 with
+    gate and up stored as one matrix."""
     t0 = time.time()
     out = {}
     out["bf16_gemv_2048x2048"] = per_matrix_figures(wl.FMT_BF16, [(0, 2048, 2048)], device)
@@ -732,6 +738,8 @@ def extra_configs(device, main_workload, tune="shape"):
         out["bf16_qwen_step_gate_up_fused"] = step_figure("qwen_bf16_fused", 1, device, tune)
     out["skinny_bf16_qwen_mlp"] = skinny_figures(device)
     out["awq_qwen_step_repacked"] = {f"M={M}": step_figure("qwen_awq_repacked", M, device, tune) for M in wl.AWQ_M}
+    # batch 1 with gate and up stored as one matrix (113 GEMVs instead of 141, the same weights)
+    out["awq_qwen_step_repacked_gate_up_fused"] = {"M=1": step_figure("qwen_awq_repacked_fused", 1, device, tune)}
     out["seconds"] = time.time() - t0
     return out
 
