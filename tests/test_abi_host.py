@@ -270,6 +270,34 @@ def test_tall_matrices_have_a_plan_at_every_batch(L):
     assert b"mma2" in kinds
 
 
+def test_int8_batches_above_8_plan_the_batched_family(L):
+    """INT8 calls above 8 rows get the batched mma.sync family (one launch per
+    16, 32 or 64 rows) as built-in plan and among the candidates, next to the
+    sliced GEMVs; at 8 rows and below it is never a candidate."""
+    buf = ctypes.create_string_buffer(256)
+    cases = ((9, 16), (16, 16), (17, 32), (32, 32), (33, 64), (64, 64), (200, 64))
+    for M, cols in cases:  # the built-in plans first (selecting a candidate replaces the plan of the batch's key)
+        assert L.mbw_plan_describe(5, M, 19456, 2560, buf, 256) == 0
+        assert buf.value.startswith(b"int8_mma fmt=int8_pc batch_cols=%d " % cols), (M, buf.value)
+    for M, _ in cases:
+        kinds = set()
+        for i in range(L.mbw_plan_candidates(5, M, 19456, 2560)):
+            assert L.mbw_plan_select(5, M, 19456, 2560, i) == 0
+            assert L.mbw_plan_describe(5, M, 19456, 2560, buf, 256) == 0
+            kinds.add(buf.value.split()[0])
+        assert b"int8_mma" in kinds and b"mma2" in kinds
+    for M in (1, 4, 8):
+        for i in range(L.mbw_plan_candidates(5, M, 19456, 2560)):
+            assert L.mbw_plan_select(5, M, 19456, 2560, i) == 0
+            assert L.mbw_plan_describe(5, M, 19456, 2560, buf, 256) == 0
+            assert not buf.value.startswith(b"int8_mma")
+    # fused INT8 calls stay on the GEMV families with fusion hooks
+    for i in range(L.mbw_plan_candidates(5 | 0x100, 16, 2048, 2048)):
+        assert L.mbw_plan_select(5 | 0x100, 16, 2048, 2048, i) == 0
+        assert L.mbw_plan_describe(5 | 0x100, 16, 2048, 2048, buf, 256) == 0
+        assert buf.value.split()[0] in (b"mma2", b"lat")
+
+
 def test_output_hook_is_thread_local(L):
     import threading
 
